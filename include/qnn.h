@@ -1,0 +1,209 @@
+/*
+ * qnn.h -- C ABI of the GB300 (sm_103a) linear-quantized GEMM and
+ * implicit-GEMM convolution library (libqnn.so).
+ *
+ * Page sources cited below (title, section):
+ *   [QI] "【量化】神经网络量化介绍" (loveleaves.github.io/p/quantization)
+ *   [MG] MegEngine 4-bit quantization article (m.xsypw.cn/d/1897816)
+ *   [FQ] "首个完全量化Vision Transformer的方法FQ-ViT" (aijishu.com)
+ *
+ * Conventions for every call:
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; shapes,
+ *    scalars and parameter structs are host values.  The library allocates
+ *    nothing and keeps no hidden buffers (one device status word aside).
+ *  - Calls are asynchronous on the given stream (NULL: the legacy default
+ *    stream) and never synchronise, except qnn_check_device_error.
+ *  - Arguments are validated on the host before any launch; a failed check
+ *    returns a status and launches nothing.  Nothing aborts or throws across
+ *    the ABI.  There is no CPU fallback: what the kernels cannot do returns
+ *    QNN_ERR_UNSUPPORTED.
+ *  - Base pointers must be 16-byte aligned (QNN_ERR_ALIGNMENT).
+ *  - 4-bit tensors hold two codes per byte along their innermost dimension,
+ *    element 2i in the low nibble; that dimension must be even.
+ *  - Rounding is round-half-to-even throughout; fp32 arithmetic is done as the
+ *    separate IEEE operations documented per call (no fused multiply-add).
+ */
+#ifndef QNN_H_
+#define QNN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qnn_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    QNN_OK = 0,
+    QNN_ERR_INVALID_ARG = 1,   /* bad shape, NULL pointer, bad enum, bad range */
+    QNN_ERR_UNSUPPORTED = 2,   /* valid request the kernels do not implement */
+    QNN_ERR_ALIGNMENT = 3,     /* pointer or row pitch not 16-byte aligned */
+    QNN_ERR_OVERFLOW_RISK = 4, /* the int32 accumulator could overflow */
+    QNN_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+    QNN_ERR_TIMEOUT = 6        /* a device-side bounded wait gave up */
+} qnn_status;
+
+typedef enum { QNN_S8 = 0, QNN_U8 = 1, QNN_S4 = 2, QNN_U4 = 3, QNN_S32 = 4, QNN_F32 = 5 } qnn_dtype;
+
+/* Quantization schemes [QI 量化模式]:
+ *   QNN_SYM : q = clip(rint(x / s))
+ *   QNN_ASYM: q = clip(rint(x / s) + z)          (offset added after rounding)
+ *   QNN_POW2: q = clip(rint(x * 2^shift))        ("integer" quantization; the
+ *             page's text writes 2 << shift, read here as 2^shift, shift being
+ *             the number of fractional bits) */
+typedef enum { QNN_SYM = 0, QNN_ASYM = 1, QNN_POW2 = 2 } qnn_scheme;
+
+/* Quantization parameters, per tensor or per channel [QI tensor量化与通道量化]. */
+typedef struct {
+    int32_t scheme;            /* qnn_scheme */
+    int32_t per_channel;       /* 0: element 0 of each array applies everywhere */
+    int32_t axis;              /* channel axis when per_channel (negative counts from the end) */
+    int32_t narrow_range;      /* signed codes: qmin = -qmax (int8 -127..127) */
+    const float *scale;        /* device [C] or [1]: SYM, ASYM; must be > 0 */
+    const int32_t *zero_point; /* device [C] or [1]: ASYM; must lie in the code range */
+    const int32_t *shift;      /* device [C] or [1]: POW2; -126..126 */
+} qnn_qparams;
+
+/* Quantize [QI 量化算子, 量化模式; MG 背景 (UINT4 0..15, INT4 -8..7)].
+ * x: fp32 tensor of `ndim` dims `shape` (host array), contiguous.  q: codes of
+ * q_dt (S8, U8, S4, U4), same shape, contiguous (4-bit: packed along the last
+ * dim).  Per element: t = x / s (IEEE fp32 divide), r = rint(t), ASYM adds
+ * (float)z after rounding, POW2 uses r = rint(x * 2^shift); then the float is
+ * clipped to [qmin, qmax] and stored.  NaN becomes the code of real zero (z,
+ * else 0); +-Inf saturate. */
+qnn_status q_quantize(const float *x, void *q, qnn_dtype q_dt, int ndim, const int64_t *shape,
+                      const qnn_qparams *p, qnn_stream_t stream);
+
+/* Dequantize [QI 反量化算子; MG 背景: r = S (q - Z)].  x = (float)(q - z) * s
+ * (integer subtract, one fp32 multiply); POW2: x = q * 2^-shift (exact). */
+qnn_status q_dequantize(const void *q, qnn_dtype q_dt, float *x, int ndim, const int64_t *shape,
+                        const qnn_qparams *p, qnn_stream_t stream);
+
+/* ---- ahead of inference: weight prepack and constant folding -------------- */
+
+/* Size in bytes of the prepacked GEMM weight operand for B of shape [N, K]. */
+size_t qnn_gemm_packed_b_bytes(int N, int K);
+
+/* Prepack int8 weights B [N, K] (row-major, the Linear weight layout: output
+ * channel n, input channel k) into the GEMM kernel's shared-memory operand
+ * image (`B_packed`, qnn_gemm_packed_b_bytes bytes, 1024-byte aligned), and
+ * write colsum[n] = sum_k B[n][k] (int32 [N]), the weight sums that the
+ * zero-point cross term needs [MG 緩解精度下降].  K must be a multiple of 16. */
+qnn_status qgemm_prepack_b(const int8_t *B, int N, int K, void *B_packed, int32_t *colsum,
+                           qnn_stream_t stream);
+
+/* Fold the per-output-channel constants ahead of inference [MG 緩解精度下降:
+ * the zero-point part that does not depend on the input is computed before
+ * inference; QI 量化乘法: scale_abc computed ahead].  For n in [0, N):
+ *   zp_term[n] = (z_a - c_a) * colsum[n]   (int32), where c_a is the centre the
+ *                kernels subtract from the activation codes as they load them:
+ *                128 for U8 activations, 0 for S8, U4 (and S4)
+ *   M[n]  = (s_a * s_w[n]) / s_o            fp32 multiply, then fp32 divide
+ *   Bq[n] = bias[n] / s_o
+ *   D[n]  = s_a * s_w[n]                    (dequantizing epilogue)
+ * s_w: device [N] if w_per_channel else [1].  bias: device [N] or NULL (zero).
+ * Outputs are device [N]; any of M, Bq, D may be NULL to skip it. */
+qnn_status q_fold_epilogue(int N, qnn_dtype a_dt, int32_t z_a, const int32_t *colsum, float s_a,
+                           const float *s_w, int w_per_channel, const float *bias, float s_o,
+                           int32_t *zp_term, float *M, float *Bq, float *D, qnn_stream_t stream);
+
+/* ---- fused epilogue -------------------------------------------------------- */
+
+typedef enum {
+    QNN_EPI_REQUANT = 0, /* quantized output of out_dt */
+    QNN_EPI_DEQUANT = 1, /* fp32 output */
+    QNN_EPI_S32 = 2      /* raw int32 accumulator (zero-point corrected) */
+} qnn_epi_mode;
+
+/* Per output element (row m, column n), with acc_c = acc - zp_term[n]:
+ * REQUANT [QI 量化乘法, 量化加法, 量化激活函数, 常见计算图优化 (conv-add
+ *         Y = Wx + (Y2 + B)); MG 算子融合優化 (Conv_Relu, Conv_Add_Relu)]:
+ *     t = Bq[n];  residual: t = (float)(res[m][n] - z_res) * R + t
+ *     v = (float)acc_c * M[n];  v = v + t;  r = rint(v);  relu: r = max(r, 0)
+ *     q = clip(r + (float)z_out)  to out_dt's range
+ * DEQUANT [QI 反量化算子]: y = (float)acc_c * D[n] + bias[n]   (fmul, fadd)
+ * S32: acc_c. */
+typedef struct {
+    int32_t mode;            /* qnn_epi_mode */
+    int32_t relu;            /* REQUANT: fused ReLU */
+    int32_t out_dt;          /* REQUANT output: S8 or U8 (GEMM), U4 or U8 (conv) */
+    int32_t z_out;           /* REQUANT output zero point */
+    const int32_t *zp_term;  /* device [N] or NULL (zero) */
+    const float *M;          /* device [N]: REQUANT */
+    const float *Bq;         /* device [N]: REQUANT */
+    const float *D;          /* device [N]: DEQUANT */
+    const float *bias;       /* device [N] or NULL: DEQUANT */
+    const void *residual;    /* device [rows, N] codes of res_dt (same layout as the
+                                output), or NULL: REQUANT only */
+    int32_t res_dt;          /* S8, U8 (GEMM); U4, U8 (conv) */
+    int32_t z_res;           /* residual zero point */
+    float R;                 /* S_res / S_out */
+    const uint8_t *ptf_shift;/* device [K] per-input-channel Power-of-Two Factor
+                                alpha_k [FQ 3.2]: the GEMM uses A[m][k] * 2^alpha_k;
+                                S8 activations with z_a = 0 only; NULL: none */
+    int32_t ptf_max_shift;   /* upper bound (0..3) on every ptf_shift value */
+} qnn_epilogue;
+
+/* Quantized GEMM [QI 量化矩阵乘; MG 緩解精度下降]:
+ *   acc[m][n] = sum_k (A[m][k] - c_a) * 2^alpha_k * B[n][k]   exact, in int32
+ * then the epilogue above with zp_term folded by q_fold_epilogue.
+ * A: device [M, K] row-major codes of a_dt (S8 or U8); K % 16 == 0.
+ * B_packed: from qgemm_prepack_b for the same N, K.
+ * C: device [M, N] row-major, of out_dt (REQUANT), fp32 (DEQUANT) or int32 (S32).
+ * C_s32: optional device [M, N] int32 that also receives acc_c (NULL: none).
+ * Fails with QNN_ERR_OVERFLOW_RISK when K * max|a| * 2^ptf_max_shift * 128 could
+ * exceed the int32 range. */
+qnn_status qgemm_s8(const void *A, qnn_dtype a_dt, const void *B_packed, int M, int N, int K,
+                    const qnn_epilogue *epi, void *C, int32_t *C_s32, qnn_stream_t stream);
+
+/* ---- implicit-GEMM convolution -------------------------------------------- */
+
+/* NHWC input [N, H, W, C], OHWI weights [OC, FH, FW, C], NHWC output
+ * [N, OH, OW, OC] with OH = (H + 2 pad_h - FH) / stride_h + 1 (same for W).
+ * GEMM view [MG conv 算子優化, Fig. 5; output transposed so that output channels
+ * are contiguous]: rows p = (n, oh, ow), columns oc, reduction k = (fh, fw, c).
+ * Padded taps hold the real value 0, i.e. the code z_in. */
+typedef struct {
+    int32_t N, H, W, C, OC, FH, FW, pad_h, pad_w, stride_h, stride_w;
+} qnn_conv_geom;
+
+/* Size in bytes of the prepacked conv weight operand. */
+size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g);
+
+/* Prepack conv weights of w_dt (S4: packed nibbles, OHWI; S8: bytes, OHWI) into
+ * the conv kernel's operand image (`W_packed`, qnn_conv_packed_w_bytes bytes)
+ * and write colsum[oc] = sum over (fh, fw, c) of W (int32 [OC]). */
+qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_conv_geom *g, void *W_packed,
+                           int32_t *colsum, qnn_stream_t stream);
+
+/* u4 activations x s4 weights [MG 緩解精度下降: UINT4 input/output, INT4
+ * weights, FP32 bias], Conv_Relu / Conv_Add_Relu through `epi`
+ * [MG 算子融合優化].  I: packed u4 NHWC; O: out_dt U4 (packed) or U8 codes, or
+ * fp32 / int32 per epi->mode; O_s32: optional int32 acc_c.  C, OC even. */
+qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
+                      const qnn_epilogue *epi, void *O, int32_t *O_s32, qnn_stream_t stream);
+
+/* u8 activations x s8 weights, same contract (I: u8 NHWC; C % 16 == 0). */
+qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
+                      const qnn_epilogue *epi, void *O, int32_t *O_s32, qnn_stream_t stream);
+
+/* ---- status ----------------------------------------------------------------- */
+
+const char *qnn_status_string(qnn_status s);
+
+/* Synchronises `stream`, then reports and clears the device status word that
+ * kernels set when a bounded wait gives up (QNN_ERR_TIMEOUT), or QNN_ERR_CUDA
+ * if the stream holds a CUDA error. */
+qnn_status qnn_check_device_error(qnn_stream_t stream);
+
+/* Launches one block that waits on a barrier nothing arrives at, giving up
+ * after `limit_ns` nanoseconds (<= 1e9) the way every kernel wait gives up:
+ * sets the device status word and returns.  For testing the timeout path. */
+qnn_status qnn_selftest_wait_timeout(uint64_t limit_ns, qnn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QNN_H_ */

@@ -1,0 +1,237 @@
+"""Thin Python binding of libqnn.so (the C ABI in include/qnn.h).
+
+Argument marshalling only: every function here forwards device pointers
+(``tensor.data_ptr()``), host scalars and the current CUDA stream to the
+function of the same name in the CUDA library and raises ``QnnError`` on a
+non-OK status.  All device memory is allocated by the caller (with torch);
+nothing here computes any part of the quantized path.  There is no fallback:
+if the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import build as _build
+
+# ---- enums (mirror include/qnn.h) ------------------------------------------------
+QNN_OK, QNN_ERR_INVALID_ARG, QNN_ERR_UNSUPPORTED, QNN_ERR_ALIGNMENT = 0, 1, 2, 3
+QNN_ERR_OVERFLOW_RISK, QNN_ERR_CUDA, QNN_ERR_TIMEOUT = 4, 5, 6
+DTYPES = {"s8": 0, "u8": 1, "s4": 2, "u4": 3, "s32": 4, "f32": 5}
+SCHEMES = {"sym": 0, "asym": 1, "pow2": 2}
+EPI_MODES = {"requant": 0, "dequant": 1, "s32": 2}
+
+
+class QnnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class QParams(ctypes.Structure):
+    _fields_ = [("scheme", ctypes.c_int32), ("per_channel", ctypes.c_int32),
+                ("axis", ctypes.c_int32), ("narrow_range", ctypes.c_int32),
+                ("scale", ctypes.c_void_p), ("zero_point", ctypes.c_void_p),
+                ("shift", ctypes.c_void_p)]
+
+
+class Epilogue(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("relu", ctypes.c_int32), ("out_dt", ctypes.c_int32),
+                ("z_out", ctypes.c_int32), ("zp_term", ctypes.c_void_p), ("M", ctypes.c_void_p),
+                ("Bq", ctypes.c_void_p), ("D", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p), ("res_dt", ctypes.c_int32),
+                ("z_res", ctypes.c_int32), ("R", ctypes.c_float),
+                ("ptf_shift", ctypes.c_void_p), ("ptf_max_shift", ctypes.c_int32)]
+
+
+class ConvGeom(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("N", "H", "W", "C", "OC", "FH", "FW", "pad_h", "pad_w", "stride_h", "stride_w")]
+
+    @property
+    def OH(self):
+        return (self.H + 2 * self.pad_h - self.FH) // self.stride_h + 1
+
+    @property
+    def OW(self):
+        return (self.W + 2 * self.pad_w - self.FW) // self.stride_w + 1
+
+
+_lib = None
+_SYMBOLS = {}
+
+
+def _declare(L):
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    c_int = ctypes.c_int
+    sig = {
+        "q_quantize": (c_int, [vp, vp, c_int, c_int, vp, vp, vp]),
+        "q_dequantize": (c_int, [vp, c_int, vp, c_int, vp, vp, vp]),
+        "qnn_gemm_packed_b_bytes": (sz, [c_int, c_int]),
+        "qgemm_prepack_b": (c_int, [vp, c_int, c_int, vp, vp, vp]),
+        "q_fold_epilogue": (c_int, [c_int, c_int, i32, vp, f32, vp, c_int, vp, f32, vp, vp, vp, vp, vp]),
+        "qgemm_s8": (c_int, [vp, c_int, vp, c_int, c_int, c_int, vp, vp, vp, vp]),
+        "qnn_conv_packed_w_bytes": (sz, [vp]),
+        "qconv_prepack_w": (c_int, [vp, c_int, vp, vp, vp, vp]),
+        "qconv_u4s4": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
+        "qconv_u8s8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
+        "qnn_status_string": (ctypes.c_char_p, [c_int]),
+        "qnn_check_device_error": (c_int, [vp]),
+        "qnn_selftest_wait_timeout": (c_int, [ctypes.c_uint64, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+        _SYMBOLS[name] = fn
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Loads libqnn.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libqnn.so not found at {path}: build it with "
+                               "integer_quantized_nn_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        _declare(L)
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    load()
+    return _SYMBOLS["qnn_status_string"](int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != QNN_OK:
+        raise QnnError(status, what)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return int(t.data_ptr())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return int(getattr(stream, "cuda_stream", stream))
+    import torch
+    return int(torch.cuda.current_stream().cuda_stream)
+
+
+def _shape(shape):
+    arr = (ctypes.c_int64 * len(shape))(*[int(s) for s in shape])
+    return arr
+
+
+def qparams(scheme="sym", scale=None, zero_point=None, shift=None, per_channel=False, axis=0,
+            narrow_range=False) -> QParams:
+    return QParams(SCHEMES[scheme], int(per_channel), int(axis), int(narrow_range), _ptr(scale),
+                   _ptr(zero_point), _ptr(shift))
+
+
+def q_quantize(x, q, q_dt: str, params: QParams, shape=None, stream=None):
+    """x: fp32 device tensor; q: uint8/int8 device tensor holding the codes
+    (4-bit: packed, last dimension halved).  shape: logical shape (default x.shape)."""
+    shp = tuple(x.shape) if shape is None else tuple(shape)
+    load()
+    _check(_SYMBOLS["q_quantize"](_ptr(x), _ptr(q), DTYPES[q_dt], len(shp), _shape(shp),
+                                  ctypes.byref(params), _stream(stream)), "q_quantize")
+
+
+def q_dequantize(q, q_dt: str, x, params: QParams, shape=None, stream=None):
+    shp = tuple(x.shape) if shape is None else tuple(shape)
+    load()
+    _check(_SYMBOLS["q_dequantize"](_ptr(q), DTYPES[q_dt], _ptr(x), len(shp), _shape(shp),
+                                    ctypes.byref(params), _stream(stream)), "q_dequantize")
+
+
+def qnn_gemm_packed_b_bytes(N: int, K: int) -> int:
+    load()
+    return int(_SYMBOLS["qnn_gemm_packed_b_bytes"](int(N), int(K)))
+
+
+def qgemm_prepack_b(B, B_packed, colsum=None, stream=None):
+    """B: int8 [N, K] device tensor; B_packed: uint8 device tensor of
+    qnn_gemm_packed_b_bytes(N, K) bytes, 1024-byte aligned."""
+    N, K = B.shape
+    load()
+    _check(_SYMBOLS["qgemm_prepack_b"](_ptr(B), int(N), int(K), _ptr(B_packed), _ptr(colsum),
+                                       _stream(stream)), "qgemm_prepack_b")
+
+
+def q_fold_epilogue(N, a_dt: str, z_a: int, colsum, s_a: float, s_w, s_o: float, bias=None,
+                    zp_term=None, M=None, Bq=None, D=None, w_per_channel=True, stream=None):
+    load()
+    _check(_SYMBOLS["q_fold_epilogue"](int(N), DTYPES[a_dt], int(z_a), _ptr(colsum), float(s_a),
+                                       _ptr(s_w), int(w_per_channel), _ptr(bias), float(s_o),
+                                       _ptr(zp_term), _ptr(M), _ptr(Bq), _ptr(D), _stream(stream)),
+           "q_fold_epilogue")
+
+
+def epilogue(mode="requant", relu=False, out_dt="s8", z_out=0, zp_term=None, M=None, Bq=None,
+             D=None, bias=None, residual=None, res_dt="s8", z_res=0, R=0.0, ptf_shift=None,
+             ptf_max_shift=0) -> Epilogue:
+    return Epilogue(EPI_MODES[mode], int(relu), DTYPES[out_dt], int(z_out), _ptr(zp_term), _ptr(M),
+                    _ptr(Bq), _ptr(D), _ptr(bias), _ptr(residual), DTYPES[res_dt], int(z_res),
+                    float(R), _ptr(ptf_shift), int(ptf_max_shift))
+
+
+def qgemm_s8(A, a_dt: str, B_packed, M: int, N: int, K: int, epi: Epilogue, C, C_s32=None,
+             stream=None):
+    load()
+    _check(_SYMBOLS["qgemm_s8"](_ptr(A), DTYPES[a_dt], _ptr(B_packed), int(M), int(N), int(K),
+                                ctypes.byref(epi), _ptr(C), _ptr(C_s32), _stream(stream)),
+           "qgemm_s8")
+
+
+def conv_geom(N, H, W, C, OC, FH, FW, pad=(1, 1), stride=(1, 1)) -> ConvGeom:
+    return ConvGeom(N, H, W, C, OC, FH, FW, pad[0], pad[1], stride[0], stride[1])
+
+
+def qnn_conv_packed_w_bytes(g: ConvGeom) -> int:
+    load()
+    return int(_SYMBOLS["qnn_conv_packed_w_bytes"](ctypes.byref(g)))
+
+
+def qconv_prepack_w(W, w_dt: str, g: ConvGeom, W_packed, colsum=None, stream=None):
+    load()
+    _check(_SYMBOLS["qconv_prepack_w"](_ptr(W), DTYPES[w_dt], ctypes.byref(g), _ptr(W_packed),
+                                       _ptr(colsum), _stream(stream)), "qconv_prepack_w")
+
+
+def qconv_u4s4(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None, stream=None):
+    load()
+    _check(_SYMBOLS["qconv_u4s4"](_ptr(I), int(z_in), _ptr(W_packed), ctypes.byref(g),
+                                  ctypes.byref(epi), _ptr(O), _ptr(O_s32), _stream(stream)),
+           "qconv_u4s4")
+
+
+def qconv_u8s8(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None, stream=None):
+    load()
+    _check(_SYMBOLS["qconv_u8s8"](_ptr(I), int(z_in), _ptr(W_packed), ctypes.byref(g),
+                                  ctypes.byref(epi), _ptr(O), _ptr(O_s32), _stream(stream)),
+           "qconv_u8s8")
+
+
+def qnn_check_device_error(stream=None) -> int:
+    """Synchronises the stream; returns the status (does not raise)."""
+    load()
+    return int(_SYMBOLS["qnn_check_device_error"](_stream(stream)))
+
+
+def qnn_selftest_wait_timeout(limit_ns: int, stream=None):
+    load()
+    _check(_SYMBOLS["qnn_selftest_wait_timeout"](int(limit_ns), _stream(stream)),
+           "qnn_selftest_wait_timeout")

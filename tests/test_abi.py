@@ -1,0 +1,76 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for
+sm_103a, loads, exports every function include/qnn.h declares, and rejects
+invalid arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from integer_quantized_nn_gb300 import qnn
+
+pytestmark = pytest.mark.cpu
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "qnn.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "sizeof")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return qnn.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("q_quantize", "q_dequantize", "qgemm_prepack_b", "q_fold_epilogue", "qgemm_s8",
+              "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_status_string",
+              "qnn_check_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    assert qnn.status_string(qnn.QNN_OK) == "ok"
+    assert "align" in qnn.status_string(qnn.QNN_ERR_ALIGNMENT)
+    assert qnn.status_string(99) == "unknown status"
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    L = lib
+    shape = (ctypes.c_int64 * 2)(4, 8)
+    p = qnn.qparams("sym")
+    # NULL tensors
+    assert L.q_quantize(None, None, 0, 2, shape, ctypes.byref(p), None) == qnn.QNN_ERR_INVALID_ARG
+    # bad dtype for a quantized tensor
+    assert L.q_quantize(16, 16, 4, 2, shape, ctypes.byref(p), None) == qnn.QNN_ERR_INVALID_ARG
+    # scheme needs a scale
+    assert L.q_dequantize(16, 0, 16, 2, shape, ctypes.byref(p), None) == qnn.QNN_ERR_INVALID_ARG
+    epi = qnn.epilogue("requant")
+    # unsupported activation type, zero sizes
+    assert L.qgemm_s8(16, 2, 1024, 4, 8, 16, ctypes.byref(epi), 16, None, None) == qnn.QNN_ERR_UNSUPPORTED
+    assert L.qgemm_s8(16, 0, 1024, 0, 8, 16, ctypes.byref(epi), 16, None, None) == qnn.QNN_ERR_INVALID_ARG
+    # K not a multiple of 16, misaligned weights
+    assert L.qgemm_s8(16, 0, 1024, 4, 8, 24, ctypes.byref(epi), 16, None, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.qgemm_s8(16, 0, 1040, 4, 8, 32, ctypes.byref(epi), 16, None, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.qgemm_prepack_b(16, 8, 24, 1024, None, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.q_fold_epilogue(0, 0, 0, None, 1.0, None, 0, None, 1.0, None, None, None, None,
+                             None) == qnn.QNN_ERR_INVALID_ARG
+    # zero point outside the code range of the activation type
+    assert L.q_fold_epilogue(8, 1, 300, 16, 1.0, 16, 0, None, 1.0, 16, None, None, None,
+                             None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.qnn_selftest_wait_timeout(10 ** 10, None) == qnn.QNN_ERR_INVALID_ARG
+
+
+def test_packed_sizes(lib):
+    assert qnn.qnn_gemm_packed_b_bytes(3072, 768) == 12 * 12 * 256 * 128
+    assert qnn.qnn_gemm_packed_b_bytes(300, 272) == 2 * 5 * 256 * 128
+    assert qnn.qnn_gemm_packed_b_bytes(0, 16) == 0
