@@ -1,0 +1,474 @@
+"""Benchmark of the quantized GEMM / implicit-GEMM conv path on one GB300.
+
+A step is one qgemm_s8 call (u8 activations with zero point x s8 per-channel
+weights, int32 accumulation, fused requant to int8) on the ViT-B MLP fc1
+layer: M = 64 x 197 tokens = 12608, K = 768, N = 3072.  Inputs are resident in
+HBM; L2 is flushed (a 256 MiB write) between timed steps, outside the timed
+events.  The line also carries the quantize GB/s of a 1 GiB fp32 -> s8
+per-row quantize and the other layer shapes as extras.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With --impl reference the CPU oracle is timed on a bounded sample of the same
+workload (the reference arm).  Under torchrun every rank runs its own replica
+(weak scaling, no collective on the data path); rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "int8 TOPS and % of GB300 dense-INT8 peak (GEMM/conv); quantize GB/s vs HBM"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return dict(FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ dist utils
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Dist:
+    def __init__(self, backend):
+        self.ws, self.rank, self.local = dist_env()
+        self.pg = None
+        if self.ws > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v):
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([float(v)], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"qnn_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(1.0)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        if not isinstance(rows, list) or not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def gpu_setup_gemm(torch, qnn, w, a_dt, device):
+    A = torch.from_numpy(np.ascontiguousarray(w["A"])).to(device)
+    B = torch.from_numpy(np.ascontiguousarray(w["B"])).to(device)
+    N, K = w["B"].shape
+    nb = qnn.qnn_gemm_packed_b_bytes(N, K)
+    buf = torch.empty(nb + 1024, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 1024
+    Bp = buf[off:off + nb]
+    colsum = torch.empty(N, dtype=torch.int32, device=device)
+    qnn.qgemm_prepack_b(B, Bp, colsum)
+    sw = torch.from_numpy(np.asarray(w["s_w"], np.float32)).to(device)
+    bias = None if w.get("bias") is None else torch.from_numpy(w["bias"]).to(device)
+    zp = torch.empty(N, dtype=torch.int32, device=device)
+    Mv = torch.empty(N, dtype=torch.float32, device=device)
+    Bq = torch.empty(N, dtype=torch.float32, device=device)
+    qnn.q_fold_epilogue(N, a_dt, w["z_a"], colsum, w["s_a"], sw, w["s_o"], bias=bias, zp_term=zp,
+                        M=Mv, Bq=Bq)
+    return dict(A=A, Bp=Bp, zp=zp, M=Mv, Bq=Bq, keep=(buf, B, colsum, sw, bias))
+
+
+def time_steps(torch, fn, steps, warmup, flush, stream):
+    """Per-step CUDA events around fn() on `stream`; L2 flushed between steps
+    outside the events.  Returns list of ms."""
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def run_gpu(args):
+    import torch
+    dist = Dist("nccl")
+    torch.cuda.set_device(dist.local)
+    device = torch.device("cuda", dist.local)
+    from integer_quantized_nn_gb300 import qnn, workloads
+    qnn.load()
+    pk, pk_kind = peaks()
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    # ---- headline workload: ViT-B fc1
+    M, K, N = 12608, 768, 3072
+    w = workloads.vit_fc1(M=M, K=K, N=N)
+    g = gpu_setup_gemm(torch, qnn, w, "u8", device)
+    C = torch.empty((M, N), dtype=torch.uint8, device=device)
+    epi = qnn.epilogue("requant", zp_term=g["zp"], M=g["M"], Bq=g["Bq"], out_dt="s8")
+
+    def step():
+        qnn.qgemm_s8(g["A"], "u8", g["Bp"], M, N, K, epi, C, stream=stream)
+
+    flops = 2.0 * M * N * K
+    dist.barrier()
+    clk = ClockSampler(dist.local)
+    clk.start()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t_wall0 = time.time()
+    times = time_steps(torch, step, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t_wall1 = time.time()
+    clocks = ClockSampler.summarize(clk.stop(), t_wall0, t_wall1)
+    st = qnn.qnn_check_device_error()
+    if st != qnn.QNN_OK:
+        raise RuntimeError(f"device status: {qnn.status_string(st)}")
+    total_ms = sum(times)
+    total_ms_max = dist.max(total_ms)
+    value = dist.ws * args.steps * flops / (total_ms_max * 1e-3) / 1e12
+    per_launch_ms = total_ms / args.steps
+    achieved = flops / (per_launch_ms * 1e-3) / 1e12
+
+    # ---- e2e: host buffers, copies inside the timed region
+    A_h = torch.from_numpy(np.ascontiguousarray(w["A"])).pin_memory()
+    C_h = torch.empty((M, N), dtype=torch.uint8).pin_memory()
+    A_d = torch.empty_like(g["A"])
+
+    def e2e_step():
+        A_d.copy_(A_h, non_blocking=True)
+        qnn.qgemm_s8(A_d, "u8", g["Bp"], M, N, K, epi, C, stream=stream)
+        C_h.copy_(C, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e_times = time_steps(torch, e2e_step, e2e_steps, max(1, args.warmup), flush, stream)
+    e2e_ms = dist.max(sum(e2e_times)) / e2e_steps
+    e2e_value = dist.ws * flops / (e2e_ms * 1e-3) / 1e12
+
+    extras = {}
+    if not args.no_extras and dist.rank == 0:
+        extras = run_extras(torch, qnn, workloads, device, flush, stream, pk, args)
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
+    cpu = None
+    if dist.rank == 0 and dist.ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_gemm(w, target_s=args.cpu_seconds)
+
+    dtype_str = "u8 x s8 -> s32 (exact on the f16 tensor pipe), requant to s8"
+    peak = float(pk["bf16_tflops"])
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": dist.ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms_max / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_str,
+        "data": "synthetic (seeded numpy PCG64; no dataset or trained weights)",
+        "config": {"workload": "ViT-B MLP fc1 qgemm_s8: u8 (Z=128) x s8 per-channel -> s8",
+                   "M": M, "K": K, "N": N, "tokens": "64 x 197", "l2": "flushed between steps "
+                   "(256 MiB write, outside the timed events)", "parallelism": f"replicas x{dist.ws}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_kind": f"{pk_kind} bf16 dense burst (the f16 MMA kind runs at the bf16 rate)",
+                     "kernel": "qgemm_kernel<256,false,false>",
+                     "algorithmic": "2*M*N*K int ops per launch"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TOPS", "h2d_bytes_per_step": M * K,
+                "d2h_bytes_per_step": M * N},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "extras": extras,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
+    out = {}
+    hbm = float(pk["hbm_gbs"])
+    peak = float(pk["bf16_tflops"])
+    steps = max(3, min(args.steps, args.extra_steps))
+
+    # quantize fp32 -> s8, per row, 1 GiB
+    R = Cc = 16384
+    x = workloads.device_normal_f32((R, Cc), 505, device)
+    scale = (x.abs().amax(dim=1) / 127.0).contiguous()
+    q = torch.empty((R, Cc), dtype=torch.uint8, device=device)
+    p = qnn.qparams("sym", scale=scale, per_channel=True, axis=0)
+    t = time_steps(torch, lambda: qnn.q_quantize(x, q, "s8", p, stream=stream), steps, 3, flush,
+                   stream)
+    ms = statistics.median(t)
+    gbs = 5.0 * R * Cc / (ms * 1e-3) / 1e9
+    out["quantize_rows_1GiB"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                 "frac_hbm": round(gbs / hbm, 4), "bytes": "5 B/elem"}
+    # dequantize s8 -> fp32
+    t = time_steps(torch, lambda: qnn.q_dequantize(q, "s8", x, p, stream=stream), steps, 3, flush,
+                   stream)
+    ms = statistics.median(t)
+    gbs = 5.0 * R * Cc / (ms * 1e-3) / 1e9
+    out["dequantize_rows_1GiB"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                   "frac_hbm": round(gbs / hbm, 4)}
+    del x, q, scale
+
+    def gemm_entry(name, w, a_dt, alpha=None):
+        Mm, Kk = w["A"].shape
+        Nn = w["B"].shape[0]
+        g = gpu_setup_gemm(torch, qnn, w, a_dt, device)
+        C = torch.empty((Mm, Nn), dtype=torch.uint8, device=device)
+        al = None
+        if alpha is not None:
+            al = torch.from_numpy(alpha.astype(np.uint8)).to(device)
+        epi = qnn.epilogue("requant", zp_term=None if al is not None else g["zp"], M=g["M"],
+                           Bq=g["Bq"], ptf_shift=al,
+                           ptf_max_shift=0 if alpha is None else int(alpha.max()))
+        t = time_steps(torch, lambda: qnn.qgemm_s8(g["A"], a_dt, g["Bp"], Mm, Nn, Kk, epi, C,
+                                                   stream=stream), steps, 3, flush, stream)
+        ms = statistics.median(t)
+        tops = 2.0 * Mm * Nn * Kk / (ms * 1e-3) / 1e12
+        out[name] = {"M": Mm, "N": Nn, "K": Kk, "ms": round(ms, 4), "TOPS": round(tops, 2),
+                     "frac_f16_peak": round(tops / peak, 4)}
+
+    gemm_entry("gemm_sym_256", workloads.gemm_sym(), "s8")
+    for nm, (Kk, Nn) in workloads.VITL_SHAPES.items():
+        w = workloads.vitl_ptf(M=12608, K=Kk, N=Nn)
+        xq = torch.from_numpy(w["x"]).to(device)
+        Aq = torch.empty(w["x"].shape, dtype=torch.uint8, device=device)
+        qnn.q_quantize(xq, Aq, "s8", qnn.qparams("sym", scale=torch.from_numpy(w["in_scale"]).to(device),
+                                                 per_channel=True, axis=1))
+        w2 = dict(A=Aq.cpu().numpy(), B=w["B"], s_w=w["s_w"], bias=w["bias"], s_a=w["s"],
+                  s_o=w["s_o"], z_a=0)
+        gemm_entry(f"vitl_{nm}_ptf", w2, "s8", alpha=w["alpha"])
+        del xq, Aq
+    for n in (2048, 4096, 8192):
+        gemm_entry(f"square_{n}", workloads.gemm_square(n), "s8")
+
+    def conv_entry(name, w, geom):
+        Nb, H, W, C, OC, F, pad, st = geom
+        g = qnn.conv_geom(Nb, H, W, C, OC, F, F, (pad, pad), (st, st))
+        Wd = torch.from_numpy(w["W"]).to(device)
+        nb = qnn.qnn_conv_packed_w_bytes(g, "s4")
+        buf = torch.empty(nb + 1024, dtype=torch.uint8, device=device)
+        off = (-buf.data_ptr()) % 1024
+        Wp = buf[off:off + nb]
+        cs = torch.empty(OC, dtype=torch.int32, device=device)
+        qnn.qconv_prepack_w(Wd, "s4", g, Wp, cs)
+        sw = torch.from_numpy(w["s_w"]).to(device)
+        bias = torch.from_numpy(w["bias"]).to(device)
+        zp = torch.empty(OC, dtype=torch.int32, device=device)
+        Mv = torch.empty(OC, dtype=torch.float32, device=device)
+        Bq = torch.empty(OC, dtype=torch.float32, device=device)
+        qnn.q_fold_epilogue(OC, "u4", w["z_in"], cs, w["s_a"], sw, w["s_o"], bias=bias, zp_term=zp,
+                            M=Mv, Bq=Bq)
+        I = torch.from_numpy(w["I"]).to(device)
+        res = None if w["res"] is None else torch.from_numpy(w["res"]).to(device)
+        R = float(np.float32(np.float32(w["s_r"]) / np.float32(w["s_o"])))
+        epi = qnn.epilogue("requant", relu=True, out_dt="u4", zp_term=zp, M=Mv, Bq=Bq, residual=res,
+                           res_dt="u4", z_res=w["z_res"], R=R)
+        O = torch.empty((Nb, g.OH, g.OW, OC // 2), dtype=torch.uint8, device=device)
+        t = time_steps(torch, lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, g, epi, O, stream=stream),
+                       steps, 3, flush, stream)
+        ms = statistics.median(t)
+        ops = 2.0 * Nb * g.OH * g.OW * OC * C * F * F
+        tops = ops / (ms * 1e-3) / 1e12
+        byts = I.numel() + O.numel() + (0 if res is None else res.numel()) + Wd.numel()
+        out[name] = {"ms": round(ms, 4), "TOPS": round(tops, 2),
+                     "frac_fp8_peak": round(tops / (2.0 * peak), 4),
+                     "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
+                     "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
+
+    conv_entry("conv3x3_u4s4_add_relu", workloads.conv_u4(), (64, 56, 56, 64, 64, 3, 1, 1))
+    conv_entry("conv1x1_u4s4_relu", workloads.conv_u4(C=256, OC=64, F=1, pad=0, residual=False, tag=1),
+               (64, 56, 56, 256, 64, 1, 0, 1))
+    return out
+
+
+def cpu_baseline_gemm(w, target_s=15.0):
+    """The oracle (plain C, OpenMP over rows) on a sample of rows of the same GEMM."""
+    from oracle import oracle
+    oracle.build()
+    A = w["A"].astype(np.int32)
+    B = w["B"].astype(np.int32)
+    N, K = B.shape
+    cs = oracle.colsum(B)
+    _, Mo, Bqo, _ = oracle.fold(cs, w["z_a"] - 128, w["s_a"], w["s_w"], w["s_o"], w["bias"])
+    rows = 64
+    t0 = time.perf_counter()
+    acc = oracle.gemm_acc(A[:rows], B, w["z_a"])
+    oracle.requant(acc, Mo, Bqo, "s8")
+    dt = time.perf_counter() - t0
+    rows = int(min(A.shape[0], max(64, rows * target_s / max(dt, 1e-6))))
+    t0 = time.perf_counter()
+    acc = oracle.gemm_acc(A[:rows], B, w["z_a"])
+    oracle.requant(acc, Mo, Bqo, "s8")
+    dt = time.perf_counter() - t0
+    tops = 2.0 * rows * N * K / dt / 1e12
+    return {"value": round(tops, 6), "unit": "TOPS", "cores": oracle.get_threads(), "kind": "oracle",
+            "sample": f"first {rows} of {A.shape[0]} rows (x all {N} columns, K={K}), "
+                      f"{dt:.1f} s; scaled to the metric's unit"}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from integer_quantized_nn_gb300 import workloads
+    from oracle import oracle
+    oracle.build()
+    M, K, N = 12608, 768, 3072
+    w = workloads.vit_fc1(M=M, K=K, N=N)
+    A = w["A"].astype(np.int32)
+    B = w["B"].astype(np.int32)
+    cs = oracle.colsum(B)
+    _, Mo, Bqo, _ = oracle.fold(cs, w["z_a"] - 128, w["s_a"], w["s_w"], w["s_o"], w["bias"])
+    # size the per-step sample so warmup + steps take about args.cpu_seconds * 4
+    t0 = time.perf_counter()
+    oracle.requant(oracle.gemm_acc(A[:16], B, w["z_a"]), Mo, Bqo, "s8")
+    per_row = (time.perf_counter() - t0) / 16
+    budget = 4.0 * args.cpu_seconds
+    rows = int(max(1, min(M, budget / max(per_row, 1e-9) / max(1, args.steps + args.warmup))))
+    rng = np.random.default_rng(0)
+
+    def step(i):
+        r0 = int(rng.integers(0, M - rows + 1))
+        acc = oracle.gemm_acc(A[r0:r0 + rows], B, w["z_a"])
+        oracle.requant(acc, Mo, Bqo, "s8")
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    ops = 2.0 * rows * N * K * args.steps
+    v = ops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TOPS", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8 x s8 -> s32 (int64 C loops), requant to s8", "data": "synthetic",
+        "config": {"workload": "ViT-B MLP fc1 qgemm_s8: u8 (Z=128) x s8 per-channel -> s8",
+                   "M": M, "K": K, "N": N, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TOPS", "cores": oracle.get_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows} consecutive rows per step (x all {N} columns, K={K})"},
+        "e2e": {"value": round(v, 6), "unit": "TOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--extra-steps", type=int, default=20)
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -169,8 +169,9 @@ typedef struct {
     int32_t N, H, W, C, OC, FH, FW, pad_h, pad_w, stride_h, stride_w;
 } qnn_conv_geom;
 
-/* Size in bytes of the prepacked conv weight operand. */
-size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g);
+/* Size in bytes of the prepacked conv weight operand for weights of w_dt
+ * (S4 or S8); 0 for an invalid geometry or type. */
+size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g, qnn_dtype w_dt);
 
 /* Prepack conv weights of w_dt (S4: packed nibbles, OHWI; S8: bytes, OHWI) into
  * the conv kernel's operand image (`W_packed`, qnn_conv_packed_w_bytes bytes)

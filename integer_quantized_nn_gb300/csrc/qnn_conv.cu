@@ -1,27 +1,361 @@
-// qnn_conv.cu -- implicit-GEMM convolution (not yet implemented on the device).
-#include <cuda_runtime.h>
-#include "qnn_internal.h"
+// qnn_conv.cu -- implicit-GEMM quantized convolution (qconv_u4s4, qconv_u8s8)
+// and its weight prepack.
+//
+// [MG conv 算子優化, Fig. 5] a convolution of an (N, IH, IW, C) input with
+// (OC, FH, FW, C) filters is the product of the (N*OH*OW) x (FH*FW*C) patch
+// matrix with the (FH*FW*C) x OC filter matrix; the implicit form never
+// writes the patch matrix: each block re-lays the input out while moving it
+// from global to shared memory.  The output is computed transposed, pixels x
+// channels, so that a thread's accumulators are consecutive output channels
+// of one pixel and pack straight into NHWC bytes or nibbles [MG conv 算子優化:
+// output transposition, 16 consecutive 4-bit channels per thread].
+//
+// Operands on the tensor cores:
+//   u4 x s4: a u4 code c zero-extended into a byte is exactly the e4m3
+//            encoding of c / 512 (codes 0..7 are the subnormals c * 2^-9, 8..15
+//            the first binade), so unpacking is two masks per 8 codes; the s4
+//            weights are prepacked as exact e4m3 integers.  kind::f8f6f4 sums
+//            the exact products c * w * 2^-9 in fp32 (|sum| < 2^24 * 2^-9 for any
+//            K below 139810) and the epilogue multiplies by 512.  The two masks
+//            deliver each group of 8 channels in the order 0,2,4,6,1,3,5,7; the
+//            weight prepack uses the same order, which leaves every sum unchanged.
+//   u8 x s8: bytes to fp16 exactly as in the GEMM (kind::f16), q - 128.
+// Padded taps read the code z_in (the real value 0 [reading of the pages]),
+// so the folded zero-point term applies to every tap alike.
+#include <cuda_fp8.h>
+#include "qnn_mma_kernel.cuh"
 
-extern "C" size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g)
+namespace qnn {
+namespace mk {
+
+constexpr int KMAX_U4_EXACT = 139810;  // 2^24 / (15 * 8): exact fp32 sums of u4 x s4 products
+
+// Per-thread im2col cursor: the 4 pixels (rows) this thread fetches in the
+// current tile and the (fh, fw, c0) position of its 16-byte group in K.
+struct ConvState {
+    int img[4];   // n * H of the row's image, or -1 past the last pixel
+    int ih0[4];
+    int iw0[4];
+    int c0, fh, fw;
+};
+
+template <int GROUP_ELEMS, int STEP_ELEMS>
+__device__ __forceinline__ void conv_cursor(const Params &p, ConvState &st, int j, int sub, int rbase)
 {
-    (void)g;
+    const int ks = j % p.KT;
+    if (ks == 0) {
+        const int t = unit_tile(p, j);
+        const int m0 = (t % p.num_m) * BM;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int r = m0 + q * 32 + rbase;
+            if (r < p.M) {
+                const int n = r / p.OHW;
+                const int rem = r - n * p.OHW;
+                const int oh = rem / p.OW;
+                const int ow = rem - oh * p.OW;
+                st.img[q] = n * p.H;
+                st.ih0[q] = oh * p.sh - p.ph;
+                st.iw0[q] = ow * p.sw - p.pw;
+            } else {
+                st.img[q] = -1;
+                st.ih0[q] = 0;
+                st.iw0[q] = 0;
+            }
+        }
+        const int k0 = sub * GROUP_ELEMS;
+        const int tap = k0 / p.Cin;
+        st.c0 = k0 - tap * p.Cin;
+        st.fh = tap / p.FW;
+        st.fw = tap - st.fh * p.FW;
+    } else {
+        st.c0 += STEP_ELEMS;
+        while (st.c0 >= p.Cin) {
+            st.c0 -= p.Cin;
+            if (++st.fw == p.FW) {
+                st.fw = 0;
+                ++st.fh;
+            }
+        }
+    }
+}
+
+// 16 bytes of the input row under the cursor: in-image data, the padding
+// pattern, or zeros past the last pixel / past the last tap.
+template <int ELEM_BITS>
+__device__ __forceinline__ uint4 conv_fetch(const Params &p, const ConvState &st, int q)
+{
+    if (st.img[q] < 0 || st.fh >= p.FH) return make_uint4(0, 0, 0, 0);
+    const int ih = st.ih0[q] + st.fh;
+    const int iw = st.iw0[q] + st.fw;
+    if (ih < 0 || ih >= p.H || iw < 0 || iw >= p.W)
+        return make_uint4(p.pad_word, p.pad_word, p.pad_word, p.pad_word);
+    const int64_t elem = ((int64_t)(st.img[q] + ih) * p.W + iw) * p.Cin + st.c0;
+    return ldg_nc_v4(p.A + (ELEM_BITS == 4 ? elem / 2 : elem));
+}
+
+struct ConvU4Op {
+    static constexpr bool F8 = true;
+    static constexpr int SCALE_LOG2 = 9;
+    struct Unit {
+        uint4 v[4];
+    };
+    using State = ConvState;
+
+    __device__ static void load(const Params &p, State &st, int j, int sub, int rbase, Unit &u)
+    {
+        conv_cursor<32, 128>(p, st, j, sub, rbase);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) u.v[q] = conv_fetch<4>(p, st, q);
+    }
+
+    __device__ static void store(const Params &, uint32_t a_stage, int sub, int rbase, const Unit &u)
+    {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int row = q * 32 + rbase;
+            const uint32_t w[4] = {u.v[q].x, u.v[q].y, u.v[q].z, u.v[q].w};
+            uint32_t b[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                b[2 * i] = w[i] & 0x0F0F0F0Fu;             // channels 0, 2, 4, 6 of the 8
+                b[2 * i + 1] = (w[i] >> 4) & 0x0F0F0F0Fu;  // channels 1, 3, 5, 7
+            }
+            const uint32_t rowaddr = a_stage + row * ROW_BYTES;
+            sts_v4(rowaddr + (((2 * sub) ^ (row & 7)) << 4), b[0], b[1], b[2], b[3]);
+            sts_v4(rowaddr + (((2 * sub + 1) ^ (row & 7)) << 4), b[4], b[5], b[6], b[7]);
+        }
+    }
+};
+
+struct ConvU8Op {
+    static constexpr bool F8 = false;
+    static constexpr int SCALE_LOG2 = 0;
+    struct Unit {
+        uint4 v[4];
+    };
+    using State = ConvState;
+
+    __device__ static void load(const Params &p, State &st, int j, int sub, int rbase, Unit &u)
+    {
+        conv_cursor<16, 64>(p, st, j, sub, rbase);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) u.v[q] = conv_fetch<8>(p, st, q);
+    }
+
+    __device__ static void store(const Params &, uint32_t a_stage, int sub, int rbase, const Unit &u)
+    {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int row = q * 32 + rbase;
+            const uint32_t w[4] = {u.v[q].x, u.v[q].y, u.v[q].z, u.v[q].w};
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                h[2 * i] = hsub2_u32(prmt(w[i], 0x64646464u, 0x4140u), 0x64806480u);
+                h[2 * i + 1] = hsub2_u32(prmt(w[i], 0x64646464u, 0x4342u), 0x64806480u);
+            }
+            const uint32_t rowaddr = a_stage + row * ROW_BYTES;
+            sts_v4(rowaddr + (((2 * sub) ^ (row & 7)) << 4), h[0], h[1], h[2], h[3]);
+            sts_v4(rowaddr + (((2 * sub + 1) ^ (row & 7)) << 4), h[4], h[5], h[6], h[7]);
+        }
+    }
+};
+
+// ---- weight prepack of s4 filters into the e4m3 operand image -----------------
+// Image: for each 256-filter block and K step of 128, 256 rows x 128 bytes,
+// 128-byte swizzled, zero beyond OC and K; byte position 8g + j of a row holds
+// the weight of K index 8g + {0,2,4,6,1,3,5,7}[j].
+__global__ void prepack_w_s4_kernel(const uint8_t *__restrict__ W, int OC, int K, int KT,
+                                    uint8_t *__restrict__ out, int64_t nchunks)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int cphys = (int)(i & 7);
+        const int64_t row_all = i >> 3;
+        const int r = (int)(row_all % 256);
+        const int64_t blk = row_all / 256;
+        const int ks = (int)(blk % KT);
+        const int nb = (int)(blk / KT);
+        const int c = cphys ^ (r & 7);
+        const int n = nb * 256 + r;
+        uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+            const int kpos = ks * 128 + c * 16 + b;
+            const int j = kpos & 7;
+            const int k = (kpos & ~7) + ((j < 4) ? 2 * j : 2 * (j - 4) + 1);
+            uint32_t code = 0;
+            if (n < OC && k < K) {
+                const uint8_t byte = W[((int64_t)n * K + k) >> 1];
+                int v = (k & 1) ? (byte >> 4) : (byte & 15);
+                if (v >= 8) v -= 16;
+                code = (uint32_t)__nv_cvt_float_to_fp8((float)v, __NV_SATFINITE, __NV_E4M3);
+            }
+            w[b >> 2] |= code << (8 * (b & 3));
+        }
+        *reinterpret_cast<uint4 *>(out + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// colsum[oc] = sum over (fh, fw, c) of the s4 weights; one warp per filter.
+__global__ void colsum_s4_kernel(const uint8_t *__restrict__ W, int OC, int K, int32_t *__restrict__ colsum)
+{
+    const int warp = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp >= OC) return;
+    int32_t s = 0;
+    for (int k = lane; k < K; k += 32) {
+        const uint8_t byte = W[((int64_t)warp * K + k) >> 1];
+        int v = (k & 1) ? (byte >> 4) : (byte & 15);
+        s += (v >= 8) ? v - 16 : v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) colsum[warp] = s;
+}
+
+inline bool geom_ok(const qnn_conv_geom *g)
+{
+    if (!g) return false;
+    if (g->N <= 0 || g->H <= 0 || g->W <= 0 || g->C <= 0 || g->OC <= 0 || g->FH <= 0 || g->FW <= 0)
+        return false;
+    if (g->pad_h < 0 || g->pad_w < 0 || g->stride_h <= 0 || g->stride_w <= 0) return false;
+    const int oh = (g->H + 2 * g->pad_h - g->FH) / g->stride_h + 1;
+    const int ow = (g->W + 2 * g->pad_w - g->FW) / g->stride_w + 1;
+    if (g->H + 2 * g->pad_h < g->FH || g->W + 2 * g->pad_w < g->FW || oh <= 0 || ow <= 0) return false;
+    const int64_t rows = (int64_t)g->N * oh * ow;
+    const int64_t K = (int64_t)g->FH * g->FW * g->C;
+    const int64_t in = (int64_t)g->N * g->H * g->W * g->C;
+    return rows < (1ll << 31) && K < (1ll << 24) && in < (1ll << 40);
+}
+
+inline size_t packed_w_u4_bytes(const qnn_conv_geom *g)
+{
+    const int K = g->FH * g->FW * g->C;
+    return (size_t)((g->OC + 255) / 256) * (size_t)((K + 127) / 128) * (size_t)gemm::B_STAGE_BYTES;
+}
+
+template <class Op, int TBN>
+qnn_status conv_launch(const Params &p, cudaStream_t s)
+{
+    if constexpr (!Op::F8) {
+        // K cut into exact chunks: int32 chunk sums of 64 columns per thread
+        if (p.nchunks > 1) return launch<Op, 128, true>(p, s);
+    }
+    return launch<Op, TBN, false>(p, s);
+}
+
+template <class Op>
+qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
+                    const qnn_epilogue *e, void *O, int32_t *O_s32, qnn_stream_t stream, bool u4)
+{
+    if (!I || !W_packed || !e || !O) return QNN_ERR_INVALID_ARG;
+    if (!geom_ok(g)) return QNN_ERR_INVALID_ARG;
+    if (g->C % (u4 ? 32 : 16) != 0) return QNN_ERR_UNSUPPORTED;
+    if (g->OC % 2 != 0) return QNN_ERR_INVALID_ARG;
+    if (z_in < 0 || z_in > (u4 ? 15 : 255)) return QNN_ERR_INVALID_ARG;
+    if (e->ptf_shift) return QNN_ERR_UNSUPPORTED;
+    if (!aligned16(I) || !aligned16(O) || (O_s32 && !aligned16(O_s32))) return QNN_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(W_packed) & 1023u) != 0) return QNN_ERR_ALIGNMENT;
+
+    Params p{};
+    const int oh = (g->H + 2 * g->pad_h - g->FH) / g->stride_h + 1;
+    const int ow = (g->W + 2 * g->pad_w - g->FW) / g->stride_w + 1;
+    p.A = static_cast<const uint8_t *>(I);
+    p.H = g->H;
+    p.W = g->W;
+    p.Cin = g->C;
+    p.OHW = oh * ow;
+    p.OW = ow;
+    p.FH = g->FH;
+    p.FW = g->FW;
+    p.ph = g->pad_h;
+    p.pw = g->pad_w;
+    p.sh = g->stride_h;
+    p.sw = g->stride_w;
+    p.pad_word = u4 ? (uint32_t)z_in * 0x11111111u : (uint32_t)z_in * 0x01010101u;
+    p.Bp = static_cast<const uint8_t *>(W_packed);
+    p.M = g->N * oh * ow;
+    p.N = g->OC;
+    p.K = g->FH * g->FW * g->C;
+    p.KT = u4 ? (p.K + 127) / 128 : (p.K + 63) / 64;
+    p.num_m = (p.M + BM - 1) / BM;
+    p.C = O;
+    p.C32 = O_s32;
+    p.vec_ok = (g->OC % 32 == 0);
+    qnn_status st = setup_epilogue(e, true, p);
+    if (st != QNN_OK) return st;
+    if (p.mode == QNN_EPI_REQUANT && p.out_bits == 4 && e->out_dt != QNN_U4) return QNN_ERR_UNSUPPORTED;
+    // exact fp32 chunk sums: u4 x s4 products are at most 120, centred u8 x s8 at most 2^14
+    if (u4) {
+        p.chunk_steps = KMAX_U4_EXACT / 128;
+        if ((int64_t)p.K * 240 > (int64_t)INT32_MAX) return QNN_ERR_OVERFLOW_RISK;
+    } else {
+        p.chunk_steps = gemm::MAX_EXACT_STEPS;
+        if ((int64_t)p.K * 255 * 128 > (int64_t)INT32_MAX) return QNN_ERR_OVERFLOW_RISK;
+    }
+    p.nchunks = (p.KT + p.chunk_steps - 1) / p.chunk_steps;
+    if (u4 && p.nchunks > 1) return QNN_ERR_UNSUPPORTED;
+    p.status = status_word();
+    if (!p.status) return QNN_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (g->OC <= 64) return conv_launch<Op, 64>(p, s);
+    if (g->OC <= 128) return conv_launch<Op, 128>(p, s);
+    return conv_launch<Op, 256>(p, s);
+}
+
+}  // namespace mk
+}  // namespace qnn
+
+extern "C" size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g, qnn_dtype w_dt)
+{
+    if (!qnn::mk::geom_ok(g)) return 0;
+    if (w_dt == QNN_S4) return qnn::mk::packed_w_u4_bytes(g);
+    if (w_dt == QNN_S8) return qnn::gemm::packed_b_bytes(g->OC, g->FH * g->FW * g->C);
     return 0;
 }
 
-extern "C" qnn_status qconv_prepack_w(const void *, qnn_dtype, const qnn_conv_geom *, void *, int32_t *,
-                                      qnn_stream_t)
+extern "C" qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_conv_geom *g,
+                                      void *W_packed, int32_t *colsum, qnn_stream_t stream)
 {
-    return QNN_ERR_UNSUPPORTED;
+    if (!W || !W_packed || !qnn::mk::geom_ok(g)) return QNN_ERR_INVALID_ARG;
+    const int K = g->FH * g->FW * g->C;
+    if (w_dt == QNN_S8) {
+        // filters [OC][FH][FW][C] are the GEMM operand B [OC, K]
+        return qgemm_prepack_b(static_cast<const int8_t *>(W), g->OC, K, W_packed, colsum, stream);
+    }
+    if (w_dt != QNN_S4) return QNN_ERR_UNSUPPORTED;
+    if (g->C % 2 != 0) return QNN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W_packed) & 1023u) != 0) return QNN_ERR_ALIGNMENT;
+    const int KT = (K + 127) / 128;
+    const int64_t nchunks = (int64_t)(qnn::mk::packed_w_u4_bytes(g) / 16);
+    int64_t blocks = (nchunks + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    cudaStream_t s = (cudaStream_t)stream;
+    qnn::mk::prepack_w_s4_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(W), g->OC, K,
+                                                               KT, static_cast<uint8_t *>(W_packed),
+                                                               nchunks);
+    if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
+    if (colsum) {
+        const int64_t threads = (int64_t)g->OC * 32;
+        qnn::mk::colsum_s4_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(
+            static_cast<const uint8_t *>(W), g->OC, K, colsum);
+        return qnn::launch_status();
+    }
+    return QNN_OK;
 }
 
-extern "C" qnn_status qconv_u4s4(const void *, int32_t, const void *, const qnn_conv_geom *,
-                                 const qnn_epilogue *, void *, int32_t *, qnn_stream_t)
+extern "C" qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed,
+                                 const qnn_conv_geom *g, const qnn_epilogue *e, void *O,
+                                 int32_t *O_s32, qnn_stream_t stream)
 {
-    return QNN_ERR_UNSUPPORTED;
+    return qnn::mk::conv_run<qnn::mk::ConvU4Op>(I, z_in, W_packed, g, e, O, O_s32, stream, true);
 }
 
-extern "C" qnn_status qconv_u8s8(const void *, int32_t, const void *, const qnn_conv_geom *,
-                                 const qnn_epilogue *, void *, int32_t *, qnn_stream_t)
+extern "C" qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_packed,
+                                 const qnn_conv_geom *g, const qnn_epilogue *e, void *O,
+                                 int32_t *O_s32, qnn_stream_t stream)
 {
-    return QNN_ERR_UNSUPPORTED;
+    return qnn::mk::conv_run<qnn::mk::ConvU8Op>(I, z_in, W_packed, g, e, O, O_s32, stream, false);
 }

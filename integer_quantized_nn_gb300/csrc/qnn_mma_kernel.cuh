@@ -1,0 +1,562 @@
+// qnn_mma_kernel.cuh -- the persistent, warp-specialised tcgen05 kernel shared
+// by the quantized GEMM and the implicit-GEMM convolutions.
+//
+// Both compute, for rows r (GEMM rows, or output pixels (n, oh, ow)) and
+// columns n (output channels),
+//     acc[r][n] = sum_k a(r, k) * B[n][k]            (exact integers)
+// followed by the fused epilogue of qnn.h (zero-point term, requant / dequant
+// / raw int32).  What differs between the ops is only how a row of the
+// activation operand is fetched and re-encoded for the MMA; that is the `Op`
+// policy (load / store of one pipeline unit, plus the MMA kind):
+//   GemmOp<PTF>  : int8 rows of A [M, K] -> fp16 (kind::f16)
+//   ConvU8Op     : im2col of u8 NHWC      -> fp16 (kind::f16)
+//   ConvU4Op     : im2col of u4 NHWC      -> e4m3 codes of c / 512 (kind::f8f6f4)
+//
+// Warp roles (512 threads, one CTA per SM, persistent over 128 x TBN tiles):
+//   warps 0-3  : converters -- fetch the activation rows of one pipeline unit
+//                (128 rows x one K step) from global memory, one unit ahead,
+//                re-encode them and store them into the 128-byte swizzled
+//                K-major stage buffer.
+//   warp 4     : TMA producer -- one bulk copy per stage of the prepacked
+//                weight tile (already in the swizzled image).
+//   warp 5     : TMEM owner and MMA issuer -- 4 x tcgen05.mma per stage into
+//                one of two TBN-column fp32 TMEM accumulators.
+//   warps 8-15 : epilogue -- tcgen05.ld, fp32 -> int32 (exact), optional
+//                int32 sums over K chunks, then the fused requant / dequant
+//                math and 16-byte stores of 32 consecutive output columns.
+// Every mbarrier wait is bounded (qnn_ptx.cuh): on time-out the role sets the
+// device status word and winds down instead of hanging.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include "qnn_gemm_layout.h"
+#include "qnn_internal.h"
+#include "qnn_ptx.cuh"
+
+namespace qnn {
+namespace mk {
+
+using gemm::BM;
+using gemm::ROW_BYTES;
+
+constexpr int STAGES = 4;
+constexpr int NUM_THREADS = 512;
+constexpr int PRODUCER_WARP = 4;
+constexpr int MMA_WARP = 5;
+constexpr int EPI_WARP0 = 8;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int A_STAGE_BYTES = BM * ROW_BYTES;
+
+struct Params {
+    // activation operand
+    const uint8_t *A;
+    int a_u8;                // GEMM: 1 if A holds u8 codes (centred at 128), 0 for s8
+    const uint8_t *ptf;      // GEMM: per-K Power-of-Two Factor shifts, or null
+    // convolution geometry (NHWC input, OHWI weights, K order (fh, fw, c))
+    int H, W, Cin, OHW, OW, FH, FW, ph, pw, sh, sw;
+    uint32_t pad_word;       // input bytes that stand for the padding value z_in
+    // weights (prepacked image) and shape of the GEMM view
+    const uint8_t *Bp;
+    int M, N, K, KT, num_m, num_tiles;
+    int chunk_steps, nchunks;
+    // epilogue
+    int mode, relu, z_out, out_bits;
+    float qmin, qmax;
+    const int32_t *zp;
+    const float *Mv;
+    const float *Bq;
+    const float *D;
+    const float *bias;
+    const uint8_t *res;
+    int res_bits, res_signed, z_res;
+    float R;
+    void *C;
+    int32_t *C32;
+    int vec_ok;              // N % 32 == 0: every 32-column piece whole and 16-byte aligned
+    uint32_t *status;
+};
+
+template <int TBN>
+struct __align__(1024) Smem {
+    uint8_t a[STAGES][A_STAGE_BYTES];
+    uint8_t b[STAGES][TBN * ROW_BYTES];
+    uint64_t a_full[STAGES];
+    uint64_t b_full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+};
+
+template <int TBN>
+constexpr size_t smem_bytes() { return sizeof(Smem<TBN>) + 1024; }
+
+// Which tile a unit (tile iteration, K step) of this CTA belongs to.
+__device__ __forceinline__ int unit_tile(const Params &p, int j) { return blockIdx.x + (j / p.KT) * gridDim.x; }
+
+// ---------------------------------------------------------------- converter
+template <class Op, int TBN>
+__device__ __forceinline__ bool convert_one(const Params &p, Smem<TBN> &s, int j, int sub, int rbase,
+                                            const typename Op::Unit &u)
+{
+    const int stage = j % STAGES;
+    const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
+    if (!mbar_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status)) return false;
+    Op::store(p, smem_u32(&s.a[stage][0]), sub, rbase, u);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&s.a_full[stage]));
+    return true;
+}
+
+// Thread t handles the 16-byte input group (t % 4) of rows (t / 4) + 32 q,
+// q = 0..3; the next unit's loads are in flight while a unit is converted.
+template <class Op, int TBN>
+__device__ void converter_role(const Params &p, Smem<TBN> &s, int units)
+{
+    const int tid = threadIdx.x;
+    const int sub = tid & 3;
+    const int rbase = tid >> 2;
+    typename Op::State st;
+    typename Op::Unit u0, u1;
+    if (units > 0) Op::load(p, st, 0, sub, rbase, u0);
+    for (int j = 0; j < units; j += 2) {
+        if (j + 1 < units) Op::load(p, st, j + 1, sub, rbase, u1);
+        if (!convert_one<Op, TBN>(p, s, j, sub, rbase, u0)) return;
+        if (j + 1 < units) {
+            if (j + 2 < units) Op::load(p, st, j + 2, sub, rbase, u0);
+            if (!convert_one<Op, TBN>(p, s, j + 1, sub, rbase, u1)) return;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- producer
+template <int TBN>
+__device__ void producer_role(const Params &p, Smem<TBN> &s, int units)
+{
+    bool ok = true;
+    int j = 0;
+    for (; j < units; ++j) {
+        const int stage = j % STAGES;
+        const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
+        if (!mbar_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status)) {
+            ok = false;
+            break;
+        }
+        const int t = unit_tile(p, j);
+        const int ks = j % p.KT;
+        // columns n0 .. n0 + TBN - 1 live in the 256-row packed block n0 / 256
+        const int n0 = (t / p.num_m) * TBN;
+        const uint8_t *src = p.Bp + ((int64_t)(n0 / gemm::BN) * p.KT + ks) * gemm::B_STAGE_BYTES +
+                             (int64_t)(n0 % gemm::BN) * ROW_BYTES;
+        const uint32_t bar = smem_u32(&s.b_full[stage]);
+        mbar_arrive_expect_tx(bar, TBN * ROW_BYTES);
+        bulk_g2s(smem_u32(&s.b[stage][0]), src, TBN * ROW_BYTES, bar);
+    }
+    if (!ok) {
+        // wind down: let the copies already issued land before the CTA exits
+        for (int i = (j > STAGES ? j - STAGES : 0); i < j; ++i) {
+            const int stage = i % STAGES;
+            const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+            if (!mbar_wait(smem_u32(&s.b_full[stage]), ph, p.status)) break;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- MMA
+template <bool F8, int TBN>
+__device__ void mma_role(const Params &p, Smem<TBN> &s, int my_tiles, uint32_t tmem)
+{
+    constexpr uint32_t IDESC = idesc_f32acc(0, 0, BM, TBN);  // f16 x f16, or e4m3 x e4m3
+    uint32_t u = 0;  // accumulation chunk counter
+    uint32_t abuf = 0;
+    bool ok = true;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+        for (int ks = 0; ks < p.KT; ++ks) {
+            const int j = i * p.KT + ks;
+            const int stage = j % STAGES;
+            const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
+            const bool first = (ks % p.chunk_steps) == 0;
+            if (first) {
+                abuf = u & 1u;
+                if (!mbar_wait(smem_u32(&s.acc_empty[abuf]), ((u >> 1) & 1u) ^ 1u, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (!mbar_wait(smem_u32(&s.a_full[stage]), ph, p.status) ||
+                !mbar_wait(smem_u32(&s.b_full[stage]), ph, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(&s.a[stage][0]);
+            const uint32_t b0 = smem_u32(&s.b[stage][0]);
+            const uint32_t d = tmem + abuf * TBN;
+            // 4 MMAs of 32 bytes of K each: 16 fp16 or 32 e4m3 values
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                if (F8)
+                    mma_f8f6f4_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), IDESC, acc);
+                else
+                    mma_f16_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), IDESC, acc);
+            }
+            mma_commit(smem_u32(&s.empty[stage]));
+            const bool last = ((ks % p.chunk_steps) == p.chunk_steps - 1) || (ks == p.KT - 1);
+            if (last) {
+                mma_commit(smem_u32(&s.acc_full[abuf]));
+                ++u;
+            }
+        }
+    }
+    // every MMA issued must have completed before the CTA winds down
+    mma_commit(smem_u32(&s.mma_done));
+    (void)mbar_wait(smem_u32(&s.mma_done), 0u, p.status);
+}
+
+// ---------------------------------------------------------------- epilogue
+__device__ __forceinline__ void st_v4(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    *reinterpret_cast<uint4 *>(ptr) = make_uint4(a, b, c, d);
+}
+
+// Residual code of column i of a 32-column piece held in rw (8-bit: 8 words of
+// 4 codes; 4-bit: 4 words of 8 codes).
+__device__ __forceinline__ int32_t res_code(const Params &p, const uint32_t (&rw)[8], int i)
+{
+    int32_t v;
+    if (p.res_bits == 8) {
+        v = (int32_t)((rw[i >> 2] >> (8 * (i & 3))) & 255u);
+        if (p.res_signed && v >= 128) v -= 256;
+    } else {
+        v = (int32_t)((rw[i >> 3] >> (4 * (i & 7))) & 15u);
+        if (p.res_signed && v >= 8) v -= 16;
+    }
+    return v;
+}
+
+// Requant / dequant / raw store of the 32 consecutive columns n0.. of row m.
+// Works in place on `ac` (the raw accumulators on entry).
+__device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, int32_t (&ac)[32])
+{
+    if (m >= p.M || n0 >= p.N) return;
+    const bool vec = p.vec_ok;
+    if (p.zp) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (vec || n0 + i < p.N) ac[i] -= __ldg(p.zp + n0 + i);
+    }
+    const int64_t base = (int64_t)m * p.N + n0;  // element offset of (m, n0)
+    if (p.C32) {
+        if (vec) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                st_v4(p.C32 + base + i, ac[i], ac[i + 1], ac[i + 2], ac[i + 3]);
+        } else {
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) p.C32[base + i] = ac[i];
+        }
+    }
+    if (p.mode == QNN_EPI_S32) {
+        int32_t *C = static_cast<int32_t *>(p.C);
+        if (vec) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) st_v4(C + base + i, ac[i], ac[i + 1], ac[i + 2], ac[i + 3]);
+        } else {
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = ac[i];
+        }
+        return;
+    }
+    if (p.mode == QNN_EPI_DEQUANT) {
+        float *C = static_cast<float *>(p.C);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int n = (vec || n0 + i < p.N) ? n0 + i : n0;
+            const float b = p.bias ? __ldg(p.bias + n) : 0.0f;
+            ac[i] = __float_as_int(__fadd_rn(__fmul_rn(__int2float_rn(ac[i]), __ldg(p.D + n)), b));
+        }
+        if (vec) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) st_v4(C + base + i, ac[i], ac[i + 1], ac[i + 2], ac[i + 3]);
+        } else {
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = __int_as_float(ac[i]);
+        }
+        return;
+    }
+    // REQUANT
+    uint32_t rw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rw[i] = 0;
+    if (p.res) {
+        if (p.res_bits == 8) {
+            if (vec) {
+                const uint4 r0 = ldg_nc_v4(p.res + base), r1 = ldg_nc_v4(p.res + base + 16);
+                rw[0] = r0.x; rw[1] = r0.y; rw[2] = r0.z; rw[3] = r0.w;
+                rw[4] = r1.x; rw[5] = r1.y; rw[6] = r1.z; rw[7] = r1.w;
+            } else {
+                for (int i = 0; i < 32 && n0 + i < p.N; ++i)
+                    rw[i >> 2] |= (uint32_t)p.res[base + i] << (8 * (i & 3));
+            }
+        } else {
+            if (vec) {
+                const uint4 r0 = ldg_nc_v4(p.res + base / 2);
+                rw[0] = r0.x; rw[1] = r0.y; rw[2] = r0.z; rw[3] = r0.w;
+            } else {
+                for (int i = 0; i < 32 && n0 + i < p.N; i += 2)
+                    rw[i >> 3] |= (uint32_t)p.res[(base + i) / 2] << (4 * (i & 7));
+            }
+        }
+    }
+    const float zo = (float)p.z_out;
+    int32_t q[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int n = (vec || n0 + i < p.N) ? n0 + i : n0;
+        float t = __ldg(p.Bq + n);
+        if (p.res) t = __fadd_rn(__fmul_rn(__int2float_rn(res_code(p, rw, i) - p.z_res), p.R), t);
+        const float v = __fadd_rn(__fmul_rn(__int2float_rn(ac[i]), __ldg(p.Mv + n)), t);
+        float r = rintf(v);
+        if (p.relu) r = fmaxf(r, 0.0f);
+        q[i] = __float2int_rn(fminf(fmaxf(__fadd_rn(r, zo), p.qmin), p.qmax));
+    }
+    uint8_t *C = static_cast<uint8_t *>(p.C);
+    if (p.out_bits == 8) {
+        uint32_t ow[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            ow[w] = (q[4 * w] & 255) | ((q[4 * w + 1] & 255) << 8) | ((q[4 * w + 2] & 255) << 16) |
+                    ((uint32_t)q[4 * w + 3] << 24);
+        if (vec) {
+            st_v4(C + base, ow[0], ow[1], ow[2], ow[3]);
+            st_v4(C + base + 16, ow[4], ow[5], ow[6], ow[7]);
+        } else {
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = (uint8_t)(ow[i >> 2] >> (8 * (i & 3)));
+        }
+    } else {
+        uint32_t ow[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) word |= (uint32_t)(q[8 * w + b] & 15) << (4 * b);
+            ow[w] = word;
+        }
+        if (vec) {
+            st_v4(C + base / 2, ow[0], ow[1], ow[2], ow[3]);
+        } else {
+            // N is even: a byte holds columns (2i, 2i+1) of this thread's row only
+            for (int i = 0; i < 32 && n0 + i < p.N; i += 2)
+                C[(base + i) / 2] = (uint8_t)(ow[i >> 3] >> (4 * (i & 7)));
+        }
+    }
+}
+
+// fp32 accumulator value -> exact int32 (the fp32 value times 2^scale_log2 is an integer)
+template <int SCALE_LOG2>
+__device__ __forceinline__ int32_t acc_to_int(uint32_t bits)
+{
+    float f = __uint_as_float(bits);
+    if (SCALE_LOG2 != 0) f = __fmul_rn(f, (float)(1 << SCALE_LOG2));
+    return __float2int_rn(f);
+}
+
+// MULTI == false: one accumulation chunk per tile; each epilogue thread owns
+// one row and TBN / 2 columns, converted and stored 32 at a time from TMEM.
+// MULTI == true : K is cut into exact chunks; each thread keeps int32 sums for
+// its row and TBN / 2 columns in registers across the chunks.
+template <int TBN, bool MULTI, int SCALE_LOG2>
+__device__ void epilogue_role(const Params &p, Smem<TBN> &s, int my_tiles, uint32_t tmem)
+{
+    constexpr int COLS = TBN / 2;
+    constexpr int PIECES = COLS / 32;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int quad = warp & 3;                 // TMEM lanes 32*quad .. +31
+    const int half = (warp - EPI_WARP0) >> 2;  // columns COLS*half .. +COLS-1
+    uint32_t u = 0;
+    for (int i = 0; i < my_tiles; ++i) {
+        const int t = blockIdx.x + i * gridDim.x;
+        const int m = (t % p.num_m) * BM + quad * 32 + lane;
+        const int nbase = (t / p.num_m) * TBN + half * COLS;
+        if (!MULTI) {
+            const uint32_t abuf = u & 1u;
+            if (!mbar_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + half * COLS;
+#pragma unroll 1
+            for (int jp = 0; jp < PIECES; ++jp) {
+                uint32_t r[32];
+                tmem_ld32(taddr + jp * 32, r);
+                tmem_ld_wait();
+                int32_t acc[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) acc[k] = acc_to_int<SCALE_LOG2>(r[k]);
+                if (jp == PIECES - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
+                }
+                epilogue_piece(p, m, nbase + jp * 32, acc);
+            }
+            ++u;
+        } else {
+            int32_t acc[PIECES][32];
+            for (int c = 0; c < p.nchunks; ++c) {
+                const uint32_t abuf = u & 1u;
+                if (!mbar_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + half * COLS;
+#pragma unroll
+                for (int jp = 0; jp < PIECES; ++jp) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + jp * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int32_t v = acc_to_int<SCALE_LOG2>(r[k]);
+                        acc[jp][k] = (c == 0) ? v : acc[jp][k] + v;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
+                ++u;
+            }
+#pragma unroll
+            for (int jp = 0; jp < PIECES; ++jp) epilogue_piece(p, m, nbase + jp * 32, acc[jp]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+template <class Op, int TBN, bool MULTI>
+__global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_constant__ Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem<TBN> &s = *reinterpret_cast<Smem<TBN> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                  ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(smem_u32(&s.a_full[i]), 4);
+            mbar_init(smem_u32(&s.b_full[i]), 1);
+            mbar_init(smem_u32(&s.empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&s.acc_full[i]), 1);
+            mbar_init(smem_u32(&s.acc_empty[i]), NUM_EPI_WARPS);
+        }
+        mbar_init(smem_u32(&s.mma_done), 1);
+        fence_mbar_init();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_u32(&s.tmem_base), 2 * TBN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+
+    const int my_tiles =
+        (blockIdx.x < p.num_tiles) ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int units = my_tiles * p.KT;
+
+    // register split of the multi-chunk kernel: 128*96 + 128*56 + 256*176 = 64512 <= 65536
+    if (warp < 4) {
+        if (MULTI) regs_dec<96>();
+        converter_role<Op, TBN>(p, s, units);
+    } else if (warp < 8) {
+        if (MULTI) regs_dec<56>();
+        if (warp == PRODUCER_WARP && lane == 0) producer_role<TBN>(p, s, units);
+        if (warp == MMA_WARP && lane == 0) mma_role<Op::F8, TBN>(p, s, my_tiles, tmem);
+        __syncwarp();
+    } else {
+        if (MULTI) regs_inc<176>();
+        epilogue_role<TBN, MULTI, Op::SCALE_LOG2>(p, s, my_tiles, tmem);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == MMA_WARP) tmem_dealloc(tmem, 2 * TBN);
+}
+
+template <class Op, int TBN, bool MULTI>
+qnn_status launch(Params p, cudaStream_t stream)
+{
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QNN_ERR_CUDA;
+    constexpr size_t SMEM = smem_bytes<TBN>();
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(qmma_kernel<Op, TBN, MULTI>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) != cudaSuccess)
+            return QNN_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    p.num_tiles = p.num_m * ((p.N + TBN - 1) / TBN);
+    int grid = qnn::sm_count();
+    if (grid > p.num_tiles) grid = p.num_tiles;
+    qmma_kernel<Op, TBN, MULTI><<<grid, NUM_THREADS, SMEM, stream>>>(p);
+    return launch_status();
+}
+
+// Shared host-side validation of the epilogue descriptor.  out_bits / res_bits
+// say how the op stores quantized outputs and residuals.
+inline qnn_status setup_epilogue(const qnn_epilogue *e, bool conv, Params &p)
+{
+    p.mode = e->mode;
+    p.relu = e->relu ? 1 : 0;
+    p.z_out = e->z_out;
+    p.zp = e->zp_term;
+    p.Mv = e->M;
+    p.Bq = e->Bq;
+    p.D = e->D;
+    p.bias = e->bias;
+    switch (e->mode) {
+    case QNN_EPI_REQUANT: {
+        if (!e->M || !e->Bq) return QNN_ERR_INVALID_ARG;
+        const bool ok_dt = conv ? (e->out_dt == QNN_U4 || e->out_dt == QNN_U8 || e->out_dt == QNN_S8)
+                                : (e->out_dt == QNN_S8 || e->out_dt == QNN_U8);
+        if (!ok_dt) return QNN_ERR_UNSUPPORTED;
+        int32_t lo, hi;
+        qrange(e->out_dt, 0, &lo, &hi);
+        if (e->z_out < lo || e->z_out > hi) return QNN_ERR_INVALID_ARG;
+        p.qmin = (float)lo;
+        p.qmax = (float)hi;
+        p.out_bits = (e->out_dt == QNN_U4) ? 4 : 8;
+        if (e->residual) {
+            const bool ok_r = conv ? (e->res_dt == QNN_U4 || e->res_dt == QNN_U8 || e->res_dt == QNN_S8 ||
+                                      e->res_dt == QNN_S4)
+                                   : (e->res_dt == QNN_S8 || e->res_dt == QNN_U8);
+            if (!ok_r) return QNN_ERR_UNSUPPORTED;
+            if (!aligned16(e->residual)) return QNN_ERR_ALIGNMENT;
+            p.res = static_cast<const uint8_t *>(e->residual);
+            p.res_bits = (e->res_dt == QNN_U4 || e->res_dt == QNN_S4) ? 4 : 8;
+            p.res_signed = (e->res_dt == QNN_S8 || e->res_dt == QNN_S4);
+            p.z_res = e->z_res;
+            p.R = e->R;
+        }
+        break;
+    }
+    case QNN_EPI_DEQUANT:
+        if (!e->D) return QNN_ERR_INVALID_ARG;
+        if (e->residual) return QNN_ERR_UNSUPPORTED;
+        break;
+    case QNN_EPI_S32:
+        if (e->residual) return QNN_ERR_UNSUPPORTED;
+        break;
+    default:
+        return QNN_ERR_INVALID_ARG;
+    }
+    return QNN_OK;
+}
+
+}  // namespace mk
+}  // namespace qnn

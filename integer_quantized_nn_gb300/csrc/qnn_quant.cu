@@ -176,18 +176,21 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const QArgs a)
 qnn_status prepare(const void *x, const void *q, int q_dt, int ndim, const int64_t *shape,
                    const qnn_qparams *p, QArgs *a)
 {
-    if (!x || !q || !shape || !p || ndim < 1 || ndim > 16) return QNN_ERR_INVALID_ARG;
+    if (!shape || !p || ndim < 1 || ndim > 16) return QNN_ERR_INVALID_ARG;
+    int64_t n = 1;
+    for (int i = 0; i < ndim; ++i) {
+        if (shape[i] < 0) return QNN_ERR_INVALID_ARG;
+        n *= shape[i];
+    }
+    a->n = n;
+    if (n == 0) return QNN_OK;  // nothing to do; pointers of empty tensors may be null
+    if (!x || !q) return QNN_ERR_INVALID_ARG;
     int32_t lo, hi;
     if (!qrange(q_dt, p->narrow_range, &lo, &hi)) return QNN_ERR_INVALID_ARG;
     if (p->scheme < QNN_SYM || p->scheme > QNN_POW2) return QNN_ERR_INVALID_ARG;
     if (p->scheme == QNN_POW2 && !p->shift) return QNN_ERR_INVALID_ARG;
     if (p->scheme != QNN_POW2 && !p->scale) return QNN_ERR_INVALID_ARG;
     if (p->scheme == QNN_ASYM && !p->zero_point) return QNN_ERR_INVALID_ARG;
-    int64_t n = 1;
-    for (int i = 0; i < ndim; ++i) {
-        if (shape[i] < 0) return QNN_ERR_INVALID_ARG;
-        n *= shape[i];
-    }
     const int bits = (q_dt == QNN_S4 || q_dt == QNN_U4) ? 4 : 8;
     if (bits == 4 && (shape[ndim - 1] % 2) != 0) return QNN_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(q)) return QNN_ERR_ALIGNMENT;

@@ -72,7 +72,7 @@ def _declare(L):
         "qgemm_prepack_b": (c_int, [vp, c_int, c_int, vp, vp, vp]),
         "q_fold_epilogue": (c_int, [c_int, c_int, i32, vp, f32, vp, c_int, vp, f32, vp, vp, vp, vp, vp]),
         "qgemm_s8": (c_int, [vp, c_int, vp, c_int, c_int, c_int, vp, vp, vp, vp]),
-        "qnn_conv_packed_w_bytes": (sz, [vp]),
+        "qnn_conv_packed_w_bytes": (sz, [vp, c_int]),
         "qconv_prepack_w": (c_int, [vp, c_int, vp, vp, vp, vp]),
         "qconv_u4s4": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
         "qconv_u8s8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
@@ -200,9 +200,9 @@ def conv_geom(N, H, W, C, OC, FH, FW, pad=(1, 1), stride=(1, 1)) -> ConvGeom:
     return ConvGeom(N, H, W, C, OC, FH, FW, pad[0], pad[1], stride[0], stride[1])
 
 
-def qnn_conv_packed_w_bytes(g: ConvGeom) -> int:
+def qnn_conv_packed_w_bytes(g: ConvGeom, w_dt: str = "s4") -> int:
     load()
-    return int(_SYMBOLS["qnn_conv_packed_w_bytes"](ctypes.byref(g)))
+    return int(_SYMBOLS["qnn_conv_packed_w_bytes"](ctypes.byref(g), DTYPES[w_dt]))
 
 
 def qconv_prepack_w(W, w_dt: str, g: ConvGeom, W_packed, colsum=None, stream=None):

@@ -1,0 +1,208 @@
+"""qconv_u4s4 / qconv_u8s8 (implicit-GEMM convolution, fused Conv_Relu /
+Conv_Add_Relu) on the GPU against the CPU oracle's direct convolution:
+bit-exact int32 accumulators and quantized outputs."""
+import numpy as np
+import pytest
+
+from integer_quantized_nn_gb300 import qnn, workloads
+from _util import dev, host, aligned_empty, f32_bits, torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="requant",
+          out_dt="u4", relu=True, z_out=0, res=None, res_dt="u4", z_res=8, s_r=None,
+          full=True, pixels=None):
+    """Runs the conv on both sides.  I_pk / W_pk: packed u4 / s4 bytes (u4=True)
+    or u8 / s8 codes (u4=False), NHWC / OHWI."""
+    t = torch()
+    N, H, W, C, OC, F, pad, st = geom
+    g = qnn.conv_geom(N, H, W, C, OC, F, F, (pad, pad), (st, st))
+    OH, OW = g.OH, g.OW
+    w_dt = "s4" if u4 else "s8"
+    Wd = dev(W_pk)
+    Wp = aligned_empty(qnn.qnn_conv_packed_w_bytes(g, w_dt))
+    colsum = t.empty(OC, dtype=t.int32, device="cuda")
+    qnn.qconv_prepack_w(Wd, w_dt, g, Wp, colsum)
+    a_dt = "u4" if u4 else "u8"
+    sw = dev(np.asarray(s_w, np.float32))
+    bd = dev(np.asarray(bias, np.float32))
+    zp = t.empty(OC, dtype=t.int32, device="cuda")
+    Mv = t.empty(OC, dtype=t.float32, device="cuda")
+    Bq = t.empty(OC, dtype=t.float32, device="cuda")
+    D = t.empty(OC, dtype=t.float32, device="cuda")
+    qnn.q_fold_epilogue(OC, a_dt, z_in, colsum, s_a, sw, s_o, bias=bd, zp_term=zp, M=Mv, Bq=Bq, D=D)
+    R = 0.0 if s_r is None else float(np.float32(np.float32(s_r) / np.float32(s_o)))
+    resd = None if res is None else dev(res)
+    epi = qnn.epilogue(mode, relu=relu, out_dt=out_dt, z_out=z_out, zp_term=zp, M=Mv, Bq=Bq, D=D,
+                       bias=bd, residual=resd, res_dt=res_dt, z_res=z_res, R=R)
+    rows = N * OH * OW
+    if mode == "requant":
+        ob = OC // 2 if out_dt == "u4" else OC
+        O = t.full((N, OH, OW, ob), 0x5A, dtype=t.uint8, device="cuda")
+    elif mode == "dequant":
+        O = t.empty((N, OH, OW, OC), dtype=t.float32, device="cuda")
+    else:
+        O = t.empty((N, OH, OW, OC), dtype=t.int32, device="cuda")
+    O32 = t.zeros((N, OH, OW, OC), dtype=t.int32, device="cuda")
+    Id = dev(I_pk)
+    fn = qnn.qconv_u4s4 if u4 else qnn.qconv_u8s8
+    fn(Id, z_in, Wp, g, epi, O, O32)
+    assert qnn.qnn_check_device_error() == qnn.QNN_OK
+
+    # oracle side
+    if u4:
+        Ic = oracle.unpack_nibbles(I_pk, signed=False)
+        Wc = oracle.unpack_nibbles(W_pk, signed=True)
+    else:
+        Ic = I_pk.astype(np.int32)
+        Wc = W_pk.astype(np.int8).astype(np.int32)
+    cs = oracle.colsum(Wc.reshape(OC, -1))
+    assert np.array_equal(host(colsum), cs)
+    zc = z_in - (0 if u4 else 128)
+    zp_o, M_o, Bq_o, D_o = oracle.fold(cs, zc, s_a, np.asarray(s_w, np.float32), s_o, bias)
+    assert np.array_equal(host(zp), zp_o)
+    if full:
+        acc = oracle.conv_acc_direct(Ic, Wc, z_in, (pad, pad), (st, st))
+        sel = np.arange(rows)
+    else:
+        # sampled output pixels: direct conv on the receptive fields they need
+        sel = pixels
+        acc_all = []
+        for pix in sel:
+            n_, rem = divmod(int(pix), OH * OW)
+            oy, ox = divmod(rem, OW)
+            sub = Ic[n_:n_ + 1]
+            a = oracle.conv_acc_direct(sub, Wc, z_in, (pad, pad), (st, st))
+            acc_all.append(a[oy * OW + ox])
+        acc = np.stack(acc_all)
+    got32 = host(O32).reshape(rows, OC)[sel]
+    assert np.array_equal(got32, acc), f"{(got32 != acc).sum()} accumulator mismatches"
+    Og = host(O)
+    if mode == "s32":
+        assert np.array_equal(Og.reshape(rows, OC)[sel], acc)
+        return acc
+    if mode == "dequant":
+        y = oracle.dequant_epilogue(acc, D_o, bias)
+        assert np.array_equal(f32_bits(Og.reshape(rows, OC)[sel]), f32_bits(y))
+        return acc
+    res_codes = None
+    if res is not None:
+        if res_dt == "u4":
+            res_codes = oracle.unpack_nibbles(res, signed=False).reshape(rows, OC)[sel]
+        else:
+            res_codes = res.reshape(rows, OC)[sel].astype(np.int32)
+    q = oracle.requant(acc, M_o, Bq_o, out_dt, relu=relu, res=res_codes, z_res=z_res, R=R, z_out=z_out)
+    exp = oracle.pack_nibbles(q) if out_dt == "u4" else oracle.pack_bytes(q)
+    got = Og.reshape(rows, -1)[sel]
+    assert np.array_equal(got, exp), f"{(got != exp).sum()} output bytes differ"
+    return acc
+
+
+def _rand_u4s4(seed, N, H, W, C, OC, F, with_res=True, OH=None, OW=None):
+    rng = np.random.default_rng(seed)
+    I = rng.integers(0, 256, size=(N, H, W, C // 2)).astype(np.uint8)
+    Wt = rng.integers(0, 256, size=(OC, F, F, C // 2)).astype(np.uint8)
+    s_w = rng.uniform(1e-3, 1e-2, size=OC).astype(np.float32)
+    bias = rng.normal(0, 1, size=OC).astype(np.float32)
+    res = None
+    if with_res:
+        res = rng.integers(0, 256, size=(N, OH or H, OW or W, OC // 2)).astype(np.uint8)
+    return I, Wt, s_w, bias, res
+
+
+@pytest.mark.parametrize("geom", [
+    (2, 9, 9, 64, 64, 3, 1, 1),      # ragged pixel tail, Conv_Add_Relu
+    (1, 7, 11, 32, 96, 3, 1, 1),     # C = 32, OC = 96 (N not a multiple of 32 per piece)
+    (2, 10, 10, 64, 128, 3, 1, 2),   # stride 2
+    (1, 6, 6, 128, 256, 3, 0, 1),    # no padding, OC = 256
+    (3, 5, 5, 64, 320, 1, 0, 1),     # 1x1, two filter blocks
+])
+def test_conv_u4s4_small(oracle, geom):
+    N, H, W, C, OC, F, pad, st = geom
+    OH = (H + 2 * pad - F) // st + 1
+    OW = (W + 2 * pad - F) // st + 1
+    I, Wt, s_w, bias, res = _rand_u4s4(31, N, H, W, C, OC, F, True, OH, OW)
+    _conv(oracle, I, Wt, geom, 8, 0.05, s_w, 0.11, bias, res=res, s_r=0.13)
+
+
+@pytest.mark.parametrize("mode", ["dequant", "s32"])
+def test_conv_u4s4_modes(oracle, mode):
+    geom = (1, 8, 8, 64, 64, 3, 1, 1)
+    I, Wt, s_w, bias, _ = _rand_u4s4(32, 1, 8, 8, 64, 64, 3, False)
+    _conv(oracle, I, Wt, geom, 5, 0.05, s_w, 0.11, bias, mode=mode)
+
+
+def test_conv_u4s4_relu_u8_out(oracle):
+    geom = (1, 8, 8, 64, 64, 3, 1, 1)
+    I, Wt, s_w, bias, _ = _rand_u4s4(33, 1, 8, 8, 64, 64, 3, False)
+    _conv(oracle, I, Wt, geom, 3, 0.05, s_w, 0.011, bias, out_dt="u8", relu=True, z_out=7)
+
+
+def test_conv_u4s4_exactness_large_sums(oracle):
+    """C = 1024: |acc| reaches 9216 * 120; in the e4m3 scaling (2^-9) the fp32
+    sums need 20+ significant bits, so any truncation in the accumulation shows."""
+    geom = (1, 6, 6, 1024, 64, 3, 1, 1)
+    I = np.full((1, 6, 6, 512), 0xFF, np.uint8)            # every code 15
+    Wt = np.full((64, 3, 3, 512), 0x88, np.uint8)           # every weight -8
+    rng = np.random.default_rng(34)
+    I[0, 2, 2, :64] = rng.integers(0, 256, size=64).astype(np.uint8)
+    Wt[::3, 1, 1, :16] = 0x11                               # +1 weights mixed in
+    s_w = np.full(64, 1e-3, np.float32)
+    acc = _conv(oracle, I, Wt, geom, 0, 1.0, s_w, 1000.0, np.zeros(64, np.float32), mode="s32")
+    assert np.abs(acc).max() >= 9216 * 100
+
+
+def test_conv_resnet_3x3_full(oracle):
+    """ResNet-50 stage-1 3x3 Conv_Add_Relu at full size (N=64, 56x56, 64 -> 64,
+    u4 x s4, u4 residual and output), every output compared."""
+    w = workloads.conv_u4()
+    geom = (64, 56, 56, 64, 64, 3, 1, 1)
+    _conv(oracle, w["I"], w["W"], geom, w["z_in"], w["s_a"], w["s_w"], w["s_o"], w["bias"],
+          res=w["res"], z_res=w["z_res"], s_r=w["s_r"])
+
+
+def test_conv_resnet_1x1_full(oracle):
+    """ResNet-50 stage-1 1x1 Conv_Relu (256 -> 64 channels) at full size."""
+    w = workloads.conv_u4(C=256, OC=64, F=1, pad=0, residual=False, tag=1)
+    geom = (64, 56, 56, 256, 64, 1, 0, 1)
+    _conv(oracle, w["I"], w["W"], geom, w["z_in"], w["s_a"], w["s_w"], w["s_o"], w["bias"])
+
+
+@pytest.mark.parametrize("geom", [(2, 9, 9, 64, 64, 3, 1, 1), (1, 7, 7, 256, 128, 3, 1, 1),
+                                  (1, 9, 9, 48, 64, 3, 1, 2)])
+def test_conv_u8s8(oracle, geom):
+    """u8 activations (zero point 100) x s8 filters; C = 256 3x3 has K = 2304,
+    above one exact fp32 chunk."""
+    N, H, W, C, OC, F, pad, st = geom
+    OH = (H + 2 * pad - F) // st + 1
+    OW = (W + 2 * pad - F) // st + 1
+    rng = np.random.default_rng(35)
+    I = rng.integers(0, 256, size=(N, H, W, C)).astype(np.uint8)
+    Wt = rng.integers(-128, 128, size=(OC, F, F, C)).astype(np.int8)
+    s_w = rng.uniform(1e-3, 1e-2, size=OC).astype(np.float32)
+    bias = rng.normal(0, 1, size=OC).astype(np.float32)
+    res = rng.integers(0, 256, size=(N, OH, OW, OC)).astype(np.uint8)
+    _conv(oracle, I, Wt, geom, 100, 0.02, s_w, 0.07, bias, u4=False, out_dt="u8", z_out=3,
+          res=res, res_dt="u8", z_res=120, s_r=0.05)
+
+
+def test_conv_errors():
+    t = torch()
+    g = qnn.conv_geom(1, 8, 8, 48, 64, 3, 3)
+    I = t.zeros(1024, dtype=t.uint8, device="cuda")
+    Wp = aligned_empty(1 << 20)
+    O = t.zeros(4096, dtype=t.uint8, device="cuda")
+    Mv = t.ones(64, dtype=t.float32, device="cuda")
+    epi = qnn.epilogue("requant", out_dt="u4", M=Mv, Bq=Mv)
+    with pytest.raises(qnn.QnnError) as e:
+        qnn.qconv_u4s4(I, 8, Wp, g, epi, O)     # C = 48 is not a multiple of 32
+    assert e.value.status == qnn.QNN_ERR_UNSUPPORTED
+    g = qnn.conv_geom(1, 8, 8, 64, 64, 3, 3)
+    with pytest.raises(qnn.QnnError) as e:
+        qnn.qconv_u4s4(I, 16, Wp, g, epi, O)    # zero point outside u4
+    assert e.value.status == qnn.QNN_ERR_INVALID_ARG
+    g = qnn.conv_geom(1, 2, 2, 64, 64, 5, 5, (0, 0))
+    with pytest.raises(qnn.QnnError) as e:
+        qnn.qconv_u4s4(I, 8, Wp, g, epi, O)     # filter larger than the padded input
+    assert e.value.status == qnn.QNN_ERR_INVALID_ARG
