@@ -375,6 +375,86 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
     return out
 
 
+def run_case(args):
+    """One workload only, for profiling: warmup + steps launches of its kernel
+    (L2 flushed before each), then a one-line JSON with the median time."""
+    import torch
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    from integer_quantized_nn_gb300 import qnn, workloads
+    qnn.load()
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    case = args.case
+    if case == "quantize":
+        R = Cc = 16384
+        x = workloads.device_normal_f32((R, Cc), 505, device)
+        scale = (x.abs().amax(dim=1) / 127.0).contiguous()
+        q = torch.empty((R, Cc), dtype=torch.uint8, device=device)
+        p = qnn.qparams("sym", scale=scale, per_channel=True, axis=0)
+        fn = lambda: qnn.q_quantize(x, q, "s8", p, stream=stream)  # noqa: E731
+    elif case in ("vit_fc1", "square_4096", "vitl_fc2"):
+        if case == "vit_fc1":
+            w, a_dt, alpha = workloads.vit_fc1(), "u8", None
+        elif case == "square_4096":
+            w, a_dt, alpha = workloads.gemm_square(4096), "s8", None
+        else:
+            v = workloads.vitl_ptf(M=12608, K=4096, N=1024)
+            xq = torch.from_numpy(v["x"]).to(device)
+            Aq = torch.empty(v["x"].shape, dtype=torch.uint8, device=device)
+            qnn.q_quantize(xq, Aq, "s8", qnn.qparams("sym", scale=torch.from_numpy(v["in_scale"]).to(device),
+                                                     per_channel=True, axis=1))
+            w = dict(A=Aq.cpu().numpy(), B=v["B"], s_w=v["s_w"], bias=v["bias"], s_a=v["s"], s_o=v["s_o"], z_a=0)
+            a_dt, alpha = "s8", v["alpha"]
+        Mm, Kk = w["A"].shape
+        Nn = w["B"].shape[0]
+        g = gpu_setup_gemm(torch, qnn, w, a_dt, device)
+        C = torch.empty((Mm, Nn), dtype=torch.uint8, device=device)
+        al = None if alpha is None else torch.from_numpy(alpha.astype(np.uint8)).to(device)
+        epi = qnn.epilogue("requant", zp_term=None if al is not None else g["zp"], M=g["M"], Bq=g["Bq"],
+                           ptf_shift=al, ptf_max_shift=0 if alpha is None else int(alpha.max()))
+        fn = lambda: qnn.qgemm_s8(g["A"], a_dt, g["Bp"], Mm, Nn, Kk, epi, C, stream=stream)  # noqa: E731
+    elif case in ("conv3x3", "conv1x1"):
+        if case == "conv3x3":
+            w, geom = workloads.conv_u4(), (64, 56, 56, 64, 64, 3, 1, 1)
+        else:
+            w = workloads.conv_u4(C=256, OC=64, F=1, pad=0, residual=False, tag=1)
+            geom = (64, 56, 56, 256, 64, 1, 0, 1)
+        Nb, H, W, C, OC, F, pad, st = geom
+        gg = qnn.conv_geom(Nb, H, W, C, OC, F, F, (pad, pad), (st, st))
+        Wd = torch.from_numpy(w["W"]).to(device)
+        nb = qnn.qnn_conv_packed_w_bytes(gg, "s4")
+        buf = torch.empty(nb + 1024, dtype=torch.uint8, device=device)
+        off = (-buf.data_ptr()) % 1024
+        Wp = buf[off:off + nb]
+        cs = torch.empty(OC, dtype=torch.int32, device=device)
+        qnn.qconv_prepack_w(Wd, "s4", gg, Wp, cs)
+        zp = torch.empty(OC, dtype=torch.int32, device=device)
+        Mv = torch.empty(OC, dtype=torch.float32, device=device)
+        Bq = torch.empty(OC, dtype=torch.float32, device=device)
+        qnn.q_fold_epilogue(OC, "u4", w["z_in"], cs, w["s_a"], torch.from_numpy(w["s_w"]).to(device),
+                            w["s_o"], bias=torch.from_numpy(w["bias"]).to(device), zp_term=zp, M=Mv, Bq=Bq)
+        I = torch.from_numpy(w["I"]).to(device)
+        res = None if w["res"] is None else torch.from_numpy(w["res"]).to(device)
+        R = float(np.float32(np.float32(w["s_r"]) / np.float32(w["s_o"])))
+        epi = qnn.epilogue("requant", relu=True, out_dt="u4", zp_term=zp, M=Mv, Bq=Bq, residual=res,
+                           res_dt="u4", z_res=w["z_res"], R=R)
+        O = torch.empty((Nb, gg.OH, gg.OW, OC // 2), dtype=torch.uint8, device=device)
+        fn = lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, gg, epi, O, stream=stream)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown case {case}")
+    t = time_steps(torch, fn, args.steps, args.warmup, flush, stream)
+    st = qnn.qnn_check_device_error()
+    print(json.dumps({"case": case, "steps": args.steps, "median_ms": statistics.median(t),
+                      "status": qnn.status_string(st)}), flush=True)
+    if st != qnn.QNN_OK:
+        raise SystemExit(1)
+
+
 def cpu_baseline_gemm(w, target_s=15.0):
     """The oracle (plain C, OpenMP over rows) on a sample of rows of the same GEMM."""
     from oracle import oracle
@@ -461,10 +541,15 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--case", default=None,
+                    help="run one workload only (profiling): quantize, vit_fc1, square_4096, "
+                         "vitl_fc2, conv3x3, conv1x1")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
