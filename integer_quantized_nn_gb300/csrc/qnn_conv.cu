@@ -80,41 +80,87 @@ __device__ __forceinline__ void conv_cursor(const Params &p, ConvState &st, int 
     }
 }
 
-// 16 bytes of the input row under the cursor: in-image data, the padding
-// pattern, or zeros past the last pixel / past the last tap.
-template <int ELEM_BITS>
-__device__ __forceinline__ uint4 conv_fetch(const Params &p, const ConvState &st, int q)
-{
-    if (st.img[q] < 0 || st.fh >= p.FH) return make_uint4(0, 0, 0, 0);
-    const int ih = st.ih0[q] + st.fh;
-    const int iw = st.iw0[q] + st.fw;
-    if (ih < 0 || ih >= p.H || iw < 0 || iw >= p.W)
-        return make_uint4(p.pad_word, p.pad_word, p.pad_word, p.pad_word);
-    const int64_t elem = ((int64_t)(st.img[q] + ih) * p.W + iw) * p.Cin + st.c0;
-    return ldg_nc_v4(p.A + (ELEM_BITS == 4 ? elem / 2 : elem));
-}
+// What a row of the unit holds: input bytes fetched by cp.async, the padding
+// pattern, or zeros (past the last pixel or past the last tap).
+enum { ROW_DATA = 0, ROW_PAD = 1, ROW_ZERO = 2 };
 
-struct ConvU4Op {
-    static constexpr bool F8 = true;
-    static constexpr int SCALE_LOG2 = 9;
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// The im2col converters fetch each unit's input rows with cp.async into a
+// per-thread staging ring of D units in shared memory ([slot][q][thread] x 16
+// bytes), so D - 1 units of loads are in flight while one is converted.
+template <int ELEM_BITS, int GROUP_ELEMS, int STEP_ELEMS, int D>
+struct ConvStaging {
+    static constexpr int DEPTH = D;
+    static constexpr int DEPTH_MULTI = D;
+    static constexpr int STG_BYTES = D * 4 * 128 * 16;
     struct Unit {
-        uint4 v[4];
+        uint32_t kinds;  // 2 bits per row q
     };
     using State = ConvState;
 
-    __device__ static void load(const Params &p, State &st, int j, int sub, int rbase, Unit &u)
+    template <int DD>
+    __device__ static void load(const Params &p, State &st, const uint4 *stg, int j, bool valid, int sub,
+                                int rbase, Unit &u)
     {
-        conv_cursor<32, 128>(p, st, j, sub, rbase);
+        if (valid) {
+            conv_cursor<GROUP_ELEMS, STEP_ELEMS>(p, st, j, sub, rbase);
+            const int slot = j % DD;
+            uint32_t kinds = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) u.v[q] = conv_fetch<4>(p, st, q);
+            for (int q = 0; q < 4; ++q) {
+                uint32_t kind = ROW_ZERO;
+                if (st.img[q] >= 0 && st.fh < p.FH) {
+                    const int ih = st.ih0[q] + st.fh;
+                    const int iw = st.iw0[q] + st.fw;
+                    if (ih < 0 || ih >= p.H || iw < 0 || iw >= p.W) {
+                        kind = ROW_PAD;
+                    } else {
+                        kind = ROW_DATA;
+                        const int64_t elem = ((int64_t)(st.img[q] + ih) * p.W + iw) * p.Cin + st.c0;
+                        const uint32_t dst = smem_u32(stg + (slot * 4 + q) * 128 + threadIdx.x);
+                        cp_async16(dst, p.A + (ELEM_BITS == 4 ? elem / 2 : elem));
+                    }
+                }
+                kinds |= kind << (2 * q);
+            }
+            u.kinds = kinds;
+        }
+        cp_async_commit();  // one group per unit, empty past the end
     }
 
-    __device__ static void store(const Params &, uint32_t a_stage, int sub, int rbase, const Unit &u)
+    // The 16 input bytes of row q of unit j (after its group has landed).
+    __device__ static uint4 fetched(const Params &p, const uint4 *stg, int slot, int q, uint32_t kinds)
     {
+        const uint32_t kind = (kinds >> (2 * q)) & 3u;
+        if (kind == ROW_DATA) return stg[(slot * 4 + q) * 128 + threadIdx.x];
+        if (kind == ROW_PAD) return make_uint4(p.pad_word, p.pad_word, p.pad_word, p.pad_word);
+        return make_uint4(0, 0, 0, 0);
+    }
+};
+
+template <int D>
+struct ConvU4Op : ConvStaging<4, 32, 128, D> {
+    using Base = ConvStaging<4, 32, 128, D>;
+    static constexpr bool F8 = true;
+    static constexpr int SCALE_LOG2 = 9;
+
+    template <int DD>
+    __device__ static void store(const Params &p, ConvState &, const uint4 *stg, uint32_t a_stage, int j,
+                                 int sub, int rbase, const typename Base::Unit &u)
+    {
+        cp_async_wait<DD - 1>();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int row = q * 32 + rbase;
-            const uint32_t w[4] = {u.v[q].x, u.v[q].y, u.v[q].z, u.v[q].w};
+            const uint4 v = Base::fetched(p, stg, j % DD, q, u.kinds);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint32_t b[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -128,27 +174,22 @@ struct ConvU4Op {
     }
 };
 
-struct ConvU8Op {
+template <int D>
+struct ConvU8Op : ConvStaging<8, 16, 64, D> {
+    using Base = ConvStaging<8, 16, 64, D>;
     static constexpr bool F8 = false;
     static constexpr int SCALE_LOG2 = 0;
-    struct Unit {
-        uint4 v[4];
-    };
-    using State = ConvState;
 
-    __device__ static void load(const Params &p, State &st, int j, int sub, int rbase, Unit &u)
+    template <int DD>
+    __device__ static void store(const Params &p, ConvState &, const uint4 *stg, uint32_t a_stage, int j,
+                                 int sub, int rbase, const typename Base::Unit &u)
     {
-        conv_cursor<16, 64>(p, st, j, sub, rbase);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) u.v[q] = conv_fetch<8>(p, st, q);
-    }
-
-    __device__ static void store(const Params &, uint32_t a_stage, int sub, int rbase, const Unit &u)
-    {
+        cp_async_wait<DD - 1>();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int row = q * 32 + rbase;
-            const uint32_t w[4] = {u.v[q].x, u.v[q].y, u.v[q].z, u.v[q].w};
+            const uint4 v = Base::fetched(p, stg, j % DD, q, u.kinds);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint32_t h[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -236,17 +277,22 @@ inline size_t packed_w_u4_bytes(const qnn_conv_geom *g)
     return (size_t)((g->OC + 255) / 256) * (size_t)((K + 127) / 128) * (size_t)gemm::B_STAGE_BYTES;
 }
 
-template <class Op, int TBN>
+// Staging depth: 8 units for tiles up to 128 columns (64 KB of staging), 2 for
+// 256-column tiles, whose units carry 4x the MMA work (and shared memory is full).
+template <template <int> class Op, int TBN>
 qnn_status conv_launch(const Params &p, cudaStream_t s)
 {
-    if constexpr (!Op::F8) {
+    if constexpr (!Op<8>::F8) {
         // K cut into exact chunks: int32 chunk sums of 64 columns per thread
-        if (p.nchunks > 1) return launch<Op, 128, true>(p, s);
+        if (p.nchunks > 1) return launch<Op<8>, 128, true>(p, s);
     }
-    return launch<Op, TBN, false>(p, s);
+    if constexpr (TBN == 256)
+        return launch<Op<2>, 256, false>(p, s);
+    else
+        return launch<Op<8>, TBN, false>(p, s);
 }
 
-template <class Op>
+template <template <int> class Op>
 qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
                     const qnn_epilogue *e, void *O, int32_t *O_s32, qnn_stream_t stream, bool u4)
 {

@@ -45,14 +45,20 @@ template <bool PTF>
 struct GemmOp {
     static constexpr bool F8 = false;
     static constexpr int SCALE_LOG2 = 0;
+    static constexpr int DEPTH = 4;        // units of A rows in flight, in registers
+    static constexpr int DEPTH_MULTI = 3;
+    static constexpr int STG_BYTES = 16;   // no staging ring
     struct Unit {
         uint4 v[4];
         uint4 alpha;
     };
     struct State {};
 
-    __device__ static void load(const Params &p, State &, int j, int sub, int rbase, Unit &u)
+    template <int D>
+    __device__ static void load(const Params &p, State &, const uint4 *, int j, bool valid, int sub,
+                                int rbase, Unit &u)
     {
+        if (!valid) return;
         const int t = unit_tile(p, j);
         const int ks = j % p.KT;
         const int m0 = (t % p.num_m) * BM;
@@ -68,7 +74,9 @@ struct GemmOp {
         if (PTF) u.alpha = (k0 < p.K) ? ldg_nc_v4(p.ptf + k0) : make_uint4(0, 0, 0, 0);
     }
 
-    __device__ static void store(const Params &p, uint32_t a_stage, int sub, int rbase, const Unit &u)
+    template <int D>
+    __device__ static void store(const Params &p, State &, const uint4 *, uint32_t a_stage, int, int sub,
+                                 int rbase, const Unit &u)
     {
         const uint32_t flip = p.a_u8 ? 0u : 0x80808080u;
         uint32_t mul[8];

@@ -61,8 +61,8 @@ struct Params {
     int M, N, K, KT, num_m, num_tiles;
     int chunk_steps, nchunks;
     // epilogue
-    int mode, relu, z_out, out_bits;
-    float qmin, qmax;
+    int mode, relu, z_out, out_bits, out_signed;
+    int32_t qmin_i, qmax_i;
     const int32_t *zp;
     const float *Mv;
     const float *Bq;
@@ -77,10 +77,12 @@ struct Params {
     uint32_t *status;
 };
 
-template <int TBN>
+template <class Op, int TBN>
 struct __align__(1024) Smem {
     uint8_t a[STAGES][A_STAGE_BYTES];
     uint8_t b[STAGES][TBN * ROW_BYTES];
+    uint4 stg[Op::STG_BYTES / 16];                   // converter staging ring (Op-specific)
+    float cols[NUM_EPI_WARPS][3 * (TBN / 2)];        // per epilogue warp: its columns' constants
     uint64_t a_full[STAGES];
     uint64_t b_full[STAGES];
     uint64_t empty[STAGES];
@@ -90,21 +92,21 @@ struct __align__(1024) Smem {
     uint32_t tmem_base;
 };
 
-template <int TBN>
-constexpr size_t smem_bytes() { return sizeof(Smem<TBN>) + 1024; }
+template <class Op, int TBN>
+constexpr size_t smem_bytes() { return sizeof(Smem<Op, TBN>) + 1024; }
 
 // Which tile a unit (tile iteration, K step) of this CTA belongs to.
 __device__ __forceinline__ int unit_tile(const Params &p, int j) { return blockIdx.x + (j / p.KT) * gridDim.x; }
 
 // ---------------------------------------------------------------- converter
-template <class Op, int TBN>
-__device__ __forceinline__ bool convert_one(const Params &p, Smem<TBN> &s, int j, int sub, int rbase,
-                                            const typename Op::Unit &u)
+template <class Op, int TBN, int D>
+__device__ __forceinline__ bool convert_one(const Params &p, Smem<Op, TBN> &s, typename Op::State &st,
+                                            int j, int sub, int rbase, const typename Op::Unit &u)
 {
     const int stage = j % STAGES;
     const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
     if (!mbar_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status)) return false;
-    Op::store(p, smem_u32(&s.a[stage][0]), sub, rbase, u);
+    Op::template store<D>(p, st, s.stg, smem_u32(&s.a[stage][0]), j, sub, rbase, u);
     fence_proxy_async_smem();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&s.a_full[stage]));
@@ -112,29 +114,41 @@ __device__ __forceinline__ bool convert_one(const Params &p, Smem<TBN> &s, int j
 }
 
 // Thread t handles the 16-byte input group (t % 4) of rows (t / 4) + 32 q,
-// q = 0..3; the next unit's loads are in flight while a unit is converted.
-template <class Op, int TBN>
-__device__ void converter_role(const Params &p, Smem<TBN> &s, int units)
+// q = 0..3, of every unit.  The loads of the next D - 1 units are in flight
+// while a unit is converted (in registers, or in the Op's staging ring).
+template <class Op, int TBN, int D>
+__device__ void converter_loop(const Params &p, Smem<Op, TBN> &s, int units)
 {
     const int tid = threadIdx.x;
     const int sub = tid & 3;
     const int rbase = tid >> 2;
     typename Op::State st;
-    typename Op::Unit u0, u1;
-    if (units > 0) Op::load(p, st, 0, sub, rbase, u0);
-    for (int j = 0; j < units; j += 2) {
-        if (j + 1 < units) Op::load(p, st, j + 1, sub, rbase, u1);
-        if (!convert_one<Op, TBN>(p, s, j, sub, rbase, u0)) return;
-        if (j + 1 < units) {
-            if (j + 2 < units) Op::load(p, st, j + 2, sub, rbase, u0);
-            if (!convert_one<Op, TBN>(p, s, j + 1, sub, rbase, u1)) return;
+    typename Op::Unit u[D];
+#pragma unroll
+    for (int d = 0; d < D - 1; ++d) Op::template load<D>(p, st, s.stg, d, d < units, sub, rbase, u[d]);
+    for (int j0 = 0; j0 < units; j0 += D) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+            const int j = j0 + d;
+            if (j >= units) return;
+            const int jn = j + D - 1;
+            Op::template load<D>(p, st, s.stg, jn, jn < units, sub, rbase, u[(d + D - 1) % D]);
+            if (!convert_one<Op, TBN, D>(p, s, st, j, sub, rbase, u[d])) return;
         }
     }
 }
 
+template <class Op, int TBN, bool MULTI>
+__device__ void converter_role(const Params &p, Smem<Op, TBN> &s, int units)
+{
+    converter_loop<Op, TBN, MULTI ? Op::DEPTH_MULTI : Op::DEPTH>(p, s, units);
+    // no asynchronous copy of this thread may still be writing when the CTA exits
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- producer
-template <int TBN>
-__device__ void producer_role(const Params &p, Smem<TBN> &s, int units)
+template <class Op, int TBN>
+__device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
 {
     bool ok = true;
     int j = 0;
@@ -166,8 +180,8 @@ __device__ void producer_role(const Params &p, Smem<TBN> &s, int units)
 }
 
 // ---------------------------------------------------------------- MMA
-template <bool F8, int TBN>
-__device__ void mma_role(const Params &p, Smem<TBN> &s, int my_tiles, uint32_t tmem)
+template <class Op, int TBN>
+__device__ void mma_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32_t tmem)
 {
     constexpr uint32_t IDESC = idesc_f32acc(0, 0, BM, TBN);  // f16 x f16, or e4m3 x e4m3
     uint32_t u = 0;  // accumulation chunk counter
@@ -200,7 +214,7 @@ __device__ void mma_role(const Params &p, Smem<TBN> &s, int my_tiles, uint32_t t
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-                if (F8)
+                if (Op::F8)
                     mma_f8f6f4_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), IDESC, acc);
                 else
                     mma_f16_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), IDESC, acc);
@@ -224,6 +238,40 @@ __device__ __forceinline__ void st_v4(void *ptr, uint32_t a, uint32_t b, uint32_
     *reinterpret_cast<uint4 *>(ptr) = make_uint4(a, b, c, d);
 }
 
+__device__ __forceinline__ int32_t cvt_rni(float f)
+{
+    int32_t d;
+    asm("cvt.rni.s32.f32 %0, %1;" : "=r"(d) : "f"(f));
+    return d;
+}
+
+__device__ __forceinline__ int32_t add_sat(int32_t a, int32_t b)
+{
+    int32_t d;
+    asm("add.sat.s32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// d = c << 2w | b << w | a for w-bit codes a, b already inside the code range
+__device__ __forceinline__ uint32_t pack_s8(int32_t a, int32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(b), "r"(a), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t pack_u8(int32_t a, int32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(b), "r"(a), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t pack_u4(int32_t a, int32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("cvt.pack.sat.u4.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(b), "r"(a), "r"(c));
+    return d;
+}
+
 // Residual code of column i of a 32-column piece held in rw (8-bit: 8 words of
 // 4 codes; 4-bit: 4 words of 8 codes).
 __device__ __forceinline__ int32_t res_code(const Params &p, const uint32_t (&rw)[8], int i)
@@ -239,16 +287,56 @@ __device__ __forceinline__ int32_t res_code(const Params &p, const uint32_t (&rw
     return v;
 }
 
+// Each epilogue warp keeps the per-column constants of its COLS columns in
+// shared memory: [0, COLS) M (requant) or D (dequant), [COLS, 2 COLS) Bq or
+// bias, [2 COLS, 3 COLS) zp_term (as int bits).  Loaded once per tile.
+template <int COLS>
+__device__ __forceinline__ void stage_columns(const Params &p, float *cols, int nbase, int lane)
+{
+    __syncwarp();
+    for (int c = lane; c < COLS; c += 32) {
+        const int n = nbase + c;
+        const bool in = n < p.N;
+        float a = 0.0f, b = 0.0f;
+        int32_t z = 0;
+        if (in) {
+            if (p.mode == QNN_EPI_REQUANT) {
+                a = __ldg(p.Mv + n);
+                b = __ldg(p.Bq + n);
+            } else if (p.mode == QNN_EPI_DEQUANT) {
+                a = __ldg(p.D + n);
+                b = p.bias ? __ldg(p.bias + n) : 0.0f;
+            }
+            if (p.zp) z = __ldg(p.zp + n);
+        }
+        cols[c] = a;
+        cols[COLS + c] = b;
+        cols[2 * COLS + c] = __int_as_float(z);
+    }
+    __syncwarp();
+}
+
 // Requant / dequant / raw store of the 32 consecutive columns n0.. of row m.
-// Works in place on `ac` (the raw accumulators on entry).
-__device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, int32_t (&ac)[32])
+// Works in place on `ac` (the raw accumulators on entry); ca / cb / cz point at
+// this piece's constants in shared memory (warp-uniform broadcast reads).
+// Requant rounds and clips in the integer domain: cvt.rni is rint for |v| <
+// 2^31 and saturates beyond, ReLU is a max with 0, z_out a saturating add,
+// then min / max to the code range -- the fp32 clip of rint(v) + z_out for
+// every finite v (M, Bq and R must be finite).
+__device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, int32_t (&ac)[32],
+                                               const float *ca, const float *cb, const float *cz)
 {
     if (m >= p.M || n0 >= p.N) return;
     const bool vec = p.vec_ok;
     if (p.zp) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (vec || n0 + i < p.N) ac[i] -= __ldg(p.zp + n0 + i);
+        for (int i = 0; i < 32; i += 4) {
+            const float4 z = *reinterpret_cast<const float4 *>(cz + i);
+            ac[i] -= __float_as_int(z.x);
+            ac[i + 1] -= __float_as_int(z.y);
+            ac[i + 2] -= __float_as_int(z.z);
+            ac[i + 3] -= __float_as_int(z.w);
+        }
     }
     const int64_t base = (int64_t)m * p.N + n0;  // element offset of (m, n0)
     if (p.C32) {
@@ -273,10 +361,13 @@ __device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, i
     if (p.mode == QNN_EPI_DEQUANT) {
         float *C = static_cast<float *>(p.C);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int n = (vec || n0 + i < p.N) ? n0 + i : n0;
-            const float b = p.bias ? __ldg(p.bias + n) : 0.0f;
-            ac[i] = __float_as_int(__fadd_rn(__fmul_rn(__int2float_rn(ac[i]), __ldg(p.D + n)), b));
+        for (int i = 0; i < 32; i += 4) {
+            const float4 d = *reinterpret_cast<const float4 *>(ca + i);
+            const float4 b = *reinterpret_cast<const float4 *>(cb + i);
+            ac[i] = __float_as_int(__fadd_rn(__fmul_rn(__int2float_rn(ac[i]), d.x), b.x));
+            ac[i + 1] = __float_as_int(__fadd_rn(__fmul_rn(__int2float_rn(ac[i + 1]), d.y), b.y));
+            ac[i + 2] = __float_as_int(__fadd_rn(__fmul_rn(__int2float_rn(ac[i + 2]), d.z), b.z));
+            ac[i + 3] = __float_as_int(__fadd_rn(__fmul_rn(__int2float_rn(ac[i + 3]), d.w), b.w));
         }
         if (vec) {
 #pragma unroll
@@ -310,25 +401,36 @@ __device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, i
             }
         }
     }
-    const float zo = (float)p.z_out;
-    int32_t q[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int n = (vec || n0 + i < p.N) ? n0 + i : n0;
-        float t = __ldg(p.Bq + n);
-        if (p.res) t = __fadd_rn(__fmul_rn(__int2float_rn(res_code(p, rw, i) - p.z_res), p.R), t);
-        const float v = __fadd_rn(__fmul_rn(__int2float_rn(ac[i]), __ldg(p.Mv + n)), t);
-        float r = rintf(v);
-        if (p.relu) r = fmaxf(r, 0.0f);
-        q[i] = __float2int_rn(fminf(fmaxf(__fadd_rn(r, zo), p.qmin), p.qmax));
+    for (int i = 0; i < 32; i += 4) {
+        const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
+        const float4 bq = *reinterpret_cast<const float4 *>(cb + i);
+        const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+        const float bb[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float t = bb[k];
+            if (p.res)
+                t = __fadd_rn(__fmul_rn(__int2float_rn(res_code(p, rw, i + k) - p.z_res), p.R), t);
+            const float v = __fadd_rn(__fmul_rn(__int2float_rn(ac[i + k]), mm[k]), t);
+            int32_t r = cvt_rni(v);
+            if (p.relu) r = max(r, 0);
+            r = add_sat(r, p.z_out);
+            ac[i + k] = min(max(r, p.qmin_i), p.qmax_i);
+        }
     }
     uint8_t *C = static_cast<uint8_t *>(p.C);
     if (p.out_bits == 8) {
         uint32_t ow[8];
+        if (p.out_signed) {
 #pragma unroll
-        for (int w = 0; w < 8; ++w)
-            ow[w] = (q[4 * w] & 255) | ((q[4 * w + 1] & 255) << 8) | ((q[4 * w + 2] & 255) << 16) |
-                    ((uint32_t)q[4 * w + 3] << 24);
+            for (int w = 0; w < 8; ++w)
+                ow[w] = pack_s8(ac[4 * w], ac[4 * w + 1], pack_s8(ac[4 * w + 2], ac[4 * w + 3], 0));
+        } else {
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                ow[w] = pack_u8(ac[4 * w], ac[4 * w + 1], pack_u8(ac[4 * w + 2], ac[4 * w + 3], 0));
+        }
         if (vec) {
             st_v4(C + base, ow[0], ow[1], ow[2], ow[3]);
             st_v4(C + base + 16, ow[4], ow[5], ow[6], ow[7]);
@@ -339,10 +441,8 @@ __device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, i
         uint32_t ow[4];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int b = 0; b < 8; ++b) word |= (uint32_t)(q[8 * w + b] & 15) << (4 * b);
-            ow[w] = word;
+            const int32_t *q = ac + 8 * w;
+            ow[w] = pack_u4(q[0], q[1], pack_u4(q[2], q[3], pack_u4(q[4], q[5], pack_u4(q[6], q[7], 0))));
         }
         if (vec) {
             st_v4(C + base / 2, ow[0], ow[1], ow[2], ow[3]);
@@ -367,8 +467,8 @@ __device__ __forceinline__ int32_t acc_to_int(uint32_t bits)
 // one row and TBN / 2 columns, converted and stored 32 at a time from TMEM.
 // MULTI == true : K is cut into exact chunks; each thread keeps int32 sums for
 // its row and TBN / 2 columns in registers across the chunks.
-template <int TBN, bool MULTI, int SCALE_LOG2>
-__device__ void epilogue_role(const Params &p, Smem<TBN> &s, int my_tiles, uint32_t tmem)
+template <class Op, int TBN, bool MULTI>
+__device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32_t tmem)
 {
     constexpr int COLS = TBN / 2;
     constexpr int PIECES = COLS / 32;
@@ -376,11 +476,13 @@ __device__ void epilogue_role(const Params &p, Smem<TBN> &s, int my_tiles, uint3
     const int lane = threadIdx.x & 31;
     const int quad = warp & 3;                 // TMEM lanes 32*quad .. +31
     const int half = (warp - EPI_WARP0) >> 2;  // columns COLS*half .. +COLS-1
+    float *cols = s.cols[warp - EPI_WARP0];
     uint32_t u = 0;
     for (int i = 0; i < my_tiles; ++i) {
         const int t = blockIdx.x + i * gridDim.x;
         const int m = (t % p.num_m) * BM + quad * 32 + lane;
         const int nbase = (t / p.num_m) * TBN + half * COLS;
+        stage_columns<COLS>(p, cols, nbase, lane);
         if (!MULTI) {
             const uint32_t abuf = u & 1u;
             if (!mbar_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
@@ -393,13 +495,14 @@ __device__ void epilogue_role(const Params &p, Smem<TBN> &s, int my_tiles, uint3
                 tmem_ld_wait();
                 int32_t acc[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) acc[k] = acc_to_int<SCALE_LOG2>(r[k]);
+                for (int k = 0; k < 32; ++k) acc[k] = acc_to_int<Op::SCALE_LOG2>(r[k]);
                 if (jp == PIECES - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
                 }
-                epilogue_piece(p, m, nbase + jp * 32, acc);
+                epilogue_piece(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
+                               cols + 2 * COLS + jp * 32);
             }
             ++u;
         } else {
@@ -416,7 +519,7 @@ __device__ void epilogue_role(const Params &p, Smem<TBN> &s, int my_tiles, uint3
                     tmem_ld_wait();
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        const int32_t v = acc_to_int<SCALE_LOG2>(r[k]);
+                        const int32_t v = acc_to_int<Op::SCALE_LOG2>(r[k]);
                         acc[jp][k] = (c == 0) ? v : acc[jp][k] + v;
                     }
                 }
@@ -426,7 +529,9 @@ __device__ void epilogue_role(const Params &p, Smem<TBN> &s, int my_tiles, uint3
                 ++u;
             }
 #pragma unroll
-            for (int jp = 0; jp < PIECES; ++jp) epilogue_piece(p, m, nbase + jp * 32, acc[jp]);
+            for (int jp = 0; jp < PIECES; ++jp)
+                epilogue_piece(p, m, nbase + jp * 32, acc[jp], cols + jp * 32, cols + COLS + jp * 32,
+                               cols + 2 * COLS + jp * 32);
         }
     }
 }
@@ -436,8 +541,8 @@ template <class Op, int TBN, bool MULTI>
 __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_constant__ Params p)
 {
     extern __shared__ uint8_t smem_raw[];
-    Smem<TBN> &s = *reinterpret_cast<Smem<TBN> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                  ~static_cast<uintptr_t>(1023));
+    Smem<Op, TBN> &s = *reinterpret_cast<Smem<Op, TBN> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -467,18 +572,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
         (blockIdx.x < p.num_tiles) ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int units = my_tiles * p.KT;
 
-    // register split of the multi-chunk kernel: 128*96 + 128*56 + 256*176 = 64512 <= 65536
+    // register split of the multi-chunk kernel: 128*128 + 128*56 + 256*160 = 64512 <= 65536
     if (warp < 4) {
-        if (MULTI) regs_dec<96>();
-        converter_role<Op, TBN>(p, s, units);
+        converter_role<Op, TBN, MULTI>(p, s, units);
     } else if (warp < 8) {
         if (MULTI) regs_dec<56>();
-        if (warp == PRODUCER_WARP && lane == 0) producer_role<TBN>(p, s, units);
-        if (warp == MMA_WARP && lane == 0) mma_role<Op::F8, TBN>(p, s, my_tiles, tmem);
+        if (warp == PRODUCER_WARP && lane == 0) producer_role<Op, TBN>(p, s, units);
+        if (warp == MMA_WARP && lane == 0) mma_role<Op, TBN>(p, s, my_tiles, tmem);
         __syncwarp();
     } else {
-        if (MULTI) regs_inc<176>();
-        epilogue_role<TBN, MULTI, Op::SCALE_LOG2>(p, s, my_tiles, tmem);
+        if (MULTI) regs_inc<160>();
+        epilogue_role<Op, TBN, MULTI>(p, s, my_tiles, tmem);
     }
 
     tc_fence_before();
@@ -493,7 +597,7 @@ qnn_status launch(Params p, cudaStream_t stream)
     static bool attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QNN_ERR_CUDA;
-    constexpr size_t SMEM = smem_bytes<TBN>();
+    constexpr size_t SMEM = smem_bytes<Op, TBN>();
     if (!attr_set[dev]) {
         if (cudaFuncSetAttribute(qmma_kernel<Op, TBN, MULTI>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) != cudaSuccess)
@@ -528,9 +632,10 @@ inline qnn_status setup_epilogue(const qnn_epilogue *e, bool conv, Params &p)
         int32_t lo, hi;
         qrange(e->out_dt, 0, &lo, &hi);
         if (e->z_out < lo || e->z_out > hi) return QNN_ERR_INVALID_ARG;
-        p.qmin = (float)lo;
-        p.qmax = (float)hi;
+        p.qmin_i = lo;
+        p.qmax_i = hi;
         p.out_bits = (e->out_dt == QNN_U4) ? 4 : 8;
+        p.out_signed = (e->out_dt == QNN_S8);
         if (e->residual) {
             const bool ok_r = conv ? (e->res_dt == QNN_U4 || e->res_dt == QNN_U8 || e->res_dt == QNN_S8 ||
                                       e->res_dt == QNN_S4)
