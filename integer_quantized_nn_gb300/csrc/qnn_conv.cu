@@ -37,7 +37,18 @@ struct ConvState {
     int ih0[4];
     int iw0[4];
     int c0, fh, fw;
+    int kstep;       // K step of the current unit
+    uint64_t kinds;  // per staging slot (8 bits): what each of the 4 rows holds, 2 bits each
 };
+
+// Places the cursor at linear K position kpos = (fh * FW + fw) * C + c0.
+__device__ __forceinline__ void conv_seek(const Params &p, ConvState &st, int kpos)
+{
+    const int tap = kpos / p.Cin;
+    st.c0 = kpos - tap * p.Cin;
+    st.fh = tap / p.FW;
+    st.fw = tap - st.fh * p.FW;
+}
 
 template <int GROUP_ELEMS, int STEP_ELEMS>
 __device__ __forceinline__ void conv_cursor(const Params &p, ConvState &st, int j, int sub, int rbase)
@@ -63,11 +74,12 @@ __device__ __forceinline__ void conv_cursor(const Params &p, ConvState &st, int 
                 st.iw0[q] = 0;
             }
         }
-        const int k0 = sub * GROUP_ELEMS;
-        const int tap = k0 / p.Cin;
-        st.c0 = k0 - tap * p.Cin;
-        st.fh = tap / p.FW;
-        st.fw = tap - st.fh * p.FW;
+        // the same K walk as unit_kstep: start at this CTA's rotated K step
+        st.kstep = unit_kstep(p, j);
+        conv_seek(p, st, st.kstep * STEP_ELEMS + sub * GROUP_ELEMS);
+    } else if (++st.kstep == p.KT) {
+        st.kstep = 0;
+        conv_seek(p, st, sub * GROUP_ELEMS);
     } else {
         st.c0 += STEP_ELEMS;
         while (st.c0 >= p.Cin) {
@@ -100,9 +112,8 @@ struct ConvStaging {
     static constexpr int DEPTH = D;
     static constexpr int DEPTH_MULTI = D;
     static constexpr int STG_BYTES = D * 4 * 128 * 16;
-    struct Unit {
-        uint32_t kinds;  // 2 bits per row q
-    };
+    static constexpr bool REG_RING = false;
+    struct Unit {};
     using State = ConvState;
 
     template <int DD>
@@ -130,15 +141,16 @@ struct ConvStaging {
                 }
                 kinds |= kind << (2 * q);
             }
-            u.kinds = kinds;
+            const int sh = 8 * slot;
+            st.kinds = (st.kinds & ~(0xFFull << sh)) | ((uint64_t)kinds << sh);
         }
         cp_async_commit();  // one group per unit, empty past the end
     }
 
     // The 16 input bytes of row q of unit j (after its group has landed).
-    __device__ static uint4 fetched(const Params &p, const uint4 *stg, int slot, int q, uint32_t kinds)
+    __device__ static uint4 fetched(const Params &p, const ConvState &st, const uint4 *stg, int slot, int q)
     {
-        const uint32_t kind = (kinds >> (2 * q)) & 3u;
+        const uint32_t kind = (uint32_t)(st.kinds >> (8 * slot + 2 * q)) & 3u;
         if (kind == ROW_DATA) return stg[(slot * 4 + q) * 128 + threadIdx.x];
         if (kind == ROW_PAD) return make_uint4(p.pad_word, p.pad_word, p.pad_word, p.pad_word);
         return make_uint4(0, 0, 0, 0);
@@ -152,14 +164,14 @@ struct ConvU4Op : ConvStaging<4, 32, 128, D> {
     static constexpr int SCALE_LOG2 = 9;
 
     template <int DD>
-    __device__ static void store(const Params &p, ConvState &, const uint4 *stg, uint32_t a_stage, int j,
-                                 int sub, int rbase, const typename Base::Unit &u)
+    __device__ static void store(const Params &p, ConvState &st, const uint4 *stg, uint32_t a_stage, int j,
+                                 int sub, int rbase, const typename Base::Unit &)
     {
         cp_async_wait<DD - 1>();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int row = q * 32 + rbase;
-            const uint4 v = Base::fetched(p, stg, j % DD, q, u.kinds);
+            const uint4 v = Base::fetched(p, st, stg, j % DD, q);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint32_t b[8];
 #pragma unroll
@@ -181,14 +193,14 @@ struct ConvU8Op : ConvStaging<8, 16, 64, D> {
     static constexpr int SCALE_LOG2 = 0;
 
     template <int DD>
-    __device__ static void store(const Params &p, ConvState &, const uint4 *stg, uint32_t a_stage, int j,
-                                 int sub, int rbase, const typename Base::Unit &u)
+    __device__ static void store(const Params &p, ConvState &st, const uint4 *stg, uint32_t a_stage, int j,
+                                 int sub, int rbase, const typename Base::Unit &)
     {
         cp_async_wait<DD - 1>();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int row = q * 32 + rbase;
-            const uint4 v = Base::fetched(p, stg, j % DD, q, u.kinds);
+            const uint4 v = Base::fetched(p, st, stg, j % DD, q);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint32_t h[8];
 #pragma unroll

@@ -48,6 +48,7 @@ struct GemmOp {
     static constexpr int DEPTH = 4;        // units of A rows in flight, in registers
     static constexpr int DEPTH_MULTI = 3;
     static constexpr int STG_BYTES = 16;   // no staging ring
+    static constexpr bool REG_RING = true;
     struct Unit {
         uint4 v[4];
         uint4 alpha;
@@ -60,7 +61,7 @@ struct GemmOp {
     {
         if (!valid) return;
         const int t = unit_tile(p, j);
-        const int ks = j % p.KT;
+        const int ks = unit_kstep(p, j);
         const int m0 = (t % p.num_m) * BM;
         const int k0 = ks * 64 + sub * 16;
 #pragma unroll

@@ -62,7 +62,7 @@ struct Params {
     int chunk_steps, nchunks;
     // epilogue
     int mode, relu, z_out, out_bits, out_signed;
-    int32_t qmin_i, qmax_i;
+    int32_t clip_lo, clip_hi;  // requant: clip of rint(v) before adding z_out (ReLU folded in)
     const int32_t *zp;
     const float *Mv;
     const float *Bq;
@@ -83,8 +83,7 @@ struct __align__(1024) Smem {
     uint8_t b[STAGES][TBN * ROW_BYTES];
     uint4 stg[Op::STG_BYTES / 16];                   // converter staging ring (Op-specific)
     float cols[NUM_EPI_WARPS][3 * (TBN / 2)];        // per epilogue warp: its columns' constants
-    uint64_t a_full[STAGES];
-    uint64_t b_full[STAGES];
+    uint64_t full[STAGES];   // 4 converter-warp arrivals + the producer's expect_tx arrival
     uint64_t empty[STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
@@ -98,18 +97,43 @@ constexpr size_t smem_bytes() { return sizeof(Smem<Op, TBN>) + 1024; }
 // Which tile a unit (tile iteration, K step) of this CTA belongs to.
 __device__ __forceinline__ int unit_tile(const Params &p, int j) { return blockIdx.x + (j / p.KT) * gridDim.x; }
 
+// The K step a unit covers.  Each CTA walks K starting at its own offset
+// (blockIdx.x mod KT), so CTAs that share a weight block read different slices
+// of it at any moment.  Integer sums do not depend on the order, and a chunk of
+// consecutive units still spans at most chunk_steps K steps.
+__device__ __forceinline__ int unit_kstep(const Params &p, int j)
+{
+    const int ks = j % p.KT + (int)(blockIdx.x % (unsigned)p.KT);
+    return ks >= p.KT ? ks - p.KT : ks;
+}
+
+// A bounded wait whose outcome is the same on every lane of the warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t *status)
+{
+    const bool ok = mbar_wait(bar, parity, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- converter
+// Converts unit j into its stage.  `ready` says whether the stage's empty
+// phase was already seen complete; before the conversion work starts, the
+// empty phase of unit j + 1 is probed so that its latency is hidden behind it.
 template <class Op, int TBN, int D>
 __device__ __forceinline__ bool convert_one(const Params &p, Smem<Op, TBN> &s, typename Op::State &st,
-                                            int j, int sub, int rbase, const typename Op::Unit &u)
+                                            int j, int units, int sub, int rbase,
+                                            const typename Op::Unit &u, bool &ready)
 {
     const int stage = j % STAGES;
     const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
-    if (!mbar_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status)) return false;
+    const bool ok = ready || mbar_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    const int jn = j + 1;
+    const bool probe = mbar_test_wait(smem_u32(&s.empty[jn % STAGES]), ((uint32_t)(jn / STAGES) & 1u) ^ 1u);
     Op::template store<D>(p, st, s.stg, smem_u32(&s.a[stage][0]), j, sub, rbase, u);
     fence_proxy_async_smem();
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&s.a_full[stage]));
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&s.full[stage]));
+    ready = probe && jn < units;
     return true;
 }
 
@@ -122,8 +146,9 @@ __device__ void converter_loop(const Params &p, Smem<Op, TBN> &s, int units)
     const int tid = threadIdx.x;
     const int sub = tid & 3;
     const int rbase = tid >> 2;
-    typename Op::State st;
+    typename Op::State st{};
     typename Op::Unit u[D];
+    bool ready = false;
 #pragma unroll
     for (int d = 0; d < D - 1; ++d) Op::template load<D>(p, st, s.stg, d, d < units, sub, rbase, u[d]);
     for (int j0 = 0; j0 < units; j0 += D) {
@@ -133,103 +158,155 @@ __device__ void converter_loop(const Params &p, Smem<Op, TBN> &s, int units)
             if (j >= units) return;
             const int jn = j + D - 1;
             Op::template load<D>(p, st, s.stg, jn, jn < units, sub, rbase, u[(d + D - 1) % D]);
-            if (!convert_one<Op, TBN, D>(p, s, st, j, sub, rbase, u[d])) return;
+            if (!convert_one<Op, TBN, D>(p, s, st, j, units, sub, rbase, u[d], ready)) return;
         }
+    }
+}
+
+// Ops whose in-flight units live in their shared-memory staging ring keep
+// only a little per-unit state, so their loop is not unrolled (one copy of the
+// converter code keeps the instruction cache warm).
+template <class Op, int TBN, int D>
+__device__ void converter_loop_rolled(const Params &p, Smem<Op, TBN> &s, int units)
+{
+    const int tid = threadIdx.x;
+    const int sub = tid & 3;
+    const int rbase = tid >> 2;
+    typename Op::State st{};
+    typename Op::Unit u;
+    bool ready = false;
+#pragma unroll 1
+    for (int d = 0; d < D - 1; ++d) Op::template load<D>(p, st, s.stg, d, d < units, sub, rbase, u);
+#pragma unroll 1
+    for (int j = 0; j < units; ++j) {
+        const int jn = j + D - 1;
+        Op::template load<D>(p, st, s.stg, jn, jn < units, sub, rbase, u);
+        if (!convert_one<Op, TBN, D>(p, s, st, j, units, sub, rbase, u, ready)) return;
     }
 }
 
 template <class Op, int TBN, bool MULTI>
 __device__ void converter_role(const Params &p, Smem<Op, TBN> &s, int units)
 {
-    converter_loop<Op, TBN, MULTI ? Op::DEPTH_MULTI : Op::DEPTH>(p, s, units);
+    if constexpr (Op::REG_RING)
+        converter_loop<Op, TBN, MULTI ? Op::DEPTH_MULTI : Op::DEPTH>(p, s, units);
+    else
+        converter_loop_rolled<Op, TBN, MULTI ? Op::DEPTH_MULTI : Op::DEPTH>(p, s, units);
     // no asynchronous copy of this thread may still be writing when the CTA exits
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- producer
+// The producer and MMA roles run on whole warps: every lane waits on the
+// barriers (so the warp never diverges around a wait) and lane 0 issues the
+// copies, MMAs and commits.  A wait that times out on any lane stops the role.
+
 template <class Op, int TBN>
 __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
 {
+    const bool leader = (threadIdx.x & 31) == 0;
     bool ok = true;
+    bool ready = false;
     int j = 0;
     for (; j < units; ++j) {
         const int stage = j % STAGES;
         const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
-        if (!mbar_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status)) {
+        if (!ready && !warp_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status)) {
             ok = false;
             break;
         }
-        const int t = unit_tile(p, j);
-        const int ks = j % p.KT;
-        // columns n0 .. n0 + TBN - 1 live in the 256-row packed block n0 / 256
-        const int n0 = (t / p.num_m) * TBN;
-        const uint8_t *src = p.Bp + ((int64_t)(n0 / gemm::BN) * p.KT + ks) * gemm::B_STAGE_BYTES +
-                             (int64_t)(n0 % gemm::BN) * ROW_BYTES;
-        const uint32_t bar = smem_u32(&s.b_full[stage]);
-        mbar_arrive_expect_tx(bar, TBN * ROW_BYTES);
-        bulk_g2s(smem_u32(&s.b[stage][0]), src, TBN * ROW_BYTES, bar);
+        const int jn = j + 1;
+        const bool probe = mbar_test_wait(smem_u32(&s.empty[jn % STAGES]), ((uint32_t)(jn / STAGES) & 1u) ^ 1u);
+        if (leader) {
+            const int t = unit_tile(p, j);
+            const int ks = unit_kstep(p, j);
+            // columns n0 .. n0 + TBN - 1 live in the 256-row packed block n0 / 256
+            const int n0 = (t / p.num_m) * TBN;
+            const uint8_t *src = p.Bp + ((int64_t)(n0 / gemm::BN) * p.KT + ks) * gemm::B_STAGE_BYTES +
+                                 (int64_t)(n0 % gemm::BN) * ROW_BYTES;
+            const uint32_t bar = smem_u32(&s.full[stage]);
+            mbar_arrive_expect_tx(bar, TBN * ROW_BYTES);
+            bulk_g2s(smem_u32(&s.b[stage][0]), src, TBN * ROW_BYTES, bar);
+        }
+        ready = __all_sync(0xffffffffu, probe) && jn < units;
     }
     if (!ok) {
         // wind down: let the copies already issued land before the CTA exits
         for (int i = (j > STAGES ? j - STAGES : 0); i < j; ++i) {
             const int stage = i % STAGES;
             const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
-            if (!mbar_wait(smem_u32(&s.b_full[stage]), ph, p.status)) break;
+            if (!warp_wait(smem_u32(&s.full[stage]), ph, p.status)) break;
         }
     }
 }
 
 // ---------------------------------------------------------------- MMA
+// The issuing loop probes the full barriers of up to STAGES upcoming units at
+// once (non-blocking, so their latencies overlap) and issues every unit found
+// ready back to back; it blocks only when the next unit is not ready yet.
 template <class Op, int TBN>
 __device__ void mma_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32_t tmem)
 {
     constexpr uint32_t IDESC = idesc_f32acc(0, 0, BM, TBN);  // f16 x f16, or e4m3 x e4m3
+    const bool leader = (threadIdx.x & 31) == 0;
+    const int units = my_tiles * p.KT;
     uint32_t u = 0;  // accumulation chunk counter
     uint32_t abuf = 0;
-    bool ok = true;
-    for (int i = 0; i < my_tiles && ok; ++i) {
-        for (int ks = 0; ks < p.KT; ++ks) {
-            const int j = i * p.KT + ks;
+    int j = 0;
+    while (j < units) {
+        uint32_t mask = 0;
+#pragma unroll
+        for (int b = 0; b < STAGES; ++b) {
+            const int jb = j + b;
+            const bool r = (jb < units) &&
+                           mbar_test_wait(smem_u32(&s.full[jb % STAGES]), (uint32_t)(jb / STAGES) & 1u);
+            mask |= (uint32_t)r << b;
+        }
+        mask = __reduce_and_sync(0xffffffffu, mask);
+        int nready = __ffs(~mask) - 1;  // leading ready units
+        if (nready == 0) {
+            if (!warp_wait(smem_u32(&s.full[j % STAGES]), (uint32_t)(j / STAGES) & 1u, p.status)) break;
+            nready = 1;
+        }
+        bool ok = true;
+        for (int r = 0; r < nready; ++r, ++j) {
+            const int ks = j % p.KT;
             const int stage = j % STAGES;
-            const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
             const bool first = (ks % p.chunk_steps) == 0;
+            const bool last = ((ks % p.chunk_steps) == p.chunk_steps - 1) || (ks == p.KT - 1);
             if (first) {
                 abuf = u & 1u;
-                if (!mbar_wait(smem_u32(&s.acc_empty[abuf]), ((u >> 1) & 1u) ^ 1u, p.status)) {
+                if (!warp_wait(smem_u32(&s.acc_empty[abuf]), ((u >> 1) & 1u) ^ 1u, p.status)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-            }
-            if (!mbar_wait(smem_u32(&s.a_full[stage]), ph, p.status) ||
-                !mbar_wait(smem_u32(&s.b_full[stage]), ph, p.status)) {
-                ok = false;
-                break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(&s.a[stage][0]);
-            const uint32_t b0 = smem_u32(&s.b[stage][0]);
-            const uint32_t d = tmem + abuf * TBN;
-            // 4 MMAs of 32 bytes of K each: 16 fp16 or 32 e4m3 values
+            if (leader) {
+                const uint32_t a0 = smem_u32(&s.a[stage][0]);
+                const uint32_t b0 = smem_u32(&s.b[stage][0]);
+                const uint32_t d = tmem + abuf * TBN;
+                // 4 MMAs of 32 bytes of K each: 16 fp16 or 32 e4m3 values
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-                if (Op::F8)
-                    mma_f8f6f4_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), IDESC, acc);
-                else
-                    mma_f16_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), IDESC, acc);
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                    if (Op::F8)
+                        mma_f8f6f4_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), IDESC, acc);
+                    else
+                        mma_f16_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), IDESC, acc);
+                }
+                mma_commit(smem_u32(&s.empty[stage]));
+                if (last) mma_commit(smem_u32(&s.acc_full[abuf]));
             }
-            mma_commit(smem_u32(&s.empty[stage]));
-            const bool last = ((ks % p.chunk_steps) == p.chunk_steps - 1) || (ks == p.KT - 1);
-            if (last) {
-                mma_commit(smem_u32(&s.acc_full[abuf]));
-                ++u;
-            }
+            __syncwarp();
+            if (last) ++u;
         }
+        if (!ok) break;
     }
     // every MMA issued must have completed before the CTA winds down
-    mma_commit(smem_u32(&s.mma_done));
-    (void)mbar_wait(smem_u32(&s.mma_done), 0u, p.status);
+    if (leader) mma_commit(smem_u32(&s.mma_done));
+    __syncwarp();
+    (void)warp_wait(smem_u32(&s.mma_done), 0u, p.status);
 }
 
 // ---------------------------------------------------------------- epilogue
@@ -289,13 +366,21 @@ __device__ __forceinline__ int32_t res_code(const Params &p, const uint32_t (&rw
 
 // Each epilogue warp keeps the per-column constants of its COLS columns in
 // shared memory: [0, COLS) M (requant) or D (dequant), [COLS, 2 COLS) Bq or
-// bias, [2 COLS, 3 COLS) zp_term (as int bits).  Loaded once per tile.
+// bias, [2 COLS, 3 COLS) zp_term (as int bits).  The loads of a tile's
+// constants are issued before the warp waits for the tile's accumulator and
+// stored to shared memory after it.
 template <int COLS>
-__device__ __forceinline__ void stage_columns(const Params &p, float *cols, int nbase, int lane)
+struct ColumnRegs {
+    float a[COLS / 32], b[COLS / 32];
+    int32_t z[COLS / 32];
+};
+
+template <int COLS>
+__device__ __forceinline__ void load_columns(const Params &p, ColumnRegs<COLS> &cr, int nbase, int lane)
 {
-    __syncwarp();
-    for (int c = lane; c < COLS; c += 32) {
-        const int n = nbase + c;
+#pragma unroll
+    for (int k = 0; k < COLS / 32; ++k) {
+        const int n = nbase + 32 * k + lane;
         const bool in = n < p.N;
         float a = 0.0f, b = 0.0f;
         int32_t z = 0;
@@ -309,22 +394,64 @@ __device__ __forceinline__ void stage_columns(const Params &p, float *cols, int 
             }
             if (p.zp) z = __ldg(p.zp + n);
         }
-        cols[c] = a;
-        cols[COLS + c] = b;
-        cols[2 * COLS + c] = __int_as_float(z);
+        cr.a[k] = a;
+        cr.b[k] = b;
+        cr.z[k] = z;
+    }
+}
+
+template <int COLS>
+__device__ __forceinline__ void store_columns(const ColumnRegs<COLS> &cr, float *cols, int lane)
+{
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < COLS / 32; ++k) {
+        cols[32 * k + lane] = cr.a[k];
+        cols[COLS + 32 * k + lane] = cr.b[k];
+        cols[2 * COLS + 32 * k + lane] = __int_as_float(cr.z[k]);
     }
     __syncwarp();
 }
 
+// The residual codes of the 32 columns n0.. of row m (8-bit: 8 words of 4
+// codes; 4-bit: 4 words of 8 codes), or zeros without a residual.
+__device__ __forceinline__ void load_residual(const Params &p, int m, int n0, uint32_t (&rw)[8])
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rw[i] = 0;
+    if (!p.res || m >= p.M || n0 >= p.N) return;
+    const int64_t base = (int64_t)m * p.N + n0;
+    if (p.res_bits == 8) {
+        if (p.vec_ok) {
+            const uint4 r0 = ldg_nc_v4(p.res + base), r1 = ldg_nc_v4(p.res + base + 16);
+            rw[0] = r0.x; rw[1] = r0.y; rw[2] = r0.z; rw[3] = r0.w;
+            rw[4] = r1.x; rw[5] = r1.y; rw[6] = r1.z; rw[7] = r1.w;
+        } else {
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i)
+                rw[i >> 2] |= (uint32_t)p.res[base + i] << (8 * (i & 3));
+        }
+    } else {
+        if (p.vec_ok) {
+            const uint4 r0 = ldg_nc_v4(p.res + base / 2);
+            rw[0] = r0.x; rw[1] = r0.y; rw[2] = r0.z; rw[3] = r0.w;
+        } else {
+            for (int i = 0; i < 32 && n0 + i < p.N; i += 2)
+                rw[i >> 3] |= (uint32_t)p.res[(base + i) / 2] << (4 * (i & 7));
+        }
+    }
+}
+
 // Requant / dequant / raw store of the 32 consecutive columns n0.. of row m.
 // Works in place on `ac` (the raw accumulators on entry); ca / cb / cz point at
-// this piece's constants in shared memory (warp-uniform broadcast reads).
-// Requant rounds and clips in the integer domain: cvt.rni is rint for |v| <
-// 2^31 and saturates beyond, ReLU is a max with 0, z_out a saturating add,
-// then min / max to the code range -- the fp32 clip of rint(v) + z_out for
-// every finite v (M, Bq and R must be finite).
+// this piece's constants in shared memory (warp-uniform broadcast reads); rw
+// holds the piece's residual codes.  Requant rounds and clips in the integer
+// domain: r = cvt.rni(v) is rint(v) for |v| < 2^31 and saturates beyond, and
+// clip(max(r, 0) + z_out) = min(max(r, lo), hi) + z_out with lo = max(0,
+// qmin - z_out) (ReLU) or qmin - z_out, hi = qmax - z_out -- the fp32 result
+// of the page's formula for every finite v (M, Bq and R must be finite).
 __device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, int32_t (&ac)[32],
-                                               const float *ca, const float *cb, const float *cz)
+                                               const float *ca, const float *cb, const float *cz,
+                                               const uint32_t (&rw)[8])
 {
     if (m >= p.M || n0 >= p.N) return;
     const bool vec = p.vec_ok;
@@ -378,29 +505,6 @@ __device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, i
         return;
     }
     // REQUANT
-    uint32_t rw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) rw[i] = 0;
-    if (p.res) {
-        if (p.res_bits == 8) {
-            if (vec) {
-                const uint4 r0 = ldg_nc_v4(p.res + base), r1 = ldg_nc_v4(p.res + base + 16);
-                rw[0] = r0.x; rw[1] = r0.y; rw[2] = r0.z; rw[3] = r0.w;
-                rw[4] = r1.x; rw[5] = r1.y; rw[6] = r1.z; rw[7] = r1.w;
-            } else {
-                for (int i = 0; i < 32 && n0 + i < p.N; ++i)
-                    rw[i >> 2] |= (uint32_t)p.res[base + i] << (8 * (i & 3));
-            }
-        } else {
-            if (vec) {
-                const uint4 r0 = ldg_nc_v4(p.res + base / 2);
-                rw[0] = r0.x; rw[1] = r0.y; rw[2] = r0.z; rw[3] = r0.w;
-            } else {
-                for (int i = 0; i < 32 && n0 + i < p.N; i += 2)
-                    rw[i >> 3] |= (uint32_t)p.res[(base + i) / 2] << (4 * (i & 7));
-            }
-        }
-    }
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
         const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
@@ -413,10 +517,7 @@ __device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, i
             if (p.res)
                 t = __fadd_rn(__fmul_rn(__int2float_rn(res_code(p, rw, i + k) - p.z_res), p.R), t);
             const float v = __fadd_rn(__fmul_rn(__int2float_rn(ac[i + k]), mm[k]), t);
-            int32_t r = cvt_rni(v);
-            if (p.relu) r = max(r, 0);
-            r = add_sat(r, p.z_out);
-            ac[i + k] = min(max(r, p.qmin_i), p.qmax_i);
+            ac[i + k] = min(max(cvt_rni(v), p.clip_lo), p.clip_hi) + p.z_out;
         }
     }
     uint8_t *C = static_cast<uint8_t *>(p.C);
@@ -482,14 +583,22 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
         const int t = blockIdx.x + i * gridDim.x;
         const int m = (t % p.num_m) * BM + quad * 32 + lane;
         const int nbase = (t / p.num_m) * TBN + half * COLS;
-        stage_columns<COLS>(p, cols, nbase, lane);
+        ColumnRegs<COLS> cr;
+        load_columns<COLS>(p, cr, nbase, lane);
         if (!MULTI) {
+            uint32_t rw_next[8];
+            load_residual(p, m, nbase, rw_next);
             const uint32_t abuf = u & 1u;
-            if (!mbar_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
+            if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
             tc_fence_after();
+            store_columns<COLS>(cr, cols, lane);
             const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + half * COLS;
 #pragma unroll 1
             for (int jp = 0; jp < PIECES; ++jp) {
+                uint32_t rw[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) rw[k] = rw_next[k];
+                if (jp + 1 < PIECES) load_residual(p, m, nbase + (jp + 1) * 32, rw_next);
                 uint32_t r[32];
                 tmem_ld32(taddr + jp * 32, r);
                 tmem_ld_wait();
@@ -502,14 +611,14 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
                     if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
                 }
                 epilogue_piece(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
-                               cols + 2 * COLS + jp * 32);
+                               cols + 2 * COLS + jp * 32, rw);
             }
             ++u;
         } else {
             int32_t acc[PIECES][32];
             for (int c = 0; c < p.nchunks; ++c) {
                 const uint32_t abuf = u & 1u;
-                if (!mbar_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
+                if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
                 tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + half * COLS;
 #pragma unroll
@@ -528,10 +637,14 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
                 if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
                 ++u;
             }
+            store_columns<COLS>(cr, cols, lane);
 #pragma unroll
-            for (int jp = 0; jp < PIECES; ++jp)
+            for (int jp = 0; jp < PIECES; ++jp) {
+                uint32_t rw[8];
+                load_residual(p, m, nbase + jp * 32, rw);
                 epilogue_piece(p, m, nbase + jp * 32, acc[jp], cols + jp * 32, cols + COLS + jp * 32,
-                               cols + 2 * COLS + jp * 32);
+                               cols + 2 * COLS + jp * 32, rw);
+            }
         }
     }
 }
@@ -548,8 +661,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(smem_u32(&s.a_full[i]), 4);
-            mbar_init(smem_u32(&s.b_full[i]), 1);
+            mbar_init(smem_u32(&s.full[i]), 5);
             mbar_init(smem_u32(&s.empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -577,9 +689,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
         converter_role<Op, TBN, MULTI>(p, s, units);
     } else if (warp < 8) {
         if (MULTI) regs_dec<56>();
-        if (warp == PRODUCER_WARP && lane == 0) producer_role<Op, TBN>(p, s, units);
-        if (warp == MMA_WARP && lane == 0) mma_role<Op, TBN>(p, s, my_tiles, tmem);
-        __syncwarp();
+        if (warp == PRODUCER_WARP) producer_role<Op, TBN>(p, s, units);
+        if (warp == MMA_WARP) mma_role<Op, TBN>(p, s, my_tiles, tmem);
     } else {
         if (MULTI) regs_inc<160>();
         epilogue_role<Op, TBN, MULTI>(p, s, my_tiles, tmem);
@@ -632,8 +743,8 @@ inline qnn_status setup_epilogue(const qnn_epilogue *e, bool conv, Params &p)
         int32_t lo, hi;
         qrange(e->out_dt, 0, &lo, &hi);
         if (e->z_out < lo || e->z_out > hi) return QNN_ERR_INVALID_ARG;
-        p.qmin_i = lo;
-        p.qmax_i = hi;
+        p.clip_lo = e->relu ? (lo - e->z_out > 0 ? lo - e->z_out : 0) : lo - e->z_out;
+        p.clip_hi = hi - e->z_out;
         p.out_bits = (e->out_dt == QNN_U4) ? 4 : 8;
         p.out_signed = (e->out_dt == QNN_S8);
         if (e->residual) {
