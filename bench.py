@@ -397,8 +397,11 @@ def run_case(args):
         q = torch.empty((R, Cc), dtype=torch.uint8, device=device)
         p = qnn.qparams("sym", scale=scale, per_channel=True, axis=0)
         fn = lambda: qnn.q_quantize(x, q, "s8", p, stream=stream)  # noqa: E731
-    elif case in ("vit_fc1", "square_4096", "vitl_fc2"):
-        if case == "vit_fc1":
+    elif case in ("vit_fc1", "square_4096", "vitl_fc2") or case.startswith("gemm:"):
+        if case.startswith("gemm:"):
+            Mg, Ng, Kg = (int(v) for v in case.split(":")[1:4])
+            w, a_dt, alpha = workloads.vit_fc1(M=Mg, K=Kg, N=Ng), "u8", None
+        elif case == "vit_fc1":
             w, a_dt, alpha = workloads.vit_fc1(), "u8", None
         elif case == "square_4096":
             w, a_dt, alpha = workloads.gemm_square(4096), "s8", None
@@ -543,7 +546,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--case", default=None,
                     help="run one workload only (profiling): quantize, vit_fc1, square_4096, "
-                         "vitl_fc2, conv3x3, conv1x1")
+                         "vitl_fc2, conv3x3, conv1x1, or gemm:M:N:K (u8 x s8 -> s8)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -37,7 +37,7 @@ struct ConvState {
     int ih0[4];
     int iw0[4];
     int c0, fh, fw;
-    int kstep;       // K step of the current unit
+    UnitCursor c;    // the unit being loaded
     uint64_t kinds;  // per staging slot (8 bits): what each of the 4 rows holds, 2 bits each
 };
 
@@ -53,10 +53,10 @@ __device__ __forceinline__ void conv_seek(const Params &p, ConvState &st, int kp
 template <int GROUP_ELEMS, int STEP_ELEMS>
 __device__ __forceinline__ void conv_cursor(const Params &p, ConvState &st, int j, int sub, int rbase)
 {
-    const int ks = j % p.KT;
-    if (ks == 0) {
-        const int t = unit_tile(p, j);
-        const int m0 = (t % p.num_m) * BM;
+    if (j == 0) st.c.begin(p);
+    else st.c.next(p);
+    if (st.c.kl == 0) {
+        const int m0 = st.c.mb * BM;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int r = m0 + q * 32 + rbase;
@@ -74,12 +74,9 @@ __device__ __forceinline__ void conv_cursor(const Params &p, ConvState &st, int 
                 st.iw0[q] = 0;
             }
         }
-        // the same K walk as unit_kstep: start at this CTA's rotated K step
-        st.kstep = unit_kstep(p, j);
-        conv_seek(p, st, st.kstep * STEP_ELEMS + sub * GROUP_ELEMS);
-    } else if (++st.kstep == p.KT) {
-        st.kstep = 0;
-        conv_seek(p, st, sub * GROUP_ELEMS);
+        conv_seek(p, st, st.c.ks * STEP_ELEMS + sub * GROUP_ELEMS);
+    } else if (st.c.ks == 0) {
+        conv_seek(p, st, sub * GROUP_ELEMS);  // the K walk wrapped around
     } else {
         st.c0 += STEP_ELEMS;
         while (st.c0 >= p.Cin) {

@@ -53,17 +53,20 @@ struct GemmOp {
         uint4 v[4];
         uint4 alpha;
     };
-    struct State {};
+    struct State {
+        UnitCursor c;
+    };
 
+    // Units are loaded in order, one call each; the cursor follows them.
     template <int D>
-    __device__ static void load(const Params &p, State &, const uint4 *, int j, bool valid, int sub,
+    __device__ static void load(const Params &p, State &st, const uint4 *, int j, bool valid, int sub,
                                 int rbase, Unit &u)
     {
         if (!valid) return;
-        const int t = unit_tile(p, j);
-        const int ks = unit_kstep(p, j);
-        const int m0 = (t % p.num_m) * BM;
-        const int k0 = ks * 64 + sub * 16;
+        if (j == 0) st.c.begin(p);
+        else st.c.next(p);
+        const int m0 = st.c.mb * BM;
+        const int k0 = st.c.ks * 64 + sub * 16;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int m = m0 + q * 32 + rbase;

@@ -94,18 +94,40 @@ struct __align__(1024) Smem {
 template <class Op, int TBN>
 constexpr size_t smem_bytes() { return sizeof(Smem<Op, TBN>) + 1024; }
 
-// Which tile a unit (tile iteration, K step) of this CTA belongs to.
-__device__ __forceinline__ int unit_tile(const Params &p, int j) { return blockIdx.x + (j / p.KT) * gridDim.x; }
-
-// The K step a unit covers.  Each CTA walks K starting at its own offset
+// Walks this CTA's units -- (tile, K step) pairs, tile by tile -- without
+// divisions in the steady state.  Each CTA walks K starting at its own offset
 // (blockIdx.x mod KT), so CTAs that share a weight block read different slices
-// of it at any moment.  Integer sums do not depend on the order, and a chunk of
+// of it at any moment; integer sums do not depend on the order, and a chunk of
 // consecutive units still spans at most chunk_steps K steps.
-__device__ __forceinline__ int unit_kstep(const Params &p, int j)
-{
-    const int ks = j % p.KT + (int)(blockIdx.x % (unsigned)p.KT);
-    return ks >= p.KT ? ks - p.KT : ks;
-}
+struct UnitCursor {
+    int kl;      // position of the unit within its tile, 0 .. KT - 1
+    int ks;      // K step the unit covers
+    int rot;     // first K step of every tile
+    int t;       // tile index
+    int mb, nb;  // tile coordinates: row block, column block
+
+    __device__ __forceinline__ void begin(const Params &p)
+    {
+        rot = (int)(blockIdx.x % (unsigned)p.KT);
+        t = blockIdx.x;
+        kl = 0;
+        ks = rot;
+        mb = t % p.num_m;
+        nb = t / p.num_m;
+    }
+    __device__ __forceinline__ void next(const Params &p)
+    {
+        if (++kl == p.KT) {
+            kl = 0;
+            ks = rot;
+            t += gridDim.x;
+            mb = t % p.num_m;
+            nb = t / p.num_m;
+        } else if (++ks == p.KT) {
+            ks = 0;
+        }
+    }
+};
 
 // A bounded wait whose outcome is the same on every lane of the warp.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t *status)
@@ -205,10 +227,13 @@ template <class Op, int TBN>
 __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
 {
     const bool leader = (threadIdx.x & 31) == 0;
+    const uint32_t b0 = smem_u32(&s.b[0][0]);
+    UnitCursor c;
+    c.begin(p);
     bool ok = true;
     bool ready = false;
     int j = 0;
-    for (; j < units; ++j) {
+    for (; j < units; ++j, c.next(p)) {
         const int stage = j % STAGES;
         const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
         if (!ready && !warp_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status)) {
@@ -218,15 +243,13 @@ __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
         const int jn = j + 1;
         const bool probe = mbar_test_wait(smem_u32(&s.empty[jn % STAGES]), ((uint32_t)(jn / STAGES) & 1u) ^ 1u);
         if (leader) {
-            const int t = unit_tile(p, j);
-            const int ks = unit_kstep(p, j);
             // columns n0 .. n0 + TBN - 1 live in the 256-row packed block n0 / 256
-            const int n0 = (t / p.num_m) * TBN;
-            const uint8_t *src = p.Bp + ((int64_t)(n0 / gemm::BN) * p.KT + ks) * gemm::B_STAGE_BYTES +
+            const int n0 = c.nb * TBN;
+            const uint8_t *src = p.Bp + ((int64_t)(n0 / gemm::BN) * p.KT + c.ks) * gemm::B_STAGE_BYTES +
                                  (int64_t)(n0 % gemm::BN) * ROW_BYTES;
             const uint32_t bar = smem_u32(&s.full[stage]);
             mbar_arrive_expect_tx(bar, TBN * ROW_BYTES);
-            bulk_g2s(smem_u32(&s.b[stage][0]), src, TBN * ROW_BYTES, bar);
+            bulk_g2s(b0 + stage * (TBN * ROW_BYTES), src, TBN * ROW_BYTES, bar);
         }
         ready = __all_sync(0xffffffffu, probe) && jn < units;
     }
@@ -241,67 +264,55 @@ __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
 }
 
 // ---------------------------------------------------------------- MMA
-// The issuing loop probes the full barriers of up to STAGES upcoming units at
-// once (non-blocking, so their latencies overlap) and issues every unit found
-// ready back to back; it blocks only when the next unit is not ready yet.
+// The issuing loop is kept as short as possible: it is the one serial
+// instruction stream every pipeline unit passes through (one wait, four MMAs,
+// one or two commits, counters instead of divisions).
 template <class Op, int TBN>
 __device__ void mma_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32_t tmem)
 {
     constexpr uint32_t IDESC = idesc_f32acc(0, 0, BM, TBN);  // f16 x f16, or e4m3 x e4m3
     const bool leader = (threadIdx.x & 31) == 0;
     const int units = my_tiles * p.KT;
+    const uint64_t adesc0 = sdesc_sw128(smem_u32(&s.a[0][0]));
+    const uint64_t bdesc0 = sdesc_sw128(smem_u32(&s.b[0][0]));
     uint32_t u = 0;  // accumulation chunk counter
-    uint32_t abuf = 0;
-    int j = 0;
-    while (j < units) {
-        uint32_t mask = 0;
+    int kl = 0;      // unit position within the tile
+    int cpos = 0;    // unit position within the accumulation chunk
+    for (int j = 0; j < units; ++j) {
+        const int stage = j & (STAGES - 1);
+        const uint32_t abuf = u & 1u;
+        const bool first = cpos == 0;
+        const bool last = (cpos == p.chunk_steps - 1) || (kl == p.KT - 1);
+        if (first && !warp_wait(smem_u32(&s.acc_empty[abuf]), ((u >> 1) & 1u) ^ 1u, p.status)) break;
+        if (!warp_wait(smem_u32(&s.full[stage]), (uint32_t)(j / STAGES) & 1u, p.status)) break;
+        tc_fence_after();
+        if (leader) {
+            // descriptor start addresses are in 16-byte units: +2 per 32-byte K slice
+            const uint64_t ad = adesc0 + (uint64_t)(stage * (A_STAGE_BYTES >> 4));
+            const uint64_t bd = bdesc0 + (uint64_t)(stage * ((TBN * ROW_BYTES) >> 4));
+            const uint32_t d = tmem + abuf * TBN;
 #pragma unroll
-        for (int b = 0; b < STAGES; ++b) {
-            const int jb = j + b;
-            const bool r = (jb < units) &&
-                           mbar_test_wait(smem_u32(&s.full[jb % STAGES]), (uint32_t)(jb / STAGES) & 1u);
-            mask |= (uint32_t)r << b;
-        }
-        mask = __reduce_and_sync(0xffffffffu, mask);
-        int nready = __ffs(~mask) - 1;  // leading ready units
-        if (nready == 0) {
-            if (!warp_wait(smem_u32(&s.full[j % STAGES]), (uint32_t)(j / STAGES) & 1u, p.status)) break;
-            nready = 1;
-        }
-        bool ok = true;
-        for (int r = 0; r < nready; ++r, ++j) {
-            const int ks = j % p.KT;
-            const int stage = j % STAGES;
-            const bool first = (ks % p.chunk_steps) == 0;
-            const bool last = ((ks % p.chunk_steps) == p.chunk_steps - 1) || (ks == p.KT - 1);
-            if (first) {
-                abuf = u & 1u;
-                if (!warp_wait(smem_u32(&s.acc_empty[abuf]), ((u >> 1) & 1u) ^ 1u, p.status)) {
-                    ok = false;
-                    break;
-                }
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                if (Op::F8)
+                    mma_f8f6f4_ss(d, ad + 2 * kk, bd + 2 * kk, IDESC, acc);
+                else
+                    mma_f16_ss(d, ad + 2 * kk, bd + 2 * kk, IDESC, acc);
             }
-            tc_fence_after();
-            if (leader) {
-                const uint32_t a0 = smem_u32(&s.a[stage][0]);
-                const uint32_t b0 = smem_u32(&s.b[stage][0]);
-                const uint32_t d = tmem + abuf * TBN;
-                // 4 MMAs of 32 bytes of K each: 16 fp16 or 32 e4m3 values
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-                    if (Op::F8)
-                        mma_f8f6f4_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), IDESC, acc);
-                    else
-                        mma_f16_ss(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), IDESC, acc);
-                }
-                mma_commit(smem_u32(&s.empty[stage]));
-                if (last) mma_commit(smem_u32(&s.acc_full[abuf]));
-            }
-            __syncwarp();
-            if (last) ++u;
+            mma_commit(smem_u32(&s.empty[stage]));
+            if (last) mma_commit(smem_u32(&s.acc_full[abuf]));
         }
-        if (!ok) break;
+        __syncwarp();
+        if (last) {
+            ++u;
+            cpos = 0;
+        } else {
+            ++cpos;
+        }
+        if (++kl == p.KT) {
+            kl = 0;
+            cpos = 0;
+        }
     }
     // every MMA issued must have completed before the CTA winds down
     if (leader) mma_commit(smem_u32(&s.mma_done));
