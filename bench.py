@@ -34,6 +34,24 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the headline GEMM kernel, from the ncu capture summarised in
+# profiles/qgemm_vit_fc1.md, valid only for the kernel sources it was taken on
+# (hash of integer_quantized_nn_gb300/csrc/*); reported as null otherwise.
+TRAFFIC_NCU = {"csrc_sha256_16": "bbe5a8b6d0c89b5f", "bytes": 14527232 + 55808}
+
+
+def csrc_hash():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "integer_quantized_nn_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -260,9 +278,12 @@ def run_gpu(args):
                    "M": M, "K": K, "N": N, "tokens": "64 x 197", "l2": "flushed between steps "
                    "(256 MiB write, outside the timed events)", "parallelism": f"replicas x{dist.ws}"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": (TRAFFIC_NCU["bytes"] if csrc_hash() == TRAFFIC_NCU["csrc_sha256_16"]
+                                 else None),
+                     "traffic_unit": "bytes per launch (ncu DRAM read + write)",
                      "peak_kind": f"{pk_kind} bf16 dense burst (the f16 MMA kind runs at the bf16 rate)",
-                     "kernel": "qgemm_kernel<256,false,false>",
+                     "kernel": "qmma_kernel<GemmOp<false>,256,false>",
                      "algorithmic": "2*M*N*K int ops per launch"},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 3), "unit": "TOPS", "h2d_bytes_per_step": M * K,
