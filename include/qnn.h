@@ -138,7 +138,8 @@ typedef struct {
     const void *residual;    /* device [rows, N] codes of res_dt (same layout as the
                                 output), or NULL: REQUANT only */
     int32_t res_dt;          /* S8, U8 (GEMM); U4, U8 (conv) */
-    int32_t z_res;           /* residual zero point */
+    int32_t z_res;           /* residual zero point, inside res_dt's code range
+                                (else QNN_ERR_INVALID_ARG) */
     float R;                 /* S_res / S_out */
     const uint8_t *ptf_shift;/* device [K] per-input-channel Power-of-Two Factor
                                 alpha_k [FQ 3.2]: the GEMM uses A[m][k] * 2^alpha_k;

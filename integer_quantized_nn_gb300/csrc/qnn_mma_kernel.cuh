@@ -62,7 +62,7 @@ struct Params {
     int chunk_steps, nchunks;
     // epilogue
     int mode, relu, z_out, out_bits, out_signed;
-    int32_t clip_lo, clip_hi;  // requant: clip of rint(v) before adding z_out (ReLU folded in)
+    float clip_lo_f, clip_hi_f;  // requant: clip of v before rounding and adding z_out (ReLU folded in)
     const int32_t *zp;
     const float *Mv;
     const float *Bq;
@@ -71,6 +71,7 @@ struct Params {
     const uint8_t *res;
     int res_bits, res_signed, z_res;
     float R;
+    float res_c;             // 1.5 * 2^23 + z_res (+ 128 or 8 for signed residual codes)
     void *C;
     int32_t *C32;
     int vec_ok;              // N % 32 == 0: every 32-column piece whole and 16-byte aligned
@@ -82,7 +83,7 @@ struct __align__(1024) Smem {
     uint8_t a[STAGES][A_STAGE_BYTES];
     uint8_t b[STAGES][TBN * ROW_BYTES];
     uint4 stg[Op::STG_BYTES / 16];                   // converter staging ring (Op-specific)
-    float cols[NUM_EPI_WARPS][3 * (TBN / 2)];        // per epilogue warp: its columns' constants
+    float cols[NUM_EPI_WARPS][4 * (TBN / 2)];        // per epilogue warp: its columns' constants
     uint64_t full[STAGES];   // 4 converter-warp arrivals + the producer's expect_tx arrival
     uint64_t empty[STAGES];
     uint64_t acc_full[2];
@@ -326,60 +327,11 @@ __device__ __forceinline__ void st_v4(void *ptr, uint32_t a, uint32_t b, uint32_
     *reinterpret_cast<uint4 *>(ptr) = make_uint4(a, b, c, d);
 }
 
-__device__ __forceinline__ int32_t cvt_rni(float f)
-{
-    int32_t d;
-    asm("cvt.rni.s32.f32 %0, %1;" : "=r"(d) : "f"(f));
-    return d;
-}
-
-__device__ __forceinline__ int32_t add_sat(int32_t a, int32_t b)
-{
-    int32_t d;
-    asm("add.sat.s32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// d = c << 2w | b << w | a for w-bit codes a, b already inside the code range
-__device__ __forceinline__ uint32_t pack_s8(int32_t a, int32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(b), "r"(a), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t pack_u8(int32_t a, int32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(b), "r"(a), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t pack_u4(int32_t a, int32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("cvt.pack.sat.u4.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(b), "r"(a), "r"(c));
-    return d;
-}
-
-// Residual code of column i of a 32-column piece held in rw (8-bit: 8 words of
-// 4 codes; 4-bit: 4 words of 8 codes).
-__device__ __forceinline__ int32_t res_code(const Params &p, const uint32_t (&rw)[8], int i)
-{
-    int32_t v;
-    if (p.res_bits == 8) {
-        v = (int32_t)((rw[i >> 2] >> (8 * (i & 3))) & 255u);
-        if (p.res_signed && v >= 128) v -= 256;
-    } else {
-        v = (int32_t)((rw[i >> 3] >> (4 * (i & 7))) & 15u);
-        if (p.res_signed && v >= 8) v -= 16;
-    }
-    return v;
-}
-
 // Each epilogue warp keeps the per-column constants of its COLS columns in
 // shared memory: [0, COLS) M (requant) or D (dequant), [COLS, 2 COLS) Bq or
-// bias, [2 COLS, 3 COLS) zp_term (as int bits).  The loads of a tile's
-// constants are issued before the warp waits for the tile's accumulator and
-// stored to shared memory after it.
+// bias, [2 COLS, 3 COLS) -zp_term as an fp32 value, [3 COLS, 4 COLS) zp_term
+// (as int bits).  The loads of a tile's constants are issued before the warp
+// waits for the tile's accumulator and stored to shared memory after it.
 template <int COLS>
 struct ColumnRegs {
     float a[COLS / 32], b[COLS / 32];
@@ -411,17 +363,28 @@ __device__ __forceinline__ void load_columns(const Params &p, ColumnRegs<COLS> &
     }
 }
 
+// Returns whether -zp_term is an fp32 value for every column of the warp
+// (always so for |zp_term| <= 2^24): then float(acc) + float(-zp_term) is the
+// correctly rounded float(acc - zp_term), the conversion the requant formula
+// starts from, without an integer round trip.
 template <int COLS>
-__device__ __forceinline__ void store_columns(const ColumnRegs<COLS> &cr, float *cols, int lane)
+__device__ __forceinline__ bool store_columns(const ColumnRegs<COLS> &cr, float *cols, int lane)
 {
     __syncwarp();
+    bool exact = true;
 #pragma unroll
     for (int k = 0; k < COLS / 32; ++k) {
+        const int32_t z = cr.z[k];
+        const int32_t nzi = (int32_t)(0u - (uint32_t)z);
+        const float nz = __int2float_rn(nzi);
+        exact = exact && z != INT32_MIN && __float2int_rn(nz) == nzi;
         cols[32 * k + lane] = cr.a[k];
         cols[COLS + 32 * k + lane] = cr.b[k];
-        cols[2 * COLS + 32 * k + lane] = __int_as_float(cr.z[k]);
+        cols[2 * COLS + 32 * k + lane] = nz;
+        cols[3 * COLS + 32 * k + lane] = __int_as_float(z);
     }
     __syncwarp();
+    return __all_sync(0xffffffffu, exact);
 }
 
 // The residual codes of the 32 columns n0.. of row m (8-bit: 8 words of 4
@@ -452,17 +415,145 @@ __device__ __forceinline__ void load_residual(const Params &p, int m, int n0, ui
     }
 }
 
-// Requant / dequant / raw store of the 32 consecutive columns n0.. of row m.
-// Works in place on `ac` (the raw accumulators on entry); ca / cb / cz point at
-// this piece's constants in shared memory (warp-uniform broadcast reads); rw
-// holds the piece's residual codes.  Requant rounds and clips in the integer
-// domain: r = cvt.rni(v) is rint(v) for |v| < 2^31 and saturates beyond, and
-// clip(max(r, 0) + z_out) = min(max(r, lo), hi) + z_out with lo = max(0,
-// qmin - z_out) (ReLU) or qmin - z_out, hi = qmax - z_out -- the fp32 result
-// of the page's formula for every finite v (M, Bq and R must be finite).
-__device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, int32_t (&ac)[32],
-                                               const float *ca, const float *cb, const float *cz,
+// fp32 1.5 * 2^23: for |x| < 2^22, x + 2^23 * 1.5 lands in [2^23, 2^24) where
+// the fp32 spacing is 1, so the sum's bits are 0x4B400000 + x rounded half to
+// even (an exact integer x when x is one); byte and nibble fields of those
+// bits are the two's-complement low bits of that integer.
+constexpr float ROUND_MAGIC = 12582912.0f;
+constexpr uint32_t ROUND_MAGIC_BITS = 0x4B400000u;
+
+// Residual term t_n = float(r - z_res) * R + Bq_n for the 32 columns: the code
+// r - z_res is rebuilt as an fp32 value from the magic-number bits (exact, as
+// |r - z_res| < 2^22), then one fmul and one fadd as in the requant formula.
+__device__ __forceinline__ void add_residual(const Params &p, const uint32_t (&rw)[8], float (&t)[32])
+{
+    if (p.res_bits == 8) {
+        const uint32_t flip = p.res_signed ? 0x80808080u : 0u;  // s8 -> offset binary
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const uint32_t x = rw[w] ^ flip;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const float d = __fsub_rn(__uint_as_float(prmt(x, ROUND_MAGIC_BITS, 0x7650u | b)), p.res_c);
+                t[4 * w + b] = __fadd_rn(__fmul_rn(d, p.R), t[4 * w + b]);
+            }
+        }
+    } else {
+        const uint32_t cx = (p.res_signed ? 8u : 0u) | ROUND_MAGIC_BITS;  // s4 -> offset binary
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const float d = __fsub_rn(__uint_as_float(((rw[w] >> (4 * b)) & 15u) ^ cx), p.res_c);
+                t[8 * w + b] = __fadd_rn(__fmul_rn(d, p.R), t[8 * w + b]);
+            }
+        }
+    }
+}
+
+// Low bytes of four words -> one word (byte k from word k).
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3)
+{
+    return prmt(prmt(c0, c1, 0x0040u), prmt(c2, c3, 0x0040u), 0x5410u);
+}
+
+// Requant / dequant of the 32 consecutive columns n0.. of row m from
+// a[k] = float(acc_c) (the correctly rounded fp32 value of the int32 sum minus
+// its zero-point term).  ca / cb point at this piece's constants in shared
+// memory (warp-uniform broadcast reads); rw holds the piece's residual codes.
+// Requant: v = float(acc_c) * M + t (one fmul, one fadd); rounding and the
+// clip are done as clamp(v, lo, hi) then a magic-number add, which equals
+// clip(rint(v)) for the integer bounds lo = qmin - z_out (or max(0, qmin -
+// z_out) with ReLU) and hi = qmax - z_out; z_out is then added to the integer
+// -- the fp32 result of the page's formula for every finite v (M, Bq and R
+// must be finite).  No conversion instructions are used.
+__device__ __forceinline__ void epilogue_float(const Params &p, int m, int n0, float (&a)[32],
+                                               const float *ca, const float *cb,
                                                const uint32_t (&rw)[8])
+{
+    if (m >= p.M || n0 >= p.N) return;
+    const bool vec = p.vec_ok;
+    const int64_t base = (int64_t)m * p.N + n0;  // element offset of (m, n0)
+    if (p.mode == QNN_EPI_DEQUANT) {
+        float *C = static_cast<float *>(p.C);
+        uint32_t y[32];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+            const float4 d = *reinterpret_cast<const float4 *>(ca + i);
+            const float4 b = *reinterpret_cast<const float4 *>(cb + i);
+            y[i] = __float_as_uint(__fadd_rn(__fmul_rn(a[i], d.x), b.x));
+            y[i + 1] = __float_as_uint(__fadd_rn(__fmul_rn(a[i + 1], d.y), b.y));
+            y[i + 2] = __float_as_uint(__fadd_rn(__fmul_rn(a[i + 2], d.z), b.z));
+            y[i + 3] = __float_as_uint(__fadd_rn(__fmul_rn(a[i + 3], d.w), b.w));
+        }
+        if (vec) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) st_v4(C + base + i, y[i], y[i + 1], y[i + 2], y[i + 3]);
+        } else {
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = __uint_as_float(y[i]);
+        }
+        return;
+    }
+    // REQUANT
+    float t[32];
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        const float4 bq = *reinterpret_cast<const float4 *>(cb + i);
+        t[i] = bq.x;
+        t[i + 1] = bq.y;
+        t[i + 2] = bq.z;
+        t[i + 3] = bq.w;
+    }
+    if (p.res) add_residual(p, rw, t);
+    uint32_t c[32];  // low bits: the output codes
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
+        const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float v = __fadd_rn(__fmul_rn(a[i + k], mm[k]), t[i + k]);
+            v = fminf(fmaxf(v, p.clip_lo_f), p.clip_hi_f);
+            c[i + k] = __float_as_uint(__fadd_rn(v, ROUND_MAGIC)) + (uint32_t)p.z_out;
+        }
+    }
+    uint8_t *C = static_cast<uint8_t *>(p.C);
+    if (p.out_bits == 8) {
+        uint32_t ow[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) ow[w] = pack_low_bytes(c[4 * w], c[4 * w + 1], c[4 * w + 2], c[4 * w + 3]);
+        if (vec) {
+            st_v4(C + base, ow[0], ow[1], ow[2], ow[3]);
+            st_v4(C + base + 16, ow[4], ow[5], ow[6], ow[7]);
+        } else {
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = (uint8_t)(ow[i >> 2] >> (8 * (i & 3)));
+        }
+    } else {
+        // codes 2k (low nibble) and 2k + 1 (high nibble) share byte k
+        uint32_t ow[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t *q = c + 8 * w;
+            const uint32_t ev = pack_low_bytes(q[0], q[2], q[4], q[6]);
+            const uint32_t od = pack_low_bytes(q[1], q[3], q[5], q[7]);
+            ow[w] = (ev & 0x0F0F0F0Fu) | ((od << 4) & 0xF0F0F0F0u);
+        }
+        if (vec) {
+            st_v4(C + base / 2, ow[0], ow[1], ow[2], ow[3]);
+        } else {
+            // N is even: a byte holds columns (2i, 2i+1) of this thread's row only
+            for (int i = 0; i < 32 && n0 + i < p.N; i += 2)
+                C[(base + i) / 2] = (uint8_t)(ow[i >> 3] >> (4 * (i & 7)));
+        }
+    }
+}
+
+// The same from int32 sums (multi-chunk K, raw int32 outputs, or zero-point
+// terms that are not fp32 values): subtracts zp_term (cz: its int bits), stores
+// the raw sums where asked, and converts for the float epilogue.
+__device__ __forceinline__ void epilogue_int(const Params &p, int m, int n0, int32_t (&ac)[32],
+                                             const float *ca, const float *cb, const float *cz,
+                                             const uint32_t (&rw)[8])
 {
     if (m >= p.M || n0 >= p.N) return;
     const bool vec = p.vec_ok;
@@ -476,7 +567,7 @@ __device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, i
             ac[i + 3] -= __float_as_int(z.w);
         }
     }
-    const int64_t base = (int64_t)m * p.N + n0;  // element offset of (m, n0)
+    const int64_t base = (int64_t)m * p.N + n0;
     if (p.C32) {
         if (vec) {
 #pragma unroll
@@ -496,74 +587,10 @@ __device__ __forceinline__ void epilogue_piece(const Params &p, int m, int n0, i
         }
         return;
     }
-    if (p.mode == QNN_EPI_DEQUANT) {
-        float *C = static_cast<float *>(p.C);
+    float a[32];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            const float4 d = *reinterpret_cast<const float4 *>(ca + i);
-            const float4 b = *reinterpret_cast<const float4 *>(cb + i);
-            ac[i] = __float_as_int(__fadd_rn(__fmul_rn(__int2float_rn(ac[i]), d.x), b.x));
-            ac[i + 1] = __float_as_int(__fadd_rn(__fmul_rn(__int2float_rn(ac[i + 1]), d.y), b.y));
-            ac[i + 2] = __float_as_int(__fadd_rn(__fmul_rn(__int2float_rn(ac[i + 2]), d.z), b.z));
-            ac[i + 3] = __float_as_int(__fadd_rn(__fmul_rn(__int2float_rn(ac[i + 3]), d.w), b.w));
-        }
-        if (vec) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) st_v4(C + base + i, ac[i], ac[i + 1], ac[i + 2], ac[i + 3]);
-        } else {
-            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = __int_as_float(ac[i]);
-        }
-        return;
-    }
-    // REQUANT
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-        const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
-        const float4 bq = *reinterpret_cast<const float4 *>(cb + i);
-        const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-        const float bb[4] = {bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float t = bb[k];
-            if (p.res)
-                t = __fadd_rn(__fmul_rn(__int2float_rn(res_code(p, rw, i + k) - p.z_res), p.R), t);
-            const float v = __fadd_rn(__fmul_rn(__int2float_rn(ac[i + k]), mm[k]), t);
-            ac[i + k] = min(max(cvt_rni(v), p.clip_lo), p.clip_hi) + p.z_out;
-        }
-    }
-    uint8_t *C = static_cast<uint8_t *>(p.C);
-    if (p.out_bits == 8) {
-        uint32_t ow[8];
-        if (p.out_signed) {
-#pragma unroll
-            for (int w = 0; w < 8; ++w)
-                ow[w] = pack_s8(ac[4 * w], ac[4 * w + 1], pack_s8(ac[4 * w + 2], ac[4 * w + 3], 0));
-        } else {
-#pragma unroll
-            for (int w = 0; w < 8; ++w)
-                ow[w] = pack_u8(ac[4 * w], ac[4 * w + 1], pack_u8(ac[4 * w + 2], ac[4 * w + 3], 0));
-        }
-        if (vec) {
-            st_v4(C + base, ow[0], ow[1], ow[2], ow[3]);
-            st_v4(C + base + 16, ow[4], ow[5], ow[6], ow[7]);
-        } else {
-            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = (uint8_t)(ow[i >> 2] >> (8 * (i & 3)));
-        }
-    } else {
-        uint32_t ow[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const int32_t *q = ac + 8 * w;
-            ow[w] = pack_u4(q[0], q[1], pack_u4(q[2], q[3], pack_u4(q[4], q[5], pack_u4(q[6], q[7], 0))));
-        }
-        if (vec) {
-            st_v4(C + base / 2, ow[0], ow[1], ow[2], ow[3]);
-        } else {
-            // N is even: a byte holds columns (2i, 2i+1) of this thread's row only
-            for (int i = 0; i < 32 && n0 + i < p.N; i += 2)
-                C[(base + i) / 2] = (uint8_t)(ow[i >> 3] >> (4 * (i & 7)));
-        }
-    }
+    for (int k = 0; k < 32; ++k) a[k] = __int2float_rn(ac[k]);
+    epilogue_float(p, m, n0, a, ca, cb, rw);
 }
 
 // fp32 accumulator value -> exact int32 (the fp32 value times 2^scale_log2 is an integer)
@@ -602,7 +629,7 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
             const uint32_t abuf = u & 1u;
             if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
             tc_fence_after();
-            store_columns<COLS>(cr, cols, lane);
+            const bool fast = store_columns<COLS>(cr, cols, lane) && !p.C32 && p.mode != QNN_EPI_S32;
             const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + half * COLS;
 #pragma unroll 1
             for (int jp = 0; jp < PIECES; ++jp) {
@@ -613,16 +640,35 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
                 uint32_t r[32];
                 tmem_ld32(taddr + jp * 32, r);
                 tmem_ld_wait();
-                int32_t acc[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) acc[k] = acc_to_int<Op::SCALE_LOG2>(r[k]);
                 if (jp == PIECES - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
                 }
-                epilogue_piece(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
-                               cols + 2 * COLS + jp * 32, rw);
+                if (fast) {
+                    // the fp32 sum is an exact integer (times 2^-SCALE_LOG2); adding the
+                    // fp32 -zp_term rounds once, like the int32 -> fp32 conversion
+                    const float *cn = cols + 2 * COLS + jp * 32;
+                    float a[32];
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4) {
+                        const float4 nz = *reinterpret_cast<const float4 *>(cn + k);
+                        const float z4[4] = {nz.x, nz.y, nz.z, nz.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float f = __uint_as_float(r[k + e]);
+                            a[k + e] = Op::SCALE_LOG2 ? __fmaf_rn(f, (float)(1 << Op::SCALE_LOG2), z4[e])
+                                                      : __fadd_rn(f, z4[e]);
+                        }
+                    }
+                    epilogue_float(p, m, nbase + jp * 32, a, cols + jp * 32, cols + COLS + jp * 32, rw);
+                } else {
+                    int32_t acc[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) acc[k] = acc_to_int<Op::SCALE_LOG2>(r[k]);
+                    epilogue_int(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
+                                 cols + 3 * COLS + jp * 32, rw);
+                }
             }
             ++u;
         } else {
@@ -653,8 +699,8 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
             for (int jp = 0; jp < PIECES; ++jp) {
                 uint32_t rw[8];
                 load_residual(p, m, nbase + jp * 32, rw);
-                epilogue_piece(p, m, nbase + jp * 32, acc[jp], cols + jp * 32, cols + COLS + jp * 32,
-                               cols + 2 * COLS + jp * 32, rw);
+                epilogue_int(p, m, nbase + jp * 32, acc[jp], cols + jp * 32, cols + COLS + jp * 32,
+                             cols + 3 * COLS + jp * 32, rw);
             }
         }
     }
@@ -754,8 +800,8 @@ inline qnn_status setup_epilogue(const qnn_epilogue *e, bool conv, Params &p)
         int32_t lo, hi;
         qrange(e->out_dt, 0, &lo, &hi);
         if (e->z_out < lo || e->z_out > hi) return QNN_ERR_INVALID_ARG;
-        p.clip_lo = e->relu ? (lo - e->z_out > 0 ? lo - e->z_out : 0) : lo - e->z_out;
-        p.clip_hi = hi - e->z_out;
+        p.clip_lo_f = (float)(e->relu ? (lo - e->z_out > 0 ? lo - e->z_out : 0) : lo - e->z_out);
+        p.clip_hi_f = (float)(hi - e->z_out);
         p.out_bits = (e->out_dt == QNN_U4) ? 4 : 8;
         p.out_signed = (e->out_dt == QNN_S8);
         if (e->residual) {
@@ -769,6 +815,13 @@ inline qnn_status setup_epilogue(const qnn_epilogue *e, bool conv, Params &p)
             p.res_signed = (e->res_dt == QNN_S8 || e->res_dt == QNN_S4);
             p.z_res = e->z_res;
             p.R = e->R;
+            {
+                int32_t rlo, rhi;
+                qrange(e->res_dt, 0, &rlo, &rhi);
+                if (e->z_res < rlo || e->z_res > rhi) return QNN_ERR_INVALID_ARG;
+                const int off = p.res_signed ? (p.res_bits == 8 ? 128 : 8) : 0;
+                p.res_c = (float)(12582912 + e->z_res + off);
+            }
         }
         break;
     }
