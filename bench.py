@@ -1,10 +1,12 @@
 """Benchmark of the quantized GEMM / implicit-GEMM conv path on one GB300.
 
-A step is one qgemm_s8 call (u8 activations with zero point x s8 per-channel
+A step is one quantized GEMM (u8 activations with zero point x s8 per-channel
 weights, int32 accumulation, fused requant to int8) on the ViT-B MLP fc1
-layer: M = 64 x 197 tokens = 12608, K = 768, N = 3072.  Inputs are resident in
-HBM; L2 is flushed (a 256 MiB write) between timed steps, outside the timed
-events.  The line also carries the quantize GB/s of a 1 GiB fp32 -> s8
+layer: M = 64 x 197 tokens = 12608, K = 768, N = 3072, run as its two kernels
+(qgemm_pack_a: A re-encoded into the workspace; qgemm_s8_packed: the GEMM),
+timed apart with events so that the roofline line holds the GEMM kernel alone.
+Inputs are resident in HBM; L2 is flushed (a 256 MiB write) between timed
+steps, outside the timed events.  The line also carries the quantize GB/s of a 1 GiB fp32 -> s8
 per-row quantize and the other layer shapes as extras.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -197,6 +199,27 @@ def time_steps(torch, fn, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def time_split(torch, fns, steps, warmup, flush, stream):
+    """Like time_steps for a step made of several calls: events before, between
+    and after the calls of fns.  Returns (whole-step ms list, per-call ms lists)."""
+    for _ in range(warmup):
+        flush()
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        for j, f in enumerate(fns):
+            f()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    whole = [e[0].elapsed_time(e[-1]) for e in ev]
+    parts = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(len(fns))]
+    return whole, parts
+
+
 def run_gpu(args):
     import torch
     dist = Dist("nccl")
@@ -217,9 +240,14 @@ def run_gpu(args):
     g = gpu_setup_gemm(torch, qnn, w, "u8", device)
     C = torch.empty((M, N), dtype=torch.uint8, device=device)
     epi = qnn.epilogue("requant", zp_term=g["zp"], M=g["M"], Bq=g["Bq"], out_dt="s8")
+    ws_buf = torch.empty(qnn.qnn_gemm_workspace_bytes(M, K), dtype=torch.uint8, device=device)
 
-    def step():
-        qnn.qgemm_s8(g["A"], "u8", g["Bp"], M, N, K, epi, C, stream=stream)
+    # a step: the A pre-pass kernel, then the GEMM kernel (timed apart)
+    def pack():
+        qnn.qgemm_pack_a(g["A"], "u8", M, K, ws_buf, stream=stream)
+
+    def gemm():
+        qnn.qgemm_s8_packed(ws_buf, "u8", g["Bp"], M, N, K, epi, C, stream=stream)
 
     flops = 2.0 * M * N * K
     dist.barrier()
@@ -228,7 +256,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     dist.barrier()
     t_wall0 = time.time()
-    times = time_steps(torch, step, args.steps, args.warmup, flush, stream)
+    times, (t_pack, t_gemm) = time_split(torch, [pack, gemm], args.steps, args.warmup, flush, stream)
     torch.cuda.synchronize()
     dist.barrier()
     t_wall1 = time.time()
@@ -239,8 +267,10 @@ def run_gpu(args):
     total_ms = sum(times)
     total_ms_max = dist.max(total_ms)
     value = dist.ws * args.steps * flops / (total_ms_max * 1e-3) / 1e12
-    per_launch_ms = total_ms / args.steps
-    achieved = flops / (per_launch_ms * 1e-3) / 1e12
+    gemm_ms = sum(t_gemm) / args.steps
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    pack_ms = sum(t_pack) / args.steps
+    pack_bytes = M * K + qnn.qnn_gemm_workspace_bytes(M, K)
 
     # ---- e2e: host buffers, copies inside the timed region
     A_h = torch.from_numpy(np.ascontiguousarray(w["A"])).pin_memory()
@@ -249,7 +279,7 @@ def run_gpu(args):
 
     def e2e_step():
         A_d.copy_(A_h, non_blocking=True)
-        qnn.qgemm_s8(A_d, "u8", g["Bp"], M, N, K, epi, C, stream=stream)
+        qnn.qgemm_s8(A_d, "u8", g["Bp"], M, N, K, epi, C, workspace=ws_buf, stream=stream)
         C_h.copy_(C, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 200))
@@ -283,12 +313,17 @@ def run_gpu(args):
                                  else None),
                      "traffic_unit": "bytes per launch (ncu DRAM read + write)",
                      "peak_kind": f"{pk_kind} bf16 dense burst (the f16 MMA kind runs at the bf16 rate)",
-                     "kernel": "qmma_kernel<GemmOp<false>,256,false>",
+                     "kernel": "qmma_kernel<GemmPackedOp,256,false>",
+                     "kernel_ms": round(gemm_ms, 5),
                      "algorithmic": "2*M*N*K int ops per launch"},
+        "prepass": {"kernel": "pack_a_kernel<false>", "ms": round(pack_ms, 5),
+                    "bytes": pack_bytes, "GB/s": round(pack_bytes / (pack_ms * 1e-3) / 1e9, 1),
+                    "frac_hbm": round(pack_bytes / (pack_ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]), 4),
+                    "algorithmic": "M*K code bytes read + the fp16 image written"},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 3), "unit": "TOPS", "h2d_bytes_per_step": M * K,
                 "d2h_bytes_per_step": M * N},
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "extras": extras,
     }
@@ -335,12 +370,17 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
         epi = qnn.epilogue("requant", zp_term=None if al is not None else g["zp"], M=g["M"],
                            Bq=g["Bq"], ptf_shift=al,
                            ptf_max_shift=0 if alpha is None else int(alpha.max()))
+        ws = torch.empty(qnn.qnn_gemm_workspace_bytes(Mm, Kk), dtype=torch.uint8, device=device)
         t = time_steps(torch, lambda: qnn.qgemm_s8(g["A"], a_dt, g["Bp"], Mm, Nn, Kk, epi, C,
-                                                   stream=stream), steps, 3, flush, stream)
+                                                   workspace=ws, stream=stream), steps, 3, flush, stream)
         ms = statistics.median(t)
+        tf = time_steps(torch, lambda: qnn.qgemm_s8(g["A"], a_dt, g["Bp"], Mm, Nn, Kk, epi, C,
+                                                    stream=stream), steps, 3, flush, stream)
+        ms_fused = statistics.median(tf)
         tops = 2.0 * Mm * Nn * Kk / (ms * 1e-3) / 1e12
         out[name] = {"M": Mm, "N": Nn, "K": Kk, "ms": round(ms, 4), "TOPS": round(tops, 2),
-                     "frac_f16_peak": round(tops / peak, 4)}
+                     "frac_f16_peak": round(tops / peak, 4),
+                     "ms_no_workspace": round(ms_fused, 4)}
 
     gemm_entry("gemm_sym_256", workloads.gemm_sym(), "s8")
     for nm, (Kk, Nn) in workloads.VITL_SHAPES.items():
@@ -441,7 +481,10 @@ def run_case(args):
         al = None if alpha is None else torch.from_numpy(alpha.astype(np.uint8)).to(device)
         epi = qnn.epilogue("requant", zp_term=None if al is not None else g["zp"], M=g["M"], Bq=g["Bq"],
                            ptf_shift=al, ptf_max_shift=0 if alpha is None else int(alpha.max()))
-        fn = lambda: qnn.qgemm_s8(g["A"], a_dt, g["Bp"], Mm, Nn, Kk, epi, C, stream=stream)  # noqa: E731
+        ws = None if getattr(args, "fused", False) else torch.empty(qnn.qnn_gemm_workspace_bytes(Mm, Kk), dtype=torch.uint8,
+                                                 device=device)
+        fn = lambda: qnn.qgemm_s8(g["A"], a_dt, g["Bp"], Mm, Nn, Kk, epi, C, workspace=ws,  # noqa: E731
+                                  stream=stream)
     elif case in ("conv3x3", "conv1x1"):
         if case == "conv3x3":
             w, geom = workloads.conv_u4(), (64, 56, 56, 64, 64, 3, 1, 1)
@@ -565,6 +608,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--fused", action="store_true",
+                    help="--case GEMMs: no workspace (A re-encoded inside the GEMM kernel)")
     ap.add_argument("--case", default=None,
                     help="run one workload only (profiling): quantize, vit_fc1, square_4096, "
                          "vitl_fc2, conv3x3, conv1x1, or gemm:M:N:K (u8 x s8 -> s8)")

@@ -147,6 +147,11 @@ typedef struct {
     int32_t ptf_max_shift;   /* upper bound (0..3) on every ptf_shift value */
 } qnn_epilogue;
 
+/* Size in bytes of the qgemm_s8 workspace for an M x K activation operand
+ * (the re-encoded A image: ceil(M / 128) * ceil(K / 64) * 16 KB); 0 if M or K
+ * is not positive. */
+size_t qnn_gemm_workspace_bytes(int M, int K);
+
 /* Quantized GEMM [QI 量化矩阵乘; MG 緩解精度下降]:
  *   acc[m][n] = sum_k (A[m][k] - c_a) * 2^alpha_k * B[n][k]   exact, in int32
  * then the epilogue above with zp_term folded by q_fold_epilogue.
@@ -154,10 +159,32 @@ typedef struct {
  * B_packed: from qgemm_prepack_b for the same N, K.
  * C: device [M, N] row-major, of out_dt (REQUANT), fp32 (DEQUANT) or int32 (S32).
  * C_s32: optional device [M, N] int32 that also receives acc_c (NULL: none).
+ * workspace: optional device scratch of at least qnn_gemm_workspace_bytes(M, K)
+ *   bytes (16-byte aligned), owned by the caller and overwritten by the call;
+ *   with it, A is re-encoded once by a pre-pass kernel on `stream` and the GEMM
+ *   streams both operands (the faster path); NULL: the GEMM re-encodes A
+ *   itself (no scratch).  Results are identical.  Two calls in flight at the
+ *   same time must not share a workspace.
  * Fails with QNN_ERR_OVERFLOW_RISK when K * max|a| * 2^ptf_max_shift * 128 could
- * exceed the int32 range. */
+ * exceed the int32 range; QNN_ERR_INVALID_ARG when workspace_bytes is too small. */
 qnn_status qgemm_s8(const void *A, qnn_dtype a_dt, const void *B_packed, int M, int N, int K,
-                    const qnn_epilogue *epi, void *C, int32_t *C_s32, qnn_stream_t stream);
+                    const qnn_epilogue *epi, void *C, int32_t *C_s32, void *workspace,
+                    size_t workspace_bytes, qnn_stream_t stream);
+
+/* The two halves of qgemm_s8 with a workspace, for callers that time them
+ * apart or reuse one re-encoded A for several GEMMs that share it:
+ * qgemm_pack_a writes A (codes of a_dt, [M, K], K % 16 == 0; u8 read as
+ * q - 128; times 2^ptf_shift[k] when ptf_shift is not NULL, S8 only) into
+ * A_packed (qnn_gemm_workspace_bytes(M, K) bytes, 16-byte aligned) as the
+ * fp16 operand image: [ceil(M/128)][ceil(K/64)][128 rows][64 fp16], each
+ * 128-byte row's 16-byte chunk c stored at chunk c ^ (row % 8), zero beyond M
+ * and K.  qgemm_s8_packed then takes that image in place of A; a_dt and epi
+ * (including ptf_shift / ptf_max_shift) must be those used for the packing. */
+qnn_status qgemm_pack_a(const void *A, qnn_dtype a_dt, int M, int K, const uint8_t *ptf_shift,
+                        void *A_packed, size_t A_packed_bytes, qnn_stream_t stream);
+qnn_status qgemm_s8_packed(const void *A_packed, qnn_dtype a_dt, const void *B_packed, int M, int N,
+                           int K, const qnn_epilogue *epi, void *C, int32_t *C_s32,
+                           qnn_stream_t stream);
 
 /* ---- implicit-GEMM convolution -------------------------------------------- */
 

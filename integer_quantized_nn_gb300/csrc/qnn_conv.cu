@@ -23,6 +23,7 @@
 // Padded taps read the code z_in (the real value 0 [reading of the pages]),
 // so the folded zero-point term applies to every tap alike.
 #include <cuda_fp8.h>
+#include <type_traits>
 #include "qnn_mma_kernel.cuh"
 
 namespace qnn {
@@ -109,6 +110,7 @@ struct ConvStaging {
     static constexpr int DEPTH = D;
     static constexpr int DEPTH_MULTI = D;
     static constexpr int STG_BYTES = D * 4 * 128 * 16;
+    static constexpr bool TMA_A = false;
     static constexpr bool REG_RING = false;
     struct Unit {};
     using State = ConvState;
@@ -144,8 +146,13 @@ struct ConvStaging {
         cp_async_commit();  // one group per unit, empty past the end
     }
 
+    // Before a unit is converted: its copy group must have landed.
+    template <int DD>
+    __device__ static void wait_unit() { cp_async_wait<DD - 1>(); }
+
     // The 16 input bytes of row q of unit j (after its group has landed).
-    __device__ static uint4 fetched(const Params &p, const ConvState &st, const uint4 *stg, int slot, int q)
+    __device__ static uint4 fetched(const Params &p, const ConvState &st, const uint4 *stg, int slot, int q,
+                                    const Unit &)
     {
         const uint32_t kind = (uint32_t)(st.kinds >> (8 * slot + 2 * q)) & 3u;
         if (kind == ROW_DATA) return stg[(slot * 4 + q) * 128 + threadIdx.x];
@@ -154,21 +161,73 @@ struct ConvStaging {
     }
 };
 
+// The same im2col fetch into a register ring: each unit's four 16-byte row
+// groups are loaded with plain non-coherent loads DEPTH - 1 units ahead
+// (padding and zero rows are resolved when the unit is loaded).
+template <int ELEM_BITS, int GROUP_ELEMS, int STEP_ELEMS>
+struct ConvRegRing {
+    static constexpr int DEPTH = 4;
+    static constexpr int DEPTH_MULTI = 3;
+    static constexpr int STG_BYTES = 16;  // no staging ring
+    static constexpr bool TMA_A = false;
+    static constexpr bool REG_RING = true;
+    struct Unit {
+        uint4 v[4];
+    };
+    using State = ConvState;
+
+    template <int DD>
+    __device__ static void load(const Params &p, State &st, const uint4 *, int j, bool valid, int sub,
+                                int rbase, Unit &u)
+    {
+        if (!valid) return;
+        conv_cursor<GROUP_ELEMS, STEP_ELEMS>(p, st, j, sub, rbase);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (st.img[q] >= 0 && st.fh < p.FH) {
+                const int ih = st.ih0[q] + st.fh;
+                const int iw = st.iw0[q] + st.fw;
+                if (ih < 0 || ih >= p.H || iw < 0 || iw >= p.W) {
+                    v = make_uint4(p.pad_word, p.pad_word, p.pad_word, p.pad_word);
+                } else {
+                    const int64_t elem = ((int64_t)(st.img[q] + ih) * p.W + iw) * p.Cin + st.c0;
+                    v = ldg_nc_v4(p.A + (ELEM_BITS == 4 ? elem / 2 : elem));
+                }
+            }
+            u.v[q] = v;
+        }
+    }
+
+    template <int DD>
+    __device__ static void wait_unit() {}
+
+    __device__ static uint4 fetched(const Params &, const ConvState &, const uint4 *, int, int q, const Unit &u)
+    {
+        return u.v[q];
+    }
+};
+
+// D = 0: register ring; D > 0: shared-memory staging ring of D units.
+template <int ELEM_BITS, int GROUP_ELEMS, int STEP_ELEMS, int D>
+using ConvFetch = typename std::conditional<D == 0, ConvRegRing<ELEM_BITS, GROUP_ELEMS, STEP_ELEMS>,
+                                            ConvStaging<ELEM_BITS, GROUP_ELEMS, STEP_ELEMS, D>>::type;
+
 template <int D>
-struct ConvU4Op : ConvStaging<4, 32, 128, D> {
-    using Base = ConvStaging<4, 32, 128, D>;
+struct ConvU4Op : ConvFetch<4, 32, 128, D> {
+    using Base = ConvFetch<4, 32, 128, D>;
     static constexpr bool F8 = true;
     static constexpr int SCALE_LOG2 = 9;
 
     template <int DD>
     __device__ static void store(const Params &p, ConvState &st, const uint4 *stg, uint32_t a_stage, int j,
-                                 int sub, int rbase, const typename Base::Unit &)
+                                 int sub, int rbase, const typename Base::Unit &u)
     {
-        cp_async_wait<DD - 1>();
+        Base::template wait_unit<DD>();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int row = q * 32 + rbase;
-            const uint4 v = Base::fetched(p, st, stg, j % DD, q);
+            const uint4 v = Base::fetched(p, st, stg, j % DD, q, u);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint32_t b[8];
 #pragma unroll
@@ -184,20 +243,20 @@ struct ConvU4Op : ConvStaging<4, 32, 128, D> {
 };
 
 template <int D>
-struct ConvU8Op : ConvStaging<8, 16, 64, D> {
-    using Base = ConvStaging<8, 16, 64, D>;
+struct ConvU8Op : ConvFetch<8, 16, 64, D> {
+    using Base = ConvFetch<8, 16, 64, D>;
     static constexpr bool F8 = false;
     static constexpr int SCALE_LOG2 = 0;
 
     template <int DD>
     __device__ static void store(const Params &p, ConvState &st, const uint4 *stg, uint32_t a_stage, int j,
-                                 int sub, int rbase, const typename Base::Unit &)
+                                 int sub, int rbase, const typename Base::Unit &u)
     {
-        cp_async_wait<DD - 1>();
+        Base::template wait_unit<DD>();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int row = q * 32 + rbase;
-            const uint4 v = Base::fetched(p, st, stg, j % DD, q);
+            const uint4 v = Base::fetched(p, st, stg, j % DD, q, u);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint32_t h[8];
 #pragma unroll
@@ -291,14 +350,11 @@ inline size_t packed_w_u4_bytes(const qnn_conv_geom *g)
 template <template <int> class Op, int TBN>
 qnn_status conv_launch(const Params &p, cudaStream_t s)
 {
-    if constexpr (!Op<8>::F8) {
+    if constexpr (!Op<0>::F8) {
         // K cut into exact chunks: int32 chunk sums of 64 columns per thread
-        if (p.nchunks > 1) return launch<Op<8>, 128, true>(p, s);
+        if (p.nchunks > 1) return launch<Op<0>, 128, true>(p, s);
     }
-    if constexpr (TBN == 256)
-        return launch<Op<2>, 256, false>(p, s);
-    else
-        return launch<Op<8>, TBN, false>(p, s);
+    return launch<Op<0>, TBN, false>(p, s);
 }
 
 template <template <int> class Op>

@@ -16,7 +16,12 @@
 // chunk results in int32.  A u8 operand is read as (q - 128) so that every
 // operand is in [-128, 127]; the fold puts the 128 back through zp_term.
 // The kernel itself is qnn_mma_kernel.cuh; this file holds the converter of
-// the A rows and the host entry point.
+// the A rows, the A pre-pass and the host entry point.
+//
+// With a workspace, A is re-encoded once by a memory-bound pre-pass into the
+// fp16 operand image (the same swizzled layout as the weights) and the GEMM
+// kernel streams both operands with bulk copies; without one, converter warps
+// re-encode A inside the GEMM kernel for every output-column tile.
 #include "qnn_mma_kernel.cuh"
 
 namespace qnn {
@@ -43,6 +48,7 @@ __device__ __forceinline__ void bytes_to_half(uint4 v, uint32_t flip, uint32_t (
 
 template <bool PTF>
 struct GemmOp {
+    static constexpr bool TMA_A = false;
     static constexpr bool F8 = false;
     static constexpr int SCALE_LOG2 = 0;
     static constexpr int DEPTH = 4;        // units of A rows in flight, in registers
@@ -108,14 +114,84 @@ struct GemmOp {
     }
 };
 
+// A operand already in the fp16 image: the producer copies it.
+struct GemmPackedOp {
+    static constexpr bool TMA_A = true;
+    static constexpr bool F8 = false;
+    static constexpr int SCALE_LOG2 = 0;
+    static constexpr int STG_BYTES = 16;
+};
+
+// Pre-pass: A [M, K] (s8, or u8 read as q - 128; times 2^alpha_k with PTF)
+// -> fp16 image [num_m][KT][128 rows][128 B], chunk c of row r at chunk
+// c ^ (r % 8), zero beyond M and K.  A thread converts 16 codes (two chunks):
+// threadIdx.x walks the 16-code groups of a row (coalesced 16-byte reads; four
+// consecutive threads fill one 128-byte image row), threadIdx.y and the grid's
+// y dimension walk the rows.  All index arithmetic is 32-bit.
+template <bool PTF>
+__global__ void __launch_bounds__(256) pack_a_kernel(const uint8_t *__restrict__ A, int M, int K, int KT,
+                                                     int rows_pad, int a_u8, const uint8_t *__restrict__ ptf,
+                                                     uint8_t *__restrict__ out)
+{
+    const int groups = KT * 4;  // 16-code groups per padded row
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= groups) return;
+    const int k0 = g * 16;
+    const uint32_t flip = a_u8 ? 0u : 0x80808080u;
+    uint32_t mul[8];
+    if (PTF) {
+        const uint4 al = (k0 < K) ? ldg_nc_v4(ptf + k0) : make_uint4(0, 0, 0, 0);
+        const uint32_t a4[4] = {al.x, al.y, al.z, al.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            mul[2 * j] = pow2_half2(a4[j], 0x4140u);
+            mul[2 * j + 1] = pow2_half2(a4[j], 0x4342u);
+        }
+    }
+    const int ks = g >> 2;
+    const int c = (g & 3) * 2;
+    for (int m = blockIdx.y * blockDim.y + threadIdx.y; m < rows_pad; m += gridDim.y * blockDim.y) {
+        uint32_t h[8];
+        if (m < M && k0 < K) {
+            bytes_to_half(ldg_nc_v4(A + (size_t)m * (size_t)K + k0), flip, h);
+            if (PTF) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) h[j] = hmul2_u32(h[j], mul[j]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) h[j] = 0;
+        }
+        const int r = m & (BM - 1);
+        uint8_t *row = out + ((size_t)((m / BM) * KT + ks) * BM + r) * ROW_BYTES;
+        *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(row + (((c + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+}
+
+inline size_t packed_a_bytes(int M, int K)
+{
+    return (size_t)((M + BM - 1) / BM) * (size_t)qnn::gemm::ksteps(K) * (size_t)A_STAGE_BYTES;
+}
+
 }  // namespace mk
 }  // namespace qnn
 
-extern "C" qnn_status qgemm_s8(const void *A, qnn_dtype a_dt, const void *B_packed, int M, int N,
-                               int K, const qnn_epilogue *e, void *C, int32_t *C_s32,
-                               qnn_stream_t stream)
+extern "C" size_t qnn_gemm_workspace_bytes(int M, int K)
 {
-    using namespace qnn::mk;
+    if (M <= 0 || K <= 0) return 0;
+    return qnn::mk::packed_a_bytes(M, K);
+}
+
+namespace qnn {
+namespace mk {
+
+// Validation and Params shared by the three GEMM entry points.  A may be the
+// codes (fused path) or the packed image (A_is_packed); the epilogue's PTF
+// fields decide the exact-chunk length either way.
+static qnn_status gemm_params(const void *A, qnn_dtype a_dt, const void *B_packed, int M, int N, int K,
+                              const qnn_epilogue *e, void *C, int32_t *C_s32, Params &p)
+{
     if (!A || !B_packed || !e || !C) return QNN_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0) return QNN_ERR_INVALID_ARG;
     if (a_dt != QNN_S8 && a_dt != QNN_U8) return QNN_ERR_UNSUPPORTED;
@@ -124,7 +200,7 @@ extern "C" qnn_status qgemm_s8(const void *A, qnn_dtype a_dt, const void *B_pack
         return QNN_ERR_ALIGNMENT;
     if ((reinterpret_cast<uintptr_t>(B_packed) & 1023u) != 0) return QNN_ERR_ALIGNMENT;
 
-    Params p{};
+    p = Params{};
     p.A = static_cast<const uint8_t *>(A);
     p.a_u8 = (a_dt == QNN_U8);
     p.Bp = static_cast<const uint8_t *>(B_packed);
@@ -151,15 +227,96 @@ extern "C" qnn_status qgemm_s8(const void *A, qnn_dtype a_dt, const void *B_pack
     if ((int64_t)K * 255 * 128 * (1 << shift) > (int64_t)INT32_MAX) return QNN_ERR_OVERFLOW_RISK;
     p.chunk_steps = qnn::gemm::MAX_EXACT_STEPS >> shift;
     p.nchunks = (p.KT + p.chunk_steps - 1) / p.chunk_steps;
+    return QNN_OK;
+}
 
+static qnn_status launch_pack_a(const uint8_t *A, int M, int K, int a_u8, const uint8_t *ptf, uint8_t *out,
+                                cudaStream_t s)
+{
+    const int KT = qnn::gemm::ksteps(K);
+    const int rows_pad = ((M + BM - 1) / BM) * BM;
+    const int groups = KT * 4;
+    // 256 threads: up to 64 groups of a row x 4 (or more) rows
+    const int bx = groups >= 64 ? 64 : groups;
+    const int by = 256 / bx;
+    const dim3 block(bx, by);
+    const int gx = (groups + bx - 1) / bx;
+    int gy = (rows_pad + by - 1) / by;
+    const int want = qnn::sm_count() * 32;  // enough blocks in flight; rows loop beyond
+    if (gy > 65535) gy = 65535;
+    if ((int64_t)gx * gy > want && gy > 1) {
+        gy = (want + gx - 1) / gx;
+        if (gy < 1) gy = 1;
+    }
+    const dim3 grid(gx, gy);
+    if (ptf)
+        pack_a_kernel<true><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, ptf, out);
+    else
+        pack_a_kernel<false><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, nullptr, out);
+    return qnn::launch_status();
+}
+
+static qnn_status launch_gemm(Params &p, bool packed, cudaStream_t s)
+{
     p.status = qnn::status_word();
     if (!p.status) return QNN_ERR_CUDA;
-    cudaStream_t s = (cudaStream_t)stream;
     const bool multi = p.nchunks > 1;
+    if (packed) {
+        p.Ap = p.A;
+        if (!multi) return launch<GemmPackedOp, 256, false>(p, s);
+        return launch<GemmPackedOp, 128, true>(p, s);
+    }
     if (!p.ptf) {
         if (!multi) return launch<GemmOp<false>, 256, false>(p, s);
         return launch<GemmOp<false>, 128, true>(p, s);
     }
     if (!multi) return launch<GemmOp<true>, 256, false>(p, s);
     return launch<GemmOp<true>, 128, true>(p, s);
+}
+
+}  // namespace mk
+}  // namespace qnn
+
+extern "C" qnn_status qgemm_pack_a(const void *A, qnn_dtype a_dt, int M, int K, const uint8_t *ptf_shift,
+                                   void *A_packed, size_t A_packed_bytes, qnn_stream_t stream)
+{
+    using namespace qnn::mk;
+    if (!A || !A_packed || M <= 0 || K <= 0) return QNN_ERR_INVALID_ARG;
+    if (a_dt != QNN_S8 && a_dt != QNN_U8) return QNN_ERR_UNSUPPORTED;
+    if (ptf_shift && a_dt != QNN_S8) return QNN_ERR_UNSUPPORTED;
+    if (K % 16 != 0) return QNN_ERR_ALIGNMENT;
+    if (!qnn::aligned16(A) || !qnn::aligned16(A_packed) || (ptf_shift && !qnn::aligned16(ptf_shift)))
+        return QNN_ERR_ALIGNMENT;
+    if (A_packed_bytes < packed_a_bytes(M, K)) return QNN_ERR_INVALID_ARG;
+    return launch_pack_a(static_cast<const uint8_t *>(A), M, K, a_dt == QNN_U8, ptf_shift,
+                         static_cast<uint8_t *>(A_packed), (cudaStream_t)stream);
+}
+
+extern "C" qnn_status qgemm_s8_packed(const void *A_packed, qnn_dtype a_dt, const void *B_packed, int M,
+                                      int N, int K, const qnn_epilogue *e, void *C, int32_t *C_s32,
+                                      qnn_stream_t stream)
+{
+    using namespace qnn::mk;
+    Params p;
+    const qnn_status st = gemm_params(A_packed, a_dt, B_packed, M, N, K, e, C, C_s32, p);
+    if (st != QNN_OK) return st;
+    return launch_gemm(p, true, (cudaStream_t)stream);
+}
+
+extern "C" qnn_status qgemm_s8(const void *A, qnn_dtype a_dt, const void *B_packed, int M, int N,
+                               int K, const qnn_epilogue *e, void *C, int32_t *C_s32,
+                               void *workspace, size_t workspace_bytes, qnn_stream_t stream)
+{
+    using namespace qnn::mk;
+    Params p;
+    qnn_status st = gemm_params(A, a_dt, B_packed, M, N, K, e, C, C_s32, p);
+    if (st != QNN_OK) return st;
+    if (!workspace) return launch_gemm(p, false, (cudaStream_t)stream);
+    if (workspace_bytes < packed_a_bytes(M, K)) return QNN_ERR_INVALID_ARG;
+    if (!qnn::aligned16(workspace)) return QNN_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    st = launch_pack_a(p.A, M, K, p.a_u8, p.ptf, static_cast<uint8_t *>(workspace), s);
+    if (st != QNN_OK) return st;
+    p.A = static_cast<const uint8_t *>(workspace);
+    return launch_gemm(p, true, s);
 }

@@ -12,13 +12,17 @@
 //   ConvU8Op     : im2col of u8 NHWC      -> fp16 (kind::f16)
 //   ConvU4Op     : im2col of u4 NHWC      -> e4m3 codes of c / 512 (kind::f8f6f4)
 //
+//   GemmPackedOp : A already re-encoded (fp16, swizzled) by a pre-pass; the
+//                  producer copies it like the weights (no converter warps)
+//
 // Warp roles (512 threads, one CTA per SM, persistent over 128 x TBN tiles):
 //   warps 0-3  : converters -- fetch the activation rows of one pipeline unit
 //                (128 rows x one K step) from global memory, one unit ahead,
 //                re-encode them and store them into the 128-byte swizzled
-//                K-major stage buffer.
+//                K-major stage buffer.  Idle for Ops with a prepacked A.
 //   warp 4     : TMA producer -- one bulk copy per stage of the prepacked
-//                weight tile (already in the swizzled image).
+//                weight tile (already in the swizzled image), and one of the
+//                prepacked activation tile for Ops with TMA_A.
 //   warp 5     : TMEM owner and MMA issuer -- 4 x tcgen05.mma per stage into
 //                one of two TBN-column fp32 TMEM accumulators.
 //   warps 8-15 : epilogue -- tcgen05.ld, fp32 -> int32 (exact), optional
@@ -53,6 +57,7 @@ struct Params {
     const uint8_t *A;
     int a_u8;                // GEMM: 1 if A holds u8 codes (centred at 128), 0 for s8
     const uint8_t *ptf;      // GEMM: per-K Power-of-Two Factor shifts, or null
+    const uint8_t *Ap;       // prepacked activation image [num_m][KT][128 rows][128 B] (TMA_A Ops)
     // convolution geometry (NHWC input, OHWI weights, K order (fh, fw, c))
     int H, W, Cin, OHW, OW, FH, FW, ph, pw, sh, sw;
     uint32_t pad_word;       // input bytes that stand for the padding value z_in
@@ -84,7 +89,7 @@ struct __align__(1024) Smem {
     uint8_t b[STAGES][TBN * ROW_BYTES];
     uint4 stg[Op::STG_BYTES / 16];                   // converter staging ring (Op-specific)
     float cols[NUM_EPI_WARPS][4 * (TBN / 2)];        // per epilogue warp: its columns' constants
-    uint64_t full[STAGES];   // 4 converter-warp arrivals + the producer's expect_tx arrival
+    uint64_t full[STAGES];   // 4 converter-warp arrivals (none with TMA_A) + the producer's expect_tx
     uint64_t empty[STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
@@ -249,7 +254,13 @@ __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
             const uint8_t *src = p.Bp + ((int64_t)(n0 / gemm::BN) * p.KT + c.ks) * gemm::B_STAGE_BYTES +
                                  (int64_t)(n0 % gemm::BN) * ROW_BYTES;
             const uint32_t bar = smem_u32(&s.full[stage]);
-            mbar_arrive_expect_tx(bar, TBN * ROW_BYTES);
+            if constexpr (Op::TMA_A) {
+                mbar_arrive_expect_tx(bar, TBN * ROW_BYTES + A_STAGE_BYTES);
+                bulk_g2s(smem_u32(&s.a[stage][0]), p.Ap + ((int64_t)c.mb * p.KT + c.ks) * A_STAGE_BYTES,
+                         A_STAGE_BYTES, bar);
+            } else {
+                mbar_arrive_expect_tx(bar, TBN * ROW_BYTES);
+            }
             bulk_g2s(b0 + stage * (TBN * ROW_BYTES), src, TBN * ROW_BYTES, bar);
         }
         ready = __all_sync(0xffffffffu, probe) && jn < units;
@@ -718,7 +729,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(smem_u32(&s.full[i]), 5);
+            mbar_init(smem_u32(&s.full[i]), Op::TMA_A ? 1 : 5);
             mbar_init(smem_u32(&s.empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -741,15 +752,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
         (blockIdx.x < p.num_tiles) ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int units = my_tiles * p.KT;
 
-    // register split of the multi-chunk kernel: 128*128 + 128*56 + 256*160 = 64512 <= 65536
+    // Register split per warpgroup (launched with 128 per thread, 65536 in all):
+    // converters keep 128 (or drop to 24 when A arrives by copy), the
+    // producer / MMA warpgroup drops to 96, and the epilogue warpgroups take
+    // the rest -- 128*128 + 128*96 + 256*144 = 65536 or 128*24 + 128*96 +
+    // 256*192 = 64512.
+    constexpr uint32_t REGS_WG1 = 96;
+    constexpr uint32_t REGS_WG0 = Op::TMA_A ? 24 : 128;
+    constexpr uint32_t REGS_EPI = ((65536u - 128u * REGS_WG0 - 128u * REGS_WG1) / 256u) & ~7u;
+    static_assert(128u * REGS_WG0 + 128u * REGS_WG1 + 256u * REGS_EPI <= 65536u, "register split");
     if (warp < 4) {
-        converter_role<Op, TBN, MULTI>(p, s, units);
+        if constexpr (Op::TMA_A) regs_dec<REGS_WG0>();
+        else converter_role<Op, TBN, MULTI>(p, s, units);
     } else if (warp < 8) {
-        if (MULTI) regs_dec<56>();
+        regs_dec<REGS_WG1>();
         if (warp == PRODUCER_WARP) producer_role<Op, TBN>(p, s, units);
         if (warp == MMA_WARP) mma_role<Op, TBN>(p, s, my_tiles, tmem);
     } else {
-        if (MULTI) regs_inc<160>();
+        regs_inc<REGS_EPI>();
         epilogue_role<Op, TBN, MULTI>(p, s, my_tiles, tmem);
     }
 

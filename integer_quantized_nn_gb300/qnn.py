@@ -71,7 +71,10 @@ def _declare(L):
         "qnn_gemm_packed_b_bytes": (sz, [c_int, c_int]),
         "qgemm_prepack_b": (c_int, [vp, c_int, c_int, vp, vp, vp]),
         "q_fold_epilogue": (c_int, [c_int, c_int, i32, vp, f32, vp, c_int, vp, f32, vp, vp, vp, vp, vp]),
-        "qgemm_s8": (c_int, [vp, c_int, vp, c_int, c_int, c_int, vp, vp, vp, vp]),
+        "qnn_gemm_workspace_bytes": (sz, [c_int, c_int]),
+        "qgemm_s8": (c_int, [vp, c_int, vp, c_int, c_int, c_int, vp, vp, vp, vp, sz, vp]),
+        "qgemm_pack_a": (c_int, [vp, c_int, c_int, c_int, vp, vp, sz, vp]),
+        "qgemm_s8_packed": (c_int, [vp, c_int, vp, c_int, c_int, c_int, vp, vp, vp, vp]),
         "qnn_conv_packed_w_bytes": (sz, [vp, c_int]),
         "qconv_prepack_w": (c_int, [vp, c_int, vp, vp, vp, vp]),
         "qconv_u4s4": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
@@ -121,6 +124,10 @@ def _ptr(t) -> Optional[int]:
     if t is None:
         return None
     return int(t.data_ptr())
+
+
+def _nbytes(t) -> int:
+    return int(t.numel()) * int(t.element_size())
 
 
 def _stream(stream) -> Optional[int]:
@@ -188,12 +195,38 @@ def epilogue(mode="requant", relu=False, out_dt="s8", z_out=0, zp_term=None, M=N
                     float(R), _ptr(ptf_shift), int(ptf_max_shift))
 
 
-def qgemm_s8(A, a_dt: str, B_packed, M: int, N: int, K: int, epi: Epilogue, C, C_s32=None,
-             stream=None):
+def qnn_gemm_workspace_bytes(M: int, K: int) -> int:
     load()
+    return int(_SYMBOLS["qnn_gemm_workspace_bytes"](int(M), int(K)))
+
+
+def qgemm_s8(A, a_dt: str, B_packed, M: int, N: int, K: int, epi: Epilogue, C, C_s32=None,
+             workspace=None, stream=None):
+    """workspace: optional uint8 device tensor of at least
+    qnn_gemm_workspace_bytes(M, K) bytes (the pre-pass path); None: no scratch."""
+    load()
+    ws_bytes = 0 if workspace is None else _nbytes(workspace)
     _check(_SYMBOLS["qgemm_s8"](_ptr(A), DTYPES[a_dt], _ptr(B_packed), int(M), int(N), int(K),
-                                ctypes.byref(epi), _ptr(C), _ptr(C_s32), _stream(stream)),
+                                ctypes.byref(epi), _ptr(C), _ptr(C_s32), _ptr(workspace),
+                                ctypes.c_size_t(ws_bytes), _stream(stream)),
            "qgemm_s8")
+
+
+def qgemm_pack_a(A, a_dt: str, M: int, K: int, A_packed, ptf_shift=None, stream=None):
+    """Re-encodes A into A_packed (uint8 device tensor of at least
+    qnn_gemm_workspace_bytes(M, K) bytes) for qgemm_s8_packed."""
+    load()
+    _check(_SYMBOLS["qgemm_pack_a"](_ptr(A), DTYPES[a_dt], int(M), int(K), _ptr(ptf_shift),
+                                    _ptr(A_packed), ctypes.c_size_t(_nbytes(A_packed)),
+                                    _stream(stream)), "qgemm_pack_a")
+
+
+def qgemm_s8_packed(A_packed, a_dt: str, B_packed, M: int, N: int, K: int, epi: Epilogue, C,
+                    C_s32=None, stream=None):
+    load()
+    _check(_SYMBOLS["qgemm_s8_packed"](_ptr(A_packed), DTYPES[a_dt], _ptr(B_packed), int(M), int(N),
+                                       int(K), ctypes.byref(epi), _ptr(C), _ptr(C_s32),
+                                       _stream(stream)), "qgemm_s8_packed")
 
 
 def conv_geom(N, H, W, C, OC, FH, FW, pad=(1, 1), stride=(1, 1)) -> ConvGeom:

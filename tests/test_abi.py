@@ -28,6 +28,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("q_quantize", "q_dequantize", "qgemm_prepack_b", "q_fold_epilogue", "qgemm_s8",
+              "qnn_gemm_workspace_bytes", "qgemm_pack_a", "qgemm_s8_packed",
               "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_status_string",
               "qnn_check_device_error"):
         assert n in names
@@ -56,11 +57,29 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert L.q_dequantize(16, 0, 16, 2, shape, ctypes.byref(p), None) == qnn.QNN_ERR_INVALID_ARG
     epi = qnn.epilogue("requant")
     # unsupported activation type, zero sizes
-    assert L.qgemm_s8(16, 2, 1024, 4, 8, 16, ctypes.byref(epi), 16, None, None) == qnn.QNN_ERR_UNSUPPORTED
-    assert L.qgemm_s8(16, 0, 1024, 0, 8, 16, ctypes.byref(epi), 16, None, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.qgemm_s8(16, 2, 1024, 4, 8, 16, ctypes.byref(epi), 16, None, None, 0, None) == qnn.QNN_ERR_UNSUPPORTED
+    assert L.qgemm_s8(16, 0, 1024, 0, 8, 16, ctypes.byref(epi), 16, None, None, 0, None) == qnn.QNN_ERR_INVALID_ARG
     # K not a multiple of 16, misaligned weights
-    assert L.qgemm_s8(16, 0, 1024, 4, 8, 24, ctypes.byref(epi), 16, None, None) == qnn.QNN_ERR_ALIGNMENT
-    assert L.qgemm_s8(16, 0, 1040, 4, 8, 32, ctypes.byref(epi), 16, None, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.qgemm_s8(16, 0, 1024, 4, 8, 24, ctypes.byref(epi), 16, None, None, 0, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.qgemm_s8(16, 0, 1040, 4, 8, 32, ctypes.byref(epi), 16, None, None, 0, None) == qnn.QNN_ERR_ALIGNMENT
+    # workspace smaller than qnn_gemm_workspace_bytes, or misaligned
+    need = L.qnn_gemm_workspace_bytes(4, 32)
+    assert need == 16384
+    assert L.qnn_gemm_workspace_bytes(129, 65) == 2 * 2 * 16384
+    assert L.qnn_gemm_workspace_bytes(0, 64) == 0
+    ok_epi = qnn.epilogue("requant")
+    ok_epi.M, ok_epi.Bq = 256, 512  # never dereferenced on the host
+    assert L.qgemm_s8(16, 0, 1024, 4, 8, 32, ctypes.byref(ok_epi), 16, None, 4096, need - 1,
+                      None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.qgemm_s8(16, 0, 1024, 4, 8, 32, ctypes.byref(ok_epi), 16, None, 4104, need,
+                      None) == qnn.QNN_ERR_ALIGNMENT
+    # the two-call form validates the same way
+    assert L.qgemm_pack_a(16, 0, 4, 32, None, 4096, need - 1, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.qgemm_pack_a(16, 0, 4, 24, None, 4096, need, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.qgemm_pack_a(16, 1, 4, 32, 4096, 4096, need, None) == qnn.QNN_ERR_UNSUPPORTED
+    assert L.qgemm_pack_a(None, 0, 4, 32, None, 4096, need, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.qgemm_s8_packed(4096, 0, 1040, 4, 8, 32, ctypes.byref(ok_epi), 16, None,
+                             None) == qnn.QNN_ERR_ALIGNMENT
     assert L.qgemm_prepack_b(16, 8, 24, 1024, None, None) == qnn.QNN_ERR_ALIGNMENT
     assert L.q_fold_epilogue(0, 0, 0, None, 1.0, None, 0, None, 1.0, None, None, None, None,
                              None) == qnn.QNN_ERR_INVALID_ARG

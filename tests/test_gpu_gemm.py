@@ -42,32 +42,48 @@ def _run(oracle, A, a_dt, B, z_a, s_a, s_w, s_o, bias=None, mode="requant", out_
                        D=g["D"], bias=g["bias"], residual=resd, res_dt=res_dt, z_res=z_res,
                        R=0.0 if R is None else float(R), ptf_shift=al, ptf_max_shift=maxs)
     cdt = {"requant": t.uint8, "dequant": t.float32, "s32": t.int32}[mode]
-    C = t.full((M, N), 0x5A if mode == "requant" else 7, dtype=cdt, device="cuda")
-    C32 = t.zeros((M, N), dtype=t.int32, device="cuda") if want_s32 else None
-    qnn.qgemm_s8(Ad, a_dt, g["Bp"], M, N, K, epi, C, C32)
-    assert qnn.qnn_check_device_error() == qnn.QNN_OK
+    outs = {}
+    # every path: A re-encoded inside the GEMM (no workspace), by the pre-pass
+    # into a workspace (pre-filled with NaN fp16 bit patterns), and the same
+    # as two calls (qgemm_pack_a, qgemm_s8_packed)
+    for path in ("fused", "workspace", "packed"):
+        C = t.full((M, N), 0x5A if mode == "requant" else 7, dtype=cdt, device="cuda")
+        C32 = t.zeros((M, N), dtype=t.int32, device="cuda") if want_s32 else None
+        ws = None
+        if path != "fused":
+            ws = t.full((qnn.qnn_gemm_workspace_bytes(M, K),), 0xFF, dtype=t.uint8, device="cuda")
+        if path == "packed":
+            qnn.qgemm_pack_a(Ad, a_dt, M, K, ws, ptf_shift=al)
+            qnn.qgemm_s8_packed(ws, a_dt, g["Bp"], M, N, K, epi, C, C32)
+        else:
+            qnn.qgemm_s8(Ad, a_dt, g["Bp"], M, N, K, epi, C, C32, workspace=ws)
+        assert qnn.qnn_check_device_error() == qnn.QNN_OK
+        outs[path] = (C, C32)
 
     sel = np.arange(M) if rows is None else rows
     A_i = A[sel].astype(np.int32)
     acc = oracle.gemm_acc(A_i, B.astype(np.int32), 0 if alpha is not None else z_a,
                           None if alpha is None else alpha.astype(np.int32))
-    if want_s32:
-        got32 = host(C32)[sel]
-        assert np.array_equal(got32, acc), f"{(got32 != acc).sum()} accumulator mismatches"
-    Cg = host(C)[sel]
-    if mode == "s32":
-        assert np.array_equal(Cg, acc)
-    elif mode == "dequant":
-        y = oracle.dequant_epilogue(acc, D_o, bias)
-        assert np.array_equal(f32_bits(Cg), f32_bits(y))
-    else:
+    if mode == "requant":
         res_codes = None
         if res is not None:
             res_codes = res[sel].astype(np.int8 if res_dt == "s8" else np.uint8).astype(np.int32)
         q = oracle.requant(acc, M_o, Bq_o, out_dt, relu=relu, res=res_codes, z_res=z_res,
                            R=0.0 if R is None else R, z_out=z_out)
         exp = oracle.pack_bytes(q)
-        assert np.array_equal(Cg, exp), f"{(Cg != exp).sum()} output mismatches"
+    elif mode == "dequant":
+        y = oracle.dequant_epilogue(acc, D_o, bias)
+    for path, (C, C32) in outs.items():
+        if want_s32:
+            got32 = host(C32)[sel]
+            assert np.array_equal(got32, acc), f"{path}: {(got32 != acc).sum()} accumulator mismatches"
+        Cg = host(C)[sel]
+        if mode == "s32":
+            assert np.array_equal(Cg, acc), path
+        elif mode == "dequant":
+            assert np.array_equal(f32_bits(Cg), f32_bits(y)), path
+        else:
+            assert np.array_equal(Cg, exp), f"{path}: {(Cg != exp).sum()} output mismatches"
     return acc
 
 
@@ -218,7 +234,10 @@ def test_gemm_square_16384_sampled(oracle):
     Mv = t.full((n,), 2.0 ** -e, dtype=t.float32, device="cuda")
     Bq = t.zeros(n, dtype=t.float32, device="cuda")
     C = t.empty((n, n), dtype=t.uint8, device="cuda")
+    C2 = t.empty((n, n), dtype=t.uint8, device="cuda")
     qnn.qgemm_s8(A, "s8", Bp, n, n, n, qnn.epilogue("requant", M=Mv, Bq=Bq), C)
+    ws = t.empty(qnn.qnn_gemm_workspace_bytes(n, n), dtype=t.uint8, device="cuda")
+    qnn.qgemm_s8(A, "s8", Bp, n, n, n, qnn.epilogue("requant", M=Mv, Bq=Bq), C2, workspace=ws)
     assert qnn.qnn_check_device_error() == qnn.QNN_OK
     rows = np.sort(np.random.default_rng(18).choice(n, 48, replace=False))
     Ah = host(A[rows]).astype(np.int32)
@@ -226,6 +245,7 @@ def test_gemm_square_16384_sampled(oracle):
     acc = oracle.gemm_acc(Ah, Bh)
     q = oracle.requant(acc, np.full(n, 2.0 ** -e, np.float32), np.zeros(n, np.float32), "s8")
     assert np.array_equal(host(C[rows]), oracle.pack_bytes(q))
+    assert np.array_equal(host(C2[rows]), oracle.pack_bytes(q))
 
 
 def test_gemm_errors():
