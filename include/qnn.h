@@ -186,6 +186,29 @@ qnn_status qgemm_s8_packed(const void *A_packed, qnn_dtype a_dt, const void *B_p
                            int K, const qnn_epilogue *epi, void *C, int32_t *C_s32,
                            qnn_stream_t stream);
 
+/* Size of the library's fixed device scratch for qgemm_s8_static_scratch:
+ * 32 MiB, enough for qnn_gemm_workspace_bytes(M, K) of any M x K activation
+ * with ceil(M / 128) * ceil(K / 64) <= 2048 (e.g. 12608 x 1024). */
+#define QNN_GEMM_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* qgemm_s8 with a workspace, for callers that cannot allocate device memory at
+ * call time (allocation is not allowed in their execution context, or their
+ * allocator is not reachable from it).  The workspace is a fixed array of
+ * QNN_GEMM_STATIC_SCRATCH_BYTES that belongs to the library (allocated when
+ * the library's device code is loaded); the call allocates and frees nothing.
+ * The pages describe no such variant; it exists only for those callers.
+ * - The array's address is looked up once per device on the first call; make
+ *   that first call on each device before capturing a stream.
+ * - Returns QNN_ERR_UNSUPPORTED when qnn_gemm_workspace_bytes(M, K) exceeds
+ *   QNN_GEMM_STATIC_SCRATCH_BYTES; other arguments as for qgemm_s8.
+ * - Every call on a device uses the same array: calls whose executions
+ *   overlap (different streams, or other host threads) race on it and give
+ *   wrong results.  Order them on one stream or with events.
+ * Results are identical to qgemm_s8's. */
+qnn_status qgemm_s8_static_scratch(const void *A, qnn_dtype a_dt, const void *B_packed, int M, int N,
+                                   int K, const qnn_epilogue *epi, void *C, int32_t *C_s32,
+                                   qnn_stream_t stream);
+
 /* ---- implicit-GEMM convolution -------------------------------------------- */
 
 /* NHWC input [N, H, W, C], OHWI weights [OC, FH, FW, C], NHWC output

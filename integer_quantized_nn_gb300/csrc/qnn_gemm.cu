@@ -22,6 +22,7 @@
 // fp16 operand image (the same swizzled layout as the weights) and the GEMM
 // kernel streams both operands with bulk copies; without one, converter warps
 // re-encode A inside the GEMM kernel for every output-column tile.
+#include <atomic>
 #include "qnn_mma_kernel.cuh"
 
 namespace qnn {
@@ -276,6 +277,60 @@ static qnn_status launch_gemm(Params &p, bool packed, cudaStream_t s)
 
 }  // namespace mk
 }  // namespace qnn
+
+// ---- fixed scratch variant ---------------------------------------------------
+// For callers that must not allocate device memory at call time (allocation
+// is not allowed inside their execution context, or their allocator is not
+// reachable from it): the re-encoded A lives in one file-scope device array
+// of QNN_GEMM_STATIC_SCRATCH_BYTES, allocated with the module.
+namespace qnn {
+namespace mk {
+
+static __device__ __align__(256) uint8_t g_gemm_scratch[QNN_GEMM_STATIC_SCRATCH_BYTES];
+
+constexpr int kScratchDevices = 64;
+static std::atomic<uintptr_t> g_scratch_addr[kScratchDevices];
+
+// Device address of the scratch array on the current device, looked up once
+// per device; nullptr if the lookup failed.
+static uint8_t *static_scratch()
+{
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kScratchDevices) return nullptr;
+    uintptr_t a = g_scratch_addr[d].load(std::memory_order_acquire);
+    if (a == 0) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_gemm_scratch) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        a = reinterpret_cast<uintptr_t>(ptr);
+        g_scratch_addr[d].store(a, std::memory_order_release);
+    }
+    return reinterpret_cast<uint8_t *>(a);
+}
+
+}  // namespace mk
+}  // namespace qnn
+
+extern "C" qnn_status qgemm_s8_static_scratch(const void *A, qnn_dtype a_dt, const void *B_packed, int M,
+                                              int N, int K, const qnn_epilogue *e, void *C, int32_t *C_s32,
+                                              qnn_stream_t stream)
+{
+    using namespace qnn::mk;
+    Params p;
+    qnn_status st = gemm_params(A, a_dt, B_packed, M, N, K, e, C, C_s32, p);
+    if (st != QNN_OK) return st;
+    if (packed_a_bytes(M, K) > (size_t)QNN_GEMM_STATIC_SCRATCH_BYTES) return QNN_ERR_UNSUPPORTED;
+    uint8_t *ws = static_scratch();
+    if (!ws) return QNN_ERR_CUDA;
+    // nothing has to start at zero: the pre-pass writes every byte the GEMM reads
+    cudaStream_t s = (cudaStream_t)stream;
+    st = launch_pack_a(p.A, M, K, p.a_u8, p.ptf, ws, s);
+    if (st != QNN_OK) return st;
+    p.A = ws;
+    return launch_gemm(p, true, s);
+}
 
 extern "C" qnn_status qgemm_pack_a(const void *A, qnn_dtype a_dt, int M, int K, const uint8_t *ptf_shift,
                                    void *A_packed, size_t A_packed_bytes, qnn_stream_t stream)

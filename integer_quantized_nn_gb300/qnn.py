@@ -75,6 +75,7 @@ def _declare(L):
         "qgemm_s8": (c_int, [vp, c_int, vp, c_int, c_int, c_int, vp, vp, vp, vp, sz, vp]),
         "qgemm_pack_a": (c_int, [vp, c_int, c_int, c_int, vp, vp, sz, vp]),
         "qgemm_s8_packed": (c_int, [vp, c_int, vp, c_int, c_int, c_int, vp, vp, vp, vp]),
+        "qgemm_s8_static_scratch": (c_int, [vp, c_int, vp, c_int, c_int, c_int, vp, vp, vp, vp]),
         "qnn_conv_packed_w_bytes": (sz, [vp, c_int]),
         "qconv_prepack_w": (c_int, [vp, c_int, vp, vp, vp, vp]),
         "qconv_u4s4": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
@@ -227,6 +228,20 @@ def qgemm_s8_packed(A_packed, a_dt: str, B_packed, M: int, N: int, K: int, epi: 
     _check(_SYMBOLS["qgemm_s8_packed"](_ptr(A_packed), DTYPES[a_dt], _ptr(B_packed), int(M), int(N),
                                        int(K), ctypes.byref(epi), _ptr(C), _ptr(C_s32),
                                        _stream(stream)), "qgemm_s8_packed")
+
+
+QNN_GEMM_STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def qgemm_s8_static_scratch(A, a_dt: str, B_packed, M: int, N: int, K: int, epi: Epilogue, C,
+                            C_s32=None, stream=None):
+    """qgemm_s8 for callers that cannot allocate at call time: the workspace is
+    the library's fixed device array (QNN_GEMM_STATIC_SCRATCH_BYTES); calls
+    that overlap in time race on it."""
+    load()
+    _check(_SYMBOLS["qgemm_s8_static_scratch"](_ptr(A), DTYPES[a_dt], _ptr(B_packed), int(M), int(N),
+                                               int(K), ctypes.byref(epi), _ptr(C), _ptr(C_s32),
+                                               _stream(stream)), "qgemm_s8_static_scratch")
 
 
 def conv_geom(N, H, W, C, OC, FH, FW, pad=(1, 1), stride=(1, 1)) -> ConvGeom:
