@@ -419,14 +419,19 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
         epi = qnn.epilogue("requant", relu=True, out_dt="u4", zp_term=zp, M=Mv, Bq=Bq, residual=res,
                            res_dt="u4", z_res=w["z_res"], R=R)
         O = torch.empty((Nb, g.OH, g.OW, OC // 2), dtype=torch.uint8, device=device)
-        t = time_steps(torch, lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, g, epi, O, stream=stream),
-                       steps, 3, flush, stream)
+        ws = torch.empty(qnn.qnn_conv_workspace_bytes(g, "u4"), dtype=torch.uint8, device=device)
+        t = time_steps(torch, lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, g, epi, O, workspace=ws,
+                                                     stream=stream), steps, 3, flush, stream)
         ms = statistics.median(t)
+        tf = time_steps(torch, lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, g, epi, O, stream=stream),
+                        steps, 3, flush, stream)
+        ms_fused = statistics.median(tf)
         ops = 2.0 * Nb * g.OH * g.OW * OC * C * F * F
         tops = ops / (ms * 1e-3) / 1e12
         byts = I.numel() + O.numel() + (0 if res is None else res.numel()) + Wd.numel()
         out[name] = {"ms": round(ms, 4), "TOPS": round(tops, 2),
                      "frac_fp8_peak": round(tops / (2.0 * peak), 4),
+                     "ms_no_workspace": round(ms_fused, 4),
                      "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
                      "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
 
@@ -511,7 +516,9 @@ def run_case(args):
         epi = qnn.epilogue("requant", relu=True, out_dt="u4", zp_term=zp, M=Mv, Bq=Bq, residual=res,
                            res_dt="u4", z_res=w["z_res"], R=R)
         O = torch.empty((Nb, gg.OH, gg.OW, OC // 2), dtype=torch.uint8, device=device)
-        fn = lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, gg, epi, O, stream=stream)  # noqa: E731
+        ws = None if getattr(args, "fused", False) else torch.empty(qnn.qnn_conv_workspace_bytes(gg, "u4"),
+                                                                     dtype=torch.uint8, device=device)
+        fn = lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, gg, epi, O, workspace=ws, stream=stream)  # noqa: E731
     else:
         raise SystemExit(f"unknown case {case}")
     t = time_steps(torch, fn, args.steps, args.warmup, flush, stream)
@@ -609,7 +616,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--fused", action="store_true",
-                    help="--case GEMMs: no workspace (A re-encoded inside the GEMM kernel)")
+                    help="--case GEMMs / convs: no workspace (A re-encoded inside the kernel)")
     ap.add_argument("--case", default=None,
                     help="run one workload only (profiling): quantize, vit_fc1, square_4096, "
                          "vitl_fc2, conv3x3, conv1x1, or gemm:M:N:K (u8 x s8 -> s8)")

@@ -225,17 +225,32 @@ typedef struct {
 size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g, qnn_dtype w_dt);
 
 /* Prepack conv weights of w_dt (S4: packed nibbles, OHWI; S8: bytes, OHWI) into
- * the conv kernel's operand image (`W_packed`, qnn_conv_packed_w_bytes bytes)
- * and write colsum[oc] = sum over (fh, fw, c) of W (int32 [OC]). */
+ * the conv kernels' operand images (`W_packed`, qnn_conv_packed_w_bytes bytes,
+ * 1024-byte aligned; for S4 it holds the images of both qconv_u4s4 paths and
+ * the column sums) and write colsum[oc] = sum over (fh, fw, c) of W (int32
+ * [OC]) when colsum is not NULL. */
 qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_conv_geom *g, void *W_packed,
                            int32_t *colsum, qnn_stream_t stream);
+
+/* Size in bytes of the qconv_u4s4 workspace for an input of in_dt (U4: the
+ * input expanded to one byte per channel, N * H * W * C); 0 for an invalid
+ * geometry or another type. */
+size_t qnn_conv_workspace_bytes(const qnn_conv_geom *g, qnn_dtype in_dt);
 
 /* u4 activations x s4 weights [MG 緩解精度下降: UINT4 input/output, INT4
  * weights, FP32 bias], Conv_Relu / Conv_Add_Relu through `epi`
  * [MG 算子融合優化].  I: packed u4 NHWC; O: out_dt U4 (packed) or U8 codes, or
- * fp32 / int32 per epi->mode; O_s32: optional int32 acc_c.  C, OC even. */
+ * fp32 / int32 per epi->mode; O_s32: optional int32 acc_c.  C a multiple of
+ * 32, OC even.
+ * workspace: optional device scratch of at least qnn_conv_workspace_bytes(g,
+ *   QNN_U4) bytes (16-byte aligned), owned by the caller and overwritten: with
+ *   it, a pre-pass expands the input to one byte per channel and the
+ *   convolution reads its taps with tensor-memory copies (the faster path);
+ *   NULL: the convolution re-encodes the packed input itself.  Results are
+ *   identical.  Calls in flight at the same time must not share a workspace. */
 qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
-                      const qnn_epilogue *epi, void *O, int32_t *O_s32, qnn_stream_t stream);
+                      const qnn_epilogue *epi, void *O, int32_t *O_s32, void *workspace,
+                      size_t workspace_bytes, qnn_stream_t stream);
 
 /* u8 activations x s8 weights, same contract (I: u8 NHWC; C % 16 == 0). */
 qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,

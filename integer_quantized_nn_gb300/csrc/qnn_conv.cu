@@ -23,6 +23,8 @@
 // Padded taps read the code z_in (the real value 0 [reading of the pages]),
 // so the folded zero-point term applies to every tap alike.
 #include <cuda_fp8.h>
+#include <cudaTypedefs.h>
+#include <atomic>
 #include <type_traits>
 #include "qnn_mma_kernel.cuh"
 
@@ -106,7 +108,7 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // per-thread staging ring of D units in shared memory ([slot][q][thread] x 16
 // bytes), so D - 1 units of loads are in flight while one is converted.
 template <int ELEM_BITS, int GROUP_ELEMS, int STEP_ELEMS, int D>
-struct ConvStaging {
+struct ConvStaging : OpBase {
     static constexpr int DEPTH = D;
     static constexpr int DEPTH_MULTI = D;
     static constexpr int STG_BYTES = D * 4 * 128 * 16;
@@ -165,7 +167,7 @@ struct ConvStaging {
 // groups are loaded with plain non-coherent loads DEPTH - 1 units ahead
 // (padding and zero rows are resolved when the unit is loaded).
 template <int ELEM_BITS, int GROUP_ELEMS, int STEP_ELEMS>
-struct ConvRegRing {
+struct ConvRegRing : OpBase {
     static constexpr int DEPTH = 4;
     static constexpr int DEPTH_MULTI = 3;
     static constexpr int STG_BYTES = 16;  // no staging ring
@@ -345,8 +347,190 @@ inline size_t packed_w_u4_bytes(const qnn_conv_geom *g)
     return (size_t)((g->OC + 255) / 256) * (size_t)((K + 127) / 128) * (size_t)gemm::B_STAGE_BYTES;
 }
 
+inline size_t round1k(size_t b) { return (b + 1023) & ~(size_t)1023; }
+
+// The TMA conv's weight image (0 when C is not a multiple of 32).
+inline size_t tma_w_bytes(const qnn_conv_geom *g)
+{
+    if (g->C % 32 != 0) return 0;
+    const int cb = (g->C % 128 == 0) ? 128 : (g->C % 64 == 0 ? 64 : 32);
+    return (size_t)((g->OC + 255) / 256) * (size_t)g->FH * g->FW * (g->C / cb) * 256 * cb;
+}
+
+// W_packed of s4 weights: [fused-path image][TMA image][colsum, int32 x OC], 1 KB aligned parts.
+inline size_t tma_w_offset(const qnn_conv_geom *g) { return round1k(packed_w_u4_bytes(g)); }
+inline size_t colsum_offset(const qnn_conv_geom *g) { return tma_w_offset(g) + round1k(tma_w_bytes(g)); }
+inline size_t packed_w_u4_total(const qnn_conv_geom *g) { return colsum_offset(g) + round1k((size_t)g->OC * 4); }
+
 // Staging depth: 8 units for tiles up to 128 columns (64 KB of staging), 2 for
 // 256-column tiles, whose units carry 4x the MMA work (and shared memory is full).
+// ---- u4 conv fed by TMA (with a workspace) --------------------------------------
+// A pre-pass expands the packed u4 input into bytes holding the e4m3 encoding of
+// (q - z_in) / 512 (exact: |q - z_in| <= 15; the byte is |q - z_in| with the
+// sign in bit 7), so that a zero byte is the real value 0.  The implicit GEMM
+// then needs no re-encoding: for each output tile -- TN images x TH rows x TW
+// columns of output pixels, at most 128 -- and each unit -- one filter tap x CB
+// input channels -- one tiled TMA box of the expanded tensor, shifted by the
+// tap and strided by the conv stride, lands as the swizzled K-major A stage;
+// taps that fall in the padding read zeros.  The kernel's sum is therefore
+// sum (q - z_in) * w; the epilogue adds z_in * colsum back before subtracting
+// zp_term, so acc_c is the same as on the fused path.
+
+// Bytes (= input channels) per operand row for C channels.
+inline int tma_cb(int C) { return C % 128 == 0 ? 128 : (C % 64 == 0 ? 64 : 32); }
+
+// Stages that fit in about 192 KB of shared memory.
+constexpr int tma_stages(int cb, int tbn)
+{
+    return (196608 / ((BM + tbn) * cb)) > 16 ? 16 : (196608 / ((BM + tbn) * cb));
+}
+
+template <int CB, int NSTAGES>
+struct ConvTmaOp : OpBase {
+    static constexpr bool TMA_A = true;
+    static constexpr bool F8 = true;
+    static constexpr int SCALE_LOG2 = 9;
+    static constexpr int ROW = CB;
+    static constexpr int STAGES = NSTAGES;
+    static constexpr int STG_BYTES = 16;
+
+    __device__ static uint32_t a_bytes(const Params &p) { return (uint32_t)(CB * p.TW * p.TH * p.TN); }
+
+    // Units walk K from 0 in every tile (no per-CTA rotation), so the tap and
+    // channel block advance by counting; a tile's box origin is decoded once.
+    static constexpr bool ROTATE_K = false;
+    struct PState {
+        int mb = -1;            // tile whose origin is cached
+        int w0, h0, n0;         // box origin of tap (0, 0), channel block 0
+        int fh, fw, cblk;       // position of the next unit in K
+    };
+
+    __device__ static void load_a(const Params &p, const UnitCursor &c, PState &ps, uint32_t dst, uint32_t bar)
+    {
+        if (c.mb != ps.mb) {
+            const int tx = c.mb % p.tiles_x;
+            const int rest = c.mb / p.tiles_x;
+            const int ty = rest % p.tiles_y;
+            const int tn = rest / p.tiles_y;
+            ps.mb = c.mb;
+            ps.w0 = tx * p.TW * p.sw - p.pw;
+            ps.h0 = ty * p.TH * p.sh - p.ph;
+            ps.n0 = tn * p.TN;
+        }
+        if (c.ks == 0) {
+            ps.fh = 0;
+            ps.fw = 0;
+            ps.cblk = 0;
+        }
+        tma_load_4d(dst, &p.tmap, ps.cblk * CB, ps.w0 + ps.fw, ps.h0 + ps.fh, ps.n0, bar);
+        if (++ps.cblk == p.cbn) {
+            ps.cblk = 0;
+            if (++ps.fw == p.FW) {
+                ps.fw = 0;
+                ++ps.fh;
+            }
+        }
+    }
+
+    // Row r of a tile is output pixel (n, oh, ow) in box order (w fastest).
+    struct RowInfo {
+        int nl, hl, wl;  // position in the box; nl = TN marks a row outside it
+    };
+    __device__ static RowInfo row_info(const Params &p, int r)
+    {
+        const int per = p.TW * p.TH;
+        RowInfo ri;
+        ri.nl = r / per;
+        const int rr = r - ri.nl * per;
+        ri.hl = rr / p.TW;
+        ri.wl = rr - ri.hl * p.TW;
+        return ri;
+    }
+    // Output row of box row ri in tile mb, or M (skipped) outside the output.
+    __device__ static int out_row(const Params &p, int mb, const RowInfo &ri)
+    {
+        const int tx = mb % p.tiles_x;
+        const int rest = mb / p.tiles_x;
+        const int ty = rest % p.tiles_y;
+        const int tn = rest / p.tiles_y;
+        const int n = tn * p.TN + ri.nl;
+        const int oh = ty * p.TH + ri.hl;
+        const int ow = tx * p.TW + ri.wl;
+        if (ri.nl >= p.TN || n >= p.Nimg || oh >= p.OH || ow >= p.OW) return p.M;
+        return (n * p.OH + oh) * p.OW + ow;
+    }
+};
+
+// Input expansion: 16 packed bytes (32 u4 codes, low nibble first) per thread
+// -> 32 bytes of e4m3((q - z) / 512) in channel order.
+__device__ __forceinline__ uint32_t e4m3_centred(uint32_t q, uint32_t z)
+{
+    return q >= z ? q - z : (0x80u | (z - q));
+}
+
+__global__ void expand_u4_kernel(const uint8_t *__restrict__ in, int64_t n16, uint32_t z, uint8_t *__restrict__ out)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = ldg_nc_v4(in + i * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t e[8];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const uint32_t byte = (w[j] >> (8 * b)) & 255u;
+                e[2 * b] = e4m3_centred(byte & 15u, z);
+                e[2 * b + 1] = e4m3_centred(byte >> 4, z);
+            }
+            o[2 * j] = e[0] | (e[1] << 8) | (e[2] << 16) | (e[3] << 24);
+            o[2 * j + 1] = e[4] | (e[5] << 8) | (e[6] << 16) | (e[7] << 24);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(out + i * 32);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// Weight image of the TMA conv: for each 256-filter block and unit (tap, CB
+// channels), 256 rows x CB bytes of e4m3 weights in channel order, in the
+// CB-byte swizzled layout (chunk c of row r at chunk c ^ ((r * CB / 128) %
+// (CB / 16))); zero beyond OC.  One thread per 16-byte chunk.
+__global__ void prepack_w_s4_tma_kernel(const uint8_t *__restrict__ W, int OC, int C, int CB, int KT,
+                                        uint8_t *__restrict__ out, int64_t nchunks)
+{
+    const int cpr = CB / 16;
+    const int cbn = C / CB;
+    const int K = KT * CB;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int cphys = (int)(i % cpr);
+        const int64_t row_all = i / cpr;
+        const int r = (int)(row_all % 256);
+        const int64_t blk = row_all / 256;
+        const int ks = (int)(blk % KT);
+        const int nb = (int)(blk / KT);
+        const int c = cphys ^ (((r * CB) >> 7) & (cpr - 1));
+        const int n = nb * 256 + r;
+        const int tap = ks / cbn;
+        const int k0 = tap * C + (ks - tap * cbn) * CB + c * 16;
+        uint32_t w[4] = {0, 0, 0, 0};
+        if (n < OC) {
+#pragma unroll
+            for (int b = 0; b < 16; ++b) {
+                const int k = k0 + b;
+                const uint8_t byte = W[((int64_t)n * K + k) >> 1];
+                int v = (k & 1) ? (byte >> 4) : (byte & 15);
+                if (v >= 8) v -= 16;
+                const uint32_t code = (uint32_t)__nv_cvt_float_to_fp8((float)v, __NV_SATFINITE, __NV_E4M3);
+                w[b >> 2] |= code << (8 * (b & 3));
+            }
+        }
+        *reinterpret_cast<uint4 *>(out + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 template <template <int> class Op, int TBN>
 qnn_status conv_launch(const Params &p, cudaStream_t s)
 {
@@ -357,9 +541,72 @@ qnn_status conv_launch(const Params &p, cudaStream_t s)
     return launch<Op<0>, TBN, false>(p, s);
 }
 
+// Output tile shape for the TMA conv: TW x TH x TN pixels (at most 128, box
+// sides within the TMA limit of 256 elements after striding) that wastes the
+// fewest of the 128 accumulator rows over the whole output; ties go to the
+// wider tile (longer contiguous input rows).
+inline void choose_tiles(int N, int OH, int OW, int sw, int sh, int &TW, int &TH, int &TN)
+{
+    int64_t best = -1;
+    TW = TH = TN = 1;
+    for (int tw = 1; tw <= 128 && tw * sw <= 256; ++tw) {
+        for (int th = 1; tw * th <= 128 && th * sh <= 256; ++th) {
+            int tn = 128 / (tw * th);
+            if (tn > N) tn = N;
+            const int64_t tiles = (int64_t)((OW + tw - 1) / tw) * ((OH + th - 1) / th) * ((N + tn - 1) / tn);
+            // score: fewest tiles; then the wider tile
+            const int64_t score = (int64_t)1 << 40;
+            const int64_t sc = score - tiles * 1024 + tw;
+            if (sc > best) {
+                best = sc;
+                TW = tw;
+                TH = th;
+                TN = tn;
+            }
+        }
+    }
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link the driver library, so that it loads on hosts
+// without a GPU driver); nullptr if unavailable.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !ptr) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+template <int CB, int TBN>
+qnn_status conv_tma_launch(const Params &p, cudaStream_t s)
+{
+    return launch<ConvTmaOp<CB, tma_stages(CB, TBN)>, TBN, false>(p, s);
+}
+
+template <int TBN>
+qnn_status conv_tma_dispatch(const Params &p, int cb, cudaStream_t s)
+{
+    if (cb == 128) return conv_tma_launch<128, TBN>(p, s);
+    if (cb == 64) return conv_tma_launch<64, TBN>(p, s);
+    return conv_tma_launch<32, TBN>(p, s);
+}
+
 template <template <int> class Op>
 qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
-                    const qnn_epilogue *e, void *O, int32_t *O_s32, qnn_stream_t stream, bool u4)
+                    const qnn_epilogue *e, void *O, int32_t *O_s32, void *workspace, size_t workspace_bytes,
+                    qnn_stream_t stream, bool u4)
 {
     if (!I || !W_packed || !e || !O) return QNN_ERR_INVALID_ARG;
     if (!geom_ok(g)) return QNN_ERR_INVALID_ARG;
@@ -408,9 +655,59 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
     }
     p.nchunks = (p.KT + p.chunk_steps - 1) / p.chunk_steps;
     if (u4 && p.nchunks > 1) return QNN_ERR_UNSUPPORTED;
+    if (workspace) {
+        if (!u4) return QNN_ERR_UNSUPPORTED;
+        if (workspace_bytes < (size_t)g->N * g->H * g->W * g->C) return QNN_ERR_INVALID_ARG;
+        if (!aligned16(workspace)) return QNN_ERR_ALIGNMENT;
+        if (g->stride_h > 8 || g->stride_w > 8) return QNN_ERR_UNSUPPORTED;
+    }
     p.status = status_word();
     if (!p.status) return QNN_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
+    if (workspace) {
+        // expanded input, then the tensor map over it: dims (C, W, H, N), bytes
+        const int64_t n16 = (int64_t)g->N * g->H * g->W * g->C / 32;
+        int64_t blocks = (n16 + 255) / 256;
+        const int64_t cap = (int64_t)sm_count() * 16;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        expand_u4_kernel<<<(int)blocks, 256, 0, s>>>(p.A, n16, (uint32_t)z_in, static_cast<uint8_t *>(workspace));
+        if (launch_status() != QNN_OK) return QNN_ERR_CUDA;
+        const int cb = tma_cb(g->C);
+        int TW, TH, TN;
+        choose_tiles(g->N, oh, ow, g->stride_w, g->stride_h, TW, TH, TN);
+        cuuint64_t dims[4] = {(cuuint64_t)g->C, (cuuint64_t)g->W, (cuuint64_t)g->H, (cuuint64_t)g->N};
+        cuuint64_t strides[3] = {(cuuint64_t)g->C, (cuuint64_t)g->W * g->C, (cuuint64_t)g->H * g->W * g->C};
+        cuuint32_t box[4] = {(cuuint32_t)cb, (cuuint32_t)(TW * g->stride_w), (cuuint32_t)(TH * g->stride_h),
+                             (cuuint32_t)TN};
+        cuuint32_t estr[4] = {1, (cuuint32_t)g->stride_w, (cuuint32_t)g->stride_h, 1};
+        const CUtensorMapSwizzle swz = cb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                 : (cb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+        const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+        if (!encode) return QNN_ERR_CUDA;
+        if (encode(&p.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, workspace, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return QNN_ERR_CUDA;
+        p.Nimg = g->N;
+        p.OH = oh;
+        p.TW = TW;
+        p.TH = TH;
+        p.TN = TN;
+        p.tiles_x = (ow + TW - 1) / TW;
+        p.tiles_y = (oh + TH - 1) / TH;
+        p.num_m = p.tiles_x * p.tiles_y * ((g->N + TN - 1) / TN);
+        p.cbn = g->C / cb;
+        p.KT = g->FH * g->FW * p.cbn;
+        p.nchunks = 1;
+        p.chunk_steps = p.KT;
+        p.Bp = static_cast<const uint8_t *>(W_packed) + tma_w_offset(g);
+        p.zcs = reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(W_packed) + colsum_offset(g));
+        p.z_cs = z_in;
+        if (g->OC <= 64) return conv_tma_dispatch<64>(p, cb, s);
+        if (g->OC <= 128) return conv_tma_dispatch<128>(p, cb, s);
+        return conv_tma_dispatch<256>(p, cb, s);
+    }
     if (g->OC <= 64) return conv_launch<Op, 64>(p, s);
     if (g->OC <= 128) return conv_launch<Op, 128>(p, s);
     return conv_launch<Op, 256>(p, s);
@@ -422,7 +719,7 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
 extern "C" size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g, qnn_dtype w_dt)
 {
     if (!qnn::mk::geom_ok(g)) return 0;
-    if (w_dt == QNN_S4) return qnn::mk::packed_w_u4_bytes(g);
+    if (w_dt == QNN_S4) return qnn::mk::packed_w_u4_total(g);
     if (w_dt == QNN_S8) return qnn::gemm::packed_b_bytes(g->OC, g->FH * g->FW * g->C);
     return 0;
 }
@@ -444,29 +741,52 @@ extern "C" qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_c
     int64_t blocks = (nchunks + 255) / 256;
     if (blocks > 65535) blocks = 65535;
     cudaStream_t s = (cudaStream_t)stream;
+    uint8_t *wp = static_cast<uint8_t *>(W_packed);
     qnn::mk::prepack_w_s4_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(W), g->OC, K,
-                                                               KT, static_cast<uint8_t *>(W_packed),
-                                                               nchunks);
+                                                               KT, wp, nchunks);
+    if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
+    // the TMA conv's image and the column sums follow the fused-path image
+    const size_t tb = qnn::mk::tma_w_bytes(g);
+    if (tb) {
+        const int cb = qnn::mk::tma_cb(g->C);
+        const int64_t tchunks = (int64_t)(tb / 16);
+        int64_t tblocks = (tchunks + 255) / 256;
+        if (tblocks > 65535) tblocks = 65535;
+        qnn::mk::prepack_w_s4_tma_kernel<<<(int)tblocks, 256, 0, s>>>(
+            static_cast<const uint8_t *>(W), g->OC, g->C, cb, g->FH * g->FW * (g->C / cb),
+            wp + qnn::mk::tma_w_offset(g), tchunks);
+        if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
+    }
+    const int64_t threads = (int64_t)g->OC * 32;
+    int32_t *cs_img = reinterpret_cast<int32_t *>(wp + qnn::mk::colsum_offset(g));
+    qnn::mk::colsum_s4_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(static_cast<const uint8_t *>(W),
+                                                                          g->OC, K, cs_img);
     if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
     if (colsum) {
-        const int64_t threads = (int64_t)g->OC * 32;
-        qnn::mk::colsum_s4_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(
-            static_cast<const uint8_t *>(W), g->OC, K, colsum);
-        return qnn::launch_status();
+        if (cudaMemcpyAsync(colsum, cs_img, (size_t)g->OC * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return QNN_ERR_CUDA;
     }
     return QNN_OK;
 }
 
+extern "C" size_t qnn_conv_workspace_bytes(const qnn_conv_geom *g, qnn_dtype in_dt)
+{
+    if (!qnn::mk::geom_ok(g) || in_dt != QNN_U4) return 0;
+    return (size_t)g->N * g->H * g->W * g->C;
+}
+
 extern "C" qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed,
                                  const qnn_conv_geom *g, const qnn_epilogue *e, void *O,
-                                 int32_t *O_s32, qnn_stream_t stream)
+                                 int32_t *O_s32, void *workspace, size_t workspace_bytes,
+                                 qnn_stream_t stream)
 {
-    return qnn::mk::conv_run<qnn::mk::ConvU4Op>(I, z_in, W_packed, g, e, O, O_s32, stream, true);
+    return qnn::mk::conv_run<qnn::mk::ConvU4Op>(I, z_in, W_packed, g, e, O, O_s32, workspace,
+                                                workspace_bytes, stream, true);
 }
 
 extern "C" qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_packed,
                                  const qnn_conv_geom *g, const qnn_epilogue *e, void *O,
                                  int32_t *O_s32, qnn_stream_t stream)
 {
-    return qnn::mk::conv_run<qnn::mk::ConvU8Op>(I, z_in, W_packed, g, e, O, O_s32, stream, false);
+    return qnn::mk::conv_run<qnn::mk::ConvU8Op>(I, z_in, W_packed, g, e, O, O_s32, nullptr, 0, stream, false);
 }

@@ -48,7 +48,7 @@ __device__ __forceinline__ void bytes_to_half(uint4 v, uint32_t flip, uint32_t (
 }
 
 template <bool PTF>
-struct GemmOp {
+struct GemmOp : OpBase {
     static constexpr bool TMA_A = false;
     static constexpr bool F8 = false;
     static constexpr int SCALE_LOG2 = 0;
@@ -116,11 +116,16 @@ struct GemmOp {
 };
 
 // A operand already in the fp16 image: the producer copies it.
-struct GemmPackedOp {
+struct GemmPackedOp : OpBase {
     static constexpr bool TMA_A = true;
     static constexpr bool F8 = false;
     static constexpr int SCALE_LOG2 = 0;
     static constexpr int STG_BYTES = 16;
+    __device__ static uint32_t a_bytes(const Params &) { return A_STAGE_BYTES; }
+    __device__ static void load_a(const Params &p, const UnitCursor &c, PState &, uint32_t dst, uint32_t bar)
+    {
+        bulk_g2s(dst, p.Ap + ((int64_t)c.mb * p.KT + c.ks) * A_STAGE_BYTES, A_STAGE_BYTES, bar);
+    }
 };
 
 // Pre-pass: A [M, K] (s8, or u8 read as q - 128; times 2^alpha_k with PTF)

@@ -31,6 +31,7 @@
 // Every mbarrier wait is bounded (qnn_ptx.cuh): on time-out the role sets the
 // device status word and winds down instead of hanging.
 #pragma once
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -44,15 +45,24 @@ namespace mk {
 using gemm::BM;
 using gemm::ROW_BYTES;
 
-constexpr int STAGES = 4;
 constexpr int NUM_THREADS = 512;
 constexpr int PRODUCER_WARP = 4;
 constexpr int MMA_WARP = 5;
 constexpr int EPI_WARP0 = 8;
-constexpr int NUM_EPI_WARPS = 8;
-constexpr int A_STAGE_BYTES = BM * ROW_BYTES;
+
+// Epilogue warps: warps 8-15, plus warps 0-3 when the Op needs no converter
+// warps (its A arrives by copy) and the tile has at least three 32-column
+// pieces.  Each group of four warps covers the 128 TMEM lanes for its share
+// of the pieces (group g: pieces g*P/G .. (g+1)*P/G - 1 of P, G groups).
+template <class Op, int TBN>
+__host__ __device__ constexpr int epi_warps() { return (Op::TMA_A && TBN >= 128) ? 12 : 8; }
+template <class Op, int TBN>
+__host__ __device__ constexpr int epi_max_pieces() { return (TBN / 32 + epi_warps<Op, TBN>() / 4 - 1) / (epi_warps<Op, TBN>() / 4); }
+constexpr int A_STAGE_BYTES = BM * ROW_BYTES;  // 128-byte rows (every Op but the TMA conv)
 
 struct Params {
+    // activation tensor map (implicit-GEMM conv fed by TMA); first, 64-byte aligned
+    alignas(64) CUtensorMap tmap;
     // activation operand
     const uint8_t *A;
     int a_u8;                // GEMM: 1 if A holds u8 codes (centred at 128), 0 for s8
@@ -61,6 +71,11 @@ struct Params {
     // convolution geometry (NHWC input, OHWI weights, K order (fh, fw, c))
     int H, W, Cin, OHW, OW, FH, FW, ph, pw, sh, sw;
     uint32_t pad_word;       // input bytes that stand for the padding value z_in
+    // TMA conv: output tile = TN images x TH rows x TW columns of pixels; unit = one filter tap
+    // x `cpu` input channels (cbn units per tap); zcs: weight column sums, z_cs: their factor
+    int Nimg, OH, TW, TH, TN, tiles_x, tiles_y, cpu, cbn;
+    const int32_t *zcs;
+    int z_cs;
     // weights (prepacked image) and shape of the GEMM view
     const uint8_t *Bp;
     int M, N, K, KT, num_m, num_tiles;
@@ -83,14 +98,28 @@ struct Params {
     uint32_t *status;
 };
 
+// Defaults every Op inherits: 4 stages of 128-byte operand rows, and GEMM
+// rows in tile order (row r of row block mb is GEMM row mb * 128 + r).
+struct OpBase {
+    static constexpr int STAGES = 4;
+    static constexpr int ROW = 128;
+    static constexpr bool ROTATE_K = true;  // each CTA starts its tiles' K walk at its own offset
+    struct PState {};                        // producer-side state of a TMA_A Op
+    struct RowInfo {                         // per-thread part of the row mapping
+        int r;
+    };
+    __device__ static RowInfo row_info(const Params &, int r) { return RowInfo{r}; }
+    __device__ static int out_row(const Params &, int mb, const RowInfo &ri) { return mb * BM + ri.r; }
+};
+
 template <class Op, int TBN>
 struct __align__(1024) Smem {
-    uint8_t a[STAGES][A_STAGE_BYTES];
-    uint8_t b[STAGES][TBN * ROW_BYTES];
+    uint8_t a[Op::STAGES][BM * Op::ROW];
+    uint8_t b[Op::STAGES][TBN * Op::ROW];
     uint4 stg[Op::STG_BYTES / 16];                   // converter staging ring (Op-specific)
-    float cols[NUM_EPI_WARPS][4 * (TBN / 2)];        // per epilogue warp: its columns' constants
-    uint64_t full[STAGES];   // 4 converter-warp arrivals (none with TMA_A) + the producer's expect_tx
-    uint64_t empty[STAGES];
+    float cols[epi_warps<Op, TBN>()][4 * 32 * epi_max_pieces<Op, TBN>()];  // per epilogue warp: its columns' constants
+    uint64_t full[Op::STAGES];   // 4 converter-warp arrivals (none with TMA_A) + the producer's expect_tx
+    uint64_t empty[Op::STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t mma_done;
@@ -112,9 +141,9 @@ struct UnitCursor {
     int t;       // tile index
     int mb, nb;  // tile coordinates: row block, column block
 
-    __device__ __forceinline__ void begin(const Params &p)
+    __device__ __forceinline__ void begin(const Params &p, bool rotate = true)
     {
-        rot = (int)(blockIdx.x % (unsigned)p.KT);
+        rot = rotate ? (int)(blockIdx.x % (unsigned)p.KT) : 0;
         t = blockIdx.x;
         kl = 0;
         ks = rot;
@@ -151,6 +180,7 @@ __device__ __forceinline__ bool convert_one(const Params &p, Smem<Op, TBN> &s, t
                                             int j, int units, int sub, int rbase,
                                             const typename Op::Unit &u, bool &ready)
 {
+    constexpr int STAGES = Op::STAGES;
     const int stage = j % STAGES;
     const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
     const bool ok = ready || mbar_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status);
@@ -233,9 +263,12 @@ template <class Op, int TBN>
 __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
 {
     const bool leader = (threadIdx.x & 31) == 0;
+    constexpr int STAGES = Op::STAGES;
+    constexpr int ROW = Op::ROW;
     const uint32_t b0 = smem_u32(&s.b[0][0]);
     UnitCursor c;
-    c.begin(p);
+    c.begin(p, Op::ROTATE_K);
+    typename Op::PState ps{};
     bool ok = true;
     bool ready = false;
     int j = 0;
@@ -251,17 +284,16 @@ __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
         if (leader) {
             // columns n0 .. n0 + TBN - 1 live in the 256-row packed block n0 / 256
             const int n0 = c.nb * TBN;
-            const uint8_t *src = p.Bp + ((int64_t)(n0 / gemm::BN) * p.KT + c.ks) * gemm::B_STAGE_BYTES +
-                                 (int64_t)(n0 % gemm::BN) * ROW_BYTES;
+            const uint8_t *src = p.Bp + ((int64_t)(n0 / gemm::BN) * p.KT + c.ks) * (gemm::BN * ROW) +
+                                 (int64_t)(n0 % gemm::BN) * ROW;
             const uint32_t bar = smem_u32(&s.full[stage]);
             if constexpr (Op::TMA_A) {
-                mbar_arrive_expect_tx(bar, TBN * ROW_BYTES + A_STAGE_BYTES);
-                bulk_g2s(smem_u32(&s.a[stage][0]), p.Ap + ((int64_t)c.mb * p.KT + c.ks) * A_STAGE_BYTES,
-                         A_STAGE_BYTES, bar);
+                mbar_arrive_expect_tx(bar, TBN * ROW + Op::a_bytes(p));
+                Op::load_a(p, c, ps, smem_u32(&s.a[stage][0]), bar);
             } else {
-                mbar_arrive_expect_tx(bar, TBN * ROW_BYTES);
+                mbar_arrive_expect_tx(bar, TBN * ROW);
             }
-            bulk_g2s(b0 + stage * (TBN * ROW_BYTES), src, TBN * ROW_BYTES, bar);
+            bulk_g2s(b0 + stage * (TBN * ROW), src, TBN * ROW, bar);
         }
         ready = __all_sync(0xffffffffu, probe) && jn < units;
     }
@@ -283,28 +315,32 @@ template <class Op, int TBN>
 __device__ void mma_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32_t tmem)
 {
     constexpr uint32_t IDESC = idesc_f32acc(0, 0, BM, TBN);  // f16 x f16, or e4m3 x e4m3
+    constexpr int STAGES = Op::STAGES;
+    constexpr int ROW = Op::ROW;
+    constexpr int KSLICES = ROW / 32;  // one MMA per 32-byte K slice of a row
     const bool leader = (threadIdx.x & 31) == 0;
     const int units = my_tiles * p.KT;
-    const uint64_t adesc0 = sdesc_sw128(smem_u32(&s.a[0][0]));
-    const uint64_t bdesc0 = sdesc_sw128(smem_u32(&s.b[0][0]));
+    const uint64_t adesc0 = sdesc_sw(smem_u32(&s.a[0][0]), ROW);
+    const uint64_t bdesc0 = sdesc_sw(smem_u32(&s.b[0][0]), ROW);
+    int stage = 0;
+    uint32_t sph = 0;  // phase of the current stage's full barrier
     uint32_t u = 0;  // accumulation chunk counter
     int kl = 0;      // unit position within the tile
     int cpos = 0;    // unit position within the accumulation chunk
     for (int j = 0; j < units; ++j) {
-        const int stage = j & (STAGES - 1);
         const uint32_t abuf = u & 1u;
         const bool first = cpos == 0;
         const bool last = (cpos == p.chunk_steps - 1) || (kl == p.KT - 1);
         if (first && !warp_wait(smem_u32(&s.acc_empty[abuf]), ((u >> 1) & 1u) ^ 1u, p.status)) break;
-        if (!warp_wait(smem_u32(&s.full[stage]), (uint32_t)(j / STAGES) & 1u, p.status)) break;
+        if (!warp_wait(smem_u32(&s.full[stage]), sph, p.status)) break;
         tc_fence_after();
         if (leader) {
             // descriptor start addresses are in 16-byte units: +2 per 32-byte K slice
-            const uint64_t ad = adesc0 + (uint64_t)(stage * (A_STAGE_BYTES >> 4));
-            const uint64_t bd = bdesc0 + (uint64_t)(stage * ((TBN * ROW_BYTES) >> 4));
+            const uint64_t ad = adesc0 + (uint64_t)(stage * ((BM * ROW) >> 4));
+            const uint64_t bd = bdesc0 + (uint64_t)(stage * ((TBN * ROW) >> 4));
             const uint32_t d = tmem + abuf * TBN;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
+            for (int kk = 0; kk < KSLICES; ++kk) {
                 const uint32_t acc = (first && kk == 0) ? 0u : 1u;
                 if (Op::F8)
                     mma_f8f6f4_ss(d, ad + 2 * kk, bd + 2 * kk, IDESC, acc);
@@ -315,6 +351,10 @@ __device__ void mma_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32
             if (last) mma_commit(smem_u32(&s.acc_full[abuf]));
         }
         __syncwarp();
+        if (++stage == STAGES) {
+            stage = 0;
+            sph ^= 1u;
+        }
         if (last) {
             ++u;
             cpos = 0;
@@ -367,6 +407,7 @@ __device__ __forceinline__ void load_columns(const Params &p, ColumnRegs<COLS> &
                 b = p.bias ? __ldg(p.bias + n) : 0.0f;
             }
             if (p.zp) z = __ldg(p.zp + n);
+            if (p.zcs) z -= p.z_cs * __ldg(p.zcs + n);
         }
         cr.a[k] = a;
         cr.b[k] = b;
@@ -620,18 +661,22 @@ __device__ __forceinline__ int32_t acc_to_int(uint32_t bits)
 template <class Op, int TBN, bool MULTI>
 __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32_t tmem)
 {
-    constexpr int COLS = TBN / 2;
-    constexpr int PIECES = COLS / 32;
+    constexpr int PIECES = epi_max_pieces<Op, TBN>();  // 32-column pieces of a warp (at most)
+    constexpr int COLS = PIECES * 32;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int quad = warp & 3;                 // TMEM lanes 32*quad .. +31
-    const int half = (warp - EPI_WARP0) >> 2;  // columns COLS*half .. +COLS-1
-    float *cols = s.cols[warp - EPI_WARP0];
+    const int quad = warp & 3;                                    // TMEM lanes 32*quad .. +31
+    const int group = warp >= EPI_WARP0 ? (warp - EPI_WARP0) >> 2 : 2;  // warps 8-11, 12-15, 0-3
+    constexpr int NG = epi_warps<Op, TBN>() / 4;
+    const int p0 = group * (TBN / 32) / NG;                       // first piece of this warp
+    const int npieces = (group + 1) * (TBN / 32) / NG - p0;       // 1 .. PIECES
+    float *cols = s.cols[warp >= EPI_WARP0 ? warp - EPI_WARP0 : warp + 8];
     uint32_t u = 0;
+    const typename Op::RowInfo ri = Op::row_info(p, quad * 32 + lane);
     for (int i = 0; i < my_tiles; ++i) {
         const int t = blockIdx.x + i * gridDim.x;
-        const int m = (t % p.num_m) * BM + quad * 32 + lane;
-        const int nbase = (t / p.num_m) * TBN + half * COLS;
+        const int m = Op::out_row(p, t % p.num_m, ri);
+        const int nbase = (t / p.num_m) * TBN + p0 * 32;
         ColumnRegs<COLS> cr;
         load_columns<COLS>(p, cr, nbase, lane);
         if (!MULTI) {
@@ -641,17 +686,17 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
             if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
             tc_fence_after();
             const bool fast = store_columns<COLS>(cr, cols, lane) && !p.C32 && p.mode != QNN_EPI_S32;
-            const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + half * COLS;
+            const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + p0 * 32;
 #pragma unroll 1
-            for (int jp = 0; jp < PIECES; ++jp) {
+            for (int jp = 0; jp < npieces; ++jp) {
                 uint32_t rw[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) rw[k] = rw_next[k];
-                if (jp + 1 < PIECES) load_residual(p, m, nbase + (jp + 1) * 32, rw_next);
+                if (jp + 1 < npieces) load_residual(p, m, nbase + (jp + 1) * 32, rw_next);
                 uint32_t r[32];
                 tmem_ld32(taddr + jp * 32, r);
                 tmem_ld_wait();
-                if (jp == PIECES - 1) {
+                if (jp == npieces - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
@@ -688,9 +733,10 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
                 const uint32_t abuf = u & 1u;
                 if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
                 tc_fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + half * COLS;
+                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + p0 * 32;
 #pragma unroll
                 for (int jp = 0; jp < PIECES; ++jp) {
+                    if (jp >= npieces) break;
                     uint32_t r[32];
                     tmem_ld32(taddr + jp * 32, r);
                     tmem_ld_wait();
@@ -708,6 +754,7 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
             store_columns<COLS>(cr, cols, lane);
 #pragma unroll
             for (int jp = 0; jp < PIECES; ++jp) {
+                if (jp >= npieces) break;
                 uint32_t rw[8];
                 load_residual(p, m, nbase + jp * 32, rw);
                 epilogue_int(p, m, nbase + jp * 32, acc[jp], cols + jp * 32, cols + COLS + jp * 32,
@@ -728,13 +775,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
+        for (int i = 0; i < Op::STAGES; ++i) {
             mbar_init(smem_u32(&s.full[i]), Op::TMA_A ? 1 : 5);
             mbar_init(smem_u32(&s.empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s.acc_full[i]), 1);
-            mbar_init(smem_u32(&s.acc_empty[i]), NUM_EPI_WARPS);
+            mbar_init(smem_u32(&s.acc_empty[i]), epi_warps<Op, TBN>());
         }
         mbar_init(smem_u32(&s.mma_done), 1);
         fence_mbar_init();
@@ -753,19 +800,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
     const int units = my_tiles * p.KT;
 
     // Register split per warpgroup (launched with 128 per thread, 65536 in all):
-    // converters keep 128 (or drop to 24 when A arrives by copy), the
-    // producer / MMA warpgroup drops to 96, and the epilogue warpgroups take
-    // the rest -- 128*128 + 128*96 + 256*144 = 65536 or 128*24 + 128*96 +
-    // 256*192 = 64512.
+    // converters keep 128, the producer / MMA warpgroup drops to 96 and the
+    // epilogue warpgroups take the rest -- 128*128 + 128*96 + 256*144 = 65536;
+    // with A arriving by copy, warpgroup 0 is a third epilogue group and the
+    // producer / MMA warpgroup drops to 72 (128*72 + 384*144 = 64512) or, for
+    // 64-column tiles, warpgroup 0 idles at 24 (128*24 + 128*96 + 256*192 =
+    // 64512).
+    constexpr bool EPI12 = epi_warps<Op, TBN>() == 12;
     constexpr uint32_t REGS_WG1 = 96;
-    constexpr uint32_t REGS_WG0 = Op::TMA_A ? 24 : 128;
-    constexpr uint32_t REGS_EPI = ((65536u - 128u * REGS_WG0 - 128u * REGS_WG1) / 256u) & ~7u;
-    static_assert(128u * REGS_WG0 + 128u * REGS_WG1 + 256u * REGS_EPI <= 65536u, "register split");
+    constexpr uint32_t REGS_WG1_E12 = 72;
+    constexpr uint32_t REGS_EPI = EPI12 ? ((65536u - 128u * REGS_WG1_E12) / 384u) & ~7u
+                                        : ((65536u - 128u * (Op::TMA_A ? 24u : 128u) - 128u * REGS_WG1) / 256u) & ~7u;
+    constexpr uint32_t REGS_WG0 = EPI12 ? REGS_EPI : (Op::TMA_A ? 24u : 128u);
+    static_assert(128u * REGS_WG0 + 128u * (EPI12 ? REGS_WG1_E12 : REGS_WG1) + 256u * REGS_EPI <= 65536u,
+                  "register split");
     if (warp < 4) {
-        if constexpr (Op::TMA_A) regs_dec<REGS_WG0>();
-        else converter_role<Op, TBN, MULTI>(p, s, units);
+        if constexpr (EPI12) {
+            regs_inc<REGS_EPI>();
+            epilogue_role<Op, TBN, MULTI>(p, s, my_tiles, tmem);
+        } else if constexpr (Op::TMA_A) {
+            regs_dec<REGS_WG0>();
+        } else {
+            converter_role<Op, TBN, MULTI>(p, s, units);
+        }
     } else if (warp < 8) {
-        regs_dec<REGS_WG1>();
+        regs_dec<EPI12 ? REGS_WG1_E12 : REGS_WG1>();
         if (warp == PRODUCER_WARP) producer_role<Op, TBN>(p, s, units);
         if (warp == MMA_WARP) mma_role<Op, TBN>(p, s, my_tiles, tmem);
     } else {

@@ -220,6 +220,36 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr)
     return d;
 }
 
+// The same for rows of `row_bytes` = 128, 64 or 32 bytes in the matching
+// 128-, 64- or 32-byte swizzled layout (8-row atoms of 8 * row_bytes; the 16-byte
+// chunk c of row r stored at chunk c ^ ((r * row_bytes / 128) % (row_bytes / 16))).
+// The tile base must be aligned to the atom size.
+__device__ __forceinline__ uint64_t sdesc_sw(uint32_t addr, int row_bytes)
+{
+    const uint64_t layout = row_bytes == 128 ? 2u : (row_bytes == 64 ? 4u : 6u);
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(16u >> 4) << 16;
+    d |= (uint64_t)((8u * (uint32_t)row_bytes) >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= layout << 61;
+    return d;
+}
+
+// Tiled 4-D TMA load of one box of `tmap` at coordinates (c0 innermost .. c3)
+// into shared memory at `dst`, completing its bytes on `bar`.  The innermost
+// coordinate times the element size must be a multiple of 16 bytes; the
+// others may be negative or past the end (those elements read as zero).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int c0, int c1, int c2, int c3,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
 // Instruction descriptor: fp32 accumulator, K-major A and B, M x N tile.
 // a_fmt / b_fmt: kind::f16 -> 0 f16, 1 bf16; kind::f8f6f4 -> 0 e4m3, 1 e5m2,
 // 3 e2m3, 4 e3m2, 5 e2m1.

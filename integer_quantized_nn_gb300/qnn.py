@@ -78,7 +78,8 @@ def _declare(L):
         "qgemm_s8_static_scratch": (c_int, [vp, c_int, vp, c_int, c_int, c_int, vp, vp, vp, vp]),
         "qnn_conv_packed_w_bytes": (sz, [vp, c_int]),
         "qconv_prepack_w": (c_int, [vp, c_int, vp, vp, vp, vp]),
-        "qconv_u4s4": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
+        "qnn_conv_workspace_bytes": (sz, [vp, c_int]),
+        "qconv_u4s4": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "qconv_u8s8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
         "qnn_status_string": (ctypes.c_char_p, [c_int]),
         "qnn_check_device_error": (c_int, [vp]),
@@ -259,10 +260,20 @@ def qconv_prepack_w(W, w_dt: str, g: ConvGeom, W_packed, colsum=None, stream=Non
                                        _ptr(colsum), _stream(stream)), "qconv_prepack_w")
 
 
-def qconv_u4s4(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None, stream=None):
+def qnn_conv_workspace_bytes(g: ConvGeom, in_dt: str = "u4") -> int:
     load()
+    return int(_SYMBOLS["qnn_conv_workspace_bytes"](ctypes.byref(g), DTYPES[in_dt]))
+
+
+def qconv_u4s4(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None, workspace=None,
+               stream=None):
+    """workspace: optional uint8 device tensor of at least
+    qnn_conv_workspace_bytes(g, "u4") bytes (the pre-pass + TMA path)."""
+    load()
+    ws_bytes = 0 if workspace is None else _nbytes(workspace)
     _check(_SYMBOLS["qconv_u4s4"](_ptr(I), int(z_in), _ptr(W_packed), ctypes.byref(g),
-                                  ctypes.byref(epi), _ptr(O), _ptr(O_s32), _stream(stream)),
+                                  ctypes.byref(epi), _ptr(O), _ptr(O_s32), _ptr(workspace),
+                                  ctypes.c_size_t(ws_bytes), _stream(stream)),
            "qconv_u4s4")
 
 

@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("q_quantize", "q_dequantize", "qgemm_prepack_b", "q_fold_epilogue", "qgemm_s8",
               "qnn_gemm_workspace_bytes", "qgemm_pack_a", "qgemm_s8_packed", "qgemm_s8_static_scratch",
-              "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_status_string",
+              "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_conv_workspace_bytes",
+              "qnn_status_string",
               "qnn_check_device_error"):
         assert n in names
 
@@ -77,6 +78,15 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert L.qnn_gemm_workspace_bytes(16384, 4096) > qnn.QNN_GEMM_STATIC_SCRATCH_BYTES
     assert L.qgemm_s8_static_scratch(16, 0, 1024, 16384, 8, 4096, ctypes.byref(ok_epi), 16, None,
                                      None) == qnn.QNN_ERR_UNSUPPORTED
+    # conv workspace: its size, and a too-small one refused before any launch
+    g = qnn.conv_geom(64, 56, 56, 64, 64, 3, 3)
+    assert qnn.qnn_conv_workspace_bytes(g, "u4") == 64 * 56 * 56 * 64
+    assert qnn.qnn_conv_workspace_bytes(g, "u8") == 0
+    cneed = qnn.qnn_conv_workspace_bytes(g, "u4")
+    assert L.qconv_u4s4(16, 8, 1024, ctypes.byref(g), ctypes.byref(ok_epi), 16, None, 4096, cneed - 1,
+                        None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.qconv_u4s4(16, 8, 1024, ctypes.byref(g), ctypes.byref(ok_epi), 16, None, 4104, cneed,
+                        None) == qnn.QNN_ERR_ALIGNMENT
     # the two-call form validates the same way
     assert L.qgemm_pack_a(16, 0, 4, 32, None, 4096, need - 1, None) == qnn.QNN_ERR_INVALID_ARG
     assert L.qgemm_pack_a(16, 0, 4, 24, None, 4096, need, None) == qnn.QNN_ERR_ALIGNMENT

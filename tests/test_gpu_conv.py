@@ -37,18 +37,28 @@ def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="re
     epi = qnn.epilogue(mode, relu=relu, out_dt=out_dt, z_out=z_out, zp_term=zp, M=Mv, Bq=Bq, D=D,
                        bias=bd, residual=resd, res_dt=res_dt, z_res=z_res, R=R)
     rows = N * OH * OW
-    if mode == "requant":
-        ob = OC // 2 if out_dt == "u4" else OC
-        O = t.full((N, OH, OW, ob), 0x5A, dtype=t.uint8, device="cuda")
-    elif mode == "dequant":
-        O = t.empty((N, OH, OW, OC), dtype=t.float32, device="cuda")
-    else:
-        O = t.empty((N, OH, OW, OC), dtype=t.int32, device="cuda")
-    O32 = t.zeros((N, OH, OW, OC), dtype=t.int32, device="cuda")
     Id = dev(I_pk)
-    fn = qnn.qconv_u4s4 if u4 else qnn.qconv_u8s8
-    fn(Id, z_in, Wp, g, epi, O, O32)
-    assert qnn.qnn_check_device_error() == qnn.QNN_OK
+    # u4: both paths -- the packed input re-encoded inside the conv kernel, and
+    # the input expanded into a workspace (pre-filled with 0xFF) read by TMA
+    outs = []
+    for path in (("fused", "workspace") if u4 else ("fused",)):
+        if mode == "requant":
+            ob = OC // 2 if out_dt == "u4" else OC
+            O = t.full((N, OH, OW, ob), 0x5A, dtype=t.uint8, device="cuda")
+        elif mode == "dequant":
+            O = t.empty((N, OH, OW, OC), dtype=t.float32, device="cuda")
+        else:
+            O = t.empty((N, OH, OW, OC), dtype=t.int32, device="cuda")
+        O32 = t.zeros((N, OH, OW, OC), dtype=t.int32, device="cuda")
+        if path == "workspace":
+            ws = t.full((qnn.qnn_conv_workspace_bytes(g, "u4"),), 0xFF, dtype=t.uint8, device="cuda")
+            qnn.qconv_u4s4(Id, z_in, Wp, g, epi, O, O32, workspace=ws)
+        elif u4:
+            qnn.qconv_u4s4(Id, z_in, Wp, g, epi, O, O32)
+        else:
+            qnn.qconv_u8s8(Id, z_in, Wp, g, epi, O, O32)
+        assert qnn.qnn_check_device_error() == qnn.QNN_OK
+        outs.append((path, O, O32))
 
     # oracle side
     if u4:
@@ -76,26 +86,29 @@ def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="re
             a = oracle.conv_acc_direct(sub, Wc, z_in, (pad, pad), (st, st))
             acc_all.append(a[oy * OW + ox])
         acc = np.stack(acc_all)
-    got32 = host(O32).reshape(rows, OC)[sel]
-    assert np.array_equal(got32, acc), f"{(got32 != acc).sum()} accumulator mismatches"
-    Og = host(O)
-    if mode == "s32":
-        assert np.array_equal(Og.reshape(rows, OC)[sel], acc)
-        return acc
     if mode == "dequant":
         y = oracle.dequant_epilogue(acc, D_o, bias)
-        assert np.array_equal(f32_bits(Og.reshape(rows, OC)[sel]), f32_bits(y))
-        return acc
-    res_codes = None
-    if res is not None:
-        if res_dt == "u4":
-            res_codes = oracle.unpack_nibbles(res, signed=False).reshape(rows, OC)[sel]
+    elif mode == "requant":
+        res_codes = None
+        if res is not None:
+            if res_dt == "u4":
+                res_codes = oracle.unpack_nibbles(res, signed=False).reshape(rows, OC)[sel]
+            else:
+                res_codes = res.reshape(rows, OC)[sel].astype(np.int32)
+        q = oracle.requant(acc, M_o, Bq_o, out_dt, relu=relu, res=res_codes, z_res=z_res, R=R,
+                           z_out=z_out)
+        exp = oracle.pack_nibbles(q) if out_dt == "u4" else oracle.pack_bytes(q)
+    for path, O, O32 in outs:
+        got32 = host(O32).reshape(rows, OC)[sel]
+        assert np.array_equal(got32, acc), f"{path}: {(got32 != acc).sum()} accumulator mismatches"
+        Og = host(O)
+        if mode == "s32":
+            assert np.array_equal(Og.reshape(rows, OC)[sel], acc), path
+        elif mode == "dequant":
+            assert np.array_equal(f32_bits(Og.reshape(rows, OC)[sel]), f32_bits(y)), path
         else:
-            res_codes = res.reshape(rows, OC)[sel].astype(np.int32)
-    q = oracle.requant(acc, M_o, Bq_o, out_dt, relu=relu, res=res_codes, z_res=z_res, R=R, z_out=z_out)
-    exp = oracle.pack_nibbles(q) if out_dt == "u4" else oracle.pack_bytes(q)
-    got = Og.reshape(rows, -1)[sel]
-    assert np.array_equal(got, exp), f"{(got != exp).sum()} output bytes differ"
+            got = Og.reshape(rows, -1)[sel]
+            assert np.array_equal(got, exp), f"{path}: {(got != exp).sum()} output bytes differ"
     return acc
 
 
