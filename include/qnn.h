@@ -243,11 +243,12 @@ size_t qnn_conv_workspace_bytes(const qnn_conv_geom *g, qnn_dtype in_dt);
  * fp32 / int32 per epi->mode; O_s32: optional int32 acc_c.  C a multiple of
  * 32, OC even.
  * workspace: optional device scratch of at least qnn_conv_workspace_bytes(g,
- *   QNN_U4) bytes (16-byte aligned), owned by the caller and overwritten: with
- *   it, a pre-pass expands the input to one byte per channel and the
- *   convolution reads its taps with tensor-memory copies (the faster path);
- *   NULL: the convolution re-encodes the packed input itself.  Results are
- *   identical.  Calls in flight at the same time must not share a workspace. */
+ *   QNN_U4) bytes (16-byte aligned), owned by the caller and overwritten: for
+ *   filters with more than one tap, a pre-pass expands the input to one byte
+ *   per channel and the convolution reads its taps with tensor-memory copies
+ *   (the faster path there); 1x1 filters and NULL: the convolution re-encodes
+ *   the packed input itself.  Results are identical.  Calls in flight at the
+ *   same time must not share a workspace. */
 qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
                       const qnn_epilogue *epi, void *O, int32_t *O_s32, void *workspace,
                       size_t workspace_bytes, qnn_stream_t stream);

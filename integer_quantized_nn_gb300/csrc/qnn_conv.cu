@@ -379,19 +379,28 @@ inline size_t packed_w_u4_total(const qnn_conv_geom *g) { return colsum_offset(g
 // Bytes (= input channels) per operand row for C channels.
 inline int tma_cb(int C) { return C % 128 == 0 ? 128 : (C % 64 == 0 ? 64 : 32); }
 
-// Stages that fit in about 192 KB of shared memory.
-constexpr int tma_stages(int cb, int tbn)
+// Resident weights (64-column tiles, the whole filter bank in at most 64 KB).
+constexpr int TMA_B_RES = 65536;
+
+// Stages that fit in about 192 KB of shared memory with `t` K steps per
+// stage, streamed or resident weights.
+constexpr int tma_stages(int cb, int tbn, int t, bool resb)
 {
-    return (196608 / ((BM + tbn) * cb)) > 16 ? 16 : (196608 / ((BM + tbn) * cb));
+    const int per = t * BM * cb + (resb ? 0 : t * tbn * cb);
+    const int n = (196608 - (resb ? TMA_B_RES : 0)) / per;
+    return n > 15 ? 15 : n;
 }
 
-template <int CB, int NSTAGES>
+template <int CB, int TBN_, int T, bool RES>
 struct ConvTmaOp : OpBase {
     static constexpr bool TMA_A = true;
     static constexpr bool F8 = true;
     static constexpr int SCALE_LOG2 = 9;
     static constexpr int ROW = CB;
-    static constexpr int STAGES = NSTAGES;
+    static constexpr int SUB = T;
+    static constexpr bool RESB = RES;
+    static constexpr int B_RES_BYTES = RES ? TMA_B_RES : 0;
+    static constexpr int STAGES = tma_stages(CB, TBN_, T, RES);
     static constexpr int STG_BYTES = 16;
 
     __device__ static uint32_t a_bytes(const Params &p) { return (uint32_t)(CB * p.TW * p.TH * p.TN); }
@@ -405,7 +414,9 @@ struct ConvTmaOp : OpBase {
         int fh, fw, cblk;       // position of the next unit in K
     };
 
-    __device__ static void load_a(const Params &p, const UnitCursor &c, PState &ps, uint32_t dst, uint32_t bar)
+    // Box of K step t of unit c (steps are walked in order: t = 0 .. SUB - 1 of each unit).
+    __device__ static void load_a(const Params &p, const UnitCursor &c, PState &ps, int t, uint32_t dst,
+                                  uint32_t bar)
     {
         if (c.mb != ps.mb) {
             const int tx = c.mb % p.tiles_x;
@@ -417,7 +428,7 @@ struct ConvTmaOp : OpBase {
             ps.h0 = ty * p.TH * p.sh - p.ph;
             ps.n0 = tn * p.TN;
         }
-        if (c.ks == 0) {
+        if (c.ks == 0 && t == 0) {
             ps.fh = 0;
             ps.fw = 0;
             ps.cblk = 0;
@@ -462,14 +473,23 @@ struct ConvTmaOp : OpBase {
 };
 
 // Input expansion: 16 packed bytes (32 u4 codes, low nibble first) per thread
-// -> 32 bytes of e4m3((q - z) / 512) in channel order.
-__device__ __forceinline__ uint32_t e4m3_centred(uint32_t q, uint32_t z)
+// -> 32 bytes of e4m3((q - z) / 512) in channel order: the byte |q - z| with
+// the sign in bit 7.  Four codes are handled per 32-bit operation: biasing
+// every byte by 16 keeps q + 16 - z in 1..31, so bytes never borrow from one
+// another; bit 4 then tells q >= z.
+__device__ __forceinline__ uint32_t e4m3_centred4(uint32_t q4, uint32_t zz)
 {
-    return q >= z ? q - z : (0x80u | (z - q));
+    const uint32_t d = (q4 | 0x10101010u) - zz;               // q + 16 - z per byte
+    const uint32_t ge = (d >> 4) & 0x01010101u;               // 1 where q >= z
+    const uint32_t m = ge * 0xFFu;                            // 0xFF where q >= z
+    const uint32_t pos = d & 0x0F0F0F0Fu;                     // q - z (q >= z)
+    const uint32_t neg = ((0x10101010u - pos) & 0x0F0F0F0Fu) | 0x80808080u;  // 0x80 | (z - q) (q < z)
+    return (pos & m) | (neg & ~m);
 }
 
 __global__ void expand_u4_kernel(const uint8_t *__restrict__ in, int64_t n16, uint32_t z, uint8_t *__restrict__ out)
 {
+    const uint32_t zz = z * 0x01010101u;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
          i += (int64_t)gridDim.x * blockDim.x) {
         const uint4 v = ldg_nc_v4(in + i * 16);
@@ -477,15 +497,10 @@ __global__ void expand_u4_kernel(const uint8_t *__restrict__ in, int64_t n16, ui
         uint32_t o[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            uint32_t e[8];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const uint32_t byte = (w[j] >> (8 * b)) & 255u;
-                e[2 * b] = e4m3_centred(byte & 15u, z);
-                e[2 * b + 1] = e4m3_centred(byte >> 4, z);
-            }
-            o[2 * j] = e[0] | (e[1] << 8) | (e[2] << 16) | (e[3] << 24);
-            o[2 * j + 1] = e[4] | (e[5] << 8) | (e[6] << 16) | (e[7] << 24);
+            const uint32_t ev = e4m3_centred4(w[j] & 0x0F0F0F0Fu, zz);         // codes 0, 2, 4, 6
+            const uint32_t od = e4m3_centred4((w[j] >> 4) & 0x0F0F0F0Fu, zz);  // codes 1, 3, 5, 7
+            o[2 * j] = prmt(ev, od, 0x5140u);      // codes 0, 1, 2, 3
+            o[2 * j + 1] = prmt(ev, od, 0x7362u);  // codes 4, 5, 6, 7
         }
         uint4 *dst = reinterpret_cast<uint4 *>(out + i * 32);
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -589,18 +604,41 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return f;
 }
 
-template <int CB, int TBN>
-qnn_status conv_tma_launch(const Params &p, cudaStream_t s)
+template <int CB, int TBN, int T, bool RES>
+qnn_status conv_tma_launch(Params p, cudaStream_t s)
 {
-    return launch<ConvTmaOp<CB, tma_stages(CB, TBN)>, TBN, false>(p, s);
+    p.KT /= T;  // units per tile
+    p.chunk_steps = p.KT;
+    return launch<ConvTmaOp<CB, TBN, T, RES>, TBN, false>(p, s);
 }
 
+// 64-column tiles group 3, 2 or 1 K steps per unit and keep the weights
+// resident when they fit; wider tiles stream one step per unit.
 template <int TBN>
 qnn_status conv_tma_dispatch(const Params &p, int cb, cudaStream_t s)
 {
-    if (cb == 128) return conv_tma_launch<128, TBN>(p, s);
-    if (cb == 64) return conv_tma_launch<64, TBN>(p, s);
-    return conv_tma_launch<32, TBN>(p, s);
+    if constexpr (TBN == 64) {
+        const int steps = p.KT;
+        if ((int64_t)steps * TBN * cb <= TMA_B_RES) {
+            const int t = steps % 3 == 0 ? 3 : (steps % 2 == 0 ? 2 : 1);
+            if (cb == 128) {
+                if (t == 3) return conv_tma_launch<128, TBN, 3, true>(p, s);
+                if (t == 2) return conv_tma_launch<128, TBN, 2, true>(p, s);
+                return conv_tma_launch<128, TBN, 1, true>(p, s);
+            }
+            if (cb == 64) {
+                if (t == 3) return conv_tma_launch<64, TBN, 3, true>(p, s);
+                if (t == 2) return conv_tma_launch<64, TBN, 2, true>(p, s);
+                return conv_tma_launch<64, TBN, 1, true>(p, s);
+            }
+            if (t == 3) return conv_tma_launch<32, TBN, 3, true>(p, s);
+            if (t == 2) return conv_tma_launch<32, TBN, 2, true>(p, s);
+            return conv_tma_launch<32, TBN, 1, true>(p, s);
+        }
+    }
+    if (cb == 128) return conv_tma_launch<128, TBN, 1, false>(p, s);
+    if (cb == 64) return conv_tma_launch<64, TBN, 1, false>(p, s);
+    return conv_tma_launch<32, TBN, 1, false>(p, s);
 }
 
 template <template <int> class Op>
@@ -655,6 +693,9 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
     }
     p.nchunks = (p.KT + p.chunk_steps - 1) / p.chunk_steps;
     if (u4 && p.nchunks > 1) return QNN_ERR_UNSUPPORTED;
+    // the workspace path pays one expansion pass over the input, which only
+    // filters with several taps (each input pixel read by several of them) repay
+    if (workspace && g->FH * g->FW == 1) workspace = nullptr;
     if (workspace) {
         if (!u4) return QNN_ERR_UNSUPPORTED;
         if (workspace_bytes < (size_t)g->N * g->H * g->W * g->C) return QNN_ERR_INVALID_ARG;

@@ -122,7 +122,7 @@ struct GemmPackedOp : OpBase {
     static constexpr int SCALE_LOG2 = 0;
     static constexpr int STG_BYTES = 16;
     __device__ static uint32_t a_bytes(const Params &) { return A_STAGE_BYTES; }
-    __device__ static void load_a(const Params &p, const UnitCursor &c, PState &, uint32_t dst, uint32_t bar)
+    __device__ static void load_a(const Params &p, const UnitCursor &c, PState &, int, uint32_t dst, uint32_t bar)
     {
         bulk_g2s(dst, p.Ap + ((int64_t)c.mb * p.KT + c.ks) * A_STAGE_BYTES, A_STAGE_BYTES, bar);
     }
@@ -156,22 +156,34 @@ __global__ void __launch_bounds__(256) pack_a_kernel(const uint8_t *__restrict__
     }
     const int ks = g >> 2;
     const int c = (g & 3) * 2;
-    for (int m = blockIdx.y * blockDim.y + threadIdx.y; m < rows_pad; m += gridDim.y * blockDim.y) {
-        uint32_t h[8];
-        if (m < M && k0 < K) {
-            bytes_to_half(ldg_nc_v4(A + (size_t)m * (size_t)K + k0), flip, h);
-            if (PTF) {
+    const int stride = gridDim.y * blockDim.y;
+    // two rows per iteration, both loads issued before either is converted
+    for (int m = blockIdx.y * blockDim.y + threadIdx.y; m < rows_pad; m += 2 * stride) {
+        const int mr[2] = {m, m + stride};
+        uint4 v[2];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) h[j] = hmul2_u32(h[j], mul[j]);
+        for (int e = 0; e < 2; ++e)
+            v[e] = (mr[e] < M && k0 < K) ? ldg_nc_v4(A + (size_t)mr[e] * (size_t)K + k0) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            if (mr[e] >= rows_pad) break;
+            uint32_t h[8];
+            // rows past M and codes past K are zero images (fp16 +0)
+            if (mr[e] < M && k0 < K) {
+                bytes_to_half(v[e], flip, h);
+                if (PTF) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) h[j] = hmul2_u32(h[j], mul[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) h[j] = 0;
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) h[j] = 0;
+            const int r = mr[e] & (BM - 1);
+            uint8_t *row = out + ((size_t)((mr[e] / BM) * KT + ks) * BM + r) * ROW_BYTES;
+            *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4 *>(row + (((c + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
         }
-        const int r = m & (BM - 1);
-        uint8_t *row = out + ((size_t)((m / BM) * KT + ks) * BM + r) * ROW_BYTES;
-        *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4 *>(row + (((c + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
     }
 }
 
@@ -248,6 +260,7 @@ static qnn_status launch_pack_a(const uint8_t *A, int M, int K, int a_u8, const 
     const dim3 block(bx, by);
     const int gx = (groups + bx - 1) / bx;
     int gy = (rows_pad + by - 1) / by;
+    gy = (gy + 1) / 2;  // two rows per thread and iteration
     const int want = qnn::sm_count() * 32;  // enough blocks in flight; rows loop beyond
     if (gy > 65535) gy = 65535;
     if ((int64_t)gx * gy > want && gy > 1) {

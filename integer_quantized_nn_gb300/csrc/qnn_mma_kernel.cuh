@@ -103,6 +103,9 @@ struct Params {
 struct OpBase {
     static constexpr int STAGES = 4;
     static constexpr int ROW = 128;
+    static constexpr int SUB = 1;            // K steps (operand sub-tiles) per pipeline unit
+    static constexpr bool RESB = false;      // weights resident in shared memory for the whole kernel
+    static constexpr int B_RES_BYTES = 0;
     static constexpr bool ROTATE_K = true;  // each CTA starts its tiles' K walk at its own offset
     struct PState {};                        // producer-side state of a TMA_A Op
     struct RowInfo {                         // per-thread part of the row mapping
@@ -114,8 +117,9 @@ struct OpBase {
 
 template <class Op, int TBN>
 struct __align__(1024) Smem {
-    uint8_t a[Op::STAGES][BM * Op::ROW];
-    uint8_t b[Op::STAGES][TBN * Op::ROW];
+    uint8_t a[Op::STAGES][Op::SUB * BM * Op::ROW];
+    uint8_t b[Op::STAGES][Op::RESB ? 1024 : Op::SUB * TBN * Op::ROW];
+    uint8_t bres[Op::RESB ? Op::B_RES_BYTES : 1024];  // resident weights: [K step][TBN rows][ROW]
     uint4 stg[Op::STG_BYTES / 16];                   // converter staging ring (Op-specific)
     float cols[epi_warps<Op, TBN>()][4 * 32 * epi_max_pieces<Op, TBN>()];  // per epilogue warp: its columns' constants
     uint64_t full[Op::STAGES];   // 4 converter-warp arrivals (none with TMA_A) + the producer's expect_tx
@@ -123,6 +127,7 @@ struct __align__(1024) Smem {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t mma_done;
+    uint64_t bres_full;
     uint32_t tmem_base;
 };
 
@@ -265,6 +270,7 @@ __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
     const bool leader = (threadIdx.x & 31) == 0;
     constexpr int STAGES = Op::STAGES;
     constexpr int ROW = Op::ROW;
+    constexpr int SUB = Op::SUB;
     const uint32_t b0 = smem_u32(&s.b[0][0]);
     UnitCursor c;
     c.begin(p, Op::ROTATE_K);
@@ -272,6 +278,18 @@ __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
     bool ok = true;
     bool ready = false;
     int j = 0;
+    if constexpr (Op::RESB) {
+        // the whole (single) weight block, once: K step ks -> bres + ks * TBN * ROW
+        if (leader && units > 0) {
+            const int steps = p.KT * SUB;
+            const uint32_t bar = smem_u32(&s.bres_full);
+            mbar_arrive_expect_tx(bar, (uint32_t)(steps * TBN * ROW));
+            for (int k = 0; k < steps; ++k)
+                bulk_g2s(smem_u32(&s.bres[0]) + k * (TBN * ROW), p.Bp + (int64_t)k * (gemm::BN * ROW), TBN * ROW,
+                         bar);
+        }
+        __syncwarp();
+    }
     for (; j < units; ++j, c.next(p)) {
         const int stage = j % STAGES;
         const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
@@ -284,16 +302,26 @@ __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
         if (leader) {
             // columns n0 .. n0 + TBN - 1 live in the 256-row packed block n0 / 256
             const int n0 = c.nb * TBN;
-            const uint8_t *src = p.Bp + ((int64_t)(n0 / gemm::BN) * p.KT + c.ks) * (gemm::BN * ROW) +
-                                 (int64_t)(n0 % gemm::BN) * ROW;
             const uint32_t bar = smem_u32(&s.full[stage]);
+            constexpr uint32_t B_BYTES = Op::RESB ? 0u : (uint32_t)(SUB * TBN * ROW);
             if constexpr (Op::TMA_A) {
-                mbar_arrive_expect_tx(bar, TBN * ROW + Op::a_bytes(p));
-                Op::load_a(p, c, ps, smem_u32(&s.a[stage][0]), bar);
+                mbar_arrive_expect_tx(bar, B_BYTES + SUB * Op::a_bytes(p));
+#pragma unroll
+                for (int t = 0; t < SUB; ++t)
+                    Op::load_a(p, c, ps, t, smem_u32(&s.a[stage][0]) + t * (BM * ROW), bar);
             } else {
-                mbar_arrive_expect_tx(bar, TBN * ROW);
+                mbar_arrive_expect_tx(bar, B_BYTES);
             }
-            bulk_g2s(b0 + stage * (TBN * ROW), src, TBN * ROW, bar);
+            if constexpr (!Op::RESB) {
+#pragma unroll
+                for (int t = 0; t < SUB; ++t) {
+                    // columns n0 .. n0 + TBN - 1 of K step ks live in the 256-row packed block n0 / 256
+                    const int ks = c.ks * SUB + t;
+                    const uint8_t *src = p.Bp + ((int64_t)(n0 / gemm::BN) * p.KT * SUB + ks) * (gemm::BN * ROW) +
+                                         (int64_t)(n0 % gemm::BN) * ROW;
+                    bulk_g2s(b0 + stage * (SUB * TBN * ROW) + t * (TBN * ROW), src, TBN * ROW, bar);
+                }
+            }
         }
         ready = __all_sync(0xffffffffu, probe) && jn < units;
     }
@@ -318,10 +346,14 @@ __device__ void mma_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32
     constexpr int STAGES = Op::STAGES;
     constexpr int ROW = Op::ROW;
     constexpr int KSLICES = ROW / 32;  // one MMA per 32-byte K slice of a row
+    constexpr int SUB = Op::SUB;
     const bool leader = (threadIdx.x & 31) == 0;
     const int units = my_tiles * p.KT;
     const uint64_t adesc0 = sdesc_sw(smem_u32(&s.a[0][0]), ROW);
-    const uint64_t bdesc0 = sdesc_sw(smem_u32(&s.b[0][0]), ROW);
+    const uint64_t bdesc0 = Op::RESB ? sdesc_sw(smem_u32(&s.bres[0]), ROW) : sdesc_sw(smem_u32(&s.b[0][0]), ROW);
+    if constexpr (Op::RESB) {
+        if (units > 0 && !warp_wait(smem_u32(&s.bres_full), 0u, p.status)) return;
+    }
     int stage = 0;
     uint32_t sph = 0;  // phase of the current stage's full barrier
     uint32_t u = 0;  // accumulation chunk counter
@@ -336,16 +368,23 @@ __device__ void mma_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32
         tc_fence_after();
         if (leader) {
             // descriptor start addresses are in 16-byte units: +2 per 32-byte K slice
-            const uint64_t ad = adesc0 + (uint64_t)(stage * ((BM * ROW) >> 4));
-            const uint64_t bd = bdesc0 + (uint64_t)(stage * ((TBN * ROW) >> 4));
+            const uint64_t ad = adesc0 + (uint64_t)(stage * ((SUB * BM * ROW) >> 4));
+            // streamed weights sit in the stage; resident ones are indexed by the K step
+            const uint64_t bd = Op::RESB ? bdesc0 + (uint64_t)(kl * SUB * ((TBN * ROW) >> 4))
+                                         : bdesc0 + (uint64_t)(stage * ((SUB * TBN * ROW) >> 4));
             const uint32_t d = tmem + abuf * TBN;
 #pragma unroll
-            for (int kk = 0; kk < KSLICES; ++kk) {
-                const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-                if (Op::F8)
-                    mma_f8f6f4_ss(d, ad + 2 * kk, bd + 2 * kk, IDESC, acc);
-                else
-                    mma_f16_ss(d, ad + 2 * kk, bd + 2 * kk, IDESC, acc);
+            for (int t = 0; t < SUB; ++t) {
+#pragma unroll
+                for (int kk = 0; kk < KSLICES; ++kk) {
+                    const uint32_t acc = (first && t == 0 && kk == 0) ? 0u : 1u;
+                    const uint64_t at = ad + (uint64_t)(t * ((BM * ROW) >> 4)) + 2 * kk;
+                    const uint64_t bt = bd + (uint64_t)(t * ((TBN * ROW) >> 4)) + 2 * kk;
+                    if (Op::F8)
+                        mma_f8f6f4_ss(d, at, bt, IDESC, acc);
+                    else
+                        mma_f16_ss(d, at, bt, IDESC, acc);
+                }
             }
             mma_commit(smem_u32(&s.empty[stage]));
             if (last) mma_commit(smem_u32(&s.acc_full[abuf]));
@@ -784,6 +823,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
             mbar_init(smem_u32(&s.acc_empty[i]), epi_warps<Op, TBN>());
         }
         mbar_init(smem_u32(&s.mma_done), 1);
+        mbar_init(smem_u32(&s.bres_full), 1);
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
