@@ -40,7 +40,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # the headline GEMM kernel, from the ncu capture summarised in
 # profiles/qgemm_vit_fc1.md, valid only for the kernel sources it was taken on
 # (hash of integer_quantized_nn_gb300/csrc/*); reported as null otherwise.
-TRAFFIC_NCU = {"csrc_sha256_16": "bbe5a8b6d0c89b5f", "bytes": 14527232 + 55808}
+TRAFFIC_NCU = {"csrc_sha256_16": "3275bd38f1cdb9a2", "bytes": 24322304 + 159744}
 
 
 def csrc_hash():
