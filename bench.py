@@ -2,9 +2,10 @@
 
 A step is one quantized GEMM (u8 activations with zero point x s8 per-channel
 weights, int32 accumulation, fused requant to int8) on the ViT-B MLP fc1
-layer: M = 64 x 197 tokens = 12608, K = 768, N = 3072, run as its two kernels
-(qgemm_pack_a: A re-encoded into the workspace; qgemm_s8_packed: the GEMM),
-timed apart with events so that the roofline line holds the GEMM kernel alone.
+layer: M = 64 x 197 tokens = 12608, K = 768, N = 3072 -- one qgemm_s8 call with
+a workspace (the A pre-pass kernel, then the GEMM kernel).  A second loop runs
+the two kernels as separate calls with events around each, for the roofline
+line (the GEMM kernel alone) and the pre-pass figures.
 Inputs are resident in HBM; L2 is flushed (a 256 MiB write) between timed
 steps, outside the timed events.  The line also carries the quantize GB/s of a 1 GiB fp32 -> s8
 per-row quantize and the other layer shapes as extras.
@@ -242,7 +243,12 @@ def run_gpu(args):
     epi = qnn.epilogue("requant", zp_term=g["zp"], M=g["M"], Bq=g["Bq"], out_dt="s8")
     ws_buf = torch.empty(qnn.qnn_gemm_workspace_bytes(M, K), dtype=torch.uint8, device=device)
 
-    # a step: the A pre-pass kernel, then the GEMM kernel (timed apart)
+    # a step: one qgemm_s8 call with the workspace -- the A pre-pass kernel, then the GEMM
+    # kernel launched as its programmatic dependent (its launch overlaps the pre-pass tail)
+    def step():
+        qnn.qgemm_s8(g["A"], "u8", g["Bp"], M, N, K, epi, C, workspace=ws_buf, stream=stream)
+
+    # the same two kernels as separate calls, for each kernel's own duration
     def pack():
         qnn.qgemm_pack_a(g["A"], "u8", M, K, ws_buf, stream=stream)
 
@@ -256,11 +262,16 @@ def run_gpu(args):
     torch.cuda.synchronize()
     dist.barrier()
     t_wall0 = time.time()
-    times, (t_pack, t_gemm) = time_split(torch, [pack, gemm], args.steps, args.warmup, flush, stream)
+    times = time_steps(torch, step, args.steps, args.warmup, flush, stream)
     torch.cuda.synchronize()
     dist.barrier()
     t_wall1 = time.time()
-    clocks = ClockSampler.summarize(clk.stop(), t_wall0, t_wall1)
+    # second loop, same steps and flushes: events around each kernel (the event between them
+    # also stops the dependent-launch overlap, so this loop's steps are a little longer)
+    _, (t_pack, t_gemm) = time_split(torch, [pack, gemm], args.steps, 1, flush, stream)
+    torch.cuda.synchronize()
+    t_wall2 = time.time()
+    clocks = ClockSampler.summarize(clk.stop(), t_wall0, t_wall2)
     st = qnn.qnn_check_device_error()
     if st != qnn.QNN_OK:
         raise RuntimeError(f"device status: {qnn.status_string(st)}")
@@ -272,20 +283,56 @@ def run_gpu(args):
     pack_ms = sum(t_pack) / args.steps
     pack_bytes = M * K + qnn.qnn_gemm_workspace_bytes(M, K)
 
-    # ---- e2e: host buffers, copies inside the timed region
-    A_h = torch.from_numpy(np.ascontiguousarray(w["A"])).pin_memory()
-    C_h = torch.empty((M, N), dtype=torch.uint8).pin_memory()
-    A_d = torch.empty_like(g["A"])
-
-    def e2e_step():
-        A_d.copy_(A_h, non_blocking=True)
-        qnn.qgemm_s8(A_d, "u8", g["Bp"], M, N, K, epi, C, workspace=ws_buf, stream=stream)
-        C_h.copy_(C, non_blocking=True)
-
+    # ---- e2e: host buffers, every step's copies inside the timed region.  Steps are
+    # pipelined as a server would run them: step i's H2D copy (its own pinned input
+    # buffer), its qgemm_s8 call and its D2H copy of the result run on three streams,
+    # so step i's GEMM overlaps step i-1's D2H and step i+1's H2D (two device buffer
+    # sets); an L2 flush (160 MiB write) precedes every GEMM on the compute stream and
+    # counts inside the timed region.
     e2e_steps = max(3, min(args.steps, 200))
-    e2e_times = time_steps(torch, e2e_step, e2e_steps, max(1, args.warmup), flush, stream)
-    e2e_ms = dist.max(sum(e2e_times)) / e2e_steps
+    A_h = [torch.from_numpy(np.ascontiguousarray(w["A"])).pin_memory() for _ in range(2)]
+    C_h = [torch.empty((M, N), dtype=torch.uint8).pin_memory() for _ in range(2)]
+    A_d = [torch.empty_like(g["A"]) for _ in range(2)]
+    C_d = [torch.empty((M, N), dtype=torch.uint8, device=device) for _ in range(2)]
+    e2e_flush = torch.empty(160 << 20, dtype=torch.uint8, device=device)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "gemm", "d2h")}
+
+    def e2e_loop(n):
+        for i in range(n):
+            b = i % 2
+            s_in.wait_event(ev["gemm"][b])        # A_d[b] free again
+            with torch.cuda.stream(s_in):
+                A_d[b].copy_(A_h[b], non_blocking=True)
+            ev["h2d"][b].record(s_in)
+            stream.wait_event(ev["h2d"][b])
+            stream.wait_event(ev["d2h"][b])       # C_d[b] free again
+            e2e_flush.fill_(i & 255)
+            qnn.qgemm_s8(A_d[b], "u8", g["Bp"], M, N, K, epi, C_d[b], workspace=ws_buf, stream=stream)
+            ev["gemm"][b].record(stream)
+            s_out.wait_event(ev["gemm"][b])
+            with torch.cuda.stream(s_out):
+                C_h[b].copy_(C_d[b], non_blocking=True)
+            ev["d2h"][b].record(s_out)
+
+    e2e_loop(max(2, args.warmup))
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    s_in.wait_event(t_start)
+    s_out.wait_event(t_start)
+    e2e_loop(e2e_steps)
+    stream.wait_stream(s_out)
+    stream.wait_stream(s_in)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist.max(t_start.elapsed_time(t_end)) / e2e_steps
     e2e_value = dist.ws * flops / (e2e_ms * 1e-3) / 1e12
+    st = qnn.qnn_check_device_error()
+    if st != qnn.QNN_OK:
+        raise RuntimeError(f"device status: {qnn.status_string(st)}")
+    if not torch.equal(C_h[(e2e_steps - 1) % 2], C.cpu()):
+        raise RuntimeError("end-to-end output differs from the device-timed output")
 
     extras = {}
     if not args.no_extras and dist.rank == 0:
@@ -315,6 +362,8 @@ def run_gpu(args):
                      "peak_kind": f"{pk_kind} bf16 dense burst (the f16 MMA kind runs at the bf16 rate)",
                      "kernel": "qmma_kernel<GemmPackedOp,256,false>",
                      "kernel_ms": round(gemm_ms, 5),
+                     "kernel_timing": "CUDA events around the GEMM kernel alone, in a second loop of "
+                                      "the same steps right after the timed one (same L2 flushes)",
                      "algorithmic": "2*M*N*K int ops per launch"},
         "prepass": {"kernel": "pack_a_kernel<false>", "ms": round(pack_ms, 5),
                     "bytes": pack_bytes, "GB/s": round(pack_bytes / (pack_ms * 1e-3) / 1e9, 1),
@@ -322,7 +371,9 @@ def run_gpu(args):
                     "algorithmic": "M*K code bytes read + the fp16 image written"},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 3), "unit": "TOPS", "h2d_bytes_per_step": M * K,
-                "d2h_bytes_per_step": M * N},
+                "d2h_bytes_per_step": M * N, "ms_per_step": round(e2e_ms, 5),
+                "pipelining": "H2D / qgemm_s8 / D2H on three streams, two buffer sets; an L2 flush "
+                              "before every GEMM inside the timed region"},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "extras": extras,

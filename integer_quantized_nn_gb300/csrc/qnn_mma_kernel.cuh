@@ -834,6 +834,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
+    // launched as a programmatic dependent (TMA_A Ops): no thread reads global memory before
+    // the preceding kernel on the stream has completed; only the prologue above overlaps it
+    if constexpr (Op::TMA_A) grid_dependency_wait();
 
     const int my_tiles =
         (blockIdx.x < p.num_tiles) ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -894,6 +897,27 @@ qnn_status launch(Params p, cudaStream_t stream)
     p.num_tiles = p.num_m * ((p.N + TBN - 1) / TBN);
     int grid = qnn::sm_count();
     if (grid > p.num_tiles) grid = p.num_tiles;
+    if constexpr (Op::TMA_A) {
+        // A comes from the kernel launched just before on the stream (the pre-pass, or
+        // whatever wrote the packed image): launched as its programmatic dependent, this
+        // kernel's launch and prologue overlap that kernel's tail; every thread waits for
+        // it (griddepcontrol.wait) before touching global memory.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = SMEM;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, qmma_kernel<Op, TBN, MULTI>, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return QNN_ERR_CUDA;
+        }
+        return launch_status();
+    }
     qmma_kernel<Op, TBN, MULTI><<<grid, NUM_THREADS, SMEM, stream>>>(p);
     return launch_status();
 }

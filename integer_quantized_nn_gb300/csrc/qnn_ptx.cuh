@@ -250,6 +250,11 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// Programmatic dependent launch: block until the grid this one depends on (the
+// preceding kernel on the stream) has completed and its writes are visible.
+// Returns at once when the kernel was not launched as a dependent.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Instruction descriptor: fp32 accumulator, K-major A and B, M x N tile.
 // a_fmt / b_fmt: kind::f16 -> 0 f16, 1 bf16; kind::f8f6f4 -> 0 e4m3, 1 e5m2,
 // 3 e2m3, 4 e3m2, 5 e2m1.
