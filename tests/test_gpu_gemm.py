@@ -275,3 +275,41 @@ def test_device_wait_timeout_reported():
     t = torch()
     x = t.ones(16, device="cuda")
     assert float(x.sum()) == 16.0
+
+
+def test_gemm_back_to_back_on_one_stream(oracle):
+    """Weights prepacked, epilogue constants folded, A packed and the GEMM run
+    back to back on one stream with no host synchronisation in between: the
+    GEMM (launched as a programmatic dependent of the preceding kernel) must
+    not read the fold's or the pre-pass's outputs before they are complete."""
+    t = torch()
+    rng = np.random.default_rng(19)
+    M, N, K = 1000, 512, 768
+    A = rng.integers(0, 256, size=(M, K)).astype(np.uint8)
+    B = rng.integers(-128, 128, size=(N, K)).astype(np.int8)
+    s_w = rng.uniform(1e-3, 1e-2, size=N).astype(np.float32)
+    bias = rng.normal(0, 1, size=N).astype(np.float32)
+    Ad, Bd, swd, bd = dev(A), dev(B), dev(s_w), dev(bias)
+    t.cuda.synchronize()
+    from _util import aligned_empty
+    Bp = aligned_empty(qnn.qnn_gemm_packed_b_bytes(N, K))
+    colsum = t.empty(N, dtype=t.int32, device="cuda")
+    zp = t.empty(N, dtype=t.int32, device="cuda")
+    Mv = t.empty(N, dtype=t.float32, device="cuda")
+    Bq = t.empty(N, dtype=t.float32, device="cuda")
+    ws = t.full((qnn.qnn_gemm_workspace_bytes(M, K),), 0xFF, dtype=t.uint8, device="cuda")
+    C = t.full((M, N), 0x5A, dtype=t.uint8, device="cuda")
+    C2 = t.full((M, N), 0x5A, dtype=t.uint8, device="cuda")
+    # no host synchronisation from here to the comparison
+    qnn.qgemm_prepack_b(Bd, Bp, colsum)
+    qnn.q_fold_epilogue(N, "u8", 131, colsum, 0.02, swd, 0.05, bias=bd, zp_term=zp, M=Mv, Bq=Bq)
+    epi = qnn.epilogue("requant", out_dt="s8", zp_term=zp, M=Mv, Bq=Bq)
+    qnn.qgemm_pack_a(Ad, "u8", M, K, ws)
+    qnn.qgemm_s8_packed(ws, "u8", Bp, M, N, K, epi, C)
+    qnn.qgemm_s8(Ad, "u8", Bp, M, N, K, epi, C2, workspace=ws)
+    assert qnn.qnn_check_device_error() == qnn.QNN_OK
+    zp_o, M_o, Bq_o, _, _ = oracle_fold(oracle, B, "u8", 131, 0.02, s_w, 0.05, bias)
+    acc = oracle.gemm_acc(A.astype(np.int32), B.astype(np.int32), 131)
+    exp = oracle.pack_bytes(oracle.requant(acc, M_o, Bq_o, "s8"))
+    assert np.array_equal(host(C), exp)
+    assert np.array_equal(host(C2), exp)
