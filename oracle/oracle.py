@@ -61,6 +61,12 @@ def lib() -> ctypes.CDLL:
         L.oracle_dequant_epilogue.argtypes = [vp, i64, i64, vp, vp, vp]
         L.oracle_conv_acc_direct.argtypes = [vp] * 2 + [ctypes.c_int] * 11 + [i32, vp]
         L.oracle_im2col.argtypes = [vp] + [ctypes.c_int] * 10 + [i32, vp]
+        L.oracle_lis_int_exp.restype = i64
+        L.oracle_lis_int_exp.argtypes = [i64, f32]
+        L.oracle_log_round.restype = ctypes.c_int
+        L.oracle_log_round.argtypes = [ctypes.c_uint64]
+        L.oracle_log_int_softmax.argtypes = [vp, i64, i64, f32, ctypes.c_int, vp]
+        L.oracle_attn_shift_v.argtypes = [vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
         L.oracle_set_threads.argtypes = [ctypes.c_int]
         L.oracle_get_threads.restype = ctypes.c_int
     return _lib
@@ -252,3 +258,42 @@ def im2col(I, fh, fw, z_in, pad=(1, 1), stride=(1, 1)):
                              stride[1], int(z_in), _p(cols))
     assert rc == 0
     return cols
+
+
+# ----------------------------------------------------------------------------
+# Log-Int-Softmax and the bit-shift attention product [FQ 3.3]
+
+def lis_int_exp(x: int, S: float) -> int:
+    """Integer exponential of one value x <= 0 (codes at scale S)."""
+    return int(lib().oracle_lis_int_exp(int(x), float(np.float32(S))))
+
+
+def log_round(v: int) -> int:
+    return int(lib().oracle_log_round(int(v)))
+
+
+def log_int_softmax(x, S: float, bits: int = 4):
+    """Rows along the last axis of int32 codes -> uint8 log2 codes (2^bits = masked)."""
+    x = _c(x, np.int32)
+    L = x.shape[-1]
+    rows = x.size // L if L else 0
+    out = np.empty(x.shape, np.uint8)
+    rc = lib().oracle_log_int_softmax(_p(x), rows, L, float(np.float32(S)), int(bits), _p(out))
+    if rc != 0:
+        raise ValueError(f"oracle_log_int_softmax: error {rc}")
+    return out
+
+
+def attn_shift_v(code, v, bits: int = 4):
+    """code [H, Lq, Lk] uint8, v [H, Lk, d] int -> int64 [H, Lq, d]:
+    sum_t 2^(2^bits - 1 - code) * v, masked codes (>= 2^bits) contributing 0."""
+    code = _c(code, np.uint8)
+    v = _c(v, np.int32)
+    H, Lq, Lk = code.shape
+    d = v.shape[-1]
+    assert v.shape == (H, Lk, d)
+    out = np.empty((H, Lq, d), np.int64)
+    rc = lib().oracle_attn_shift_v(_p(code), _p(v), H, Lq, Lk, d, int(bits), _p(out))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_shift_v: error {rc}")
+    return out

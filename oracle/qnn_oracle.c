@@ -20,7 +20,8 @@
  *         (zero-point formula split), conv 算子優化 (img2col / implicit GEMM,
  *         Fig. 5; column permutation, Fig. 8).
  *   [FQ]  "首个完全量化Vision Transformer的方法FQ-ViT" (aijishu.com):
- *         3.2 Power-of-Two Factor.
+ *         3.2 Power-of-Two Factor; 3.3 Log Int Softmax (Attention Map 的 Log2
+ *         量化, Softmax 的量化推理, Integer-only 推理, Softmax 的量化的实现).
  *
  * Readings of points the pages leave open are stated next to the code that
  * takes them.  Parity status: every function here is pinned by tests that do
@@ -374,5 +375,140 @@ int oracle_im2col(const int32_t *I, int n_, int h, int w, int c, int fh, int fw,
                     cols[p * K + ((int64_t)r * fw + t) * c + ic] = v;
                 }
     }
+    return OR_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * Log-Int-Softmax [FQ 3.3].  Each row of integer logit codes x (real values
+ * x * S) becomes a row of log2 codes k: the attention probability is 2^-k, or 0
+ * where k = 2^bits (the mask).  Steps, in the page's order:
+ *   1. x <- x - max(x) over the row (Softmax 的量化推理: subtract the maximum);
+ *   2. an integer exponential of every x (int_exp below) and their sum s;
+ *   3. v = round(s / e) for every element's exponential e (1 / probability);
+ *   4. k = log_round(v); k >= 2^bits is masked (probability 0).
+ * Readings (the page prints the algorithm as floating-point tensor code of an
+ * integer-only method):
+ *   - integer steps are exact integer arithmetic;
+ *   - the constants derived from S -- floor(-0.6931 / S), floor((b/a) / S),
+ *     floor((c/a) / S^2) -- are fp32 operations, as in the printed code (an fp32
+ *     scale; the coefficient ratios b/a and c/a computed in double, then rounded
+ *     to fp32 when combined with the scale);
+ *   - round(s / e) rounds the exact rational half to even;
+ *   - an element whose exponential is 0 has v = infinity: masked. */
+typedef struct {
+    int64_t x0_int, b_int, c_int;
+} lis_consts;
+
+static lis_consts lis_constants(float S)
+{
+    /* second-order approximation a r^2 + b r + c of exp on [-ln 2, 0] */
+    const double a = 0.35815147, b = 0.96963238, c = 1.0;
+    lis_consts k;
+    const float s2 = S * S;
+    k.x0_int = (int64_t)floorf((float)-0.6931 / S);
+    k.b_int = (int64_t)floorf((float)(b / a) / S);
+    k.c_int = (int64_t)floorf((float)(c / a) / s2);
+    return k;
+}
+
+/* Integer exponential of x <= 0 (Integer-only 推理): x is clamped to 30 * x0_int,
+ * split as x = q * x0_int + r with q = floor(x / x0_int) and r in (x0_int, 0], the
+ * polynomial z = r (r + b_int) + c_int evaluated on r, and z scaled by 2^(30 - q).
+ * The result times a S^2 / 2^30 approximates exp(x S). */
+int64_t oracle_lis_int_exp(int64_t x, float S)
+{
+    const lis_consts k = lis_constants(S);
+    const int64_t n = 30;
+    if (x < n * k.x0_int) x = n * k.x0_int;
+    /* floor(x / x0_int) for x <= 0 < -x0_int: the exact quotient is >= 0 */
+    const int64_t q = x / k.x0_int;  /* both non-positive: C truncation is the floor */
+    const int64_t r = x - k.x0_int * q;
+    const int64_t z = r * (r + k.b_int) + k.c_int;
+    const int64_t e = z * ((int64_t)1 << (n - q));
+    return e > 0 ? e : 0;
+}
+
+/* round(v) for v = num / den > 0, half to even, exact. */
+static uint64_t round_ratio_half_even(uint64_t num, uint64_t den)
+{
+    uint64_t q = num / den, rem = num % den;
+    if (2 * rem > den || (2 * rem == den && (q & 1))) ++q;
+    return q;
+}
+
+/* log_round [FQ 3.3, Softmax 的量化的实现]: big = floor(log2 v), plus one when
+ * v - 2^big >= 2^(big - 1); v >= 1.  Reading: evaluated exactly on the integer v
+ * (the printed code takes log2 in floating point). */
+int oracle_log_round(uint64_t v)
+{
+    int big = 0;
+    while (big < 63 && (v >> (big + 1)) != 0) ++big;
+    if (big >= 1 && v - ((uint64_t)1 << big) >= ((uint64_t)1 << (big - 1))) ++big;
+    return big;
+}
+
+/* The whole row operation; code[i] = k for k < 2^bits, else 2^bits (masked:
+ * probability 0).  Returns OR_ERR_ARG for a non-positive or non-finite S, bits
+ * outside 1..5, L <= 0 or constants with x0_int >= 0, b_int <= 0 or c_int <= 0
+ * (S too coarse), and OR_ERR_RANGE for c_int >= 2^31 (S finer than about 2^-15)
+ * or when L exponentials of the largest value, c_int * 2^30 each (the
+ * exponential of 0), could reach 2^64. */
+int oracle_log_int_softmax(const int32_t *x, int64_t rows, int64_t L, float S, int bits,
+                           uint8_t *code)
+{
+    if (!(S > 0.0f) || !isfinite(S) || bits < 1 || bits > 5 || L <= 0 || rows < 0)
+        return OR_ERR_ARG;
+    const lis_consts k = lis_constants(S);
+    if (k.x0_int >= 0 || k.c_int <= 0 || k.b_int <= 0) return OR_ERR_ARG;
+    if (k.c_int >= ((int64_t)1 << 31)) return OR_ERR_RANGE;
+    if ((unsigned __int128)k.c_int * ((uint64_t)1 << 30) * (uint64_t)L >> 64) return OR_ERR_RANGE;
+    const int kmax = 1 << bits;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const int32_t *xr = x + r * L;
+        int32_t mx = xr[0];
+        for (int64_t i = 1; i < L; ++i)
+            if (xr[i] > mx) mx = xr[i];
+        uint64_t s = 0;
+        for (int64_t i = 0; i < L; ++i) s += (uint64_t)oracle_lis_int_exp((int64_t)xr[i] - mx, S);
+        for (int64_t i = 0; i < L; ++i) {
+            const uint64_t e = (uint64_t)oracle_lis_int_exp((int64_t)xr[i] - mx, S);
+            int kk = kmax;
+            if (e != 0) {
+                kk = oracle_log_round(round_ratio_half_even(s, e));
+                if (kk > kmax) kk = kmax;
+            }
+            code[r * L + i] = (uint8_t)kk;
+        }
+    }
+    return OR_OK;
+}
+
+/* AttnQ x V as bit shifts [FQ 3.3, Attention Map 的 Log2 量化: the MatMul between
+ * the log2-quantized attention map and the value codes becomes shifts].  With
+ * attention probabilities 2^-k (k < 2^bits; k = 2^bits is zero):
+ *   out[i][j] = sum_t 2^(2^bits - 1 - k[i][t]) * v[t][j]     (int64, exact)
+ * i.e. 2^(2^bits - 1) times the product of the dequantized map and the value
+ * codes.  Reading (the page's equation is missing from the text): the product
+ * is kept exact, a left shift of v into the wider sum, rather than shifting v
+ * right and truncating. */
+int oracle_attn_shift_v(const uint8_t *code, const int32_t *v, int64_t heads, int64_t Lq, int64_t Lk,
+                        int64_t d, int bits, int64_t *out)
+{
+    if (bits < 1 || bits > 5) return OR_ERR_ARG;
+    const int64_t kmax = (int64_t)1 << bits;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t h = 0; h < heads; ++h)
+        for (int64_t i = 0; i < Lq; ++i) {
+            const uint8_t *cr = code + (h * Lq + i) * Lk;
+            for (int64_t j = 0; j < d; ++j) {
+                int64_t acc = 0;
+                for (int64_t t = 0; t < Lk; ++t) {
+                    if (cr[t] >= kmax) continue;
+                    acc += v[(h * Lk + t) * d + j] * ((int64_t)1 << (kmax - 1 - cr[t]));
+                }
+                out[(h * Lq + i) * d + j] = acc;
+            }
+        }
     return OR_OK;
 }
