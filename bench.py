@@ -489,6 +489,29 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
     conv_entry("conv3x3_u4s4_add_relu", workloads.conv_u4(), (64, 56, 56, 64, 64, 3, 1, 1))
     conv_entry("conv1x1_u4s4_relu", workloads.conv_u4(C=256, OC=64, F=1, pad=0, residual=False, tag=1),
                (64, 56, 56, 256, 64, 1, 0, 1))
+
+    # Log-Int-Softmax over ViT-B attention maps at batch 64, then the shift product with V
+    Bh, Lt, dh = 64 * 12, 197, 64
+    rows = Bh * Lt
+    xl = workloads.device_attention_logits(rows, Lt, 1234, device)
+    codes = torch.empty((rows, Lt), dtype=torch.uint8, device=device)
+    t = time_steps(torch, lambda: qnn.q_log_int_softmax(xl, rows, Lt, workloads.ATTN_S, 4, codes,
+                                                        stream=stream), steps, 3, flush, stream)
+    ms = statistics.median(t)
+    gbs = 5.0 * rows * Lt / (ms * 1e-3) / 1e9
+    out["log_int_softmax_vitb_b64"] = {"rows": rows, "L": Lt, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                       "frac_hbm": round(gbs / hbm, 4), "bytes": "4 B in + 1 B out /elem"}
+    vq = workloads.device_uniform_s8((Bh, Lt, dh), 77, device)
+    ov = torch.empty((Bh, Lt, dh), dtype=torch.int32, device=device)
+    t = time_steps(torch, lambda: qnn.q_attn_shift_v(codes, vq, Bh, Lt, Lt, dh, 4, ov, stream=stream),
+                   steps, 3, flush, stream)
+    ms = statistics.median(t)
+    byts = Bh * Lt * Lt + Bh * Lt * dh + 4 * Bh * Lt * dh
+    out["attn_shift_v_vitb_b64"] = {"heads": Bh, "Lq": Lt, "Lk": Lt, "d": dh, "ms": round(ms, 4),
+                                    "GMAC/s": round(Bh * Lt * Lt * dh / (ms * 1e-3) / 1e9, 1),
+                                    "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
+                                    "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
+    del xl, codes, vq, ov
     return out
 
 
@@ -570,6 +593,22 @@ def run_case(args):
         ws = None if getattr(args, "fused", False) else torch.empty(qnn.qnn_conv_workspace_bytes(gg, "u4"),
                                                                      dtype=torch.uint8, device=device)
         fn = lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, gg, epi, O, workspace=ws, stream=stream)  # noqa: E731
+    elif case in ("lis", "shift", "attn"):
+        Bh, Lt, dh = 64 * 12, 197, 64
+        xl = workloads.device_attention_logits(Bh * Lt, Lt, 1234, device)
+        codes = torch.empty((Bh * Lt, Lt), dtype=torch.uint8, device=device)
+        qnn.q_log_int_softmax(xl, Bh * Lt, Lt, workloads.ATTN_S, 4, codes, stream=stream)
+        if case == "lis":
+            fn = lambda: qnn.q_log_int_softmax(xl, Bh * Lt, Lt, workloads.ATTN_S, 4, codes,  # noqa: E731
+                                               stream=stream)
+        else:
+            vq = workloads.device_uniform_s8((Bh, Lt, dh), 77, device)
+            ov = torch.empty((Bh, Lt, dh), dtype=torch.int32, device=device)
+
+            def fn():
+                if case == "attn":
+                    qnn.q_log_int_softmax(xl, Bh * Lt, Lt, workloads.ATTN_S, 4, codes, stream=stream)
+                qnn.q_attn_shift_v(codes, vq, Bh, Lt, Lt, dh, 4, ov, stream=stream)
     else:
         raise SystemExit(f"unknown case {case}")
     t = time_steps(torch, fn, args.steps, args.warmup, flush, stream)
@@ -670,7 +709,8 @@ def main():
                     help="--case GEMMs / convs: no workspace (A re-encoded inside the kernel)")
     ap.add_argument("--case", default=None,
                     help="run one workload only (profiling): quantize, vit_fc1, square_4096, "
-                         "vitl_fc2, conv3x3, conv1x1, or gemm:M:N:K (u8 x s8 -> s8)")
+                         "vitl_fc2, conv3x3, conv1x1, gemm:M:N:K (u8 x s8 -> s8), lis, shift, "
+                         "attn (ViT-B b64 Log-Int-Softmax, shift product, both)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -257,6 +257,39 @@ qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed, const q
 qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
                       const qnn_epilogue *epi, void *O, int32_t *O_s32, qnn_stream_t stream);
 
+/* ---- Log-Int-Softmax attention [FQ 3.3] ------------------------------------ */
+
+/* Log-Int-Softmax [FQ 3.3: Softmax 的量化推理, Integer-only 推理, Softmax 的量化的实现]
+ * over `rows` rows of L int32 logit codes x (row-major [rows][L]; real value
+ * x * S, e.g. the int32 accumulator of Q K^T with S = s_q s_k / sqrt(d)).
+ * code (u8 [rows][L]) receives per element the log2 code k of its attention
+ * probability 2^-k, or 2^bits where the probability is quantized to 0:
+ *   x0 = floor(fp32(-0.6931) / S), b = floor(fp32(b'/a') / S),
+ *   c = floor(fp32(c'/a') / (S*S))  with (a', b', c') = (0.35815147, 0.96963238, 1),
+ *   the ratios in double, the divisions and S*S in fp32;
+ *   d = max(x - max(row), 30 x0), q = floor(d / x0), r = d - x0 q,
+ *   e = (r (r + b) + c) * 2^(30 - q)   (exact integers; 0 if negative);
+ *   s = sum of e over the row; v = round(s / e) (exact, half to even);
+ *   k = floor(log2 v), plus one when v - 2^k >= 2^(k-1); k >= 2^bits -> 2^bits.
+ * bits in 1..5.  Fails with QNN_ERR_INVALID_ARG for S not finite and positive,
+ * L <= 0, or S so coarse that x0 >= 0, b <= 0 or c <= 0; QNN_ERR_OVERFLOW_RISK
+ * when c >= 2^31 (S finer than about 2^-15) or L c 2^30 >= 2^64 (the row sum
+ * must fit 64 bits). */
+qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t L, float S, int bits,
+                             uint8_t *code, qnn_stream_t stream);
+
+/* The attention-times-value product with log2 codes as shifts [FQ 3.3,
+ * Attention Map 的 Log2 量化: with probabilities 2^-k the MatMul of the attention
+ * map and the value codes becomes a BitShift]:
+ *   out[b][i][j] = sum_t 2^(N - code[b][i][t]) * v[b][t][j],  N = 2^bits - 1,
+ * masked codes (>= 2^bits) contributing 0 -- 2^N times the product of the
+ * dequantized map and v, exact in int32 (the real product is out * 2^-N * s_v).
+ * code: u8 [batch][Lq][Lk] (q_log_int_softmax's output); v: s8 [batch][Lk][d];
+ * out: int32 [batch][Lq][d].  bits in 1..4; d % 16 == 0; batch <= 65535.
+ * QNN_ERR_OVERFLOW_RISK when Lk * 128 * 2^N > 2^31 (Lk <= 512 at 4 bits). */
+qnn_status q_attn_shift_v(const uint8_t *code, const int8_t *v, int64_t batch, int Lq, int Lk, int d,
+                          int bits, int32_t *out, qnn_stream_t stream);
+
 /* ---- status ----------------------------------------------------------------- */
 
 const char *qnn_status_string(qnn_status s);

@@ -81,6 +81,8 @@ def _declare(L):
         "qnn_conv_workspace_bytes": (sz, [vp, c_int]),
         "qconv_u4s4": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "qconv_u8s8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
+        "q_log_int_softmax": (c_int, [vp, i64, i64, f32, c_int, vp, vp]),
+        "q_attn_shift_v": (c_int, [vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp]),
         "qnn_status_string": (ctypes.c_char_p, [c_int]),
         "qnn_check_device_error": (c_int, [vp]),
         "qnn_selftest_wait_timeout": (c_int, [ctypes.c_uint64, vp]),
@@ -282,6 +284,20 @@ def qconv_u8s8(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None
     _check(_SYMBOLS["qconv_u8s8"](_ptr(I), int(z_in), _ptr(W_packed), ctypes.byref(g),
                                   ctypes.byref(epi), _ptr(O), _ptr(O_s32), _stream(stream)),
            "qconv_u8s8")
+
+
+def q_log_int_softmax(x, rows: int, L: int, S: float, bits: int, code, stream=None):
+    """Log-Int-Softmax of int32 rows x [rows, L] into u8 log2 codes (2^bits: masked)."""
+    load()
+    _check(_SYMBOLS["q_log_int_softmax"](_ptr(x), int(rows), int(L), float(S), int(bits), _ptr(code),
+                                          _stream(stream)), "q_log_int_softmax")
+
+
+def q_attn_shift_v(code, v, batch: int, Lq: int, Lk: int, d: int, bits: int, out, stream=None):
+    """out[b, i, j] = sum_t 2^(2^bits - 1 - code[b, i, t]) v[b, t, j] (int32)."""
+    load()
+    _check(_SYMBOLS["q_attn_shift_v"](_ptr(code), _ptr(v), int(batch), int(Lq), int(Lk), int(d),
+                                       int(bits), _ptr(out), _stream(stream)), "q_attn_shift_v")
 
 
 def qnn_check_device_error(stream=None) -> int:

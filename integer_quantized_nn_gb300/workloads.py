@@ -17,6 +17,8 @@ Workloads (the layer shapes of the pages' models stand in for their datasets):
                   power-of-two factors (5% outlier channels x40)
   gemm_square   : s8 x s8 square GEMMs M=N=K, requant to s8
   quant_rows    : fp32 -> s8 per-row symmetric quantize of a 16384^2 tensor
+  vit_attention : ViT-B self-attention maps (12 heads, 197 tokens, head dim 64):
+                  int32 logit codes of Q K^T, s8 value codes, for Log-Int-Softmax
 """
 from __future__ import annotations
 
@@ -24,7 +26,7 @@ import math
 import numpy as np
 
 # workload ids (seed = 1000 * id + tensor id)
-GEMM_SYM, VIT_FC1, CONV_U4, VITL_PTF, SQUARE = 1, 2, 3, 4, 5
+GEMM_SYM, VIT_FC1, CONV_U4, VITL_PTF, SQUARE, ATTN = 1, 2, 3, 4, 5, 6
 
 
 def rng(workload: int, tensor: int) -> np.random.Generator:
@@ -142,6 +144,35 @@ def quant_rows(rows=16384, cols=16384, tag=0):
     x = rng(SQUARE, 10 * tag + 5).standard_normal(size=(rows, cols), dtype=np.float32)
     scale = (np.abs(x).max(axis=1) / np.float32(127.0)).astype(np.float32)
     return dict(x=x, scale=scale)
+
+
+# Scale of the attention logit codes: s_q s_k / sqrt(64) with s_q = s_k = 0.04
+# (a product of the int8 Q and K codes over the head dimension 64).
+ATTN_S = float(np.float32(0.04 * 0.04 / 8.0))
+
+
+def vit_attention(B=4, H=12, L=197, d=64, tag=0):
+    """Attention logits as int32 codes at scale ATTN_S: real logits N(0, 2.5) per
+    element (a spread whose softmax over 197 tokens leaves most probabilities
+    below 1/16 and a few near the top), plus one sink column (token 0, the class
+    token) raised by 4; value codes round(N(0, 40)) clipped to s8.
+    x: int32 [B*H, L, L]; v: int8 [B*H, L, d]."""
+    g = rng(ATTN, 10 * tag + 0)
+    z = g.normal(0.0, 2.5, size=(B * H, L, L))
+    z[:, :, 0] += 4.0
+    x = np.rint(z / ATTN_S).astype(np.int32)
+    v = _normal_codes(rng(ATTN, 10 * tag + 1), 0.0, 40.0, -128, 127, (B * H, L, d), np.int8)
+    return dict(x=x, v=v, S=ATTN_S, bits=4)
+
+
+def device_attention_logits(rows, L, seed, device):
+    """The vit_attention logit distribution drawn on the device (int32 [rows, L])."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    z = torch.randn((rows, L), generator=g, device=device, dtype=torch.float32) * 2.5
+    z[:, 0] += 4.0
+    return torch.round(z / ATTN_S).to(torch.int32)
 
 
 def device_uniform_s8(shape, seed, device):

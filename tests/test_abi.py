@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     for n in ("q_quantize", "q_dequantize", "qgemm_prepack_b", "q_fold_epilogue", "qgemm_s8",
               "qnn_gemm_workspace_bytes", "qgemm_pack_a", "qgemm_s8_packed", "qgemm_s8_static_scratch",
               "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_conv_workspace_bytes",
-              "qnn_status_string",
+              "q_log_int_softmax", "q_attn_shift_v", "qnn_status_string",
               "qnn_check_device_error"):
         assert n in names
 
@@ -101,6 +101,31 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert L.q_fold_epilogue(8, 1, 300, 16, 1.0, 16, 0, None, 1.0, 16, None, None, None,
                              None) == qnn.QNN_ERR_INVALID_ARG
     assert L.qnn_selftest_wait_timeout(10 ** 10, None) == qnn.QNN_ERR_INVALID_ARG
+
+
+def test_lis_arguments_rejected_on_host(lib):
+    L = lib
+    ok = qnn.QNN_OK
+    # bits, lengths, scales
+    assert L.q_log_int_softmax(16, 4, 8, 0.01, 0, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_log_int_softmax(16, 4, 8, 0.01, 6, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_log_int_softmax(16, 4, 0, 0.01, 4, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_log_int_softmax(16, 4, 8, 0.0, 4, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_log_int_softmax(16, 4, 8, float("inf"), 4, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_log_int_softmax(16, 4, 8, 50.0, 4, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    # c_int >= 2^31, and a row sum that could pass 2^64 (L c 2^30 >= 2^64)
+    assert L.q_log_int_softmax(16, 4, 8, 2.0 ** -16, 4, 16, None) == qnn.QNN_ERR_OVERFLOW_RISK
+    assert L.q_log_int_softmax(16, 4, 256, 2e-4, 4, 16, None) == qnn.QNN_ERR_OVERFLOW_RISK
+    # nothing to do; NULL and misaligned tensors
+    assert L.q_log_int_softmax(None, 0, 8, 0.01, 4, None, None) == ok
+    assert L.q_log_int_softmax(None, 4, 8, 0.01, 4, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_log_int_softmax(20, 4, 8, 0.01, 4, 16, None) == qnn.QNN_ERR_ALIGNMENT
+    # shift product
+    assert L.q_attn_shift_v(16, 16, 1, 4, 8, 16, 5, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_attn_shift_v(16, 16, 1, 4, 8, 8, 4, 16, None) == qnn.QNN_ERR_UNSUPPORTED
+    assert L.q_attn_shift_v(16, 16, 1, 4, 513, 16, 4, 16, None) == qnn.QNN_ERR_OVERFLOW_RISK
+    assert L.q_attn_shift_v(16, 16, 1, 4, 512, 16, 4, 20, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.q_attn_shift_v(None, None, 0, 4, 512, 16, 4, None, None) == ok
 
 
 def test_packed_sizes(lib):
