@@ -286,7 +286,9 @@ qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t L, float S,
  * dequantized map and v, exact in int32 (the real product is out * 2^-N * s_v).
  * code: u8 [batch][Lq][Lk] (q_log_int_softmax's output); v: s8 [batch][Lk][d];
  * out: int32 [batch][Lq][d].  bits in 1..4; d % 16 == 0; batch <= 65535.
- * QNN_ERR_OVERFLOW_RISK when Lk * 128 * 2^N > 2^31 (Lk <= 512 at 4 bits). */
+ * QNN_ERR_OVERFLOW_RISK when Lk * 128 * 2^N > 2^31 (Lk <= 512 at 4 bits).
+ * d <= 128 with Lk <= 512 runs on the tensor cores (the weight split into two
+ * fp16 halves, exact fp32 sums), other shapes on the CUDA cores; both exact. */
 qnn_status q_attn_shift_v(const uint8_t *code, const int8_t *v, int64_t batch, int Lq, int Lk, int d,
                           int bits, int32_t *out, qnn_stream_t stream);
 

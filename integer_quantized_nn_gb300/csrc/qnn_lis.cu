@@ -18,18 +18,24 @@
 // from v = round(s / e) per element: for each threshold of log_round (v >= 2,
 // 3, 6, 12, ..., 3 * 2^(j-2)) the warp first computes, once per row, the largest
 // e whose rounded ratio still reaches it -- E_j, one exact u64 division per lane
-// -- and each element's code is then the number of E_j >= e, a binary search
-// over the row's E table in shared memory.  That equals log_round(round(s/e))
-// exactly, half-to-even ties included.
+// by a multiply-high with a precomputed reciprocal (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994, section 4) --
+// so that an element's code is the number of E_j >= e.  An fp32 estimate of
+// s / e gives that count to within one; two exact u64 comparisons against the
+// table settle it.  That equals log_round(round(s/e)) exactly, half-to-even ties
+// included.
 //
 // q_attn_shift_v: out[b][i][j] = sum_t 2^(2^bits - 1 - k[b][i][t]) v[b][t][j]
 // over unmasked codes, exact in int32 (the host rejects shapes that could
-// overflow).  A 64 x 64 output tile per block, 4 x 4 per thread, the weights
-// 2^(N - k) expanded into shared memory once per 64-token chunk.
+// overflow).  For d <= 128 and Lk <= 512 it runs on the tensor pipe (below);
+// otherwise on the CUDA cores: a 64 x 64 output tile per block, 4 x 4 per
+// thread, the weights 2^(N - k) expanded into shared memory per 64 tokens.
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include "qnn_internal.h"
+#include "qnn_ptx.cuh"
 
 namespace qnn {
 namespace {
@@ -46,10 +52,15 @@ struct LisArgs {
     int32_t b, c;     // b_int, c_int
     float rcp_x0n;    // fp32 1 / x0n, the quotient estimate
     int kmax;         // 2^bits
+    // floor(n / D_j) = (t + ((n - t) >> 1)) >> (l_j - 1), t = mulhi(m_j, n), for
+    // the divisors D_j = 2 L_j - 1 of the cutoff table
+    uint64_t magic[32];
+    uint32_t magic_l[32];
 };
 
-// Integer exponential of x - mx (mx the row maximum; thr = mx + 30 x0_int).
-__device__ __forceinline__ uint64_t lis_exp(int32_t x, int32_t mx, int64_t thr, const LisArgs &a)
+// Integer exponential of x - mx (mx the row maximum; thr = mx + 30 x0_int),
+// and its fp32 value.
+__device__ __forceinline__ uint64_t lis_exp(int32_t x, int32_t mx, int64_t thr, const LisArgs &a, float &ef)
 {
     // nd = -(x - mx) clamped to 30 |x0_int|; the unsigned difference is exact
     // whenever x >= thr, the only case it is used
@@ -65,21 +76,28 @@ __device__ __forceinline__ uint64_t lis_exp(int32_t x, int32_t mx, int64_t thr, 
     }
     // the page's remainder is -r (in (x0_int, 0]): z = (-r)(-r + b) + c
     const int64_t z = (int64_t)a.c - (int64_t)r * (int64_t)(a.b - r);
-    return z > 0 ? (uint64_t)z << (30 - q) : 0ull;
+    if (z <= 0) {
+        ef = 0.0f;
+        return 0ull;
+    }
+    // z < 2^31: its fp32 value scaled by 2^(30 - q) through the exponent field
+    ef = __int_as_float(__float_as_int(__int2float_rn((int32_t)z)) + ((30 - q) << 23));
+    return (uint64_t)z << (30 - q);
 }
 
-// E table of one row: lane j-1 computes E_j, the largest e with
+// Cutoff table of one row: Et[j] for j = 1..kmax is E_j, the largest e with
 // round_half_even(s / e) >= L_j, L_1 = 2 and L_j = 3 * 2^(j-2) (the values of v
-// where log_round steps up).  round(s/e) >= L  <=>  2s > (2L-1) e, or equality
-// with L even; so E = floor(2s / (2L-1)), minus one when (2L-1) divides 2s and L
-// is odd.
-__device__ __forceinline__ void lis_table(uint64_t s, int lane, int kmax, uint64_t *E)
+// where log_round steps up); Et[0] = 2^64 - 1 and Et[kmax + 1] = 0 bound the
+// search.  round(s/e) >= L  <=>  2s > (2L-1) e, or equality with L even; so
+// E = floor(2s / (2L-1)), minus one when (2L-1) divides 2s and L is odd.
+__device__ __forceinline__ void lis_table(uint64_t s, int lane, const LisArgs &a, uint64_t *Et)
 {
-    if (lane < kmax) {
+    if (lane < a.kmax) {
         const int j = lane + 1;
         const uint64_t Lj = j == 1 ? 2ull : (3ull << (j - 2));
         const uint64_t D = 2 * Lj - 1;
-        const uint64_t q1 = s / D;
+        const uint64_t t = __umul64hi(a.magic[lane], s);
+        const uint64_t q1 = (t + ((s - t) >> 1)) >> (a.magic_l[lane] - 1);
         const uint64_t r1 = s - q1 * D;
         uint64_t Ej = 2 * q1, r2 = 2 * r1;
         if (r2 >= D) {
@@ -87,19 +105,27 @@ __device__ __forceinline__ void lis_table(uint64_t s, int lane, int kmax, uint64
             r2 -= D;
         }
         if (r2 == 0 && (Lj & 1)) Ej -= 1;  // s >= 1, so Ej >= 1 here
-        E[lane] = Ej;
+        Et[j] = Ej;
     }
+    if (lane == 0) Et[0] = ~0ull;
+    if (lane == 1) Et[a.kmax + 1] = 0ull;
     __syncwarp();
 }
 
-// Code of one exponential: the number of E_j >= e, kmax when masked.
-__device__ __forceinline__ uint32_t lis_code(uint64_t e, const uint64_t *E, int kmax)
+// Code of one exponential e (fp32 value ef): the number of E_j >= e, at most
+// kmax.  s3 = fp32 s / 3.  The estimate kh = floor(log2(s / (3 e))) + 2, from the
+// exponent field of s / (3 e), is the count of thresholds L_j <= s / e (L_j = 3 *
+// 2^(j-2) for j >= 2; for 1 <= s/e < 3 it gives 0 or 1); rounding s / e to an
+// integer moves the count by at most one, and so does the estimate's error.
+__device__ __forceinline__ uint32_t lis_code(uint64_t e, float ef, float s3, const uint64_t *Et, int kmax)
 {
-    if (e <= E[kmax - 1]) return (uint32_t)kmax;
-    int pos = 0;
-    for (int step = kmax >> 1; step; step >>= 1)
-        if (E[pos + step - 1] >= e) pos += step;
-    return (uint32_t)pos;
+    if (e == 0) return (uint32_t)kmax;
+    const float w = __fdividef(s3, ef);
+    int kh = ((__float_as_int(w) >> 23) & 0xff) - 125;
+    kh = min(max(kh, 0), kmax);
+    const uint64_t Ea = Et[kh], Eb = Et[kh + 1];
+    const int k = Eb >= e ? kh + 1 : (Ea >= e ? kh : kh - 1);
+    return (uint32_t)min(k, kmax);
 }
 
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v)
@@ -112,11 +138,11 @@ __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v)
 // R > 0: rows of L <= 32 R held in registers.  R == 0: any L, three passes over
 // the row (the later two from cache).
 template <int R>
-__global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(LisArgs a)
+__global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(const __grid_constant__ LisArgs a)
 {
-    __shared__ uint64_t Etab[kLisWarps][32];
+    __shared__ uint64_t Etab[kLisWarps][34];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    uint64_t *E = Etab[w];
+    uint64_t *Et = Etab[w];
     const int64_t L = a.L;
     for (int64_t row = (int64_t)blockIdx.x * kLisWarps + w; row < a.rows;
          row += (int64_t)gridDim.x * kLisWarps) {
@@ -134,18 +160,20 @@ __global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(LisArgs
             mx = __reduce_max_sync(kFull, mx);
             const int64_t thr = (int64_t)mx + a.dmin;
             uint64_t ev[R];
+            float ef[R];
             uint64_t s = 0;
 #pragma unroll
             for (int j = 0; j < R; ++j) {
-                ev[j] = lis_exp(xv[j], mx, thr, a);
+                ev[j] = lis_exp(xv[j], mx, thr, a, ef[j]);
                 if (lane + 32 * j < L) s += ev[j];
             }
             s = warp_sum_u64(s);
-            lis_table(s, lane, a.kmax, E);
+            lis_table(s, lane, a, Et);
+            const float s3 = __ull2float_rn(s) * (1.0f / 3.0f);
 #pragma unroll
             for (int j = 0; j < R; ++j) {
                 const int64_t i = lane + 32 * j;
-                if (i < L) __stcs(cr + i, (uint8_t)lis_code(ev[j], E, a.kmax));
+                if (i < L) __stcs(cr + i, (uint8_t)lis_code(ev[j], ef[j], s3, Et, a.kmax));
             }
         } else {
             int32_t mx = INT32_MIN;
@@ -153,13 +181,17 @@ __global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(LisArgs
             mx = __reduce_max_sync(kFull, mx);
             const int64_t thr = (int64_t)mx + a.dmin;
             uint64_t s = 0;
-            for (int64_t i = lane; i < L; i += 32) s += lis_exp(__ldg(xr + i), mx, thr, a);
+            float ef;
+            for (int64_t i = lane; i < L; i += 32) s += lis_exp(__ldg(xr + i), mx, thr, a, ef);
             s = warp_sum_u64(s);
-            lis_table(s, lane, a.kmax, E);
-            for (int64_t i = lane; i < L; i += 32)
-                __stcs(cr + i, (uint8_t)lis_code(lis_exp(__ldg(xr + i), mx, thr, a), E, a.kmax));
+            lis_table(s, lane, a, Et);
+            const float s3 = __ull2float_rn(s) * (1.0f / 3.0f);
+            for (int64_t i = lane; i < L; i += 32) {
+                const uint64_t e = lis_exp(__ldg(xr + i), mx, thr, a, ef);
+                __stcs(cr + i, (uint8_t)lis_code(e, ef, s3, Et, a.kmax));
+            }
         }
-        __syncwarp();  // E is rewritten for the next row
+        __syncwarp();  // Et is rewritten for the next row
     }
 }
 
@@ -240,6 +272,209 @@ __global__ void __launch_bounds__(256) attn_shift_v_kernel(ShiftArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// bit-shift product on the tensor pipe.  The weight 2^(N - k) (N = 2^bits - 1
+// <= 15) is split into lo = 2^(N - k) for N - k < 8 and hi = 2^(N - k - 8) for
+// N - k >= 8, both <= 128 and exact in fp16, as are the s8 values; every product
+// is an integer below 2^14 in magnitude and each of the two sums stays below
+// 2^23 for Lk <= 512, so the fp32 accumulators of two kind::f16 MMAs (lo and hi,
+// adjacent TMEM column ranges) hold them exactly, and out = lo + 256 hi.
+//
+// One CTA per (head, 128 query rows), 8 warps, two CTAs per SM.  Per round of
+// up to 128 tokens: all threads expand the codes into the fp16 images A_lo /
+// A_hi (128 rows x 2 K atoms of 64, K-major, 128-byte swizzle: 16-byte chunk c
+// of row r at chunk c ^ (r % 8)), stage the value rows in shared memory and
+// transpose them into the B image (d rows = value columns, same layout); one
+// thread then issues the MMAs (M = 128, N = d, K = 16 each) and commits to an
+// mbarrier that every thread waits on (bounded) before the next round reuses
+// the images.  The epilogue reads TMEM with 32x32b.x16 loads, converts the exact
+// fp32 sums to integers and writes 16 consecutive int32 per thread and piece.
+constexpr int kMmaRows = 128;
+constexpr int kMmaKC = 128;  // tokens per round: two 64-element K atoms
+
+struct ShiftMmaArgs {
+    const uint8_t *code;  // [B][Lq][Lk]
+    const int8_t *v;      // [B][Lk][d]
+    int32_t *out;         // [B][Lq][d]
+    uint64_t code_bytes;  // B * Lq * Lk: no word load starts at or past it
+    int Lq, Lk, d;
+    uint32_t tab0, tab1;  // high bytes of the fp16 weights, by code & 7 (bytes 0..7)
+    uint32_t tmem_cols;
+    uint32_t *status;
+};
+
+__host__ __device__ constexpr uint32_t shift_mma_smem(int d, bool hi)
+{
+    return 1024u + (hi ? 2u : 1u) * 2u * kMmaRows * 128u + 2u * (uint32_t)d * 128u + (uint32_t)(kMmaKC * d) + 64u;
+}
+
+// fp32 value of an exact integer with |f| <= 2^22 -> int32 without the conversion pipe.
+__device__ __forceinline__ int32_t exact_f2i_small(uint32_t fbits)
+{
+    return __float_as_int(__fadd_rn(__int_as_float(fbits), 12582912.0f)) - 0x4B400000;
+}
+
+template <bool HI>
+__global__ void __launch_bounds__(256) attn_shift_mma_kernel(const __grid_constant__ ShiftMmaArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *A_lo = base;
+    uint8_t *A_hi = base + 2 * kMmaRows * 128;
+    uint8_t *Bs = base + (HI ? 2 : 1) * 2 * kMmaRows * 128;
+    const int d = a.d;
+    const uint32_t batom = (uint32_t)d * 128u;  // bytes of one K atom of B
+    uint8_t *raw = Bs + 2 * batom;              // value rows of the round, [token][d]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(raw + kMmaKC * d);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t b = blockIdx.y;
+    const int i0 = blockIdx.x * kMmaRows;
+    if (tid == 0) {
+        mbar_init(smem_u32(bar), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t idesc = idesc_f32acc(0, 0, kMmaRows, (uint32_t)d);
+    const int8_t *vb = a.v + b * (int64_t)a.Lk * d;
+    const int rounds = (a.Lk + kMmaKC - 1) / kMmaKC;
+    bool ok = true;
+    for (int rd = 0; rd < rounds && ok; ++rd) {
+        const int t0 = rd * kMmaKC;
+        const int nks = min(kMmaKC / 16, (a.Lk - t0 + 15) / 16);  // K steps of 16 this round
+        const int ntok = nks * 16;                                 // tokens written (zero past Lk)
+        // ---- A: a warp per row and 4 tokens per lane: two aligned word loads and a funnel shift
+        const int gpr = ntok / 4;
+        for (int it = tid; it < kMmaRows * 32; it += 256) {
+            const int row = it >> 5, g = it & 31;
+            if (g >= gpr) continue;
+            const int i = i0 + row;
+            const int t = t0 + 4 * g;
+            uint32_t c = 0xFFFFFFFFu;  // >= 2^bits: weight 0
+            if (i < a.Lq && t < a.Lk) {
+                const uint64_t addr = (uint64_t)((b * a.Lq + i) * (int64_t)a.Lk + t);
+                const uint64_t a0 = addr & ~3ull;
+                const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(a.code + a0));
+                const uint32_t w1 = (a0 + 4 < a.code_bytes) ? __ldg(reinterpret_cast<const uint32_t *>(a.code + a0 + 4)) : 0u;
+                c = __funnelshift_r(w0, w1, (uint32_t)(addr & 3u) * 8u);
+                const int nv = a.Lk - t;
+                if (nv < 4) c |= 0xFFFFFFFFu << (8 * nv);
+            }
+            // weight high bytes: the table by code & 7; bit 3 splits lo from hi; codes >= 16 are 0
+            const uint32_t x = c & 0x07070707u;
+            const uint32_t sel = prmt(x | (x >> 4), 0u, 0x4420u);
+            const uint32_t tb = prmt(a.tab0, a.tab1, sel);
+            const uint32_t b3 = prmt(c << 4, 0u, 0xBA98u);
+            const uint32_t big = prmt(((c & 0xF0F0F0F0u) >> 1) + 0x78787878u, 0u, 0xBA98u);
+            const int kk = t - t0;
+            const uint32_t off = (uint32_t)(kk >> 6) * (kMmaRows * 128u) + (uint32_t)(row >> 3) * 1024u +
+                                 (uint32_t)(row & 7) * 128u + ((((uint32_t)(kk & 63) >> 3) ^ (uint32_t)(row & 7)) << 4) +
+                                 (uint32_t)(kk & 7) * 2u;
+            if constexpr (HI) {
+                const uint32_t lo = tb & b3 & ~big, hi = tb & ~b3 & ~big;
+                *reinterpret_cast<uint2 *>(A_lo + off) = make_uint2(prmt(lo, 0u, 0x1404u), prmt(lo, 0u, 0x3424u));
+                *reinterpret_cast<uint2 *>(A_hi + off) = make_uint2(prmt(hi, 0u, 0x1404u), prmt(hi, 0u, 0x3424u));
+            } else {
+                const uint32_t lo = tb & ~b3 & ~big;
+                *reinterpret_cast<uint2 *>(A_lo + off) = make_uint2(prmt(lo, 0u, 0x1404u), prmt(lo, 0u, 0x3424u));
+            }
+        }
+        // ---- value rows of the round into shared memory (16-byte loads, zero past Lk)
+        const int chunks = ntok * d / 16;
+        for (int it = tid; it < chunks; it += 256) {
+            const int tt = (it * 16) / d, cc = (it * 16) % d;
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (t0 + tt < a.Lk) w = __ldg(reinterpret_cast<const uint4 *>(vb + (int64_t)(t0 + tt) * d + cc));
+            *reinterpret_cast<uint4 *>(raw + tt * d + cc) = w;
+        }
+        __syncthreads();
+        // ---- B: column j, 8 tokens -> one 16-byte chunk of fp16; lanes 0..7 of a quarter
+        // warp take 8 consecutive columns, so its 8 chunks land on distinct banks
+        const int groups = ntok / 8;
+        for (int it = tid; it < d * groups; it += 256) {
+            const int j = it % d, gk = it / d;
+            uint32_t bytes[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint8_t *src = raw + (gk * 8 + 4 * h) * d + j;
+                bytes[h] = (uint32_t)src[0] | ((uint32_t)src[d] << 8) | ((uint32_t)src[2 * d] << 16) |
+                           ((uint32_t)src[3 * d] << 24);
+                bytes[h] ^= 0x80808080u;  // s8 -> u8 = v + 128
+            }
+            // fp16 1024 + u in each half, minus 1152: exactly v
+            uint4 o;
+            o.x = hsub2_u32(prmt(bytes[0], 0x64646464u, 0x5140u), 0x64806480u);
+            o.y = hsub2_u32(prmt(bytes[0], 0x64646464u, 0x7362u), 0x64806480u);
+            o.z = hsub2_u32(prmt(bytes[1], 0x64646464u, 0x5140u), 0x64806480u);
+            o.w = hsub2_u32(prmt(bytes[1], 0x64646464u, 0x7362u), 0x64806480u);
+            const int kk = gk * 8;
+            const uint32_t off = (uint32_t)(kk >> 6) * batom + (uint32_t)(j >> 3) * 1024u + (uint32_t)(j & 7) * 128u +
+                                 ((((uint32_t)(kk & 63) >> 3) ^ (uint32_t)(j & 7)) << 4);
+            *reinterpret_cast<uint4 *>(Bs + off) = o;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint64_t alo = sdesc_sw128(smem_u32(A_lo)), ahi = sdesc_sw128(smem_u32(A_hi));
+            const uint64_t bd = sdesc_sw128(smem_u32(Bs));
+            for (int ks = 0; ks < nks; ++ks) {
+                // descriptor addresses in 16-byte units: a K atom further, or 32 bytes (+2) per K step
+                const uint64_t aoff = (uint64_t)((ks >> 2) * (kMmaRows * 128 / 16) + (ks & 3) * 2);
+                const uint64_t boff = (uint64_t)((ks >> 2) * (batom / 16) + (ks & 3) * 2);
+                const uint32_t acc = (rd > 0 || ks > 0) ? 1u : 0u;
+                mma_f16_ss(tmem, alo + aoff, bd + boff, idesc, acc);
+                if constexpr (HI) mma_f16_ss(tmem + (uint32_t)d, ahi + aoff, bd + boff, idesc, acc);
+            }
+            mma_commit(smem_u32(bar));
+        }
+        __syncwarp();
+        ok = mbar_wait(smem_u32(bar), (uint32_t)(rd & 1), a.status);
+        tc_fence_after();
+    }
+    if (ok) {
+        // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows), pieces of 16 columns
+        const int quad = warp & 3, half = warp >> 2;
+        const int i = i0 + quad * 32 + lane;
+        int32_t *orow = a.out + (b * a.Lq + i) * (int64_t)d;
+        const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+        const bool small = a.Lk <= 256;  // |lo|, |hi| <= 2^14 Lk <= 2^22
+        for (int p = half; p < d / 16; p += 2) {
+            uint32_t lo[16], hi[16];
+            tmem_ld16(trow + (uint32_t)(p * 16), lo);
+            if constexpr (HI) tmem_ld16(trow + (uint32_t)(d + p * 16), hi);
+            tmem_ld_wait();
+            int32_t o[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                int32_t vlo = small ? exact_f2i_small(lo[q]) : __float2int_rn(__int_as_float(lo[q]));
+                if constexpr (HI) {
+                    const int32_t vhi = small ? exact_f2i_small(hi[q]) : __float2int_rn(__int_as_float(hi[q]));
+                    vlo = (int32_t)((uint32_t)vlo + ((uint32_t)vhi << 8));
+                }
+                o[q] = vlo;
+            }
+            if (i < a.Lq) {
+                int4 *dst = reinterpret_cast<int4 *>(orow + p * 16);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dst[q] = make_int4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
+}
+
 // Constants of the integer exponential from the scale S: fp32 quotients of the
 // page's constants, floored.  Returns false when they leave the supported range.
 struct LisConsts {
@@ -291,6 +526,16 @@ extern "C" qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t 
     a.c = (int32_t)k.c;
     a.rcp_x0n = 1.0f / (float)a.x0n;
     a.kmax = 1 << bits;
+    for (int j = 1; j <= 32; ++j) {
+        // D = 2 L_j - 1 is odd and >= 3: l = ceil(log2 D), m = floor(2^64 (2^l - D) / D) + 1
+        const uint64_t Lj = j == 1 ? 2ull : (3ull << (j - 2));
+        const uint64_t D = 2 * Lj - 1;
+        int l = 0;
+        while ((1ull << l) < D) ++l;
+        const unsigned __int128 num = ((unsigned __int128)1 << 64) * (((unsigned __int128)1 << l) - D);
+        a.magic[j - 1] = (uint64_t)(num / D) + 1;
+        a.magic_l[j - 1] = (uint32_t)l;
+    }
     const int64_t want = (rows + kLisWarps - 1) / kLisWarps;
     const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * 8);
     cudaStream_t s = (cudaStream_t)stream;
@@ -314,8 +559,46 @@ extern "C" qnn_status q_attn_shift_v(const uint8_t *code, const int8_t *v, int64
     if (batch == 0 || Lq == 0) return QNN_OK;
     if (code == nullptr || v == nullptr || out == nullptr) return QNN_ERR_INVALID_ARG;
     if (!aligned16(code) || !aligned16(v) || !aligned16(out)) return QNN_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (d <= 128 && Lk <= 512) {
+        // tensor pipe: weights split into two fp16 halves when N = 2^bits - 1 >= 8
+        const bool hi = bits == 4;
+        const int N = (1 << bits) - 1;
+        uint8_t tab[8];
+        for (int m = 0; m < 8; ++m) {
+            const int e = hi ? 7 - m : N - m;  // exponent of the weight for code & 7 == m
+            tab[m] = (uint8_t)(e >= 0 ? (e + 15) << 2 : 0);
+        }
+        ShiftMmaArgs m{};
+        m.code = code;
+        m.v = v;
+        m.out = out;
+        m.code_bytes = (uint64_t)batch * (uint64_t)Lq * (uint64_t)Lk;
+        m.Lq = Lq;
+        m.Lk = Lk;
+        m.d = d;
+        m.tab0 = (uint32_t)tab[0] | ((uint32_t)tab[1] << 8) | ((uint32_t)tab[2] << 16) | ((uint32_t)tab[3] << 24);
+        m.tab1 = (uint32_t)tab[4] | ((uint32_t)tab[5] << 8) | ((uint32_t)tab[6] << 16) | ((uint32_t)tab[7] << 24);
+        uint32_t cols = 32;
+        while (cols < (uint32_t)(hi ? 2 * d : d)) cols *= 2;
+        m.tmem_cols = cols;
+        m.status = status_word();
+        const uint32_t smem = shift_mma_smem(d, hi);
+        const dim3 grid((Lq + kMmaRows - 1) / kMmaRows, (unsigned)batch);
+        // the largest dynamic shared memory (d = 128) is set once per kernel and process
+        static std::atomic<int> attr_set[2];
+        auto kern = hi ? attn_shift_mma_kernel<true> : attn_shift_mma_kernel<false>;
+        if (!attr_set[hi].load(std::memory_order_acquire)) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)shift_mma_smem(128, hi)) != cudaSuccess)
+                return QNN_ERR_CUDA;
+            attr_set[hi].store(1, std::memory_order_release);
+        }
+        kern<<<grid, 256, smem, s>>>(m);
+        return launch_status();
+    }
     ShiftArgs a{code, v, out, Lq, Lk, d, 1 << bits};
     const dim3 grid((Lq + kShM - 1) / kShM, (d + kShN - 1) / kShN, (unsigned)batch);
-    attn_shift_v_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(a);
+    attn_shift_v_kernel<<<grid, 256, 0, s>>>(a);
     return launch_status();
 }

@@ -110,11 +110,15 @@ def _shift_gpu(code, v, bits):
 
 
 @pytest.mark.parametrize("shape", [(3, 197, 197, 64), (2, 1, 5, 16), (5, 65, 63, 80), (1, 130, 512, 48),
-                                   (2, 64, 64, 64)])
+                                   (2, 64, 64, 64), (1, 257, 300, 128), (2, 40, 70, 144), (1, 33, 1100, 32)])
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
 def test_attn_shift_v(oracle, shape, bits):
-    """Ragged query / token / column tiles, masked codes, every bit width."""
+    """Ragged query / token / column tiles, masked codes, every bit width; d <= 128
+    with Lk <= 512 on the tensor pipe (one to four token rounds), the last two shapes
+    on the CUDA-core kernel."""
     Bh, Lq, Lk, d = shape
+    if Lk * 128 * 2 ** (2 ** bits - 1) > 2 ** 31:
+        pytest.skip("int32 range: refused by the host check")
     rng = np.random.default_rng(Lq * 7 + bits)
     code = rng.integers(0, 2 ** bits + 1, size=(Bh, Lq, Lk)).astype(np.uint8)
     v = rng.integers(-128, 128, size=(Bh, Lk, d)).astype(np.int8)
@@ -124,12 +128,15 @@ def test_attn_shift_v(oracle, shape, bits):
 
 def test_attn_shift_v_extremes(oracle):
     """The int32 range's edge: Lk = 512 at 4 bits with every code 0 and v = -128
-    reaches exactly -2^31; v = 127 the largest positive sum."""
-    code = np.zeros((1, 3, 512), np.uint8)
-    for val in (-128, 127):
-        v = np.full((1, 512, 16), val, np.int8)
-        want = oracle.attn_shift_v(code, v, 4)
-        assert np.array_equal(_shift_gpu(code, v, 4).astype(np.int64), want)
+    reaches exactly -2^31, v = 127 the largest positive sum; Lk = 256 puts the
+    tensor-pipe sums at 2^22, the edge of their exact conversion."""
+    for Lk in (512, 256, 257):
+        code = np.zeros((1, 3, Lk), np.uint8)
+        code[0, 2, ::3] = 8  # a row of mixed halves
+        for val in (-128, 127):
+            v = np.full((1, Lk, 16), val, np.int8)
+            want = oracle.attn_shift_v(code, v, 4)
+            assert np.array_equal(_shift_gpu(code, v, 4).astype(np.int64), want)
     t = __import__("torch")
     with pytest.raises(qnn.QnnError):  # Lk = 513 could overflow int32
         qnn.q_attn_shift_v(t.zeros((1, 1, 513), dtype=t.uint8, device="cuda"),
