@@ -31,6 +31,7 @@
 // otherwise on the CUDA cores: a 64 x 64 output tile per block, 4 x 4 per
 // thread, the weights 2^(N - k) expanded into shared memory per 64 tokens.
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -47,10 +48,11 @@ struct LisArgs {
     const int32_t *x;
     uint8_t *code;
     int64_t rows, L;
-    int32_t x0n;      // -x0_int (> 0)
-    int32_t dmin;     // 30 * x0_int: the clamp of x - max(x)
+    uint32_t x0n;     // -x0_int (> 0)
+    uint32_t ndmax;   // 30 |x0_int|: the clamp of max(x) - x
     int32_t b, c;     // b_int, c_int
-    float rcp_x0n;    // fp32 1 / x0n, the quotient estimate
+    uint32_t qm;      // floor(nd / x0n) = mulhi(nd, qm) >> ql for nd <= 30 x0n < 2^21
+    uint32_t ql;      // (x0n == 1: qm = 0, q = nd)
     int kmax;         // 2^bits
     // floor(n / D_j) = (t + ((n - t) >> 1)) >> (l_j - 1), t = mulhi(m_j, n), for
     // the divisors D_j = 2 L_j - 1 of the cutoff table
@@ -58,31 +60,23 @@ struct LisArgs {
     uint32_t magic_l[32];
 };
 
-// Integer exponential of x - mx (mx the row maximum; thr = mx + 30 x0_int),
-// and its fp32 value.
-__device__ __forceinline__ uint64_t lis_exp(int32_t x, int32_t mx, int64_t thr, const LisArgs &a, float &ef)
+// Integer exponential of x - mx (mx the row maximum) and its fp32 value.  The
+// host has checked that 0 < z <= c_int < 2^31 for every remainder, so z is
+// formed in 32 bits.
+__device__ __forceinline__ uint64_t lis_exp(int32_t x, int32_t mx, const LisArgs &a, float &ef)
 {
-    // nd = -(x - mx) clamped to 30 |x0_int|; the unsigned difference is exact
-    // whenever x >= thr, the only case it is used
-    const uint32_t nd = ((int64_t)x < thr) ? (uint32_t)(-a.dmin) : (uint32_t)mx - (uint32_t)x;
-    int32_t q = (int32_t)__float2uint_rz(__uint2float_rn(nd) * a.rcp_x0n);
-    int32_t r = (int32_t)nd - q * a.x0n;  // nd < 2^20: the estimate is off by one at most
-    if (r < 0) {
-        --q;
-        r += a.x0n;
-    } else if (r >= a.x0n) {
-        ++q;
-        r -= a.x0n;
-    }
+    // nd = -(max(x - mx, 30 x0_int)): mx >= x, so the unsigned difference is exact
+    const uint32_t nd = min((uint32_t)mx - (uint32_t)x, a.ndmax);
+    const uint32_t q = a.qm ? __umulhi(nd, a.qm) >> a.ql : nd;
+    const int32_t r = (int32_t)(nd - q * a.x0n);
     // the page's remainder is -r (in (x0_int, 0]): z = (-r)(-r + b) + c
-    const int64_t z = (int64_t)a.c - (int64_t)r * (int64_t)(a.b - r);
-    if (z <= 0) {
-        ef = 0.0f;
-        return 0ull;
-    }
-    // z < 2^31: its fp32 value scaled by 2^(30 - q) through the exponent field
-    ef = __int_as_float(__float_as_int(__int2float_rn((int32_t)z)) + ((30 - q) << 23));
-    return (uint64_t)z << (30 - q);
+    const int32_t z = a.c - r * (a.b - r);
+    const uint32_t sh = 30u - q;
+    // z scaled by 2^sh through the exponent field of its fp32 value
+    ef = __int_as_float(__float_as_int(__int2float_rn(z)) + (int32_t)(sh << 23));
+    // (z << sh) as two words: z < 2^31, sh <= 30
+    const uint32_t lo = (uint32_t)z << sh, hi = __funnelshift_l((uint32_t)z, 0u, sh);
+    return ((uint64_t)hi << 32) | lo;
 }
 
 // Cutoff table of one row: Et[j] for j = 1..kmax is E_j, the largest e with
@@ -113,31 +107,36 @@ __device__ __forceinline__ void lis_table(uint64_t s, int lane, const LisArgs &a
 }
 
 // Code of one exponential e (fp32 value ef): the number of E_j >= e, at most
-// kmax.  s3 = fp32 s / 3.  The estimate kh = floor(log2(s / (3 e))) + 2, from the
-// exponent field of s / (3 e), is the count of thresholds L_j <= s / e (L_j = 3 *
-// 2^(j-2) for j >= 2; for 1 <= s/e < 3 it gives 0 or 1); rounding s / e to an
-// integer moves the count by at most one, and so does the estimate's error.
-__device__ __forceinline__ uint32_t lis_code(uint64_t e, float ef, float s3, const uint64_t *Et, int kmax)
+// kmax.  kh, the number of thresholds L_j = 3 * 2^(j-2) (j >= 2) at or below
+// the fp32 estimate of v = s / e, comes from its exponent E and first mantissa
+// bit (v >= 1.5 * 2^E); below 2 it is taken as 0.  Rounding v to an integer
+// and the estimate's relative error (< 2^-20) move the count by at most one,
+// and only upwards while L_kh < 2^19 (kmax <= 16): one exact comparison with
+// E_{kh+1} settles it.  For kmax = 32 the count may also lie one below.
+template <bool WIDE>
+__device__ __forceinline__ uint32_t lis_code(uint64_t e, float ef, float sf, const uint64_t *Et, int kmax)
 {
-    if (e == 0) return (uint32_t)kmax;
-    const float w = __fdividef(s3, ef);
-    int kh = ((__float_as_int(w) >> 23) & 0xff) - 125;
-    kh = min(max(kh, 0), kmax);
-    const uint64_t Ea = Et[kh], Eb = Et[kh + 1];
-    const int k = Eb >= e ? kh + 1 : (Ea >= e ? kh : kh - 1);
+    // t = 2 (E + 127) + (first mantissa bit); kh = E + that bit for E >= 1
+    const int t = __float_as_int(__fdividef(sf, ef)) >> 22;
+    const int kh = t >= 256 ? min(((t + 1) >> 1) - 127, kmax) : 0;
+    int k = Et[kh + 1] >= e ? kh + 1 : kh;
+    if constexpr (WIDE) k = Et[kh] >= e ? k : kh - 1;
     return (uint32_t)min(k, kmax);
 }
 
+// Sum over the warp of per-lane u64 values whose total is below 2^64, as three
+// limbs of 22, 22 and 20 bits, each summed by one warp reduction (below 2^27).
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v)
 {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
+    const uint32_t l0 = __reduce_add_sync(kFull, (uint32_t)v & 0x3FFFFFu);
+    const uint32_t l1 = __reduce_add_sync(kFull, (uint32_t)(v >> 22) & 0x3FFFFFu);
+    const uint32_t l2 = __reduce_add_sync(kFull, (uint32_t)(v >> 44));
+    return (uint64_t)l0 + ((uint64_t)l1 << 22) + ((uint64_t)l2 << 44);
 }
 
 // R > 0: rows of L <= 32 R held in registers.  R == 0: any L, three passes over
 // the row (the later two from cache).
-template <int R>
+template <int R, bool WIDE>
 __global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(const __grid_constant__ LisArgs a)
 {
     __shared__ uint64_t Etab[kLisWarps][34];
@@ -151,44 +150,43 @@ __global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(const _
         if constexpr (R > 0) {
             int32_t xv[R];
             int32_t mx = INT32_MIN;
+            const int Li = (int)L;  // <= 256 here
 #pragma unroll
             for (int j = 0; j < R; ++j) {
-                const int64_t i = lane + 32 * j;
-                xv[j] = i < L ? __ldcs(xr + i) : INT32_MIN;
+                const int i = lane + 32 * j;
+                xv[j] = i < Li ? __ldcs(xr + i) : INT32_MIN;
                 mx = max(mx, xv[j]);
             }
             mx = __reduce_max_sync(kFull, mx);
-            const int64_t thr = (int64_t)mx + a.dmin;
             uint64_t ev[R];
             float ef[R];
             uint64_t s = 0;
 #pragma unroll
             for (int j = 0; j < R; ++j) {
-                ev[j] = lis_exp(xv[j], mx, thr, a, ef[j]);
-                if (lane + 32 * j < L) s += ev[j];
+                ev[j] = lis_exp(xv[j], mx, a, ef[j]);
+                if (lane + 32 * j < Li) s += ev[j];
             }
             s = warp_sum_u64(s);
             lis_table(s, lane, a, Et);
-            const float s3 = __ull2float_rn(s) * (1.0f / 3.0f);
+            const float sf = __ull2float_rn(s);
 #pragma unroll
             for (int j = 0; j < R; ++j) {
-                const int64_t i = lane + 32 * j;
-                if (i < L) __stcs(cr + i, (uint8_t)lis_code(ev[j], ef[j], s3, Et, a.kmax));
+                const int i = lane + 32 * j;
+                if (i < Li) __stcs(cr + i, (uint8_t)lis_code<WIDE>(ev[j], ef[j], sf, Et, a.kmax));
             }
         } else {
             int32_t mx = INT32_MIN;
             for (int64_t i = lane; i < L; i += 32) mx = max(mx, __ldg(xr + i));
             mx = __reduce_max_sync(kFull, mx);
-            const int64_t thr = (int64_t)mx + a.dmin;
             uint64_t s = 0;
             float ef;
-            for (int64_t i = lane; i < L; i += 32) s += lis_exp(__ldg(xr + i), mx, thr, a, ef);
+            for (int64_t i = lane; i < L; i += 32) s += lis_exp(__ldg(xr + i), mx, a, ef);
             s = warp_sum_u64(s);
             lis_table(s, lane, a, Et);
-            const float s3 = __ull2float_rn(s) * (1.0f / 3.0f);
+            const float sf = __ull2float_rn(s);
             for (int64_t i = lane; i < L; i += 32) {
-                const uint64_t e = lis_exp(__ldg(xr + i), mx, thr, a, ef);
-                __stcs(cr + i, (uint8_t)lis_code(e, ef, s3, Et, a.kmax));
+                const uint64_t e = lis_exp(__ldg(xr + i), mx, a, ef);
+                __stcs(cr + i, (uint8_t)lis_code<WIDE>(e, ef, sf, Et, a.kmax));
             }
         }
         __syncwarp();  // Et is rewritten for the next row
@@ -280,17 +278,21 @@ __global__ void __launch_bounds__(256) attn_shift_v_kernel(ShiftArgs a)
 // 2^23 for Lk <= 512, so the fp32 accumulators of two kind::f16 MMAs (lo and hi,
 // adjacent TMEM column ranges) hold them exactly, and out = lo + 256 hi.
 //
-// One CTA per (head, 128 query rows), 8 warps, two CTAs per SM.  Per round of
-// up to 128 tokens: all threads expand the codes into the fp16 images A_lo /
-// A_hi (128 rows x 2 K atoms of 64, K-major, 128-byte swizzle: 16-byte chunk c
-// of row r at chunk c ^ (r % 8)), stage the value rows in shared memory and
-// transpose them into the B image (d rows = value columns, same layout); one
+// One CTA per (head, 128 query rows), 8 warps, up to four CTAs per SM.  Per
+// round of up to 64 tokens: all threads expand the codes into the fp16 images
+// A_lo / A_hi (128 rows x one K atom of 64, K-major, 128-byte swizzle: 16-byte
+// chunk c of row r at chunk c ^ (r % 8)), stage the value rows in shared memory
+// and transpose them into the B image (d rows = value columns, same layout); one
 // thread then issues the MMAs (M = 128, N = d, K = 16 each) and commits to an
 // mbarrier that every thread waits on (bounded) before the next round reuses
-// the images.  The epilogue reads TMEM with 32x32b.x16 loads, converts the exact
-// fp32 sums to integers and writes 16 consecutive int32 per thread and piece.
+// the images; the next round's global loads are issued before that wait.  The
+// epilogue reads TMEM with 32x32b.x16 loads, converts the exact fp32 sums to
+// integers and writes 16 consecutive int32 per thread and piece.
 constexpr int kMmaRows = 128;
-constexpr int kMmaKC = 128;  // tokens per round: two 64-element K atoms
+constexpr int kMmaKC = 64;   // tokens per round: one 64-element K atom
+constexpr int kMmaGroups = kMmaKC / 4;                 // 4-token groups per row and round
+constexpr int kAItems = kMmaRows * kMmaGroups / 256;   // code words per thread and round
+constexpr int kVMax = kMmaKC * 128 / 16 / 256;         // value chunks per thread at d = 128
 
 struct ShiftMmaArgs {
     const uint8_t *code;  // [B][Lq][Lk]
@@ -299,13 +301,16 @@ struct ShiftMmaArgs {
     uint64_t code_bytes;  // B * Lq * Lk: no word load starts at or past it
     int Lq, Lk, d;
     uint32_t tab0, tab1;  // high bytes of the fp16 weights, by code & 7 (bytes 0..7)
+    // n / m = mulhi(n, ceil(2^32 / m)) for the small n used here
+    uint32_t rcp_c;       // m = d / 16 (0 when d == 16: the quotient is n)
+    uint32_t rcp_d;       // m = d
     uint32_t tmem_cols;
     uint32_t *status;
 };
 
 __host__ __device__ constexpr uint32_t shift_mma_smem(int d, bool hi)
 {
-    return 1024u + (hi ? 2u : 1u) * 2u * kMmaRows * 128u + 2u * (uint32_t)d * 128u + (uint32_t)(kMmaKC * d) + 64u;
+    return 1024u + (hi ? 2u : 1u) * kMmaRows * 128u + (uint32_t)d * 128u + (uint32_t)(kMmaKC * d) + 64u;
 }
 
 // fp32 value of an exact integer with |f| <= 2^22 -> int32 without the conversion pipe.
@@ -314,19 +319,63 @@ __device__ __forceinline__ int32_t exact_f2i_small(uint32_t fbits)
     return __float_as_int(__fadd_rn(__int_as_float(fbits), 12582912.0f)) - 0x4B400000;
 }
 
+// Global loads of one round into registers: per thread 8 words of 4 codes (16
+// lanes per row, lane g holding tokens 4g .. 4g+3: two aligned word loads and a
+// funnel shift, codes past Lk or rows past Lq set to 0xFF, i.e. weight 0) and up
+// to 2 chunks of 16 value bytes (zero past Lk).
+__device__ __forceinline__ void shift_load_round(const ShiftMmaArgs &a, int64_t b, int i0, int tid, int rd,
+                                                 const int8_t *vb, uint32_t (&cw)[kAItems], uint4 (&vw)[kVMax])
+{
+    const int d = a.d;
+    const int t0 = rd * kMmaKC;
+    const int ntok = min(kMmaKC, (a.Lk - t0 + 15) / 16 * 16);
+    const int gpr = ntok / 4, g = tid % kMmaGroups;
+    const int t = t0 + 4 * g;
+    const int r0 = tid / kMmaGroups;
+    const uint64_t rb = (uint64_t)((b * a.Lq + i0 + r0) * (int64_t)a.Lk) + (uint64_t)t;
+#pragma unroll
+    for (int u = 0; u < kAItems; ++u) {
+        const int i = i0 + r0 + (256 / kMmaGroups) * u;
+        uint32_t c = 0xFFFFFFFFu;
+        if (g < gpr && i < a.Lq && t < a.Lk) {
+            const uint64_t addr = rb + (uint64_t)((256 / kMmaGroups) * u) * (uint64_t)a.Lk;
+            const uint64_t a0 = addr & ~3ull;
+            const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(a.code + a0));
+            const uint32_t w1 =
+                (a0 + 4 < a.code_bytes) ? __ldg(reinterpret_cast<const uint32_t *>(a.code + a0 + 4)) : 0u;
+            c = __funnelshift_r(w0, w1, (uint32_t)(addr & 3u) * 8u);
+            const int nv = a.Lk - t;
+            if (nv < 4) c |= 0xFFFFFFFFu << (8 * nv);
+        }
+        cw[u] = c;
+    }
+    const int chunks = ntok * d / 16;
+#pragma unroll
+    for (int u = 0; u < kVMax; ++u) {
+        const int it = tid + 256 * u;
+        vw[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (it < chunks) {
+            const int tt = a.rcp_c ? (int)__umulhi((uint32_t)it, a.rcp_c) : it;
+            const int cc = (it - tt * (d >> 4)) * 16;
+            if (t0 + tt < a.Lk) vw[u] = __ldg(reinterpret_cast<const uint4 *>(vb + (int64_t)(t0 + tt) * d + cc));
+        }
+    }
+}
+
 template <bool HI>
-__global__ void __launch_bounds__(256) attn_shift_mma_kernel(const __grid_constant__ ShiftMmaArgs a)
+__global__ void __launch_bounds__(256, 4) attn_shift_mma_kernel(const __grid_constant__ ShiftMmaArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *A_lo = base;
-    uint8_t *A_hi = base + 2 * kMmaRows * 128;
-    uint8_t *Bs = base + (HI ? 2 : 1) * 2 * kMmaRows * 128;
+    uint8_t *A_hi = base + kMmaRows * 128;
+    uint8_t *Bs = base + (HI ? 2 : 1) * kMmaRows * 128;
     const int d = a.d;
-    const uint32_t batom = (uint32_t)d * 128u;  // bytes of one K atom of B
-    uint8_t *raw = Bs + 2 * batom;              // value rows of the round, [token][d]
+    const uint32_t batom = (uint32_t)d * 128u;  // bytes of the K atom of B
+    uint8_t *raw = Bs + batom;                  // value rows of the round, [token][d]
     uint64_t *bar = reinterpret_cast<uint64_t *>(raw + kMmaKC * d);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+    uint32_t *ok_flag = tmem_slot + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t b = blockIdx.y;
@@ -346,78 +395,70 @@ __global__ void __launch_bounds__(256) attn_shift_mma_kernel(const __grid_consta
     const uint32_t idesc = idesc_f32acc(0, 0, kMmaRows, (uint32_t)d);
     const int8_t *vb = a.v + b * (int64_t)a.Lk * d;
     const int rounds = (a.Lk + kMmaKC - 1) / kMmaKC;
+    const int g = tid % kMmaGroups;
+    uint32_t cw[kAItems];
+    uint4 vw[kVMax];
+    shift_load_round(a, b, i0, tid, 0, vb, cw, vw);
     bool ok = true;
     for (int rd = 0; rd < rounds && ok; ++rd) {
         const int t0 = rd * kMmaKC;
         const int nks = min(kMmaKC / 16, (a.Lk - t0 + 15) / 16);  // K steps of 16 this round
         const int ntok = nks * 16;                                 // tokens written (zero past Lk)
-        // ---- A: a warp per row and 4 tokens per lane: two aligned word loads and a funnel shift
         const int gpr = ntok / 4;
-        for (int it = tid; it < kMmaRows * 32; it += 256) {
-            const int row = it >> 5, g = it & 31;
-            if (g >= gpr) continue;
-            const int i = i0 + row;
-            const int t = t0 + 4 * g;
-            uint32_t c = 0xFFFFFFFFu;  // >= 2^bits: weight 0
-            if (i < a.Lq && t < a.Lk) {
-                const uint64_t addr = (uint64_t)((b * a.Lq + i) * (int64_t)a.Lk + t);
-                const uint64_t a0 = addr & ~3ull;
-                const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(a.code + a0));
-                const uint32_t w1 = (a0 + 4 < a.code_bytes) ? __ldg(reinterpret_cast<const uint32_t *>(a.code + a0 + 4)) : 0u;
-                c = __funnelshift_r(w0, w1, (uint32_t)(addr & 3u) * 8u);
-                const int nv = a.Lk - t;
-                if (nv < 4) c |= 0xFFFFFFFFu << (8 * nv);
-            }
-            // weight high bytes: the table by code & 7; bit 3 splits lo from hi; codes >= 16 are 0
-            const uint32_t x = c & 0x07070707u;
-            const uint32_t sel = prmt(x | (x >> 4), 0u, 0x4420u);
-            const uint32_t tb = prmt(a.tab0, a.tab1, sel);
-            const uint32_t b3 = prmt(c << 4, 0u, 0xBA98u);
-            const uint32_t big = prmt(((c & 0xF0F0F0F0u) >> 1) + 0x78787878u, 0u, 0xBA98u);
-            const int kk = t - t0;
-            const uint32_t off = (uint32_t)(kk >> 6) * (kMmaRows * 128u) + (uint32_t)(row >> 3) * 1024u +
-                                 (uint32_t)(row & 7) * 128u + ((((uint32_t)(kk & 63) >> 3) ^ (uint32_t)(row & 7)) << 4) +
-                                 (uint32_t)(kk & 7) * 2u;
-            if constexpr (HI) {
-                const uint32_t lo = tb & b3 & ~big, hi = tb & ~b3 & ~big;
-                *reinterpret_cast<uint2 *>(A_lo + off) = make_uint2(prmt(lo, 0u, 0x1404u), prmt(lo, 0u, 0x3424u));
-                *reinterpret_cast<uint2 *>(A_hi + off) = make_uint2(prmt(hi, 0u, 0x1404u), prmt(hi, 0u, 0x3424u));
-            } else {
-                const uint32_t lo = tb & ~b3 & ~big;
-                *reinterpret_cast<uint2 *>(A_lo + off) = make_uint2(prmt(lo, 0u, 0x1404u), prmt(lo, 0u, 0x3424u));
+        const int chunks = ntok * d / 16;
+        if (g < gpr) {
+#pragma unroll
+            for (int u = 0; u < kAItems; ++u) {
+                const int row = tid / kMmaGroups + (256 / kMmaGroups) * u;
+                // rows past Lq hold zero weights from the first round on
+                if (rd > 0 && i0 + row >= a.Lq) continue;
+                const uint32_t c = cw[u];
+                // weight high bytes: the table by code & 7; bit 3 splits lo from hi; codes >= 16 are 0
+                const uint32_t x = c & 0x07070707u;
+                const uint32_t sel = prmt(x | (x >> 4), 0u, 0x4420u);
+                const uint32_t tb = prmt(a.tab0, a.tab1, sel);
+                const uint32_t b3 = prmt(c << 4, 0u, 0xBA98u);
+                const uint32_t big = prmt(((c & 0xF0F0F0F0u) >> 1) + 0x78787878u, 0u, 0xBA98u);
+                const int kk = 4 * g;
+                const uint32_t off = (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u +
+                                     ((((uint32_t)kk >> 3) ^ (uint32_t)(row & 7)) << 4) + (uint32_t)(kk & 7) * 2u;
+                if constexpr (HI) {
+                    const uint32_t lo = tb & b3 & ~big, hi = tb & ~b3 & ~big;
+                    *reinterpret_cast<uint2 *>(A_lo + off) = make_uint2(prmt(lo, 0u, 0x1404u), prmt(lo, 0u, 0x3424u));
+                    *reinterpret_cast<uint2 *>(A_hi + off) = make_uint2(prmt(hi, 0u, 0x1404u), prmt(hi, 0u, 0x3424u));
+                } else {
+                    const uint32_t lo = tb & ~b3 & ~big;
+                    *reinterpret_cast<uint2 *>(A_lo + off) = make_uint2(prmt(lo, 0u, 0x1404u), prmt(lo, 0u, 0x3424u));
+                }
             }
         }
-        // ---- value rows of the round into shared memory (16-byte loads, zero past Lk)
-        const int chunks = ntok * d / 16;
-        for (int it = tid; it < chunks; it += 256) {
-            const int tt = (it * 16) / d, cc = (it * 16) % d;
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            if (t0 + tt < a.Lk) w = __ldg(reinterpret_cast<const uint4 *>(vb + (int64_t)(t0 + tt) * d + cc));
-            *reinterpret_cast<uint4 *>(raw + tt * d + cc) = w;
+#pragma unroll
+        for (int u = 0; u < kVMax; ++u) {
+            const int it = tid + 256 * u;
+            if (it < chunks) *reinterpret_cast<uint4 *>(raw + it * 16) = vw[u];  // rows of d bytes
         }
         __syncthreads();
-        // ---- B: column j, 8 tokens -> one 16-byte chunk of fp16; lanes 0..7 of a quarter
-        // warp take 8 consecutive columns, so its 8 chunks land on distinct banks
+        // ---- B: column j, 8 tokens -> one 16-byte chunk of fp16 (1024 + (v + 128) - 1152
+        // = v, exactly); lanes 0..7 of a quarter warp take 8 consecutive columns, so
+        // its 8 chunks land on distinct banks
         const int groups = ntok / 8;
         for (int it = tid; it < d * groups; it += 256) {
-            const int j = it % d, gk = it / d;
+            const int gk = (int)__umulhi((uint32_t)it, a.rcp_d), j = it - gk * d;
             uint32_t bytes[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint8_t *src = raw + (gk * 8 + 4 * h) * d + j;
-                bytes[h] = (uint32_t)src[0] | ((uint32_t)src[d] << 8) | ((uint32_t)src[2 * d] << 16) |
-                           ((uint32_t)src[3 * d] << 24);
-                bytes[h] ^= 0x80808080u;  // s8 -> u8 = v + 128
+                bytes[h] = prmt(prmt((uint32_t)src[0], (uint32_t)src[d], 0x0040u),
+                                prmt((uint32_t)src[2 * d], (uint32_t)src[3 * d], 0x0040u), 0x5410u) ^
+                           0x80808080u;
             }
-            // fp16 1024 + u in each half, minus 1152: exactly v
             uint4 o;
             o.x = hsub2_u32(prmt(bytes[0], 0x64646464u, 0x5140u), 0x64806480u);
             o.y = hsub2_u32(prmt(bytes[0], 0x64646464u, 0x7362u), 0x64806480u);
             o.z = hsub2_u32(prmt(bytes[1], 0x64646464u, 0x5140u), 0x64806480u);
             o.w = hsub2_u32(prmt(bytes[1], 0x64646464u, 0x7362u), 0x64806480u);
-            const int kk = gk * 8;
-            const uint32_t off = (uint32_t)(kk >> 6) * batom + (uint32_t)(j >> 3) * 1024u + (uint32_t)(j & 7) * 128u +
-                                 ((((uint32_t)(kk & 63) >> 3) ^ (uint32_t)(j & 7)) << 4);
+            const uint32_t off = (uint32_t)(j >> 3) * 1024u + (uint32_t)(j & 7) * 128u +
+                                 ((((uint32_t)gk) ^ (uint32_t)(j & 7)) << 4);
             *reinterpret_cast<uint4 *>(Bs + off) = o;
         }
         fence_proxy_async_smem();
@@ -427,9 +468,8 @@ __global__ void __launch_bounds__(256) attn_shift_mma_kernel(const __grid_consta
             const uint64_t alo = sdesc_sw128(smem_u32(A_lo)), ahi = sdesc_sw128(smem_u32(A_hi));
             const uint64_t bd = sdesc_sw128(smem_u32(Bs));
             for (int ks = 0; ks < nks; ++ks) {
-                // descriptor addresses in 16-byte units: a K atom further, or 32 bytes (+2) per K step
-                const uint64_t aoff = (uint64_t)((ks >> 2) * (kMmaRows * 128 / 16) + (ks & 3) * 2);
-                const uint64_t boff = (uint64_t)((ks >> 2) * (batom / 16) + (ks & 3) * 2);
+                // descriptor addresses in 16-byte units: 32 bytes (+2) per K step of 16
+                const uint64_t aoff = (uint64_t)(ks * 2), boff = aoff;
                 const uint32_t acc = (rd > 0 || ks > 0) ? 1u : 0u;
                 mma_f16_ss(tmem, alo + aoff, bd + boff, idesc, acc);
                 if constexpr (HI) mma_f16_ss(tmem + (uint32_t)d, ahi + aoff, bd + boff, idesc, acc);
@@ -437,7 +477,15 @@ __global__ void __launch_bounds__(256) attn_shift_mma_kernel(const __grid_consta
             mma_commit(smem_u32(bar));
         }
         __syncwarp();
-        ok = mbar_wait(smem_u32(bar), (uint32_t)(rd & 1), a.status);
+        // the next round's codes and values travel while the MMAs run; one warp
+        // polls the barrier, the others wait at the CTA barrier without issuing
+        if (rd + 1 < rounds) shift_load_round(a, b, i0, tid, rd + 1, vb, cw, vw);
+        if (warp == 0) {
+            const bool done = mbar_wait(smem_u32(bar), (uint32_t)(rd & 1), a.status);
+            if (lane == 0) *ok_flag = done ? 1u : 0u;
+        }
+        __syncthreads();
+        ok = *reinterpret_cast<volatile uint32_t *>(ok_flag) != 0u;
         tc_fence_after();
     }
     if (ok) {
@@ -515,35 +563,68 @@ extern "C" qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t 
     if (rows == 0) return QNN_OK;
     if (x == nullptr || code == nullptr) return QNN_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(code)) return QNN_ERR_ALIGNMENT;
+    // z = c - r (b - r) must stay in (0, c] for every remainder r in [0, x0n):
+    // r <= b, and the largest r (b - r), at r nearest b / 2, below c
+    const int64_t x0n = -k.x0;
+    if (30 * x0n >= (1 << 21) || k.b < x0n - 1) return QNN_ERR_INVALID_ARG;
+    for (int64_t r : {std::min(x0n - 1, k.b / 2), std::min(x0n - 1, (k.b + 1) / 2), x0n - 1})
+        if (r * (k.b - r) >= k.c) return QNN_ERR_INVALID_ARG;
     LisArgs a{};
     a.x = x;
     a.code = code;
     a.rows = rows;
     a.L = L;
-    a.x0n = (int32_t)(-k.x0);
-    a.dmin = (int32_t)(30 * k.x0);
+    a.x0n = (uint32_t)x0n;
+    a.ndmax = (uint32_t)(30 * x0n);
     a.b = (int32_t)k.b;
     a.c = (int32_t)k.c;
-    a.rcp_x0n = 1.0f / (float)a.x0n;
+    // nd <= 30 x0n: with l = floor(log2 x0n) and m = ceil(2^(32 + l) / x0n) < 2^32 the
+    // error m x0n - 2^(32+l) < x0n keeps mulhi(nd, m) >> l = floor(nd / x0n) exact
+    // (nd x0n < 2^(32 + l)); a power of two 2^l takes m = 2^31, shift l - 1
+    int l = 0;
+    while ((2ll << l) <= x0n) ++l;
+    if (x0n == 1) {
+        a.qm = 0;
+        a.ql = 0;
+    } else if (x0n == (1ll << l)) {
+        a.qm = 1u << 31;
+        a.ql = (uint32_t)(l - 1);
+    } else {
+        a.qm = (uint32_t)(((1ull << (32 + l)) + (uint64_t)x0n - 1) / (uint64_t)x0n);
+        a.ql = (uint32_t)l;
+    }
     a.kmax = 1 << bits;
     for (int j = 1; j <= 32; ++j) {
         // D = 2 L_j - 1 is odd and >= 3: l = ceil(log2 D), m = floor(2^64 (2^l - D) / D) + 1
         const uint64_t Lj = j == 1 ? 2ull : (3ull << (j - 2));
         const uint64_t D = 2 * Lj - 1;
-        int l = 0;
-        while ((1ull << l) < D) ++l;
-        const unsigned __int128 num = ((unsigned __int128)1 << 64) * (((unsigned __int128)1 << l) - D);
+        int lj = 0;
+        while ((1ull << lj) < D) ++lj;
+        const unsigned __int128 num = ((unsigned __int128)1 << 64) * (((unsigned __int128)1 << lj) - D);
         a.magic[j - 1] = (uint64_t)(num / D) + 1;
-        a.magic_l[j - 1] = (uint32_t)l;
+        a.magic_l[j - 1] = (uint32_t)lj;
     }
     const int64_t want = (rows + kLisWarps - 1) / kLisWarps;
     const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * 8);
     cudaStream_t s = (cudaStream_t)stream;
-    if (L <= 32) log_int_softmax_kernel<1><<<grid, kLisWarps * 32, 0, s>>>(a);
-    else if (L <= 64) log_int_softmax_kernel<2><<<grid, kLisWarps * 32, 0, s>>>(a);
-    else if (L <= 128) log_int_softmax_kernel<4><<<grid, kLisWarps * 32, 0, s>>>(a);
-    else if (L <= 256) log_int_softmax_kernel<8><<<grid, kLisWarps * 32, 0, s>>>(a);
-    else log_int_softmax_kernel<0><<<grid, kLisWarps * 32, 0, s>>>(a);
+    const int R = L <= 256 ? (int)((L + 31) / 32) : 0;
+#define QNN_LIS(RR)                                                                         \
+    case RR:                                                                                \
+        if (bits == 5) log_int_softmax_kernel<RR, true><<<grid, kLisWarps * 32, 0, s>>>(a); \
+        else log_int_softmax_kernel<RR, false><<<grid, kLisWarps * 32, 0, s>>>(a);          \
+        break;
+    switch (R) {
+        QNN_LIS(1)
+        QNN_LIS(2)
+        QNN_LIS(3)
+        QNN_LIS(4)
+        QNN_LIS(5)
+        QNN_LIS(6)
+        QNN_LIS(7)
+        QNN_LIS(8)
+        QNN_LIS(0)
+    }
+#undef QNN_LIS
     return launch_status();
 }
 
@@ -579,6 +660,8 @@ extern "C" qnn_status q_attn_shift_v(const uint8_t *code, const int8_t *v, int64
         m.d = d;
         m.tab0 = (uint32_t)tab[0] | ((uint32_t)tab[1] << 8) | ((uint32_t)tab[2] << 16) | ((uint32_t)tab[3] << 24);
         m.tab1 = (uint32_t)tab[4] | ((uint32_t)tab[5] << 8) | ((uint32_t)tab[6] << 16) | ((uint32_t)tab[7] << 24);
+        m.rcp_d = (uint32_t)((0x100000000ull + (uint64_t)d - 1) / (uint64_t)d);
+        m.rcp_c = d == 16 ? 0u : (uint32_t)((0x100000000ull + (uint64_t)(d / 16) - 1) / (uint64_t)(d / 16));
         uint32_t cols = 32;
         while (cols < (uint32_t)(hi ? 2 * d : d)) cols *= 2;
         m.tmem_cols = cols;

@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
         L.oracle_log_round.argtypes = [ctypes.c_uint64]
         L.oracle_log_int_softmax.argtypes = [vp, i64, i64, f32, ctypes.c_int, vp]
         L.oracle_attn_shift_v.argtypes = [vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
+        L.oracle_int_layernorm.argtypes = [vp, i64, i64, vp, f32, vp, vp, vp, vp]
         L.oracle_set_threads.argtypes = [ctypes.c_int]
         L.oracle_get_threads.restype = ctypes.c_int
     return _lib
@@ -297,3 +298,23 @@ def attn_shift_v(code, v, bits: int = 4):
     if rc != 0:
         raise ValueError(f"oracle_attn_shift_v: error {rc}")
     return out
+
+
+# ----------------------------------------------------------------------------
+# Integer LayerNorm over PTF-quantized rows [FQ 3.2]
+
+def int_layernorm(x, s: float, gamma, beta, out_scale, alpha=None):
+    """x int codes [..., C] (real x * s * 2^alpha[c]) -> int64 output codes
+    (unclipped), per the integer mode of the page's QIntLayerNorm."""
+    x = _c(x, np.int32)
+    C = x.shape[-1]
+    rows = x.size // C
+    g = _c(np.broadcast_to(np.asarray(gamma, np.float32), (C,)), np.float32)
+    b = _c(np.broadcast_to(np.asarray(beta, np.float32), (C,)), np.float32)
+    o = _c(np.broadcast_to(np.asarray(out_scale, np.float32), (C,)), np.float32)
+    al = None if alpha is None else _c(alpha, np.uint8)
+    y = np.empty(x.shape, np.int64)
+    rc = lib().oracle_int_layernorm(_p(x), rows, C, _p(al), float(np.float32(s)), _p(g), _p(b), _p(o), _p(y))
+    if rc != 0:
+        raise ValueError(f"oracle_int_layernorm: error {rc}")
+    return y

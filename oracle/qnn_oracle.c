@@ -20,7 +20,8 @@
  *         (zero-point formula split), conv 算子優化 (img2col / implicit GEMM,
  *         Fig. 5; column permutation, Fig. 8).
  *   [FQ]  "首个完全量化Vision Transformer的方法FQ-ViT" (aijishu.com):
- *         3.2 Power-of-Two Factor; 3.3 Log Int Softmax (Attention Map 的 Log2
+ *         3.2 Power-of-Two Factor (LayerNorm 的量化推理, LayerNorm 的量化实现);
+ *         3.3 Log Int Softmax (Attention Map 的 Log2
  *         量化, Softmax 的量化推理, Integer-only 推理, Softmax 的量化的实现).
  *
  * Readings of points the pages leave open are stated next to the code that
@@ -510,5 +511,91 @@ int oracle_attn_shift_v(const uint8_t *code, const int32_t *v, int64_t heads, in
                 out[(h * Lq + i) * d + j] = acc;
             }
         }
+    return OR_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * Integer LayerNorm over PTF-quantized rows [FQ 3.2, LayerNorm 的量化推理 and
+ * LayerNorm 的量化实现, the integer mode of the printed module].  Row r of C codes
+ * x (real value x * s * 2^alpha[c]; alpha NULL = all 0):
+ *   1. x' = x * 2^alpha[c]                    (the PTF shift; exact integers)
+ *   2. mean = fp32(sum x' / C) * s;  std = (s / C) * sqrt(fp32(C sum x'^2 - (sum x')^2))
+ *   3. per channel c: A = ((s / std) * gamma[c]) / o[c]; sign, a = |A|;
+ *      N = clamp(7 - floor(log2 a), 0, 31); M = clamp(floor(a * 2^N), 0, 255);
+ *      B = round(((beta[c] - (mean / std) * gamma[c]) / o[c]) * 2^N)
+ *   4. y = round((sign * M * x' + B) / 2^N)
+ * (o = the output scale).  Readings: the integer sums and C sum x'^2 - (sum x')^2
+ * are exact (int64) -- the page computes them as float tensors; the float steps
+ * are single fp32 operations in the printed order (division, multiplication,
+ * IEEE sqrt); floor(log2 a) is the exact binary exponent of a (N = 31 for
+ * a == 0 or subnormal a); both round() are half to even, on the exact value; a
+ * row whose variance numerator is 0 (all x' equal; the page divides by zero)
+ * gives M = N = 0 and B = round(beta[c] / o[c]).  y is not clipped here: the
+ * consumer's quantizer clips it.  Returns OR_ERR_ARG for C <= 0, s or an o[c]
+ * not finite and positive, or alpha > 30. */
+static int64_t round_shift_half_even(int64_t num, int N)
+{
+    if (N == 0) return num;
+    const int64_t q = num >> N;  /* floor: arithmetic shift (gcc) */
+    const int64_t rem = num - q * ((int64_t)1 << N);
+    const int64_t half = (int64_t)1 << (N - 1);
+    return (rem > half || (rem == half && (q & 1))) ? q + 1 : q;
+}
+
+static int64_t rint_to_i64(float v)
+{
+    const double r = nearbyint((double)v);  /* default mode: half to even */
+    if (r >= 9.2e18) return INT64_MAX;
+    if (r <= -9.2e18) return INT64_MIN;
+    return (int64_t)r;
+}
+
+int oracle_int_layernorm(const int32_t *x, int64_t rows, int64_t C, const uint8_t *alpha, float s,
+                         const float *gamma, const float *beta, const float *o, int64_t *y)
+{
+    if (C <= 0 || rows < 0 || !(s > 0.0f) || !isfinite(s)) return OR_ERR_ARG;
+    for (int64_t c = 0; c < C; ++c) {
+        if (!(o[c] > 0.0f) || !isfinite(o[c])) return OR_ERR_ARG;
+        if (alpha && alpha[c] > 30) return OR_ERR_ARG;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const int32_t *xr = x + r * C;
+        int64_t sum = 0, sum2 = 0;
+        for (int64_t c = 0; c < C; ++c) {
+            const int64_t v = (int64_t)xr[c] * ((int64_t)1 << (alpha ? alpha[c] : 0));
+            sum += v;
+            sum2 += v * v;
+        }
+        const int64_t var_num = C * sum2 - sum * sum;
+        const float Cf = (float)C;
+        const float mean = ((float)sum / Cf) * s;
+        const float stdv = (s / Cf) * sqrtf((float)var_num);
+        const float s_over_std = s / stdv;
+        const float mean_over_std = mean / stdv;
+        for (int64_t c = 0; c < C; ++c) {
+            const int64_t v = (int64_t)xr[c] * ((int64_t)1 << (alpha ? alpha[c] : 0));
+            int64_t M = 0, B;
+            int N = 0, sign = 0;
+            if (var_num == 0) {
+                B = rint_to_i64(beta[c] / o[c]);
+            } else {
+                const float A = (s_over_std * gamma[c]) / o[c];
+                sign = (A > 0.0f) - (A < 0.0f);
+                const float a = fabsf(A);
+                if (a == 0.0f || !isnormal(a)) {
+                    N = 31;
+                } else {
+                    const int e = ilogbf(a);
+                    N = 7 - e < 0 ? 0 : (7 - e > 31 ? 31 : 7 - e);
+                }
+                const float m = floorf(ldexpf(a, N));
+                M = m < 0.0f ? 0 : (m > 255.0f ? 255 : (int64_t)m);
+                const float t = ((beta[c] - mean_over_std * gamma[c]) / o[c]);
+                B = rint_to_i64(ldexpf(t, N));
+            }
+            y[r * C + c] = round_shift_half_even(sign * M * v + B, N);
+        }
+    }
     return OR_OK;
 }
