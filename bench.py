@@ -512,6 +512,21 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
                                     "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
                                     "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
     del xl, codes, vq, ov
+
+    # integer LayerNorm over ViT-B activations at batch 64 (PTF factors), s8 out
+    wl = workloads.vit_layernorm()
+    lx = torch.from_numpy(wl["x"]).to(device)
+    la = torch.from_numpy(wl["alpha"]).to(device)
+    lg, lb, lo = (torch.from_numpy(wl[k]).to(device) for k in ("gamma", "beta", "o"))
+    R, C = wl["x"].shape
+    ly = torch.empty((R, C), dtype=torch.int8, device=device)
+    t = time_steps(torch, lambda: qnn.q_int_layernorm(lx, R, C, wl["s"], lg, lb, lo, ly, alpha=la,
+                                                      alpha_max=int(wl["alpha"].max()), stream=stream),
+                   steps, 3, flush, stream)
+    ms = statistics.median(t)
+    gbs = 2.0 * R * C / (ms * 1e-3) / 1e9
+    out["int_layernorm_vitb_b64"] = {"rows": R, "C": C, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                     "frac_hbm": round(gbs / hbm, 4), "bytes": "1 B in + 1 B out /elem"}
     return out
 
 
@@ -593,6 +608,15 @@ def run_case(args):
         ws = None if getattr(args, "fused", False) else torch.empty(qnn.qnn_conv_workspace_bytes(gg, "u4"),
                                                                      dtype=torch.uint8, device=device)
         fn = lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, gg, epi, O, workspace=ws, stream=stream)  # noqa: E731
+    elif case == "layernorm":
+        wl = workloads.vit_layernorm()
+        lx = torch.from_numpy(wl["x"]).to(device)
+        la = torch.from_numpy(wl["alpha"]).to(device)
+        lg, lb, lo = (torch.from_numpy(wl[k]).to(device) for k in ("gamma", "beta", "o"))
+        R, C = wl["x"].shape
+        ly = torch.empty((R, C), dtype=torch.int8, device=device)
+        fn = lambda: qnn.q_int_layernorm(lx, R, C, wl["s"], lg, lb, lo, ly, alpha=la,  # noqa: E731
+                                         alpha_max=int(wl["alpha"].max()), stream=stream)
     elif case in ("lis", "shift", "attn"):
         Bh, Lt, dh = 64 * 12, 197, 64
         xl = workloads.device_attention_logits(Bh * Lt, Lt, 1234, device)
@@ -710,7 +734,7 @@ def main():
     ap.add_argument("--case", default=None,
                     help="run one workload only (profiling): quantize, vit_fc1, square_4096, "
                          "vitl_fc2, conv3x3, conv1x1, gemm:M:N:K (u8 x s8 -> s8), lis, shift, "
-                         "attn (ViT-B b64 Log-Int-Softmax, shift product, both)")
+                         "attn (ViT-B b64 Log-Int-Softmax, shift product, both), layernorm")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -292,6 +292,27 @@ qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t L, float S,
 qnn_status q_attn_shift_v(const uint8_t *code, const int8_t *v, int64_t batch, int Lq, int Lk, int d,
                           int bits, int32_t *out, qnn_stream_t stream);
 
+/* ---- integer LayerNorm [FQ 3.2] --------------------------------------------- */
+
+/* LayerNorm of `rows` rows of C s8 codes x (row-major [rows][C]) quantized with
+ * the Power-of-Two Factor [FQ 3.2: LayerNorm 的量化推理, LayerNorm 的量化实现]:
+ * the real value of x[r][c] is x s 2^alpha[c] (alpha: u8 [C], NULL = all 0,
+ * every value <= alpha_max <= 3).  With x' = x 2^alpha, per row
+ *   mean = fp32(sum x' / C) * s,  std = (s / C) * sqrt(fp32(C sum x'^2 - (sum x')^2))
+ * (exact integer sums) and per channel c, in fp32 operations in this order,
+ *   A = ((s / std) * gamma[c]) / o[c],  N = clamp(7 - floor(log2 |A|), 0, 31)
+ *   (N = 31 for A zero or subnormal),  M = clamp(floor(|A| 2^N), 0, 255),
+ *   B = round(((beta[c] - (mean / std) * gamma[c]) / o[c]) * 2^N)  (clamped to
+ *   +-2^62 first),  y = round((sign(A) M x' + B) / 2^N)   (exact; half to even)
+ * where o = out_scale [C].  A row whose variance numerator is 0 gives
+ * y = round(beta[c] / o[c]).  y: QNN_S8 [rows][C] (clipped to -128..127, the
+ * next layer's int8 input) or QNN_S32 (clipped to the int32 range).  gamma,
+ * beta, out_scale: fp32 [C], out_scale > 0.  C % 4 == 0 (QNN_ERR_ALIGNMENT);
+ * QNN_ERR_OVERFLOW_RISK when C (128 2^alpha_max)^2 >= 2^32. */
+qnn_status q_int_layernorm(const int8_t *x, int64_t rows, int C, const uint8_t *alpha, int alpha_max, float s,
+                           const float *gamma, const float *beta, const float *out_scale, qnn_dtype y_dt,
+                           void *y, qnn_stream_t stream);
+
 /* ---- status ----------------------------------------------------------------- */
 
 const char *qnn_status_string(qnn_status s);

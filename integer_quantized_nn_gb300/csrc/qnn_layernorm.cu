@@ -1,0 +1,154 @@
+// qnn_layernorm.cu -- q_int_layernorm: integer LayerNorm over PTF-quantized rows.
+//
+// [FQ] "首个完全量化Vision Transformer的方法FQ-ViT" (aijishu.com), section 3.2
+// (LayerNorm 的量化推理, LayerNorm 的量化实现): the LayerNorm input is quantized
+// with one layer scale s and per-channel power-of-two factors 2^alpha; the row
+// statistics come from the shifted integer codes x' = x 2^alpha, and each
+// output is an integer multiply-add and a rounding shift:
+//   mean = (sum x' / C) s,  std = (s / C) sqrt(C sum x'^2 - (sum x')^2)
+//   A = (s / std) gamma / o,  N = clamp(7 - floor(log2 |A|), 0, 31),
+//   M = clamp(floor(|A| 2^N), 0, 255),  B = round((beta - (mean / std) gamma) / o 2^N)
+//   y = round((sign(A) M x' + B) / 2^N)
+// The integer sums and the variance numerator are exact; the float steps are
+// single IEEE fp32 operations in that order; both roundings are half to even.
+//
+// One warp per row, a grid-stride loop over rows.  Pass 1 reads the row as
+// 4-byte words (4 codes per lane and step), shifts by alpha and reduces sum x'
+// and sum x'^2 with warp reductions; one lane's worth of fp32 work gives the row
+// constants; pass 2 re-reads the row (from cache) with the per-channel gamma,
+// beta, o and alpha (vector loads) and writes 4 outputs per step.  The op is
+// bound by its fp32 divisions (two per element) more than by its bytes.
+#include <cuda_runtime.h>
+#include <algorithm>
+#include <cstdint>
+#include "qnn_internal.h"
+
+namespace qnn {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kLnWarps = 8;
+
+struct LnArgs {
+    const int8_t *x;
+    const uint8_t *alpha;  // [C] or nullptr
+    const float *gamma, *beta, *o;
+    void *y;
+    int64_t rows;
+    int C;
+    float s;
+};
+
+__device__ __forceinline__ int64_t round_shift_he(int64_t num, int N)
+{
+    if (N == 0) return num;
+    const int64_t q = num >> N;
+    const int64_t rem = num - (q << N);
+    const int64_t half = 1ll << (N - 1);
+    return (rem > half || (rem == half && (q & 1))) ? q + 1 : q;
+}
+
+__device__ __forceinline__ float pow2f(int n) { return __int_as_float((n + 127) << 23); }
+
+template <bool S8>
+__global__ void __launch_bounds__(kLnWarps * 32) int_layernorm_kernel(const __grid_constant__ LnArgs a)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int words = a.C >> 2;
+    for (int64_t row = (int64_t)blockIdx.x * kLnWarps + w; row < a.rows; row += (int64_t)gridDim.x * kLnWarps) {
+        const uint32_t *xr = reinterpret_cast<const uint32_t *>(a.x + row * a.C);
+        int32_t sum = 0;
+        uint32_t sum2 = 0;
+        for (int k = lane; k < words; k += 32) {
+            const uint32_t xw = __ldg(xr + k);
+            const uint32_t aw = a.alpha ? __ldg(reinterpret_cast<const uint32_t *>(a.alpha) + k) : 0u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int32_t v = (int32_t)(int8_t)(xw >> (8 * q)) * (1 << ((aw >> (8 * q)) & 0xffu));
+                sum += v;
+                sum2 += (uint32_t)(v * v);
+            }
+        }
+        sum = __reduce_add_sync(kFull, sum);
+        sum2 = __reduce_add_sync(kFull, sum2);
+        const int64_t var_num = (int64_t)a.C * (int64_t)sum2 - (int64_t)sum * (int64_t)sum;
+        const float Cf = (float)a.C;
+        const float mean = __fmul_rn(__fdiv_rn((float)sum, Cf), a.s);
+        const float stdv = __fmul_rn(__fdiv_rn(a.s, Cf), __fsqrt_rn(__ll2float_rn(var_num)));
+        const float sos = __fdiv_rn(a.s, stdv);
+        const float mos = __fdiv_rn(mean, stdv);
+        for (int k = lane; k < words; k += 32) {
+            const uint32_t xw = __ldg(xr + k);
+            const uint32_t aw = a.alpha ? __ldg(reinterpret_cast<const uint32_t *>(a.alpha) + k) : 0u;
+            const float4 g4 = __ldg(reinterpret_cast<const float4 *>(a.gamma) + k);
+            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(a.beta) + k);
+            const float4 o4 = __ldg(reinterpret_cast<const float4 *>(a.o) + k);
+            const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, bs[4] = {b4.x, b4.y, b4.z, b4.w},
+                        os[4] = {o4.x, o4.y, o4.z, o4.w};
+            int64_t yv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t v = (int64_t)((int32_t)(int8_t)(xw >> (8 * q)) * (1 << ((aw >> (8 * q)) & 0xffu)));
+                int64_t M = 0, B;
+                int N = 0, sign = 0;
+                const float lim = 4611686018427387904.0f;  // 2^62: B is rounded after this clamp
+                if (var_num == 0) {
+                    B = __float2ll_rn(fminf(fmaxf(__fdiv_rn(bs[q], os[q]), -lim), lim));
+                } else {
+                    const float A = __fdiv_rn(__fmul_rn(sos, gs[q]), os[q]);
+                    sign = (A > 0.0f) - (A < 0.0f);
+                    const float am = fabsf(A);
+                    const int ex = (__float_as_int(am) >> 23) & 0xff;  // 0: zero or subnormal
+                    N = ex == 0 ? 31 : min(max(7 - (ex - 127), 0), 31);
+                    M = min((int64_t)floorf(fminf(__fmul_rn(am, pow2f(N)), 256.0f)), (int64_t)255);
+                    const float t = __fdiv_rn(__fsub_rn(bs[q], __fmul_rn(mos, gs[q])), os[q]);
+                    B = __float2ll_rn(fminf(fmaxf(__fmul_rn(t, pow2f(N)), -lim), lim));
+                }
+                yv[q] = round_shift_he((int64_t)sign * M * v + B, N);
+            }
+            if constexpr (S8) {
+                uint32_t ow = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    ow |= ((uint32_t)(uint8_t)(int8_t)min(max(yv[q], (int64_t)-128), (int64_t)127)) << (8 * q);
+                reinterpret_cast<uint32_t *>(a.y)[row * words + k] = ow;
+            } else {
+                int4 ov;
+                ov.x = (int32_t)min(max(yv[0], (int64_t)INT32_MIN), (int64_t)INT32_MAX);
+                ov.y = (int32_t)min(max(yv[1], (int64_t)INT32_MIN), (int64_t)INT32_MAX);
+                ov.z = (int32_t)min(max(yv[2], (int64_t)INT32_MIN), (int64_t)INT32_MAX);
+                ov.w = (int32_t)min(max(yv[3], (int64_t)INT32_MIN), (int64_t)INT32_MAX);
+                reinterpret_cast<int4 *>(a.y)[row * words + k] = ov;
+            }
+        }
+    }
+}
+
+}  // namespace
+}  // namespace qnn
+
+extern "C" qnn_status q_int_layernorm(const int8_t *x, int64_t rows, int C, const uint8_t *alpha, int alpha_max,
+                                      float s, const float *gamma, const float *beta, const float *out_scale,
+                                      qnn_dtype y_dt, void *y, qnn_stream_t stream)
+{
+    using namespace qnn;
+    if (rows < 0 || C <= 0 || alpha_max < 0 || alpha_max > 3) return QNN_ERR_INVALID_ARG;
+    if (!(s > 0.0f) || !(s < INFINITY)) return QNN_ERR_INVALID_ARG;
+    if (y_dt != QNN_S8 && y_dt != QNN_S32) return QNN_ERR_UNSUPPORTED;
+    if (C % 4 != 0) return QNN_ERR_ALIGNMENT;
+    // sum x'^2 <= C (128 2^alpha_max)^2 must fit 32 bits
+    if ((uint64_t)C * (uint64_t)(128u << alpha_max) * (uint64_t)(128u << alpha_max) >= (1ull << 32))
+        return QNN_ERR_OVERFLOW_RISK;
+    if (rows == 0) return QNN_OK;
+    if (!x || !gamma || !beta || !out_scale || !y) return QNN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out_scale) || !aligned16(y) ||
+        (alpha && !aligned16(alpha)))
+        return QNN_ERR_ALIGNMENT;
+    LnArgs a{x, alpha, gamma, beta, out_scale, y, rows, C, s};
+    const int64_t want = (rows + kLnWarps - 1) / kLnWarps;
+    const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * 8);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (y_dt == QNN_S8) int_layernorm_kernel<true><<<grid, kLnWarps * 32, 0, st>>>(a);
+    else int_layernorm_kernel<false><<<grid, kLnWarps * 32, 0, st>>>(a);
+    return launch_status();
+}

@@ -83,6 +83,7 @@ def _declare(L):
         "qconv_u8s8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
         "q_log_int_softmax": (c_int, [vp, i64, i64, f32, c_int, vp, vp]),
         "q_attn_shift_v": (c_int, [vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp]),
+        "q_int_layernorm": (c_int, [vp, i64, c_int, vp, c_int, f32, vp, vp, vp, c_int, vp, vp]),
         "qnn_status_string": (ctypes.c_char_p, [c_int]),
         "qnn_check_device_error": (c_int, [vp]),
         "qnn_selftest_wait_timeout": (c_int, [ctypes.c_uint64, vp]),
@@ -298,6 +299,15 @@ def q_attn_shift_v(code, v, batch: int, Lq: int, Lk: int, d: int, bits: int, out
     load()
     _check(_SYMBOLS["q_attn_shift_v"](_ptr(code), _ptr(v), int(batch), int(Lq), int(Lk), int(d),
                                        int(bits), _ptr(out), _stream(stream)), "q_attn_shift_v")
+
+
+def q_int_layernorm(x, rows: int, C: int, s: float, gamma, beta, out_scale, y, y_dt: str = "s8",
+                    alpha=None, alpha_max: int = 0, stream=None):
+    """Integer LayerNorm of s8 rows x [rows, C] with PTF factors alpha (u8 [C])."""
+    load()
+    _check(_SYMBOLS["q_int_layernorm"](_ptr(x), int(rows), int(C), _ptr(alpha), int(alpha_max), float(s),
+                                        _ptr(gamma), _ptr(beta), _ptr(out_scale), DTYPES[y_dt], _ptr(y),
+                                        _stream(stream)), "q_int_layernorm")
 
 
 def qnn_check_device_error(stream=None) -> int:

@@ -19,6 +19,8 @@ Workloads (the layer shapes of the pages' models stand in for their datasets):
   quant_rows    : fp32 -> s8 per-row symmetric quantize of a 16384^2 tensor
   vit_attention : ViT-B self-attention maps (12 heads, 197 tokens, head dim 64):
                   int32 logit codes of Q K^T, s8 value codes, for Log-Int-Softmax
+  vit_layernorm : ViT-B LayerNorm inputs (197 tokens x 768 channels), s8 codes with
+                  per-channel power-of-two factors, for the integer LayerNorm
 """
 from __future__ import annotations
 
@@ -26,7 +28,7 @@ import math
 import numpy as np
 
 # workload ids (seed = 1000 * id + tensor id)
-GEMM_SYM, VIT_FC1, CONV_U4, VITL_PTF, SQUARE, ATTN = 1, 2, 3, 4, 5, 6
+GEMM_SYM, VIT_FC1, CONV_U4, VITL_PTF, SQUARE, ATTN, LNORM = 1, 2, 3, 4, 5, 6, 7
 
 
 def rng(workload: int, tensor: int) -> np.random.Generator:
@@ -173,6 +175,20 @@ def device_attention_logits(rows, L, seed, device):
     z = torch.randn((rows, L), generator=g, device=device, dtype=torch.float32) * 2.5
     z[:, 0] += 4.0
     return torch.round(z / ATTN_S).to(torch.int32)
+
+
+def vit_layernorm(rows=64 * 197, C=768, tag=0):
+    """LayerNorm input codes x = clip(round(N(0, 30))) (s8) at layer scale s = 0.02
+    with per-channel factors alpha: 5% of the channels (seeded) carry 2^3, the
+    inter-channel spread PTF is for; gamma = U(0.5, 1.5) with random signs,
+    beta ~ N(0, 0.2); one output scale 0.04 for all channels."""
+    x = _normal_codes(rng(LNORM, 10 * tag + 0), 0.0, 30.0, -128, 127, (rows, C), np.int8)
+    g = rng(LNORM, 10 * tag + 1)
+    alpha = np.where(g.random(C) < 0.05, 3, 0).astype(np.uint8)
+    gamma = (g.uniform(0.5, 1.5, size=C) * g.choice([-1.0, 1.0], size=C)).astype(np.float32)
+    beta = g.normal(0.0, 0.2, size=C).astype(np.float32)
+    o = np.full(C, 0.04, np.float32)
+    return dict(x=x, alpha=alpha, s=0.02, gamma=gamma, beta=beta, o=o)
 
 
 def device_uniform_s8(shape, seed, device):

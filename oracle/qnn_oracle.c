@@ -531,8 +531,9 @@ int oracle_attn_shift_v(const uint8_t *code, const int32_t *v, int64_t heads, in
  * a == 0 or subnormal a); both round() are half to even, on the exact value; a
  * row whose variance numerator is 0 (all x' equal; the page divides by zero)
  * gives M = N = 0 and B = round(beta[c] / o[c]).  y is not clipped here: the
- * consumer's quantizer clips it.  Returns OR_ERR_ARG for C <= 0, s or an o[c]
- * not finite and positive, or alpha > 30. */
+ * consumer's quantizer clips it.  B is rounded after clamping to +-2^62.
+ * Returns OR_ERR_ARG for C <= 0, s or an o[c] not finite and positive, or
+ * alpha > 30. */
 static int64_t round_shift_half_even(int64_t num, int N)
 {
     if (N == 0) return num;
@@ -542,12 +543,14 @@ static int64_t round_shift_half_even(int64_t num, int N)
     return (rem > half || (rem == half && (q & 1))) ? q + 1 : q;
 }
 
+/* round half to even of an fp32 value, clamped to +-2^62 first (a bound no
+ * real LayerNorm constant reaches; it keeps sign * M * x' + B inside int64). */
 static int64_t rint_to_i64(float v)
 {
-    const double r = nearbyint((double)v);  /* default mode: half to even */
-    if (r >= 9.2e18) return INT64_MAX;
-    if (r <= -9.2e18) return INT64_MIN;
-    return (int64_t)r;
+    const float lim = 4611686018427387904.0f; /* 2^62 */
+    if (v > lim) v = lim;
+    if (v < -lim) v = -lim;
+    return (int64_t)nearbyintf(v); /* default mode: half to even */
 }
 
 int oracle_int_layernorm(const int32_t *x, int64_t rows, int64_t C, const uint8_t *alpha, float s,

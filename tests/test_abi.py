@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     for n in ("q_quantize", "q_dequantize", "qgemm_prepack_b", "q_fold_epilogue", "qgemm_s8",
               "qnn_gemm_workspace_bytes", "qgemm_pack_a", "qgemm_s8_packed", "qgemm_s8_static_scratch",
               "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_conv_workspace_bytes",
-              "q_log_int_softmax", "q_attn_shift_v", "qnn_status_string",
+              "q_log_int_softmax", "q_attn_shift_v", "q_int_layernorm", "qnn_status_string",
               "qnn_check_device_error"):
         assert n in names
 
@@ -126,6 +126,26 @@ def test_lis_arguments_rejected_on_host(lib):
     assert L.q_attn_shift_v(16, 16, 1, 4, 513, 16, 4, 16, None) == qnn.QNN_ERR_OVERFLOW_RISK
     assert L.q_attn_shift_v(16, 16, 1, 4, 512, 16, 4, 20, None) == qnn.QNN_ERR_ALIGNMENT
     assert L.q_attn_shift_v(None, None, 0, 4, 512, 16, 4, None, None) == ok
+
+
+def test_int_layernorm_arguments_rejected_on_host(lib):
+    L = lib
+    args = lambda **k: dict(dict(x=16, rows=4, C=768, al=None, amax=0, s=0.1, g=16, b=16, o=16, dt=0, y=16), **k)
+
+    def call(**k):
+        a = args(**k)
+        return L.q_int_layernorm(a["x"], a["rows"], a["C"], a["al"], a["amax"], a["s"], a["g"], a["b"], a["o"],
+                                 a["dt"], a["y"], None)
+    assert call(amax=4) == qnn.QNN_ERR_INVALID_ARG
+    assert call(s=0.0) == qnn.QNN_ERR_INVALID_ARG
+    assert call(s=float("inf")) == qnn.QNN_ERR_INVALID_ARG
+    assert call(C=0) == qnn.QNN_ERR_INVALID_ARG
+    assert call(dt=1) == qnn.QNN_ERR_UNSUPPORTED
+    assert call(C=770) == qnn.QNN_ERR_ALIGNMENT
+    assert call(C=8192, amax=3) == qnn.QNN_ERR_OVERFLOW_RISK
+    assert call(rows=0, x=None, y=None) == qnn.QNN_OK
+    assert call(x=None) == qnn.QNN_ERR_INVALID_ARG
+    assert call(g=20) == qnn.QNN_ERR_ALIGNMENT
 
 
 def test_packed_sizes(lib):
