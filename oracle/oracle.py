@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_log_int_softmax.argtypes = [vp, i64, i64, f32, ctypes.c_int, vp]
         L.oracle_attn_shift_v.argtypes = [vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
         L.oracle_int_layernorm.argtypes = [vp, i64, i64, vp, f32, vp, vp, vp, vp]
+        L.oracle_eltwise_s8.argtypes = [ctypes.c_int, vp, vp, i64, f32, ctypes.c_int, vp]
+        L.oracle_quantize_rows_dynamic.argtypes = [vp, i64, i64, ctypes.c_int, vp, vp]
         L.oracle_set_threads.argtypes = [ctypes.c_int]
         L.oracle_get_threads.restype = ctypes.c_int
     return _lib
@@ -318,3 +320,32 @@ def int_layernorm(x, s: float, gamma, beta, out_scale, alpha=None):
     if rc != 0:
         raise ValueError(f"oracle_int_layernorm: error {rc}")
     return y
+
+
+# ----------------------------------------------------------------------------
+# Standalone quantized elementwise ops and dynamic per-row quantization [QI]
+
+ELTWISE = {"add": 0, "mul": 1, "relu": 2}
+
+
+def eltwise_s8(op: str, a, b=None, M: float = 1.0, relu: bool = False):
+    a = _c(a, np.int32)
+    b = a if b is None else _c(b, np.int32)
+    assert a.shape == b.shape
+    out = np.empty(a.shape, np.int32)
+    rc = lib().oracle_eltwise_s8(ELTWISE[op], _p(a), _p(b), a.size, float(np.float32(M)), int(relu), _p(out))
+    if rc != 0:
+        raise ValueError(f"oracle_eltwise_s8: error {rc}")
+    return out
+
+
+def quantize_rows_dynamic(x, narrow: bool = False):
+    """x fp32 [rows, cols] -> (int32 codes, fp32 per-row scales max|x| / 127)."""
+    x = _c(x, np.float32)
+    rows, cols = x.shape
+    q = np.empty(x.shape, np.int32)
+    sc = np.empty(rows, np.float32)
+    rc = lib().oracle_quantize_rows_dynamic(_p(x), rows, cols, int(narrow), _p(q), _p(sc))
+    if rc != 0:
+        raise ValueError(f"oracle_quantize_rows_dynamic: error {rc}")
+    return q, sc

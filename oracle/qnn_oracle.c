@@ -602,3 +602,55 @@ int oracle_int_layernorm(const int32_t *x, int64_t rows, int64_t C, const uint8_
     }
     return OR_OK;
 }
+
+/* ---------------------------------------------------------------------------
+ * Standalone quantized elementwise ops on s8 codes [QI 量化乘法, 量化加法,
+ * 量化激活函数], symmetric (zero points 0):
+ *   MUL : out = clip(rint((float)(a * b) * M)),  M = s_a s_b / s_c computed ahead
+ *   ADD : out = clip(rint((float)(a + b) * M)),  M = s_ab / s_c, the operands
+ *         sharing one scale s_ab (the page requires it)
+ *   RELU: out = max(a, 0)   (a passive op: same scale in and out, no rounding)
+ * then, with relu set, max(out, 0).  Readings: the rescale is a multiplication by
+ * the precomputed fp32 M (the page divides by scale_abc = 1 / M; the library's
+ * requant epilogue multiplies too); clip to [-128, 127]; rint is half to even.
+ * The integer variant of the page (a shift by round(log2 scale_abc)) is the case
+ * M = 2^-k, exact in fp32.  op: 0 ADD, 1 MUL, 2 RELU. */
+int oracle_eltwise_s8(int op, const int32_t *a, const int32_t *b, int64_t n, float M, int relu, int32_t *out)
+{
+    if (op < 0 || op > 2) return OR_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) {
+        int32_t v;
+        if (op == 2) {
+            v = a[i] > 0 ? a[i] : 0;
+        } else {
+            const int32_t t = op == 0 ? a[i] + b[i] : a[i] * b[i];
+            const float r = rintf((float)t * M);
+            v = (int32_t)clamp_f(r, -128.0f, 127.0f);
+        }
+        if (relu && v < 0) v = 0;
+        out[i] = v;
+    }
+    return OR_OK;
+}
+
+/* Dynamic per-row symmetric quantization [QI 量化参数选择, 最大值截断: the scale
+ * is the largest magnitude over 127 -- the page writes -127 for symmetry; QI
+ * 量化算子: q = clip(round(x / s))]:  s[r] = max_c |x[r][c]| / 127 (one fp32
+ * division), q = clip(rint(x / s[r]), qmin, qmax) (one IEEE division each, as in
+ * oracle_quantize).  A row of zeros gets s = 0 and codes 0.  narrow selects
+ * [-127, 127], else [-128, 127].  Inputs must be finite. */
+int oracle_quantize_rows_dynamic(const float *x, int64_t rows, int64_t cols, int narrow, int32_t *q, float *scale)
+{
+    if (rows < 0 || cols <= 0) return OR_ERR_ARG;
+    const float qmin = narrow ? -127.0f : -128.0f;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols;
+        float amax = 0.0f;
+        for (int64_t c = 0; c < cols; ++c) amax = fmaxf(amax, fabsf(xr[c]));
+        const float sc = amax / 127.0f;
+        scale[r] = sc;
+        for (int64_t c = 0; c < cols; ++c)
+            q[r * cols + c] = sc == 0.0f ? 0 : (int32_t)clamp_f(rintf(xr[c] / sc), qmin, 127.0f);
+    }
+    return OR_OK;
+}
