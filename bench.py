@@ -527,6 +527,26 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
     gbs = 2.0 * R * C / (ms * 1e-3) / 1e9
     out["int_layernorm_vitb_b64"] = {"rows": R, "C": C, "ms": round(ms, 4), "GB/s": round(gbs, 1),
                                      "frac_hbm": round(gbs / hbm, 4), "bytes": "1 B in + 1 B out /elem"}
+
+    # standalone quantized add (shared scale) on the ViT-B residual stream, and the
+    # dynamic per-token quantize of the same fp32 activations
+    ea = workloads.device_uniform_s8((R, C), 91, device)
+    eb = workloads.device_uniform_s8((R, C), 92, device)
+    eo = torch.empty((R, C), dtype=torch.int8, device=device)
+    t = time_steps(torch, lambda: qnn.q_eltwise_s8("add", ea, eb, R * C, 0.5, eo, stream=stream), steps, 3,
+                   flush, stream)
+    ms = statistics.median(t)
+    gbs = 3.0 * R * C / (ms * 1e-3) / 1e9
+    out["eltwise_add_s8_vitb_b64"] = {"n": R * C, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                      "frac_hbm": round(gbs / hbm, 4), "bytes": "3 B /elem"}
+    xf = workloads.device_normal_f32((R, C), 93, device)
+    dsc = torch.empty(R, dtype=torch.float32, device=device)
+    t = time_steps(torch, lambda: qnn.q_quantize_rows_dynamic(xf, R, C, eo, dsc, stream=stream), steps, 3,
+                   flush, stream)
+    ms = statistics.median(t)
+    gbs = 5.0 * R * C / (ms * 1e-3) / 1e9
+    out["quantize_rows_dynamic_vitb_b64"] = {"rows": R, "cols": C, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                             "frac_hbm": round(gbs / hbm, 4), "bytes": "4 B in + 1 B out /elem"}
     return out
 
 
@@ -608,6 +628,18 @@ def run_case(args):
         ws = None if getattr(args, "fused", False) else torch.empty(qnn.qnn_conv_workspace_bytes(gg, "u4"),
                                                                      dtype=torch.uint8, device=device)
         fn = lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, gg, epi, O, workspace=ws, stream=stream)  # noqa: E731
+    elif case == "eltwise":
+        R, C = 64 * 197, 768
+        ea = workloads.device_uniform_s8((R, C), 91, device)
+        eb = workloads.device_uniform_s8((R, C), 92, device)
+        eo = torch.empty((R, C), dtype=torch.int8, device=device)
+        fn = lambda: qnn.q_eltwise_s8("add", ea, eb, R * C, 0.5, eo, stream=stream)  # noqa: E731
+    elif case == "dynquant":
+        R, C = 64 * 197, 768
+        xf = workloads.device_normal_f32((R, C), 93, device)
+        eo = torch.empty((R, C), dtype=torch.int8, device=device)
+        dsc = torch.empty(R, dtype=torch.float32, device=device)
+        fn = lambda: qnn.q_quantize_rows_dynamic(xf, R, C, eo, dsc, stream=stream)  # noqa: E731
     elif case == "layernorm":
         wl = workloads.vit_layernorm()
         lx = torch.from_numpy(wl["x"]).to(device)
@@ -734,7 +766,7 @@ def main():
     ap.add_argument("--case", default=None,
                     help="run one workload only (profiling): quantize, vit_fc1, square_4096, "
                          "vitl_fc2, conv3x3, conv1x1, gemm:M:N:K (u8 x s8 -> s8), lis, shift, "
-                         "attn (ViT-B b64 Log-Int-Softmax, shift product, both), layernorm")
+                         "attn (ViT-B b64 Log-Int-Softmax, shift product, both), layernorm, eltwise, dynquant")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

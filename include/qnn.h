@@ -313,6 +313,30 @@ qnn_status q_int_layernorm(const int8_t *x, int64_t rows, int C, const uint8_t *
                            const float *gamma, const float *beta, const float *out_scale, qnn_dtype y_dt,
                            void *y, qnn_stream_t stream);
 
+/* ---- standalone elementwise ops and dynamic quantization [QI] ----------------- */
+
+typedef enum { QNN_ADD = 0, QNN_MUL = 1, QNN_RELU = 2 } qnn_eltwise_op;
+
+/* Elementwise ops on n symmetric s8 codes [QI 量化加法, 量化乘法, 量化激活函数]:
+ *   QNN_ADD : out = clip(rint((float)(a + b) * M))  -- a and b share one scale
+ *             (the page requires it), M = s_ab / s_out
+ *   QNN_MUL : out = clip(rint((float)(a * b) * M))  -- M = s_a s_b / s_out, computed
+ *             ahead; M = 2^-k is the page's shift variant
+ *   QNN_RELU: out = max(a, 0)                        -- passive: b and M unused
+ * clip to [-128, 127], rint half to even, one fp32 multiply; relu != 0 applies
+ * max(., 0) after the rescale.  a, b, out: device s8 [n], 16-byte aligned. */
+qnn_status q_eltwise_s8(qnn_eltwise_op op, const int8_t *a, const int8_t *b, int64_t n, float M, int relu,
+                        int8_t *out, qnn_stream_t stream);
+
+/* Dynamic per-row symmetric quantization [QI 量化参数选择: max truncation, the scale
+ * the largest magnitude over 127; 量化算子]: for each of `rows` rows of `cols`
+ * fp32 values, scale[r] = max|x[r]| / 127 (IEEE fp32 division) and
+ * q[r][c] = clip(rint(x[r][c] / scale[r])) (one IEEE division each) to [-128, 127],
+ * or [-127, 127] with narrow != 0.  A row of zeros gets scale 0 and codes 0.
+ * x must be finite.  cols % 4 == 0.  q: s8 [rows][cols]; scale: fp32 [rows]. */
+qnn_status q_quantize_rows_dynamic(const float *x, int64_t rows, int64_t cols, int narrow, int8_t *q,
+                                   float *scale, qnn_stream_t stream);
+
 /* ---- status ----------------------------------------------------------------- */
 
 const char *qnn_status_string(qnn_status s);

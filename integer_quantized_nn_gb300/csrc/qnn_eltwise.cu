@@ -1,0 +1,147 @@
+// qnn_eltwise.cu -- standalone quantized elementwise ops and dynamic per-row
+// quantization: memory-bound kernels.
+//
+// q_eltwise_s8 [QI] "【量化】神经网络量化介绍", sections 量化乘法 / 量化加法 /
+// 量化激活函数: on symmetric s8 codes,
+//   ADD : clip(rint((a + b) * M))   (operands sharing one scale; M = s_ab / s_c)
+//   MUL : clip(rint((a * b) * M))   (M = s_a s_b / s_c, computed ahead)
+//   RELU: max(a, 0)                 (passive: scale unchanged)
+// with an optional ReLU after the rescale.  The integer sum or product is exact in
+// fp32 (|t| <= 2^14); one fp32 multiply, round half to even, clip to [-128, 127].
+// Each thread handles 16 elements per step: two 16-byte loads and one 16-byte
+// store; a grid-stride loop, the n % 16 tail by the first threads.
+//
+// q_quantize_rows_dynamic [QI 量化参数选择 (最大值截断), 量化算子]: per row the
+// scale max|x| / 127 (one IEEE division), then q = clip(rint(x / s)) with one
+// IEEE division per element; a zero row gets scale 0 and codes 0.  One warp per
+// row: the row is read twice (the second time from cache), 4 floats per lane and
+// step, codes stored as 4-byte words.
+#include <cuda_runtime.h>
+#include <algorithm>
+#include <cstdint>
+#include "qnn_internal.h"
+
+namespace qnn {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int OP>
+__device__ __forceinline__ int32_t elt(int32_t a, int32_t b, float M, bool relu)
+{
+    int32_t v;
+    if constexpr (OP == QNN_RELU) {
+        v = max(a, 0);
+    } else {
+        const int32_t t = OP == QNN_ADD ? a + b : a * b;
+        v = min(max(__float2int_rn(__fmul_rn((float)t, M)), -128), 127);
+    }
+    return relu ? max(v, 0) : v;
+}
+
+template <int OP>
+__global__ void __launch_bounds__(256) eltwise_s8_kernel(const int8_t *__restrict__ a, const int8_t *__restrict__ b,
+                                                         int64_t n, float M, int relu, int8_t *__restrict__ out)
+{
+    const int64_t nv = n >> 4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+        const uint4 av = __ldcs(reinterpret_cast<const uint4 *>(a) + i);
+        uint4 bv = av;
+        if constexpr (OP != QNN_RELU) bv = __ldcs(reinterpret_cast<const uint4 *>(b) + i);
+        const uint32_t aw[4] = {av.x, av.y, av.z, av.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
+        uint32_t ow[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t o = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int32_t x = (int32_t)(int8_t)(aw[w] >> (8 * q)), y = (int32_t)(int8_t)(bw[w] >> (8 * q));
+                o |= (uint32_t)(uint8_t)elt<OP>(x, y, M, relu != 0) << (8 * q);
+            }
+            ow[w] = o;
+        }
+        __stcs(reinterpret_cast<uint4 *>(out) + i, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+    }
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < (n & 15)) {
+        const int64_t k = (nv << 4) + t;
+        out[k] = (int8_t)elt<OP>(a[k], OP == QNN_RELU ? 0 : b[k], M, relu != 0);
+    }
+}
+
+__global__ void __launch_bounds__(256) quantize_rows_dynamic_kernel(const float *__restrict__ x, int64_t rows,
+                                                                    int64_t cols, int narrow, int8_t *__restrict__ q,
+                                                                    float *__restrict__ scale)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t words = cols >> 2;
+    const int32_t qmin = narrow ? -127 : -128;
+    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < rows;
+         row += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        const float4 *xr = reinterpret_cast<const float4 *>(x + row * cols);
+        float amax = 0.0f;
+        for (int64_t k = lane; k < words; k += 32) {
+            const float4 v = __ldg(xr + k);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+        // magnitudes are non-negative: their bit patterns order like the values
+        amax = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
+        const float s = __fdiv_rn(amax, 127.0f);
+        if (lane == 0) scale[row] = s;
+        uint32_t *qr = reinterpret_cast<uint32_t *>(q + row * cols);
+        for (int64_t k = lane; k < words; k += 32) {
+            const float4 v = __ldcs(xr + k);
+            const float vs[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int32_t c = s == 0.0f ? 0 : min(max(__float2int_rn(__fdiv_rn(vs[j], s)), qmin), 127);
+                o |= (uint32_t)(uint8_t)c << (8 * j);
+            }
+            __stcs(qr + k, o);
+        }
+    }
+}
+
+int grid_for(int64_t work, int per_block)
+{
+    const int64_t want = (work + per_block - 1) / per_block;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 8));
+}
+
+}  // namespace
+}  // namespace qnn
+
+extern "C" qnn_status q_eltwise_s8(qnn_eltwise_op op, const int8_t *a, const int8_t *b, int64_t n, float M,
+                                   int relu, int8_t *out, qnn_stream_t stream)
+{
+    using namespace qnn;
+    if (n < 0 || (op != QNN_ADD && op != QNN_MUL && op != QNN_RELU)) return QNN_ERR_INVALID_ARG;
+    if (op != QNN_RELU && !(M == M && M < INFINITY && M > -INFINITY)) return QNN_ERR_INVALID_ARG;
+    if (n == 0) return QNN_OK;
+    if (!a || !out || (op != QNN_RELU && !b)) return QNN_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(out) || (op != QNN_RELU && !aligned16(b))) return QNN_ERR_ALIGNMENT;
+    const int grid = grid_for(std::max<int64_t>(n >> 4, 16), 256);
+    cudaStream_t s = (cudaStream_t)stream;
+    switch (op) {
+    case QNN_ADD: eltwise_s8_kernel<QNN_ADD><<<grid, 256, 0, s>>>(a, b, n, M, relu, out); break;
+    case QNN_MUL: eltwise_s8_kernel<QNN_MUL><<<grid, 256, 0, s>>>(a, b, n, M, relu, out); break;
+    default: eltwise_s8_kernel<QNN_RELU><<<grid, 256, 0, s>>>(a, a, n, M, relu, out); break;
+    }
+    return launch_status();
+}
+
+extern "C" qnn_status q_quantize_rows_dynamic(const float *x, int64_t rows, int64_t cols, int narrow, int8_t *q,
+                                              float *scale, qnn_stream_t stream)
+{
+    using namespace qnn;
+    if (rows < 0 || cols <= 0) return QNN_ERR_INVALID_ARG;
+    if (cols % 4 != 0) return QNN_ERR_ALIGNMENT;
+    if (rows == 0) return QNN_OK;
+    if (!x || !q || !scale) return QNN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return QNN_ERR_ALIGNMENT;
+    const int grid = grid_for(rows, 8);
+    quantize_rows_dynamic_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(x, rows, cols, narrow, q, scale);
+    return launch_status();
+}

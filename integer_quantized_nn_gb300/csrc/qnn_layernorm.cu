@@ -88,23 +88,36 @@ __global__ void __launch_bounds__(kLnWarps * 32) int_layernorm_kernel(const __gr
             int64_t yv[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int64_t v = (int64_t)((int32_t)(int8_t)(xw >> (8 * q)) * (1 << ((aw >> (8 * q)) & 0xffu)));
-                int64_t M = 0, B;
-                int N = 0, sign = 0;
-                const float lim = 4611686018427387904.0f;  // 2^62: B is rounded after this clamp
+                const int32_t v = (int32_t)(int8_t)(xw >> (8 * q)) * (1 << ((aw >> (8 * q)) & 0xffu));
+                int32_t M = 0;  // signed: sign(A) M
+                int N = 0;
+                float bt;       // B before rounding
                 if (var_num == 0) {
-                    B = __float2ll_rn(fminf(fmaxf(__fdiv_rn(bs[q], os[q]), -lim), lim));
+                    bt = __fdiv_rn(bs[q], os[q]);
                 } else {
                     const float A = __fdiv_rn(__fmul_rn(sos, gs[q]), os[q]);
-                    sign = (A > 0.0f) - (A < 0.0f);
                     const float am = fabsf(A);
                     const int ex = (__float_as_int(am) >> 23) & 0xff;  // 0: zero or subnormal
-                    N = ex == 0 ? 31 : min(max(7 - (ex - 127), 0), 31);
-                    M = min((int64_t)floorf(fminf(__fmul_rn(am, pow2f(N)), 256.0f)), (int64_t)255);
+                    N = ex == 0 ? 31 : min(max(134 - ex, 0), 31);  // 7 - (ex - 127)
+                    M = min(__float2int_rd(fminf(__fmul_rn(am, pow2f(N)), 256.0f)), 255);
+                    if (A < 0.0f) M = -M;
                     const float t = __fdiv_rn(__fsub_rn(bs[q], __fmul_rn(mos, gs[q])), os[q]);
-                    B = __float2ll_rn(fminf(fmaxf(__fmul_rn(t, pow2f(N)), -lim), lim));
+                    bt = __fmul_rn(t, pow2f(N));
                 }
-                yv[q] = round_shift_he((int64_t)sign * M * v + B, N);
+                // |M x'| < 2^18: with |B| < 2^30 and N <= 30 everything fits 32 bits
+                if (fabsf(bt) < 1073741824.0f && N <= 30) {
+                    const int32_t num = M * v + __float2int_rn(bt);
+                    int32_t y32 = num;
+                    if (N > 0) {
+                        const int32_t qf = num >> N, rem = num & ((1 << N) - 1), half = 1 << (N - 1);
+                        y32 = (rem > half || (rem == half && (qf & 1))) ? qf + 1 : qf;
+                    }
+                    yv[q] = y32;
+                } else {
+                    const float lim = 4611686018427387904.0f;  // 2^62: B is rounded after this clamp
+                    const int64_t B = __float2ll_rn(fminf(fmaxf(bt, -lim), lim));
+                    yv[q] = round_shift_he((int64_t)M * v + B, N);
+                }
             }
             if constexpr (S8) {
                 uint32_t ow = 0;

@@ -21,6 +21,7 @@ QNN_ERR_OVERFLOW_RISK, QNN_ERR_CUDA, QNN_ERR_TIMEOUT = 4, 5, 6
 DTYPES = {"s8": 0, "u8": 1, "s4": 2, "u4": 3, "s32": 4, "f32": 5}
 SCHEMES = {"sym": 0, "asym": 1, "pow2": 2}
 EPI_MODES = {"requant": 0, "dequant": 1, "s32": 2}
+ELTWISE_OPS = {"add": 0, "mul": 1, "relu": 2}
 
 
 class QnnError(RuntimeError):
@@ -84,6 +85,8 @@ def _declare(L):
         "q_log_int_softmax": (c_int, [vp, i64, i64, f32, c_int, vp, vp]),
         "q_attn_shift_v": (c_int, [vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp]),
         "q_int_layernorm": (c_int, [vp, i64, c_int, vp, c_int, f32, vp, vp, vp, c_int, vp, vp]),
+        "q_eltwise_s8": (c_int, [c_int, vp, vp, i64, f32, c_int, vp, vp]),
+        "q_quantize_rows_dynamic": (c_int, [vp, i64, i64, c_int, vp, vp, vp]),
         "qnn_status_string": (ctypes.c_char_p, [c_int]),
         "qnn_check_device_error": (c_int, [vp]),
         "qnn_selftest_wait_timeout": (c_int, [ctypes.c_uint64, vp]),
@@ -308,6 +311,20 @@ def q_int_layernorm(x, rows: int, C: int, s: float, gamma, beta, out_scale, y, y
     _check(_SYMBOLS["q_int_layernorm"](_ptr(x), int(rows), int(C), _ptr(alpha), int(alpha_max), float(s),
                                         _ptr(gamma), _ptr(beta), _ptr(out_scale), DTYPES[y_dt], _ptr(y),
                                         _stream(stream)), "q_int_layernorm")
+
+
+def q_eltwise_s8(op: str, a, b, n: int, M: float, out, relu: bool = False, stream=None):
+    """Quantized elementwise add / mul / relu on s8 codes."""
+    load()
+    _check(_SYMBOLS["q_eltwise_s8"](ELTWISE_OPS[op], _ptr(a), _ptr(b), int(n), float(M), int(relu), _ptr(out),
+                                     _stream(stream)), "q_eltwise_s8")
+
+
+def q_quantize_rows_dynamic(x, rows: int, cols: int, q, scale, narrow: bool = False, stream=None):
+    """Per-row scale max|x| / 127 and s8 codes."""
+    load()
+    _check(_SYMBOLS["q_quantize_rows_dynamic"](_ptr(x), int(rows), int(cols), int(narrow), _ptr(q), _ptr(scale),
+                                                _stream(stream)), "q_quantize_rows_dynamic")
 
 
 def qnn_check_device_error(stream=None) -> int:

@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
     for n in ("q_quantize", "q_dequantize", "qgemm_prepack_b", "q_fold_epilogue", "qgemm_s8",
               "qnn_gemm_workspace_bytes", "qgemm_pack_a", "qgemm_s8_packed", "qgemm_s8_static_scratch",
               "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_conv_workspace_bytes",
-              "q_log_int_softmax", "q_attn_shift_v", "q_int_layernorm", "qnn_status_string",
+              "q_log_int_softmax", "q_attn_shift_v", "q_int_layernorm", "q_eltwise_s8",
+              "q_quantize_rows_dynamic", "qnn_status_string",
               "qnn_check_device_error"):
         assert n in names
 
@@ -146,6 +147,19 @@ def test_int_layernorm_arguments_rejected_on_host(lib):
     assert call(rows=0, x=None, y=None) == qnn.QNN_OK
     assert call(x=None) == qnn.QNN_ERR_INVALID_ARG
     assert call(g=20) == qnn.QNN_ERR_ALIGNMENT
+
+
+def test_eltwise_arguments_rejected_on_host(lib):
+    L = lib
+    assert L.q_eltwise_s8(3, 16, 16, 16, 1.0, 0, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_eltwise_s8(0, 16, 16, -1, 1.0, 0, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_eltwise_s8(1, 16, 16, 16, float("inf"), 0, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_eltwise_s8(0, 16, None, 16, 1.0, 0, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_eltwise_s8(0, 17, 16, 16, 1.0, 0, 16, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.q_eltwise_s8(0, None, None, 0, 1.0, 0, None, None) == qnn.QNN_OK
+    assert L.q_quantize_rows_dynamic(16, 2, 6, 0, 16, 16, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.q_quantize_rows_dynamic(16, 2, 0, 0, 16, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_quantize_rows_dynamic(None, 2, 8, 0, 16, 16, None) == qnn.QNN_ERR_INVALID_ARG
 
 
 def test_packed_sizes(lib):
