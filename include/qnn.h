@@ -257,6 +257,34 @@ qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed, const q
 qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
                       const qnn_epilogue *epi, void *O, int32_t *O_s32, qnn_stream_t stream);
 
+/* ---- weight zero points (Z_w != 0) --------------------------------------------- */
+
+/* Prepack u8 weights B [N, K] with per-output-channel zero points z_w (device
+ * int32 [N]) [MG 緩解精度下降: with Z_w != 0 the product has all four terms]:
+ * the image holds the centred values w - 128 (exact in fp16, like the u8
+ * activations), and colsum[n] = sum_k (B[n][k] - z_w[n]) -- pass it to
+ * q_fold_epilogue, which then folds (z_a - c_a) * colsum into zp_term.
+ * K % 16 == 0; B_packed 1024-byte aligned (qnn_gemm_packed_b_bytes). */
+qnn_status qgemm_prepack_b_u8(const uint8_t *B, const int32_t *z_w, int N, int K, void *B_packed, int32_t *colsum,
+                              qnn_stream_t stream);
+
+/* Workspace of qgemm_zw: the A image of qnn_gemm_workspace_bytes(M, K) and the
+ * per-row sums (int32 [M], 256-byte padded). */
+size_t qnn_gemm_zw_workspace_bytes(int M, int K);
+
+/* qgemm_s8 for weights with zero points (prepacked by qgemm_prepack_b_u8):
+ *   acc_c[m][n] = sum_k (a_k - z_a)(w_k - z_w[n])
+ * = acc - zp_term[n] + (128 - z_w[n]) * rowsum[m], where acc is the product of
+ * the centred codes, zp_term[n] = (z_a - c_a) colsum[n] is folded ahead, and
+ * rowsum[m] = sum_k (a_k - c_a) -- the term [MG 緩解精度下降] marks as costly
+ * because it depends on the input -- is summed by the A pre-pass into the
+ * workspace at run time.  Then the same epilogue as qgemm_s8.  a_dt S8 or U8; no
+ * PTF; workspace required (qnn_gemm_zw_workspace_bytes).  QNN_ERR_OVERFLOW_RISK
+ * when K * 255 * 255 > 2^31 - 1. */
+qnn_status qgemm_zw(const void *A, qnn_dtype a_dt, const void *B_packed, const int32_t *z_w, int M, int N, int K,
+                    const qnn_epilogue *epi, void *C, int32_t *C_s32, void *workspace, size_t workspace_bytes,
+                    qnn_stream_t stream);
+
 /* ---- Log-Int-Softmax attention [FQ 3.3] ------------------------------------ */
 
 /* Log-Int-Softmax [FQ 3.3: Softmax 的量化推理, Integer-only 推理, Softmax 的量化的实现]

@@ -15,6 +15,9 @@ namespace qnn {
 namespace {
 
 // One thread per 16-byte chunk of the packed image.
+// FLIP: B holds u8 codes, packed as their centred values w - 128 (the byte with
+// its top bit flipped, read as s8).
+template <bool FLIP>
 __global__ void prepack_b_kernel(const int8_t *__restrict__ B, int N, int K, uint8_t *__restrict__ out,
                                  int64_t nchunks)
 {
@@ -35,8 +38,10 @@ __global__ void prepack_b_kernel(const int8_t *__restrict__ B, int N, int K, uin
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             int v0 = 0, v1 = 0;
-            if (n < N && k0 + 2 * j < K) v0 = B[(int64_t)n * K + k0 + 2 * j];
-            if (n < N && k0 + 2 * j + 1 < K) v1 = B[(int64_t)n * K + k0 + 2 * j + 1];
+            if (n < N && k0 + 2 * j < K) v0 = FLIP ? (int8_t)(B[(int64_t)n * K + k0 + 2 * j] ^ 0x80)
+                                                   : B[(int64_t)n * K + k0 + 2 * j];
+            if (n < N && k0 + 2 * j + 1 < K) v1 = FLIP ? (int8_t)(B[(int64_t)n * K + k0 + 2 * j + 1] ^ 0x80)
+                                                       : B[(int64_t)n * K + k0 + 2 * j + 1];
             const uint32_t h0 = __half_as_ushort(__int2half_rn(v0));
             const uint32_t h1 = __half_as_ushort(__int2half_rn(v1));
             w[j] = h0 | (h1 << 16);
@@ -56,6 +61,20 @@ __global__ void colsum_s8_kernel(const int8_t *__restrict__ B, int N, int K, int
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) colsum[warp] = s;
+}
+
+// u8 weights with zero points: colsum[n] = sum_k (B[n][k] - z_w[n]).  One warp per channel.
+__global__ void colsum_u8_kernel(const uint8_t *__restrict__ B, const int32_t *__restrict__ z_w, int N, int K,
+                                 int32_t *__restrict__ colsum)
+{
+    const int warp = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp >= N) return;
+    int32_t s = 0;
+    for (int k = lane; k < K; k += 32) s += (int32_t)B[(int64_t)warp * K + k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) colsum[warp] = s - K * z_w[warp];
 }
 
 __global__ void fold_kernel(int N, int32_t zcoef, const int32_t *__restrict__ colsum, float s_a,
@@ -93,12 +112,34 @@ extern "C" qnn_status qgemm_prepack_b(const int8_t *B, int N, int K, void *B_pac
     int64_t blocks = (nchunks + 255) / 256;
     if (blocks > 65535) blocks = 65535;
     cudaStream_t s = (cudaStream_t)stream;
-    qnn::prepack_b_kernel<<<(int)blocks, 256, 0, s>>>(B, N, K, static_cast<uint8_t *>(B_packed),
-                                                       nchunks);
+    qnn::prepack_b_kernel<false><<<(int)blocks, 256, 0, s>>>(B, N, K, static_cast<uint8_t *>(B_packed),
+                                                              nchunks);
     if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
     if (colsum) {
         const int64_t threads = (int64_t)N * 32;
         qnn::colsum_s8_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(B, N, K, colsum);
+        return qnn::launch_status();
+    }
+    return QNN_OK;
+}
+
+extern "C" qnn_status qgemm_prepack_b_u8(const uint8_t *B, const int32_t *z_w, int N, int K, void *B_packed,
+                                         int32_t *colsum, qnn_stream_t stream)
+{
+    if (!B || !B_packed || !z_w || N <= 0 || K <= 0) return QNN_ERR_INVALID_ARG;
+    if (K % 16 != 0) return QNN_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(B_packed) & 1023u) != 0) return QNN_ERR_ALIGNMENT;
+    if (!qnn::aligned16(B) || !qnn::aligned16(z_w)) return QNN_ERR_ALIGNMENT;
+    const int64_t nchunks = (int64_t)(qnn::gemm::packed_b_bytes(N, K) / 16);
+    int64_t blocks = (nchunks + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    cudaStream_t s = (cudaStream_t)stream;
+    qnn::prepack_b_kernel<true><<<(int)blocks, 256, 0, s>>>(reinterpret_cast<const int8_t *>(B), N, K,
+                                                             static_cast<uint8_t *>(B_packed), nchunks);
+    if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
+    if (colsum) {
+        const int64_t threads = (int64_t)N * 32;
+        qnn::colsum_u8_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(B, z_w, N, K, colsum);
         return qnn::launch_status();
     }
     return QNN_OK;

@@ -134,10 +134,14 @@ struct GemmPackedOp : OpBase {
 // threadIdx.x walks the 16-code groups of a row (coalesced 16-byte reads; four
 // consecutive threads fill one 128-byte image row), threadIdx.y and the grid's
 // y dimension walk the rows.  All index arithmetic is 32-bit.
-template <bool PTF>
+// ROWSUM: also accumulate rowsum[m] += sum of the row's centred codes (a - 128 for
+// u8, a for s8) -- the per-row factor of a weight zero point's term; rowsum
+// must be zero on entry.  Lanes holding the same row combine their 16-code
+// partial sums with one warp reduction before a single atomic add.
+template <bool PTF, bool ROWSUM>
 __global__ void __launch_bounds__(256) pack_a_kernel(const uint8_t *__restrict__ A, int M, int K, int KT,
                                                      int rows_pad, int a_u8, const uint8_t *__restrict__ ptf,
-                                                     uint8_t *__restrict__ out)
+                                                     uint8_t *__restrict__ out, int32_t *__restrict__ rowsum)
 {
     const int groups = KT * 4;  // 16-code groups per padded row
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
@@ -178,6 +182,23 @@ __global__ void __launch_bounds__(256) pack_a_kernel(const uint8_t *__restrict__
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) h[j] = 0;
+            }
+            if (ROWSUM) {
+                int32_t part = 0;
+                if (mr[e] < M && k0 < K) {
+                    // offset-binary bytes (centred value + 128), summed 4 at a time
+                    const uint32_t fl = a_u8 ? 0u : 0x80808080u;
+                    uint32_t acc = 0;
+                    acc = __dp4a(v[e].x ^ fl, 0x01010101u, acc);
+                    acc = __dp4a(v[e].y ^ fl, 0x01010101u, acc);
+                    acc = __dp4a(v[e].z ^ fl, 0x01010101u, acc);
+                    acc = __dp4a(v[e].w ^ fl, 0x01010101u, acc);
+                    part = (int32_t)acc - 16 * 128;
+                }
+                const unsigned same = __match_any_sync(__activemask(), mr[e]);
+                part = __reduce_add_sync(same, part);
+                if ((threadIdx.x + threadIdx.y * blockDim.x) % 32 == (unsigned)(__ffs(same) - 1) && mr[e] < M && part != 0)
+                    atomicAdd(rowsum + mr[e], part);
             }
             const int r = mr[e] & (BM - 1);
             uint8_t *row = out + ((size_t)((mr[e] / BM) * KT + ks) * BM + r) * ROW_BYTES;
@@ -249,7 +270,7 @@ static qnn_status gemm_params(const void *A, qnn_dtype a_dt, const void *B_packe
 }
 
 static qnn_status launch_pack_a(const uint8_t *A, int M, int K, int a_u8, const uint8_t *ptf, uint8_t *out,
-                                cudaStream_t s)
+                                cudaStream_t s, int32_t *rowsum = nullptr)
 {
     const int KT = qnn::gemm::ksteps(K);
     const int rows_pad = ((M + BM - 1) / BM) * BM;
@@ -268,10 +289,12 @@ static qnn_status launch_pack_a(const uint8_t *A, int M, int K, int a_u8, const 
         if (gy < 1) gy = 1;
     }
     const dim3 grid(gx, gy);
-    if (ptf)
-        pack_a_kernel<true><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, ptf, out);
+    if (rowsum)
+        pack_a_kernel<false, true><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, nullptr, out, rowsum);
+    else if (ptf)
+        pack_a_kernel<true, false><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, ptf, out, nullptr);
     else
-        pack_a_kernel<false><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, nullptr, out);
+        pack_a_kernel<false, false><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, nullptr, out, nullptr);
     return qnn::launch_status();
 }
 
@@ -374,6 +397,39 @@ extern "C" qnn_status qgemm_s8_packed(const void *A_packed, qnn_dtype a_dt, cons
     const qnn_status st = gemm_params(A_packed, a_dt, B_packed, M, N, K, e, C, C_s32, p);
     if (st != QNN_OK) return st;
     return launch_gemm(p, true, (cudaStream_t)stream);
+}
+
+extern "C" size_t qnn_gemm_zw_workspace_bytes(int M, int K)
+{
+    if (M <= 0 || K <= 0) return 0;
+    return qnn::mk::packed_a_bytes(M, K) + (((size_t)M * 4 + 255) & ~(size_t)255);
+}
+
+extern "C" qnn_status qgemm_zw(const void *A, qnn_dtype a_dt, const void *B_packed, const int32_t *z_w, int M,
+                               int N, int K, const qnn_epilogue *e, void *C, int32_t *C_s32, void *workspace,
+                               size_t workspace_bytes, qnn_stream_t stream)
+{
+    using namespace qnn::mk;
+    Params p;
+    qnn_status st = gemm_params(A, a_dt, B_packed, M, N, K, e, C, C_s32, p);
+    if (st != QNN_OK) return st;
+    if (p.ptf) return QNN_ERR_UNSUPPORTED;
+    if (!z_w) return QNN_ERR_INVALID_ARG;
+    if (!qnn::aligned16(z_w)) return QNN_ERR_ALIGNMENT;
+    // |sum_k (a - z_a)(w - z_w)| <= K * 255 * 255 must stay inside int32
+    if ((int64_t)K * 255 * 255 > (int64_t)INT32_MAX) return QNN_ERR_OVERFLOW_RISK;
+    if (!workspace || workspace_bytes < qnn_gemm_zw_workspace_bytes(M, K)) return QNN_ERR_INVALID_ARG;
+    if (!qnn::aligned16(workspace)) return QNN_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t *img = static_cast<uint8_t *>(workspace);
+    int32_t *rowsum = reinterpret_cast<int32_t *>(img + packed_a_bytes(M, K));
+    if (cudaMemsetAsync(rowsum, 0, (size_t)M * 4, s) != cudaSuccess) return QNN_ERR_CUDA;
+    st = launch_pack_a(p.A, M, K, p.a_u8, nullptr, img, s, rowsum);
+    if (st != QNN_OK) return st;
+    p.A = img;
+    p.zw = z_w;
+    p.rowsum = rowsum;
+    return launch_gemm(p, true, s);
 }
 
 extern "C" qnn_status qgemm_s8(const void *A, qnn_dtype a_dt, const void *B_packed, int M, int N,

@@ -84,6 +84,10 @@ struct Params {
     int mode, relu, z_out, out_bits, out_signed;
     float clip_lo_f, clip_hi_f;  // requant: clip of v before rounding and adding z_out (ReLU folded in)
     const int32_t *zp;
+    // weight zero points (Z_w != 0): acc_c += (128 - zw[n]) * rowsum[m], rowsum the
+    // per-row sums of the centred activation codes written by the A pre-pass
+    const int32_t *zw;
+    const int32_t *rowsum;
     const float *Mv;
     const float *Bq;
     const float *D;
@@ -658,6 +662,16 @@ __device__ __forceinline__ void epilogue_int(const Params &p, int m, int n0, int
             ac[i + 3] -= __float_as_int(z.w);
         }
     }
+    if (p.rowsum) {
+        // the weight zero point's term (128 - z_w[n]) * sum_k (a_k - centre), in
+        // wrapping 32-bit arithmetic: the final sum fits int32 (host check)
+        const uint32_t rs = (uint32_t)__ldg(p.rowsum + m);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int n = n0 + i < p.N ? n0 + i : p.N - 1;
+            ac[i] = (int32_t)((uint32_t)ac[i] + (uint32_t)(128 - __ldg(p.zw + n)) * rs);
+        }
+    }
     const int64_t base = (int64_t)m * p.N + n0;
     if (p.C32) {
         if (vec) {
@@ -724,7 +738,7 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
             const uint32_t abuf = u & 1u;
             if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
             tc_fence_after();
-            const bool fast = store_columns<COLS>(cr, cols, lane) && !p.C32 && p.mode != QNN_EPI_S32;
+            const bool fast = store_columns<COLS>(cr, cols, lane) && !p.C32 && p.mode != QNN_EPI_S32 && !p.rowsum;
             const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + p0 * 32;
 #pragma unroll 1
             for (int jp = 0; jp < npieces; ++jp) {

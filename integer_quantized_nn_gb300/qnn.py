@@ -87,6 +87,9 @@ def _declare(L):
         "q_int_layernorm": (c_int, [vp, i64, c_int, vp, c_int, f32, vp, vp, vp, c_int, vp, vp]),
         "q_eltwise_s8": (c_int, [c_int, vp, vp, i64, f32, c_int, vp, vp]),
         "q_quantize_rows_dynamic": (c_int, [vp, i64, i64, c_int, vp, vp, vp]),
+        "qgemm_prepack_b_u8": (c_int, [vp, vp, c_int, c_int, vp, vp, vp]),
+        "qnn_gemm_zw_workspace_bytes": (sz, [c_int, c_int]),
+        "qgemm_zw": (c_int, [vp, c_int, vp, vp, c_int, c_int, c_int, vp, vp, vp, vp, sz, vp]),
         "qnn_status_string": (ctypes.c_char_p, [c_int]),
         "qnn_check_device_error": (c_int, [vp]),
         "qnn_selftest_wait_timeout": (c_int, [ctypes.c_uint64, vp]),
@@ -288,6 +291,29 @@ def qconv_u8s8(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None
     _check(_SYMBOLS["qconv_u8s8"](_ptr(I), int(z_in), _ptr(W_packed), ctypes.byref(g),
                                   ctypes.byref(epi), _ptr(O), _ptr(O_s32), _stream(stream)),
            "qconv_u8s8")
+
+
+def qgemm_prepack_b_u8(B, z_w, B_packed, colsum=None, stream=None):
+    """u8 weights [N, K] with per-channel zero points z_w (int32 [N])."""
+    load()
+    N, K = B.shape
+    _check(_SYMBOLS["qgemm_prepack_b_u8"](_ptr(B), _ptr(z_w), N, K, _ptr(B_packed), _ptr(colsum), _stream(stream)),
+           "qgemm_prepack_b_u8")
+
+
+def qnn_gemm_zw_workspace_bytes(M: int, K: int) -> int:
+    load()
+    return int(_SYMBOLS["qnn_gemm_zw_workspace_bytes"](int(M), int(K)))
+
+
+def qgemm_zw(A, a_dt: str, B_packed, z_w, M: int, N: int, K: int, epi: Epilogue, C, C_s32=None, workspace=None,
+             stream=None):
+    """qgemm_s8 for u8 weights with zero points (the run-time row-sum term)."""
+    load()
+    ws_bytes = 0 if workspace is None else _nbytes(workspace)
+    _check(_SYMBOLS["qgemm_zw"](_ptr(A), DTYPES[a_dt], _ptr(B_packed), _ptr(z_w), int(M), int(N), int(K),
+                                ctypes.byref(epi), _ptr(C), _ptr(C_s32), _ptr(workspace), ws_bytes, _stream(stream)),
+           "qgemm_zw")
 
 
 def q_log_int_softmax(x, rows: int, L: int, S: float, bits: int, code, stream=None):

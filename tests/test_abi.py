@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
               "qnn_gemm_workspace_bytes", "qgemm_pack_a", "qgemm_s8_packed", "qgemm_s8_static_scratch",
               "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_conv_workspace_bytes",
               "q_log_int_softmax", "q_attn_shift_v", "q_int_layernorm", "q_eltwise_s8",
-              "q_quantize_rows_dynamic", "qnn_status_string",
+              "q_quantize_rows_dynamic", "qgemm_prepack_b_u8", "qgemm_zw", "qnn_gemm_zw_workspace_bytes",
+              "qnn_status_string",
               "qnn_check_device_error"):
         assert n in names
 
@@ -160,6 +161,27 @@ def test_eltwise_arguments_rejected_on_host(lib):
     assert L.q_quantize_rows_dynamic(16, 2, 6, 0, 16, 16, None) == qnn.QNN_ERR_ALIGNMENT
     assert L.q_quantize_rows_dynamic(16, 2, 0, 0, 16, 16, None) == qnn.QNN_ERR_INVALID_ARG
     assert L.q_quantize_rows_dynamic(None, 2, 8, 0, 16, 16, None) == qnn.QNN_ERR_INVALID_ARG
+
+
+def test_gemm_zw_arguments_rejected_on_host(lib):
+    L = lib
+    epi = qnn.epilogue("requant")
+    epi.M, epi.Bq = 256, 512
+    need = L.qnn_gemm_zw_workspace_bytes(4, 32)
+    assert need == L.qnn_gemm_workspace_bytes(4, 32) + 256
+    assert L.qnn_gemm_zw_workspace_bytes(300, 64) == L.qnn_gemm_workspace_bytes(300, 64) + 1280
+    # no zero points, no workspace, a small one, PTF, K too large for int32
+    assert L.qgemm_zw(16, 1, 1024, None, 4, 8, 32, ctypes.byref(epi), 16, None, 4096, need, None) == \
+        qnn.QNN_ERR_INVALID_ARG
+    assert L.qgemm_zw(16, 1, 1024, 16, 4, 8, 32, ctypes.byref(epi), 16, None, None, 0, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.qgemm_zw(16, 1, 1024, 16, 4, 8, 32, ctypes.byref(epi), 16, None, 4096, need - 1, None) == \
+        qnn.QNN_ERR_INVALID_ARG
+    assert L.qgemm_zw(16, 1, 1024, 16, 4, 8, 40000, ctypes.byref(epi), 16, None, 4096, 1 << 40, None) == \
+        qnn.QNN_ERR_OVERFLOW_RISK
+    assert L.qgemm_zw(16, 1, 1024, 20, 4, 8, 32, ctypes.byref(epi), 16, None, 4096, need, None) == \
+        qnn.QNN_ERR_ALIGNMENT
+    assert L.qgemm_prepack_b_u8(16, None, 8, 32, 1024, None, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.qgemm_prepack_b_u8(16, 16, 8, 24, 1024, None, None) == qnn.QNN_ERR_ALIGNMENT
 
 
 def test_packed_sizes(lib):
