@@ -39,17 +39,20 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the headline GEMM kernel, from the ncu capture summarised in
-# profiles/qgemm_vit_fc1.md, valid only for the kernel sources it was taken on
-# (hash of integer_quantized_nn_gb300/csrc/*); reported as null otherwise.
-TRAFFIC_NCU = {"csrc_sha256_16": "3275bd38f1cdb9a2", "bytes": 24322304 + 159744}
+# profiles/qgemm_vit_fc1.md, valid only for the sources that kernel is built
+# from (hash of HEADLINE_SOURCES); reported as null otherwise.
+TRAFFIC_NCU = {"csrc_sha256_16": "660afddee5e8b918", "bytes": 24323840 + 77568}
+
+
+HEADLINE_SOURCES = ("qnn_gemm.cu", "qnn_gemm_layout.h", "qnn_internal.h", "qnn_mma_kernel.cuh", "qnn_ptx.cuh")
 
 
 def csrc_hash():
-    import glob
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "integer_quantized_nn_gb300", "csrc", "*"))):
-        h.update(os.path.basename(f).encode())
+    for name in HEADLINE_SOURCES:
+        f = os.path.join(ROOT, "integer_quantized_nn_gb300", "csrc", name)
+        h.update(name.encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -200,6 +200,32 @@ def test_conv_u8s8(oracle, geom):
           res=res, res_dt="u8", z_res=120, s_r=0.05)
 
 
+def test_conv_resnet_stem_7x7_stride2(oracle):
+    """The ResNet-50 stem shape: 7x7, stride 2, padding 3 (a 64 x 64 crop of the
+    224 x 224 input, batch 2).  u8 x s8 with the 3 colour channels widened to 16:
+    the extra channels hold the input zero point and carry zero weights."""
+    N, H, W, C, OC, F, pad, st = 2, 64, 64, 16, 64, 7, 3, 2
+    OH = (H + 2 * pad - F) // st + 1
+    rng = np.random.default_rng(36)
+    z_in = 110
+    I = np.full((N, H, W, C), z_in, np.uint8)
+    I[..., :3] = rng.integers(0, 256, size=(N, H, W, 3)).astype(np.uint8)
+    Wt = np.zeros((OC, F, F, C), np.int8)
+    Wt[..., :3] = rng.integers(-128, 128, size=(OC, F, F, 3)).astype(np.int8)
+    s_w = rng.uniform(1e-3, 1e-2, size=OC).astype(np.float32)
+    bias = rng.normal(0, 1, size=OC).astype(np.float32)
+    _conv(oracle, I, Wt, (N, H, W, C, OC, F, pad, st), z_in, 0.02, s_w, 0.05, bias, u4=False, out_dt="u8",
+          relu=True)
+    assert OH == 32
+
+
+def test_conv_u4s4_7x7_stride2(oracle):
+    """u4 x s4 at 7x7, stride 2, padding 3, C = 64 (K = 3136, more than one exact chunk)."""
+    geom = (1, 20, 20, 64, 64, 7, 3, 2)
+    I, Wt, s_w, bias, _ = _rand_u4s4(37, 1, 20, 20, 64, 64, 7, False)
+    _conv(oracle, I, Wt, geom, 6, 0.05, s_w, 0.3, bias)
+
+
 def test_conv_errors():
     t = torch()
     g = qnn.conv_geom(1, 8, 8, 48, 64, 3, 3)
