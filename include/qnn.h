@@ -145,6 +145,13 @@ typedef struct {
                                 alpha_k [FQ 3.2]: the GEMM uses A[m][k] * 2^alpha_k;
                                 S8 activations with z_a = 0 only; NULL: none */
     int32_t ptf_max_shift;   /* upper bound (0..3) on every ptf_shift value */
+    const float *row_scale;  /* device [rows] per-row activation scales (dynamic per-token
+                                quantization, q_quantize_rows_dynamic), or NULL: the
+                                per-channel factor is first scaled by the row's,
+                                M[n] -> row_scale[m] * M[n] (REQUANT) and
+                                D[n] -> row_scale[m] * D[n] (DEQUANT), one fp32
+                                multiply; fold with s_a = 1 so that M = s_w / s_o and
+                                D = s_w */
 } qnn_epilogue;
 
 /* Size in bytes of the qgemm_s8 workspace for an M x K activation operand

@@ -88,6 +88,7 @@ struct Params {
     // per-row sums of the centred activation codes written by the A pre-pass
     const int32_t *zw;
     const int32_t *rowsum;
+    const float *row_scale;  // per-row activation scales (dynamic quantization), or null
     const float *Mv;
     const float *Bq;
     const float *D;
@@ -569,12 +570,21 @@ __device__ __forceinline__ void epilogue_float(const Params &p, int m, int n0, f
     if (m >= p.M || n0 >= p.N) return;
     const bool vec = p.vec_ok;
     const int64_t base = (int64_t)m * p.N + n0;  // element offset of (m, n0)
+    // per-row activation scale: the column factor becomes fl(rs * factor); rs = 1
+    // (exact) without one
+    const float rs = p.row_scale ? __ldg(p.row_scale + m) : 1.0f;
     if (p.mode == QNN_EPI_DEQUANT) {
         float *C = static_cast<float *>(p.C);
         uint32_t y[32];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-            const float4 d = *reinterpret_cast<const float4 *>(ca + i);
+            float4 d = *reinterpret_cast<const float4 *>(ca + i);
+            if (p.row_scale) {
+                d.x = __fmul_rn(rs, d.x);
+                d.y = __fmul_rn(rs, d.y);
+                d.z = __fmul_rn(rs, d.z);
+                d.w = __fmul_rn(rs, d.w);
+            }
             const float4 b = *reinterpret_cast<const float4 *>(cb + i);
             y[i] = __float_as_uint(__fadd_rn(__fmul_rn(a[i], d.x), b.x));
             y[i + 1] = __float_as_uint(__fadd_rn(__fmul_rn(a[i + 1], d.y), b.y));
@@ -604,7 +614,11 @@ __device__ __forceinline__ void epilogue_float(const Params &p, int m, int n0, f
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
         const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
-        const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+        float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+        if (p.row_scale) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mm[k] = __fmul_rn(rs, mm[k]);
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             float v = __fadd_rn(__fmul_rn(a[i + k], mm[k]), t[i + k]);
@@ -948,6 +962,8 @@ inline qnn_status setup_epilogue(const qnn_epilogue *e, bool conv, Params &p)
     p.Bq = e->Bq;
     p.D = e->D;
     p.bias = e->bias;
+    p.row_scale = e->row_scale;
+    if (e->row_scale && !aligned16(e->row_scale)) return QNN_ERR_ALIGNMENT;
     switch (e->mode) {
     case QNN_EPI_REQUANT: {
         if (!e->M || !e->Bq) return QNN_ERR_INVALID_ARG;

@@ -43,7 +43,8 @@ class Epilogue(ctypes.Structure):
                 ("Bq", ctypes.c_void_p), ("D", ctypes.c_void_p), ("bias", ctypes.c_void_p),
                 ("residual", ctypes.c_void_p), ("res_dt", ctypes.c_int32),
                 ("z_res", ctypes.c_int32), ("R", ctypes.c_float),
-                ("ptf_shift", ctypes.c_void_p), ("ptf_max_shift", ctypes.c_int32)]
+                ("ptf_shift", ctypes.c_void_p), ("ptf_max_shift", ctypes.c_int32),
+                ("row_scale", ctypes.c_void_p)]
 
 
 class ConvGeom(ctypes.Structure):
@@ -200,10 +201,10 @@ def q_fold_epilogue(N, a_dt: str, z_a: int, colsum, s_a: float, s_w, s_o: float,
 
 def epilogue(mode="requant", relu=False, out_dt="s8", z_out=0, zp_term=None, M=None, Bq=None,
              D=None, bias=None, residual=None, res_dt="s8", z_res=0, R=0.0, ptf_shift=None,
-             ptf_max_shift=0) -> Epilogue:
+             ptf_max_shift=0, row_scale=None) -> Epilogue:
     return Epilogue(EPI_MODES[mode], int(relu), DTYPES[out_dt], int(z_out), _ptr(zp_term), _ptr(M),
                     _ptr(Bq), _ptr(D), _ptr(bias), _ptr(residual), DTYPES[res_dt], int(z_res),
-                    float(R), _ptr(ptf_shift), int(ptf_max_shift))
+                    float(R), _ptr(ptf_shift), int(ptf_max_shift), _ptr(row_scale))
 
 
 def qnn_gemm_workspace_bytes(M: int, K: int) -> int:

@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
         L.oracle_int_layernorm.argtypes = [vp, i64, i64, vp, f32, vp, vp, vp, vp]
         L.oracle_eltwise_s8.argtypes = [ctypes.c_int, vp, vp, i64, f32, ctypes.c_int, vp]
         L.oracle_quantize_rows_dynamic.argtypes = [vp, i64, i64, ctypes.c_int, vp, vp]
+        L.oracle_requant_rowscale.argtypes = [vp, i64, i64, vp, vp, vp, ctypes.c_int, vp, i32, f32, i32, i32,
+                                              i32, vp]
+        L.oracle_dequant_rowscale.argtypes = [vp, i64, i64, vp, vp, vp, vp]
         L.oracle_set_threads.argtypes = [ctypes.c_int]
         L.oracle_get_threads.restype = ctypes.c_int
     return _lib
@@ -349,3 +352,28 @@ def quantize_rows_dynamic(x, narrow: bool = False):
     if rc != 0:
         raise ValueError(f"oracle_quantize_rows_dynamic: error {rc}")
     return q, sc
+
+
+def requant_rowscale(acc_c, r, Mv, Bq, dt_out, relu=False, res=None, z_res=0, R=0.0, z_out=0, narrow=False):
+    """requant with per-row activation scales: M[m][n] = r[m] * Mv[n] (fp32) first."""
+    acc_c = _c(acc_c, np.int32)
+    rows, N = acc_c.shape
+    qmin, qmax = qrange(dt_out, narrow)
+    rr = _c(r, np.float32)
+    Mv = _c(Mv, np.float32)
+    Bq = _c(Bq, np.float32)
+    rs = None if res is None else _c(res, np.int32)
+    q = np.empty((rows, N), np.int32)
+    rc = lib().oracle_requant_rowscale(_p(acc_c), rows, N, _p(rr), _p(Mv), _p(Bq), int(relu), _p(rs), int(z_res),
+                                       np.float32(R), int(z_out), qmin, qmax, _p(q))
+    assert rc == 0
+    return q
+
+
+def dequant_rowscale(acc_c, r, D, bias=None):
+    acc_c = _c(acc_c, np.int32)
+    rows, N = acc_c.shape
+    y = np.empty((rows, N), np.float32)
+    b = None if bias is None else _c(bias, np.float32)
+    lib().oracle_dequant_rowscale(_p(acc_c), rows, N, _p(_c(r, np.float32)), _p(_c(D, np.float32)), _p(b), _p(y))
+    return y

@@ -30,6 +30,7 @@
  * exact rational arithmetic, invariants, numpy library routines).
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <stddef.h>
 #ifdef _OPENMP
@@ -292,6 +293,27 @@ int oracle_requant(const int32_t *acc_c, int64_t rows, int64_t N, const float *M
     return OR_OK;
 }
 
+/* Per-row activation scales r[m] (a dynamically quantized input, one scale per
+ * row: QI 量化参数选择's max truncation per token) feeding the requant: the
+ * folded per-channel factor is multiplied by the row's scale first, in fp32,
+ * M[m][n] = r[m] * Mv[n], then the requant above.  Reading: the per-row and
+ * per-channel factors are combined before they meet the accumulator (the pages
+ * fold one scalar s_a; with per-row scales the fold uses s_a = 1). */
+int oracle_requant_rowscale(const int32_t *acc_c, int64_t rows, int64_t N, const float *r, const float *Mv,
+                            const float *Bq, int relu, const int32_t *res, int32_t z_res, float R,
+                            int32_t z_out, int32_t qmin, int32_t qmax, int32_t *q)
+{
+    float *Mrow = (float *)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+    if (!Mrow) return OR_ERR_ARG;
+    for (int64_t m = 0; m < rows; ++m) {
+        for (int64_t n = 0; n < N; ++n) Mrow[n] = r[m] * Mv[n];
+        oracle_requant(acc_c + m * N, 1, N, Mrow, Bq, relu, res ? res + m * N : NULL, z_res, R, z_out, qmin,
+                       qmax, q + m * N);
+    }
+    free(Mrow);
+    return OR_OK;
+}
+
 /* Dequantizing epilogue [QI 反量化算子; MG 背景]: y = (float)acc_c * D[n] + bias[n]
  * as one fmul and one fadd.  bias may be NULL (zero). */
 void oracle_dequant_epilogue(const int32_t *acc_c, int64_t rows, int64_t N,
@@ -303,6 +325,20 @@ void oracle_dequant_epilogue(const int32_t *acc_c, int64_t rows, int64_t N,
             float v = (float)acc_c[i] * D[n];
             float b = bias ? bias[n] : 0.0f;
             y[i] = v + b;
+        }
+    }
+}
+
+/* The dequantizing epilogue with per-row activation scales: y = (float)acc_c *
+ * (r[m] * D[n]) + bias[n], the product r[m] * D[n] formed first in fp32. */
+void oracle_dequant_rowscale(const int32_t *acc_c, int64_t rows, int64_t N, const float *r, const float *D,
+                             const float *bias, float *y)
+{
+    for (int64_t m = 0; m < rows; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            const float d = r[m] * D[n];
+            const float v = (float)acc_c[m * N + n] * d;
+            y[m * N + n] = v + (bias ? bias[n] : 0.0f);
         }
     }
 }

@@ -419,3 +419,35 @@ def test_conv1x1_is_gemm(oracle):
     got = oracle.conv_acc_direct(I, W, 8, (0, 0), (1, 1))
     ref = (I.reshape(-1, 12).astype(np.int64) - 8) @ W.reshape(7, 12).astype(np.int64).T
     assert np.array_equal(got, ref)
+
+
+def test_requant_rowscale_reduces_and_scales(oracle):
+    """Per-row activation scales (a dynamically quantized input feeding the GEMM):
+    r = 1 is the plain requant, r = 2^k equals the plain requant with M * 2^k
+    (both exact in fp32), and the result tracks the exact rational
+    round(acc r M + Bq) except within fp32 error of a tie."""
+    g = np.random.default_rng(40)
+    acc = g.integers(-200000, 200000, size=(12, 24)).astype(np.int32)
+    Mv = g.uniform(1e-5, 1e-3, size=24).astype(np.float32)
+    Bq = g.normal(0, 3, size=24).astype(np.float32)
+    ones = np.ones(12, np.float32)
+    assert np.array_equal(oracle.requant_rowscale(acc, ones, Mv, Bq, "s8"), oracle.requant(acc, Mv, Bq, "s8"))
+    r = (2.0 ** g.integers(-3, 4, size=12)).astype(np.float32)
+    q = oracle.requant_rowscale(acc, r, Mv, Bq, "s8")
+    for m in range(12):
+        assert np.array_equal(q[m:m + 1], oracle.requant(acc[m:m + 1], Mv * r[m], Bq, "s8"))
+    r = g.uniform(0.01, 0.1, size=12).astype(np.float32)
+    q = oracle.requant_rowscale(acc, r, Mv, Bq, "s8")
+    near = 0
+    for m in range(12):
+        for n in range(24):
+            exact = Fraction(int(acc[m, n])) * Fraction(float(r[m])) * Fraction(float(Mv[n])) + Fraction(float(Bq[n]))
+            want = min(max(brute.round_half_even(exact), -128), 127)
+            if q[m, n] != want:
+                frac = exact - (exact.numerator // exact.denominator)
+                assert abs(frac - Fraction(1, 2)) < abs(exact) * Fraction(1, 2 ** 21) + Fraction(1, 2 ** 20)
+                near += 1
+    assert near <= 2
+    y = oracle.dequant_rowscale(acc, r, Mv, Bq)
+    ref = acc.astype(np.float64) * r[:, None].astype(np.float64) * Mv.astype(np.float64) + Bq
+    assert np.allclose(y, ref, rtol=1e-6, atol=1e-6)
