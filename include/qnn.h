@@ -372,6 +372,19 @@ qnn_status q_eltwise_s8(qnn_eltwise_op op, const int8_t *a, const int8_t *b, int
 qnn_status q_quantize_rows_dynamic(const float *x, int64_t rows, int64_t cols, int narrow, int8_t *q,
                                    float *scale, qnn_stream_t stream);
 
+/* ---- layouts ------------------------------------------------------------------ */
+
+/* NHWC <-> NCHW64 for quantized codes [MG conv 算子優化: the conv output laid out
+ * NCHW64, each 64 consecutive channels of a pixel contiguous].  The convolutions
+ * of this library read and write NHWC; NCHW64 tensors go through this
+ * memory-bound block permutation:
+ *   nchw64[n][c / 64][h][w][c % 64] = nhwc[n][h][w][c]   (to_nchw64 != 0; else back)
+ * dt: S4 / U4 (two codes per byte, element 2i in the low nibble: a block is 32
+ * bytes) or S8 / U8 (64 bytes).  C % 64 == 0; 16-byte aligned pointers; src and
+ * dst must not overlap. */
+qnn_status q_layout_nchw64(const void *src, int to_nchw64, int N, int H, int W, int C, qnn_dtype dt, void *dst,
+                           qnn_stream_t stream);
+
 /* ---- status ----------------------------------------------------------------- */
 
 const char *qnn_status_string(qnn_status s);

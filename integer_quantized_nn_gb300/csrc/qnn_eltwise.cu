@@ -11,6 +11,11 @@
 // Each thread handles 16 elements per step: two 16-byte loads and one 16-byte
 // store; a grid-stride loop, the n % 16 tail by the first threads.
 //
+// q_layout_nchw64: NHWC <-> NCHW64 [MG conv 算子優化: outputs in NCHW64, 64
+// consecutive channels of a pixel contiguous] for packed 4-bit or 8-bit codes:
+// a permutation of blocks of 64 channels (32 or 64 bytes), moved as 16-byte
+// chunks, one per thread and step, both sides coalesced along the block.
+//
 // q_quantize_rows_dynamic [QI 量化参数选择 (最大值截断), 量化算子]: per row the
 // scale max|x| / 127 (one IEEE division), then q = clip(rint(x / s)) with one
 // IEEE division per element; a zero row gets scale 0 and codes 0.  One warp per
@@ -104,6 +109,39 @@ __global__ void __launch_bounds__(256) quantize_rows_dynamic_kernel(const float 
     }
 }
 
+// chunk i of the destination (16 bytes); blk = bytes per 64-channel block.
+template <bool TO_NCHW64>
+__global__ void __launch_bounds__(256) nchw64_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                     int64_t chunks, int H, int W, int CB, int cpb)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int j = (int)(i % cpb);  // chunk within a block
+        const int64_t blk = i / cpb;    // destination block index
+        int64_t s;
+        if (TO_NCHW64) {
+            // dst block (n, cb, h, w) <- src block (n, h, w, cb)
+            const int w = (int)(blk % W);
+            const int64_t t1 = blk / W;
+            const int h = (int)(t1 % H);
+            const int64_t t2 = t1 / H;
+            const int cb = (int)(t2 % CB);
+            const int64_t n = t2 / CB;
+            s = (((n * H + h) * W + w) * CB + cb) * cpb + j;
+        } else {
+            // dst block (n, h, w, cb) <- src block (n, cb, h, w)
+            const int cb = (int)(blk % CB);
+            const int64_t t1 = blk / CB;
+            const int w = (int)(t1 % W);
+            const int64_t t2 = t1 / W;
+            const int h = (int)(t2 % H);
+            const int64_t n = t2 / H;
+            s = (((n * CB + cb) * H + h) * W + w) * cpb + j;
+        }
+        __stcs(dst + i, __ldcs(src + s));
+    }
+}
+
 int grid_for(int64_t work, int per_block)
 {
     const int64_t want = (work + per_block - 1) / per_block;
@@ -141,7 +179,40 @@ extern "C" qnn_status q_quantize_rows_dynamic(const float *x, int64_t rows, int6
     if (rows == 0) return QNN_OK;
     if (!x || !q || !scale) return QNN_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return QNN_ERR_ALIGNMENT;
-    const int grid = grid_for(rows, 8);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_rows_dynamic_kernel, 256, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    // one wave of resident blocks, 8 rows (warps) per block
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * per_sm));
     quantize_rows_dynamic_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(x, rows, cols, narrow, q, scale);
+    return launch_status();
+}
+
+extern "C" qnn_status q_layout_nchw64(const void *src, int to_nchw64, int N, int H, int W, int C, qnn_dtype dt,
+                                      void *dst, qnn_stream_t stream)
+{
+    using namespace qnn;
+    if (N < 0 || H <= 0 || W <= 0 || C <= 0) return QNN_ERR_INVALID_ARG;
+    int bits;
+    switch (dt) {
+    case QNN_S4: case QNN_U4: bits = 4; break;
+    case QNN_S8: case QNN_U8: bits = 8; break;
+    default: return QNN_ERR_UNSUPPORTED;
+    }
+    if (C % 64 != 0) return QNN_ERR_ALIGNMENT;
+    if (N == 0) return QNN_OK;
+    if (!src || !dst) return QNN_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return QNN_ERR_ALIGNMENT;
+    const int cpb = bits * 64 / 8 / 16;  // 16-byte chunks per 64-channel block: 2 or 4
+    const int64_t chunks = (int64_t)N * H * W * (C / 64) * cpb;
+    const int grid = grid_for(chunks, 256);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (to_nchw64)
+        nchw64_kernel<true><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), chunks,
+                                                  H, W, C / 64, cpb);
+    else
+        nchw64_kernel<false><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
+                                                   chunks, H, W, C / 64, cpb);
     return launch_status();
 }

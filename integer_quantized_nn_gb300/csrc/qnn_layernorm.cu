@@ -159,9 +159,17 @@ extern "C" qnn_status q_int_layernorm(const int8_t *x, int64_t rows, int C, cons
         return QNN_ERR_ALIGNMENT;
     LnArgs a{x, alpha, gamma, beta, out_scale, y, rows, C, s};
     const int64_t want = (rows + kLnWarps - 1) / kLnWarps;
-    const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * 8);
     cudaStream_t st = (cudaStream_t)stream;
-    if (y_dt == QNN_S8) int_layernorm_kernel<true><<<grid, kLnWarps * 32, 0, st>>>(a);
-    else int_layernorm_kernel<false><<<grid, kLnWarps * 32, 0, st>>>(a);
+    // one wave of resident blocks (the grid-stride loop covers the rest)
+    auto launch = [&](auto kern) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLnWarps * 32, 0) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * per_sm);
+        kern<<<grid, kLnWarps * 32, 0, st>>>(a);
+    };
+    if (y_dt == QNN_S8) launch(int_layernorm_kernel<true>);
+    else launch(int_layernorm_kernel<false>);
     return launch_status();
 }

@@ -605,13 +605,21 @@ extern "C" qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t 
         a.magic_l[j - 1] = (uint32_t)lj;
     }
     const int64_t want = (rows + kLisWarps - 1) / kLisWarps;
-    const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * 8);
     cudaStream_t s = (cudaStream_t)stream;
     const int R = L <= 256 ? (int)((L + 31) / 32) : 0;
-#define QNN_LIS(RR)                                                                         \
-    case RR:                                                                                \
-        if (bits == 5) log_int_softmax_kernel<RR, true><<<grid, kLisWarps * 32, 0, s>>>(a); \
-        else log_int_softmax_kernel<RR, false><<<grid, kLisWarps * 32, 0, s>>>(a);          \
+    // one wave of resident blocks (the grid-stride loop covers the rest)
+    auto launch = [&](auto kern) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLisWarps * 32, 0) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * per_sm);
+        kern<<<grid, kLisWarps * 32, 0, s>>>(a);
+    };
+#define QNN_LIS(RR)                                                     \
+    case RR:                                                            \
+        if (bits == 5) launch(log_int_softmax_kernel<RR, true>);        \
+        else launch(log_int_softmax_kernel<RR, false>);                 \
         break;
     switch (R) {
         QNN_LIS(1)

@@ -91,6 +91,7 @@ def _declare(L):
         "qgemm_prepack_b_u8": (c_int, [vp, vp, c_int, c_int, vp, vp, vp]),
         "qnn_gemm_zw_workspace_bytes": (sz, [c_int, c_int]),
         "qgemm_zw": (c_int, [vp, c_int, vp, vp, c_int, c_int, c_int, vp, vp, vp, vp, sz, vp]),
+        "q_layout_nchw64": (c_int, [vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, vp]),
         "qnn_status_string": (ctypes.c_char_p, [c_int]),
         "qnn_check_device_error": (c_int, [vp]),
         "qnn_selftest_wait_timeout": (c_int, [ctypes.c_uint64, vp]),
@@ -352,6 +353,13 @@ def q_quantize_rows_dynamic(x, rows: int, cols: int, q, scale, narrow: bool = Fa
     load()
     _check(_SYMBOLS["q_quantize_rows_dynamic"](_ptr(x), int(rows), int(cols), int(narrow), _ptr(q), _ptr(scale),
                                                 _stream(stream)), "q_quantize_rows_dynamic")
+
+
+def q_layout_nchw64(src, to_nchw64: bool, N: int, H: int, W: int, C: int, dt: str, dst, stream=None):
+    """NHWC <-> NCHW64 block permutation of packed codes."""
+    load()
+    _check(_SYMBOLS["q_layout_nchw64"](_ptr(src), int(bool(to_nchw64)), int(N), int(H), int(W), int(C), DTYPES[dt],
+                                        _ptr(dst), _stream(stream)), "q_layout_nchw64")
 
 
 def qnn_check_device_error(stream=None) -> int:

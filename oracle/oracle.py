@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
         L.oracle_requant_rowscale.argtypes = [vp, i64, i64, vp, vp, vp, ctypes.c_int, vp, i32, f32, i32, i32,
                                               i32, vp]
         L.oracle_dequant_rowscale.argtypes = [vp, i64, i64, vp, vp, vp, vp]
+        L.oracle_nhwc_to_nchw64.argtypes = [vp] + [ctypes.c_int] * 4 + [vp]
         L.oracle_set_threads.argtypes = [ctypes.c_int]
         L.oracle_get_threads.restype = ctypes.c_int
     return _lib
@@ -376,4 +377,15 @@ def dequant_rowscale(acc_c, r, D, bias=None):
     y = np.empty((rows, N), np.float32)
     b = None if bias is None else _c(bias, np.float32)
     lib().oracle_dequant_rowscale(_p(acc_c), rows, N, _p(_c(r, np.float32)), _p(_c(D, np.float32)), _p(b), _p(y))
+    return y
+
+
+def nhwc_to_nchw64(x):
+    """codes [N, H, W, C] -> [N, C / 64, H, W, 64]."""
+    x = _c(x, np.int32)
+    N, H, W, C = x.shape
+    y = np.empty((N, C // 64, H, W, 64), np.int32)
+    rc = lib().oracle_nhwc_to_nchw64(_p(x), N, H, W, C, _p(y))
+    if rc != 0:
+        raise ValueError(f"oracle_nhwc_to_nchw64: error {rc}")
     return y

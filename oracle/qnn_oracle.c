@@ -690,3 +690,22 @@ int oracle_quantize_rows_dynamic(const float *x, int64_t rows, int64_t cols, int
     }
     return OR_OK;
 }
+
+/* ---------------------------------------------------------------------------
+ * NHWC <-> NCHW64 [MG conv 算子優化: the output is written in NCHW64, each 64
+ * consecutive output channels of a pixel contiguous].  On codes (one int32 per
+ * element): nchw64[n][cb][h][w][j] = nhwc[n][h][w][64 cb + j], C % 64 == 0. */
+int oracle_nhwc_to_nchw64(const int32_t *src, int N, int H, int W, int C, int32_t *dst)
+{
+    if (N < 0 || H <= 0 || W <= 0 || C <= 0 || C % 64) return OR_ERR_ARG;
+    const int CB = C / 64;
+    for (int n = 0; n < N; ++n)
+        for (int h = 0; h < H; ++h)
+            for (int w = 0; w < W; ++w)
+                for (int c = 0; c < C; ++c) {
+                    const int cb = c / 64, j = c % 64;
+                    dst[((((int64_t)n * CB + cb) * H + h) * W + w) * 64 + j] =
+                        src[(((int64_t)n * H + h) * W + w) * C + c];
+                }
+    return OR_OK;
+}

@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
               "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_conv_workspace_bytes",
               "q_log_int_softmax", "q_attn_shift_v", "q_int_layernorm", "q_eltwise_s8",
               "q_quantize_rows_dynamic", "qgemm_prepack_b_u8", "qgemm_zw", "qnn_gemm_zw_workspace_bytes",
-              "qnn_status_string",
+              "q_layout_nchw64", "qnn_status_string",
               "qnn_check_device_error"):
         assert n in names
 
@@ -182,6 +182,15 @@ def test_gemm_zw_arguments_rejected_on_host(lib):
         qnn.QNN_ERR_ALIGNMENT
     assert L.qgemm_prepack_b_u8(16, None, 8, 32, 1024, None, None) == qnn.QNN_ERR_INVALID_ARG
     assert L.qgemm_prepack_b_u8(16, 16, 8, 24, 1024, None, None) == qnn.QNN_ERR_ALIGNMENT
+
+
+def test_layout_arguments_rejected_on_host(lib):
+    L = lib
+    assert L.q_layout_nchw64(16, 1, 1, 2, 2, 96, 3, 16, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.q_layout_nchw64(16, 1, 1, 2, 2, 64, 4, 16, None) == qnn.QNN_ERR_UNSUPPORTED
+    assert L.q_layout_nchw64(16, 1, 1, 0, 2, 64, 3, 16, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.q_layout_nchw64(None, 1, 0, 2, 2, 64, 3, None, None) == qnn.QNN_OK
+    assert L.q_layout_nchw64(20, 1, 1, 2, 2, 64, 3, 16, None) == qnn.QNN_ERR_ALIGNMENT
 
 
 def test_packed_sizes(lib):

@@ -75,3 +75,26 @@ def test_eltwise_errors():
     s = t.zeros(2, dtype=t.float32, device="cuda")
     with pytest.raises(qnn.QnnError):
         qnn.q_quantize_rows_dynamic(x, 2, 6, a, s)
+
+
+@pytest.mark.parametrize("dt", ["u4", "s8"])
+@pytest.mark.parametrize("shape", [(1, 1, 1, 64), (2, 7, 5, 192), (64, 56, 56, 256)])
+def test_layout_nchw64(oracle, dt, shape):
+    """NHWC <-> NCHW64 (MegEngine's conv output layout) against the oracle's
+    permutation of the codes, both directions, packed bytes compared."""
+    t = __import__("torch")
+    N, H, W, C = shape
+    rng = np.random.default_rng(C + H)
+    lo, hi = (0, 15) if dt == "u4" else (-128, 127)
+    codes = rng.integers(lo, hi + 1, size=shape).astype(np.int32)
+    pack = oracle.pack_nibbles if dt == "u4" else oracle.pack_bytes
+    src = pack(codes)
+    want = pack(oracle.nhwc_to_nchw64(codes))
+    d_src = dev(src)
+    d_dst = t.empty(want.size, dtype=t.uint8, device="cuda")
+    qnn.q_layout_nchw64(d_src, True, N, H, W, C, dt, d_dst)
+    back = t.empty(src.size, dtype=t.uint8, device="cuda")
+    qnn.q_layout_nchw64(d_dst, False, N, H, W, C, dt, back)
+    t.cuda.synchronize()
+    assert np.array_equal(host(d_dst), want.reshape(-1))
+    assert np.array_equal(host(back), src.reshape(-1))

@@ -451,3 +451,21 @@ def test_requant_rowscale_reduces_and_scales(oracle):
     y = oracle.dequant_rowscale(acc, r, Mv, Bq)
     ref = acc.astype(np.float64) * r[:, None].astype(np.float64) * Mv.astype(np.float64) + Bq
     assert np.allclose(y, ref, rtol=1e-6, atol=1e-6)
+
+
+def test_nchw64_layout(oracle):
+    """MegEngine 4-bit article, conv 算子優化: NCHW64 keeps each 64 consecutive
+    channels of a pixel together.  With C = 64 it is NHWC itself; in general
+    every element lands at [n][c // 64][h][w][c % 64] (checked by explicit loops)."""
+    g = np.random.default_rng(43)
+    x = g.integers(-8, 8, size=(2, 3, 5, 64))
+    assert np.array_equal(oracle.nhwc_to_nchw64(x)[:, 0], x)
+    x = g.integers(0, 16, size=(2, 3, 4, 192))
+    y = oracle.nhwc_to_nchw64(x)
+    for n in range(2):
+        for h in range(3):
+            for w in range(4):
+                for c in range(192):
+                    assert y[n, c // 64, h, w, c % 64] == x[n, h, w, c]
+    with pytest.raises(ValueError):
+        oracle.nhwc_to_nchw64(np.zeros((1, 2, 2, 48), np.int32))
