@@ -239,6 +239,18 @@ size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g, qnn_dtype w_dt);
 qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_conv_geom *g, void *W_packed,
                            int32_t *colsum, qnn_stream_t stream);
 
+/* Prepack u4 filters (packed nibbles, OHWI) with per-filter zero points z_w
+ * (device int32 [OC]) for qconv_u4s4 [MG 背景: UINT4 codes are asymmetric; 緩解
+ * 精度下降: with Z_w != 0 every term of the product appears].  The filters are
+ * constants, so the weight zero point is taken out here: the images hold
+ * u - z_w[oc] in [-15, 15] (exact in e4m3, like the s4 values) and colsum[oc] =
+ * sum (u - z_w[oc]); the conv then computes sum (q - z_in)(u - z_w) with no
+ * run-time term.  Same buffer size as S4 (qnn_conv_packed_w_bytes(g, QNN_S4)).
+ * QNN_ERR_OVERFLOW_RISK when FH FW C 225 >= 2^24 (the kernel's fp32 sums must
+ * stay exact). */
+qnn_status qconv_prepack_w_u4(const void *W, const int32_t *z_w, const qnn_conv_geom *g, void *W_packed,
+                              int32_t *colsum, qnn_stream_t stream);
+
 /* Size in bytes of the qconv_u4s4 workspace for an input of in_dt (U4: the
  * input expanded to one byte per channel, N * H * W * C); 0 for an invalid
  * geometry or another type. */

@@ -277,8 +277,18 @@ struct ConvU8Op : ConvFetch<8, 16, 64, D> {
 // Image: for each 256-filter block and K step of 128, 256 rows x 128 bytes,
 // 128-byte swizzled, zero beyond OC and K; byte position 8g + j of a row holds
 // the weight of K index 8g + {0,2,4,6,1,3,5,7}[j].
+// With z_w (u4 filters with per-filter zero points) the weight is the centred
+// nibble u - z_w[oc] in [-15, 15], exact in e4m3 like the s4 values; else the
+// nibble read as s4.
+__device__ __forceinline__ int filter_value(uint8_t byte, int k, const int32_t *z_w, int n)
+{
+    int v = (k & 1) ? (byte >> 4) : (byte & 15);
+    if (z_w) return v - z_w[n];
+    return v >= 8 ? v - 16 : v;
+}
+
 __global__ void prepack_w_s4_kernel(const uint8_t *__restrict__ W, int OC, int K, int KT,
-                                    uint8_t *__restrict__ out, int64_t nchunks)
+                                    uint8_t *__restrict__ out, int64_t nchunks, const int32_t *__restrict__ z_w)
 {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -298,9 +308,7 @@ __global__ void prepack_w_s4_kernel(const uint8_t *__restrict__ W, int OC, int K
             const int k = (kpos & ~7) + ((j < 4) ? 2 * j : 2 * (j - 4) + 1);
             uint32_t code = 0;
             if (n < OC && k < K) {
-                const uint8_t byte = W[((int64_t)n * K + k) >> 1];
-                int v = (k & 1) ? (byte >> 4) : (byte & 15);
-                if (v >= 8) v -= 16;
+                const int v = filter_value(W[((int64_t)n * K + k) >> 1], k, z_w, n);
                 code = (uint32_t)__nv_cvt_float_to_fp8((float)v, __NV_SATFINITE, __NV_E4M3);
             }
             w[b >> 2] |= code << (8 * (b & 3));
@@ -310,17 +318,14 @@ __global__ void prepack_w_s4_kernel(const uint8_t *__restrict__ W, int OC, int K
 }
 
 // colsum[oc] = sum over (fh, fw, c) of the s4 weights; one warp per filter.
-__global__ void colsum_s4_kernel(const uint8_t *__restrict__ W, int OC, int K, int32_t *__restrict__ colsum)
+__global__ void colsum_s4_kernel(const uint8_t *__restrict__ W, int OC, int K, int32_t *__restrict__ colsum,
+                                 const int32_t *__restrict__ z_w)
 {
     const int warp = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (warp >= OC) return;
     int32_t s = 0;
-    for (int k = lane; k < K; k += 32) {
-        const uint8_t byte = W[((int64_t)warp * K + k) >> 1];
-        int v = (k & 1) ? (byte >> 4) : (byte & 15);
-        s += (v >= 8) ? v - 16 : v;
-    }
+    for (int k = lane; k < K; k += 32) s += filter_value(W[((int64_t)warp * K + k) >> 1], k, z_w, warp);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) colsum[warp] = s;
@@ -513,7 +518,7 @@ __global__ void expand_u4_kernel(const uint8_t *__restrict__ in, int64_t n16, ui
 // CB-byte swizzled layout (chunk c of row r at chunk c ^ ((r * CB / 128) %
 // (CB / 16))); zero beyond OC.  One thread per 16-byte chunk.
 __global__ void prepack_w_s4_tma_kernel(const uint8_t *__restrict__ W, int OC, int C, int CB, int KT,
-                                        uint8_t *__restrict__ out, int64_t nchunks)
+                                        uint8_t *__restrict__ out, int64_t nchunks, const int32_t *__restrict__ z_w)
 {
     const int cpr = CB / 16;
     const int cbn = C / CB;
@@ -535,9 +540,7 @@ __global__ void prepack_w_s4_tma_kernel(const uint8_t *__restrict__ W, int OC, i
 #pragma unroll
             for (int b = 0; b < 16; ++b) {
                 const int k = k0 + b;
-                const uint8_t byte = W[((int64_t)n * K + k) >> 1];
-                int v = (k & 1) ? (byte >> 4) : (byte & 15);
-                if (v >= 8) v -= 16;
+                const int v = filter_value(W[((int64_t)n * K + k) >> 1], k, z_w, n);
                 const uint32_t code = (uint32_t)__nv_cvt_float_to_fp8((float)v, __NV_SATFINITE, __NV_E4M3);
                 w[b >> 2] |= code << (8 * (b & 3));
             }
@@ -765,6 +768,15 @@ extern "C" size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g, qnn_dtype w_dt
     return 0;
 }
 
+namespace qnn {
+namespace mk {
+// The 4-bit filter images and column sums; z_w: u4 filters with per-filter zero
+// points (device int32 [OC]), or null for s4 filters.
+static qnn_status prepack_w4(const void *W, const int32_t *z_w, const qnn_conv_geom *g, void *W_packed,
+                             int32_t *colsum, qnn_stream_t stream);
+}  // namespace mk
+}  // namespace qnn
+
 extern "C" qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_conv_geom *g,
                                       void *W_packed, int32_t *colsum, qnn_stream_t stream)
 {
@@ -775,6 +787,24 @@ extern "C" qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_c
         return qgemm_prepack_b(static_cast<const int8_t *>(W), g->OC, K, W_packed, colsum, stream);
     }
     if (w_dt != QNN_S4) return QNN_ERR_UNSUPPORTED;
+    return qnn::mk::prepack_w4(W, nullptr, g, W_packed, colsum, stream);
+}
+
+extern "C" qnn_status qconv_prepack_w_u4(const void *W, const int32_t *z_w, const qnn_conv_geom *g, void *W_packed,
+                                         int32_t *colsum, qnn_stream_t stream)
+{
+    if (!W || !W_packed || !z_w || !qnn::mk::geom_ok(g)) return QNN_ERR_INVALID_ARG;
+    if (!qnn::aligned16(z_w)) return QNN_ERR_ALIGNMENT;
+    // |u - z_w| <= 15: every fp32 sum in the kernel's 2^-9 units stays exact while
+    // K * 15 * 15 < 2^24
+    if ((int64_t)g->FH * g->FW * g->C * 225 >= (1ll << 24)) return QNN_ERR_OVERFLOW_RISK;
+    return qnn::mk::prepack_w4(W, z_w, g, W_packed, colsum, stream);
+}
+
+static qnn_status qnn::mk::prepack_w4(const void *W, const int32_t *z_w, const qnn_conv_geom *g, void *W_packed,
+                                      int32_t *colsum, qnn_stream_t stream)
+{
+    const int K = g->FH * g->FW * g->C;
     if (g->C % 2 != 0) return QNN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(W_packed) & 1023u) != 0) return QNN_ERR_ALIGNMENT;
     const int KT = (K + 127) / 128;
@@ -784,7 +814,7 @@ extern "C" qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_c
     cudaStream_t s = (cudaStream_t)stream;
     uint8_t *wp = static_cast<uint8_t *>(W_packed);
     qnn::mk::prepack_w_s4_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(W), g->OC, K,
-                                                               KT, wp, nchunks);
+                                                               KT, wp, nchunks, z_w);
     if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
     // the TMA conv's image and the column sums follow the fused-path image
     const size_t tb = qnn::mk::tma_w_bytes(g);
@@ -795,13 +825,13 @@ extern "C" qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_c
         if (tblocks > 65535) tblocks = 65535;
         qnn::mk::prepack_w_s4_tma_kernel<<<(int)tblocks, 256, 0, s>>>(
             static_cast<const uint8_t *>(W), g->OC, g->C, cb, g->FH * g->FW * (g->C / cb),
-            wp + qnn::mk::tma_w_offset(g), tchunks);
+            wp + qnn::mk::tma_w_offset(g), tchunks, z_w);
         if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
     }
     const int64_t threads = (int64_t)g->OC * 32;
     int32_t *cs_img = reinterpret_cast<int32_t *>(wp + qnn::mk::colsum_offset(g));
     qnn::mk::colsum_s4_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(static_cast<const uint8_t *>(W),
-                                                                          g->OC, K, cs_img);
+                                                                          g->OC, K, cs_img, z_w);
     if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
     if (colsum) {
         if (cudaMemcpyAsync(colsum, cs_img, (size_t)g->OC * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)

@@ -92,6 +92,7 @@ def _declare(L):
         "qnn_gemm_zw_workspace_bytes": (sz, [c_int, c_int]),
         "qgemm_zw": (c_int, [vp, c_int, vp, vp, c_int, c_int, c_int, vp, vp, vp, vp, sz, vp]),
         "q_layout_nchw64": (c_int, [vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, vp]),
+        "qconv_prepack_w_u4": (c_int, [vp, vp, vp, vp, vp, vp]),
         "qnn_status_string": (ctypes.c_char_p, [c_int]),
         "qnn_check_device_error": (c_int, [vp]),
         "qnn_selftest_wait_timeout": (c_int, [ctypes.c_uint64, vp]),
@@ -269,6 +270,13 @@ def qconv_prepack_w(W, w_dt: str, g: ConvGeom, W_packed, colsum=None, stream=Non
     load()
     _check(_SYMBOLS["qconv_prepack_w"](_ptr(W), DTYPES[w_dt], ctypes.byref(g), _ptr(W_packed),
                                        _ptr(colsum), _stream(stream)), "qconv_prepack_w")
+
+
+def qconv_prepack_w_u4(W, z_w, g: ConvGeom, W_packed, colsum=None, stream=None):
+    """u4 filters (packed nibbles, OHWI) with per-filter zero points z_w (int32 [OC])."""
+    load()
+    _check(_SYMBOLS["qconv_prepack_w_u4"](_ptr(W), _ptr(z_w), ctypes.byref(g), _ptr(W_packed), _ptr(colsum),
+                                           _stream(stream)), "qconv_prepack_w_u4")
 
 
 def qnn_conv_workspace_bytes(g: ConvGeom, in_dt: str = "u4") -> int:

@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
               "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_conv_workspace_bytes",
               "q_log_int_softmax", "q_attn_shift_v", "q_int_layernorm", "q_eltwise_s8",
               "q_quantize_rows_dynamic", "qgemm_prepack_b_u8", "qgemm_zw", "qnn_gemm_zw_workspace_bytes",
-              "q_layout_nchw64", "qnn_status_string",
+              "q_layout_nchw64", "qconv_prepack_w_u4", "qnn_status_string",
               "qnn_check_device_error"):
         assert n in names
 
@@ -191,6 +191,15 @@ def test_layout_arguments_rejected_on_host(lib):
     assert L.q_layout_nchw64(16, 1, 1, 0, 2, 64, 3, 16, None) == qnn.QNN_ERR_INVALID_ARG
     assert L.q_layout_nchw64(None, 1, 0, 2, 2, 64, 3, None, None) == qnn.QNN_OK
     assert L.q_layout_nchw64(20, 1, 1, 2, 2, 64, 3, 16, None) == qnn.QNN_ERR_ALIGNMENT
+
+
+def test_conv_u4_zero_point_prepack_rejected_on_host(lib):
+    L = lib
+    g = qnn.conv_geom(1, 8, 8, 64, 64, 3, 3)
+    assert L.qconv_prepack_w_u4(16, None, ctypes.byref(g), 1024, None, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.qconv_prepack_w_u4(16, 20, ctypes.byref(g), 1024, None, None) == qnn.QNN_ERR_ALIGNMENT
+    big = qnn.conv_geom(1, 8, 8, 8320, 64, 3, 3)  # 9 * 8320 * 225 >= 2^24
+    assert L.qconv_prepack_w_u4(16, 16, ctypes.byref(big), 1024, None, None) == qnn.QNN_ERR_OVERFLOW_RISK
 
 
 def test_packed_sizes(lib):

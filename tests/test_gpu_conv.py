@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="requant",
           out_dt="u4", relu=True, z_out=0, res=None, res_dt="u4", z_res=8, s_r=None,
-          full=True, pixels=None):
+          full=True, pixels=None, w_zp=None):
     """Runs the conv on both sides.  I_pk / W_pk: packed u4 / s4 bytes (u4=True)
     or u8 / s8 codes (u4=False), NHWC / OHWI."""
     t = torch()
@@ -23,7 +23,10 @@ def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="re
     Wd = dev(W_pk)
     Wp = aligned_empty(qnn.qnn_conv_packed_w_bytes(g, w_dt))
     colsum = t.empty(OC, dtype=t.int32, device="cuda")
-    qnn.qconv_prepack_w(Wd, w_dt, g, Wp, colsum)
+    if w_zp is None:
+        qnn.qconv_prepack_w(Wd, w_dt, g, Wp, colsum)
+    else:
+        qnn.qconv_prepack_w_u4(Wd, dev(np.asarray(w_zp, np.int32)), g, Wp, colsum)
     a_dt = "u4" if u4 else "u8"
     sw = dev(np.asarray(s_w, np.float32))
     bd = dev(np.asarray(bias, np.float32))
@@ -63,7 +66,10 @@ def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="re
     # oracle side
     if u4:
         Ic = oracle.unpack_nibbles(I_pk, signed=False)
-        Wc = oracle.unpack_nibbles(W_pk, signed=True)
+        if w_zp is None:
+            Wc = oracle.unpack_nibbles(W_pk, signed=True)
+        else:  # u4 filters: the zero-point-centred codes u - z_w[oc]
+            Wc = oracle.unpack_nibbles(W_pk, signed=False) - np.asarray(w_zp, np.int32).reshape(-1, 1, 1, 1)
     else:
         Ic = I_pk.astype(np.int32)
         Wc = W_pk.astype(np.int8).astype(np.int32)
@@ -224,6 +230,29 @@ def test_conv_u4s4_7x7_stride2(oracle):
     geom = (1, 20, 20, 64, 64, 7, 3, 2)
     I, Wt, s_w, bias, _ = _rand_u4s4(37, 1, 20, 20, 64, 64, 7, False)
     _conv(oracle, I, Wt, geom, 6, 0.05, s_w, 0.3, bias)
+
+
+@pytest.mark.parametrize("geom", [(2, 9, 9, 64, 64, 3, 1, 1), (2, 10, 10, 64, 128, 3, 1, 2), (3, 5, 5, 64, 96, 1, 0, 1),
+                                  (1, 12, 12, 32, 64, 7, 3, 2)])
+def test_conv_u4u4(oracle, geom):
+    """u4 activations x u4 filters with per-filter zero points (both operands
+    asymmetric, MegEngine article 背景 / 緩解精度下降); the fused and the TMA path."""
+    N, H, W, C, OC, F, pad, st = geom
+    OH = (H + 2 * pad - F) // st + 1
+    OW = (W + 2 * pad - F) // st + 1
+    I, Wt, s_w, bias, res = _rand_u4s4(38 + C, N, H, W, C, OC, F, True, OH, OW)
+    z_w = np.random.default_rng(39).integers(0, 16, size=OC).astype(np.int32)
+    z_w[:2] = (0, 15)
+    _conv(oracle, I, Wt, geom, 9, 0.05, s_w, 0.2, bias, res=res, s_r=0.13, w_zp=z_w)
+
+
+def test_conv_u4u4_resnet_3x3_full(oracle):
+    """ResNet-50 stage-1 3x3 Conv_Add_Relu at full size with u4 filters and zero points."""
+    w = workloads.conv_u4()
+    z_w = np.random.default_rng(44).integers(0, 16, size=64).astype(np.int32)
+    geom = (64, 56, 56, 64, 64, 3, 1, 1)
+    _conv(oracle, w["I"], w["W"], geom, w["z_in"], w["s_a"], w["s_w"], w["s_o"] * 2, w["bias"],
+          res=w["res"], z_res=w["z_res"], s_r=w["s_r"], w_zp=z_w)
 
 
 def test_conv_errors():
