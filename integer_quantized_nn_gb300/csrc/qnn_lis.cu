@@ -54,10 +54,6 @@ struct LisArgs {
     uint32_t qm;      // floor(nd / x0n) = mulhi(nd, qm) >> ql for nd <= 30 x0n < 2^21
     uint32_t ql;      // (x0n == 1: qm = 0, q = nd)
     int kmax;         // 2^bits
-    // floor(n / D_j) = (t + ((n - t) >> 1)) >> (l_j - 1), t = mulhi(m_j, n), for
-    // the divisors D_j = 2 L_j - 1 of the cutoff table
-    uint64_t magic[32];
-    uint32_t magic_l[32];
 };
 
 // Integer exponential of x - mx (mx the row maximum) and its fp32 value.  The
@@ -79,49 +75,54 @@ __device__ __forceinline__ uint64_t lis_exp(int32_t x, int32_t mx, const LisArgs
     return ((uint64_t)hi << 32) | lo;
 }
 
-// Cutoff table of one row: Et[j] for j = 1..kmax is E_j, the largest e with
-// round_half_even(s / e) >= L_j, L_1 = 2 and L_j = 3 * 2^(j-2) (the values of v
-// where log_round steps up); Et[0] = 2^64 - 1 and Et[kmax + 1] = 0 bound the
-// search.  round(s/e) >= L  <=>  2s > (2L-1) e, or equality with L even; so
-// E = floor(2s / (2L-1)), minus one when (2L-1) divides 2s and L is odd.
-__device__ __forceinline__ void lis_table(uint64_t s, int lane, const LisArgs &a, uint64_t *Et)
+// round_half_even(s / e) >= L  <=>  2s > (2L - 1) e, or equality with L even
+// (exact: 2s has 65 bits, (2L - 1) e at most 95).
+__device__ __forceinline__ bool ratio_reaches(uint64_t s, uint64_t e, uint64_t L)
 {
-    if (lane < a.kmax) {
-        const int j = lane + 1;
-        const uint64_t Lj = j == 1 ? 2ull : (3ull << (j - 2));
-        const uint64_t D = 2 * Lj - 1;
-        const uint64_t t = __umul64hi(a.magic[lane], s);
-        const uint64_t q1 = (t + ((s - t) >> 1)) >> (a.magic_l[lane] - 1);
-        const uint64_t r1 = s - q1 * D;
-        uint64_t Ej = 2 * q1, r2 = 2 * r1;
-        if (r2 >= D) {
-            Ej += 1;
-            r2 -= D;
-        }
-        if (r2 == 0 && (Lj & 1)) Ej -= 1;  // s >= 1, so Ej >= 1 here
-        Et[j] = Ej;
-    }
-    if (lane == 0) Et[0] = ~0ull;
-    if (lane == 1) Et[a.kmax + 1] = 0ull;
-    __syncwarp();
+    const uint64_t D = 2 * L - 1;
+    const uint64_t plo = D * e, phi = __umul64hi(D, e);
+    const uint64_t slo = s << 1, shi = s >> 63;
+    if (shi != phi) return shi > phi;
+    if (slo != plo) return slo > plo;
+    return (L & 1) == 0;
 }
 
-// Code of one exponential e (fp32 value ef): the number of E_j >= e, at most
-// kmax.  kh, the number of thresholds L_j = 3 * 2^(j-2) (j >= 2) at or below
-// the fp32 estimate of v = s / e, comes from its exponent E and first mantissa
-// bit (v >= 1.5 * 2^E); below 2 it is taken as 0.  Rounding v to an integer
-// and the estimate's relative error (< 2^-20) move the count by at most one,
-// and only upwards while L_kh < 2^19 (kmax <= 16): one exact comparison with
-// E_{kh+1} settles it.  For kmax = 32 the count may also lie one below.
+// L_j, the values of v at which log_round steps up: L_1 = 2, L_j = 3 * 2^(j-2).
+__device__ __forceinline__ uint64_t step_value(int j) { return j <= 1 ? 2ull : (3ull << (j - 2)); }
+
+// Code of one exponential e (fp32 value ef) in a row whose sum is s (fp32 value
+// sf): the number k of thresholds j <= kmax with round_half_even(s / e) >= L_j.
+// The fp32 estimate w of v = s / e (relative error below 2^-21) gives
+// kh = #{j : L_j <= w} from its exponent E and first mantissa bit (v >= 1.5 *
+// 2^E; 0 below 2).  Rounding v to an integer crosses at most the next threshold
+// L_{kh+1}, exactly when v > L_{kh+1} - 1/2 (ties: to even), so k = kh + [w >
+// L_{kh+1} - 1/2] unless w lies within 2^-19 of that half-way point -- or, for
+// 5-bit codes, of L_kh - 1/2 (below which v can fall once L_kh exceeds 2^19).
+// Those rare cases return `near` and are settled by lis_code_exact.
 template <bool WIDE>
-__device__ __forceinline__ uint32_t lis_code(uint64_t e, float ef, float sf, const uint64_t *Et, int kmax)
+__device__ __forceinline__ int lis_code_fast(float sf, float ef, int kmax, int &kh, bool &near)
 {
-    // t = 2 (E + 127) + (first mantissa bit); kh = E + that bit for E >= 1
-    const int t = __float_as_int(__fdividef(sf, ef)) >> 22;
-    const int kh = t >= 256 ? min(((t + 1) >> 1) - 127, kmax) : 0;
-    int k = Et[kh + 1] >= e ? kh + 1 : kh;
-    if constexpr (WIDE) k = Et[kh] >= e ? k : kh - 1;
-    return (uint32_t)min(k, kmax);
+    const float w = __fdividef(sf, ef);
+    const int t = __float_as_int(w) >> 22;  // 2 (E + 127) + first mantissa bit
+    kh = t >= 256 ? min(((t + 1) >> 1) - 127, kmax + 1) : 0;
+    // L_{kh+1} - 1/2: 1.5 for kh = 0, else 1.5 * 2^kh - 0.5
+    const float hn = kh == 0 ? 1.5f : __fsub_rn(__int_as_float(((kh + 127) << 23) | 0x400000), 0.5f);
+    near = fabsf(__fsub_rn(w, hn)) <= hn * 1.9073486e-6f;  // 2^-19
+    if constexpr (WIDE) {
+        if (kh >= 1) {
+            const float hl = kh == 1 ? 1.5f : __fsub_rn(__int_as_float(((kh + 126) << 23) | 0x400000), 0.5f);
+            near = near || fabsf(__fsub_rn(w, hl)) <= hl * 1.9073486e-6f;
+        }
+    }
+    return min(kh + (w > hn ? 1 : 0), kmax);
+}
+
+// The exact count around kh: v lies within one threshold of kh either way.
+__device__ __noinline__ int lis_code_exact(uint64_t s, uint64_t e, int kh, int kmax)
+{
+    int k = kh >= 1 ? kh - 1 + (int)ratio_reaches(s, e, step_value(kh)) : 0;
+    k += (int)ratio_reaches(s, e, step_value(kh + 1));
+    return min(k, kmax);
 }
 
 // Sum over the warp of per-lane u64 values whose total is below 2^64, as three
@@ -139,9 +140,7 @@ __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v)
 template <int R, bool WIDE>
 __global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(const __grid_constant__ LisArgs a)
 {
-    __shared__ uint64_t Etab[kLisWarps][34];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    uint64_t *Et = Etab[w];
     const int64_t L = a.L;
     for (int64_t row = (int64_t)blockIdx.x * kLisWarps + w; row < a.rows;
          row += (int64_t)gridDim.x * kLisWarps) {
@@ -167,12 +166,17 @@ __global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(const _
                 if (lane + 32 * j < Li) s += ev[j];
             }
             s = warp_sum_u64(s);
-            lis_table(s, lane, a, Et);
             const float sf = __ull2float_rn(s);
+            int kc[R], khs[R];
+            bool nr[R];
+#pragma unroll
+            for (int j = 0; j < R; ++j) kc[j] = lis_code_fast<WIDE>(sf, ef[j], a.kmax, khs[j], nr[j]);
 #pragma unroll
             for (int j = 0; j < R; ++j) {
+                // the exact comparisons only where an estimate fell near a half-way point
+                if (__any_sync(kFull, nr[j]) && nr[j]) kc[j] = lis_code_exact(s, ev[j], khs[j], a.kmax);
                 const int i = lane + 32 * j;
-                if (i < Li) __stcs(cr + i, (uint8_t)lis_code<WIDE>(ev[j], ef[j], sf, Et, a.kmax));
+                if (i < Li) __stcs(cr + i, (uint8_t)kc[j]);
             }
         } else {
             int32_t mx = INT32_MIN;
@@ -182,14 +186,16 @@ __global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(const _
             float ef;
             for (int64_t i = lane; i < L; i += 32) s += lis_exp(__ldg(xr + i), mx, a, ef);
             s = warp_sum_u64(s);
-            lis_table(s, lane, a, Et);
             const float sf = __ull2float_rn(s);
             for (int64_t i = lane; i < L; i += 32) {
                 const uint64_t e = lis_exp(__ldg(xr + i), mx, a, ef);
-                __stcs(cr + i, (uint8_t)lis_code<WIDE>(e, ef, sf, Et, a.kmax));
+                int kh;
+                bool nr;
+                int k = lis_code_fast<WIDE>(sf, ef, a.kmax, kh, nr);
+                if (nr) k = lis_code_exact(s, e, kh, a.kmax);
+                __stcs(cr + i, (uint8_t)k);
             }
         }
-        __syncwarp();  // Et is rewritten for the next row
     }
 }
 
@@ -290,8 +296,6 @@ __global__ void __launch_bounds__(256) attn_shift_v_kernel(ShiftArgs a)
 // integers and writes 16 consecutive int32 per thread and piece.
 constexpr int kMmaRows = 128;
 constexpr int kMmaKC = 64;   // tokens per round: one 64-element K atom
-constexpr int kMmaGroups = kMmaKC / 4;                 // 4-token groups per row and round
-constexpr int kAItems = kMmaRows * kMmaGroups / 256;   // code words per thread and round
 constexpr int kVMax = kMmaKC * 128 / 16 / 256;         // value chunks per thread at d = 128
 
 struct ShiftMmaArgs {
@@ -305,12 +309,13 @@ struct ShiftMmaArgs {
     uint32_t rcp_c;       // m = d / 16 (0 when d == 16: the quotient is n)
     uint32_t rcp_d;       // m = d
     uint32_t tmem_cols;
+    uint32_t tile_bytes;  // shared memory for the CTA's rows of codes (min(128, Lq) Lk + 32, rounded up)
     uint32_t *status;
 };
 
-__host__ __device__ constexpr uint32_t shift_mma_smem(int d, bool hi)
+__host__ __device__ constexpr uint32_t shift_mma_smem(int d, bool hi, uint32_t tile_bytes)
 {
-    return 1024u + (hi ? 2u : 1u) * kMmaRows * 128u + (uint32_t)d * 128u + (uint32_t)(kMmaKC * d) + 64u;
+    return 1024u + (hi ? 2u : 1u) * kMmaRows * 128u + (uint32_t)d * 128u + (uint32_t)(kMmaKC * d) + 64u + tile_bytes;
 }
 
 // fp32 value of an exact integer with |f| <= 2^22 -> int32 without the conversion pipe.
@@ -319,36 +324,14 @@ __device__ __forceinline__ int32_t exact_f2i_small(uint32_t fbits)
     return __float_as_int(__fadd_rn(__int_as_float(fbits), 12582912.0f)) - 0x4B400000;
 }
 
-// Global loads of one round into registers: per thread 8 words of 4 codes (16
-// lanes per row, lane g holding tokens 4g .. 4g+3: two aligned word loads and a
-// funnel shift, codes past Lk or rows past Lq set to 0xFF, i.e. weight 0) and up
-// to 2 chunks of 16 value bytes (zero past Lk).
-__device__ __forceinline__ void shift_load_round(const ShiftMmaArgs &a, int64_t b, int i0, int tid, int rd,
-                                                 const int8_t *vb, uint32_t (&cw)[kAItems], uint4 (&vw)[kVMax])
+// The value rows of one round into registers: up to 2 chunks of 16 bytes per
+// thread (zero past Lk).
+__device__ __forceinline__ void shift_load_values(const ShiftMmaArgs &a, int tid, int rd, const int8_t *vb,
+                                                  uint4 (&vw)[kVMax])
 {
     const int d = a.d;
     const int t0 = rd * kMmaKC;
     const int ntok = min(kMmaKC, (a.Lk - t0 + 15) / 16 * 16);
-    const int gpr = ntok / 4, g = tid % kMmaGroups;
-    const int t = t0 + 4 * g;
-    const int r0 = tid / kMmaGroups;
-    const uint64_t rb = (uint64_t)((b * a.Lq + i0 + r0) * (int64_t)a.Lk) + (uint64_t)t;
-#pragma unroll
-    for (int u = 0; u < kAItems; ++u) {
-        const int i = i0 + r0 + (256 / kMmaGroups) * u;
-        uint32_t c = 0xFFFFFFFFu;
-        if (g < gpr && i < a.Lq && t < a.Lk) {
-            const uint64_t addr = rb + (uint64_t)((256 / kMmaGroups) * u) * (uint64_t)a.Lk;
-            const uint64_t a0 = addr & ~3ull;
-            const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(a.code + a0));
-            const uint32_t w1 =
-                (a0 + 4 < a.code_bytes) ? __ldg(reinterpret_cast<const uint32_t *>(a.code + a0 + 4)) : 0u;
-            c = __funnelshift_r(w0, w1, (uint32_t)(addr & 3u) * 8u);
-            const int nv = a.Lk - t;
-            if (nv < 4) c |= 0xFFFFFFFFu << (8 * nv);
-        }
-        cw[u] = c;
-    }
     const int chunks = ntok * d / 16;
 #pragma unroll
     for (int u = 0; u < kVMax; ++u) {
@@ -374,15 +357,31 @@ __global__ void __launch_bounds__(256, 4) attn_shift_mma_kernel(const __grid_con
     const uint32_t batom = (uint32_t)d * 128u;  // bytes of the K atom of B
     uint8_t *raw = Bs + batom;                  // value rows of the round, [token][d]
     uint64_t *bar = reinterpret_cast<uint64_t *>(raw + kMmaKC * d);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+    uint64_t *tbar = bar + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 2);
     uint32_t *ok_flag = tmem_slot + 1;
+    uint8_t *tile = reinterpret_cast<uint8_t *>(bar) + 64;  // the CTA's rows of codes
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t b = blockIdx.y;
     const int i0 = blockIdx.x * kMmaRows;
+    const int rows_here = min(kMmaRows, a.Lq - i0);
+    // the CTA's codes are one contiguous range: rows i0 .. i0 + rows_here of head b
+    const uint64_t tile_start = (uint64_t)((b * a.Lq + i0) * (int64_t)a.Lk);
+    const uint64_t tile_end = tile_start + (uint64_t)rows_here * (uint64_t)a.Lk;
+    const uint64_t s0 = tile_start & ~15ull;  // bulk copies start and end on 16-byte boundaries
+    const uint64_t e1 = min((tile_end + 15) & ~15ull, a.code_bytes & ~15ull);
+    const uint32_t toff = (uint32_t)(tile_start - s0);
     if (tid == 0) {
         mbar_init(smem_u32(bar), 1);
+        mbar_init(smem_u32(tbar), 1);
         fence_mbar_init();
+        if (e1 > s0) {
+            mbar_arrive_expect_tx(smem_u32(tbar), (uint32_t)(e1 - s0));
+            bulk_g2s(smem_u32(tile), a.code + s0, (uint32_t)(e1 - s0), smem_u32(tbar));
+        } else {
+            mbar_arrive(smem_u32(tbar));
+        }
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
@@ -395,41 +394,57 @@ __global__ void __launch_bounds__(256, 4) attn_shift_mma_kernel(const __grid_con
     const uint32_t idesc = idesc_f32acc(0, 0, kMmaRows, (uint32_t)d);
     const int8_t *vb = a.v + b * (int64_t)a.Lk * d;
     const int rounds = (a.Lk + kMmaKC - 1) / kMmaKC;
-    const int g = tid % kMmaGroups;
-    uint32_t cw[kAItems];
     uint4 vw[kVMax];
-    shift_load_round(a, b, i0, tid, 0, vb, cw, vw);
+    shift_load_values(a, tid, 0, vb, vw);
     bool ok = true;
+    {
+        // the code tile: bulk copy (one warp polls its barrier), then the bytes past the
+        // last whole 16-byte block of the buffer, if this tile reaches them, by plain loads
+        if (warp == 0) {
+            const bool done = mbar_wait(smem_u32(tbar), 0u, a.status);
+            if (lane == 0) *ok_flag = done ? 1u : 0u;
+        }
+        __syncthreads();
+        ok = *reinterpret_cast<volatile uint32_t *>(ok_flag) != 0u;
+        for (uint64_t x = max(e1, tile_start) + tid; x < tile_end; x += 256) tile[x - s0] = a.code[x];
+        __syncthreads();
+    }
     for (int rd = 0; rd < rounds && ok; ++rd) {
         const int t0 = rd * kMmaKC;
         const int nks = min(kMmaKC / 16, (a.Lk - t0 + 15) / 16);  // K steps of 16 this round
         const int ntok = nks * 16;                                 // tokens written (zero past Lk)
-        const int gpr = ntok / 4;
+        const int gpr = ntok / 4;  // 4-token groups per row this round
         const int chunks = ntok * d / 16;
-        if (g < gpr) {
-#pragma unroll
-            for (int u = 0; u < kAItems; ++u) {
-                const int row = tid / kMmaGroups + (256 / kMmaGroups) * u;
-                // rows past Lq hold zero weights from the first round on
-                if (rd > 0 && i0 + row >= a.Lq) continue;
-                const uint32_t c = cw[u];
-                // weight high bytes: the table by code & 7; bit 3 splits lo from hi; codes >= 16 are 0
-                const uint32_t x = c & 0x07070707u;
-                const uint32_t sel = prmt(x | (x >> 4), 0u, 0x4420u);
-                const uint32_t tb = prmt(a.tab0, a.tab1, sel);
-                const uint32_t b3 = prmt(c << 4, 0u, 0xBA98u);
-                const uint32_t big = prmt(((c & 0xF0F0F0F0u) >> 1) + 0x78787878u, 0u, 0xBA98u);
-                const int kk = 4 * g;
-                const uint32_t off = (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u +
-                                     ((((uint32_t)kk >> 3) ^ (uint32_t)(row & 7)) << 4) + (uint32_t)(kk & 7) * 2u;
-                if constexpr (HI) {
-                    const uint32_t lo = tb & b3 & ~big, hi = tb & ~b3 & ~big;
-                    *reinterpret_cast<uint2 *>(A_lo + off) = make_uint2(prmt(lo, 0u, 0x1404u), prmt(lo, 0u, 0x3424u));
-                    *reinterpret_cast<uint2 *>(A_hi + off) = make_uint2(prmt(hi, 0u, 0x1404u), prmt(hi, 0u, 0x3424u));
-                } else {
-                    const uint32_t lo = tb & ~b3 & ~big;
-                    *reinterpret_cast<uint2 *>(A_lo + off) = make_uint2(prmt(lo, 0u, 0x1404u), prmt(lo, 0u, 0x3424u));
-                }
+        // rows past Lq get zero weights in the first round and keep them
+        const int nrows = rd == 0 ? kMmaRows : rows_here;
+        const uint32_t rcp_gpr = (uint32_t)((0x100000000ull + (uint64_t)gpr - 1) / (uint64_t)gpr);
+        for (int it = tid; it < nrows * gpr; it += 256) {
+            const int row = (int)__umulhi((uint32_t)it, rcp_gpr);  // it / gpr (it < 2^16)
+            const int kk = 4 * (it - row * gpr);
+            const int t = t0 + kk;
+            uint32_t c = 0xFFFFFFFFu;  // >= 2^bits: weight 0
+            if (row < rows_here && t < a.Lk) {
+                const uint32_t off = toff + (uint32_t)row * (uint32_t)a.Lk + (uint32_t)t;
+                const uint32_t *wp = reinterpret_cast<const uint32_t *>(tile + (off & ~3u));
+                c = __funnelshift_r(wp[0], wp[1], (off & 3u) * 8u);
+                const int nv = a.Lk - t;
+                if (nv < 4) c |= 0xFFFFFFFFu << (8 * nv);
+            }
+            // weight high bytes: the table by code & 7; bit 3 splits lo from hi; codes >= 16 are 0
+            const uint32_t x = c & 0x07070707u;
+            const uint32_t sel = prmt(x | (x >> 4), 0u, 0x4420u);
+            const uint32_t tb = prmt(a.tab0, a.tab1, sel);
+            const uint32_t b3 = prmt(c << 4, 0u, 0xBA98u);
+            const uint32_t big = prmt(((c & 0xF0F0F0F0u) >> 1) + 0x78787878u, 0u, 0xBA98u);
+            const uint32_t off = (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u +
+                                 ((((uint32_t)kk >> 3) ^ (uint32_t)(row & 7)) << 4) + (uint32_t)(kk & 7) * 2u;
+            if constexpr (HI) {
+                const uint32_t lo = tb & b3 & ~big, hi = tb & ~b3 & ~big;
+                *reinterpret_cast<uint2 *>(A_lo + off) = make_uint2(prmt(lo, 0u, 0x1404u), prmt(lo, 0u, 0x3424u));
+                *reinterpret_cast<uint2 *>(A_hi + off) = make_uint2(prmt(hi, 0u, 0x1404u), prmt(hi, 0u, 0x3424u));
+            } else {
+                const uint32_t lo = tb & ~b3 & ~big;
+                *reinterpret_cast<uint2 *>(A_lo + off) = make_uint2(prmt(lo, 0u, 0x1404u), prmt(lo, 0u, 0x3424u));
             }
         }
 #pragma unroll
@@ -479,7 +494,7 @@ __global__ void __launch_bounds__(256, 4) attn_shift_mma_kernel(const __grid_con
         __syncwarp();
         // the next round's codes and values travel while the MMAs run; one warp
         // polls the barrier, the others wait at the CTA barrier without issuing
-        if (rd + 1 < rounds) shift_load_round(a, b, i0, tid, rd + 1, vb, cw, vw);
+        if (rd + 1 < rounds) shift_load_values(a, tid, rd + 1, vb, vw);
         if (warp == 0) {
             const bool done = mbar_wait(smem_u32(bar), (uint32_t)(rd & 1), a.status);
             if (lane == 0) *ok_flag = done ? 1u : 0u;
@@ -594,16 +609,6 @@ extern "C" qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t 
         a.ql = (uint32_t)l;
     }
     a.kmax = 1 << bits;
-    for (int j = 1; j <= 32; ++j) {
-        // D = 2 L_j - 1 is odd and >= 3: l = ceil(log2 D), m = floor(2^64 (2^l - D) / D) + 1
-        const uint64_t Lj = j == 1 ? 2ull : (3ull << (j - 2));
-        const uint64_t D = 2 * Lj - 1;
-        int lj = 0;
-        while ((1ull << lj) < D) ++lj;
-        const unsigned __int128 num = ((unsigned __int128)1 << 64) * (((unsigned __int128)1 << lj) - D);
-        a.magic[j - 1] = (uint64_t)(num / D) + 1;
-        a.magic_l[j - 1] = (uint32_t)lj;
-    }
     const int64_t want = (rows + kLisWarps - 1) / kLisWarps;
     cudaStream_t s = (cudaStream_t)stream;
     const int R = L <= 256 ? (int)((L + 31) / 32) : 0;
@@ -668,15 +673,16 @@ extern "C" qnn_status q_attn_shift_v(const uint8_t *code, const int8_t *v, int64
         uint32_t cols = 32;
         while (cols < (uint32_t)(hi ? 2 * d : d)) cols *= 2;
         m.tmem_cols = cols;
+        m.tile_bytes = ((uint32_t)std::min(Lq, kMmaRows) * (uint32_t)Lk + 32u + 127u) & ~127u;
         m.status = status_word();
-        const uint32_t smem = shift_mma_smem(d, hi);
+        const uint32_t smem = shift_mma_smem(d, hi, m.tile_bytes);
         const dim3 grid((Lq + kMmaRows - 1) / kMmaRows, (unsigned)batch);
         // the largest dynamic shared memory (d = 128) is set once per kernel and process
         static std::atomic<int> attr_set[2];
         auto kern = hi ? attn_shift_mma_kernel<true> : attn_shift_mma_kernel<false>;
         if (!attr_set[hi].load(std::memory_order_acquire)) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)shift_mma_smem(128, hi)) != cudaSuccess)
+                                     (int)shift_mma_smem(128, hi, 128u * 512u + 128u)) != cudaSuccess)
                 return QNN_ERR_CUDA;
             attr_set[hi].store(1, std::memory_order_release);
         }
