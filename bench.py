@@ -514,6 +514,14 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
                                     "GMAC/s": round(Bh * Lt * Lt * dh / (ms * 1e-3) / 1e9, 1),
                                     "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
                                     "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
+    # the same two steps in one kernel (codes kept in shared memory)
+    t = time_steps(torch, lambda: qnn.q_lis_attn_v(xl, workloads.ATTN_S, vq, Bh, Lt, Lt, dh, 4, ov, stream=stream),
+                   steps, 3, flush, stream)
+    ms = statistics.median(t)
+    byts = 4 * Bh * Lt * Lt + Bh * Lt * dh + 4 * Bh * Lt * dh
+    out["lis_attn_v_fused_vitb_b64"] = {"ms": round(ms, 4), "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
+                                        "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / hbm, 4),
+                                        "bytes": "int32 logits + V + int32 out"}
     del xl, codes, vq, ov
 
     # integer LayerNorm over ViT-B activations at batch 64 (PTF factors), s8 out
@@ -652,7 +660,7 @@ def run_case(args):
         ly = torch.empty((R, C), dtype=torch.int8, device=device)
         fn = lambda: qnn.q_int_layernorm(lx, R, C, wl["s"], lg, lb, lo, ly, alpha=la,  # noqa: E731
                                          alpha_max=int(wl["alpha"].max()), stream=stream)
-    elif case in ("lis", "shift", "attn"):
+    elif case in ("lis", "shift", "attn", "fused"):
         Bh, Lt, dh = 64 * 12, 197, 64
         xl = workloads.device_attention_logits(Bh * Lt, Lt, 1234, device)
         codes = torch.empty((Bh * Lt, Lt), dtype=torch.uint8, device=device)
@@ -665,6 +673,9 @@ def run_case(args):
             ov = torch.empty((Bh, Lt, dh), dtype=torch.int32, device=device)
 
             def fn():
+                if case == "fused":
+                    qnn.q_lis_attn_v(xl, workloads.ATTN_S, vq, Bh, Lt, Lt, dh, 4, ov, stream=stream)
+                    return
                 if case == "attn":
                     qnn.q_log_int_softmax(xl, Bh * Lt, Lt, workloads.ATTN_S, 4, codes, stream=stream)
                 qnn.q_attn_shift_v(codes, vq, Bh, Lt, Lt, dh, 4, ov, stream=stream)
@@ -769,7 +780,8 @@ def main():
     ap.add_argument("--case", default=None,
                     help="run one workload only (profiling): quantize, vit_fc1, square_4096, "
                          "vitl_fc2, conv3x3, conv1x1, gemm:M:N:K (u8 x s8 -> s8), lis, shift, "
-                         "attn (ViT-B b64 Log-Int-Softmax, shift product, both), layernorm, eltwise, dynquant")
+                         "attn (ViT-B b64 Log-Int-Softmax, shift product, both), fused (both in one kernel), layernorm, "
+                         "eltwise, dynquant")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

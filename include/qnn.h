@@ -339,6 +339,15 @@ qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t L, float S,
 qnn_status q_attn_shift_v(const uint8_t *code, const int8_t *v, int64_t batch, int Lq, int Lk, int d,
                           int bits, int32_t *out, qnn_stream_t stream);
 
+/* The two calls above in one kernel [FQ 3.3, Integer-only 推理: the whole
+ * attention after Q K^T stays integer]: for each head, q_log_int_softmax of the
+ * logit rows x (int32 [batch][Lq][Lk], scale S) and q_attn_shift_v of the
+ * resulting codes with v -- the same out, bit for bit, but the log2 codes live
+ * only in shared memory and never reach global memory.  Lk <= 256, d <= 128,
+ * bits 1..4; the other conditions of both calls apply. */
+qnn_status q_lis_attn_v(const int32_t *x, float S, const int8_t *v, int64_t batch, int Lq, int Lk, int d, int bits,
+                        int32_t *out, qnn_stream_t stream);
+
 /* ---- integer LayerNorm [FQ 3.2] --------------------------------------------- */
 
 /* LayerNorm of `rows` rows of C s8 codes x (row-major [rows][C]) quantized with

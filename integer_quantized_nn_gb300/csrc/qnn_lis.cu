@@ -311,6 +311,9 @@ struct ShiftMmaArgs {
     uint32_t tmem_cols;
     uint32_t tile_bytes;  // shared memory for the CTA's rows of codes (min(128, Lq) Lk + 32, rounded up)
     uint32_t *status;
+    // fused form: the codes are computed here from int32 logits (Log-Int-Softmax)
+    const int32_t *x;     // [B][Lq][Lk] or null
+    LisArgs lis;          // its constants (x, code, rows, L unused)
 };
 
 __host__ __device__ constexpr uint32_t shift_mma_smem(int d, bool hi, uint32_t tile_bytes)
@@ -345,7 +348,53 @@ __device__ __forceinline__ void shift_load_values(const ShiftMmaArgs &a, int tid
     }
 }
 
-template <bool HI>
+// Log-Int-Softmax of the CTA's rows straight into the shared code tile (row r
+// at r * Lk): warp w takes rows w, w + 8, ...; a row of L <= 256 values is held
+// in registers, up to 8 per lane.
+template <bool WIDE>
+__device__ __forceinline__ void lis_rows_to_tile(const ShiftMmaArgs &a, int64_t row0, int rows_here, uint8_t *tile,
+                                                 int warp, int lane)
+{
+    const LisArgs &la = a.lis;
+    const int L = a.Lk;
+    for (int r = warp; r < rows_here; r += 8) {
+        const int32_t *xr = a.x + (row0 + r) * (int64_t)L;
+        int32_t xv[8];
+        int32_t mx = INT32_MIN;
+        // slots past the row (32 j >= L) are skipped by the whole warp
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = lane + 32 * j;
+            xv[j] = (32 * j < L && i < L) ? __ldcs(xr + i) : INT32_MIN;
+            mx = max(mx, xv[j]);
+        }
+        mx = __reduce_max_sync(kFull, mx);
+        uint64_t ev[8];
+        float ef[8];
+        uint64_t s = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (32 * j >= L) break;
+            ev[j] = lis_exp(xv[j], mx, la, ef[j]);
+            if (lane + 32 * j < L) s += ev[j];
+        }
+        s = warp_sum_u64(s);
+        const float sf = __ull2float_rn(s);
+        uint8_t *tr = tile + r * L;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (32 * j >= L) break;  // warp-uniform
+            int kh;
+            bool nr;
+            int k = lis_code_fast<WIDE>(sf, ef[j], la.kmax, kh, nr);
+            if (__any_sync(kFull, nr) && nr) k = lis_code_exact(s, ev[j], kh, la.kmax);
+            const int i = lane + 32 * j;
+            if (i < L) tr[i] = (uint8_t)k;
+        }
+    }
+}
+
+template <bool HI, bool FUSED>
 __global__ void __launch_bounds__(256, 4) attn_shift_mma_kernel(const __grid_constant__ ShiftMmaArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -371,12 +420,14 @@ __global__ void __launch_bounds__(256, 4) attn_shift_mma_kernel(const __grid_con
     const uint64_t tile_end = tile_start + (uint64_t)rows_here * (uint64_t)a.Lk;
     const uint64_t s0 = tile_start & ~15ull;  // bulk copies start and end on 16-byte boundaries
     const uint64_t e1 = min((tile_end + 15) & ~15ull, a.code_bytes & ~15ull);
-    const uint32_t toff = (uint32_t)(tile_start - s0);
+    const uint32_t toff = FUSED ? 0u : (uint32_t)(tile_start - s0);
     if (tid == 0) {
         mbar_init(smem_u32(bar), 1);
         mbar_init(smem_u32(tbar), 1);
         fence_mbar_init();
-        if (e1 > s0) {
+        if (FUSED) {
+            mbar_arrive(smem_u32(tbar));
+        } else if (e1 > s0) {
             mbar_arrive_expect_tx(smem_u32(tbar), (uint32_t)(e1 - s0));
             bulk_g2s(smem_u32(tile), a.code + s0, (uint32_t)(e1 - s0), smem_u32(tbar));
         } else {
@@ -406,7 +457,12 @@ __global__ void __launch_bounds__(256, 4) attn_shift_mma_kernel(const __grid_con
         }
         __syncthreads();
         ok = *reinterpret_cast<volatile uint32_t *>(ok_flag) != 0u;
-        for (uint64_t x = max(e1, tile_start) + tid; x < tile_end; x += 256) tile[x - s0] = a.code[x];
+        if constexpr (FUSED) {
+            if (a.lis.kmax == 32) lis_rows_to_tile<true>(a, b * a.Lq + i0, rows_here, tile, warp, lane);
+            else lis_rows_to_tile<false>(a, b * a.Lq + i0, rows_here, tile, warp, lane);
+        } else {
+            for (uint64_t x = max(e1, tile_start) + tid; x < tile_end; x += 256) tile[x - s0] = a.code[x];
+        }
         __syncthreads();
     }
     for (int rd = 0; rd < rounds && ok; ++rd) {
@@ -565,29 +621,25 @@ qnn_status lis_constants(float S, LisConsts *k)
 }  // namespace
 }  // namespace qnn
 
-extern "C" qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t L, float S, int bits,
-                                        uint8_t *code, qnn_stream_t stream)
+namespace qnn {
+namespace {
+
+// Validated Log-Int-Softmax constants for scale S, code width bits and row length L.
+qnn_status lis_prepare(float S, int bits, int64_t L, LisArgs &a)
 {
-    using namespace qnn;
-    if (rows < 0 || L <= 0 || bits < 1 || bits > 5) return QNN_ERR_INVALID_ARG;
+    if (L <= 0 || bits < 1 || bits > 5) return QNN_ERR_INVALID_ARG;
     LisConsts k;
     const qnn_status st = lis_constants(S, &k);
     if (st != QNN_OK) return st;
     // s <= L * c_int * 2^30 must stay below 2^64
     if ((uint64_t)L > ((1ull << 34) - 1) / (uint64_t)k.c) return QNN_ERR_OVERFLOW_RISK;
-    if (rows == 0) return QNN_OK;
-    if (x == nullptr || code == nullptr) return QNN_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(code)) return QNN_ERR_ALIGNMENT;
     // z = c - r (b - r) must stay in (0, c] for every remainder r in [0, x0n):
     // r <= b, and the largest r (b - r), at r nearest b / 2, below c
     const int64_t x0n = -k.x0;
     if (30 * x0n >= (1 << 21) || k.b < x0n - 1) return QNN_ERR_INVALID_ARG;
     for (int64_t r : {std::min(x0n - 1, k.b / 2), std::min(x0n - 1, (k.b + 1) / 2), x0n - 1})
         if (r * (k.b - r) >= k.c) return QNN_ERR_INVALID_ARG;
-    LisArgs a{};
-    a.x = x;
-    a.code = code;
-    a.rows = rows;
+    a = LisArgs{};
     a.L = L;
     a.x0n = (uint32_t)x0n;
     a.ndmax = (uint32_t)(30 * x0n);
@@ -609,6 +661,81 @@ extern "C" qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t 
         a.ql = (uint32_t)l;
     }
     a.kmax = 1 << bits;
+    return QNN_OK;
+}
+
+// Shape checks shared by the shift product and the fused attention.
+qnn_status shift_check(int64_t batch, int Lq, int Lk, int d, int bits)
+{
+    if (batch < 0 || Lq < 0 || Lk <= 0 || d <= 0 || bits < 1 || bits > 4) return QNN_ERR_INVALID_ARG;
+    if (d % 16 != 0) return QNN_ERR_UNSUPPORTED;
+    if (batch > 65535) return QNN_ERR_UNSUPPORTED;
+    // |sum| <= Lk * 128 * 2^(2^bits - 1) must fit int32
+    if ((int64_t)Lk * 128 * (1ll << ((1 << bits) - 1)) > (1ll << 31)) return QNN_ERR_OVERFLOW_RISK;
+    return QNN_OK;
+}
+
+// The tensor-pipe shift product (fused: codes computed from m.x first).
+template <bool FUSED>
+qnn_status launch_shift_mma(ShiftMmaArgs &m, const uint8_t *code, const int8_t *v, int32_t *out, int64_t batch,
+                            int Lq, int Lk, int d, int bits, cudaStream_t s)
+{
+    // weights split into two fp16 halves when N = 2^bits - 1 >= 8
+    const bool hi = bits == 4;
+    const int N = (1 << bits) - 1;
+    uint8_t tab[8];
+    for (int j = 0; j < 8; ++j) {
+        const int e = hi ? 7 - j : N - j;  // exponent of the weight for code & 7 == j
+        tab[j] = (uint8_t)(e >= 0 ? (e + 15) << 2 : 0);
+    }
+    m.code = code;
+    m.v = v;
+    m.out = out;
+    m.code_bytes = (uint64_t)batch * (uint64_t)Lq * (uint64_t)Lk;
+    m.Lq = Lq;
+    m.Lk = Lk;
+    m.d = d;
+    m.tab0 = (uint32_t)tab[0] | ((uint32_t)tab[1] << 8) | ((uint32_t)tab[2] << 16) | ((uint32_t)tab[3] << 24);
+    m.tab1 = (uint32_t)tab[4] | ((uint32_t)tab[5] << 8) | ((uint32_t)tab[6] << 16) | ((uint32_t)tab[7] << 24);
+    m.rcp_d = (uint32_t)((0x100000000ull + (uint64_t)d - 1) / (uint64_t)d);
+    m.rcp_c = d == 16 ? 0u : (uint32_t)((0x100000000ull + (uint64_t)(d / 16) - 1) / (uint64_t)(d / 16));
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(hi ? 2 * d : d)) cols *= 2;
+    m.tmem_cols = cols;
+    m.tile_bytes = ((uint32_t)std::min(Lq, kMmaRows) * (uint32_t)Lk + 32u + 127u) & ~127u;
+    m.status = status_word();
+    const uint32_t smem = shift_mma_smem(d, hi, m.tile_bytes);
+    const dim3 grid((Lq + kMmaRows - 1) / kMmaRows, (unsigned)batch);
+    // the largest dynamic shared memory (d = 128, Lk = 512) is set once per kernel and process
+    static std::atomic<int> attr_set[2];
+    auto kern = hi ? attn_shift_mma_kernel<true, FUSED> : attn_shift_mma_kernel<false, FUSED>;
+    if (!attr_set[hi].load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)shift_mma_smem(128, hi, 128u * 512u + 128u)) != cudaSuccess)
+            return QNN_ERR_CUDA;
+        attr_set[hi].store(1, std::memory_order_release);
+    }
+    kern<<<grid, 256, smem, s>>>(m);
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace qnn
+
+extern "C" qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t L, float S, int bits,
+                                        uint8_t *code, qnn_stream_t stream)
+{
+    using namespace qnn;
+    if (rows < 0) return QNN_ERR_INVALID_ARG;
+    LisArgs a;
+    const qnn_status st = lis_prepare(S, bits, L, a);
+    if (st != QNN_OK) return st;
+    if (rows == 0) return QNN_OK;
+    if (x == nullptr || code == nullptr) return QNN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(code)) return QNN_ERR_ALIGNMENT;
+    a.x = x;
+    a.code = code;
+    a.rows = rows;
     const int64_t want = (rows + kLisWarps - 1) / kLisWarps;
     cudaStream_t s = (cudaStream_t)stream;
     const int R = L <= 256 ? (int)((L + 31) / 32) : 0;
@@ -640,57 +767,35 @@ extern "C" qnn_status q_attn_shift_v(const uint8_t *code, const int8_t *v, int64
                                      int d, int bits, int32_t *out, qnn_stream_t stream)
 {
     using namespace qnn;
-    if (batch < 0 || Lq < 0 || Lk <= 0 || d <= 0 || bits < 1 || bits > 4) return QNN_ERR_INVALID_ARG;
-    if (d % 16 != 0) return QNN_ERR_UNSUPPORTED;
-    if (batch > 65535) return QNN_ERR_UNSUPPORTED;
-    // |sum| <= Lk * 128 * 2^(2^bits - 1) must fit int32
-    if ((int64_t)Lk * 128 * (1ll << ((1 << bits) - 1)) > (1ll << 31)) return QNN_ERR_OVERFLOW_RISK;
+    qnn_status st = shift_check(batch, Lq, Lk, d, bits);
+    if (st != QNN_OK) return st;
     if (batch == 0 || Lq == 0) return QNN_OK;
     if (code == nullptr || v == nullptr || out == nullptr) return QNN_ERR_INVALID_ARG;
     if (!aligned16(code) || !aligned16(v) || !aligned16(out)) return QNN_ERR_ALIGNMENT;
     cudaStream_t s = (cudaStream_t)stream;
     if (d <= 128 && Lk <= 512) {
-        // tensor pipe: weights split into two fp16 halves when N = 2^bits - 1 >= 8
-        const bool hi = bits == 4;
-        const int N = (1 << bits) - 1;
-        uint8_t tab[8];
-        for (int m = 0; m < 8; ++m) {
-            const int e = hi ? 7 - m : N - m;  // exponent of the weight for code & 7 == m
-            tab[m] = (uint8_t)(e >= 0 ? (e + 15) << 2 : 0);
-        }
         ShiftMmaArgs m{};
-        m.code = code;
-        m.v = v;
-        m.out = out;
-        m.code_bytes = (uint64_t)batch * (uint64_t)Lq * (uint64_t)Lk;
-        m.Lq = Lq;
-        m.Lk = Lk;
-        m.d = d;
-        m.tab0 = (uint32_t)tab[0] | ((uint32_t)tab[1] << 8) | ((uint32_t)tab[2] << 16) | ((uint32_t)tab[3] << 24);
-        m.tab1 = (uint32_t)tab[4] | ((uint32_t)tab[5] << 8) | ((uint32_t)tab[6] << 16) | ((uint32_t)tab[7] << 24);
-        m.rcp_d = (uint32_t)((0x100000000ull + (uint64_t)d - 1) / (uint64_t)d);
-        m.rcp_c = d == 16 ? 0u : (uint32_t)((0x100000000ull + (uint64_t)(d / 16) - 1) / (uint64_t)(d / 16));
-        uint32_t cols = 32;
-        while (cols < (uint32_t)(hi ? 2 * d : d)) cols *= 2;
-        m.tmem_cols = cols;
-        m.tile_bytes = ((uint32_t)std::min(Lq, kMmaRows) * (uint32_t)Lk + 32u + 127u) & ~127u;
-        m.status = status_word();
-        const uint32_t smem = shift_mma_smem(d, hi, m.tile_bytes);
-        const dim3 grid((Lq + kMmaRows - 1) / kMmaRows, (unsigned)batch);
-        // the largest dynamic shared memory (d = 128) is set once per kernel and process
-        static std::atomic<int> attr_set[2];
-        auto kern = hi ? attn_shift_mma_kernel<true> : attn_shift_mma_kernel<false>;
-        if (!attr_set[hi].load(std::memory_order_acquire)) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)shift_mma_smem(128, hi, 128u * 512u + 128u)) != cudaSuccess)
-                return QNN_ERR_CUDA;
-            attr_set[hi].store(1, std::memory_order_release);
-        }
-        kern<<<grid, 256, smem, s>>>(m);
-        return launch_status();
+        return launch_shift_mma<false>(m, code, v, out, batch, Lq, Lk, d, bits, s);
     }
     ShiftArgs a{code, v, out, Lq, Lk, d, 1 << bits};
     const dim3 grid((Lq + kShM - 1) / kShM, (d + kShN - 1) / kShN, (unsigned)batch);
     attn_shift_v_kernel<<<grid, 256, 0, s>>>(a);
     return launch_status();
+}
+
+extern "C" qnn_status q_lis_attn_v(const int32_t *x, float S, const int8_t *v, int64_t batch, int Lq, int Lk, int d,
+                                   int bits, int32_t *out, qnn_stream_t stream)
+{
+    using namespace qnn;
+    qnn_status st = shift_check(batch, Lq, Lk, d, bits);
+    if (st != QNN_OK) return st;
+    if (d > 128 || Lk > 256) return QNN_ERR_UNSUPPORTED;
+    ShiftMmaArgs m{};
+    st = lis_prepare(S, bits, Lk, m.lis);
+    if (st != QNN_OK) return st;
+    if (batch == 0 || Lq == 0) return QNN_OK;
+    if (x == nullptr || v == nullptr || out == nullptr) return QNN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(v) || !aligned16(out)) return QNN_ERR_ALIGNMENT;
+    m.x = x;
+    return launch_shift_mma<true>(m, nullptr, v, out, batch, Lq, Lk, d, bits, (cudaStream_t)stream);
 }

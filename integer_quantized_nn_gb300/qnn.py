@@ -93,6 +93,7 @@ def _declare(L):
         "qgemm_zw": (c_int, [vp, c_int, vp, vp, c_int, c_int, c_int, vp, vp, vp, vp, sz, vp]),
         "q_layout_nchw64": (c_int, [vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, vp]),
         "qconv_prepack_w_u4": (c_int, [vp, vp, vp, vp, vp, vp]),
+        "q_lis_attn_v": (c_int, [vp, f32, vp, i64, c_int, c_int, c_int, c_int, vp, vp]),
         "qnn_status_string": (ctypes.c_char_p, [c_int]),
         "qnn_check_device_error": (c_int, [vp]),
         "qnn_selftest_wait_timeout": (c_int, [ctypes.c_uint64, vp]),
@@ -368,6 +369,13 @@ def q_layout_nchw64(src, to_nchw64: bool, N: int, H: int, W: int, C: int, dt: st
     load()
     _check(_SYMBOLS["q_layout_nchw64"](_ptr(src), int(bool(to_nchw64)), int(N), int(H), int(W), int(C), DTYPES[dt],
                                         _ptr(dst), _stream(stream)), "q_layout_nchw64")
+
+
+def q_lis_attn_v(x, S: float, v, batch: int, Lq: int, Lk: int, d: int, bits: int, out, stream=None):
+    """Log-Int-Softmax of int32 logits x and the shift product with v in one kernel."""
+    load()
+    _check(_SYMBOLS["q_lis_attn_v"](_ptr(x), float(S), _ptr(v), int(batch), int(Lq), int(Lk), int(d), int(bits),
+                                     _ptr(out), _stream(stream)), "q_lis_attn_v")
 
 
 def qnn_check_device_error(stream=None) -> int:

@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     for n in ("q_quantize", "q_dequantize", "qgemm_prepack_b", "q_fold_epilogue", "qgemm_s8",
               "qnn_gemm_workspace_bytes", "qgemm_pack_a", "qgemm_s8_packed", "qgemm_s8_static_scratch",
               "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_conv_workspace_bytes",
-              "q_log_int_softmax", "q_attn_shift_v", "q_int_layernorm", "q_eltwise_s8",
+              "q_log_int_softmax", "q_attn_shift_v", "q_lis_attn_v", "q_int_layernorm", "q_eltwise_s8",
               "q_quantize_rows_dynamic", "qgemm_prepack_b_u8", "qgemm_zw", "qnn_gemm_zw_workspace_bytes",
               "q_layout_nchw64", "qconv_prepack_w_u4", "qnn_status_string",
               "qnn_check_device_error"):

@@ -161,3 +161,35 @@ def test_lis_then_shift_vit_base(oracle):
     k = oracle.log_int_softmax(x, S, bits)
     assert np.array_equal(host(cd), k)
     assert np.array_equal(host(od).astype(np.int64), oracle.attn_shift_v(k, v, bits))
+
+
+@pytest.mark.parametrize("shape", [(4 * 12, 197, 197, 64), (3, 130, 70, 80), (2, 1, 1, 16), (1, 200, 256, 128),
+                                   (2, 64, 33, 48)])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_lis_attn_fused(oracle, shape, bits):
+    """q_lis_attn_v (Log-Int-Softmax into shared memory, then the shift product)
+    against the oracle's two steps; ragged query, token and column tiles."""
+    t = __import__("torch")
+    Bh, Lq, Lk, d = shape
+    rng = np.random.default_rng(Bh * 31 + Lk + bits)
+    S = workloads.ATTN_S if Lk <= 197 else 2.0 ** -9  # L c_int 2^30 < 2^64 at L = 256
+    x = np.rint(rng.normal(0.0, 2.5, size=(Bh, Lq, Lk)) / S).astype(np.int32)
+    x[:, :, 0] += np.int32(4.0 / S)
+    v = rng.integers(-128, 128, size=(Bh, Lk, d)).astype(np.int8)
+    out = t.full((Bh, Lq, d), 7, dtype=t.int32, device="cuda")
+    qnn.q_lis_attn_v(dev(x), S, dev(v), Bh, Lq, Lk, d, bits, out)
+    t.cuda.synchronize()
+    k = oracle.log_int_softmax(x, S, bits)
+    want = oracle.attn_shift_v(k, v, bits)
+    assert np.array_equal(host(out).astype(np.int64), want)
+
+
+def test_lis_attn_fused_errors():
+    t = __import__("torch")
+    x = t.zeros((1, 4, 300), dtype=t.int32, device="cuda")
+    v = t.zeros((1, 300, 16), dtype=t.int8, device="cuda")
+    o = t.zeros((1, 4, 16), dtype=t.int32, device="cuda")
+    with pytest.raises(qnn.QnnError):  # Lk > 256
+        qnn.q_lis_attn_v(x, 2e-4, v, 1, 4, 300, 16, 4, o)
+    with pytest.raises(qnn.QnnError):  # bits 5 has no shift product
+        qnn.q_lis_attn_v(x, 2e-4, v, 1, 4, 200, 16, 5, o)
