@@ -563,23 +563,25 @@ __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t c0, uint32_t c1, uin
 // z_out) with ReLU) and hi = qmax - z_out; z_out is then added to the integer
 // -- the fp32 result of the page's formula for every finite v (M, Bq and R
 // must be finite).  No conversion instructions are used.
-__device__ __forceinline__ void epilogue_float(const Params &p, int m, int n0, float (&a)[32],
-                                               const float *ca, const float *cb,
-                                               const uint32_t (&rw)[8])
+// RS: per-row activation scales -- each column factor becomes fl(rs * factor)
+// (instantiated separately so that the common path carries none of it).
+template <bool RS>
+__device__ __forceinline__ void epilogue_float_t(const Params &p, int m, int n0, float (&a)[32],
+                                                 const float *ca, const float *cb,
+                                                 const uint32_t (&rw)[8])
 {
     if (m >= p.M || n0 >= p.N) return;
     const bool vec = p.vec_ok;
     const int64_t base = (int64_t)m * p.N + n0;  // element offset of (m, n0)
-    // per-row activation scale: the column factor becomes fl(rs * factor); rs = 1
-    // (exact) without one
-    const float rs = p.row_scale ? __ldg(p.row_scale + m) : 1.0f;
+    float rs = 1.0f;
+    if constexpr (RS) rs = __ldg(p.row_scale + m);
     if (p.mode == QNN_EPI_DEQUANT) {
         float *C = static_cast<float *>(p.C);
         uint32_t y[32];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
             float4 d = *reinterpret_cast<const float4 *>(ca + i);
-            if (p.row_scale) {
+            if constexpr (RS) {
                 d.x = __fmul_rn(rs, d.x);
                 d.y = __fmul_rn(rs, d.y);
                 d.z = __fmul_rn(rs, d.z);
@@ -615,7 +617,7 @@ __device__ __forceinline__ void epilogue_float(const Params &p, int m, int n0, f
     for (int i = 0; i < 32; i += 4) {
         const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
         float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-        if (p.row_scale) {
+        if constexpr (RS) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) mm[k] = __fmul_rn(rs, mm[k]);
         }
@@ -655,6 +657,19 @@ __device__ __forceinline__ void epilogue_float(const Params &p, int m, int n0, f
                 C[(base + i) / 2] = (uint8_t)(ow[i >> 3] >> (4 * (i & 7)));
         }
     }
+}
+
+__device__ __forceinline__ void epilogue_float_rowscale(const Params &p, int m, int n0, float (&a)[32], const float *ca,
+                                                     const float *cb, const uint32_t (&rw)[8])
+{
+    epilogue_float_t<true>(p, m, n0, a, ca, cb, rw);
+}
+
+__device__ __forceinline__ void epilogue_float(const Params &p, int m, int n0, float (&a)[32], const float *ca,
+                                               const float *cb, const uint32_t (&rw)[8])
+{
+    if (p.row_scale) epilogue_float_rowscale(p, m, n0, a, ca, cb, rw);
+    else epilogue_float_t<false>(p, m, n0, a, ca, cb, rw);
 }
 
 // The same from int32 sums (multi-chunk K, raw int32 outputs, or zero-point
@@ -752,7 +767,8 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
             const uint32_t abuf = u & 1u;
             if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
             tc_fence_after();
-            const bool fast = store_columns<COLS>(cr, cols, lane) && !p.C32 && p.mode != QNN_EPI_S32 && !p.rowsum;
+            const bool fast = store_columns<COLS>(cr, cols, lane) && !p.C32 && p.mode != QNN_EPI_S32 && !p.rowsum &&
+                              !p.row_scale;
             const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + p0 * 32;
 #pragma unroll 1
             for (int jp = 0; jp < npieces; ++jp) {
@@ -784,7 +800,7 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
                                                       : __fadd_rn(f, z4[e]);
                         }
                     }
-                    epilogue_float(p, m, nbase + jp * 32, a, cols + jp * 32, cols + COLS + jp * 32, rw);
+                    epilogue_float_t<false>(p, m, nbase + jp * 32, a, cols + jp * 32, cols + COLS + jp * 32, rw);
                 } else {
                     int32_t acc[32];
 #pragma unroll
