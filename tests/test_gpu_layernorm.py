@@ -105,3 +105,18 @@ def test_int_layernorm_errors():
         qnn.q_int_layernorm(x, 4, 8, 0.1, f, f, f, y, y_dt="u8")
     with pytest.raises(qnn.QnnError):
         qnn.q_int_layernorm(x, 4, 8, 0.1, f[1:], f, f, y)  # misaligned gamma
+
+
+def test_int_layernorm_scales_across_binades(oracle):
+    """Output scales and gammas spread over many binades (each o[c] = 2^U(-20, 10)
+    times a random mantissa): every division by o[c] must round exactly as the
+    IEEE division the printed module performs."""
+    rng = np.random.default_rng(77)
+    C, rows = 256, 64
+    x = np.clip(np.rint(rng.normal(0, 50, size=(rows, C))), -128, 127).astype(np.int32)
+    o = (2.0 ** rng.uniform(-20, 10, size=C) * rng.uniform(1.0, 2.0, size=C)).astype(np.float32)
+    gamma = (2.0 ** rng.uniform(-12, 6, size=C) * rng.choice([-1, 1], size=C)).astype(np.float32)
+    beta = (rng.normal(0, 1, size=C) * 2.0 ** rng.uniform(-10, 10, size=C)).astype(np.float32)
+    for s in (0.013, 2.0 ** -9):
+        got = _ln_gpu(x, s, gamma, beta, o, y_dt="s32")
+        assert np.array_equal(got, _want(oracle, x, s, gamma, beta, o, None, "s32"))
