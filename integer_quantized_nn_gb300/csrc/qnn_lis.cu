@@ -91,30 +91,24 @@ __device__ __forceinline__ bool ratio_reaches(uint64_t s, uint64_t e, uint64_t L
 __device__ __forceinline__ uint64_t step_value(int j) { return j <= 1 ? 2ull : (3ull << (j - 2)); }
 
 // Code of one exponential e (fp32 value ef) in a row whose sum is s (fp32 value
-// sf): the number k of thresholds j <= kmax with round_half_even(s / e) >= L_j.
-// The fp32 estimate w of v = s / e (relative error below 2^-21) gives
-// kh = #{j : L_j <= w} from its exponent E and first mantissa bit (v >= 1.5 *
-// 2^E; 0 below 2).  Rounding v to an integer crosses at most the next threshold
-// L_{kh+1}, exactly when v > L_{kh+1} - 1/2 (ties: to even), so k = kh + [w >
-// L_{kh+1} - 1/2] unless w lies within 2^-19 of that half-way point -- or, for
-// 5-bit codes, of L_kh - 1/2 (below which v can fall once L_kh exceeds 2^19).
-// Those rare cases return `near` and are settled by lis_code_exact.
-template <bool WIDE>
+// sf): the number k of thresholds j <= kmax with round_half_even(s / e) >= L_j,
+// L_1 = 2 and L_j = 3 * 2^(j-2).  round(v) >= L exactly when v + 1/2 > L (ties:
+// to even), so with the fp32 estimate w of v = s / e (relative error below
+// 2^-21) and u = w + 1/2, k = #{j : L_j < u}: from u's exponent E and first
+// mantissa bit, ((t + 1) >> 1) - 127 with t = 2 (E + 127) + that bit, and 0 below
+// 2.  Every L_j is 2 or has the mantissa 1.5, so u lies near a threshold only
+// when its mantissa is within 32 units (2^-18.6 relative, well above the error)
+// of 1.5, 1 or 2; those rare cases return `near` and are settled by
+// lis_code_exact around kh.
 __device__ __forceinline__ int lis_code_fast(float sf, float ef, int kmax, int &kh, bool &near)
 {
-    const float w = __fdividef(sf, ef);
-    const int t = __float_as_int(w) >> 22;  // 2 (E + 127) + first mantissa bit
+    const float u = __fadd_rn(__fdividef(sf, ef), 0.5f);
+    const int bu = __float_as_int(u);
+    const int m = bu & 0x7FFFFF;
+    const int t = bu >> 22;
     kh = t >= 256 ? min(((t + 1) >> 1) - 127, kmax + 1) : 0;
-    // L_{kh+1} - 1/2: 1.5 for kh = 0, else 1.5 * 2^kh - 0.5
-    const float hn = kh == 0 ? 1.5f : __fsub_rn(__int_as_float(((kh + 127) << 23) | 0x400000), 0.5f);
-    near = fabsf(__fsub_rn(w, hn)) <= hn * 1.9073486e-6f;  // 2^-19
-    if constexpr (WIDE) {
-        if (kh >= 1) {
-            const float hl = kh == 1 ? 1.5f : __fsub_rn(__int_as_float(((kh + 126) << 23) | 0x400000), 0.5f);
-            near = near || fabsf(__fsub_rn(w, hl)) <= hl * 1.9073486e-6f;
-        }
-    }
-    return min(kh + (w > hn ? 1 : 0), kmax);
+    near = abs(m - 0x400000) <= 32 || m <= 32 || m >= 0x7FFFFF - 32;
+    return min(kh, kmax);
 }
 
 // The exact count around kh: v lies within one threshold of kh either way.
@@ -137,7 +131,7 @@ __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v)
 
 // R > 0: rows of L <= 32 R held in registers.  R == 0: any L, three passes over
 // the row (the later two from cache).
-template <int R, bool WIDE>
+template <int R>
 __global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(const __grid_constant__ LisArgs a)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -170,7 +164,7 @@ __global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(const _
             int kc[R], khs[R];
             bool nr[R];
 #pragma unroll
-            for (int j = 0; j < R; ++j) kc[j] = lis_code_fast<WIDE>(sf, ef[j], a.kmax, khs[j], nr[j]);
+            for (int j = 0; j < R; ++j) kc[j] = lis_code_fast(sf, ef[j], a.kmax, khs[j], nr[j]);
 #pragma unroll
             for (int j = 0; j < R; ++j) {
                 // the exact comparisons only where an estimate fell near a half-way point
@@ -191,7 +185,7 @@ __global__ void __launch_bounds__(kLisWarps * 32) log_int_softmax_kernel(const _
                 const uint64_t e = lis_exp(__ldg(xr + i), mx, a, ef);
                 int kh;
                 bool nr;
-                int k = lis_code_fast<WIDE>(sf, ef, a.kmax, kh, nr);
+                int k = lis_code_fast(sf, ef, a.kmax, kh, nr);
                 if (nr) k = lis_code_exact(s, e, kh, a.kmax);
                 __stcs(cr + i, (uint8_t)k);
             }
@@ -351,7 +345,6 @@ __device__ __forceinline__ void shift_load_values(const ShiftMmaArgs &a, int tid
 // Log-Int-Softmax of the CTA's rows straight into the shared code tile (row r
 // at r * Lk): warp w takes rows w, w + 8, ...; a row of L <= 256 values is held
 // in registers, up to 8 per lane.
-template <bool WIDE>
 __device__ __forceinline__ void lis_rows_to_tile(const ShiftMmaArgs &a, int64_t row0, int rows_here, uint8_t *tile,
                                                  int warp, int lane)
 {
@@ -386,7 +379,7 @@ __device__ __forceinline__ void lis_rows_to_tile(const ShiftMmaArgs &a, int64_t 
             if (32 * j >= L) break;  // warp-uniform
             int kh;
             bool nr;
-            int k = lis_code_fast<WIDE>(sf, ef[j], la.kmax, kh, nr);
+            int k = lis_code_fast(sf, ef[j], la.kmax, kh, nr);
             if (__any_sync(kFull, nr) && nr) k = lis_code_exact(s, ev[j], kh, la.kmax);
             const int i = lane + 32 * j;
             if (i < L) tr[i] = (uint8_t)k;
@@ -458,8 +451,7 @@ __global__ void __launch_bounds__(256, 4) attn_shift_mma_kernel(const __grid_con
         __syncthreads();
         ok = *reinterpret_cast<volatile uint32_t *>(ok_flag) != 0u;
         if constexpr (FUSED) {
-            if (a.lis.kmax == 32) lis_rows_to_tile<true>(a, b * a.Lq + i0, rows_here, tile, warp, lane);
-            else lis_rows_to_tile<false>(a, b * a.Lq + i0, rows_here, tile, warp, lane);
+            lis_rows_to_tile(a, b * a.Lq + i0, rows_here, tile, warp, lane);
         } else {
             for (uint64_t x = max(e1, tile_start) + tid; x < tile_end; x += 256) tile[x - s0] = a.code[x];
         }
@@ -743,10 +735,9 @@ extern "C" qnn_status q_log_int_softmax(const int32_t *x, int64_t rows, int64_t 
     // slightly faster than one wave of the resident blocks)
     const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * 8);
     auto launch = [&](auto kern) { kern<<<grid, kLisWarps * 32, 0, s>>>(a); };
-#define QNN_LIS(RR)                                                     \
-    case RR:                                                            \
-        if (bits == 5) launch(log_int_softmax_kernel<RR, true>);        \
-        else launch(log_int_softmax_kernel<RR, false>);                 \
+#define QNN_LIS(RR)                              \
+    case RR:                                     \
+        launch(log_int_softmax_kernel<RR>);      \
         break;
     switch (R) {
         QNN_LIS(1)

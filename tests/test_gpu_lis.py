@@ -193,3 +193,18 @@ def test_lis_attn_fused_errors():
         qnn.q_lis_attn_v(x, 2e-4, v, 1, 4, 300, 16, 4, o)
     with pytest.raises(qnn.QnnError):  # bits 5 has no shift product
         qnn.q_lis_attn_v(x, 2e-4, v, 1, 4, 200, 16, 5, o)
+
+
+@pytest.mark.parametrize("bits", [4, 5])
+def test_lis_ties_at_large_thresholds(oracle, bits):
+    """Rows whose largest element has v = s / e exactly half-way below a log_round
+    step L_j = 3 * 2^(j-2) (one element at 0 and n at -45 with S = 2^-6: v = 1 +
+    n / 2^q for q halvings), so the half-to-even rounding decides the code at
+    large thresholds as well as small ones."""
+    S = 2.0 ** -6
+    for q, L in ((1, 48), (1, 384), (1, 1536), (10, 3), (10, 12), (3, 24)):
+        n = int((L - 1.5) * 2 ** q)
+        x = np.array([[0] + [-45 * q] * n], np.int32)
+        got = _lis_gpu(x, S, bits)
+        want = oracle.log_int_softmax(x, S, bits)
+        assert np.array_equal(got, want), (q, L, got[0, :3], want[0, :3])
