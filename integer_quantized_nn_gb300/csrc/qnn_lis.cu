@@ -13,23 +13,23 @@
 // q_log_int_softmax: one warp per row.  Per element the exponential is
 //   e = z * 2^(30 - q), q = floor(d / x0_int), r = d - x0_int q,
 //   z = r (r + b_int) + c_int, d = max(x - max(x), 30 x0_int)
-// in exact integers (q from an fp32 quotient estimate with a remainder
-// correction).  The row sum s is a u64 warp reduction.  The code is not formed
-// from v = round(s / e) per element: for each threshold of log_round (v >= 2,
-// 3, 6, 12, ..., 3 * 2^(j-2)) the warp first computes, once per row, the largest
-// e whose rounded ratio still reaches it -- E_j, one exact u64 division per lane
-// by a multiply-high with a precomputed reciprocal (Granlund and Montgomery,
-// "Division by invariant integers using multiplication", 1994, section 4) --
-// so that an element's code is the number of E_j >= e.  An fp32 estimate of
-// s / e gives that count to within one; two exact u64 comparisons against the
-// table settle it.  That equals log_round(round(s/e)) exactly, half-to-even ties
-// included.
+// in exact integers (q by a multiply-high with a host-computed reciprocal).  The
+// row sum s is a u64 warp reduction.  The code is not formed from v = round(s /
+// e) per element: round(v) reaches a step L_j of log_round (2, 3, 6, 12, ...,
+// 3 * 2^(j-2)) exactly when v + 1/2 > L_j, so an fp32 estimate of v + 1/2 gives
+// the count of steps from its exponent and first mantissa bit; where that
+// estimate lies within fp32 error of a step, exact 128-bit comparisons of 2s
+// with (2L - 1) e decide.  That equals log_round(round(s/e)) exactly, half-to-
+// even ties included.
 //
 // q_attn_shift_v: out[b][i][j] = sum_t 2^(2^bits - 1 - k[b][i][t]) v[b][t][j]
 // over unmasked codes, exact in int32 (the host rejects shapes that could
 // overflow).  For d <= 128 and Lk <= 512 it runs on the tensor pipe (below);
 // otherwise on the CUDA cores: a 64 x 64 output tile per block, 4 x 4 per
 // thread, the weights 2^(N - k) expanded into shared memory per 64 tokens.
+//
+// q_lis_attn_v: the tensor-pipe kernel with its shared code tile filled by
+// Log-Int-Softmax of the CTA's logit rows instead of a copy of stored codes.
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <atomic>
