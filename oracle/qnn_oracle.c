@@ -564,12 +564,14 @@ int oracle_attn_shift_v(const uint8_t *code, const int32_t *v, int64_t heads, in
  * are exact (int64) -- the page computes them as float tensors; the float steps
  * are single fp32 operations in the printed order (division, multiplication,
  * IEEE sqrt); floor(log2 a) is the exact binary exponent of a (N = 31 for
- * a == 0 or subnormal a); both round() are half to even, on the exact value; a
+ * a == 0 or subnormal a; N = 0 for a = +inf, whose log2 is infinite, which
+ * finite gamma reaches when (s / std) gamma overflows); both round() are half
+ * to even, on the exact value; a
  * row whose variance numerator is 0 (all x' equal; the page divides by zero)
  * gives M = N = 0 and B = round(beta[c] / o[c]).  y is not clipped here: the
  * consumer's quantizer clips it.  B is rounded after clamping to +-2^62.
- * Returns OR_ERR_ARG for C <= 0, s or an o[c] not finite and positive, or
- * alpha > 30. */
+ * Returns OR_ERR_ARG for C <= 0, s or an o[c] not finite and positive, a
+ * gamma[c] or beta[c] not finite, or alpha > 30. */
 static int64_t round_shift_half_even(int64_t num, int N)
 {
     if (N == 0) return num;
@@ -595,6 +597,7 @@ int oracle_int_layernorm(const int32_t *x, int64_t rows, int64_t C, const uint8_
     if (C <= 0 || rows < 0 || !(s > 0.0f) || !isfinite(s)) return OR_ERR_ARG;
     for (int64_t c = 0; c < C; ++c) {
         if (!(o[c] > 0.0f) || !isfinite(o[c])) return OR_ERR_ARG;
+        if (!isfinite(gamma[c]) || !isfinite(beta[c])) return OR_ERR_ARG;
         if (alpha && alpha[c] > 30) return OR_ERR_ARG;
     }
 #pragma omp parallel for schedule(static)
@@ -622,7 +625,9 @@ int oracle_int_layernorm(const int32_t *x, int64_t rows, int64_t C, const uint8_
                 const float A = (s_over_std * gamma[c]) / o[c];
                 sign = (A > 0.0f) - (A < 0.0f);
                 const float a = fabsf(A);
-                if (a == 0.0f || !isnormal(a)) {
+                if (isinf(a)) {
+                    N = 0;
+                } else if (a == 0.0f || !isnormal(a)) {
                     N = 31;
                 } else {
                     const int e = ilogbf(a);

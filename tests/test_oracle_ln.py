@@ -98,3 +98,21 @@ def test_int_layernorm_errors(oracle):
             oracle.int_layernorm(x, kw["s"], 1.0, 0.0, kw["o"])
     with pytest.raises(ValueError):
         oracle.int_layernorm(x, 1.0, 1.0, 0.0, 1.0, alpha=np.array([0, 0, 31, 0], np.uint8))
+    for g, b in ((float("inf"), 0.0), (float("nan"), 0.0), (1.0, float("-inf"))):
+        with pytest.raises(ValueError):
+            oracle.int_layernorm(x, 1.0, g, b, 1.0)
+
+
+def test_int_layernorm_overflowing_scale(oracle):
+    """A finite gamma whose A = (s / std) gamma / o overflows to +-inf: log2 |A|
+    is infinite, so N = clamp(7 - inf) = 0 and M = clamp(inf) = 255; with
+    mean 0 and beta 0, B = 0 and y = sign(A) 255 x' exactly.  The other
+    channel keeps its ordinary constants (y = x for gamma = o)."""
+    x = np.array([[1, -1, 1, -1], [3, -3, -3, 3]], np.int32)
+    gamma = np.array([3e38, -3e38, 0.5, 0.5], np.float32)
+    o = np.array([1e-3, 1e-3, 0.5, 0.5], np.float32)
+    y = oracle.int_layernorm(x, 1.0, gamma, 0.0, o)
+    sgn = np.array([1, -1, 1, 1])
+    unit = np.sign(x)
+    assert np.array_equal(y[:, :2], 255 * sgn[:2] * x[:, :2])
+    assert np.array_equal(y[:, 2:], unit[:, 2:])
