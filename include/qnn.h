@@ -357,13 +357,14 @@ qnn_status q_lis_attn_v(const int32_t *x, float S, const int8_t *v, int64_t batc
  *   mean = fp32(sum x' / C) * s,  std = (s / C) * sqrt(fp32(C sum x'^2 - (sum x')^2))
  * (exact integer sums) and per channel c, in fp32 operations in this order,
  *   A = ((s / std) * gamma[c]) / o[c],  N = clamp(7 - floor(log2 |A|), 0, 31)
- *   (N = 31 for A zero or subnormal),  M = clamp(floor(|A| 2^N), 0, 255),
+ *   (N = 31 for A zero or subnormal, 0 for A infinite),  M = clamp(floor(|A| 2^N), 0, 255),
  *   B = round(((beta[c] - (mean / std) * gamma[c]) / o[c]) * 2^N)  (clamped to
  *   +-2^62 first),  y = round((sign(A) M x' + B) / 2^N)   (exact; half to even)
  * where o = out_scale [C].  A row whose variance numerator is 0 gives
  * y = round(beta[c] / o[c]).  y: QNN_S8 [rows][C] (clipped to -128..127, the
  * next layer's int8 input) or QNN_S32 (clipped to the int32 range).  gamma,
- * beta, out_scale: fp32 [C], out_scale > 0.  C % 4 == 0 (QNN_ERR_ALIGNMENT);
+ * beta, out_scale: fp32 [C], gamma and beta finite, out_scale finite and > 0 (the
+ * device values are not checked; others give unspecified codes).  C % 4 == 0 (QNN_ERR_ALIGNMENT);
  * QNN_ERR_OVERFLOW_RISK when C (128 2^alpha_max)^2 >= 2^32. */
 qnn_status q_int_layernorm(const int8_t *x, int64_t rows, int C, const uint8_t *alpha, int alpha_max, float s,
                            const float *gamma, const float *beta, const float *out_scale, qnn_dtype y_dt,

@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(kLnWarps * 32) int_layernorm_kernel(const __gr
         const float stdv = __fmul_rn(__fdiv_rn(a.s, Cf), __fsqrt_rn(__ll2float_rn(var_num)));
         const float sos = __fdiv_rn(a.s, stdv);
         const float mos = __fdiv_rn(mean, stdv);
+#pragma unroll 2
         for (int k = lane; k < words; k += 32) {
             const uint32_t xw = __ldg(xr + k);
             const uint32_t aw = a.alpha ? __ldg(reinterpret_cast<const uint32_t *>(a.alpha) + k) : 0u;
@@ -85,53 +86,57 @@ __global__ void __launch_bounds__(kLnWarps * 32) int_layernorm_kernel(const __gr
             const float4 o4 = __ldg(reinterpret_cast<const float4 *>(a.o) + k);
             const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, bs[4] = {b4.x, b4.y, b4.z, b4.w},
                         os[4] = {o4.x, o4.y, o4.z, o4.w};
-            int64_t yv[4];
+            // the four channels' constants first, straight-line, then one test for the
+            // 32-bit form of the rounding shift (|M x'| < 2^18, |B| < 2^30, N <= 30)
+            int32_t v[4], M[4], N[4];  // M signed: sign(A) M
+            float bt[4];               // B before rounding
+            bool fits = true;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int32_t v = (int32_t)(int8_t)(xw >> (8 * q)) * (1 << ((aw >> (8 * q)) & 0xffu));
-                int32_t M = 0;  // signed: sign(A) M
-                int N = 0;
-                float bt;       // B before rounding
+                v[q] = (int32_t)(int8_t)(xw >> (8 * q)) * (1 << ((aw >> (8 * q)) & 0xffu));
                 if (var_num == 0) {
-                    bt = __fdiv_rn(bs[q], os[q]);
+                    M[q] = 0;
+                    N[q] = 0;
+                    bt[q] = __fdiv_rn(bs[q], os[q]);
                 } else {
                     const float A = __fdiv_rn(__fmul_rn(sos, gs[q]), os[q]);
                     const float am = fabsf(A);
-                    const int ex = (__float_as_int(am) >> 23) & 0xff;  // 0: zero or subnormal
-                    N = ex == 0 ? 31 : min(max(134 - ex, 0), 31);  // 7 - (ex - 127)
-                    M = min(__float2int_rd(fminf(__fmul_rn(am, pow2f(N)), 256.0f)), 255);
-                    if (A < 0.0f) M = -M;
+                    // 7 - floor(log2 am) from the biased exponent: 0 (zero or subnormal)
+                    // clamps to 31, 255 (infinite) to 0
+                    const int ex = (__float_as_int(am) >> 23) & 0xff;
+                    N[q] = min(max(134 - ex, 0), 31);
+                    const int32_t m = min(__float2int_rd(fminf(__fmul_rn(am, pow2f(N[q])), 256.0f)), 255);
+                    M[q] = A < 0.0f ? -m : m;
                     const float t = __fdiv_rn(__fsub_rn(bs[q], __fmul_rn(mos, gs[q])), os[q]);
-                    bt = __fmul_rn(t, pow2f(N));
+                    bt[q] = __fmul_rn(t, pow2f(N[q]));
                 }
-                // |M x'| < 2^18: with |B| < 2^30 and N <= 30 everything fits 32 bits
-                if (fabsf(bt) < 1073741824.0f && N <= 30) {
-                    const int32_t num = M * v + __float2int_rn(bt);
-                    int32_t y32 = num;
-                    if (N > 0) {
-                        const int32_t qf = num >> N, rem = num & ((1 << N) - 1), half = 1 << (N - 1);
-                        y32 = (rem > half || (rem == half && (qf & 1))) ? qf + 1 : qf;
-                    }
-                    yv[q] = y32;
-                } else {
+                fits = fits && fabsf(bt[q]) < 1073741824.0f && N[q] <= 30;
+            }
+            int32_t yv[4];
+            if (fits) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    // half-even division by 2^N: floor((num + 2^(N-1) - 1 + (quotient & 1)) / 2^N)
+                    const int32_t num = M[q] * v[q] + __float2int_rn(bt[q]);
+                    const int32_t bias = ((1 << N[q]) >> 1) - 1 + ((num >> N[q]) & 1);
+                    yv[q] = N[q] == 0 ? num : (num + bias) >> N[q];
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
                     const float lim = 4611686018427387904.0f;  // 2^62: B is rounded after this clamp
-                    const int64_t B = __float2ll_rn(fminf(fmaxf(bt, -lim), lim));
-                    yv[q] = round_shift_he((int64_t)M * v + B, N);
+                    const int64_t B = __float2ll_rn(fminf(fmaxf(bt[q], -lim), lim));
+                    const int64_t y64 = round_shift_he((int64_t)M[q] * v[q] + B, N[q]);
+                    yv[q] = (int32_t)min(max(y64, (int64_t)INT32_MIN), (int64_t)INT32_MAX);
                 }
             }
             if constexpr (S8) {
                 uint32_t ow = 0;
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    ow |= ((uint32_t)(uint8_t)(int8_t)min(max(yv[q], (int64_t)-128), (int64_t)127)) << (8 * q);
+                for (int q = 0; q < 4; ++q) ow |= ((uint32_t)(uint8_t)(int8_t)min(max(yv[q], -128), 127)) << (8 * q);
                 reinterpret_cast<uint32_t *>(a.y)[row * words + k] = ow;
             } else {
-                int4 ov;
-                ov.x = (int32_t)min(max(yv[0], (int64_t)INT32_MIN), (int64_t)INT32_MAX);
-                ov.y = (int32_t)min(max(yv[1], (int64_t)INT32_MIN), (int64_t)INT32_MAX);
-                ov.z = (int32_t)min(max(yv[2], (int64_t)INT32_MIN), (int64_t)INT32_MAX);
-                ov.w = (int32_t)min(max(yv[3], (int64_t)INT32_MIN), (int64_t)INT32_MAX);
-                reinterpret_cast<int4 *>(a.y)[row * words + k] = ov;
+                reinterpret_cast<int4 *>(a.y)[row * words + k] = make_int4(yv[0], yv[1], yv[2], yv[3]);
             }
         }
     }

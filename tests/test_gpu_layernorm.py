@@ -107,6 +107,28 @@ def test_int_layernorm_errors():
         qnn.q_int_layernorm(x, 4, 8, 0.1, f[1:], f, f, y)  # misaligned gamma
 
 
+def test_int_layernorm_overflowing_and_huge_constants(oracle):
+    """gamma near the fp32 maximum over a tiny o (A overflows to +-inf: N = 0,
+    M = 255), and gammas / betas large enough that B leaves the 32-bit range or
+    reaches the 2^62 clamp: the 64-bit form of the rounding shift."""
+    rng = np.random.default_rng(5)
+    C, rows = 64, 9
+    x = np.clip(np.rint(rng.normal(0, 30, size=(rows, C))), -128, 127).astype(np.int32)
+    x[0] = 7  # a zero-variance row next to the others
+    gamma = rng.uniform(0.5, 2.0, size=C).astype(np.float32)
+    gamma[0::8] = 3e38
+    gamma[1::8] = -3e38
+    gamma[2::8] = 1e20
+    beta = rng.normal(0, 1, size=C).astype(np.float32)
+    beta[3::8] = 1e25
+    beta[4::8] = -3e9
+    o = np.full(C, 1e-3, np.float32)
+    for y_dt in ("s8", "s32"):
+        got = _ln_gpu(x, 0.05, gamma, beta, o, y_dt=y_dt)
+        want = _want(oracle, x, 0.05, gamma, beta, o, None, y_dt)
+        assert np.array_equal(got, want), f"{(got != want).sum()} mismatches"
+
+
 def test_int_layernorm_scales_across_binades(oracle):
     """Output scales and gammas spread over many binades (each o[c] = 2^U(-20, 10)
     times a random mantissa): every division by o[c] must round exactly as the
