@@ -94,16 +94,35 @@ __global__ void __launch_bounds__(256) quantize_rows_dynamic_kernel(const float 
         amax = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
         const float s = __fdiv_rn(amax, 127.0f);
         if (lane == 0) scale[row] = s;
+        // The code is rint(RN(x / s)).  With s a normal number well inside the range,
+        // q0 = RN(x RN(1 / s)) carries two roundings of relative size 2^-24, so
+        // |q0 - RN(x / s)| < 1.6 2^-23 |q0| (plus a subnormal ulp, only where |q0| is
+        // far below 1/2).  When q0 lies more than 2^-20 |q0| away from every
+        // half-integer, RN(x / s) lies strictly inside the same unit interval around
+        // rint(q0), so both round to the same integer; the rare elements nearer a
+        // half-integer, and whole rows with an extreme scale, take the IEEE division.
+        const bool recip = s >= 0x1p-100f && s <= 0x1p100f;
+        const float y = recip ? __frcp_rn(s) : 0.0f;
         uint32_t *qr = reinterpret_cast<uint32_t *>(q + row * cols);
         for (int64_t k = lane; k < words; k += 32) {
             const float4 v = __ldcs(xr + k);
             const float vs[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o = 0;
+            int32_t c[4];
+            bool near = !recip;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int32_t c = s == 0.0f ? 0 : min(max(__float2int_rn(__fdiv_rn(vs[j], s)), qmin), 127);
-                o |= (uint32_t)(uint8_t)c << (8 * j);
+                const float q0 = __fmul_rn(vs[j], y);
+                const float d = fabsf(__fsub_rn(q0, rintf(q0)));  // exact: |q0| < 2^23
+                near = near || __fsub_rn(0.5f, d) <= 0x1p-20f * fabsf(q0);
+                c[j] = __float2int_rn(q0);
             }
+            if (near) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) c[j] = s == 0.0f ? 0 : __float2int_rn(__fdiv_rn(vs[j], s));
+            }
+            uint32_t o = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o |= (uint32_t)(uint8_t)min(max(c[j], qmin), 127) << (8 * j);
             __stcs(qr + k, o);
         }
     }

@@ -63,6 +63,30 @@ def test_quantize_rows_dynamic(oracle, shape):
         assert np.array_equal(q, wq), f"{(q != wq).sum()} mismatches"
 
 
+def test_quantize_rows_dynamic_near_half_quotients(oracle):
+    """Elements whose quotient x / s lies within a few units in the last place
+    of a half-integer k + 1/2 (and exactly on it): rint(RN(x / s)) must follow
+    the IEEE quotient, ties to even, in every row scale's binade."""
+    rng = np.random.default_rng(11)
+    rows, cols = 64, 256
+    amax = (2.0 ** rng.uniform(-90, 90, size=rows) * rng.uniform(1.0, 2.0, size=rows)).astype(np.float32)
+    amax[:4] = [127.0, 1.0, 3.0, 254.0]
+    s = (amax / np.float32(127.0)).astype(np.float32)
+    k = rng.integers(-127, 127, size=(rows, cols)).astype(np.float32) + np.float32(0.5)
+    x = (k * s[:, None]).astype(np.float32)
+    steps = rng.integers(-3, 4, size=(rows, cols))
+    for d in range(1, 4):  # nudge by up to three units in the last place either way
+        x = np.where(steps >= d, np.nextafter(x, np.float32(np.inf)), x)
+        x = np.where(steps <= -d, np.nextafter(x, np.float32(-np.inf)), x)
+    x = np.clip(x, -amax[:, None], amax[:, None]).astype(np.float32)
+    x[:, 0] = amax  # the row maximum fixes s
+    for narrow in (False, True):
+        q, sg = _dyn_gpu(x, narrow)
+        wq, ws = oracle.quantize_rows_dynamic(x, narrow)
+        assert np.array_equal(f32_bits(sg), f32_bits(ws))
+        assert np.array_equal(q, wq), f"{(q != wq).sum()} mismatches"
+
+
 def test_eltwise_errors():
     t = __import__("torch")
     a = t.zeros(32, dtype=t.int8, device="cuda")
