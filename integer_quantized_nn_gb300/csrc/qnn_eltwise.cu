@@ -75,6 +75,60 @@ __global__ void __launch_bounds__(256) eltwise_s8_kernel(const int8_t *__restric
     }
 }
 
+// The row's scale s = max|x| / 127 and its reciprocal route.  The code is
+// rint(RN(x / s)).  With s a normal number well inside the range, q0 =
+// RN(x RN(1 / s)) carries two roundings of relative size 2^-24, so
+// |q0 - RN(x / s)| < 1.6 2^-23 |q0| (plus a subnormal ulp, only where |q0| is far
+// below 1/2).  When q0 lies more than 2^-20 |q0| away from every half-integer,
+// RN(x / s) lies strictly inside the same unit interval around rint(q0), so both
+// round to the same integer; the rare elements nearer a half-integer, and whole
+// rows with an extreme scale, take the IEEE division.
+struct DynScale {
+    float s, y;
+    bool recip;
+};
+
+__device__ __forceinline__ DynScale dyn_scale(float amax)
+{
+    DynScale d;
+    d.s = __fdiv_rn(amax, 127.0f);
+    d.recip = d.s >= 0x1p-100f && d.s <= 0x1p100f;
+    d.y = d.recip ? __frcp_rn(d.s) : 0.0f;
+    return d;
+}
+
+__device__ __forceinline__ float abs_max4(float m, const float4 &v)
+{
+    return fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+}
+
+// four codes of one 16-byte group, packed little-endian
+__device__ __forceinline__ uint32_t dyn_quant4(const float4 &v, const DynScale &d, int32_t qmin)
+{
+    const float vs[4] = {v.x, v.y, v.z, v.w};
+    int32_t c[4];
+    bool near = !d.recip;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float q0 = __fmul_rn(vs[j], d.y);
+        const float dist = fabsf(__fsub_rn(q0, rintf(q0)));  // exact: |q0| < 2^23
+        near = near || __fsub_rn(0.5f, dist) <= 0x1p-20f * fabsf(q0);
+        c[j] = __float2int_rn(q0);
+    }
+    if (near) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c[j] = d.s == 0.0f ? 0 : __float2int_rn(__fdiv_rn(vs[j], d.s));
+    }
+    uint32_t o = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o |= (uint32_t)(uint8_t)min(max(c[j], qmin), 127) << (8 * j);
+    return o;
+}
+
+// One warp per row.  R > 0: the row (at most 32 R groups of 4 values) is read
+// once into registers, all its loads in flight together; R = 0: any length, the
+// row read twice (the second time from cache).
+template <int R>
 __global__ void __launch_bounds__(256) quantize_rows_dynamic_kernel(const float *__restrict__ x, int64_t rows,
                                                                     int64_t cols, int narrow, int8_t *__restrict__ q,
                                                                     float *__restrict__ scale)
@@ -85,45 +139,31 @@ __global__ void __launch_bounds__(256) quantize_rows_dynamic_kernel(const float 
     for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < rows;
          row += ((int64_t)gridDim.x * blockDim.x) >> 5) {
         const float4 *xr = reinterpret_cast<const float4 *>(x + row * cols);
-        float amax = 0.0f;
-        for (int64_t k = lane; k < words; k += 32) {
-            const float4 v = __ldg(xr + k);
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-        }
-        // magnitudes are non-negative: their bit patterns order like the values
-        amax = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
-        const float s = __fdiv_rn(amax, 127.0f);
-        if (lane == 0) scale[row] = s;
-        // The code is rint(RN(x / s)).  With s a normal number well inside the range,
-        // q0 = RN(x RN(1 / s)) carries two roundings of relative size 2^-24, so
-        // |q0 - RN(x / s)| < 1.6 2^-23 |q0| (plus a subnormal ulp, only where |q0| is
-        // far below 1/2).  When q0 lies more than 2^-20 |q0| away from every
-        // half-integer, RN(x / s) lies strictly inside the same unit interval around
-        // rint(q0), so both round to the same integer; the rare elements nearer a
-        // half-integer, and whole rows with an extreme scale, take the IEEE division.
-        const bool recip = s >= 0x1p-100f && s <= 0x1p100f;
-        const float y = recip ? __frcp_rn(s) : 0.0f;
         uint32_t *qr = reinterpret_cast<uint32_t *>(q + row * cols);
-        for (int64_t k = lane; k < words; k += 32) {
-            const float4 v = __ldcs(xr + k);
-            const float vs[4] = {v.x, v.y, v.z, v.w};
-            int32_t c[4];
-            bool near = !recip;
+        float amax = 0.0f;
+        if constexpr (R > 0) {
+            float4 v[R];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float q0 = __fmul_rn(vs[j], y);
-                const float d = fabsf(__fsub_rn(q0, rintf(q0)));  // exact: |q0| < 2^23
-                near = near || __fsub_rn(0.5f, d) <= 0x1p-20f * fabsf(q0);
-                c[j] = __float2int_rn(q0);
+            for (int u = 0; u < R; ++u) {
+                const int k = lane + 32 * u;
+                v[u] = k < words ? __ldcs(xr + k) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                amax = abs_max4(amax, v[u]);
             }
-            if (near) {
+            // magnitudes are non-negative: their bit patterns order like the values
+            amax = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
+            const DynScale d = dyn_scale(amax);
+            if (lane == 0) scale[row] = d.s;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) c[j] = s == 0.0f ? 0 : __float2int_rn(__fdiv_rn(vs[j], s));
+            for (int u = 0; u < R; ++u) {
+                const int k = lane + 32 * u;
+                if (k < words) __stcs(qr + k, dyn_quant4(v[u], d, qmin));
             }
-            uint32_t o = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) o |= (uint32_t)(uint8_t)min(max(c[j], qmin), 127) << (8 * j);
-            __stcs(qr + k, o);
+        } else {
+            for (int64_t k = lane; k < words; k += 32) amax = abs_max4(amax, __ldg(xr + k));
+            amax = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
+            const DynScale d = dyn_scale(amax);
+            if (lane == 0) scale[row] = d.s;
+            for (int64_t k = lane; k < words; k += 32) __stcs(qr + k, dyn_quant4(__ldcs(xr + k), d, qmin));
         }
     }
 }
@@ -198,13 +238,22 @@ extern "C" qnn_status q_quantize_rows_dynamic(const float *x, int64_t rows, int6
     if (rows == 0) return QNN_OK;
     if (!x || !q || !scale) return QNN_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return QNN_ERR_ALIGNMENT;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_rows_dynamic_kernel, 256, 0) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
-    // one wave of resident blocks, 8 rows (warps) per block
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * per_sm));
-    quantize_rows_dynamic_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(x, rows, cols, narrow, q, scale);
+    // the smallest register-resident row that holds cols / 4 groups, else two passes
+    const int64_t words = cols / 4;
+    auto launch = [&](auto kern) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)
+            per_sm = 1;
+        // one wave of resident blocks, 8 rows (warps) per block
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * per_sm));
+        kern<<<grid, 256, 0, (cudaStream_t)stream>>>(x, rows, cols, narrow, q, scale);
+    };
+    if (words <= 32) launch(quantize_rows_dynamic_kernel<1>);
+    else if (words <= 64) launch(quantize_rows_dynamic_kernel<2>);
+    else if (words <= 128) launch(quantize_rows_dynamic_kernel<4>);
+    else if (words <= 192) launch(quantize_rows_dynamic_kernel<6>);
+    else if (words <= 256) launch(quantize_rows_dynamic_kernel<8>);
+    else launch(quantize_rows_dynamic_kernel<0>);
     return launch_status();
 }
 

@@ -16,8 +16,10 @@
 // 4-byte words (4 codes per lane and step), shifts by alpha and reduces sum x'
 // and sum x'^2 with warp reductions; one lane's worth of fp32 work gives the row
 // constants; pass 2 re-reads the row (from cache) with the per-channel gamma,
-// beta, o and alpha (vector loads) and writes 4 outputs per step.  The op is
-// bound by its fp32 divisions (two per element) more than by its bytes.
+// beta, o and alpha (vector loads), forms the four channels' A, N, M and B
+// without branches, and takes the 32-bit rounding shift when all four fit (the
+// 64-bit one only for extreme constants); 4 outputs per step.  The op is bound
+// by instruction issue (two IEEE divisions per element among them), not bytes.
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>

@@ -48,7 +48,7 @@ def _dyn_gpu(x, narrow):
     return host(q).astype(np.int32), host(s)
 
 
-@pytest.mark.parametrize("shape", [(1, 4), (37, 768), (5, 1028), (64 * 197, 768)])
+@pytest.mark.parametrize("shape", [(1, 4), (3, 132), (9, 500), (37, 768), (4, 1024), (5, 1028), (64 * 197, 768)])
 def test_quantize_rows_dynamic(oracle, shape):
     rng = np.random.default_rng(shape[1])
     x = (rng.standard_normal(shape) * rng.uniform(0.01, 30.0, (shape[0], 1))).astype(np.float32)
