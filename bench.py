@@ -386,6 +386,69 @@ def run_gpu(args):
     dist.close()
 
 
+def _aligned_1024(torch, nbytes, device):
+    buf = torch.empty(nbytes + 1024, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 1024
+    return buf[off:off + nbytes]
+
+
+def setup_conv_u8zw(torch, qnn, workloads, device, stream):
+    """ResNet-50 stage-1 3x3 Conv_Add_Relu, u8 activations x u8 filters with
+    per-filter zero points (qconv_prepack_w_u8 + qconv_u8u8).  Returns the call
+    and its op / byte counts."""
+    wc = workloads.conv_u8()
+    Nb, H, W, C, OC = 64, 56, 56, 64, 64
+    g = qnn.conv_geom(Nb, H, W, C, OC, 3, 3, (1, 1), (1, 1))
+    Wp = _aligned_1024(torch, qnn.qnn_conv_packed_w_bytes(g, "u8"), device)
+    cs = torch.empty(OC, dtype=torch.int32, device=device)
+    qnn.qconv_prepack_w_u8(torch.from_numpy(wc["W"]).to(device), torch.from_numpy(wc["z_w"]).to(device), g, Wp, cs)
+    zp = torch.empty(OC, dtype=torch.int32, device=device)
+    Mv = torch.empty(OC, dtype=torch.float32, device=device)
+    Bq = torch.empty(OC, dtype=torch.float32, device=device)
+    qnn.q_fold_epilogue(OC, "u8", wc["z_in"], cs, wc["s_a"], torch.from_numpy(wc["s_w"]).to(device), wc["s_o"],
+                        bias=torch.from_numpy(wc["bias"]).to(device), zp_term=zp, M=Mv, Bq=Bq, w_per_channel=True)
+    I8 = torch.from_numpy(wc["I"]).to(device)
+    res8 = torch.from_numpy(wc["res"]).to(device)
+    R = float(np.float32(np.float32(wc["s_r"]) / np.float32(wc["s_o"])))
+    epi = qnn.epilogue("requant", relu=True, out_dt="u8", zp_term=zp, M=Mv, Bq=Bq, residual=res8, res_dt="u8",
+                       z_res=wc["z_res"], R=R)
+    O8 = torch.empty((Nb, g.OH, g.OW, OC), dtype=torch.uint8, device=device)
+    keep = (Wp, cs, zp, Mv, Bq, I8, res8, O8, epi)
+
+    def fn():
+        qnn.qconv_u8u8(keep[5], wc["z_in"], keep[0], g, keep[8], keep[7], stream=stream)
+
+    return fn, {"ops": 2.0 * Nb * g.OH * g.OW * OC * C * 9,
+                "bytes": I8.numel() + O8.numel() + res8.numel() + OC * C * 9}
+
+
+def setup_gemm_zw(torch, qnn, workloads, device, stream):
+    """ViT-B fc1 with u8 weights carrying per-channel zero points
+    (qgemm_prepack_b_u8 + qgemm_zw with its workspace)."""
+    wz = workloads.vit_fc1_zw()
+    Mm, Kk = wz["A"].shape
+    Nn = wz["B"].shape[0]
+    Bp = _aligned_1024(torch, qnn.qnn_gemm_packed_b_bytes(Nn, Kk), device)
+    cs = torch.empty(Nn, dtype=torch.int32, device=device)
+    zwd = torch.from_numpy(wz["z_w"]).to(device)
+    qnn.qgemm_prepack_b_u8(torch.from_numpy(wz["B"]).to(device), zwd, Bp, cs)
+    zp = torch.empty(Nn, dtype=torch.int32, device=device)
+    Mv = torch.empty(Nn, dtype=torch.float32, device=device)
+    Bq = torch.empty(Nn, dtype=torch.float32, device=device)
+    qnn.q_fold_epilogue(Nn, "u8", wz["z_a"], cs, wz["s_a"], torch.from_numpy(wz["s_w"]).to(device), wz["s_o"],
+                        bias=torch.from_numpy(wz["bias"]).to(device), zp_term=zp, M=Mv, Bq=Bq, w_per_channel=True)
+    A = torch.from_numpy(wz["A"]).to(device)
+    C = torch.empty((Mm, Nn), dtype=torch.uint8, device=device)
+    epi = qnn.epilogue("requant", out_dt="s8", zp_term=zp, M=Mv, Bq=Bq)
+    ws = torch.empty(qnn.qnn_gemm_zw_workspace_bytes(Mm, Kk), dtype=torch.uint8, device=device)
+    keep = (Bp, cs, zp, Mv, Bq)
+
+    def fn():
+        qnn.qgemm_zw(A, "u8", keep[0], zwd, Mm, Nn, Kk, epi, C, workspace=ws, stream=stream)
+
+    return fn, {"ops": 2.0 * Mm * Nn * Kk, "M": Mm, "N": Nn, "K": Kk}
+
+
 def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
     out = {}
     hbm = float(pk["hbm_gbs"])
@@ -492,6 +555,25 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
     conv_entry("conv3x3_u4s4_add_relu", workloads.conv_u4(), (64, 56, 56, 64, 64, 3, 1, 1))
     conv_entry("conv1x1_u4s4_relu", workloads.conv_u4(C=256, OC=64, F=1, pad=0, residual=False, tag=1),
                (64, 56, 56, 256, 64, 1, 0, 1))
+
+    # weight zero points: ResNet-50 3x3 with u8 activations x u8 filters (zero point taken
+    # out at prepack), and ViT-B fc1 with u8 weights (the run-time row-sum term)
+    fn, info = setup_conv_u8zw(torch, qnn, workloads, device, stream)
+    t = time_steps(torch, fn, steps, 3, flush, stream)
+    ms = statistics.median(t)
+    tops = info["ops"] / (ms * 1e-3) / 1e12
+    out["conv3x3_u8u8_zw_add_relu"] = {"ms": round(ms, 4), "TOPS": round(tops, 2),
+                                       "frac_f16_peak": round(tops / peak, 4),
+                                       "GB/s": round(info["bytes"] / (ms * 1e-3) / 1e9, 1),
+                                       "frac_hbm": round(info["bytes"] / (ms * 1e-3) / 1e9 / hbm, 4)}
+    del fn, info
+    fn, info = setup_gemm_zw(torch, qnn, workloads, device, stream)
+    t = time_steps(torch, fn, steps, 3, flush, stream)
+    ms = statistics.median(t)
+    tops = info["ops"] / (ms * 1e-3) / 1e12
+    out["vit_fc1_zw"] = {"M": info["M"], "N": info["N"], "K": info["K"], "ms": round(ms, 4),
+                         "TOPS": round(tops, 2), "frac_f16_peak": round(tops / peak, 4)}
+    del fn, info
 
     # Log-Int-Softmax over ViT-B attention maps at batch 64, then the shift product with V
     Bh, Lt, dh = 64 * 12, 197, 64
@@ -639,6 +721,10 @@ def run_case(args):
         ws = None if getattr(args, "fused", False) else torch.empty(qnn.qnn_conv_workspace_bytes(gg, "u4"),
                                                                      dtype=torch.uint8, device=device)
         fn = lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, gg, epi, O, workspace=ws, stream=stream)  # noqa: E731
+    elif case == "conv_u8zw":
+        fn, _ = setup_conv_u8zw(torch, qnn, workloads, device, stream)
+    elif case == "gemm_zw":
+        fn, _ = setup_gemm_zw(torch, qnn, workloads, device, stream)
     elif case == "eltwise":
         R, C = 64 * 197, 768
         ea = workloads.device_uniform_s8((R, C), 91, device)
@@ -781,7 +867,8 @@ def main():
                     help="run one workload only (profiling): quantize, vit_fc1, square_4096, "
                          "vitl_fc2, conv3x3, conv1x1, gemm:M:N:K (u8 x s8 -> s8), lis, shift, "
                          "attn (ViT-B b64 Log-Int-Softmax, shift product, both), fused (both in one kernel), layernorm, "
-                         "eltwise, dynquant")
+                         "eltwise, dynquant, conv_u8zw (3x3 u8 x u8 filters with zero points), "
+                         "gemm_zw (ViT-B fc1 with u8 weights and zero points)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

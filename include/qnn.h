@@ -228,7 +228,8 @@ typedef struct {
 } qnn_conv_geom;
 
 /* Size in bytes of the prepacked conv weight operand for weights of w_dt
- * (S4 or S8); 0 for an invalid geometry or type. */
+ * (S4 or S8; U4 and U8, the filters with zero points, take the same size as
+ * S4 and S8); 0 for an invalid geometry or type. */
 size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g, qnn_dtype w_dt);
 
 /* Prepack conv weights of w_dt (S4: packed nibbles, OHWI; S8: bytes, OHWI) into
@@ -274,6 +275,26 @@ qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed, const q
 
 /* u8 activations x s8 weights, same contract (I: u8 NHWC; C % 16 == 0). */
 qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
+                      const qnn_epilogue *epi, void *O, int32_t *O_s32, qnn_stream_t stream);
+
+/* Prepack u8 filters (bytes, OHWI) with per-filter zero points z_w (device int32
+ * [OC], each in 0..255) for qconv_u8u8 [MG 背景: asymmetric codes carry a zero
+ * point; 緩解精度下降: with Z_w != 0 every term of the product appears].  As for
+ * u4 filters the weight zero point is taken out here, the filters being
+ * constants: the image holds w - z_w[oc] in [-255, 255] (exact in fp16) and
+ * colsum[oc] = sum (w - z_w[oc]), so the conv computes sum (q - z_in)(w - z_w)
+ * with no run-time term.  W 16-byte aligned, C % 16 == 0 (QNN_ERR_UNSUPPORTED
+ * otherwise); W_packed 1024-byte aligned, qnn_conv_packed_w_bytes(g, QNN_U8)
+ * bytes. */
+qnn_status qconv_prepack_w_u8(const void *W, const int32_t *z_w, const qnn_conv_geom *g, void *W_packed,
+                              int32_t *colsum, qnn_stream_t stream);
+
+/* u8 activations x u8 filters with zero points (prepacked by qconv_prepack_w_u8),
+ * the contract of qconv_u8s8.  The centred filter values reach 255 in magnitude,
+ * so the kernel's exact fp32 partial sums span 512 K values instead of 1024
+ * (longer filters are summed in more chunks, exactly); QNN_ERR_OVERFLOW_RISK
+ * when FH FW C 255^2 > 2^31 - 1. */
+qnn_status qconv_u8u8(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
                       const qnn_epilogue *epi, void *O, int32_t *O_s32, qnn_stream_t stream);
 
 /* ---- weight zero points (Z_w != 0) --------------------------------------------- */

@@ -644,10 +644,12 @@ qnn_status conv_tma_dispatch(const Params &p, int cb, cudaStream_t s)
     return conv_tma_launch<32, TBN, 1, false>(p, s);
 }
 
+// u4: qconv_u4s4; else the u8 conv, whose filter values reach 255 in magnitude
+// when wide_w (u8 filters less their zero points) and 128 otherwise (s8).
 template <template <int> class Op>
 qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
                     const qnn_epilogue *e, void *O, int32_t *O_s32, void *workspace, size_t workspace_bytes,
-                    qnn_stream_t stream, bool u4)
+                    qnn_stream_t stream, bool u4, bool wide_w = false)
 {
     if (!I || !W_packed || !e || !O) return QNN_ERR_INVALID_ARG;
     if (!geom_ok(g)) return QNN_ERR_INVALID_ARG;
@@ -686,10 +688,15 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
     qnn_status st = setup_epilogue(e, true, p);
     if (st != QNN_OK) return st;
     if (p.mode == QNN_EPI_REQUANT && p.out_bits == 4 && e->out_dt != QNN_U4) return QNN_ERR_UNSUPPORTED;
-    // exact fp32 chunk sums: u4 x s4 products are at most 120, centred u8 x s8 at most 2^14
+    // exact fp32 chunk sums: u4 x s4 products are at most 120, centred u8 x s8 at most
+    // 2^14, centred u8 x (u8 - z_w) below 2^15 (half as many steps per chunk)
     if (u4) {
         p.chunk_steps = KMAX_U4_EXACT / 128;
         if ((int64_t)p.K * 240 > (int64_t)INT32_MAX) return QNN_ERR_OVERFLOW_RISK;
+    } else if (wide_w) {
+        p.chunk_steps = gemm::MAX_EXACT_STEPS / 2;
+        // |(q - z_in)(w - z_w)| <= 255^2 per tap
+        if ((int64_t)p.K * 255 * 255 > (int64_t)INT32_MAX) return QNN_ERR_OVERFLOW_RISK;
     } else {
         p.chunk_steps = gemm::MAX_EXACT_STEPS;
         if ((int64_t)p.K * 255 * 128 > (int64_t)INT32_MAX) return QNN_ERR_OVERFLOW_RISK;
@@ -763,8 +770,9 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
 extern "C" size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g, qnn_dtype w_dt)
 {
     if (!qnn::mk::geom_ok(g)) return 0;
-    if (w_dt == QNN_S4) return qnn::mk::packed_w_u4_total(g);
-    if (w_dt == QNN_S8) return qnn::gemm::packed_b_bytes(g->OC, g->FH * g->FW * g->C);
+    // u4 / u8 filters with zero points (qconv_prepack_w_u4 / _u8) take the images of s4 / s8
+    if (w_dt == QNN_S4 || w_dt == QNN_U4) return qnn::mk::packed_w_u4_total(g);
+    if (w_dt == QNN_S8 || w_dt == QNN_U8) return qnn::gemm::packed_b_bytes(g->OC, g->FH * g->FW * g->C);
     return 0;
 }
 
@@ -788,6 +796,23 @@ extern "C" qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_c
     }
     if (w_dt != QNN_S4) return QNN_ERR_UNSUPPORTED;
     return qnn::mk::prepack_w4(W, nullptr, g, W_packed, colsum, stream);
+}
+
+namespace qnn {
+qnn_status prepack_b_u8_minus_zw(const uint8_t *B, const int32_t *z_w, int N, int K, void *B_packed,
+                                 int32_t *colsum, cudaStream_t s);
+}  // namespace qnn
+
+extern "C" qnn_status qconv_prepack_w_u8(const void *W, const int32_t *z_w, const qnn_conv_geom *g, void *W_packed,
+                                         int32_t *colsum, qnn_stream_t stream)
+{
+    if (!W || !W_packed || !z_w || !qnn::mk::geom_ok(g)) return QNN_ERR_INVALID_ARG;
+    if (g->C % 16 != 0) return QNN_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(W_packed) & 1023u) != 0) return QNN_ERR_ALIGNMENT;
+    if (!qnn::aligned16(W) || !qnn::aligned16(z_w)) return QNN_ERR_ALIGNMENT;
+    // filters [OC][FH][FW][C] are the GEMM operand B [OC, K]
+    return qnn::prepack_b_u8_minus_zw(static_cast<const uint8_t *>(W), z_w, g->OC, g->FH * g->FW * g->C, W_packed,
+                                      colsum, (cudaStream_t)stream);
 }
 
 extern "C" qnn_status qconv_prepack_w_u4(const void *W, const int32_t *z_w, const qnn_conv_geom *g, void *W_packed,
@@ -860,4 +885,12 @@ extern "C" qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_pack
                                  int32_t *O_s32, qnn_stream_t stream)
 {
     return qnn::mk::conv_run<qnn::mk::ConvU8Op>(I, z_in, W_packed, g, e, O, O_s32, nullptr, 0, stream, false);
+}
+
+extern "C" qnn_status qconv_u8u8(const void *I, int32_t z_in, const void *W_packed,
+                                 const qnn_conv_geom *g, const qnn_epilogue *e, void *O,
+                                 int32_t *O_s32, qnn_stream_t stream)
+{
+    return qnn::mk::conv_run<qnn::mk::ConvU8Op>(I, z_in, W_packed, g, e, O, O_s32, nullptr, 0, stream, false,
+                                                true);
 }

@@ -14,12 +14,25 @@
 namespace qnn {
 namespace {
 
-// One thread per 16-byte chunk of the packed image.
-// FLIP: B holds u8 codes, packed as their centred values w - 128 (the byte with
-// its top bit flipped, read as s8).
-template <bool FLIP>
+// One thread per 16-byte chunk of the packed image.  MODE says what B holds and
+// which value of each code goes into the image:
+//   kPackS8   : s8 codes, as they are;
+//   kPackU8   : u8 codes, centred: w - 128 (the byte with its top bit flipped, read as s8);
+//   kPackU8Zw : u8 codes less their row's zero point: w - z_w[n], in [-255, 255].
+// All are integers of at most 255 in magnitude, exact in fp16.
+constexpr int kPackS8 = 0, kPackU8 = 1, kPackU8Zw = 2;
+
+template <int MODE>
+__device__ __forceinline__ int packed_code(const int8_t *B, int64_t idx, const int32_t *z_w, int n)
+{
+    if constexpr (MODE == kPackS8) return B[idx];
+    else if constexpr (MODE == kPackU8) return (int8_t)(B[idx] ^ 0x80);
+    else return (int)(uint8_t)B[idx] - z_w[n];
+}
+
+template <int MODE>
 __global__ void prepack_b_kernel(const int8_t *__restrict__ B, int N, int K, uint8_t *__restrict__ out,
-                                 int64_t nchunks)
+                                 int64_t nchunks, const int32_t *__restrict__ z_w)
 {
     using namespace gemm;
     const int KT = ksteps(K);
@@ -38,10 +51,8 @@ __global__ void prepack_b_kernel(const int8_t *__restrict__ B, int N, int K, uin
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             int v0 = 0, v1 = 0;
-            if (n < N && k0 + 2 * j < K) v0 = FLIP ? (int8_t)(B[(int64_t)n * K + k0 + 2 * j] ^ 0x80)
-                                                   : B[(int64_t)n * K + k0 + 2 * j];
-            if (n < N && k0 + 2 * j + 1 < K) v1 = FLIP ? (int8_t)(B[(int64_t)n * K + k0 + 2 * j + 1] ^ 0x80)
-                                                       : B[(int64_t)n * K + k0 + 2 * j + 1];
+            if (n < N && k0 + 2 * j < K) v0 = packed_code<MODE>(B, (int64_t)n * K + k0 + 2 * j, z_w, n);
+            if (n < N && k0 + 2 * j + 1 < K) v1 = packed_code<MODE>(B, (int64_t)n * K + k0 + 2 * j + 1, z_w, n);
             const uint32_t h0 = __half_as_ushort(__int2half_rn(v0));
             const uint32_t h1 = __half_as_ushort(__int2half_rn(v1));
             w[j] = h0 | (h1 << 16);
@@ -112,8 +123,8 @@ extern "C" qnn_status qgemm_prepack_b(const int8_t *B, int N, int K, void *B_pac
     int64_t blocks = (nchunks + 255) / 256;
     if (blocks > 65535) blocks = 65535;
     cudaStream_t s = (cudaStream_t)stream;
-    qnn::prepack_b_kernel<false><<<(int)blocks, 256, 0, s>>>(B, N, K, static_cast<uint8_t *>(B_packed),
-                                                              nchunks);
+    qnn::prepack_b_kernel<qnn::kPackS8><<<(int)blocks, 256, 0, s>>>(B, N, K, static_cast<uint8_t *>(B_packed),
+                                                                     nchunks, nullptr);
     if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
     if (colsum) {
         const int64_t threads = (int64_t)N * 32;
@@ -134,8 +145,9 @@ extern "C" qnn_status qgemm_prepack_b_u8(const uint8_t *B, const int32_t *z_w, i
     int64_t blocks = (nchunks + 255) / 256;
     if (blocks > 65535) blocks = 65535;
     cudaStream_t s = (cudaStream_t)stream;
-    qnn::prepack_b_kernel<true><<<(int)blocks, 256, 0, s>>>(reinterpret_cast<const int8_t *>(B), N, K,
-                                                             static_cast<uint8_t *>(B_packed), nchunks);
+    qnn::prepack_b_kernel<qnn::kPackU8><<<(int)blocks, 256, 0, s>>>(reinterpret_cast<const int8_t *>(B), N, K,
+                                                                     static_cast<uint8_t *>(B_packed), nchunks,
+                                                                     nullptr);
     if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
     if (colsum) {
         const int64_t threads = (int64_t)N * 32;
@@ -144,6 +156,27 @@ extern "C" qnn_status qgemm_prepack_b_u8(const uint8_t *B, const int32_t *z_w, i
     }
     return QNN_OK;
 }
+
+namespace qnn {
+// The u8 conv filters [OC, K] with per-filter zero points: image of w - z_w[n]
+// and colsum[n] = sum_k (w - z_w[n]).  Arguments checked by the caller.
+qnn_status prepack_b_u8_minus_zw(const uint8_t *B, const int32_t *z_w, int N, int K, void *B_packed,
+                                 int32_t *colsum, cudaStream_t s)
+{
+    const int64_t nchunks = (int64_t)(gemm::packed_b_bytes(N, K) / 16);
+    int64_t blocks = (nchunks + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    prepack_b_kernel<kPackU8Zw><<<(int)blocks, 256, 0, s>>>(reinterpret_cast<const int8_t *>(B), N, K,
+                                                            static_cast<uint8_t *>(B_packed), nchunks, z_w);
+    if (launch_status() != QNN_OK) return QNN_ERR_CUDA;
+    if (colsum) {
+        const int64_t threads = (int64_t)N * 32;
+        colsum_u8_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(B, z_w, N, K, colsum);
+        return launch_status();
+    }
+    return QNN_OK;
+}
+}  // namespace qnn
 
 extern "C" qnn_status q_fold_epilogue(int N, qnn_dtype a_dt, int32_t z_a, const int32_t *colsum,
                                       float s_a, const float *s_w, int w_per_channel,

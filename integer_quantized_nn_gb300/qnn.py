@@ -83,6 +83,8 @@ def _declare(L):
         "qnn_conv_workspace_bytes": (sz, [vp, c_int]),
         "qconv_u4s4": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "qconv_u8s8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
+        "qconv_u8u8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
+        "qconv_prepack_w_u8": (c_int, [vp, vp, vp, vp, vp, vp]),
         "q_log_int_softmax": (c_int, [vp, i64, i64, f32, c_int, vp, vp]),
         "q_attn_shift_v": (c_int, [vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp]),
         "q_int_layernorm": (c_int, [vp, i64, c_int, vp, c_int, f32, vp, vp, vp, c_int, vp, vp]),
@@ -280,6 +282,13 @@ def qconv_prepack_w_u4(W, z_w, g: ConvGeom, W_packed, colsum=None, stream=None):
                                            _stream(stream)), "qconv_prepack_w_u4")
 
 
+def qconv_prepack_w_u8(W, z_w, g: ConvGeom, W_packed, colsum=None, stream=None):
+    """u8 filters (bytes, OHWI) with per-filter zero points z_w (int32 [OC]), for qconv_u8u8."""
+    load()
+    _check(_SYMBOLS["qconv_prepack_w_u8"](_ptr(W), _ptr(z_w), ctypes.byref(g), _ptr(W_packed), _ptr(colsum),
+                                           _stream(stream)), "qconv_prepack_w_u8")
+
+
 def qnn_conv_workspace_bytes(g: ConvGeom, in_dt: str = "u4") -> int:
     load()
     return int(_SYMBOLS["qnn_conv_workspace_bytes"](ctypes.byref(g), DTYPES[in_dt]))
@@ -302,6 +311,14 @@ def qconv_u8s8(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None
     _check(_SYMBOLS["qconv_u8s8"](_ptr(I), int(z_in), _ptr(W_packed), ctypes.byref(g),
                                   ctypes.byref(epi), _ptr(O), _ptr(O_s32), _stream(stream)),
            "qconv_u8s8")
+
+
+def qconv_u8u8(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None, stream=None):
+    """u8 activations x u8 filters prepacked by qconv_prepack_w_u8."""
+    load()
+    _check(_SYMBOLS["qconv_u8u8"](_ptr(I), int(z_in), _ptr(W_packed), ctypes.byref(g),
+                                  ctypes.byref(epi), _ptr(O), _ptr(O_s32), _stream(stream)),
+           "qconv_u8u8")
 
 
 def qgemm_prepack_b_u8(B, z_w, B_packed, colsum=None, stream=None):

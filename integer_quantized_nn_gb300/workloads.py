@@ -21,6 +21,9 @@ Workloads (the layer shapes of the pages' models stand in for their datasets):
                   int32 logit codes of Q K^T, s8 value codes, for Log-Int-Softmax
   vit_layernorm : ViT-B LayerNorm inputs (197 tokens x 768 channels), s8 codes with
                   per-channel power-of-two factors, for the integer LayerNorm
+  conv_u8       : ResNet-50 stage-1 3x3 Conv_Add_Relu with u8 activations and u8
+                  filters carrying per-filter zero points (both operands asymmetric)
+  vit_fc1_zw    : ViT-B MLP fc1 with u8 weights carrying per-channel zero points
 """
 from __future__ import annotations
 
@@ -28,7 +31,7 @@ import math
 import numpy as np
 
 # workload ids (seed = 1000 * id + tensor id)
-GEMM_SYM, VIT_FC1, CONV_U4, VITL_PTF, SQUARE, ATTN, LNORM = 1, 2, 3, 4, 5, 6, 7
+GEMM_SYM, VIT_FC1, CONV_U4, VITL_PTF, SQUARE, ATTN, LNORM, CONV_U8, VIT_FC1_ZW = 1, 2, 3, 4, 5, 6, 7, 8, 9
 
 
 def rng(workload: int, tensor: int) -> np.random.Generator:
@@ -94,6 +97,51 @@ def conv_u4(N=64, H=56, W=56, C=64, OC=64, F=3, pad=1, stride=1, residual=True, 
     return dict(I=I, W=Wt, z_in=8, s_a=s_a, s_w=s_w, bias=bias, s_o=s_o, z_out=0,
                 res=res, z_res=8, s_r=float(np.float32(1.25 * s_o)), relu=True,
                 pad=(pad, pad), stride=(stride, stride), F=F, out_dt="u4")
+
+
+def conv_u8(N=64, H=56, W=56, C=64, OC=64, F=3, pad=1, stride=1, residual=True, tag=0):
+    """NHWC u8 input codes uniform in 0..255 with Z_I = 128; OHWI u8 filters
+    round(N(z_w[oc], 40)) clipped, per-filter zero points z_w uniform in 96..160;
+    weight scales U(1e-3, 1e-2), bias N(0, 1); optional u8 residual uniform in
+    0..255 (Z_r = 128, S_r = 1.25 S_o); u8 output with ReLU and Z_o = 0."""
+    wl = CONV_U8
+    I = _uniform_int(rng(wl, 10 * tag + 0), 0, 255, (N, H, W, C), np.uint8)
+    z_w = _uniform_int(rng(wl, 10 * tag + 1), 96, 160, (OC,), np.int32)
+    Wt = np.clip(np.rint(rng(wl, 10 * tag + 2).normal(0.0, 40.0, size=(OC, F, F, C)) + z_w.reshape(-1, 1, 1, 1)),
+                 0, 255).astype(np.uint8)
+    s_w = rng(wl, 10 * tag + 3).uniform(1e-3, 1e-2, size=OC).astype(np.float32)
+    bias = rng(wl, 10 * tag + 4).normal(0.0, 1.0, size=OC).astype(np.float32)
+    OH = (H + 2 * pad - F) // stride + 1
+    OW = (W + 2 * pad - F) // stride + 1
+    res = None
+    if residual:
+        res = _uniform_int(rng(wl, 10 * tag + 5), 0, 255, (N, OH, OW, OC), np.uint8)
+    s_a = 0.02
+    K = F * F * C
+    # std of (q - 128) for uniform codes sqrt(65535 / 12) ~ 73.9; of w - z_w about 40
+    std = math.sqrt((s_a * 0.0055 * 73.9 * 40.0) ** 2 * K + 1.0)
+    s_o = float(np.float32(3.0 * std / 255.0))
+    return dict(I=I, W=Wt, z_w=z_w, z_in=128, s_a=s_a, s_w=s_w, bias=bias, s_o=s_o, z_out=0,
+                res=res, z_res=128, s_r=float(np.float32(1.25 * s_o)), relu=True,
+                pad=(pad, pad), stride=(stride, stride), F=F, out_dt="u8")
+
+
+def vit_fc1_zw(M=12608, K=768, N=3072, tag=0):
+    """vit_fc1 with asymmetric u8 weights: activations as in vit_fc1 (u8, Z_a =
+    128, S_a = 0.02); weights round(N(z_w[n], 25)) clipped to 0..255 with
+    per-channel zero points z_w uniform in 96..160; scales, bias and the output
+    scale as in vit_fc1."""
+    A = _normal_codes(rng(VIT_FC1_ZW, 10 * tag + 0), 128.0, 30.0, 0, 255, (M, K), np.uint8)
+    z_w = _uniform_int(rng(VIT_FC1_ZW, 10 * tag + 1), 96, 160, (N,), np.int32)
+    B = np.clip(np.rint(rng(VIT_FC1_ZW, 10 * tag + 2).normal(0.0, 25.0, size=(N, K)) + z_w[:, None]),
+                0, 255).astype(np.uint8)
+    s_w = rng(VIT_FC1_ZW, 10 * tag + 3).uniform(1e-3, 1e-2, size=N).astype(np.float32)
+    bias = rng(VIT_FC1_ZW, 10 * tag + 4).normal(0.0, 1.0, size=N).astype(np.float32)
+    s_a = 0.02
+    std = math.sqrt((s_a * 0.0055 * 30.0 * 25.0) ** 2 * K + 1.0)
+    s_o = float(np.float32(4.0 * std / 127.0))
+    return dict(A=A, B=B, z_w=z_w, a_dt="u8", z_a=128, s_a=s_a, s_w=s_w, bias=bias, s_o=s_o,
+                z_out=0, out_dt="s8")
 
 
 def vitl_ptf(M=12608, K=1024, N=3072, tag=0):

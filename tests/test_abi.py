@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
               "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_conv_workspace_bytes",
               "q_log_int_softmax", "q_attn_shift_v", "q_lis_attn_v", "q_int_layernorm", "q_eltwise_s8",
               "q_quantize_rows_dynamic", "qgemm_prepack_b_u8", "qgemm_zw", "qnn_gemm_zw_workspace_bytes",
-              "q_layout_nchw64", "qconv_prepack_w_u4", "qnn_status_string",
+              "q_layout_nchw64", "qconv_prepack_w_u4", "qconv_prepack_w_u8", "qconv_u8u8", "qnn_status_string",
               "qnn_check_device_error"):
         assert n in names
 
@@ -200,6 +200,26 @@ def test_conv_u4_zero_point_prepack_rejected_on_host(lib):
     assert L.qconv_prepack_w_u4(16, 20, ctypes.byref(g), 1024, None, None) == qnn.QNN_ERR_ALIGNMENT
     big = qnn.conv_geom(1, 8, 8, 8320, 64, 3, 3)  # 9 * 8320 * 225 >= 2^24
     assert L.qconv_prepack_w_u4(16, 16, ctypes.byref(big), 1024, None, None) == qnn.QNN_ERR_OVERFLOW_RISK
+
+
+def test_conv_u8_zero_point_rejected_on_host(lib):
+    L = lib
+    g = qnn.conv_geom(1, 8, 8, 64, 64, 3, 3)
+    assert L.qconv_prepack_w_u8(16, None, ctypes.byref(g), 1024, None, None) == qnn.QNN_ERR_INVALID_ARG
+    assert L.qconv_prepack_w_u8(16, 20, ctypes.byref(g), 1024, None, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.qconv_prepack_w_u8(16, 16, ctypes.byref(g), 1040, None, None) == qnn.QNN_ERR_ALIGNMENT
+    assert L.qconv_prepack_w_u8(20, 16, ctypes.byref(g), 1024, None, None) == qnn.QNN_ERR_ALIGNMENT
+    odd = qnn.conv_geom(1, 8, 8, 8, 64, 3, 3)
+    assert L.qconv_prepack_w_u8(16, 16, ctypes.byref(odd), 1024, None, None) == qnn.QNN_ERR_UNSUPPORTED
+    # the u8 filters take the s8 image, the u4 filters the s4 one
+    assert qnn.qnn_conv_packed_w_bytes(g, "u8") == qnn.qnn_conv_packed_w_bytes(g, "s8") > 0
+    assert qnn.qnn_conv_packed_w_bytes(g, "u4") == qnn.qnn_conv_packed_w_bytes(g, "s4") > 0
+    # 9 * 3680 * 255^2 > 2^31 - 1: refused before any launch
+    epi = qnn.epilogue("requant", out_dt="u8")
+    epi.M, epi.Bq = 256, 512  # never dereferenced on the host
+    big = qnn.conv_geom(1, 8, 8, 3680, 64, 3, 3)
+    assert L.qconv_u8u8(16, 8, 1024, ctypes.byref(big), ctypes.byref(epi), 16, None,
+                        None) == qnn.QNN_ERR_OVERFLOW_RISK
 
 
 def test_packed_sizes(lib):

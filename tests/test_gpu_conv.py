@@ -25,8 +25,10 @@ def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="re
     colsum = t.empty(OC, dtype=t.int32, device="cuda")
     if w_zp is None:
         qnn.qconv_prepack_w(Wd, w_dt, g, Wp, colsum)
-    else:
+    elif u4:
         qnn.qconv_prepack_w_u4(Wd, dev(np.asarray(w_zp, np.int32)), g, Wp, colsum)
+    else:
+        qnn.qconv_prepack_w_u8(Wd, dev(np.asarray(w_zp, np.int32)), g, Wp, colsum)
     a_dt = "u4" if u4 else "u8"
     sw = dev(np.asarray(s_w, np.float32))
     bd = dev(np.asarray(bias, np.float32))
@@ -58,8 +60,10 @@ def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="re
             qnn.qconv_u4s4(Id, z_in, Wp, g, epi, O, O32, workspace=ws)
         elif u4:
             qnn.qconv_u4s4(Id, z_in, Wp, g, epi, O, O32)
-        else:
+        elif w_zp is None:
             qnn.qconv_u8s8(Id, z_in, Wp, g, epi, O, O32)
+        else:
+            qnn.qconv_u8u8(Id, z_in, Wp, g, epi, O, O32)
         assert qnn.qnn_check_device_error() == qnn.QNN_OK
         outs.append((path, O, O32))
 
@@ -72,7 +76,10 @@ def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="re
             Wc = oracle.unpack_nibbles(W_pk, signed=False) - np.asarray(w_zp, np.int32).reshape(-1, 1, 1, 1)
     else:
         Ic = I_pk.astype(np.int32)
-        Wc = W_pk.astype(np.int8).astype(np.int32)
+        if w_zp is None:
+            Wc = W_pk.astype(np.int8).astype(np.int32)
+        else:  # u8 filters: the zero-point-centred codes w - z_w[oc]
+            Wc = W_pk.astype(np.uint8).astype(np.int32) - np.asarray(w_zp, np.int32).reshape(-1, 1, 1, 1)
     cs = oracle.colsum(Wc.reshape(OC, -1))
     assert np.array_equal(host(colsum), cs)
     zc = z_in - (0 if u4 else 128)
@@ -253,6 +260,52 @@ def test_conv_u4u4_resnet_3x3_full(oracle):
     geom = (64, 56, 56, 64, 64, 3, 1, 1)
     _conv(oracle, w["I"], w["W"], geom, w["z_in"], w["s_a"], w["s_w"], w["s_o"] * 2, w["bias"],
           res=w["res"], z_res=w["z_res"], s_r=w["s_r"], w_zp=z_w)
+
+
+@pytest.mark.parametrize("geom", [(2, 9, 9, 64, 64, 3, 1, 1),    # K = 576: exact chunks of 512 + 64
+                                  (1, 7, 7, 256, 128, 3, 1, 1),  # K = 2304: five chunks
+                                  (2, 6, 6, 512, 64, 1, 0, 1),   # K = 512: one chunk, exactly full
+                                  (1, 9, 9, 48, 96, 3, 1, 2)])   # stride 2, OC = 96
+def test_conv_u8u8(oracle, geom):
+    """u8 activations x u8 filters with per-filter zero points (MegEngine article
+    背景 / 緩解精度下降): the filter values w - z_w reach 255 in magnitude."""
+    N, H, W, C, OC, F, pad, st = geom
+    OH = (H + 2 * pad - F) // st + 1
+    OW = (W + 2 * pad - F) // st + 1
+    rng = np.random.default_rng(40 + C)
+    I = rng.integers(0, 256, size=(N, H, W, C)).astype(np.uint8)
+    Wt = rng.integers(0, 256, size=(OC, F, F, C)).astype(np.uint8)
+    z_w = rng.integers(0, 256, size=OC).astype(np.int32)
+    z_w[:2] = (0, 255)
+    s_w = rng.uniform(1e-3, 1e-2, size=OC).astype(np.float32)
+    bias = rng.normal(0, 1, size=OC).astype(np.float32)
+    res = rng.integers(0, 256, size=(N, OH, OW, OC)).astype(np.uint8)
+    _conv(oracle, I, Wt, geom, 77, 0.02, s_w, 0.5, bias, u4=False, out_dt="u8", z_out=3,
+          res=res, res_dt="u8", z_res=120, s_r=0.4, w_zp=z_w)
+
+
+@pytest.mark.parametrize("geom", [(1, 6, 6, 512, 64, 1, 0, 1), (1, 8, 8, 64, 64, 3, 1, 1)])
+def test_conv_u8u8_extreme_codes(oracle, geom):
+    """The largest products of one sign: inputs 0 (centred -128) against filters
+    255 with zero point 0 and filters 0 with zero point 255 (+-255), so every
+    512-term chunk sum reaches 512 * 32640, just below 2^24; raw int32 out."""
+    N, H, W, C, OC, F, pad, st = geom
+    I = np.zeros((N, H, W, C), np.uint8)
+    Wt = np.zeros((OC, F, F, C), np.uint8)
+    Wt[0::2] = 255
+    z_w = np.where(np.arange(OC) % 2 == 0, 0, 255).astype(np.int32)
+    s_w = np.full(OC, 1e-3, np.float32)
+    _conv(oracle, I, Wt, geom, 200, 0.02, s_w, 1.0, np.zeros(OC, np.float32), u4=False, mode="s32",
+          w_zp=z_w)
+
+
+def test_conv_u8u8_resnet_3x3_full(oracle):
+    """ResNet-50 stage-1 3x3 Conv_Add_Relu at full size (64 x 56 x 56 x 64) with u8
+    activations and u8 filters with per-filter zero points, compared in full."""
+    w = workloads.conv_u8()
+    geom = (64, 56, 56, 64, 64, 3, 1, 1)
+    _conv(oracle, w["I"], w["W"], geom, w["z_in"], w["s_a"], w["s_w"], w["s_o"], w["bias"], u4=False,
+          out_dt="u8", res=w["res"], res_dt="u8", z_res=w["z_res"], s_r=w["s_r"], w_zp=w["z_w"])
 
 
 def test_conv_errors():
