@@ -411,6 +411,23 @@ def test_conv_implicit_gemm_identity(oracle):
         assert np.array_equal(oracle.gemm_acc(cols, Bm, 8), direct)
 
 
+def test_conv_filter_zero_point_terms(oracle):
+    """MegEngine article, 緩解精度下降, for asymmetric filters: the conv over
+    (q_I - Z_I)(q_W - Z_W) is the conv with q_W less Z_W times the conv with a
+    filter of ones (the input's receptive-field sum, padded taps 0), both terms
+    by brute force, at full u8 ranges."""
+    g = np.random.default_rng(17)
+    I = g.integers(0, 256, size=(1, 5, 6, 3)).astype(np.int32)
+    W = g.integers(0, 256, size=(4, 3, 3, 3)).astype(np.int32)
+    z_w = np.array([0, 255, 128, 77], np.int32)
+    ones = np.ones((1, 3, 3, 3), np.int32)
+    for pad, st, z_in in (((1, 1), (1, 1), 100), ((0, 0), (2, 2), 255), ((1, 1), (2, 1), 0)):
+        got = oracle.conv_acc_direct(I, W - z_w.reshape(-1, 1, 1, 1), z_in, pad, st)
+        full = np.array(brute.conv_acc(I.tolist(), W.tolist(), z_in, pad, st), np.int64)
+        rsum = np.array(brute.conv_acc(I.tolist(), ones.tolist(), z_in, pad, st), np.int64)
+        assert np.array_equal(got, full - rsum * z_w[None, :])
+
+
 def test_conv1x1_is_gemm(oracle):
     """A 1x1, stride-1, unpadded conv is a GEMM of the pixel matrix (numpy int64)."""
     g = np.random.default_rng(16)
