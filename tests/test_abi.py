@@ -37,6 +37,29 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+def _declared_arities():
+    """Function name -> number of parameters, from the header's prototypes."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(([^)]*)\)\s*;", src, flags=re.M | re.S):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_matches_header_arity(lib):
+    """Every function the binding declares exists in the header with the same
+    number of parameters (a ctypes signature with a missing or extra argument
+    would pass garbage across the boundary)."""
+    arity = _declared_arities()
+    assert len(arity) >= 30
+    assert set(arity) == set(qnn._SYMBOLS), set(arity) ^ set(qnn._SYMBOLS)
+    for name, fn in qnn._SYMBOLS.items():
+        assert name in arity, name
+        assert len(fn.argtypes) == arity[name], (name, len(fn.argtypes), arity[name])
+
+
 def test_library_exports_every_declared_symbol(lib):
     missing = [n for n in _declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
