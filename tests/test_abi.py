@@ -249,3 +249,31 @@ def test_packed_sizes(lib):
     assert qnn.qnn_gemm_packed_b_bytes(3072, 768) == 12 * 12 * 256 * 128
     assert qnn.qnn_gemm_packed_b_bytes(300, 272) == 2 * 5 * 256 * 128
     assert qnn.qnn_gemm_packed_b_bytes(0, 16) == 0
+
+
+def test_struct_layouts_match_header(tmp_path):
+    """The ctypes mirrors of qnn_qparams, qnn_epilogue and qnn_conv_geom have
+    the C structs' size and field offsets: a C probe compiled against
+    include/qnn.h (plain C, no CUDA headers) prints them."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"qnn_qparams": qnn.QParams, "qnn_epilogue": qnn.Epilogue, "qnn_conv_geom": qnn.ConvGeom}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "qnn.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'    printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'    printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["    return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert got[(cname, fname)] == getattr(py, fname).offset, (cname, fname)
