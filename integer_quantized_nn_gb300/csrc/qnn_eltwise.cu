@@ -17,10 +17,12 @@
 // chunks, one per thread and step, both sides coalesced along the block.
 //
 // q_quantize_rows_dynamic [QI 量化参数选择 (最大值截断), 量化算子]: per row the
-// scale max|x| / 127 (one IEEE division), then q = clip(rint(x / s)) with one
-// IEEE division per element; a zero row gets scale 0 and codes 0.  One warp per
-// row: the row is read twice (the second time from cache), 4 floats per lane and
-// step, codes stored as 4-byte words.
+// scale max|x| / 127 (one IEEE division), then q = clip(rint(x / s)), the code of
+// the IEEE quotient (formed through the row's reciprocal, with the IEEE division
+// wherever that could decide the code differently -- see dyn_quant4); a zero row
+// gets scale 0 and codes 0.  One warp per row: rows of up to 1024 values are
+// held in registers (one read), longer ones read twice (the second time from
+// cache); 4 floats per lane and step, codes stored as 4-byte words.
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>
