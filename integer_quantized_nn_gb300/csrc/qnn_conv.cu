@@ -1,5 +1,6 @@
-// qnn_conv.cu -- implicit-GEMM quantized convolution (qconv_u4s4, qconv_u8s8)
-// and its weight prepack.
+// qnn_conv.cu -- implicit-GEMM quantized convolution (qconv_u4s4, qconv_u8s8,
+// qconv_u8u8) and its weight prepack (s4 / s8 filters, and u4 / u8 filters with
+// per-filter zero points, taken out at prepack).
 //
 // [MG conv 算子優化, Fig. 5] a convolution of an (N, IH, IW, C) input with
 // (OC, FH, FW, C) filters is the product of the (N*OH*OW) x (FH*FW*C) patch
@@ -19,7 +20,9 @@
 //            K below 139810) and the epilogue multiplies by 512.  The two masks
 //            deliver each group of 8 channels in the order 0,2,4,6,1,3,5,7; the
 //            weight prepack uses the same order, which leaves every sum unchanged.
-//   u8 x s8: bytes to fp16 exactly as in the GEMM (kind::f16), q - 128.
+//   u8 x s8: bytes to fp16 exactly as in the GEMM (kind::f16), q - 128; u8
+//            filters less their zero points (u8u8) reach 255 in magnitude, so
+//            their exact fp32 chunks are half as long (512 products).
 // Padded taps read the code z_in (the real value 0 [reading of the pages]),
 // so the folded zero-point term applies to every tap alike.
 #include <cuda_fp8.h>

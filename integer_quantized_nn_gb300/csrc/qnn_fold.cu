@@ -1,5 +1,6 @@
 // qnn_fold.cu -- work done once per weight tensor, ahead of inference:
-// prepacking the GEMM weight operand, the weight column sums and the folded
+// prepacking the GEMM weight operand (s8; u8 centred at 128; u8 less per-row
+// zero points for the u8 conv filters), the weight column sums and the folded
 // epilogue constants.
 //
 // Folding [MG 緩解精度下降: the zero-point part that does not depend on the
