@@ -344,7 +344,8 @@ def _requant_case(oracle, relu, residual, out_dt, seed):
 
 
 @pytest.mark.parametrize("relu,residual,out_dt", [(False, False, "s8"), (True, False, "u8"),
-                                                  (True, True, "u8"), (False, True, "s8")])
+                                                  (True, True, "u8"), (False, True, "s8"),
+                                                  (True, True, "u4"), (False, False, "u4")])
 def test_requant_vs_exact_rational(oracle, relu, residual, out_dt):
     """The fp32 requant pipeline equals exact-rational requantization
     (dequantize everything, sum, add bias and residual, divide by S_o, round
