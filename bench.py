@@ -783,7 +783,7 @@ def cpu_baseline_gemm(w, target_s=15.0):
     B = w["B"].astype(np.int32)
     N, K = B.shape
     cs = oracle.colsum(B)
-    _, Mo, Bqo, _ = oracle.fold(cs, w["z_a"] - 128, w["s_a"], w["s_w"], w["s_o"], w["bias"])
+    _, Mo, Bqo, _ = oracle.fold(cs, w["z_a"], w["s_a"], w["s_w"], w["s_o"], w["bias"])
     rows = 64
     t0 = time.perf_counter()
     acc = oracle.gemm_acc(A[:rows], B, w["z_a"])
@@ -813,7 +813,7 @@ def run_reference(args):
     A = w["A"].astype(np.int32)
     B = w["B"].astype(np.int32)
     cs = oracle.colsum(B)
-    _, Mo, Bqo, _ = oracle.fold(cs, w["z_a"] - 128, w["s_a"], w["s_w"], w["s_o"], w["bias"])
+    _, Mo, Bqo, _ = oracle.fold(cs, w["z_a"], w["s_a"], w["s_w"], w["s_o"], w["bias"])
     # size the per-step sample so warmup + steps take about args.cpu_seconds * 4
     t0 = time.perf_counter()
     oracle.requant(oracle.gemm_acc(A[:16], B, w["z_a"]), Mo, Bqo, "s8")

@@ -194,8 +194,8 @@ def colsum(B):
     return out
 
 
-def fold(colsum_, zcoef, s_a, s_w, s_o, bias=None):
-    """Returns (zp_term, M, Bq, D) as folded ahead of inference."""
+def fold(colsum_, z_a, s_a, s_w, s_o, bias=None):
+    """Returns (zp_term, M, Bq, D) as folded ahead of inference; zp_term = z_a * colsum."""
     cs = _c(colsum_, np.int32)
     N = cs.shape[0]
     sw = _c(np.atleast_1d(s_w), np.float32)
@@ -205,7 +205,7 @@ def fold(colsum_, zcoef, s_a, s_w, s_o, bias=None):
     Mv = np.empty(N, np.float32)
     Bq = np.empty(N, np.float32)
     D = np.empty(N, np.float32)
-    rc = lib().oracle_fold(N, int(zcoef), _p(cs), np.float32(s_a), _p(sw), per_ch, _p(b),
+    rc = lib().oracle_fold(N, int(z_a), _p(cs), np.float32(s_a), _p(sw), per_ch, _p(b),
                            np.float32(s_o), _p(zp), _p(Mv), _p(Bq), _p(D))
     if rc != 0:
         raise OverflowError("zp_term does not fit int32")

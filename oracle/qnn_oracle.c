@@ -229,22 +229,22 @@ void oracle_colsum(const int32_t *B, int64_t N, int64_t K, int32_t *colsum)
 /* ---------------------------------------------------------------------------
  * Constants folded ahead of inference [MG 緩解精度下降; QI 量化乘法:
  * "scale_abc can be computed ahead"].
- *   zp_term[n] = zcoef * colsum[n]       (int32; zcoef = Z_a - c_a where c_a is
- *                                        the centre the library subtracts from
- *                                        a u8 operand, see the library header)
+ *   zp_term[n] = Z_a * colsum[n]         (int32: the input-independent term
+ *                                        of sum (q_a - Z_a) q_w, subtracted from
+ *                                        sum q_a q_w)
  *   M[n]  = (s_a * s_w[n]) / s_o          fmul, then fdiv
  *   Bq[n] = bias[n] / s_o
  *   D[n]  = s_a * s_w[n]                  (dequantizing epilogue)
  * s_w is per output channel when w_per_channel, else s_w[0]; bias may be NULL
  * (zero).
  * ------------------------------------------------------------------------- */
-int oracle_fold(int64_t N, int32_t zcoef, const int32_t *colsum, float s_a,
+int oracle_fold(int64_t N, int32_t z_a, const int32_t *colsum, float s_a,
                 const float *s_w, int w_per_channel, const float *bias, float s_o,
                 int32_t *zp_term, float *Mv, float *Bq, float *D)
 {
     int bad = 0;
     for (int64_t n = 0; n < N; ++n) {
-        int64_t z = (int64_t)zcoef * (int64_t)colsum[n];
+        int64_t z = (int64_t)z_a * (int64_t)colsum[n];
         if (z > INT32_MAX || z < INT32_MIN) bad = 1;
         zp_term[n] = (int32_t)z;
         float sw = s_w[w_per_channel ? n : 0];

@@ -51,10 +51,24 @@ def gpu_gemm_setup(B, a_dt, z_a, s_a, s_w, s_o, bias=None):
     return dict(Bd=Bd, Bp=Bp, colsum=colsum, zp=zp, M=Mv, Bq=Bq, D=D, bias=bd, sw=sw)
 
 
+def library_zp_term(zp_page, colsum, centre):
+    """The zero-point term in the library's operand encoding.  The oracle folds
+    the page's term Z_a * colsum (sum (q - Z_a) w = sum q w - Z_a colsum); the
+    library feeds a u8 operand to the MMA as q - 128 (centre 128), so the term it
+    subtracts is sum (q - 128) w - sum (q - Z_a) w = (Z_a - 128) colsum =
+    Z_a colsum - 128 colsum."""
+    z = np.asarray(zp_page, np.int64) - int(centre) * np.asarray(colsum, np.int64)
+    assert np.all(np.abs(z) < 2 ** 31)
+    return z.astype(np.int32)
+
+
 def oracle_fold(oracle, B, a_dt, z_a, s_a, s_w, s_o, bias=None):
+    """Oracle fold (the page's zp_term = Z_a * colsum), with zp_term translated
+    to the library's encoding for comparison with q_fold_epilogue."""
     cs = oracle.colsum(B.astype(np.int32))
     centre = 128 if a_dt == "u8" else 0
-    return oracle.fold(cs, z_a - centre, s_a, np.asarray(s_w, np.float32), s_o, bias) + (cs,)
+    zp, Mv, Bq, D = oracle.fold(cs, z_a, s_a, np.asarray(s_w, np.float32), s_o, bias)
+    return library_zp_term(zp, cs, centre), Mv, Bq, D, cs
 
 
 def f32_bits(a):

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 from integer_quantized_nn_gb300 import qnn
-from _util import aligned_empty, dev, host, f32_bits
+from _util import aligned_empty, dev, host, f32_bits, library_zp_term
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +44,8 @@ def _run(oracle, A, a_dt, z_a, B, z_w, s_w, bias, s_a=0.02, s_o=None, rows=None)
     Bc = B.astype(np.int32) - z_w[:, None]  # the zero-point-centred weights
     cs_o = oracle.colsum(Bc)
     centre = 128 if a_dt == "u8" else 0
-    zp_o, M_o, Bq_o, _ = oracle.fold(cs_o, z_a - centre, s_a, s_w, s_o, bias)
+    zp_o, M_o, Bq_o, _ = oracle.fold(cs_o, z_a, s_a, s_w, s_o, bias)
+    zp_o = library_zp_term(zp_o, cs_o, centre)
     assert np.array_equal(host(cs), cs_o)
     assert np.array_equal(host(zp), zp_o)
     assert np.array_equal(f32_bits(host(Mv)), f32_bits(M_o))

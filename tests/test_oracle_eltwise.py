@@ -14,6 +14,8 @@ from fractions import Fraction
 import numpy as np
 import pytest
 
+from _exact import F, fl32, near_half_inputs, round_half_away
+
 pytestmark = pytest.mark.cpu
 
 
@@ -89,6 +91,49 @@ def test_dynamic_quantize_properties(oracle):
         amax = np.abs(x).max(axis=1)
         assert np.all(s == (amax / np.float32(127.0)).astype(np.float32))
         assert q[7, 11] == -127
+
+
+def _dynamic_rows(rng):
+    """Rows whose largest magnitude A fixes s = fl32(A / 127), the other entries
+    placed a few ulps either side of (k + 1/2) s; rows with A = 127 * 2^e make s a
+    power of two, so x / s is exact and (k + 1/2) s is an exact tie."""
+    rows = []
+    for i, A in enumerate([127.0, -127.0 * 2.0 ** -5, 3.7, 0.61, -11.3, 127.0 * 4.0, 1e-3]):
+        A = np.float32(A)
+        s = fl32(F(abs(A)) / 127)
+        body = near_half_inputs(s, range(-127, 126, 3), ulps=2)
+        body = body[np.abs(body) < abs(A)]
+        row = np.concatenate([[A], body, rng.permutation(body)[:40]]).astype(np.float32)
+        rows.append(rng.permutation(row))
+    n = max(len(r) for r in rows)
+    return np.stack([np.pad(r, (0, n - len(r))) for r in rows]).astype(np.float32)
+
+
+@pytest.mark.parametrize("narrow", [False, True])
+def test_dynamic_quantize_exact(oracle, narrow):
+    """Quantization intro, 量化参数选择 (最大值截断) and 量化算子: the row scale is the
+    correctly rounded quotient max|x| / 127, and each code is round half to even
+    of the correctly rounded quotient x / s, clipped.  Inputs sit next to and on
+    rounding decision points, so multiplying by a rounded reciprocal of s, or
+    rounding ties away from zero, gives other codes (both are asserted present)."""
+    rng = np.random.default_rng(5)
+    x = _dynamic_rows(rng)
+    q, s = oracle.quantize_rows_dynamic(x, narrow)
+    qmin = -127 if narrow else -128
+    recip_differs = away_differs = 0
+    for r in range(x.shape[0]):
+        amax = max(abs(F(v)) for v in x[r])
+        sr = fl32(amax / 127)
+        assert s[r] == sr, (r, s[r], sr)
+        inv = F(fl32(1 / F(sr)))
+        for c in range(x.shape[1]):
+            t = F(fl32(F(x[r, c]) / F(sr)))
+            want = max(qmin, min(127, _round_half_even(t)))
+            assert q[r, c] == want, (r, c, float(x[r, c]), int(q[r, c]), want)
+            tr = F(fl32(F(x[r, c]) * inv))
+            recip_differs += max(qmin, min(127, _round_half_even(tr))) != want
+            away_differs += max(qmin, min(127, round_half_away(t))) != want
+    assert recip_differs > 0 and away_differs > 0
 
 
 def test_eltwise_errors(oracle):

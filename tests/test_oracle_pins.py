@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 
 from oracle import brute
+from _exact import F, fl32, near_half_inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 pytestmark = pytest.mark.cpu
@@ -26,20 +27,6 @@ def _golden(name):
             if line and not line.startswith("#"):
                 rows.append(line.split())
     return rows
-
-
-def fl32(fr: Fraction) -> np.float32:
-    """Correctly rounded (nearest, ties to even) fp32 value of an exact rational."""
-    c = np.float32(float(fr))
-    cands = [np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))]
-    best, bd = None, None
-    for x in cands:
-        if not np.isfinite(x):
-            continue
-        d = abs(Fraction(float(x)) - fr)
-        if bd is None or d < bd or (d == bd and (int(np.float32(x).view(np.uint32)) & 1) == 0):
-            best, bd = x, d
-    return np.float32(best)
 
 
 # ---------------------------------------------------------------- quantize ---
@@ -108,28 +95,41 @@ def test_nan_maps_to_zero_point(oracle):
     assert int(oracle.quantize(x, oracle.SYM, "s8", scale=0.1)[0]) == 0
 
 
-def _exact_quant(x, s, z, lo, hi):
-    t = Fraction(float(x)) / Fraction(float(s))
-    return min(max(brute.round_half_even(t) + z, lo), hi), t
+def ieee_quotient_code(x, s, z, lo, hi):
+    """The code of reading c2: one IEEE fp32 division x / s (correctly rounded,
+    ties to even), then round half to even, + z, clip."""
+    t = fl32(Fraction(float(x)) / Fraction(float(s)))
+    return min(max(brute.round_half_even(Fraction(float(t))) + z, lo), hi)
+
+
+def reciprocal_code(x, s, z, lo, hi):
+    """The same with x * RN(1 / s) in place of the division (not the reading)."""
+    t = fl32(Fraction(float(x)) * Fraction(float(fl32(1 / Fraction(float(s))))))
+    return min(max(brute.round_half_even(Fraction(float(t))) + z, lo), hi)
 
 
 @pytest.mark.parametrize("dt,scheme,z", [("s8", 0, 0), ("u8", 1, 128), ("s4", 0, 0),
                                          ("u4", 1, 8)])
-def test_quantize_vs_exact_rational(oracle, dt, scheme, z):
-    """The fp32 pipeline equals exact-rational round-half-even except within an
-    fp32 rounding of a tie (counted and bounded)."""
+def test_quantize_is_ieee_division(oracle, dt, scheme, z):
+    """Quantization intro, 量化算子: q = round(x / scale), read as one IEEE fp32
+    division then half-even rounding (reading c2), + offset after rounding
+    (量化模式), clip.  Every code must equal that reading evaluated in exact
+    rational arithmetic, including inputs placed a few ulps either side of
+    (k + 1/2) * s, where multiplying by a rounded reciprocal gives another code
+    (the test asserts such inputs are present)."""
     g = np.random.default_rng(11)
-    x = g.normal(0, 3, size=4000).astype(np.float32)
-    s = np.float32(0.037)
-    q = oracle.quantize(x, scheme, dt, scale=s, zp=z)
     lo, hi = oracle.qrange(dt)
-    near = 0
-    for xi, qi in zip(x, q):
-        e, t = _exact_quant(xi, s, z, lo, hi)
-        if e != qi:
-            assert brute.distance_to_tie(t) < abs(t) * Fraction(1, 2 ** 22) + Fraction(1, 2 ** 40)
-            near += 1
-    assert near <= 2
+    span = range(lo - z - 2, hi - z + 2)
+    discriminating = 0
+    for s in (np.float32(0.037), np.float32(0.1), np.float32(0.0071), np.float32(0.013), np.float32(3.3)):
+        x = np.concatenate([g.normal(0, 3, size=500).astype(np.float32) * np.float32(s / 0.037),
+                            near_half_inputs(s, span)])
+        q = oracle.quantize(x, scheme, dt, scale=s, zp=z)
+        for xi, qi in zip(x, q):
+            want = ieee_quotient_code(xi, s, z, lo, hi)
+            assert qi == want, (dt, float(s), float(xi), int(qi), want)
+            discriminating += reciprocal_code(xi, s, z, lo, hi) != want
+    assert discriminating > 0
 
 
 def test_pow2_closed_form(oracle):
@@ -256,9 +256,9 @@ def test_gemm_overflow_detected(oracle):
 
 def test_zero_point_fold_identity(oracle):
     """MegEngine article, 緩解精度下降: sum (q_I - Z_I) q_W = sum q_I q_W - Z_I sum q_W,
-    the second term computable before inference.  The library centres a u8
-    operand at 128, so its folded term is (Z - 128) * colsum; both forms must
-    give the unexpanded sum."""
+    the second term computable before inference.  With the operand centred at
+    128 (as the library feeds a u8 operand to the MMA) the folded term becomes
+    Z colsum - 128 colsum; both forms must give the unexpanded sum."""
     g = np.random.default_rng(8)
     A = g.integers(0, 256, size=(9, 70)).astype(np.int32)
     B = g.integers(-128, 128, size=(11, 70)).astype(np.int32)
@@ -268,7 +268,8 @@ def test_zero_point_fold_identity(oracle):
         direct = oracle.gemm_acc(A, B, z)
         zp, *_ = oracle.fold(cs, z, 1.0, np.ones(11, np.float32), 1.0)
         assert np.array_equal(oracle.gemm_acc(A, B, 0) - zp[None, :], direct)
-        zp_c, *_ = oracle.fold(cs, z - 128, 1.0, np.ones(11, np.float32), 1.0)
+        assert np.array_equal(zp, z * B.sum(axis=1))
+        zp_c = zp.astype(np.int64) - 128 * cs.astype(np.int64)
         assert np.array_equal(oracle.gemm_acc(A, B, 128) - zp_c[None, :], direct)
 
 
@@ -466,9 +467,6 @@ def test_requant_rowscale_reduces_and_scales(oracle):
                 assert abs(frac - Fraction(1, 2)) < abs(exact) * Fraction(1, 2 ** 21) + Fraction(1, 2 ** 20)
                 near += 1
     assert near <= 2
-    y = oracle.dequant_rowscale(acc, r, Mv, Bq)
-    ref = acc.astype(np.float64) * r[:, None].astype(np.float64) * Mv.astype(np.float64) + Bq
-    assert np.allclose(y, ref, rtol=1e-6, atol=1e-6)
 
 
 def test_nchw64_layout(oracle):
@@ -487,3 +485,88 @@ def test_nchw64_layout(oracle):
                     assert y[n, c // 64, h, w, c % 64] == x[n, h, w, c]
     with pytest.raises(ValueError):
         oracle.nhwc_to_nchw64(np.zeros((1, 2, 2, 48), np.int32))
+
+
+def _rowscale_inputs(seed):
+    g = np.random.default_rng(seed)
+    acc = np.concatenate([g.integers(-200000, 200000, size=(10, 24)),
+                          g.integers(-2 ** 31, 2 ** 31, size=(2, 24))]).astype(np.int32)
+    r = g.uniform(0.01, 0.1, size=12).astype(np.float32)
+    Mv = g.uniform(1e-5, 1e-3, size=24).astype(np.float32)
+    bias = g.normal(0, 3, size=24).astype(np.float32)
+    return acc, r, Mv, bias
+
+
+def test_dequant_rowscale_steps_exact(oracle):
+    """Per-row activation scales in the dequantizing epilogue (reading r32):
+    d = fl(r[m] * D[n]) first, then y = fl(fl(float(acc) * d) + bias[n]) -- each
+    step one correctly rounded fp32 operation, evaluated here in exact rational
+    arithmetic (float(acc) rounds to nearest even above 2^24).  Grouping the
+    product as (acc * r) * D instead changes many results (asserted)."""
+    acc, r, D, bias = _rowscale_inputs(41)
+    y = oracle.dequant_rowscale(acc, r, D, bias)
+    y0 = oracle.dequant_rowscale(acc, r, D)
+    regrouped = 0
+    for m in range(acc.shape[0]):
+        for n in range(acc.shape[1]):
+            a = F(fl32(int(acc[m, n])))
+            d = F(fl32(F(r[m]) * F(D[n])))
+            v = fl32(a * d)
+            assert y0[m, n] == v
+            assert y[m, n] == fl32(F(v) + F(bias[n])), (m, n)
+            regrouped += fl32(F(fl32(a * F(r[m]))) * F(D[n])) != v
+    assert regrouped > 0
+
+
+@pytest.mark.parametrize("relu,residual", [(False, False), (True, True)])
+def test_requant_rowscale_steps_exact(oracle, relu, residual):
+    """The requant with per-row scales as its fp32 steps (reading r32 with the
+    requant order of 常见计算图优化, Y = Wx + (Y2 + B)): Mrow = fl(r[m] * M[n]);
+    t = Bq, with a residual t = fl(fl(float(res - z_res) * R) + t); v =
+    fl(fl(float(acc) * Mrow) + t); q = clip(round_half_even(v) [, max 0] +
+    z_out).  Exact rational evaluation of each correctly rounded step."""
+    acc, r, Mv, Bq = _rowscale_inputs(42)
+    g = np.random.default_rng(43)
+    res = g.integers(0, 256, size=acc.shape).astype(np.int32) if residual else None
+    z_res, R, z_out = 120, np.float32(0.731), 3
+    q = oracle.requant_rowscale(acc, r, Mv, Bq, "u8", relu=relu, res=res, z_res=z_res,
+                                R=R if residual else 0.0, z_out=z_out)
+    for m in range(acc.shape[0]):
+        for n in range(acc.shape[1]):
+            mrow = F(fl32(F(r[m]) * F(Mv[n])))
+            t = F(Bq[n])
+            if residual:
+                t = F(fl32(F(fl32(F(fl32(int(res[m, n]) - z_res)) * F(R))) + t))
+            v = F(fl32(F(fl32(F(fl32(int(acc[m, n]))) * mrow)) + t))
+            k = brute.round_half_even(v)
+            if relu:
+                k = max(k, 0)
+            assert q[m, n] == min(max(k + z_out, 0), 255), (m, n)
+
+
+def test_requant_rowscale_on_ties(oracle):
+    """Per-row scales in the requant, on rounding decision points: for each row
+    the bias is chosen so that v = fl(fl(float(acc) * fl(r * M)) + Bq) is
+    exactly k + 1/2 (Bq = T - p is exact for p within a factor 2 of T), so the
+    result is round-half-even of a tie.  A factor formed in another order
+    (fl(fl(acc * r) * M), or M / (1 / r)) moves v off the tie for many elements
+    (asserted), so a reordering in the oracle shows up here."""
+    g = np.random.default_rng(44)
+    N = 64
+    Mv = g.uniform(1e-5, 1e-3, size=N).astype(np.float32)
+    other = 0
+    for m in range(16):
+        r = np.float32(g.uniform(0.01, 0.1))
+        mrow = [F(fl32(F(r) * F(Mv[n]))) for n in range(N)]
+        acc = np.array([int(round(float(g.uniform(40, 120) / float(mrow[n]))) * (1 if g.random() < 0.5 else -1))
+                        for n in range(N)], np.int32)
+        p = [F(fl32(F(fl32(int(acc[n]))) * mrow[n])) for n in range(N)]
+        T = [Fraction(2 * int(np.floor(float(pv))) + 1, 2) for pv in p]
+        Bq = np.array([fl32(T[n] - p[n]) for n in range(N)], np.float32)
+        assert all(F(Bq[n]) == T[n] - p[n] for n in range(N))
+        q = oracle.requant_rowscale(acc[None, :], np.array([r], np.float32), Mv, Bq, "s8")[0]
+        for n in range(N):
+            assert q[n] == min(max(brute.round_half_even(T[n]), -128), 127), (m, n)
+            alt = F(fl32(F(fl32(F(fl32(F(fl32(int(acc[n]))) * F(r))) * F(Mv[n]))) + F(Bq[n])))
+            other += alt != T[n]
+    assert other > 0
