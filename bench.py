@@ -38,9 +38,9 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# the headline GEMM kernel, from the ncu capture summarised in
-# profiles/qgemm_vit_fc1.md, valid only for the sources that kernel is built
-# from (hash of HEADLINE_SOURCES); reported as null otherwise.
+# the headline GEMM kernel, taken from a kept ncu capture of this workload (not
+# measured in this run); valid only for the sources that kernel is built from
+# (hash of HEADLINE_SOURCES) and reported as null otherwise.
 TRAFFIC_NCU = {"csrc_sha256_16": "977db6c9e8207326", "bytes": 24323840 + 61696}
 
 
@@ -341,10 +341,16 @@ def run_gpu(args):
     if not args.no_extras and dist.rank == 0:
         extras = run_extras(torch, qnn, workloads, device, flush, stream, pk, args)
 
-    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1), and the
+    # oracle's single-thread / all-core times for every workload
     cpu = None
+    otab = None
     if dist.rank == 0 and dist.ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_gemm(w, target_s=args.cpu_seconds)
+        if not args.no_oracle_table:
+            gms = {k: v["ms"] for k, v in extras.items() if isinstance(v, dict) and "ms" in v}
+            gms["vit_fc1"] = round(total_ms_max / args.steps, 5)
+            otab = oracle_table(gms)
 
     dtype_str = "u8 x s8 -> s32 (exact on the f16 tensor pipe), requant to s8"
     peak = float(pk["bf16_tflops"])
@@ -361,7 +367,8 @@ def run_gpu(args):
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": (TRAFFIC_NCU["bytes"] if csrc_hash() == TRAFFIC_NCU["csrc_sha256_16"]
                                  else None),
-                     "traffic_unit": "bytes per launch (ncu DRAM read + write)",
+                     "traffic_unit": "bytes per launch (ncu DRAM read + write); a constant from a "
+                                     "kept ncu capture of the same kernel sources, not measured in this run",
                      "peak_kind": f"{pk_kind} bf16 dense burst (the f16 MMA kind runs at the bf16 rate)",
                      "kernel": "qmma_kernel<GemmPackedOp,256,false>",
                      "kernel_ms": round(gemm_ms, 5),
@@ -373,6 +380,7 @@ def run_gpu(args):
                     "frac_hbm": round(pack_bytes / (pack_ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]), 4),
                     "algorithmic": "M*K code bytes read + the fp16 image written"},
         "cpu_baseline": cpu,
+        "oracle_cpu": otab,
         "e2e": {"value": round(e2e_value, 3), "unit": "TOPS", "h2d_bytes_per_step": M * K,
                 "d2h_bytes_per_step": M * N, "ms_per_step": round(e2e_ms, 5),
                 "pipelining": "H2D / qgemm_s8 / D2H on three streams, two buffer sets; an L2 flush "
@@ -449,6 +457,33 @@ def setup_gemm_zw(torch, qnn, workloads, device, stream):
     return fn, {"ops": 2.0 * Mm * Nn * Kk, "M": Mm, "N": Nn, "K": Kk}
 
 
+def square_16384(torch, qnn, workloads, device, flush, stream, peak, steps, out):
+    """qgemm_s8 at M = N = K = 16384 (8.80 T int ops per call), operands drawn on
+    the device; requant multiplier 2^-21 (2^-(ceil(log2 K) + 7)), s8 out."""
+    n = 16384
+    A = workloads.device_uniform_s8((n, n), 5160, device)
+    B = workloads.device_uniform_s8((n, n), 5161, device)
+    Bp = _aligned_1024(torch, qnn.qnn_gemm_packed_b_bytes(n, n), device)
+    cs = torch.empty(n, dtype=torch.int32, device=device)
+    qnn.qgemm_prepack_b(B, Bp, cs)
+    del B
+    zp = torch.empty(n, dtype=torch.int32, device=device)
+    Mv = torch.empty(n, dtype=torch.float32, device=device)
+    Bq = torch.empty(n, dtype=torch.float32, device=device)
+    qnn.q_fold_epilogue(n, "s8", 0, cs, 1.0, torch.ones(n, dtype=torch.float32, device=device), 2.0 ** 21,
+                        zp_term=zp, M=Mv, Bq=Bq)
+    C = torch.empty((n, n), dtype=torch.uint8, device=device)
+    epi = qnn.epilogue("requant", zp_term=zp, M=Mv, Bq=Bq, out_dt="s8")
+    ws = torch.empty(qnn.qnn_gemm_workspace_bytes(n, n), dtype=torch.uint8, device=device)
+    t = time_steps(torch, lambda: qnn.qgemm_s8(A, "s8", Bp, n, n, n, epi, C, workspace=ws, stream=stream),
+                   max(3, min(steps, 10)), 3, flush, stream)
+    ms = statistics.median(t)
+    tops = 2.0 * n ** 3 / (ms * 1e-3) / 1e12
+    out["square_16384"] = {"M": n, "N": n, "K": n, "ms": round(ms, 4), "TOPS": round(tops, 2),
+                           "frac_f16_peak": round(tops / peak, 4)}
+    del A, Bp, C, ws
+
+
 def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
     out = {}
     hbm = float(pk["hbm_gbs"])
@@ -474,7 +509,18 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
     gbs = 5.0 * R * Cc / (ms * 1e-3) / 1e9
     out["dequantize_rows_1GiB"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
                                    "frac_hbm": round(gbs / hbm, 4)}
-    del x, q, scale
+    # pack fp32 -> u4 (asymmetric, zero point 8, per row), two codes per byte: 4.5 B/elem
+    q4 = torch.empty((R, Cc // 2), dtype=torch.uint8, device=device)
+    s4 = (scale * (127.0 / 7.5)).contiguous()
+    z4 = torch.full((R,), 8, dtype=torch.int32, device=device)
+    p4 = qnn.qparams("asym", scale=s4, zero_point=z4, per_channel=True, axis=0)
+    t = time_steps(torch, lambda: qnn.q_quantize(x, q4, "u4", p4, stream=stream), steps, 3, flush,
+                   stream)
+    ms = statistics.median(t)
+    gbs = 4.5 * R * Cc / (ms * 1e-3) / 1e9
+    out["pack_u4_rows_1GiB"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                "frac_hbm": round(gbs / hbm, 4), "bytes": "4.5 B/elem (4 read, 0.5 write)"}
+    del x, q, q4, scale, s4, z4
 
     def gemm_entry(name, w, a_dt, alpha=None):
         Mm, Kk = w["A"].shape
@@ -512,6 +558,7 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
         del xq, Aq
     for n in (2048, 4096, 8192):
         gemm_entry(f"square_{n}", workloads.gemm_square(n), "s8")
+    square_16384(torch, qnn, workloads, device, flush, stream, peak, steps, out)
 
     def conv_entry(name, w, geom):
         Nb, H, W, C, OC, F, pad, st = geom
@@ -800,6 +847,104 @@ def cpu_baseline_gemm(w, target_s=15.0):
                       f"{dt:.1f} s; scaled to the metric's unit"}
 
 
+def oracle_table(gpu_ms):
+    """The oracle on the host cores for each workload: single-threaded and with
+    OpenMP on every core available to the process (over output rows, pixels or
+    channels).  Timed in full where the run is short enough; the largest GEMMs
+    run on a leading sample of output rows and the time is scaled by the row
+    count ("extrapolated").  gpu_ms: the GPU's time per call for the speedup."""
+    from oracle import oracle
+    from integer_quantized_nn_gb300 import workloads
+    oracle.build()
+    ncores = oracle.get_threads()
+    out = {"cores": ncores, "entries": {}}
+
+    def timed(fn, threads):
+        oracle.set_threads(threads)
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    def record(name, work, unit, fn_rows, total_rows, rows_1, rows_n):
+        e = {"work": work, "unit": unit}
+        for tag, threads, rows in (("1thread", 1, rows_1), ("ncore", ncores, rows_n)):
+            rows = min(rows, total_rows)
+            dt = timed(lambda: fn_rows(rows), threads) * total_rows / rows
+            e[f"s_{tag}"] = round(dt, 3)
+            e[f"{unit}_{tag}"] = round(work / dt / (1e12 if unit == "TOPS" else 1e9), 6)
+            e[f"timed_{tag}"] = ("full" if rows == total_rows else
+                                 f"extrapolated from the first {rows} of {total_rows} output rows")
+        if name in gpu_ms:
+            e["gpu_ms"] = gpu_ms[name]
+            e["gpu_speedup_vs_ncore"] = round(e["s_ncore"] * 1e3 / gpu_ms[name], 1)
+        out["entries"][name] = e
+
+    def gemm(name, A, B, z_a, alpha, s_a, s_w, s_o, bias, rows_1, rows_n):
+        B32 = B.astype(np.int32)
+        _, Mo, Bqo, _ = oracle.fold(oracle.colsum(B32), z_a, s_a, s_w, s_o, bias)
+
+        def fn(r):
+            oracle.requant(oracle.gemm_acc(A[:r], B32, z_a, alpha), Mo, Bqo, "s8")
+        record(name, 2.0 * A.shape[0] * B.shape[0] * B.shape[1], "TOPS", fn, A.shape[0], rows_1, rows_n)
+
+    w = workloads.gemm_sym()
+    gemm("gemm_sym_256", w["A"].astype(np.int32), w["B"], 0, None, 1.0, w["s_w"], 1024.0, None, 256, 256)
+    w = workloads.vit_fc1()
+    gemm("vit_fc1", w["A"].astype(np.int32), w["B"], 128, None, w["s_a"], w["s_w"], w["s_o"], w["bias"],
+         1024, 12608)
+    for nm, (Kk, Nn) in workloads.VITL_SHAPES.items():
+        v = workloads.vitl_ptf(M=12608, K=Kk, N=Nn)
+        A = oracle.quantize(v["x"], oracle.SYM, "s8", scale=v["in_scale"], per_channel=True, axis=1)
+        full = nm == "proj"
+        gemm(f"vitl_{nm}_ptf", A, v["B"], 0, v["alpha"], v["s"], v["s_w"], v["s_o"], v["bias"],
+             12608 if full else 64, 12608 if full else 64)
+        del v, A
+    for n, r1 in ((2048, 64), (4096, 64), (8192, 16), (16384, 8)):
+        if n <= 8192:
+            w = workloads.gemm_square(n)
+            A, B = w["A"][:64].astype(np.int32), w["B"]
+        else:
+            g = np.random.default_rng(5160)
+            A = g.integers(-128, 128, size=(64, n), dtype=np.int8).astype(np.int32)
+            B = g.integers(-128, 128, size=(n, n), dtype=np.int8)
+        e = int(math.ceil(math.log2(n))) + 7
+        B32 = B.astype(np.int32)
+        _, Mo, Bqo, _ = oracle.fold(oracle.colsum(B32), 0, 1.0, np.ones(n, np.float32), float(2.0 ** e))
+
+        def fn(r, A=A, B32=B32, Mo=Mo, Bqo=Bqo):
+            oracle.requant(oracle.gemm_acc(A[:r], B32, 0), Mo, Bqo, "s8")
+        record(f"square_{n}", 2.0 * n ** 3, "TOPS", fn, n, r1, 64)
+        del A, B, B32
+
+    def conv(name, w, geom):
+        Nb, H, W, C, OC, F, pad, st = geom
+        Ic = oracle.unpack_nibbles(w["I"], signed=False)
+        Wc = oracle.unpack_nibbles(w["W"], signed=True)
+        _, Mo, Bqo, _ = oracle.fold(oracle.colsum(Wc.reshape(OC, -1)), w["z_in"], w["s_a"], w["s_w"], w["s_o"],
+                                    w["bias"])
+        OH = (H + 2 * pad - F) // st + 1
+        OW = (W + 2 * pad - F) // st + 1
+        res = None if w["res"] is None else oracle.unpack_nibbles(w["res"], signed=False).reshape(-1, OC)
+        R = float(np.float32(np.float32(w["s_r"]) / np.float32(w["s_o"])))
+
+        def fn(nimg):
+            acc = oracle.conv_acc_direct(Ic[:nimg], Wc, w["z_in"], (pad, pad), (st, st))
+            rr = None if res is None else res[:nimg * OH * OW]
+            oracle.requant(acc, Mo, Bqo, "u4", relu=True, res=rr, z_res=w["z_res"], R=R)
+        record(name, 2.0 * Nb * OH * OW * OC * C * F * F, "TOPS", fn, Nb, Nb, Nb)
+
+    conv("conv3x3_u4s4_add_relu", workloads.conv_u4(), (64, 56, 56, 64, 64, 3, 1, 1))
+    conv("conv1x1_u4s4_relu", workloads.conv_u4(C=256, OC=64, F=1, pad=0, residual=False, tag=1),
+         (64, 56, 56, 256, 64, 1, 0, 1))
+
+    q = workloads.quant_rows()
+    record("quantize_rows_1GiB", 5.0 * q["x"].size, "GB/s",
+           lambda r: oracle.quantize(q["x"][:r], oracle.SYM, "s8", scale=q["scale"][:r], per_channel=True, axis=0),
+           q["x"].shape[0], q["x"].shape[0], q["x"].shape[0])
+    oracle.set_threads(ncores)
+    return out
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     ws, rank, _ = dist_env()
@@ -861,6 +1006,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-oracle-table", action="store_true",
+                    help="skip the per-workload single-thread / all-core oracle timings")
     ap.add_argument("--fused", action="store_true",
                     help="--case GEMMs / convs: no workspace (A re-encoded inside the kernel)")
     ap.add_argument("--case", default=None,

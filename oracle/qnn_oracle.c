@@ -104,6 +104,7 @@ int oracle_quantize(const float *x, int64_t outer, int64_t C, int64_t inner,
                     int32_t qmax, int32_t *q)
 {
     if (scheme < OR_SYM || scheme > OR_POW2) return OR_ERR_ARG;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int64_t o = 0; o < outer; ++o) {
         for (int64_t c = 0; c < C; ++c) {
             int64_t ch = per_channel ? c : 0;
