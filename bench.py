@@ -165,7 +165,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ GPU arm
-def gpu_setup_gemm(torch, qnn, w, a_dt, device):
+def gpu_setup_gemm(torch, qnn, w, a_dt, device, ptf=None):
     A = torch.from_numpy(np.ascontiguousarray(w["A"])).to(device)
     B = torch.from_numpy(np.ascontiguousarray(w["B"])).to(device)
     N, K = w["B"].shape
@@ -174,7 +174,10 @@ def gpu_setup_gemm(torch, qnn, w, a_dt, device):
     off = (-buf.data_ptr()) % 1024
     Bp = buf[off:off + nb]
     colsum = torch.empty(N, dtype=torch.int32, device=device)
-    qnn.qgemm_prepack_b(B, Bp, colsum)
+    if ptf is None:
+        qnn.qgemm_prepack_b(B, Bp, colsum)
+    else:
+        qnn.qgemm_prepack_b_ptf(B, ptf, Bp, colsum)
     sw = torch.from_numpy(np.asarray(w["s_w"], np.float32)).to(device)
     bias = None if w.get("bias") is None else torch.from_numpy(w["bias"]).to(device)
     zp = torch.empty(N, dtype=torch.int32, device=device)
@@ -522,16 +525,16 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
                                 "frac_hbm": round(gbs / hbm, 4), "bytes": "4.5 B/elem (4 read, 0.5 write)"}
     del x, q, q4, scale, s4, z4
 
-    def gemm_entry(name, w, a_dt, alpha=None):
+    def gemm_entry(name, w, a_dt, alpha=None, ptf_in_weights=False):
         Mm, Kk = w["A"].shape
         Nn = w["B"].shape[0]
-        g = gpu_setup_gemm(torch, qnn, w, a_dt, device)
-        C = torch.empty((Mm, Nn), dtype=torch.uint8, device=device)
         al = None
         if alpha is not None:
             al = torch.from_numpy(alpha.astype(np.uint8)).to(device)
+        g = gpu_setup_gemm(torch, qnn, w, a_dt, device, ptf=al if ptf_in_weights else None)
+        C = torch.empty((Mm, Nn), dtype=torch.uint8, device=device)
         epi = qnn.epilogue("requant", zp_term=None if al is not None else g["zp"], M=g["M"],
-                           Bq=g["Bq"], ptf_shift=al,
+                           Bq=g["Bq"], ptf_shift=None if ptf_in_weights else al,
                            ptf_max_shift=0 if alpha is None else int(alpha.max()))
         ws = torch.empty(qnn.qnn_gemm_workspace_bytes(Mm, Kk), dtype=torch.uint8, device=device)
         t = time_steps(torch, lambda: qnn.qgemm_s8(g["A"], a_dt, g["Bp"], Mm, Nn, Kk, epi, C,
@@ -554,7 +557,11 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
                                                  per_channel=True, axis=1))
         w2 = dict(A=Aq.cpu().numpy(), B=w["B"], s_w=w["s_w"], bias=w["bias"], s_a=w["s"],
                   s_o=w["s_o"], z_a=0)
-        gemm_entry(f"vitl_{nm}_ptf", w2, "s8", alpha=w["alpha"])
+        # the layer's PTF factors folded into its weights at prepack (qgemm_prepack_b_ptf)
+        gemm_entry(f"vitl_{nm}_ptf", w2, "s8", alpha=w["alpha"], ptf_in_weights=True)
+        if nm == "fc2":
+            # the same factors applied to the activations by the A pre-pass
+            gemm_entry(f"vitl_{nm}_ptf_on_activations", w2, "s8", alpha=w["alpha"])
         del xq, Aq
     for n in (2048, 4096, 8192):
         gemm_entry(f"square_{n}", workloads.gemm_square(n), "s8")
@@ -730,11 +737,11 @@ def run_case(args):
             a_dt, alpha = "s8", v["alpha"]
         Mm, Kk = w["A"].shape
         Nn = w["B"].shape[0]
-        g = gpu_setup_gemm(torch, qnn, w, a_dt, device)
-        C = torch.empty((Mm, Nn), dtype=torch.uint8, device=device)
         al = None if alpha is None else torch.from_numpy(alpha.astype(np.uint8)).to(device)
+        g = gpu_setup_gemm(torch, qnn, w, a_dt, device, ptf=al)
+        C = torch.empty((Mm, Nn), dtype=torch.uint8, device=device)
         epi = qnn.epilogue("requant", zp_term=None if al is not None else g["zp"], M=g["M"], Bq=g["Bq"],
-                           ptf_shift=al, ptf_max_shift=0 if alpha is None else int(alpha.max()))
+                           ptf_max_shift=0 if alpha is None else int(alpha.max()))
         ws = None if getattr(args, "fused", False) else torch.empty(qnn.qnn_gemm_workspace_bytes(Mm, Kk), dtype=torch.uint8,
                                                  device=device)
         fn = lambda: qnn.qgemm_s8(g["A"], a_dt, g["Bp"], Mm, Nn, Kk, epi, C, workspace=ws,  # noqa: E731

@@ -90,9 +90,29 @@ size_t qnn_gemm_packed_b_bytes(int N, int K);
  * channel n, input channel k) into the GEMM kernel's shared-memory operand
  * image (`B_packed`, qnn_gemm_packed_b_bytes bytes, 1024-byte aligned), and
  * write colsum[n] = sum_k B[n][k] (int32 [N]), the weight sums that the
- * zero-point cross term needs [MG 緩解精度下降].  K must be a multiple of 16. */
+ * zero-point cross term needs [MG 緩解精度下降].  K must be a multiple of 16.
+ * The image ends with a small trailer of bounds on the weight magnitudes (per
+ * K step of 64 and per column); the GEMM reads it to size the runs of K over
+ * which its fp32 partial sums stay exact integers, so a B_packed must come
+ * from one of the prepack calls for the same N and K (a GEMM given a trailer
+ * that does not match its K reports QNN_ERR_INVALID_ARG through
+ * qnn_check_device_error). */
 qnn_status qgemm_prepack_b(const int8_t *B, int N, int K, void *B_packed, int32_t *colsum,
                            qnn_stream_t stream);
+
+/* Prepack int8 weights with per-input-channel Power-of-Two Factors folded in
+ * [FQ 3.2: the activation codes x_q of a PTF quantizer enter the next layer as
+ * x_q * 2^alpha_k; since sum_k (a_k 2^alpha_k) B[n][k] = sum_k a_k (B[n][k]
+ * 2^alpha_k), the factor can ride on the constant operand]: the image holds
+ * B[n][k] * 2^ptf_shift[k] (|.| <= 1024, exact in fp16) and colsum[n] =
+ * sum_k B[n][k] 2^ptf_shift[k].  ptf_shift: device u8 [K], every value 0..3 (a
+ * larger one is reported as QNN_ERR_INVALID_ARG by qnn_check_device_error).
+ * Call qgemm_s8 with the UNSHIFTED activation codes, epi->ptf_shift = NULL and
+ * epi->ptf_max_shift = the largest shift: the result is exactly that of
+ * epi->ptf_shift = ptf_shift on plain weights, without the per-call shift of
+ * A. */
+qnn_status qgemm_prepack_b_ptf(const int8_t *B, const uint8_t *ptf_shift, int N, int K, void *B_packed,
+                               int32_t *colsum, qnn_stream_t stream);
 
 /* Fold the per-output-channel constants ahead of inference [MG 緩解精度下降:
  * the zero-point part that does not depend on the input is computed before
@@ -144,7 +164,11 @@ typedef struct {
     const uint8_t *ptf_shift;/* device [K] per-input-channel Power-of-Two Factor
                                 alpha_k [FQ 3.2]: the GEMM uses A[m][k] * 2^alpha_k;
                                 S8 activations with z_a = 0 only; NULL: none */
-    int32_t ptf_max_shift;   /* upper bound (0..3) on every ptf_shift value */
+    int32_t ptf_max_shift;   /* upper bound (0..3) on every shift: of ptf_shift, or,
+                                with ptf_shift NULL, of the shifts folded into the
+                                weights by qgemm_prepack_b_ptf (0: none).  A shift
+                                byte above it is reported as QNN_ERR_INVALID_ARG
+                                by qnn_check_device_error. */
     const float *row_scale;  /* device [rows] per-row activation scales (dynamic per-token
                                 quantization, q_quantize_rows_dynamic), or NULL: the
                                 per-channel factor is first scaled by the row's,
@@ -162,6 +186,10 @@ size_t qnn_gemm_workspace_bytes(int M, int K);
 /* Quantized GEMM [QI 量化矩阵乘; MG 緩解精度下降]:
  *   acc[m][n] = sum_k (A[m][k] - c_a) * 2^alpha_k * B[n][k]   exact, in int32
  * then the epilogue above with zp_term folded by q_fold_epilogue.
+ * The products run on fp16 tensor cores with fp32 partial sums, which are exact
+ * integers while they stay within 2^24: K is summed in runs no longer than the
+ * weight magnitudes recorded at prepack allow (every K at once when
+ * 128 * 2^(A's shift) * max_n sum_k |B'[n][k]| <= 2^24), the runs added in int32.
  * A: device [M, K] row-major codes of a_dt (S8 or U8); K % 16 == 0.
  * B_packed: from qgemm_prepack_b for the same N, K.
  * C: device [M, N] row-major, of out_dt (REQUANT), fp32 (DEQUANT) or int32 (S32).
@@ -433,8 +461,11 @@ qnn_status q_layout_nchw64(const void *src, int to_nchw64, int N, int H, int W, 
 const char *qnn_status_string(qnn_status s);
 
 /* Synchronises `stream`, then reports and clears the device status word that
- * kernels set when a bounded wait gives up (QNN_ERR_TIMEOUT), or QNN_ERR_CUDA
- * if the stream holds a CUDA error. */
+ * kernels set when a bounded wait gives up (QNN_ERR_TIMEOUT) or a device-side
+ * argument check fails (QNN_ERR_INVALID_ARG: a Power-of-Two-Factor shift above
+ * its stated bound; a GEMM weight image whose trailer does not match its K, or
+ * whose values need more exact runs than the kernel was launched for), or
+ * QNN_ERR_CUDA if the stream holds a CUDA error. */
 qnn_status qnn_check_device_error(qnn_stream_t stream);
 
 /* Launches one block that waits on a barrier nothing arrives at, giving up

@@ -97,6 +97,7 @@ extern "C" qnn_status qnn_check_device_error(qnn_stream_t stream)
         if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return QNN_ERR_CUDA;
         if (v & qnn::kStatusTimeout) return QNN_ERR_TIMEOUT;
+        if (v & qnn::kStatusBadArg) return QNN_ERR_INVALID_ARG;
     }
     return QNN_OK;
 }

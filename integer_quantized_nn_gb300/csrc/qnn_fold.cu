@@ -1,7 +1,8 @@
 // qnn_fold.cu -- work done once per weight tensor, ahead of inference:
 // prepacking the GEMM weight operand (s8; u8 centred at 128; u8 less per-row
-// zero points for the u8 conv filters), the weight column sums and the folded
-// epilogue constants.
+// zero points for the u8 conv filters; s8 times per-input-channel
+// Power-of-Two Factors), its trailer of magnitude bounds, the weight column
+// sums and the folded epilogue constants.
 //
 // Folding [MG 緩解精度下降: the zero-point part that does not depend on the
 // input is computed before inference; QI 量化乘法: scale_abc = s_a s_b / s_c is
@@ -11,31 +12,46 @@
 #include <cstdint>
 #include "qnn_gemm_layout.h"
 #include "qnn_internal.h"
+#include "qnn_ptx.cuh"
 
 namespace qnn {
 namespace {
 
-// One thread per 16-byte chunk of the packed image.  MODE says what B holds and
-// which value of each code goes into the image:
+// What B holds and which value of each code goes into the image (MODE):
 //   kPackS8   : s8 codes, as they are;
 //   kPackU8   : u8 codes, centred: w - 128 (the byte with its top bit flipped, read as s8);
-//   kPackU8Zw : u8 codes less their row's zero point: w - z_w[n], in [-255, 255].
-// All are integers of at most 255 in magnitude, exact in fp16.
-constexpr int kPackS8 = 0, kPackU8 = 1, kPackU8Zw = 2;
+//   kPackU8Zw : u8 codes less their row's zero point: w - z_w[n], in [-255, 255];
+//   kPackPtf  : s8 codes times the Power-of-Two Factor of their input channel,
+//               w * 2^alpha[k] [FQ 3.2: the activation codes are multiplied by
+//               2^alpha before the product; the factor is moved onto the
+//               constant operand, sum_k (a_k 2^alpha_k) w_k = sum_k a_k (w_k 2^alpha_k)],
+//               |w 2^alpha| <= 1024 for alpha <= 3.
+// All are integers of at most 2048 in magnitude, exact in fp16.
+constexpr int kPackS8 = 0, kPackU8 = 1, kPackU8Zw = 2, kPackPtf = 3;
+
+struct PackSrc {
+    const int8_t *B;       // [N, K] codes
+    const int32_t *z_w;    // kPackU8Zw: [N]
+    const uint8_t *ptf;    // kPackPtf: [K] shifts (validated by trailer_kernel; 0..3)
+    int N, K;
+};
 
 template <int MODE>
-__device__ __forceinline__ int packed_code(const int8_t *B, int64_t idx, const int32_t *z_w, int n)
+__device__ __forceinline__ int packed_code(const PackSrc &s, int n, int k)
 {
-    if constexpr (MODE == kPackS8) return B[idx];
-    else if constexpr (MODE == kPackU8) return (int8_t)(B[idx] ^ 0x80);
-    else return (int)(uint8_t)B[idx] - z_w[n];
+    const int64_t idx = (int64_t)n * s.K + k;
+    if constexpr (MODE == kPackS8) return s.B[idx];
+    else if constexpr (MODE == kPackU8) return (int8_t)(s.B[idx] ^ 0x80);
+    else if constexpr (MODE == kPackU8Zw) return (int)(uint8_t)s.B[idx] - s.z_w[n];
+    else return (int)s.B[idx] * (1 << (s.ptf[k] & 15u));
 }
 
+// One thread per 16-byte chunk of the packed image.
 template <int MODE>
-__global__ void prepack_b_kernel(const int8_t *__restrict__ B, int N, int K, uint8_t *__restrict__ out,
-                                 int64_t nchunks, const int32_t *__restrict__ z_w)
+__global__ void prepack_b_kernel(const PackSrc src, uint8_t *__restrict__ out, int64_t nchunks)
 {
     using namespace gemm;
+    const int N = src.N, K = src.K;
     const int KT = ksteps(K);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -52,8 +68,8 @@ __global__ void prepack_b_kernel(const int8_t *__restrict__ B, int N, int K, uin
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             int v0 = 0, v1 = 0;
-            if (n < N && k0 + 2 * j < K) v0 = packed_code<MODE>(B, (int64_t)n * K + k0 + 2 * j, z_w, n);
-            if (n < N && k0 + 2 * j + 1 < K) v1 = packed_code<MODE>(B, (int64_t)n * K + k0 + 2 * j + 1, z_w, n);
+            if (n < N && k0 + 2 * j < K) v0 = packed_code<MODE>(src, n, k0 + 2 * j);
+            if (n < N && k0 + 2 * j + 1 < K) v1 = packed_code<MODE>(src, n, k0 + 2 * j + 1);
             const uint32_t h0 = __half_as_ushort(__int2half_rn(v0));
             const uint32_t h1 = __half_as_ushort(__int2half_rn(v1));
             w[j] = h0 | (h1 << 16);
@@ -62,17 +78,87 @@ __global__ void prepack_b_kernel(const int8_t *__restrict__ B, int N, int K, uin
     }
 }
 
-// One warp per output channel.
-__global__ void colsum_s8_kernel(const int8_t *__restrict__ B, int N, int K, int32_t *__restrict__ colsum)
+__device__ __forceinline__ int warp_sum(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// The image's trailer (zeroed beforehand): one warp per column n forms the sum
+// of |value| over each K step of 64 and over all of K, and folds them into the
+// trailer's maxima.  With kPackPtf, warp 0 also records the largest shift and
+// flags shifts above 3 (device status word: invalid argument).
+template <int MODE>
+__global__ void trailer_kernel(const PackSrc src, int32_t *__restrict__ tr, uint32_t *status)
+{
+    using namespace gemm;
+    const int warp = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    const int KT = ksteps(src.K);
+    if (warp == 0) {
+        if (MODE == kPackPtf) {
+            int amax = 0;
+            for (int k = lane; k < src.K; k += 32) amax = max(amax, (int)src.ptf[k]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (lane == 0) {
+                if (amax > 3 && status) atomicOr(status, kStatusBadArg);
+                atomicMax(tr + TR_SHIFT_MAX, amax);
+            }
+        }
+        if (lane == 0) {
+            tr[TR_MAGIC] = TRAILER_MAGIC;
+            tr[TR_KT] = KT;
+        }
+    }
+    if (warp >= src.N) return;
+    int32_t smax = 0;
+    int64_t tot = 0;
+    for (int s = 0; s < KT; ++s) {
+        int v = 0;
+        for (int j = lane; j < BK; j += 32) {
+            const int k = s * BK + j;
+            if (k < src.K) v += abs(packed_code<MODE>(src, warp, k));
+        }
+        v = warp_sum(v);
+        smax = max(smax, v);
+        tot += v;
+    }
+    if (lane == 0) {
+        atomicMax(tr + TR_STEP_MAX, smax);
+        atomicMax(tr + TR_TOTAL_MAX, (int32_t)(tot < INT32_MAX ? tot : INT32_MAX));
+    }
+}
+
+// colsum[n] = sum_k of the image values.  One warp per output channel.
+template <int MODE>
+__global__ void colsum_code_kernel(const PackSrc src, int32_t *__restrict__ colsum)
 {
     const int warp = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
-    if (warp >= N) return;
+    if (warp >= src.N) return;
     int32_t s = 0;
-    for (int k = lane; k < K; k += 32) s += B[(int64_t)warp * K + k];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    for (int k = lane; k < src.K; k += 32) s += packed_code<MODE>(src, warp, k);
+    s = warp_sum(s);
     if (lane == 0) colsum[warp] = s;
+}
+
+// Image, then trailer, of B in the form MODE on stream s.
+template <int MODE>
+qnn_status pack_b(const PackSrc &src, void *B_packed, cudaStream_t s)
+{
+    const int64_t nchunks = (int64_t)(gemm::packed_b_image_bytes(src.N, src.K) / 16);
+    int64_t blocks = (nchunks + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    uint8_t *out = static_cast<uint8_t *>(B_packed);
+    prepack_b_kernel<MODE><<<(int)blocks, 256, 0, s>>>(src, out, nchunks);
+    if (launch_status() != QNN_OK) return QNN_ERR_CUDA;
+    int32_t *tr = reinterpret_cast<int32_t *>(out + gemm::packed_b_image_bytes(src.N, src.K));
+    if (cudaMemsetAsync(tr, 0, gemm::TRAILER_BYTES, s) != cudaSuccess) return QNN_ERR_CUDA;
+    const int64_t threads = (int64_t)src.N * 32;
+    trailer_kernel<MODE><<<(int)((threads + 255) / 256), 256, 0, s>>>(src, tr, status_word());
+    return launch_status();
 }
 
 // u8 weights with zero points: colsum[n] = sum_k (B[n][k] - z_w[n]).  One warp per channel.
@@ -120,19 +206,29 @@ extern "C" qnn_status qgemm_prepack_b(const int8_t *B, int N, int K, void *B_pac
     if (K % 16 != 0) return QNN_ERR_ALIGNMENT;
     if ((reinterpret_cast<uintptr_t>(B_packed) & 1023u) != 0) return QNN_ERR_ALIGNMENT;
     if (!qnn::aligned16(B)) return QNN_ERR_ALIGNMENT;
-    const int64_t nchunks = (int64_t)(qnn::gemm::packed_b_bytes(N, K) / 16);
-    int64_t blocks = (nchunks + 255) / 256;
-    if (blocks > 65535) blocks = 65535;
     cudaStream_t s = (cudaStream_t)stream;
-    qnn::prepack_b_kernel<qnn::kPackS8><<<(int)blocks, 256, 0, s>>>(B, N, K, static_cast<uint8_t *>(B_packed),
-                                                                     nchunks, nullptr);
-    if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
-    if (colsum) {
-        const int64_t threads = (int64_t)N * 32;
-        qnn::colsum_s8_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(B, N, K, colsum);
-        return qnn::launch_status();
-    }
-    return QNN_OK;
+    const qnn::PackSrc src{B, nullptr, nullptr, N, K};
+    qnn_status st = qnn::pack_b<qnn::kPackS8>(src, B_packed, s);
+    if (st != QNN_OK || !colsum) return st;
+    const int64_t threads = (int64_t)N * 32;
+    qnn::colsum_code_kernel<qnn::kPackS8><<<(int)((threads + 255) / 256), 256, 0, s>>>(src, colsum);
+    return qnn::launch_status();
+}
+
+extern "C" qnn_status qgemm_prepack_b_ptf(const int8_t *B, const uint8_t *ptf_shift, int N, int K, void *B_packed,
+                                          int32_t *colsum, qnn_stream_t stream)
+{
+    if (!B || !ptf_shift || !B_packed || N <= 0 || K <= 0) return QNN_ERR_INVALID_ARG;
+    if (K % 16 != 0) return QNN_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(B_packed) & 1023u) != 0) return QNN_ERR_ALIGNMENT;
+    if (!qnn::aligned16(B) || !qnn::aligned16(ptf_shift)) return QNN_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    const qnn::PackSrc src{B, nullptr, ptf_shift, N, K};
+    qnn_status st = qnn::pack_b<qnn::kPackPtf>(src, B_packed, s);
+    if (st != QNN_OK || !colsum) return st;
+    const int64_t threads = (int64_t)N * 32;
+    qnn::colsum_code_kernel<qnn::kPackPtf><<<(int)((threads + 255) / 256), 256, 0, s>>>(src, colsum);
+    return qnn::launch_status();
 }
 
 extern "C" qnn_status qgemm_prepack_b_u8(const uint8_t *B, const int32_t *z_w, int N, int K, void *B_packed,
@@ -142,20 +238,13 @@ extern "C" qnn_status qgemm_prepack_b_u8(const uint8_t *B, const int32_t *z_w, i
     if (K % 16 != 0) return QNN_ERR_ALIGNMENT;
     if ((reinterpret_cast<uintptr_t>(B_packed) & 1023u) != 0) return QNN_ERR_ALIGNMENT;
     if (!qnn::aligned16(B) || !qnn::aligned16(z_w)) return QNN_ERR_ALIGNMENT;
-    const int64_t nchunks = (int64_t)(qnn::gemm::packed_b_bytes(N, K) / 16);
-    int64_t blocks = (nchunks + 255) / 256;
-    if (blocks > 65535) blocks = 65535;
     cudaStream_t s = (cudaStream_t)stream;
-    qnn::prepack_b_kernel<qnn::kPackU8><<<(int)blocks, 256, 0, s>>>(reinterpret_cast<const int8_t *>(B), N, K,
-                                                                     static_cast<uint8_t *>(B_packed), nchunks,
-                                                                     nullptr);
-    if (qnn::launch_status() != QNN_OK) return QNN_ERR_CUDA;
-    if (colsum) {
-        const int64_t threads = (int64_t)N * 32;
-        qnn::colsum_u8_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(B, z_w, N, K, colsum);
-        return qnn::launch_status();
-    }
-    return QNN_OK;
+    const qnn::PackSrc src{reinterpret_cast<const int8_t *>(B), z_w, nullptr, N, K};
+    qnn_status st = qnn::pack_b<qnn::kPackU8>(src, B_packed, s);
+    if (st != QNN_OK || !colsum) return st;
+    const int64_t threads = (int64_t)N * 32;
+    qnn::colsum_u8_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(B, z_w, N, K, colsum);
+    return qnn::launch_status();
 }
 
 namespace qnn {
@@ -164,18 +253,12 @@ namespace qnn {
 qnn_status prepack_b_u8_minus_zw(const uint8_t *B, const int32_t *z_w, int N, int K, void *B_packed,
                                  int32_t *colsum, cudaStream_t s)
 {
-    const int64_t nchunks = (int64_t)(gemm::packed_b_bytes(N, K) / 16);
-    int64_t blocks = (nchunks + 255) / 256;
-    if (blocks > 65535) blocks = 65535;
-    prepack_b_kernel<kPackU8Zw><<<(int)blocks, 256, 0, s>>>(reinterpret_cast<const int8_t *>(B), N, K,
-                                                            static_cast<uint8_t *>(B_packed), nchunks, z_w);
-    if (launch_status() != QNN_OK) return QNN_ERR_CUDA;
-    if (colsum) {
-        const int64_t threads = (int64_t)N * 32;
-        colsum_u8_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(B, z_w, N, K, colsum);
-        return launch_status();
-    }
-    return QNN_OK;
+    const PackSrc src{reinterpret_cast<const int8_t *>(B), z_w, nullptr, N, K};
+    qnn_status st = pack_b<kPackU8Zw>(src, B_packed, s);
+    if (st != QNN_OK || !colsum) return st;
+    const int64_t threads = (int64_t)N * 32;
+    colsum_u8_kernel<<<(int)((threads + 255) / 256), 256, 0, s>>>(B, z_w, N, K, colsum);
+    return launch_status();
 }
 }  // namespace qnn
 

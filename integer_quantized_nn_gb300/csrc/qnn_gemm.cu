@@ -11,9 +11,11 @@
 // one: every int8 code (and every PTF-shifted code, |a 2^alpha| <= 1024) is an
 // exact fp16 value, every product is exact in fp32, and an fp32 sum of
 // integers is exact while its magnitude stays <= 2^24.  The K loop is cut into
-// chunks of at most (16 >> ptf_max_shift) steps of 64 (|sum| <= 2^24); each
-// chunk accumulates in its own TMEM buffer and the epilogue warps add the
-// chunk results in int32.  A u8 operand is read as (q - 128) so that every
+// chunks whose partial sums provably stay within 2^24: by default (16 >>
+// ptf_max_shift) steps of 64, or longer as the prepack's trailer certifies from
+// the weight values actually stored (qnn_gemm_layout.h); each chunk
+// accumulates in its own TMEM buffer and the epilogue warps add the chunk
+// results in int32.  A u8 operand is read as (q - 128) so that every
 // operand is in [-128, 127]; the fold puts the 128 back through zp_term.
 // The kernel itself is qnn_mma_kernel.cuh; this file holds the converter of
 // the A rows, the A pre-pass and the host entry point.
@@ -27,6 +29,14 @@
 
 namespace qnn {
 namespace mk {
+
+// Whether any of 16 shift bytes exceeds `bound` (the host's ptf_max_shift, on
+// which the exact-chunk length rests).
+__device__ __forceinline__ bool ptf_bytes_above(uint4 a, uint32_t bound)
+{
+    const uint32_t b4 = bound * 0x01010101u;
+    return (__vcmpgtu4(a.x, b4) | __vcmpgtu4(a.y, b4) | __vcmpgtu4(a.z, b4) | __vcmpgtu4(a.w, b4)) != 0u;
+}
 
 // fp16x2 multipliers 2^alpha for the two alpha bytes selected by `sel`.
 __device__ __forceinline__ uint32_t pow2_half2(uint32_t alpha4, uint32_t sel)
@@ -93,6 +103,7 @@ struct GemmOp : OpBase {
         uint32_t mul[8];
         if (PTF) {
             const uint32_t al[4] = {u.alpha.x, u.alpha.y, u.alpha.z, u.alpha.w};
+            if (ptf_bytes_above(u.alpha, (uint32_t)p.ptf_max)) atomicOr(p.status, kStatusBadArg);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 mul[2 * i] = pow2_half2(al[i], 0x4140u);
@@ -141,7 +152,8 @@ struct GemmPackedOp : OpBase {
 template <bool PTF, bool ROWSUM>
 __global__ void __launch_bounds__(256) pack_a_kernel(const uint8_t *__restrict__ A, int M, int K, int KT,
                                                      int rows_pad, int a_u8, const uint8_t *__restrict__ ptf,
-                                                     uint8_t *__restrict__ out, int32_t *__restrict__ rowsum)
+                                                     uint8_t *__restrict__ out, int32_t *__restrict__ rowsum,
+                                                     int ptf_max, uint32_t *status)
 {
     const int groups = KT * 4;  // 16-code groups per padded row
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
@@ -151,6 +163,7 @@ __global__ void __launch_bounds__(256) pack_a_kernel(const uint8_t *__restrict__
     uint32_t mul[8];
     if (PTF) {
         const uint4 al = (k0 < K) ? ldg_nc_v4(ptf + k0) : make_uint4(0, 0, 0, 0);
+        if (blockIdx.y == 0 && threadIdx.y == 0 && ptf_bytes_above(al, (uint32_t)ptf_max)) atomicOr(status, kStatusBadArg);
         const uint32_t a4[4] = {al.x, al.y, al.z, al.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -254,24 +267,32 @@ static qnn_status gemm_params(const void *A, qnn_dtype a_dt, const void *B_packe
     qnn_status st = setup_epilogue(e, false, p);
     if (st != QNN_OK) return st;
 
-    int shift = 0;
+    // shift: bound on the Power-of-Two-Factor shifts, applied here to A
+    // (ptf_shift) or already folded into the weights (qgemm_prepack_b_ptf:
+    // ptf_shift NULL, ptf_max_shift the bound)
+    if (e->ptf_max_shift < 0 || e->ptf_max_shift > 3) return QNN_ERR_INVALID_ARG;
+    const int shift = e->ptf_max_shift;
     if (e->ptf_shift) {
         if (a_dt != QNN_S8 || e->zp_term) return QNN_ERR_UNSUPPORTED;
-        if (e->ptf_max_shift < 0 || e->ptf_max_shift > 3) return QNN_ERR_INVALID_ARG;
         if (!qnn::aligned16(e->ptf_shift)) return QNN_ERR_ALIGNMENT;
-        shift = e->ptf_max_shift;
         p.ptf = e->ptf_shift;
+        p.ptf_max = shift;
+        p.a_shift = shift;
     }
     // |acc_c| <= K * 255 * 128 * 2^shift must stay inside int32
     if ((int64_t)K * 255 * 128 * (1 << shift) > (int64_t)INT32_MAX) return QNN_ERR_OVERFLOW_RISK;
     p.chunk_steps = qnn::gemm::MAX_EXACT_STEPS >> shift;
     p.nchunks = (p.KT + p.chunk_steps - 1) / p.chunk_steps;
+    p.btrail = reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(B_packed) +
+                                                 qnn::gemm::packed_b_image_bytes(N, K));
     return QNN_OK;
 }
 
-static qnn_status launch_pack_a(const uint8_t *A, int M, int K, int a_u8, const uint8_t *ptf, uint8_t *out,
-                                cudaStream_t s, int32_t *rowsum = nullptr)
+static qnn_status launch_pack_a(const uint8_t *A, int M, int K, int a_u8, const uint8_t *ptf, int ptf_max,
+                                uint8_t *out, cudaStream_t s, int32_t *rowsum = nullptr)
 {
+    uint32_t *status = qnn::status_word();
+    if (!status) return QNN_ERR_CUDA;
     const int KT = qnn::gemm::ksteps(K);
     const int rows_pad = ((M + BM - 1) / BM) * BM;
     const int groups = KT * 4;
@@ -290,11 +311,13 @@ static qnn_status launch_pack_a(const uint8_t *A, int M, int K, int a_u8, const 
     }
     const dim3 grid(gx, gy);
     if (rowsum)
-        pack_a_kernel<false, true><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, nullptr, out, rowsum);
+        pack_a_kernel<false, true><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, nullptr, out, rowsum, 0, status);
     else if (ptf)
-        pack_a_kernel<true, false><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, ptf, out, nullptr);
+        pack_a_kernel<true, false><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, ptf, out, nullptr, ptf_max,
+                                                          status);
     else
-        pack_a_kernel<false, false><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, nullptr, out, nullptr);
+        pack_a_kernel<false, false><<<grid, block, 0, s>>>(A, M, K, KT, rows_pad, a_u8, nullptr, out, nullptr, 0,
+                                                           status);
     return qnn::launch_status();
 }
 
@@ -306,7 +329,7 @@ static qnn_status launch_gemm(Params &p, bool packed, cudaStream_t s)
     if (packed) {
         p.Ap = p.A;
         if (!multi) return launch<GemmPackedOp, 256, false>(p, s);
-        return launch<GemmPackedOp, 128, true>(p, s);
+        return launch<GemmPackedOp, 256, true>(p, s);
     }
     if (!p.ptf) {
         if (!multi) return launch<GemmOp<false>, 256, false>(p, s);
@@ -367,7 +390,7 @@ extern "C" qnn_status qgemm_s8_static_scratch(const void *A, qnn_dtype a_dt, con
     if (!ws) return QNN_ERR_CUDA;
     // nothing has to start at zero: the pre-pass writes every byte the GEMM reads
     cudaStream_t s = (cudaStream_t)stream;
-    st = launch_pack_a(p.A, M, K, p.a_u8, p.ptf, ws, s);
+    st = launch_pack_a(p.A, M, K, p.a_u8, p.ptf, p.ptf_max, ws, s);
     if (st != QNN_OK) return st;
     p.A = ws;
     return launch_gemm(p, true, s);
@@ -384,7 +407,8 @@ extern "C" qnn_status qgemm_pack_a(const void *A, qnn_dtype a_dt, int M, int K, 
     if (!qnn::aligned16(A) || !qnn::aligned16(A_packed) || (ptf_shift && !qnn::aligned16(ptf_shift)))
         return QNN_ERR_ALIGNMENT;
     if (A_packed_bytes < packed_a_bytes(M, K)) return QNN_ERR_INVALID_ARG;
-    return launch_pack_a(static_cast<const uint8_t *>(A), M, K, a_dt == QNN_U8, ptf_shift,
+    // the shift bytes are checked against the largest allowed shift, 3
+    return launch_pack_a(static_cast<const uint8_t *>(A), M, K, a_dt == QNN_U8, ptf_shift, 3,
                          static_cast<uint8_t *>(A_packed), (cudaStream_t)stream);
 }
 
@@ -424,7 +448,7 @@ extern "C" qnn_status qgemm_zw(const void *A, qnn_dtype a_dt, const void *B_pack
     uint8_t *img = static_cast<uint8_t *>(workspace);
     int32_t *rowsum = reinterpret_cast<int32_t *>(img + packed_a_bytes(M, K));
     if (cudaMemsetAsync(rowsum, 0, (size_t)M * 4, s) != cudaSuccess) return QNN_ERR_CUDA;
-    st = launch_pack_a(p.A, M, K, p.a_u8, nullptr, img, s, rowsum);
+    st = launch_pack_a(p.A, M, K, p.a_u8, nullptr, 0, img, s, rowsum);
     if (st != QNN_OK) return st;
     p.A = img;
     p.zw = z_w;
@@ -444,7 +468,7 @@ extern "C" qnn_status qgemm_s8(const void *A, qnn_dtype a_dt, const void *B_pack
     if (workspace_bytes < packed_a_bytes(M, K)) return QNN_ERR_INVALID_ARG;
     if (!qnn::aligned16(workspace)) return QNN_ERR_ALIGNMENT;
     cudaStream_t s = (cudaStream_t)stream;
-    st = launch_pack_a(p.A, M, K, p.a_u8, p.ptf, static_cast<uint8_t *>(workspace), s);
+    st = launch_pack_a(p.A, M, K, p.a_u8, p.ptf, p.ptf_max, static_cast<uint8_t *>(workspace), s);
     if (st != QNN_OK) return st;
     p.A = static_cast<const uint8_t *>(workspace);
     return launch_gemm(p, true, s);

@@ -79,7 +79,14 @@ struct Params {
     // weights (prepacked image) and shape of the GEMM view
     const uint8_t *Bp;
     int M, N, K, KT, num_m, num_tiles;
+    // exact fp32 chunks: chunk_steps K steps each (host bound); with btrail (the
+    // trailer of a prepacked GEMM weight image) the kernel derives the length from
+    // the recorded weight magnitudes instead, for activation codes of magnitude at
+    // most 128 * 2^a_shift
     int chunk_steps, nchunks;
+    const int32_t *btrail;
+    int a_shift;
+    int ptf_max;             // GEMM with ptf: bound the host was given for every shift byte
     // epilogue
     int mode, relu, z_out, out_bits, out_signed;
     float clip_lo_f, clip_hi_f;  // requant: clip of v before rounding and adding z_out (ReLU folded in)
@@ -133,6 +140,8 @@ struct __align__(1024) Smem {
     uint64_t acc_empty[2];
     uint64_t mma_done;
     uint64_t bres_full;
+    uint64_t plan_ready;         // the chunk plan below has been written
+    int32_t plan_steps, plan_count;
     uint32_t tmem_base;
 };
 
@@ -173,6 +182,30 @@ struct UnitCursor {
         }
     }
 };
+
+// Length (K steps) of the exact accumulation chunks and their number per tile.
+// From the weight image's trailer when there is one (the bound certified by the
+// prepack for the values actually stored), else the host's bound.  A trailer
+// that does not belong to this K is reported as an invalid argument.
+struct ChunkPlan {
+    int steps, count;
+};
+
+__device__ __forceinline__ ChunkPlan chunk_plan(const Params &p, bool report)
+{
+    int L = p.chunk_steps;
+    if (p.btrail) {
+        const int32_t magic = __ldg(p.btrail + gemm::TR_MAGIC);
+        const int32_t kt = __ldg(p.btrail + gemm::TR_KT);
+        if (magic == gemm::TRAILER_MAGIC && kt == p.KT) {
+            L = gemm::certified_chunk_steps(__ldg(p.btrail + gemm::TR_STEP_MAX), __ldg(p.btrail + gemm::TR_TOTAL_MAX),
+                                            (int64_t)128 << p.a_shift, p.KT);
+        } else if (report) {
+            atomicOr(p.status, kStatusBadArg);
+        }
+    }
+    return ChunkPlan{L, (p.KT + L - 1) / L};
+}
 
 // A bounded wait whose outcome is the same on every lane of the warp.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t *status)
@@ -344,7 +377,7 @@ __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
 // The issuing loop is kept as short as possible: it is the one serial
 // instruction stream every pipeline unit passes through (one wait, four MMAs,
 // one or two commits, counters instead of divisions).
-template <class Op, int TBN>
+template <class Op, int TBN, bool MULTI>
 __device__ void mma_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32_t tmem)
 {
     constexpr uint32_t IDESC = idesc_f32acc(0, 0, BM, TBN);  // f16 x f16, or e4m3 x e4m3
@@ -359,18 +392,32 @@ __device__ void mma_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32
     if constexpr (Op::RESB) {
         if (units > 0 && !warp_wait(smem_u32(&s.bres_full), 0u, p.status)) return;
     }
+    // The chunk plan (MULTI) is published in shared memory by warp 6 at kernel
+    // start; it is first needed once the first stage has landed, so its global
+    // load does not delay the first MMAs.  One chunk per tile: the two TMEM
+    // accumulators alternate by tile; several: every chunk goes to accumulator 0
+    // and the epilogue keeps the int32 running sums in accumulator 1's columns
+    // (for the first unit both choices are accumulator 0, phase 0).
+    int chunk_steps = p.KT;
+    bool single = true;
     int stage = 0;
     uint32_t sph = 0;  // phase of the current stage's full barrier
     uint32_t u = 0;  // accumulation chunk counter
     int kl = 0;      // unit position within the tile
     int cpos = 0;    // unit position within the accumulation chunk
     for (int j = 0; j < units; ++j) {
-        const uint32_t abuf = u & 1u;
+        const uint32_t abuf = single ? (u & 1u) : 0u;
+        const uint32_t uph = single ? ((u >> 1) & 1u) : (u & 1u);
         const bool first = cpos == 0;
-        const bool last = (cpos == p.chunk_steps - 1) || (kl == p.KT - 1);
-        if (first && !warp_wait(smem_u32(&s.acc_empty[abuf]), ((u >> 1) & 1u) ^ 1u, p.status)) break;
+        if (first && !warp_wait(smem_u32(&s.acc_empty[abuf]), uph ^ 1u, p.status)) break;
         if (!warp_wait(smem_u32(&s.full[stage]), sph, p.status)) break;
         tc_fence_after();
+        if (MULTI && j == 0) {
+            if (!warp_wait(smem_u32(&s.plan_ready), 0u, p.status)) break;
+            chunk_steps = s.plan_steps;
+            single = s.plan_count == 1;
+        }
+        const bool last = (cpos == chunk_steps - 1) || (kl == p.KT - 1);
         if (leader) {
             // descriptor start addresses are in 16-byte units: +2 per 32-byte K slice
             const uint64_t ad = adesc0 + (uint64_t)(stage * ((SUB * BM * ROW) >> 4));
@@ -736,10 +783,67 @@ __device__ __forceinline__ int32_t acc_to_int(uint32_t bits)
     return __float2int_rn(f);
 }
 
-// MULTI == false: one accumulation chunk per tile; each epilogue thread owns
-// one row and TBN / 2 columns, converted and stored 32 at a time from TMEM.
-// MULTI == true : K is cut into exact chunks; each thread keeps int32 sums for
-// its row and TBN / 2 columns in registers across the chunks.
+// One tile whose K fits one accumulation chunk: the thread's row and its
+// warp's columns are converted and stored 32 at a time straight from TMEM
+// (the accumulator buffer is released after the last piece is read).
+template <class Op, int TBN, int COLS>
+__device__ __forceinline__ bool epilogue_stream_tile(const Params &p, Smem<Op, TBN> &s, float *cols,
+                                                     const ColumnRegs<COLS> &cr, int m, int nbase, int npieces,
+                                                     uint32_t taddr0, uint32_t abuf, uint32_t u, int lane)
+{
+    uint32_t rw_next[8];
+    load_residual(p, m, nbase, rw_next);
+    if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return false;
+    tc_fence_after();
+    const bool fast = store_columns<COLS>(cr, cols, lane) && !p.C32 && p.mode != QNN_EPI_S32 && !p.rowsum &&
+                      !p.row_scale;
+#pragma unroll 1
+    for (int jp = 0; jp < npieces; ++jp) {
+        uint32_t rw[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) rw[k] = rw_next[k];
+        if (jp + 1 < npieces) load_residual(p, m, nbase + (jp + 1) * 32, rw_next);
+        uint32_t r[32];
+        tmem_ld32(taddr0 + jp * 32, r);
+        tmem_ld_wait();
+        if (jp == npieces - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
+        }
+        if (fast) {
+            // the fp32 sum is an exact integer (times 2^-SCALE_LOG2); adding the
+            // fp32 -zp_term rounds once, like the int32 -> fp32 conversion
+            const float *cn = cols + 2 * COLS + jp * 32;
+            float a[32];
+#pragma unroll
+            for (int k = 0; k < 32; k += 4) {
+                const float4 nz = *reinterpret_cast<const float4 *>(cn + k);
+                const float z4[4] = {nz.x, nz.y, nz.z, nz.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float f = __uint_as_float(r[k + e]);
+                    a[k + e] = Op::SCALE_LOG2 ? __fmaf_rn(f, (float)(1 << Op::SCALE_LOG2), z4[e])
+                                              : __fadd_rn(f, z4[e]);
+                }
+            }
+            epilogue_float_t<false>(p, m, nbase + jp * 32, a, cols + jp * 32, cols + COLS + jp * 32, rw);
+        } else {
+            int32_t acc[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) acc[k] = acc_to_int<Op::SCALE_LOG2>(r[k]);
+            epilogue_int(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
+                         cols + 3 * COLS + jp * 32, rw);
+        }
+    }
+    return true;
+}
+
+// MULTI == false: one accumulation chunk per tile (epilogue_stream_tile).
+// MULTI == true : K is cut into exact chunks (their number is read at run time,
+// chunk_plan); each thread keeps int32 sums for its row and its warp's columns
+// in registers across the chunks, reading each chunk 16 columns at a time; a
+// plan of one chunk takes the streaming path.
 template <class Op, int TBN, bool MULTI>
 __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, uint32_t tmem)
 {
@@ -755,92 +859,64 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
     float *cols = s.cols[warp >= EPI_WARP0 ? warp - EPI_WARP0 : warp + 8];
     uint32_t u = 0;
     const typename Op::RowInfo ri = Op::row_info(p, quad * 32 + lane);
+    int nch = 1;
+    if constexpr (MULTI) {
+        if (!warp_wait(smem_u32(&s.plan_ready), 0u, p.status)) return;
+        nch = s.plan_count;
+    }
     for (int i = 0; i < my_tiles; ++i) {
         const int t = blockIdx.x + i * gridDim.x;
         const int m = Op::out_row(p, t % p.num_m, ri);
         const int nbase = (t / p.num_m) * TBN + p0 * 32;
         ColumnRegs<COLS> cr;
         load_columns<COLS>(p, cr, nbase, lane);
-        if (!MULTI) {
-            uint32_t rw_next[8];
-            load_residual(p, m, nbase, rw_next);
+        if (nch == 1) {
             const uint32_t abuf = u & 1u;
-            if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
-            tc_fence_after();
-            const bool fast = store_columns<COLS>(cr, cols, lane) && !p.C32 && p.mode != QNN_EPI_S32 && !p.rowsum &&
-                              !p.row_scale;
             const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + p0 * 32;
-#pragma unroll 1
-            for (int jp = 0; jp < npieces; ++jp) {
-                uint32_t rw[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) rw[k] = rw_next[k];
-                if (jp + 1 < npieces) load_residual(p, m, nbase + (jp + 1) * 32, rw_next);
-                uint32_t r[32];
-                tmem_ld32(taddr + jp * 32, r);
-                tmem_ld_wait();
-                if (jp == npieces - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
-                }
-                if (fast) {
-                    // the fp32 sum is an exact integer (times 2^-SCALE_LOG2); adding the
-                    // fp32 -zp_term rounds once, like the int32 -> fp32 conversion
-                    const float *cn = cols + 2 * COLS + jp * 32;
-                    float a[32];
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        const float4 nz = *reinterpret_cast<const float4 *>(cn + k);
-                        const float z4[4] = {nz.x, nz.y, nz.z, nz.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float f = __uint_as_float(r[k + e]);
-                            a[k + e] = Op::SCALE_LOG2 ? __fmaf_rn(f, (float)(1 << Op::SCALE_LOG2), z4[e])
-                                                      : __fadd_rn(f, z4[e]);
-                        }
-                    }
-                    epilogue_float_t<false>(p, m, nbase + jp * 32, a, cols + jp * 32, cols + COLS + jp * 32, rw);
-                } else {
-                    int32_t acc[32];
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) acc[k] = acc_to_int<Op::SCALE_LOG2>(r[k]);
-                    epilogue_int(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
-                                 cols + 3 * COLS + jp * 32, rw);
-                }
-            }
+            if (!epilogue_stream_tile<Op, TBN, COLS>(p, s, cols, cr, m, nbase, npieces, taddr, abuf, u, lane))
+                return;
             ++u;
-        } else {
-            int32_t acc[PIECES][32];
-            for (int c = 0; c < p.nchunks; ++c) {
-                const uint32_t abuf = u & 1u;
-                if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return;
+        } else if constexpr (MULTI) {
+            // every chunk arrives in accumulator 0; its fp32 sums (exact integers)
+            // are added into int32 running sums kept in accumulator 1's columns,
+            // then accumulator 0 is released for the next chunk
+            const uint32_t lanes = (uint32_t)(quad * 32) << 16;
+            const uint32_t fbuf = tmem + lanes + p0 * 32;
+            const uint32_t ibuf = tmem + lanes + TBN + p0 * 32;
+            for (int c = 0; c < nch; ++c) {
+                if (!warp_wait(smem_u32(&s.acc_full[0]), u & 1u, p.status)) return;
                 tc_fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + p0 * 32;
-#pragma unroll
-                for (int jp = 0; jp < PIECES; ++jp) {
-                    if (jp >= npieces) break;
-                    uint32_t r[32];
-                    tmem_ld32(taddr + jp * 32, r);
+#pragma unroll 1
+                for (int q = 0; q < 2 * npieces; ++q) {
+                    uint32_t r[16], t[16];
+                    tmem_ld16(fbuf + q * 16, r);
+                    if (c > 0) tmem_ld16(ibuf + q * 16, t);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
+                    for (int k = 0; k < 16; ++k) {
                         const int32_t v = acc_to_int<Op::SCALE_LOG2>(r[k]);
-                        acc[jp][k] = (c == 0) ? v : acc[jp][k] + v;
+                        r[k] = (uint32_t)(c > 0 ? (int32_t)t[k] + v : v);
                     }
+                    tmem_st16(ibuf + q * 16, r);
                 }
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
+                if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[0]));
                 ++u;
             }
             store_columns<COLS>(cr, cols, lane);
-#pragma unroll
-            for (int jp = 0; jp < PIECES; ++jp) {
-                if (jp >= npieces) break;
+#pragma unroll 1
+            for (int jp = 0; jp < npieces; ++jp) {
                 uint32_t rw[8];
                 load_residual(p, m, nbase + jp * 32, rw);
-                epilogue_int(p, m, nbase + jp * 32, acc[jp], cols + jp * 32, cols + COLS + jp * 32,
+                uint32_t r[32];
+                tmem_ld32(ibuf + jp * 32, r);
+                tmem_ld_wait();
+                int32_t acc[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) acc[k] = (int32_t)r[k];
+                epilogue_int(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
                              cols + 3 * COLS + jp * 32, rw);
             }
         }
@@ -868,6 +944,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
         }
         mbar_init(smem_u32(&s.mma_done), 1);
         mbar_init(smem_u32(&s.bres_full), 1);
+        mbar_init(smem_u32(&s.plan_ready), 1);
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
@@ -913,7 +990,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
     } else if (warp < 8) {
         regs_dec<EPI12 ? REGS_WG1_E12 : REGS_WG1>();
         if (warp == PRODUCER_WARP) producer_role<Op, TBN>(p, s, units);
-        if (warp == MMA_WARP) mma_role<Op, TBN>(p, s, my_tiles, tmem);
+        if (warp == MMA_WARP) mma_role<Op, TBN, MULTI>(p, s, my_tiles, tmem);
+        if (warp == MMA_WARP + 1) {
+            if (lane == 0) {
+                const ChunkPlan plan = chunk_plan(p, blockIdx.x == 0);
+                // a kernel built for one chunk per tile must not be given weights
+                // whose sums need more (they would not be exact): reported, not hidden
+                if (!MULTI && plan.count > 1 && blockIdx.x == 0) atomicOr(p.status, kStatusBadArg);
+                s.plan_steps = plan.steps;
+                s.plan_count = plan.count;
+                mbar_arrive(smem_u32(&s.plan_ready));  // release: the plan's stores are visible to waiters
+            }
+            __syncwarp();
+            if (Op::TMA_A && blockIdx.x == 0 && p.ptf) {
+                // A arrived already multiplied by 2^ptf (the pre-pass): the exact-chunk
+                // length rests on every shift byte being at most ptf_max
+                bool above = false;
+                for (int k = lane; k < p.K; k += 32) above |= __ldg(p.ptf + k) > (uint8_t)p.ptf_max;
+                if (__any_sync(0xffffffffu, above) && lane == 0) atomicOr(p.status, kStatusBadArg);
+            }
+        }
     } else {
         regs_inc<REGS_EPI>();
         epilogue_role<Op, TBN, MULTI>(p, s, my_tiles, tmem);

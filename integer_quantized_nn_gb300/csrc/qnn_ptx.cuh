@@ -6,8 +6,10 @@
 
 namespace qnn {
 
-// Status bits a kernel ORs into the device status word.
+// Status bits a kernel ORs into the device status word: a bounded wait gave up;
+// a device-side argument check failed (a value the host could not see).
 constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusBadArg = 2u;
 
 // A wait that has not completed after this many nanoseconds gives up.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -215,6 +217,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 __device__ __forceinline__ void tmem_ld_wait()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: thread i of the warp writes the 16
+// columns of TMEM lane (lane base + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile stored in the

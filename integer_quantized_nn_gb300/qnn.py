@@ -91,6 +91,7 @@ def _declare(L):
         "q_eltwise_s8": (c_int, [c_int, vp, vp, i64, f32, c_int, vp, vp]),
         "q_quantize_rows_dynamic": (c_int, [vp, i64, i64, c_int, vp, vp, vp]),
         "qgemm_prepack_b_u8": (c_int, [vp, vp, c_int, c_int, vp, vp, vp]),
+        "qgemm_prepack_b_ptf": (c_int, [vp, vp, c_int, c_int, vp, vp, vp]),
         "qnn_gemm_zw_workspace_bytes": (sz, [c_int, c_int]),
         "qgemm_zw": (c_int, [vp, c_int, vp, vp, c_int, c_int, c_int, vp, vp, vp, vp, sz, vp]),
         "q_layout_nchw64": (c_int, [vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, vp]),
@@ -327,6 +328,14 @@ def qgemm_prepack_b_u8(B, z_w, B_packed, colsum=None, stream=None):
     N, K = B.shape
     _check(_SYMBOLS["qgemm_prepack_b_u8"](_ptr(B), _ptr(z_w), N, K, _ptr(B_packed), _ptr(colsum), _stream(stream)),
            "qgemm_prepack_b_u8")
+
+
+def qgemm_prepack_b_ptf(B, ptf_shift, B_packed, colsum=None, stream=None):
+    """s8 weights [N, K] times 2^ptf_shift[k] (u8 [K], each 0..3) folded into the image."""
+    load()
+    N, K = B.shape
+    _check(_SYMBOLS["qgemm_prepack_b_ptf"](_ptr(B), _ptr(ptf_shift), N, K, _ptr(B_packed), _ptr(colsum),
+                                           _stream(stream)), "qgemm_prepack_b_ptf")
 
 
 def qnn_gemm_zw_workspace_bytes(M: int, K: int) -> int:

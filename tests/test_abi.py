@@ -29,6 +29,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("q_quantize", "q_dequantize", "qgemm_prepack_b", "q_fold_epilogue", "qgemm_s8",
               "qnn_gemm_workspace_bytes", "qgemm_pack_a", "qgemm_s8_packed", "qgemm_s8_static_scratch",
+              "qgemm_prepack_b_ptf",
               "qconv_prepack_w", "qconv_u4s4", "qconv_u8s8", "qnn_conv_workspace_bytes",
               "q_log_int_softmax", "q_attn_shift_v", "q_lis_attn_v", "q_int_layernorm", "q_eltwise_s8",
               "q_quantize_rows_dynamic", "qgemm_prepack_b_u8", "qgemm_zw", "qnn_gemm_zw_workspace_bytes",
@@ -246,8 +247,9 @@ def test_conv_u8_zero_point_rejected_on_host(lib):
 
 
 def test_packed_sizes(lib):
-    assert qnn.qnn_gemm_packed_b_bytes(3072, 768) == 12 * 12 * 256 * 128
-    assert qnn.qnn_gemm_packed_b_bytes(300, 272) == 2 * 5 * 256 * 128
+    # the operand image, then a 1 KB trailer of weight magnitude bounds
+    assert qnn.qnn_gemm_packed_b_bytes(3072, 768) == 12 * 12 * 256 * 128 + 1024
+    assert qnn.qnn_gemm_packed_b_bytes(300, 272) == 2 * 5 * 256 * 128 + 1024
     assert qnn.qnn_gemm_packed_b_bytes(0, 16) == 0
 
 

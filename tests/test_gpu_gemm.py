@@ -313,3 +313,115 @@ def test_gemm_back_to_back_on_one_stream(oracle):
     exp = oracle.pack_bytes(oracle.requant(acc, M_o, Bq_o, "s8"))
     assert np.array_equal(host(C), exp)
     assert np.array_equal(host(C2), exp)
+
+
+def _ptf_in_weights(oracle, A, B, alpha, s_a, s_w, s_o, bias, rows=None, mode="requant"):
+    """Power-of-Two Factors folded into the prepacked weights (qgemm_prepack_b_ptf)
+    and the unshifted activation codes: every path must give the oracle's
+    sum_k (A << alpha_k) B exactly, and the column sums sum_k B 2^alpha_k."""
+    t = torch()
+    M, K = A.shape
+    N = B.shape[0]
+    from _util import aligned_empty
+    Bp = aligned_empty(qnn.qnn_gemm_packed_b_bytes(N, K))
+    colsum = t.empty(N, dtype=t.int32, device="cuda")
+    qnn.qgemm_prepack_b_ptf(dev(B), dev(alpha.astype(np.uint8)), Bp, colsum)
+    Bsh = B.astype(np.int32) << alpha.astype(np.int32)[None, :]
+    assert np.array_equal(host(colsum), oracle.colsum(Bsh))
+    zp = t.empty(N, dtype=t.int32, device="cuda")
+    Mv = t.empty(N, dtype=t.float32, device="cuda")
+    Bq = t.empty(N, dtype=t.float32, device="cuda")
+    qnn.q_fold_epilogue(N, "s8", 0, colsum, s_a, dev(np.asarray(s_w, np.float32)), s_o, bias=dev(bias), zp_term=zp,
+                        M=Mv, Bq=Bq, w_per_channel=True)
+    _, M_o, Bq_o, _ = oracle.fold(oracle.colsum(Bsh), 0, s_a, np.asarray(s_w, np.float32), s_o, bias)
+    epi = qnn.epilogue(mode, zp_term=zp, M=Mv, Bq=Bq, out_dt="s8", ptf_max_shift=int(alpha.max()))
+    Ad = dev(A)
+    sel = np.arange(M) if rows is None else rows
+    acc = oracle.gemm_acc(A[sel].astype(np.int32), B.astype(np.int32), 0, alpha.astype(np.int32))
+    exp = oracle.pack_bytes(oracle.requant(acc, M_o, Bq_o, "s8")) if mode == "requant" else acc
+    for path in ("fused", "workspace", "packed"):
+        C = t.full((M, N), 0x5A, dtype=t.uint8 if mode == "requant" else t.int32, device="cuda")
+        ws = t.full((qnn.qnn_gemm_workspace_bytes(M, K),), 0xFF, dtype=t.uint8, device="cuda")
+        if path == "packed":
+            qnn.qgemm_pack_a(Ad, "s8", M, K, ws)
+            qnn.qgemm_s8_packed(ws, "s8", Bp, M, N, K, epi, C)
+        else:
+            qnn.qgemm_s8(Ad, "s8", Bp, M, N, K, epi, C, workspace=None if path == "fused" else ws)
+        assert qnn.qnn_check_device_error() == qnn.QNN_OK, path
+        got = host(C)[sel]
+        assert np.array_equal(got, exp), f"{path}: {(got != exp).sum()} mismatches"
+
+
+def test_gemm_ptf_in_weights(oracle):
+    """FQ-ViT 3.2 Power-of-Two Factor moved onto the weights at prepack: the same
+    integers as shifting the activations, on ragged and multi-step shapes."""
+    w = workloads.vitl_ptf(M=300, K=512, N=256)
+    codes = oracle.quantize(w["x"], 0, "s8", scale=w["in_scale"], per_channel=True, axis=1).astype(np.int8)
+    _ptf_in_weights(oracle, codes, w["B"], w["alpha"], w["s"], w["s_w"], w["s_o"], w["bias"])
+    rng = np.random.default_rng(30)
+    M, N, K = 389, 300, 1088
+    A = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    B = rng.integers(-128, 128, size=(N, K)).astype(np.int8)
+    al = rng.integers(0, 4, size=K)
+    _ptf_in_weights(oracle, A, B, al, 0.02, rng.uniform(1e-3, 1e-2, N), 3.0, rng.normal(0, 1, N).astype(np.float32))
+    # extreme values: every product 128 * 1024, every exact run two K steps long
+    A2 = np.full((256, 1024), -128, np.int8)
+    B2 = np.full((256, 1024), -128, np.int8)
+    _ptf_in_weights(oracle, A2, B2, np.full(1024, 3), 1.0, np.ones(256), 2.0 ** 30, np.zeros(256, np.float32),
+                    mode="s32")
+
+
+@pytest.mark.parametrize("name", ["qkv", "fc2"])
+def test_gemm_vitl_ptf_in_weights_sampled(oracle, name):
+    """ViT-L GEMMs at full size with the PTF factors folded into the weights;
+    160 sampled rows compared with the oracle."""
+    K, N = workloads.VITL_SHAPES[name]
+    w = workloads.vitl_ptf(M=12608, K=K, N=N)
+    A = oracle.quantize(w["x"], 0, "s8", scale=w["in_scale"], per_channel=True, axis=1).astype(np.int8)
+    rows = np.unique(np.concatenate([np.arange(0, 16), np.arange(12608 - 80, 12608),
+                                     np.random.default_rng(31).choice(12608, 64, replace=False)]))
+    _ptf_in_weights(oracle, A, w["B"], w["alpha"], w["s"], w["s_w"], w["s_o"], w["bias"], rows=rows)
+
+
+def test_gemm_device_argument_checks():
+    """Conditions only the device can see are reported by qnn_check_device_error
+    as QNN_ERR_INVALID_ARG: a PTF shift byte above ptf_max_shift (fused, pre-pass
+    and two-call paths); a prepack shift above 3; weights whose folded factors
+    need more exact runs than the launch was planned for; a weight image whose
+    trailer belongs to another K."""
+    t = torch()
+    from _util import aligned_empty
+    M, N, K = 256, 256, 1024
+    A = t.full((M, K), -128, dtype=t.int8, device="cuda")
+    B = t.full((N, K), -128, dtype=t.int8, device="cuda")
+    Bp = aligned_empty(qnn.qnn_gemm_packed_b_bytes(N, K))
+    qnn.qgemm_prepack_b(B, Bp, None)
+    C = t.empty((M, N), dtype=t.int32, device="cuda")
+    ws = t.empty(qnn.qnn_gemm_workspace_bytes(M, K), dtype=t.uint8, device="cuda")
+    al = t.zeros(K, dtype=t.uint8, device="cuda")
+    al[700] = 3
+    epi = qnn.epilogue("s32", ptf_shift=al, ptf_max_shift=1)
+    assert qnn.qnn_check_device_error() == qnn.QNN_OK
+    for wsp in (None, ws):
+        qnn.qgemm_s8(A, "s8", Bp, M, N, K, epi, C, workspace=wsp)
+        assert qnn.qnn_check_device_error() == qnn.QNN_ERR_INVALID_ARG
+    qnn.qgemm_pack_a(A, "s8", M, K, ws, ptf_shift=al)
+    assert qnn.qnn_check_device_error() == qnn.QNN_OK
+    qnn.qgemm_s8_packed(ws, "s8", Bp, M, N, K, epi, C)
+    assert qnn.qnn_check_device_error() == qnn.QNN_ERR_INVALID_ARG
+    # shifts folded into the weights: a bound of 0 launches the one-run kernel,
+    # which finds that these weights need runs of two K steps
+    Bf = aligned_empty(qnn.qnn_gemm_packed_b_bytes(N, K))
+    qnn.qgemm_prepack_b_ptf(B, t.full((K,), 3, dtype=t.uint8, device="cuda"), Bf, None)
+    assert qnn.qnn_check_device_error() == qnn.QNN_OK
+    for wsp in (None, ws):
+        qnn.qgemm_s8(A, "s8", Bf, M, N, K, qnn.epilogue("s32"), C, workspace=wsp)
+        assert qnn.qnn_check_device_error() == qnn.QNN_ERR_INVALID_ARG
+        qnn.qgemm_s8(A, "s8", Bf, M, N, K, qnn.epilogue("s32", ptf_max_shift=3), C, workspace=wsp)
+        assert qnn.qnn_check_device_error() == qnn.QNN_OK
+        assert bool((C == 1024 * 128 * 1024).all())
+    qnn.qgemm_prepack_b_ptf(B, t.full((K,), 4, dtype=t.uint8, device="cuda"), Bf, None)
+    assert qnn.qnn_check_device_error() == qnn.QNN_ERR_INVALID_ARG
+    # an image prepacked for K = 1024 used as K = 512 (in bounds: a smaller view)
+    qnn.qgemm_s8(A[:, :512].contiguous(), "s8", Bp, M, N, 512, qnn.epilogue("s32"), C)
+    assert qnn.qnn_check_device_error() == qnn.QNN_ERR_INVALID_ARG
