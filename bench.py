@@ -712,7 +712,15 @@ def run_case(args):
         flush_buf.fill_(1)
 
     case = args.case
-    if case == "quantize":
+    if case == "dequantize":
+        R = Cc = 16384
+        x = workloads.device_normal_f32((R, Cc), 505, device)
+        scale = (x.abs().amax(dim=1) / 127.0).contiguous()
+        q = torch.empty((R, Cc), dtype=torch.uint8, device=device)
+        p = qnn.qparams("sym", scale=scale, per_channel=True, axis=0)
+        qnn.q_quantize(x, q, "s8", p, stream=stream)
+        fn = lambda: qnn.q_dequantize(q, "s8", x, p, stream=stream)  # noqa: E731
+    elif case == "quantize":
         R = Cc = 16384
         x = workloads.device_normal_f32((R, Cc), 505, device)
         scale = (x.abs().amax(dim=1) / 127.0).contiguous()
@@ -1018,7 +1026,7 @@ def main():
     ap.add_argument("--fused", action="store_true",
                     help="--case GEMMs / convs: no workspace (A re-encoded inside the kernel)")
     ap.add_argument("--case", default=None,
-                    help="run one workload only (profiling): quantize, vit_fc1, square_4096, "
+                    help="run one workload only (profiling): quantize, dequantize, vit_fc1, square_4096, "
                          "vitl_fc2, conv3x3, conv1x1, gemm:M:N:K (u8 x s8 -> s8), lis, shift, "
                          "attn (ViT-B b64 Log-Int-Softmax, shift product, both), fused (both in one kernel), layernorm, "
                          "eltwise, dynquant, conv_u8zw (3x3 u8 x u8 filters with zero points), "

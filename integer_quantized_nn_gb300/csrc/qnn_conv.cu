@@ -112,6 +112,7 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // bytes), so D - 1 units of loads are in flight while one is converted.
 template <int ELEM_BITS, int GROUP_ELEMS, int STEP_ELEMS, int D>
 struct ConvStaging : OpBase {
+    static constexpr bool CACHE_COLS = true;
     static constexpr int DEPTH = D;
     static constexpr int DEPTH_MULTI = D;
     static constexpr int STG_BYTES = D * 4 * 128 * 16;
@@ -171,6 +172,7 @@ struct ConvStaging : OpBase {
 // (padding and zero rows are resolved when the unit is loaded).
 template <int ELEM_BITS, int GROUP_ELEMS, int STEP_ELEMS>
 struct ConvRegRing : OpBase {
+    static constexpr bool CACHE_COLS = true;
     static constexpr int DEPTH = 4;
     static constexpr int DEPTH_MULTI = 3;
     static constexpr int STG_BYTES = 16;  // no staging ring
@@ -244,6 +246,144 @@ struct ConvU4Op : ConvFetch<4, 32, 128, D> {
             sts_v4(rowaddr + (((2 * sub) ^ (row & 7)) << 4), b[0], b[1], b[2], b[3]);
             sts_v4(rowaddr + (((2 * sub + 1) ^ (row & 7)) << 4), b[4], b[5], b[6], b[7]);
         }
+    }
+};
+
+// ---- 1x1 u4 conv fed by copies of the packed input -------------------------------
+// A 1x1, stride-1, unpadded convolution is the GEMM of the NHWC pixel matrix
+// [N*H*W, C] with the filters [MG conv 算子優化: the implicit GEMM of a 1x1
+// filter needs no img2col].  The packed u4 input is brought to shared memory as
+// it lies in global memory, 128 pixels x 256 channels (16 KB) per unit, into a
+// staging ring of DEPTH slots, by asynchronous copies; the converter warps then
+// unpack the nibbles into the e4m3 operand stage shared-memory to shared-memory
+// [MG conv 算子優化: INT4 values unpacked on their way to the tensor cores], and
+// the filters stay resident.  Global memory is read once, 16 bytes at a time
+// or in 16 KB boxes, and never through registers.
+//   THREAD_COPY (C = 256, a pixel's codes are one 128-byte row): every
+//     converter thread copies (cp.async, 16 bytes each) exactly the 8 chunks it
+//     will unpack, so no thread waits for another's copies.
+//   otherwise (C a multiple of 256): one tiled 2-D TMA box of 128 pixels x 128
+//     bytes per unit (128-byte swizzled), issued by warp 0 once the four warps
+//     have released the slot; full / empty mbarriers per slot.
+template <bool THREAD_COPY>
+struct ConvU4PackedOp : OpBase {
+    static constexpr bool CACHE_COLS = true;
+    static constexpr bool TMA_A = false;
+    static constexpr bool F8 = true;
+    static constexpr int SCALE_LOG2 = 9;
+    static constexpr int SUB = 2;              // two K steps of 128 channels per unit
+    static constexpr int STAGES = 3;
+    static constexpr bool RESB = true;
+    static constexpr int B_RES_BYTES = 32768;  // filters of up to 512 channels x 64 outputs
+    static constexpr bool ROTATE_K = false;    // resident filters are indexed by the unit's K position
+    static constexpr int DEPTH = 4;            // staging slots (units of packed input in flight)
+    static constexpr int DEPTH_MULTI = 4;
+    static constexpr bool REG_RING = false;
+    static constexpr int SLOT = BM * 128;      // 128 pixels x 128 packed bytes
+    static constexpr int STG_BYTES = DEPTH * SLOT + 1024;  // slots, then 2 * DEPTH mbarriers
+    struct Unit {};
+    struct State {
+        UnitCursor c;
+    };
+
+    __device__ static uint64_t *slot_full(uint4 *stg) { return reinterpret_cast<uint64_t *>(stg + DEPTH * SLOT / 16); }
+    __device__ static uint64_t *slot_empty(uint4 *stg) { return slot_full(stg) + DEPTH; }
+
+    __device__ static void init(uint4 *stg)
+    {
+        for (int i = 0; i < DEPTH; ++i) {
+            mbar_init(smem_u32(slot_full(stg) + i), 1);
+            mbar_init(smem_u32(slot_empty(stg) + i), 4);  // the four converter warps
+        }
+    }
+
+    // Unit jn's input into slot jn % DEPTH (valid: jn is one of this CTA's units).
+    template <int DD>
+    __device__ static bool load(const Params &p, State &st, const uint4 *stg_c, int jn, bool valid, int sub, int rbase,
+                                Unit &)
+    {
+        uint4 *stg = const_cast<uint4 *>(stg_c);
+        const int slot = jn % DEPTH;
+        if constexpr (THREAD_COPY) {
+            // one copy group per unit (empty past the end); rows past the last
+            // pixel are zero-filled
+            if (valid) {
+                if (jn == 0) st.c.begin(p, false);
+                else st.c.next(p);
+                const uint32_t dst = smem_u32(stg + slot * (SLOT / 16));
+#pragma unroll
+                for (int t = 0; t < SUB; ++t) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int row = q * 32 + rbase;
+                        const int pix = st.c.mb * BM + row;
+                        const int chunk = 4 * t + sub;
+                        const bool in = pix < p.M;
+                        const uint8_t *src = p.A + (int64_t)(in ? pix : 0) * 128 + chunk * 16;
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + row * 128 + chunk * 16),
+                                     "l"(src), "r"(in ? 16 : 0)
+                                     : "memory");
+                    }
+                }
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            return true;
+        } else {
+            if (!valid) return true;
+            if (jn == 0) st.c.begin(p, false);
+            else st.c.next(p);
+            if (threadIdx.x >= 32) return true;
+            const uint32_t use = (uint32_t)(jn / DEPTH);
+            if (!warp_wait_idle(smem_u32(slot_empty(stg) + slot), (use & 1u) ^ 1u, p.status)) return false;
+            if (threadIdx.x == 0) {
+                const uint32_t bar = smem_u32(slot_full(stg) + slot);
+                mbar_arrive_expect_tx(bar, (uint32_t)SLOT);
+                tma_load_2d(smem_u32(stg + slot * (SLOT / 16)), &p.tmap, st.c.ks * 128, st.c.mb * BM, bar);
+            }
+            __syncwarp();
+            return true;
+        }
+    }
+
+    // Unit j: wait for its input, unpack 4 rows x 2 K steps of 32 channels per
+    // thread (two masks per 8 codes: channels 0,2,4,6 then 1,3,5,7, the order of
+    // the weight image), then release the slot.
+    template <int DD>
+    __device__ static bool store(const Params &p, State &, const uint4 *stg_c, uint32_t a_stage, int j, int sub,
+                                 int rbase, const Unit &)
+    {
+        uint4 *stg = const_cast<uint4 *>(stg_c);
+        const int slot = j % DEPTH;
+        if constexpr (THREAD_COPY) {
+            asm volatile("cp.async.wait_group %0;" ::"n"(DEPTH - 1) : "memory");
+        } else {
+            if (!warp_wait_idle(smem_u32(slot_full(stg) + slot), (uint32_t)(j / DEPTH) & 1u, p.status)) return false;
+        }
+        const uint32_t src = smem_u32(stg + slot * (SLOT / 16));
+#pragma unroll
+        for (int t = 0; t < SUB; ++t) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int row = q * 32 + rbase;
+                const int chunk = THREAD_COPY ? 4 * t + sub : (4 * t + sub) ^ (row & 7);
+                const uint4 v = lds_v4(src + row * 128 + (chunk << 4));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t b[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    b[2 * i] = w[i] & 0x0F0F0F0Fu;
+                    b[2 * i + 1] = (w[i] >> 4) & 0x0F0F0F0Fu;
+                }
+                const uint32_t rowaddr = a_stage + t * (BM * ROW_BYTES) + row * ROW_BYTES;
+                sts_v4(rowaddr + (((2 * sub) ^ (row & 7)) << 4), b[0], b[1], b[2], b[3]);
+                sts_v4(rowaddr + (((2 * sub + 1) ^ (row & 7)) << 4), b[4], b[5], b[6], b[7]);
+            }
+        }
+        if constexpr (!THREAD_COPY) {
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(slot_empty(stg) + slot));
+        }
+        return true;
     }
 };
 
@@ -401,6 +541,7 @@ constexpr int tma_stages(int cb, int tbn, int t, bool resb)
 
 template <int CB, int TBN_, int T, bool RES>
 struct ConvTmaOp : OpBase {
+    static constexpr bool CACHE_COLS = true;
     static constexpr bool TMA_A = true;
     static constexpr bool F8 = true;
     static constexpr int SCALE_LOG2 = 9;
@@ -647,6 +788,36 @@ qnn_status conv_tma_dispatch(const Params &p, int cb, cudaStream_t s)
     return conv_tma_launch<32, TBN, 1, false>(p, s);
 }
 
+// The 1x1 u4 conv on asynchronous copies of the packed input (p holds the fused
+// path's parameters): with C = 256 per-thread 16-byte copies; otherwise a 2-D
+// tensor map over the packed NHWC input viewed as [pixels][C / 2 bytes], boxes
+// of 128 pixels x 128 bytes (256 channels), 128-byte swizzled.
+static qnn_status conv1x1_bulk_launch(Params p, const qnn_conv_geom *g, cudaStream_t s)
+{
+    if (g->C == 256) {
+        // a pixel's codes are one 128-byte row: each thread copies its own chunks
+        p.KT = 1;
+        p.chunk_steps = 1;
+        p.nchunks = 1;
+        return launch<ConvU4PackedOp<true>, 64, false>(p, s);
+    }
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return QNN_ERR_CUDA;
+    const cuuint64_t row_bytes = (cuuint64_t)g->C / 2;
+    cuuint64_t dims[2] = {row_bytes, (cuuint64_t)p.M};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {128, (cuuint32_t)BM};
+    cuuint32_t estr[2] = {1, 1};
+    if (encode(&p.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(p.A), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return QNN_ERR_CUDA;
+    p.KT = g->C / 256;  // units (256 channels) per tile
+    p.chunk_steps = p.KT;
+    p.nchunks = 1;
+    return launch<ConvU4PackedOp<false>, 64, false>(p, s);
+}
+
 // u4: qconv_u4s4; else the u8 conv, whose filter values reach 255 in magnitude
 // when wide_w (u8 filters less their zero points) and 128 otherwise (s8).
 template <template <int> class Op>
@@ -762,6 +933,9 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
         if (g->OC <= 128) return conv_tma_dispatch<128>(p, cb, s);
         return conv_tma_dispatch<256>(p, cb, s);
     }
+    if (u4 && g->FH == 1 && g->FW == 1 && g->stride_h == 1 && g->stride_w == 1 && g->pad_h == 0 && g->pad_w == 0 &&
+        g->C % 256 == 0 && (int64_t)(g->C / 128) * 64 * 128 <= ConvU4PackedOp<true>::B_RES_BYTES && g->OC <= 64)
+        return conv1x1_bulk_launch(p, g, s);
     if (g->OC <= 64) return conv_launch<Op, 64>(p, s);
     if (g->OC <= 128) return conv_launch<Op, 128>(p, s);
     return conv_launch<Op, 256>(p, s);

@@ -35,6 +35,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <type_traits>
 #include "qnn_gemm_layout.h"
 #include "qnn_internal.h"
 #include "qnn_ptx.cuh"
@@ -119,12 +120,15 @@ struct OpBase {
     static constexpr bool RESB = false;      // weights resident in shared memory for the whole kernel
     static constexpr int B_RES_BYTES = 0;
     static constexpr bool ROTATE_K = true;  // each CTA starts its tiles' K walk at its own offset
+    static constexpr bool CACHE_COLS = false;  // epilogue keeps column constants across tiles of one column block
     struct PState {};                        // producer-side state of a TMA_A Op
     struct RowInfo {                         // per-thread part of the row mapping
         int r;
     };
     __device__ static RowInfo row_info(const Params &, int r) { return RowInfo{r}; }
     __device__ static int out_row(const Params &, int mb, const RowInfo &ri) { return mb * BM + ri.r; }
+    // barriers the Op keeps in its staging area, initialised by thread 0 at kernel start
+    __device__ static void init(uint4 *) {}
 };
 
 template <class Op, int TBN>
@@ -214,6 +218,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_
     return __all_sync(0xffffffffu, ok);
 }
 
+// The same for warps off the MMA issue path, which may be suspended while they wait.
+__device__ __forceinline__ bool warp_wait_idle(uint32_t bar, uint32_t parity, uint32_t *status)
+{
+    const bool ok = mbar_wait_idle(bar, parity, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- converter
 // Converts unit j into its stage.  `ready` says whether the stage's empty
 // phase was already seen complete; before the conversion work starts, the
@@ -226,11 +237,17 @@ __device__ __forceinline__ bool convert_one(const Params &p, Smem<Op, TBN> &s, t
     constexpr int STAGES = Op::STAGES;
     const int stage = j % STAGES;
     const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
-    const bool ok = ready || mbar_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status);
+    const bool ok = ready || mbar_wait_idle(smem_u32(&s.empty[stage]), ph ^ 1u, p.status);
     if (!__all_sync(0xffffffffu, ok)) return false;
     const int jn = j + 1;
     const bool probe = mbar_test_wait(smem_u32(&s.empty[jn % STAGES]), ((uint32_t)(jn / STAGES) & 1u) ^ 1u);
-    Op::template store<D>(p, st, s.stg, smem_u32(&s.a[stage][0]), j, sub, rbase, u);
+    if constexpr (std::is_void<decltype(Op::template store<D>(p, st, s.stg, 0u, j, sub, rbase, u))>::value) {
+        Op::template store<D>(p, st, s.stg, smem_u32(&s.a[stage][0]), j, sub, rbase, u);
+    } else {
+        // Ops whose store waits on its own barriers report a wait that gave up
+        if (!__all_sync(0xffffffffu, Op::template store<D>(p, st, s.stg, smem_u32(&s.a[stage][0]), j, sub, rbase, u)))
+            return false;
+    }
     fence_proxy_async_smem();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&s.full[stage]));
@@ -276,12 +293,21 @@ __device__ void converter_loop_rolled(const Params &p, Smem<Op, TBN> &s, int uni
     typename Op::State st{};
     typename Op::Unit u;
     bool ready = false;
+    // loads that can give up (Ops waiting on their own barriers) return false then
+    auto load = [&](int jj) -> bool {
+        if constexpr (std::is_void<decltype(Op::template load<D>(p, st, s.stg, jj, true, sub, rbase, u))>::value) {
+            Op::template load<D>(p, st, s.stg, jj, jj < units, sub, rbase, u);
+            return true;
+        } else {
+            return __all_sync(0xffffffffu, Op::template load<D>(p, st, s.stg, jj, jj < units, sub, rbase, u));
+        }
+    };
 #pragma unroll 1
-    for (int d = 0; d < D - 1; ++d) Op::template load<D>(p, st, s.stg, d, d < units, sub, rbase, u);
+    for (int d = 0; d < D - 1; ++d)
+        if (!load(d)) return;
 #pragma unroll 1
     for (int j = 0; j < units; ++j) {
-        const int jn = j + D - 1;
-        Op::template load<D>(p, st, s.stg, jn, jn < units, sub, rbase, u);
+        if (!load(j + D - 1)) return;
         if (!convert_one<Op, TBN, D>(p, s, st, j, units, sub, rbase, u, ready)) return;
     }
 }
@@ -331,7 +357,7 @@ __device__ void producer_role(const Params &p, Smem<Op, TBN> &s, int units)
     for (; j < units; ++j, c.next(p)) {
         const int stage = j % STAGES;
         const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
-        if (!ready && !warp_wait(smem_u32(&s.empty[stage]), ph ^ 1u, p.status)) {
+        if (!ready && !warp_wait_idle(smem_u32(&s.empty[stage]), ph ^ 1u, p.status)) {
             ok = false;
             break;
         }
@@ -788,15 +814,16 @@ __device__ __forceinline__ int32_t acc_to_int(uint32_t bits)
 // (the accumulator buffer is released after the last piece is read).
 template <class Op, int TBN, int COLS>
 __device__ __forceinline__ bool epilogue_stream_tile(const Params &p, Smem<Op, TBN> &s, float *cols,
-                                                     const ColumnRegs<COLS> &cr, int m, int nbase, int npieces,
-                                                     uint32_t taddr0, uint32_t abuf, uint32_t u, int lane)
+                                                     const ColumnRegs<COLS> &cr, bool fresh, bool &exact, int m,
+                                                     int nbase, int npieces, uint32_t taddr0, uint32_t abuf,
+                                                     uint32_t u, int lane)
 {
     uint32_t rw_next[8];
     load_residual(p, m, nbase, rw_next);
-    if (!warp_wait(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return false;
+    if (!warp_wait_idle(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return false;
     tc_fence_after();
-    const bool fast = store_columns<COLS>(cr, cols, lane) && !p.C32 && p.mode != QNN_EPI_S32 && !p.rowsum &&
-                      !p.row_scale;
+    if (fresh) exact = store_columns<COLS>(cr, cols, lane);
+    const bool fast = exact && !p.C32 && p.mode != QNN_EPI_S32 && !p.rowsum && !p.row_scale;
 #pragma unroll 1
     for (int jp = 0; jp < npieces; ++jp) {
         uint32_t rw[8];
@@ -861,19 +888,26 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
     const typename Op::RowInfo ri = Op::row_info(p, quad * 32 + lane);
     int nch = 1;
     if constexpr (MULTI) {
-        if (!warp_wait(smem_u32(&s.plan_ready), 0u, p.status)) return;
+        if (!warp_wait_idle(smem_u32(&s.plan_ready), 0u, p.status)) return;
         nch = s.plan_count;
     }
+    // the column constants in shared memory serve every tile of the same column
+    // block: they are loaded again only when the block changes
+    int cur_nbase = -1;
+    bool exact = false;
     for (int i = 0; i < my_tiles; ++i) {
         const int t = blockIdx.x + i * gridDim.x;
         const int m = Op::out_row(p, t % p.num_m, ri);
         const int nbase = (t / p.num_m) * TBN + p0 * 32;
+        const bool fresh = !Op::CACHE_COLS || nbase != cur_nbase;
+        cur_nbase = nbase;
         ColumnRegs<COLS> cr;
-        load_columns<COLS>(p, cr, nbase, lane);
+        if (fresh) load_columns<COLS>(p, cr, nbase, lane);
         if (nch == 1) {
             const uint32_t abuf = u & 1u;
             const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + p0 * 32;
-            if (!epilogue_stream_tile<Op, TBN, COLS>(p, s, cols, cr, m, nbase, npieces, taddr, abuf, u, lane))
+            if (!epilogue_stream_tile<Op, TBN, COLS>(p, s, cols, cr, fresh, exact, m, nbase, npieces, taddr, abuf,
+                                                     u, lane))
                 return;
             ++u;
         } else if constexpr (MULTI) {
@@ -884,7 +918,7 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
             const uint32_t fbuf = tmem + lanes + p0 * 32;
             const uint32_t ibuf = tmem + lanes + TBN + p0 * 32;
             for (int c = 0; c < nch; ++c) {
-                if (!warp_wait(smem_u32(&s.acc_full[0]), u & 1u, p.status)) return;
+                if (!warp_wait_idle(smem_u32(&s.acc_full[0]), u & 1u, p.status)) return;
                 tc_fence_after();
 #pragma unroll 1
                 for (int q = 0; q < 2 * npieces; ++q) {
@@ -905,7 +939,7 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
                 if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[0]));
                 ++u;
             }
-            store_columns<COLS>(cr, cols, lane);
+            if (fresh) exact = store_columns<COLS>(cr, cols, lane);
 #pragma unroll 1
             for (int jp = 0; jp < npieces; ++jp) {
                 uint32_t rw[8];
@@ -945,6 +979,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qmma_kernel(const __grid_const
         mbar_init(smem_u32(&s.mma_done), 1);
         mbar_init(smem_u32(&s.bres_full), 1);
         mbar_init(smem_u32(&s.plan_ready), 1);
+        Op::init(s.stg);
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
@@ -1028,6 +1063,7 @@ qnn_status launch(Params p, cudaStream_t stream)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QNN_ERR_CUDA;
     constexpr size_t SMEM = smem_bytes<Op, TBN>();
+    static_assert(SMEM <= 232448, "shared memory per block");
     if (!attr_set[dev]) {
         if (cudaFuncSetAttribute(qmma_kernel<Op, TBN, MULTI>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) != cudaSuccess)

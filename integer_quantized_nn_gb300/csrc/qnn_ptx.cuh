@@ -104,6 +104,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     return mbar_wait_slow(bar, parity, status, kWaitLimitNs);
 }
 
+// The same bounded wait for threads that expect to wait long (epilogue,
+// producer and converter roles): between checks mbarrier.try_wait lets the
+// hardware suspend the thread until the phase completes or a short time
+// passes, so waiting warps do not take issue slots from the ones at work.
+__device__ __forceinline__ bool mbar_wait_idle_slow(uint32_t bar, uint32_t parity, uint32_t *status)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 7u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (status) atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, uint32_t *status)
+{
+    if (mbar_test_wait(bar, parity)) return true;
+    return mbar_wait_idle_slow(bar, parity, status);
+}
+
 // ---- proxies / bulk copies ---------------------------------------------------
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
@@ -280,6 +302,24 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int 
         "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
+}
+
+// Tiled 2-D TMA load of one box of `tmap` at (c0 innermost, c1); same rules.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 // Programmatic dependent launch: block until the grid this one depends on (the

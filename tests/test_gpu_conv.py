@@ -151,6 +151,29 @@ def test_conv_u4s4_small(oracle, geom):
     _conv(oracle, I, Wt, geom, 8, 0.05, s_w, 0.11, bias, res=res, s_r=0.13)
 
 
+@pytest.mark.parametrize("geom,residual", [
+    ((3, 7, 9, 256, 64, 1, 0, 1), True),    # 189 pixels: a ragged 128-pixel tile, Conv_Add_Relu
+    ((2, 10, 13, 512, 64, 1, 0, 1), False),  # C = 512: two 256-channel units per tile
+    ((1, 16, 16, 256, 48, 1, 0, 1), True),   # OC = 48: a partial 32-column piece
+    ((1, 1, 1, 256, 64, 1, 0, 1), False),    # a single pixel
+])
+def test_conv_u4s4_1x1_tensor_copies(oracle, geom, residual):
+    """1x1 convs whose packed input tiles arrive by tensor copies and are unpacked
+    in shared memory (C a multiple of 256, up to 64 filters)."""
+    N, H, W, C, OC, F, pad, st = geom
+    I, Wt, s_w, bias, res = _rand_u4s4(37, N, H, W, C, OC, F, residual, H, W)
+    _conv(oracle, I, Wt, geom, 8, 0.05, s_w, 0.11, bias, res=res, s_r=0.13)
+    _conv(oracle, I, Wt, geom, 5, 0.05, s_w, 0.11, bias, mode="s32")
+
+
+def test_conv_u4u4_1x1_tensor_copies(oracle):
+    """The same path with u4 filters carrying per-filter zero points."""
+    geom = (2, 9, 9, 256, 64, 1, 0, 1)
+    I, Wt, s_w, bias, _ = _rand_u4s4(38, 2, 9, 9, 256, 64, 1, False)
+    z_w = np.random.default_rng(39).integers(0, 16, size=64)
+    _conv(oracle, I, Wt, geom, 8, 0.05, s_w, 0.11, bias, w_zp=z_w)
+
+
 @pytest.mark.parametrize("mode", ["dequant", "s32"])
 def test_conv_u4s4_modes(oracle, mode):
     geom = (1, 8, 8, 64, 64, 3, 1, 1)
