@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
         L.oracle_dequant_epilogue.argtypes = [vp, i64, i64, vp, vp, vp]
         L.oracle_conv_acc_direct.argtypes = [vp] * 2 + [ctypes.c_int] * 11 + [i32, vp]
         L.oracle_im2col.argtypes = [vp] + [ctypes.c_int] * 10 + [i32, vp]
+        L.oracle_conv_acc_layout.argtypes = [vp] * 2 + [ctypes.c_int] * 11 + [i32, ctypes.c_int, vp]
         L.oracle_lis_int_exp.restype = i64
         L.oracle_lis_int_exp.argtypes = [i64, f32]
         L.oracle_log_round.restype = ctypes.c_int
@@ -253,6 +254,28 @@ def conv_acc_direct(I, W, z_in, pad=(1, 1), stride=(1, 1)):
                                       stride[0], stride[1], int(z_in), _p(acc))
     if rc != 0:
         raise OverflowError("conv accumulator out of range or bad geometry")
+    return acc
+
+
+LAYOUTS = {"nhwc": 0, "nchw": 1, "nchw64": 2}
+
+
+def conv_acc_layout(I, W, z_in, N, H, Wd, C, layout, pad=(1, 1), stride=(1, 1)):
+    """Direct conv of codes I stored in `layout` ("nhwc", "nchw", "nchw64": any array
+    of N*H*Wd*C codes in that element order) with OHWI codes W; returns the int32
+    accumulators as a flat array in the same layout."""
+    I = _c(I, np.int32).ravel()
+    W = _c(W, np.int32)
+    OC, FH, FW, C2 = W.shape
+    assert C2 == C and I.size == N * H * Wd * C
+    OH, OW = conv_out_hw(H, Wd, FH, FW, pad[0], pad[1], stride[0], stride[1])
+    acc = np.empty(N * OH * OW * OC, np.int32)
+    rc = lib().oracle_conv_acc_layout(_p(I), _p(W), N, H, Wd, C, OC, FH, FW, pad[0], pad[1], stride[0], stride[1],
+                                      int(z_in), LAYOUTS[layout], _p(acc))
+    if rc == 1:
+        raise OverflowError("conv accumulator does not fit int32")
+    if rc != 0:
+        raise ValueError(f"oracle_conv_acc_layout: error {rc}")
     return acc
 
 

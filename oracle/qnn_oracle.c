@@ -390,6 +390,58 @@ int oracle_conv_acc_direct(const int32_t *I, const int32_t *W, int n_, int h, in
     return bad ? OR_ERR_RANGE : OR_OK;
 }
 
+/* The same convolution accumulator with the input and the output in one of
+ * three layouts [MG conv 算子優化: the library's conv writes NCHW64, each 64
+ * consecutive channels of a pixel contiguous]; weights stay OHWI.  Element
+ * (b, ch, y, x) of a tensor with C channels sits at
+ *   layout 0 (NHWC)  : ((b * H + y) * W + x) * C + ch
+ *   layout 1 (NCHW)  : ((b * C + ch) * H + y) * W + x
+ *   layout 2 (NCHW64): (((b * (C / 64) + ch / 64) * H + y) * W + x) * 64 + ch % 64
+ * (C % 64 == 0 for NCHW64).  The sum is the direct one above, with the same
+ * padding reading, written out with explicit indices for each layout. */
+static int64_t layout_index(int layout, int b, int ch, int y, int x, int C, int H, int W)
+{
+    switch (layout) {
+    case 1: return (((int64_t)b * C + ch) * H + y) * W + x;
+    case 2: return ((((int64_t)b * (C / 64) + ch / 64) * H + y) * W + x) * 64 + ch % 64;
+    default: return (((int64_t)b * H + y) * W + x) * C + ch;
+    }
+}
+
+int oracle_conv_acc_layout(const int32_t *I, const int32_t *W, int n_, int h, int w, int c, int oc, int fh, int fw,
+                           int ph, int pw, int sh, int sw, int32_t z_in, int layout, int32_t *acc)
+{
+    int oh_ = conv_out_dim(h, fh, ph, sh), ow_ = conv_out_dim(w, fw, pw, sw);
+    if (oh_ <= 0 || ow_ <= 0 || layout < 0 || layout > 2) return OR_ERR_ARG;
+    if (layout == 2 && (c % 64 != 0 || oc % 64 != 0)) return OR_ERR_ARG;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(|:bad)
+    for (int64_t p = 0; p < (int64_t)n_ * oh_ * ow_; ++p) {
+        int b = (int)(p / ((int64_t)oh_ * ow_));
+        int oy = (int)((p / ow_) % oh_);
+        int ox = (int)(p % ow_);
+        for (int o = 0; o < oc; ++o) {
+            int64_t s = 0;
+            for (int r = 0; r < fh; ++r) {
+                int iy = oy * sh - ph + r;
+                if (iy < 0 || iy >= h) continue;
+                for (int t = 0; t < fw; ++t) {
+                    int ix = ox * sw - pw + t;
+                    if (ix < 0 || ix >= w) continue;
+                    for (int ic = 0; ic < c; ++ic) {
+                        int32_t q = I[layout_index(layout, b, ic, iy, ix, c, h, w)];
+                        int32_t wt = W[(((int64_t)o * fh + r) * fw + t) * c + ic];
+                        s += (int64_t)(q - z_in) * (int64_t)wt;
+                    }
+                }
+            }
+            if (s > INT32_MAX || s < INT32_MIN) bad = 1;
+            acc[layout_index(layout, b, o, oy, ox, oc, oh_, ow_)] = (int32_t)s;
+        }
+    }
+    return bad ? OR_ERR_RANGE : OR_OK;
+}
+
 /* Explicit img2col [MG conv 算子優化, Fig. 5]: cols[p][(r, t, ic)] holds the
  * input code under tap (r, t) of output pixel p, or z_in where the tap falls in
  * the padding.  K order is (fh, fw, ic), matching OHWI weights read as [OC, K]. */

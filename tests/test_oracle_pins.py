@@ -570,3 +570,57 @@ def test_requant_rowscale_on_ties(oracle):
             alt = F(fl32(F(fl32(F(fl32(F(fl32(int(acc[n]))) * F(r))) * F(Mv[n]))) + F(Bq[n])))
             other += alt != T[n]
     assert other > 0
+
+
+@pytest.mark.parametrize("geom", [(2, 5, 6, 64, 64, 3, 1, 1), (1, 7, 4, 128, 64, 3, 1, 2), (2, 4, 6, 64, 128, 1, 0, 1)])
+def test_conv_layouts(oracle, geom):
+    """MegEngine 4-bit article, conv 算子優化 (the conv in NCHW64, each 64
+    consecutive channels of a pixel contiguous) and NCHW: the accumulator of the
+    conv with its input and output in NCHW or NCHW64 is the NHWC conv's, brute
+    forced on the NHWC view of the same codes, moved by numpy transposes."""
+    n_, h, w, c, oc, f, pad, st = geom
+    g = np.random.default_rng(44)
+    I = g.integers(0, 16, size=(n_, h, w, c)).astype(np.int32)
+    W = g.integers(-8, 8, size=(oc, f, f, c)).astype(np.int32)
+    ref = np.array(brute.conv_acc(I.tolist(), W.tolist(), 8, (pad, pad), (st, st)), np.int64)
+    oh, ow = (h + 2 * pad - f) // st + 1, (w + 2 * pad - f) // st + 1
+    ref = ref.reshape(n_, oh, ow, oc)
+    got = oracle.conv_acc_layout(I, W, 8, n_, h, w, c, "nhwc", (pad, pad), (st, st))
+    assert np.array_equal(got.reshape(n_, oh, ow, oc), ref)
+    got = oracle.conv_acc_layout(I.transpose(0, 3, 1, 2), W, 8, n_, h, w, c, "nchw", (pad, pad), (st, st))
+    assert np.array_equal(got.reshape(n_, oc, oh, ow), ref.transpose(0, 3, 1, 2))
+    I64 = I.reshape(n_, h, w, c // 64, 64).transpose(0, 3, 1, 2, 4)
+    got = oracle.conv_acc_layout(I64, W, 8, n_, h, w, c, "nchw64", (pad, pad), (st, st))
+    assert np.array_equal(got.reshape(n_, oc // 64, oh, ow, 64),
+                          ref.reshape(n_, oh, ow, oc // 64, 64).transpose(0, 3, 1, 2, 4))
+    if c == 64 and oc == 64:
+        # one 64-channel block: NCHW64 is NHWC itself
+        got = oracle.conv_acc_layout(I, W, 8, n_, h, w, c, "nchw64", (pad, pad), (st, st))
+        assert np.array_equal(got.reshape(n_, oh, ow, oc), ref)
+
+
+def test_conv_layout_indices_by_hand(oracle):
+    """Explicit indices: a single nonzero input code at (b, ch, y, x) and a 1x1
+    filter that picks channel ch into output channel o put (q - z) w exactly at
+    output (b, o, y, x) of each layout, and the zero point everywhere else."""
+    n_, h, w, c, oc = 2, 3, 4, 128, 64
+    b, ch, y, x, o = 1, 70, 2, 3, 5
+    for layout in ("nchw", "nchw64", "nhwc"):
+        I = np.zeros(n_ * h * w * c, np.int32)
+        if layout == "nchw":
+            I[((b * c + ch) * h + y) * w + x] = 9
+        elif layout == "nchw64":
+            I[(((b * (c // 64) + ch // 64) * h + y) * w + x) * 64 + ch % 64] = 9
+        else:
+            I[((b * h + y) * w + x) * c + ch] = 9
+        W = np.zeros((oc, 1, 1, c), np.int32)
+        W[o, 0, 0, ch] = 3
+        acc = oracle.conv_acc_layout(I, W, 0, n_, h, w, c, layout, (0, 0), (1, 1))
+        nz = np.flatnonzero(acc)
+        if layout == "nchw":
+            want = ((b * oc + o) * h + y) * w + x
+        elif layout == "nchw64":
+            want = (((b * (oc // 64) + o // 64) * h + y) * w + x) * 64 + o % 64
+        else:
+            want = ((b * h + y) * w + x) * oc + o
+        assert nz.tolist() == [want] and acc[want] == 27, layout
