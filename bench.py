@@ -567,9 +567,25 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
         gemm_entry(f"square_{n}", workloads.gemm_square(n), "s8")
     square_16384(torch, qnn, workloads, device, flush, stream, peak, steps, out)
 
-    def conv_entry(name, w, geom):
+    def relayout_u4(packed, shape, layout):
+        """Packed NHWC nibbles -> the same codes packed in `layout` (data movement only)."""
+        if layout == "nhwc":
+            return packed
+        Nb, H, W, C = shape
+        codes = np.empty(packed.shape[:-1] + (packed.shape[-1] * 2,), np.uint8)
+        codes[..., 0::2] = packed & 15
+        codes[..., 1::2] = packed >> 4
+        codes = codes.reshape(Nb, H, W, C)
+        if layout == "nchw":
+            codes = codes.transpose(0, 3, 1, 2)
+        else:
+            codes = codes.reshape(Nb, H, W, C // 64, 64).transpose(0, 3, 1, 2, 4)
+        flat = np.ascontiguousarray(codes).reshape(-1)
+        return (flat[0::2] | (flat[1::2] << 4)).astype(np.uint8)
+
+    def conv_entry(name, w, geom, layout="nhwc"):
         Nb, H, W, C, OC, F, pad, st = geom
-        g = qnn.conv_geom(Nb, H, W, C, OC, F, F, (pad, pad), (st, st))
+        g = qnn.conv_geom(Nb, H, W, C, OC, F, F, (pad, pad), (st, st), layout=layout)
         Wd = torch.from_numpy(w["W"]).to(device)
         nb = qnn.qnn_conv_packed_w_bytes(g, "s4")
         buf = torch.empty(nb + 1024, dtype=torch.uint8, device=device)
@@ -584,8 +600,9 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
         Bq = torch.empty(OC, dtype=torch.float32, device=device)
         qnn.q_fold_epilogue(OC, "u4", w["z_in"], cs, w["s_a"], sw, w["s_o"], bias=bias, zp_term=zp,
                             M=Mv, Bq=Bq)
-        I = torch.from_numpy(w["I"]).to(device)
-        res = None if w["res"] is None else torch.from_numpy(w["res"]).to(device)
+        I = torch.from_numpy(relayout_u4(w["I"], (Nb, H, W, C), layout)).to(device)
+        res = None if w["res"] is None else torch.from_numpy(
+            relayout_u4(w["res"], (Nb, g.OH, g.OW, OC), layout)).to(device)
         R = float(np.float32(np.float32(w["s_r"]) / np.float32(w["s_o"])))
         epi = qnn.epilogue("requant", relu=True, out_dt="u4", zp_term=zp, M=Mv, Bq=Bq, residual=res,
                            res_dt="u4", z_res=w["z_res"], R=R)
@@ -594,21 +611,26 @@ def run_extras(torch, qnn, workloads, device, flush, stream, pk, args):
         t = time_steps(torch, lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, g, epi, O, workspace=ws,
                                                      stream=stream), steps, 3, flush, stream)
         ms = statistics.median(t)
-        tf = time_steps(torch, lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, g, epi, O, stream=stream),
-                        steps, 3, flush, stream)
-        ms_fused = statistics.median(tf)
+        ms_fused = None
+        if layout != "nchw":
+            tf = time_steps(torch, lambda: qnn.qconv_u4s4(I, w["z_in"], Wp, g, epi, O, stream=stream),
+                            steps, 3, flush, stream)
+            ms_fused = statistics.median(tf)
         ops = 2.0 * Nb * g.OH * g.OW * OC * C * F * F
         tops = ops / (ms * 1e-3) / 1e12
         byts = I.numel() + O.numel() + (0 if res is None else res.numel()) + Wd.numel()
         out[name] = {"ms": round(ms, 4), "TOPS": round(tops, 2),
                      "frac_fp8_peak": round(tops / (2.0 * peak), 4),
-                     "ms_no_workspace": round(ms_fused, 4),
+                     "ms_no_workspace": None if ms_fused is None else round(ms_fused, 4),
                      "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
                      "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
 
     conv_entry("conv3x3_u4s4_add_relu", workloads.conv_u4(), (64, 56, 56, 64, 64, 3, 1, 1))
     conv_entry("conv1x1_u4s4_relu", workloads.conv_u4(C=256, OC=64, F=1, pad=0, residual=False, tag=1),
                (64, 56, 56, 256, 64, 1, 0, 1))
+    # the same 3x3 Conv_Add_Relu with input, residual and output in NCHW and NCHW64
+    conv_entry("conv3x3_u4s4_add_relu_nchw", workloads.conv_u4(), (64, 56, 56, 64, 64, 3, 1, 1), layout="nchw")
+    conv_entry("conv3x3_u4s4_add_relu_nchw64", workloads.conv_u4(), (64, 56, 56, 64, 64, 3, 1, 1), layout="nchw64")
 
     # weight zero points: ResNet-50 3x3 with u8 activations x u8 filters (zero point taken
     # out at prepack), and ViT-B fc1 with u8 weights (the run-time row-sum term)

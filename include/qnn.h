@@ -246,13 +246,27 @@ qnn_status qgemm_s8_static_scratch(const void *A, qnn_dtype a_dt, const void *B_
 
 /* ---- implicit-GEMM convolution -------------------------------------------- */
 
-/* NHWC input [N, H, W, C], OHWI weights [OC, FH, FW, C], NHWC output
- * [N, OH, OW, OC] with OH = (H + 2 pad_h - FH) / stride_h + 1 (same for W).
+/* Layouts of a conv's input, output and residual [MG conv 算子優化: the conv
+ * writes NCHW64, each 64 consecutive channels of a pixel contiguous].  Element
+ * (n, c, y, x) of a tensor with C channels sits at
+ *   QNN_LAYOUT_NHWC  : ((n * H + y) * W + x) * C + c
+ *   QNN_LAYOUT_NCHW  : ((n * C + c) * H + y) * W + x
+ *   QNN_LAYOUT_NCHW64: (((n * (C / 64) + c / 64) * H + y) * W + x) * 64 + c % 64
+ * counted in codes (4-bit tensors: two per byte, element 2i in the low nibble,
+ * so that NCHW packs neighbouring pixels of a row together). */
+typedef enum { QNN_LAYOUT_NHWC = 0, QNN_LAYOUT_NCHW = 1, QNN_LAYOUT_NCHW64 = 2 } qnn_layout;
+
+/* Input [N, H, W, C] and output [N, OH, OW, OC] in `layout` (the residual, when
+ * there is one, in the output's), OHWI weights [OC, FH, FW, C], with OH = (H +
+ * 2 pad_h - FH) / stride_h + 1 (same for W).
  * GEMM view [MG conv 算子優化, Fig. 5; output transposed so that output channels
  * are contiguous]: rows p = (n, oh, ow), columns oc, reduction k = (fh, fw, c).
- * Padded taps hold the real value 0, i.e. the code z_in. */
+ * Padded taps hold the real value 0, i.e. the code z_in.
+ * NCHW64 needs C and OC multiples of 64; NCHW with 4-bit codes needs W and OW
+ * even. */
 typedef struct {
     int32_t N, H, W, C, OC, FH, FW, pad_h, pad_w, stride_h, stride_w;
+    int32_t layout;          /* qnn_layout of input, output and residual (0: NHWC) */
 } qnn_conv_geom;
 
 /* Size in bytes of the prepacked conv weight operand for weights of w_dt
@@ -296,12 +310,14 @@ size_t qnn_conv_workspace_bytes(const qnn_conv_geom *g, qnn_dtype in_dt);
  *   per channel and the convolution reads its taps with tensor-memory copies
  *   (the faster path there); 1x1 filters and NULL: the convolution re-encodes
  *   the packed input itself.  Results are identical.  Calls in flight at the
- *   same time must not share a workspace. */
+ *   same time must not share a workspace.  An NCHW input needs the workspace
+ *   (the pre-pass reads it and writes the expanded NHWC bytes the convolution
+ *   reads, for every filter size): QNN_ERR_UNSUPPORTED without one. */
 qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
                       const qnn_epilogue *epi, void *O, int32_t *O_s32, void *workspace,
                       size_t workspace_bytes, qnn_stream_t stream);
 
-/* u8 activations x s8 weights, same contract (I: u8 NHWC; C % 16 == 0). */
+/* u8 activations x s8 weights, same contract (I: u8 codes in g->layout; C % 16 == 0). */
 qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
                       const qnn_epilogue *epi, void *O, int32_t *O_s32, qnn_stream_t stream);
 

@@ -40,6 +40,7 @@ constexpr int KMAX_U4_EXACT = 139810;  // 2^24 / (15 * 8): exact fp32 sums of u4
 // current tile and the (fh, fw, c0) position of its 16-byte group in K.
 struct ConvState {
     int img[4];   // n * H of the row's image, or -1 past the last pixel
+    int nim[4];   // n
     int ih0[4];
     int iw0[4];
     int c0, fh, fw;
@@ -72,10 +73,12 @@ __device__ __forceinline__ void conv_cursor(const Params &p, ConvState &st, int 
                 const int oh = rem / p.OW;
                 const int ow = rem - oh * p.OW;
                 st.img[q] = n * p.H;
+                st.nim[q] = n;
                 st.ih0[q] = oh * p.sh - p.ph;
                 st.iw0[q] = ow * p.sw - p.pw;
             } else {
                 st.img[q] = -1;
+                st.nim[q] = 0;
                 st.ih0[q] = 0;
                 st.iw0[q] = 0;
             }
@@ -197,8 +200,22 @@ struct ConvRegRing : OpBase {
                 const int iw = st.iw0[q] + st.fw;
                 if (ih < 0 || ih >= p.H || iw < 0 || iw >= p.W) {
                     v = make_uint4(p.pad_word, p.pad_word, p.pad_word, p.pad_word);
+                } else if (p.layout == QNN_LAYOUT_NCHW) {
+                    // 8-bit codes only (the host sends 4-bit NCHW inputs through the
+                    // expansion pre-pass): the group's 16 channels, one per plane
+                    const int64_t plane = (int64_t)p.H * p.W;
+                    const uint8_t *src = p.A + ((int64_t)st.nim[q] * p.Cin + st.c0) * plane + (int64_t)ih * p.W + iw;
+                    uint32_t w4[4] = {0, 0, 0, 0};
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) w4[j >> 2] |= (uint32_t)__ldg(src + j * plane) << (8 * (j & 3));
+                    v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 } else {
-                    const int64_t elem = ((int64_t)(st.img[q] + ih) * p.W + iw) * p.Cin + st.c0;
+                    // NHWC; NCHW64 keeps a group's channels together inside its 64-channel block
+                    const int64_t elem =
+                        p.layout == QNN_LAYOUT_NHWC
+                            ? ((int64_t)(st.img[q] + ih) * p.W + iw) * p.Cin + st.c0
+                            : ((((int64_t)st.nim[q] * (p.Cin >> 6) + (st.c0 >> 6)) * p.H + ih) * p.W + iw) * 64 +
+                                  (st.c0 & 63);
                     v = ldg_nc_v4(p.A + (ELEM_BITS == 4 ? elem / 2 : elem));
                 }
             }
@@ -483,6 +500,8 @@ inline bool geom_ok(const qnn_conv_geom *g)
     const int oh = (g->H + 2 * g->pad_h - g->FH) / g->stride_h + 1;
     const int ow = (g->W + 2 * g->pad_w - g->FW) / g->stride_w + 1;
     if (g->H + 2 * g->pad_h < g->FH || g->W + 2 * g->pad_w < g->FW || oh <= 0 || ow <= 0) return false;
+    if (g->layout < QNN_LAYOUT_NHWC || g->layout > QNN_LAYOUT_NCHW64) return false;
+    if (g->layout == QNN_LAYOUT_NCHW64 && (g->C % 64 != 0 || g->OC % 64 != 0)) return false;
     const int64_t rows = (int64_t)g->N * oh * ow;
     const int64_t K = (int64_t)g->FH * g->FW * g->C;
     const int64_t in = (int64_t)g->N * g->H * g->W * g->C;
@@ -657,6 +676,75 @@ __global__ void expand_u4_kernel(const uint8_t *__restrict__ in, int64_t n16, ui
     }
 }
 
+// The same expansion from inputs in the other layouts, written in NHWC (the
+// convolution reads taps of the NHWC bytes); e4m3 of (q - z) / 512 is the byte
+// |q - z| with the sign in bit 7.
+__device__ __forceinline__ uint32_t e4m3_centred1(uint32_t q, uint32_t z)
+{
+    return q >= z ? q - z : (0x80u | (z - q));
+}
+
+// NCHW64: [N][C / 64][H][W][32 bytes] -> [N][H][W][C]; one thread per 16 input
+// bytes (32 channels of one pixel), 32 output bytes.
+__global__ void expand_u4_nchw64_kernel(const uint8_t *__restrict__ in, int64_t n16, int HW, int CB, uint32_t z,
+                                        uint8_t *__restrict__ out)
+{
+    const uint32_t zz = z * 0x01010101u;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t blk = i >> 1;  // (n, cb, pixel)
+        const int half = (int)(i & 1);
+        const int pix = (int)(blk % HW);
+        const int64_t t = blk / HW;
+        const int cb = (int)(t % CB);
+        const int64_t n = t / CB;
+        const uint4 v = ldg_nc_v4(in + i * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t ev = e4m3_centred4(w[j] & 0x0F0F0F0Fu, zz);
+            const uint32_t od = e4m3_centred4((w[j] >> 4) & 0x0F0F0F0Fu, zz);
+            o[2 * j] = prmt(ev, od, 0x5140u);
+            o[2 * j + 1] = prmt(ev, od, 0x7362u);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(out + ((n * HW + pix) * (int64_t)CB * 64 + cb * 64 + half * 32));
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// NCHW: [N][C][H][W / 2 bytes] -> [N][H][W][C]; one block per image row (n, h):
+// the row of every channel plane is read into shared memory (C * W / 2 bytes),
+// then each thread writes 16 channels of one pixel (16 bytes).
+__global__ void expand_u4_nchw_kernel(const uint8_t *__restrict__ in, int H, int W, int C, uint32_t z,
+                                      uint8_t *__restrict__ out)
+{
+    extern __shared__ uint8_t rowbuf[];
+    const int n = blockIdx.x / H;
+    const int h = blockIdx.x - n * H;
+    const int rb = W / 2;  // bytes of one plane row
+    for (int i = threadIdx.x; i < C * rb; i += blockDim.x) {
+        const int c = i / rb;
+        const int x = i - c * rb;
+        rowbuf[i] = __ldg(in + (((int64_t)n * C + c) * H + h) * rb + x);
+    }
+    __syncthreads();
+    const int groups = C / 16;
+    uint8_t *orow = out + ((int64_t)n * H + h) * W * (int64_t)C;
+    for (int i = threadIdx.x; i < W * groups; i += blockDim.x) {
+        const int w = i / groups;
+        const int c0 = (i - w * groups) * 16;
+        uint32_t o[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint32_t q = (rowbuf[(c0 + j) * rb + (w >> 1)] >> (4 * (w & 1))) & 15u;
+            o[j >> 2] |= e4m3_centred1(q, z) << (8 * (j & 3));
+        }
+        *reinterpret_cast<uint4 *>(orow + (int64_t)w * C + c0) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 // Weight image of the TMA conv: for each 256-filter block and unit (tap, CB
 // channels), 256 rows x CB bytes of e4m3 weights in channel order, in the
 // CB-byte swizzled layout (chunk c of row r at chunk c ^ ((r * CB / 128) %
@@ -707,11 +795,11 @@ qnn_status conv_launch(const Params &p, cudaStream_t s)
 // sides within the TMA limit of 256 elements after striding) that wastes the
 // fewest of the 128 accumulator rows over the whole output; ties go to the
 // wider tile (longer contiguous input rows).
-inline void choose_tiles(int N, int OH, int OW, int sw, int sh, int &TW, int &TH, int &TN)
+inline void choose_tiles(int N, int OH, int OW, int sw, int sh, int &TW, int &TH, int &TN, bool even_tw = false)
 {
     int64_t best = -1;
     TW = TH = TN = 1;
-    for (int tw = 1; tw <= 128 && tw * sw <= 256; ++tw) {
+    for (int tw = even_tw ? 2 : 1; tw <= 128 && tw * sw <= 256; tw += even_tw ? 2 : 1) {
         for (int th = 1; tw * th <= 128 && th * sh <= 256; ++th) {
             int tn = 128 / (tw * th);
             if (tn > N) tn = N;
@@ -859,9 +947,15 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
     p.C = O;
     p.C32 = O_s32;
     p.vec_ok = (g->OC % 32 == 0);
+    p.layout = g->layout;
+    const bool nchw = g->layout == QNN_LAYOUT_NCHW;
     qnn_status st = setup_epilogue(e, true, p);
     if (st != QNN_OK) return st;
     if (p.mode == QNN_EPI_REQUANT && p.out_bits == 4 && e->out_dt != QNN_U4) return QNN_ERR_UNSUPPORTED;
+    // NCHW packs 4-bit codes along W: pixel pairs of even widths share bytes
+    if (nchw && u4 && (g->W % 2 != 0 || ow % 2 != 0)) return QNN_ERR_INVALID_ARG;
+    if (nchw && p.res && p.res_bits == 4 && ow % 2 != 0) return QNN_ERR_INVALID_ARG;
+    if (nchw && p.mode == QNN_EPI_REQUANT && p.out_bits == 4 && ow % 2 != 0) return QNN_ERR_INVALID_ARG;
     // exact fp32 chunk sums: u4 x s4 products are at most 120, centred u8 x s8 at most
     // 2^14, centred u8 x (u8 - z_w) below 2^15 (half as many steps per chunk)
     if (u4) {
@@ -879,7 +973,9 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
     if (u4 && p.nchunks > 1) return QNN_ERR_UNSUPPORTED;
     // the workspace path pays one expansion pass over the input, which only
     // filters with several taps (each input pixel read by several of them) repay
-    if (workspace && g->FH * g->FW == 1) workspace = nullptr;
+    // (a 4-bit NCHW input always takes the pre-pass, which reorders it to NHWC)
+    if (workspace && g->FH * g->FW == 1 && !(u4 && nchw)) workspace = nullptr;
+    if (u4 && nchw && !workspace) return QNN_ERR_UNSUPPORTED;
     if (workspace) {
         if (!u4) return QNN_ERR_UNSUPPORTED;
         if (workspace_bytes < (size_t)g->N * g->H * g->W * g->C) return QNN_ERR_INVALID_ARG;
@@ -896,11 +992,20 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
         const int64_t cap = (int64_t)sm_count() * 16;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        expand_u4_kernel<<<(int)blocks, 256, 0, s>>>(p.A, n16, (uint32_t)z_in, static_cast<uint8_t *>(workspace));
+        uint8_t *xw = static_cast<uint8_t *>(workspace);
+        if (g->layout == QNN_LAYOUT_NHWC) {
+            expand_u4_kernel<<<(int)blocks, 256, 0, s>>>(p.A, n16, (uint32_t)z_in, xw);
+        } else if (g->layout == QNN_LAYOUT_NCHW64) {
+            expand_u4_nchw64_kernel<<<(int)blocks, 256, 0, s>>>(p.A, n16, g->H * g->W, g->C / 64, (uint32_t)z_in, xw);
+        } else {
+            const size_t rowbuf = (size_t)g->C * (g->W / 2);
+            if (rowbuf > 48 * 1024 || (int64_t)g->N * g->H > INT32_MAX) return QNN_ERR_UNSUPPORTED;
+            expand_u4_nchw_kernel<<<g->N * g->H, 256, rowbuf, s>>>(p.A, g->H, g->W, g->C, (uint32_t)z_in, xw);
+        }
         if (launch_status() != QNN_OK) return QNN_ERR_CUDA;
         const int cb = tma_cb(g->C);
         int TW, TH, TN;
-        choose_tiles(g->N, oh, ow, g->stride_w, g->stride_h, TW, TH, TN);
+        choose_tiles(g->N, oh, ow, g->stride_w, g->stride_h, TW, TH, TN, nchw);
         cuuint64_t dims[4] = {(cuuint64_t)g->C, (cuuint64_t)g->W, (cuuint64_t)g->H, (cuuint64_t)g->N};
         cuuint64_t strides[3] = {(cuuint64_t)g->C, (cuuint64_t)g->W * g->C, (cuuint64_t)g->H * g->W * g->C};
         cuuint32_t box[4] = {(cuuint32_t)cb, (cuuint32_t)(TW * g->stride_w), (cuuint32_t)(TH * g->stride_h),
@@ -933,7 +1038,8 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
         if (g->OC <= 128) return conv_tma_dispatch<128>(p, cb, s);
         return conv_tma_dispatch<256>(p, cb, s);
     }
-    if (u4 && g->FH == 1 && g->FW == 1 && g->stride_h == 1 && g->stride_w == 1 && g->pad_h == 0 && g->pad_w == 0 &&
+    if (u4 && g->layout == QNN_LAYOUT_NHWC && g->FH == 1 && g->FW == 1 && g->stride_h == 1 && g->stride_w == 1 &&
+        g->pad_h == 0 && g->pad_w == 0 &&
         g->C % 256 == 0 && (int64_t)(g->C / 128) * 64 * 128 <= ConvU4PackedOp<true>::B_RES_BYTES && g->OC <= 64)
         return conv1x1_bulk_launch(p, g, s);
     if (g->OC <= 64) return conv_launch<Op, 64>(p, s);

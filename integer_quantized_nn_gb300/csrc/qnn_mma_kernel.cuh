@@ -108,6 +108,9 @@ struct Params {
     void *C;
     int32_t *C32;
     int vec_ok;              // N % 32 == 0: every 32-column piece whole and 16-byte aligned
+    // conv layout of the input, the output and the residual (qnn_layout; GEMMs: 0).
+    // Output / residual rows m = (n, oh, ow) = n * OHW + pixel.
+    int layout;
     uint32_t *status;
 };
 
@@ -556,6 +559,23 @@ __device__ __forceinline__ bool store_columns(const ColumnRegs<COLS> &cr, float 
     return __all_sync(0xffffffffu, exact);
 }
 
+// Element offset (in codes) of output element (row m, column n) in the layout
+// of the output and the residual, and the distance between consecutive
+// columns: NHWC (and every GEMM) m * N + n; NCHW (image, channel, pixel); NCHW64
+// (image, channel block, pixel, channel in block).
+__device__ __forceinline__ int64_t out_off(const Params &p, int m, int n)
+{
+    if (p.layout == QNN_LAYOUT_NHWC) return (int64_t)m * p.N + n;
+    const int img = m / p.OHW;
+    const int pix = m - img * p.OHW;
+    if (p.layout == QNN_LAYOUT_NCHW) return ((int64_t)img * p.N + n) * p.OHW + pix;
+    return (((int64_t)img * (p.N >> 6) + (n >> 6)) * p.OHW + pix) * 64 + (n & 63);
+}
+__device__ __forceinline__ int64_t out_cstride(const Params &p)
+{
+    return p.layout == QNN_LAYOUT_NCHW ? p.OHW : 1;
+}
+
 // The residual codes of the 32 columns n0.. of row m (8-bit: 8 words of 4
 // codes; 4-bit: 4 words of 8 codes), or zeros without a residual.
 __device__ __forceinline__ void load_residual(const Params &p, int m, int n0, uint32_t (&rw)[8])
@@ -563,7 +583,19 @@ __device__ __forceinline__ void load_residual(const Params &p, int m, int n0, ui
 #pragma unroll
     for (int i = 0; i < 8; ++i) rw[i] = 0;
     if (!p.res || m >= p.M || n0 >= p.N) return;
-    const int64_t base = (int64_t)m * p.N + n0;
+    const int64_t base = out_off(p, m, n0);
+    if (p.layout == QNN_LAYOUT_NCHW) {
+        // one code per channel plane
+        const int64_t cs = p.OHW;
+        for (int i = 0; i < 32 && n0 + i < p.N; ++i) {
+            const int64_t e = base + (int64_t)i * cs;
+            if (p.res_bits == 8)
+                rw[i >> 2] |= (uint32_t)p.res[e] << (8 * (i & 3));
+            else
+                rw[i >> 3] |= (((uint32_t)p.res[e >> 1] >> (4 * (int)(e & 1))) & 15u) << (4 * (i & 7));
+        }
+        return;
+    }
     if (p.res_bits == 8) {
         if (p.vec_ok) {
             const uint4 r0 = ldg_nc_v4(p.res + base), r1 = ldg_nc_v4(p.res + base + 16);
@@ -638,16 +670,38 @@ __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t c0, uint32_t c1, uin
 // must be finite).  No conversion instructions are used.
 // RS: per-row activation scales -- each column factor becomes fl(rs * factor)
 // (instantiated separately so that the common path carries none of it).
+// Packed 4-bit NCHW output: neighbouring pixels of a row share a byte, and they
+// are rows m, m + 1 of one warp (lanes 2j, 2j + 1; the host requires even output
+// widths and even tile widths), so the even lane merges its partner's codes
+// and writes the bytes.  Called by every lane; `valid` says whether the lane's
+// row exists.
+__device__ __forceinline__ void store_nchw_u4(const Params &p, int m, int n0, const uint32_t (&c)[32], bool valid)
+{
+    uint8_t *C = static_cast<uint8_t *>(p.C);
+    const bool even = (threadIdx.x & 1) == 0;
+    const int64_t base = valid ? out_off(p, m, n0) : 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, c[i], 1);
+        if (even && valid && n0 + i < p.N)
+            C[(base + (int64_t)i * p.OHW) >> 1] = (uint8_t)((c[i] & 15u) | ((hi & 15u) << 4));
+    }
+}
+
 template <bool RS>
 __device__ __forceinline__ void epilogue_float_t(const Params &p, int m, int n0, float (&a)[32],
                                                  const float *ca, const float *cb,
                                                  const uint32_t (&rw)[8])
 {
-    if (m >= p.M || n0 >= p.N) return;
-    const bool vec = p.vec_ok;
-    const int64_t base = (int64_t)m * p.N + n0;  // element offset of (m, n0)
+    const bool valid = m < p.M && n0 < p.N;
+    // NCHW u4 outputs pair up lanes: every lane takes part (warp-uniform test)
+    const bool pair = p.layout == QNN_LAYOUT_NCHW && p.mode == QNN_EPI_REQUANT && p.out_bits == 4;
+    if (!valid && !pair) return;
+    const bool vec = p.vec_ok && p.layout != QNN_LAYOUT_NCHW;
+    const int64_t base = valid ? out_off(p, m, n0) : 0;  // element offset of (m, n0)
+    const int64_t cs = out_cstride(p);
     float rs = 1.0f;
-    if constexpr (RS) rs = __ldg(p.row_scale + m);
+    if constexpr (RS) rs = valid ? __ldg(p.row_scale + m) : 1.0f;
     if (p.mode == QNN_EPI_DEQUANT) {
         float *C = static_cast<float *>(p.C);
         uint32_t y[32];
@@ -670,7 +724,7 @@ __device__ __forceinline__ void epilogue_float_t(const Params &p, int m, int n0,
 #pragma unroll
             for (int i = 0; i < 32; i += 4) st_v4(C + base + i, y[i], y[i + 1], y[i + 2], y[i + 3]);
         } else {
-            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = __uint_as_float(y[i]);
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i * cs] = __uint_as_float(y[i]);
         }
         return;
     }
@@ -701,7 +755,16 @@ __device__ __forceinline__ void epilogue_float_t(const Params &p, int m, int n0,
             c[i + k] = __float_as_uint(__fadd_rn(v, ROUND_MAGIC)) + (uint32_t)p.z_out;
         }
     }
+    if (pair) {
+        store_nchw_u4(p, m, n0, c, valid);
+        return;
+    }
     uint8_t *C = static_cast<uint8_t *>(p.C);
+    if (p.layout == QNN_LAYOUT_NCHW) {
+        // 8-bit codes, one per channel plane
+        for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i * cs] = (uint8_t)c[i];
+        return;
+    }
     if (p.out_bits == 8) {
         uint32_t ow[8];
 #pragma unroll
@@ -752,8 +815,11 @@ __device__ __forceinline__ void epilogue_int(const Params &p, int m, int n0, int
                                              const float *ca, const float *cb, const float *cz,
                                              const uint32_t (&rw)[8])
 {
-    if (m >= p.M || n0 >= p.N) return;
-    const bool vec = p.vec_ok;
+    const bool valid = m < p.M && n0 < p.N;
+    const bool pair = p.layout == QNN_LAYOUT_NCHW && p.mode == QNN_EPI_REQUANT && p.out_bits == 4;
+    if (!valid && !pair) return;
+    const bool vec = p.vec_ok && p.layout != QNN_LAYOUT_NCHW;
+    const int64_t cs = out_cstride(p);
     if (p.zp) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
@@ -767,30 +833,31 @@ __device__ __forceinline__ void epilogue_int(const Params &p, int m, int n0, int
     if (p.rowsum) {
         // the weight zero point's term (128 - z_w[n]) * sum_k (a_k - centre), in
         // wrapping 32-bit arithmetic: the final sum fits int32 (host check)
-        const uint32_t rs = (uint32_t)__ldg(p.rowsum + m);
+        const uint32_t rs = valid ? (uint32_t)__ldg(p.rowsum + m) : 0u;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int n = n0 + i < p.N ? n0 + i : p.N - 1;
             ac[i] = (int32_t)((uint32_t)ac[i] + (uint32_t)(128 - __ldg(p.zw + n)) * rs);
         }
     }
-    const int64_t base = (int64_t)m * p.N + n0;
-    if (p.C32) {
+    const int64_t base = valid ? out_off(p, m, n0) : 0;
+    if (p.C32 && valid) {
         if (vec) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
                 st_v4(p.C32 + base + i, ac[i], ac[i + 1], ac[i + 2], ac[i + 3]);
         } else {
-            for (int i = 0; i < 32 && n0 + i < p.N; ++i) p.C32[base + i] = ac[i];
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) p.C32[base + i * cs] = ac[i];
         }
     }
     if (p.mode == QNN_EPI_S32) {
+        if (!valid) return;
         int32_t *C = static_cast<int32_t *>(p.C);
         if (vec) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) st_v4(C + base + i, ac[i], ac[i + 1], ac[i + 2], ac[i + 3]);
         } else {
-            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = ac[i];
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i * cs] = ac[i];
         }
         return;
     }

@@ -49,7 +49,7 @@ class Epilogue(ctypes.Structure):
 
 class ConvGeom(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("N", "H", "W", "C", "OC", "FH", "FW", "pad_h", "pad_w", "stride_h", "stride_w")]
+                ("N", "H", "W", "C", "OC", "FH", "FW", "pad_h", "pad_w", "stride_h", "stride_w", "layout")]
 
     @property
     def OH(self):
@@ -261,8 +261,11 @@ def qgemm_s8_static_scratch(A, a_dt: str, B_packed, M: int, N: int, K: int, epi:
                                                _stream(stream)), "qgemm_s8_static_scratch")
 
 
-def conv_geom(N, H, W, C, OC, FH, FW, pad=(1, 1), stride=(1, 1)) -> ConvGeom:
-    return ConvGeom(N, H, W, C, OC, FH, FW, pad[0], pad[1], stride[0], stride[1])
+LAYOUTS = {"nhwc": 0, "nchw": 1, "nchw64": 2}
+
+
+def conv_geom(N, H, W, C, OC, FH, FW, pad=(1, 1), stride=(1, 1), layout="nhwc") -> ConvGeom:
+    return ConvGeom(N, H, W, C, OC, FH, FW, pad[0], pad[1], stride[0], stride[1], LAYOUTS[layout])
 
 
 def qnn_conv_packed_w_bytes(g: ConvGeom, w_dt: str = "s4") -> int:

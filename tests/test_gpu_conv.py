@@ -349,3 +349,151 @@ def test_conv_errors():
     with pytest.raises(qnn.QnnError) as e:
         qnn.qconv_u4s4(I, 8, Wp, g, epi, O)     # filter larger than the padded input
     assert e.value.status == qnn.QNN_ERR_INVALID_ARG
+
+
+# ---- NCHW / NCHW64 layouts -------------------------------------------------------
+
+def _to_layout(x, layout):
+    """NHWC array [N, H, W, C] -> the same codes in `layout` (a flat-able array)."""
+    N, H, W, C = x.shape
+    if layout == "nchw":
+        return np.ascontiguousarray(x.transpose(0, 3, 1, 2))
+    if layout == "nchw64":
+        return np.ascontiguousarray(x.reshape(N, H, W, C // 64, 64).transpose(0, 3, 1, 2, 4))
+    return np.ascontiguousarray(x)
+
+
+def _from_layout(flat, layout, N, H, W, C):
+    if layout == "nchw":
+        return flat.reshape(N, C, H, W).transpose(0, 2, 3, 1)
+    if layout == "nchw64":
+        return flat.reshape(N, C // 64, H, W, 64).transpose(0, 2, 3, 1, 4).reshape(N, H, W, C)
+    return flat.reshape(N, H, W, C)
+
+
+def _conv_layout(oracle, geom, layout, u4=True, mode="requant", residual=True, workspace=True, seed=50,
+                 z_in=None, out_dt=None):
+    """The conv with input, output and residual in `layout`, against the oracle's
+    direct conv in that layout (oracle.conv_acc_layout) and its requant."""
+    t = torch()
+    N, H, W, C, OC, F, pad, st = geom
+    g = qnn.conv_geom(N, H, W, C, OC, F, F, (pad, pad), (st, st), layout=layout)
+    OH, OW = g.OH, g.OW
+    rng = np.random.default_rng(seed)
+    if u4:
+        I = rng.integers(0, 16, size=(N, H, W, C)).astype(np.int32)
+        Wc = rng.integers(-8, 8, size=(OC, F, F, C)).astype(np.int32)
+        z_in = 8 if z_in is None else z_in
+        out_dt = out_dt or "u4"
+    else:
+        I = rng.integers(0, 256, size=(N, H, W, C)).astype(np.int32)
+        Wc = rng.integers(-128, 128, size=(OC, F, F, C)).astype(np.int32)
+        z_in = 100 if z_in is None else z_in
+        out_dt = out_dt or "u8"
+    res = rng.integers(0, 16 if u4 else 256, size=(N, OH, OW, OC)).astype(np.int32) if residual else None
+    s_w = rng.uniform(1e-3, 1e-2, size=OC).astype(np.float32)
+    bias = rng.normal(0, 1, size=OC).astype(np.float32)
+    s_a, s_o = 0.05, (0.11 if u4 else 0.9)
+    pk = oracle.pack_nibbles if u4 else oracle.pack_bytes
+    Id = dev(pk(_to_layout(I, layout).ravel()))
+    Wpk = oracle.pack_nibbles(Wc.reshape(OC, F, F, C)) if u4 else Wc.astype(np.int8)
+    w_dt = "s4" if u4 else "s8"
+    Wp = aligned_empty(qnn.qnn_conv_packed_w_bytes(g, w_dt))
+    colsum = t.empty(OC, dtype=t.int32, device="cuda")
+    qnn.qconv_prepack_w(dev(Wpk), w_dt, g, Wp, colsum)
+    zp = t.empty(OC, dtype=t.int32, device="cuda")
+    Mv = t.empty(OC, dtype=t.float32, device="cuda")
+    Bq = t.empty(OC, dtype=t.float32, device="cuda")
+    D = t.empty(OC, dtype=t.float32, device="cuda")
+    qnn.q_fold_epilogue(OC, "u4" if u4 else "u8", z_in, colsum, s_a, dev(s_w), s_o, bias=dev(bias), zp_term=zp,
+                        M=Mv, Bq=Bq, D=D)
+    s_r = 0.13 if u4 else 1.1
+    R = float(np.float32(np.float32(s_r) / np.float32(s_o)))
+    res_dt = "u4" if u4 else "u8"
+    resd = None if res is None else dev(pk(_to_layout(res, layout).ravel()))
+    epi = qnn.epilogue(mode, relu=True, out_dt=out_dt, zp_term=zp, M=Mv, Bq=Bq, D=D, bias=dev(bias),
+                       residual=resd if mode == "requant" else None, res_dt=res_dt, z_res=8 if u4 else 128, R=R)
+    n_out = N * OH * OW * OC
+    if mode == "requant":
+        O = t.full((n_out // 2 if out_dt == "u4" else n_out,), 0x5A, dtype=t.uint8, device="cuda")
+    elif mode == "dequant":
+        O = t.empty(n_out, dtype=t.float32, device="cuda")
+    else:
+        O = t.empty(n_out, dtype=t.int32, device="cuda")
+    O32 = t.zeros(n_out, dtype=t.int32, device="cuda")
+    if u4:
+        ws = t.full((qnn.qnn_conv_workspace_bytes(g, "u4"),), 0xFF, dtype=t.uint8, device="cuda") if workspace else None
+        qnn.qconv_u4s4(Id, z_in, Wp, g, epi, O, O32, workspace=ws)
+    else:
+        qnn.qconv_u8s8(Id, z_in, Wp, g, epi, O, O32)
+    assert qnn.qnn_check_device_error() == qnn.QNN_OK
+    acc = oracle.conv_acc_layout(_to_layout(I, layout), Wc, z_in, N, H, W, C, layout, (pad, pad), (st, st))
+    assert np.array_equal(host(O32), acc), f"{(host(O32) != acc).sum()} accumulator mismatches"
+    acc_rows = _from_layout(acc, layout, N, OH, OW, OC).reshape(-1, OC)
+    _, M_o, Bq_o, D_o = oracle.fold(oracle.colsum(Wc.reshape(OC, -1)), z_in, s_a, s_w, s_o, bias)
+    if mode == "s32":
+        assert np.array_equal(host(O), acc)
+    elif mode == "dequant":
+        y = oracle.dequant_epilogue(acc_rows, D_o, bias)
+        got = _from_layout(host(O), layout, N, OH, OW, OC).reshape(-1, OC)
+        assert np.array_equal(f32_bits(got), f32_bits(y))
+    else:
+        rr = None if res is None else res.reshape(-1, OC)
+        q = oracle.requant(acc_rows, M_o, Bq_o, out_dt, relu=True, res=rr, z_res=8 if u4 else 128, R=R)
+        exp = (oracle.pack_nibbles if out_dt == "u4" else oracle.pack_bytes)(
+            _to_layout(q.reshape(N, OH, OW, OC), layout).ravel())
+        got = host(O)
+        assert np.array_equal(got, exp), f"{(got != exp).sum()} output bytes differ"
+
+
+@pytest.mark.parametrize("layout", ["nchw", "nchw64"])
+def test_conv_u4s4_resnet_3x3_layouts_full(oracle, layout):
+    """ResNet-50 stage-1 3x3 Conv_Add_Relu at full size with input, residual and
+    output in NCHW and in NCHW64 (MegEngine article, conv 算子優化), every output."""
+    _conv_layout(oracle, (64, 56, 56, 64, 64, 3, 1, 1), layout)
+
+
+@pytest.mark.parametrize("layout,geom,workspace", [
+    ("nchw", (2, 10, 12, 64, 64, 3, 1, 1), True),
+    ("nchw", (2, 9, 12, 128, 64, 3, 1, 2), True),    # stride 2, ragged output rows
+    ("nchw", (1, 8, 6, 256, 64, 1, 0, 1), True),     # 1x1: an NCHW input takes the pre-pass
+    ("nchw64", (2, 9, 9, 64, 128, 3, 1, 1), True),
+    ("nchw64", (2, 9, 9, 128, 64, 3, 1, 1), False),  # the fused path reads NCHW64 directly
+    ("nchw64", (1, 7, 5, 256, 64, 1, 0, 1), False),  # 1x1, fused
+])
+def test_conv_u4s4_layouts(oracle, layout, geom, workspace):
+    _conv_layout(oracle, geom, layout, workspace=workspace)
+
+
+@pytest.mark.parametrize("layout,mode", [("nchw", "dequant"), ("nchw", "s32"), ("nchw64", "dequant")])
+def test_conv_u4s4_layouts_modes(oracle, layout, mode):
+    _conv_layout(oracle, (2, 8, 8, 64, 64, 3, 1, 1), layout, mode=mode, residual=False)
+
+
+@pytest.mark.parametrize("layout,geom", [("nchw", (2, 9, 9, 64, 64, 3, 1, 1)), ("nchw", (1, 7, 7, 64, 96, 3, 1, 2)),
+                                         ("nchw64", (2, 9, 9, 64, 64, 3, 1, 1)),
+                                         ("nchw64", (1, 6, 6, 256, 128, 3, 1, 1))])
+def test_conv_u8s8_layouts(oracle, layout, geom):
+    """u8 x s8 convs with NCHW (channel planes gathered) and NCHW64 inputs / outputs."""
+    _conv_layout(oracle, geom, layout, u4=False)
+
+
+def test_conv_layout_errors():
+    t = torch()
+    epi = qnn.epilogue("s32")
+    O = t.empty(1 << 16, dtype=t.int32, device="cuda")
+    I = t.zeros(1 << 16, dtype=t.uint8, device="cuda")
+    Wp = aligned_empty(1 << 20)
+    g = qnn.conv_geom(1, 8, 8, 64, 64, 3, 3, layout="nchw")
+    with pytest.raises(qnn.QnnError) as e:   # a 4-bit NCHW input needs the pre-pass's workspace
+        qnn.qconv_u4s4(I, 8, Wp, g, epi, O)
+    assert e.value.status == qnn.QNN_ERR_UNSUPPORTED
+    g = qnn.conv_geom(1, 8, 8, 32, 64, 3, 3, layout="nchw64")
+    with pytest.raises(qnn.QnnError) as e:   # NCHW64 needs whole 64-channel blocks
+        qnn.qconv_u4s4(I, 8, Wp, g, epi, O)
+    assert e.value.status == qnn.QNN_ERR_INVALID_ARG
+    g = qnn.conv_geom(1, 7, 7, 64, 64, 3, 3, layout="nchw")
+    ws = t.empty(1 << 16, dtype=t.uint8, device="cuda")
+    with pytest.raises(qnn.QnnError) as e:   # packed NCHW rows need an even width
+        qnn.qconv_u4s4(I, 8, Wp, g, epi, O, workspace=ws)
+    assert e.value.status == qnn.QNN_ERR_INVALID_ARG
