@@ -233,7 +233,11 @@ qnn_status qgemm_s8_packed(const void *A_packed, qnn_dtype a_dt, const void *B_p
  * the library's device code is loaded); the call allocates and frees nothing.
  * The pages describe no such variant; it exists only for those callers.
  * - The array's address is looked up once per device on the first call; make
- *   that first call on each device before capturing a stream.
+ *   that first call on each device before capturing a stream.  The looked-up
+ *   address is kept for the life of the process: after cudaDeviceReset (or any
+ *   reset of the device's primary context, which reloads the library's device
+ *   code) it is stale, so do not call this entry point on a device again after
+ *   resetting it.
  * - Returns QNN_ERR_UNSUPPORTED when qnn_gemm_workspace_bytes(M, K) exceeds
  *   QNN_GEMM_STATIC_SCRATCH_BYTES; other arguments as for qgemm_s8.
  * - Every call on a device uses the same array: calls whose executions

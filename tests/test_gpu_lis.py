@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 from integer_quantized_nn_gb300 import qnn, workloads
-from _util import dev, host
+from _util import dev, host, torch
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "lis_worked_example.txt")
@@ -118,7 +118,15 @@ def test_attn_shift_v(oracle, shape, bits):
     on the CUDA-core kernel."""
     Bh, Lq, Lk, d = shape
     if Lk * 128 * 2 ** (2 ** bits - 1) > 2 ** 31:
-        pytest.skip("int32 range: refused by the host check")
+        # beyond the int32 range of the sums: the host refuses the shape before launching
+        t = torch()
+        code = t.zeros((Bh, Lq, Lk), dtype=t.uint8, device="cuda")
+        v = t.zeros((Bh, Lk, d), dtype=t.int8, device="cuda")
+        out = t.zeros((Bh, Lq, d), dtype=t.int32, device="cuda")
+        with pytest.raises(qnn.QnnError) as e:
+            qnn.q_attn_shift_v(code, v, Bh, Lq, Lk, d, bits, out)
+        assert e.value.status == qnn.QNN_ERR_OVERFLOW_RISK
+        return
     rng = np.random.default_rng(Lq * 7 + bits)
     code = rng.integers(0, 2 ** bits + 1, size=(Bh, Lq, Lk)).astype(np.uint8)
     v = rng.integers(-128, 128, size=(Bh, Lk, d)).astype(np.int8)
