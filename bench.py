@@ -424,10 +424,11 @@ def setup_conv_u8zw(torch, qnn, workloads, device, stream):
     epi = qnn.epilogue("requant", relu=True, out_dt="u8", zp_term=zp, M=Mv, Bq=Bq, residual=res8, res_dt="u8",
                        z_res=wc["z_res"], R=R)
     O8 = torch.empty((Nb, g.OH, g.OW, OC), dtype=torch.uint8, device=device)
-    keep = (Wp, cs, zp, Mv, Bq, I8, res8, O8, epi)
+    ws8 = torch.empty(qnn.qnn_conv_workspace_bytes(g, "u8"), dtype=torch.uint8, device=device)
+    keep = (Wp, cs, zp, Mv, Bq, I8, res8, O8, epi, ws8)
 
     def fn():
-        qnn.qconv_u8u8(keep[5], wc["z_in"], keep[0], g, keep[8], keep[7], stream=stream)
+        qnn.qconv_u8u8(keep[5], wc["z_in"], keep[0], g, keep[8], keep[7], workspace=keep[9], stream=stream)
 
     return fn, {"ops": 2.0 * Nb * g.OH * g.OW * OC * C * 9,
                 "bytes": I8.numel() + O8.numel() + res8.numel() + OC * C * 9}

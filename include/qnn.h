@@ -298,9 +298,10 @@ qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_conv_geom *g
 qnn_status qconv_prepack_w_u4(const void *W, const int32_t *z_w, const qnn_conv_geom *g, void *W_packed,
                               int32_t *colsum, qnn_stream_t stream);
 
-/* Size in bytes of the qconv_u4s4 workspace for an input of in_dt (U4: the
- * input expanded to one byte per channel, N * H * W * C); 0 for an invalid
- * geometry or another type. */
+/* Size in bytes of the conv workspace for an input of in_dt (U4, for qconv_u4s4:
+ * the input expanded to one byte per channel, N * H * W * C; U8, for qconv_u8s8
+ * and qconv_u8u8: one fp16 value per channel, 2 * N * H * W * C); 0 for an
+ * invalid geometry or another type. */
 size_t qnn_conv_workspace_bytes(const qnn_conv_geom *g, qnn_dtype in_dt);
 
 /* u4 activations x s4 weights [MG 緩解精度下降: UINT4 input/output, INT4
@@ -321,9 +322,16 @@ qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed, const q
                       const qnn_epilogue *epi, void *O, int32_t *O_s32, void *workspace,
                       size_t workspace_bytes, qnn_stream_t stream);
 
-/* u8 activations x s8 weights, same contract (I: u8 codes in g->layout; C % 16 == 0). */
+/* u8 activations x s8 weights, same contract (I: u8 codes in g->layout; C % 16 == 0).
+ * workspace: optional device scratch of at least qnn_conv_workspace_bytes(g,
+ *   QNN_U8) bytes (16-byte aligned), owned by the caller and overwritten: when C
+ *   is a multiple of 64 and the filter has more than one tap, a pre-pass writes
+ *   the input as fp16 values q - z_in (NHWC) and the convolution reads each tap
+ *   with tensor-memory copies (the faster path); otherwise, and with NULL, the
+ *   convolution re-encodes the codes itself.  Results are identical. */
 qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
-                      const qnn_epilogue *epi, void *O, int32_t *O_s32, qnn_stream_t stream);
+                      const qnn_epilogue *epi, void *O, int32_t *O_s32, void *workspace, size_t workspace_bytes,
+                      qnn_stream_t stream);
 
 /* Prepack u8 filters (bytes, OHWI) with per-filter zero points z_w (device int32
  * [OC], each in 0..255) for qconv_u8u8 [MG 背景: asymmetric codes carry a zero
@@ -343,7 +351,8 @@ qnn_status qconv_prepack_w_u8(const void *W, const int32_t *z_w, const qnn_conv_
  * (longer filters are summed in more chunks, exactly); QNN_ERR_OVERFLOW_RISK
  * when FH FW C 255^2 > 2^31 - 1. */
 qnn_status qconv_u8u8(const void *I, int32_t z_in, const void *W_packed, const qnn_conv_geom *g,
-                      const qnn_epilogue *epi, void *O, int32_t *O_s32, qnn_stream_t stream);
+                      const qnn_epilogue *epi, void *O, int32_t *O_s32, void *workspace, size_t workspace_bytes,
+                      qnn_stream_t stream);
 
 /* ---- weight zero points (Z_w != 0) --------------------------------------------- */
 

@@ -529,6 +529,13 @@ inline size_t tma_w_offset(const qnn_conv_geom *g) { return round1k(packed_w_u4_
 inline size_t colsum_offset(const qnn_conv_geom *g) { return tma_w_offset(g) + round1k(tma_w_bytes(g)); }
 inline size_t packed_w_u4_total(const qnn_conv_geom *g) { return colsum_offset(g) + round1k((size_t)g->OC * 4); }
 
+// W_packed of 8-bit filters: [GEMM image of [OC, K] + its trailer][colsum, int32 x OC], 1 KB aligned parts.
+inline size_t colsum8_offset(const qnn_conv_geom *g)
+{
+    return round1k(gemm::packed_b_bytes(g->OC, g->FH * g->FW * g->C));
+}
+inline size_t packed_w_8_total(const qnn_conv_geom *g) { return colsum8_offset(g) + round1k((size_t)g->OC * 4); }
+
 // Staging depth: 8 units for tiles up to 128 columns (64 KB of staging), 2 for
 // 256-column tiles, whose units carry 4x the MMA work (and shared memory is full).
 // ---- u4 conv fed by TMA (with a workspace) --------------------------------------
@@ -551,27 +558,33 @@ constexpr int TMA_B_RES = 65536;
 
 // Stages that fit in about 192 KB of shared memory with `t` K steps per
 // stage, streamed or resident weights.
-constexpr int tma_stages(int cb, int tbn, int t, bool resb)
+constexpr int tma_stages(int cb, int tbn, int t, bool resb, int bank = TMA_B_RES)
 {
     const int per = t * BM * cb + (resb ? 0 : t * tbn * cb);
-    const int n = (196608 - (resb ? TMA_B_RES : 0)) / per;
+    const int n = (196608 - (resb ? bank : 0)) / per;
     return n > 15 ? 15 : n;
 }
 
-template <int CB, int TBN_, int T, bool RES>
+// Resident filter bank of the fp16 (u8) TMA conv: up to 10 K steps of 64 channels
+// for 64 filters (a 3x3 filter over 64 channels is 9).
+constexpr int TMA_B_RES16 = 81920;
+
+// EB: bytes per element of the expanded input -- 1 (e4m3 of u4 codes, kind::f8f6f4)
+// or 2 (fp16 of u8 codes less z_in, kind::f16); a row of a stage is CB elements.
+template <int CB, int TBN_, int T, bool RES, int EB = 1>
 struct ConvTmaOp : OpBase {
     static constexpr bool CACHE_COLS = true;
     static constexpr bool TMA_A = true;
-    static constexpr bool F8 = true;
-    static constexpr int SCALE_LOG2 = 9;
-    static constexpr int ROW = CB;
+    static constexpr bool F8 = EB == 1;
+    static constexpr int SCALE_LOG2 = EB == 1 ? 9 : 0;
+    static constexpr int ROW = CB * EB;
     static constexpr int SUB = T;
     static constexpr bool RESB = RES;
-    static constexpr int B_RES_BYTES = RES ? TMA_B_RES : 0;
-    static constexpr int STAGES = tma_stages(CB, TBN_, T, RES);
+    static constexpr int B_RES_BYTES = RES ? (EB == 2 ? TMA_B_RES16 : TMA_B_RES) : 0;
+    static constexpr int STAGES = tma_stages(CB * EB, TBN_, T, RES, B_RES_BYTES);
     static constexpr int STG_BYTES = 16;
 
-    __device__ static uint32_t a_bytes(const Params &p) { return (uint32_t)(CB * p.TW * p.TH * p.TN); }
+    __device__ static uint32_t a_bytes(const Params &p) { return (uint32_t)(ROW * p.TW * p.TH * p.TN); }
 
     // Units walk K from 0 in every tile (no per-CTA rotation), so the tap and
     // channel block advance by counting; a tile's box origin is decoded once.
@@ -745,6 +758,78 @@ __global__ void expand_u4_nchw_kernel(const uint8_t *__restrict__ in, int H, int
     }
 }
 
+// u8 codes -> fp16 values q - z (exact: |q - z| <= 255), written NHWC, for the
+// tensor-copy path of the u8 convs: each byte is placed in the mantissa of fp16
+// 1024 and 1024 + z subtracted.  A zero fp16 (the tensor copy's fill outside the
+// input) is then the real value 0, the padding reading.
+__device__ __forceinline__ void u8_to_half_centred(uint4 v, uint32_t zh2, uint32_t (&h)[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        h[2 * i] = hsub2_u32(prmt(w[i], 0x64646464u, 0x4140u), zh2);
+        h[2 * i + 1] = hsub2_u32(prmt(w[i], 0x64646464u, 0x4342u), zh2);
+    }
+}
+
+// NHWC or NCHW64 input: one thread per 16 input bytes (16 channels of one pixel).
+template <bool NCHW64>
+__global__ void expand_u8_kernel(const uint8_t *__restrict__ in, int64_t n16, int HW, int C, uint32_t zh2,
+                                 uint8_t *__restrict__ out)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t o;
+        if (NCHW64) {
+            const int64_t blk = i >> 2;  // (n, cb, pixel)
+            const int quarter = (int)(i & 3);
+            const int pix = (int)(blk % HW);
+            const int64_t t = blk / HW;
+            const int CB = C / 64;
+            const int cb = (int)(t % CB);
+            const int64_t n = t / CB;
+            o = (n * HW + pix) * (int64_t)C + cb * 64 + quarter * 16;
+        } else {
+            o = i * 16;
+        }
+        uint32_t h[8];
+        u8_to_half_centred(ldg_nc_v4(in + i * 16), zh2, h);
+        uint4 *dst = reinterpret_cast<uint4 *>(out + o * 2);
+        dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+        dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+}
+
+// NCHW input: one block per image row (n, h); the row of every channel plane
+// through shared memory (C * W bytes), then 16 channels of one pixel per thread.
+__global__ void expand_u8_nchw_kernel(const uint8_t *__restrict__ in, int H, int W, int C, uint32_t zh2,
+                                      uint8_t *__restrict__ out)
+{
+    extern __shared__ uint8_t rowbuf8[];
+    const int n = blockIdx.x / H;
+    const int h = blockIdx.x - n * H;
+    for (int i = threadIdx.x; i < C * W; i += blockDim.x) {
+        const int c = i / W;
+        const int x = i - c * W;
+        rowbuf8[i] = __ldg(in + (((int64_t)n * C + c) * H + h) * W + x);
+    }
+    __syncthreads();
+    const int groups = C / 16;
+    uint8_t *orow = out + (((int64_t)n * H + h) * W * (int64_t)C) * 2;
+    for (int i = threadIdx.x; i < W * groups; i += blockDim.x) {
+        const int w = i / groups;
+        const int c0 = (i - w * groups) * 16;
+        uint32_t b4[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) b4[j >> 2] |= (uint32_t)rowbuf8[(c0 + j) * W + w] << (8 * (j & 3));
+        uint32_t hh[8];
+        u8_to_half_centred(make_uint4(b4[0], b4[1], b4[2], b4[3]), zh2, hh);
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + ((int64_t)w * C + c0) * 2);
+        dst[0] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+        dst[1] = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+    }
+}
+
 // Weight image of the TMA conv: for each 256-filter block and unit (tap, CB
 // channels), 256 rows x CB bytes of e4m3 weights in channel order, in the
 // CB-byte swizzled layout (chunk c of row r at chunk c ^ ((r * CB / 128) %
@@ -847,6 +932,20 @@ qnn_status conv_tma_launch(Params p, cudaStream_t s)
     return launch<ConvTmaOp<CB, TBN, T, RES>, TBN, false>(p, s);
 }
 
+// The u8 convs on the expanded fp16 input: one K step (64 channels of one tap)
+// per unit, streamed weights (the GEMM image of the filters), exact chunks as
+// long as the weight image's trailer certifies for activations up to p.amax.
+template <int TBN>
+qnn_status conv_tma_u8_launch(Params p, bool wide_w, cudaStream_t s)
+{
+    // the host's bound, for |q - z_in| <= 255 and |w| <= 128 (s8) or 255 (u8 less z_w)
+    p.chunk_steps = wide_w ? 4 : 8;
+    p.nchunks = (p.KT + p.chunk_steps - 1) / p.chunk_steps;
+    if (TBN == 64 && (int64_t)p.KT * TBN * 128 <= TMA_B_RES16)
+        return launch<ConvTmaOp<64, TBN, 1, true, 2>, TBN, true>(p, s);  // filters resident
+    return launch<ConvTmaOp<64, TBN, 1, false, 2>, TBN, true>(p, s);
+}
+
 // 64-column tiles group 3, 2 or 1 K steps per unit and keep the weights
 // resident when they fit; wider tiles stream one step per unit.
 template <int TBN>
@@ -904,6 +1003,67 @@ static qnn_status conv1x1_bulk_launch(Params p, const qnn_conv_geom *g, cudaStre
     p.chunk_steps = p.KT;
     p.nchunks = 1;
     return launch<ConvU4PackedOp<false>, 64, false>(p, s);
+}
+
+// The u8 convs with a workspace: the input expanded to fp16 (q - z_in) in NHWC,
+// then one tiled 4-D TMA box (64 channels x TW x TH x TN pixels, 128-byte rows)
+// per filter tap, as for u4.  The sum is sum (q - z_in) w; the epilogue adds
+// (z_in - 128) colsum back (the fold's zp_term is for codes centred at 128), so
+// acc_c is that of the fused path.
+static qnn_status conv_tma_u8_run(Params p, const qnn_conv_geom *g, int32_t z_in, const void *W_packed,
+                                  void *workspace, int oh, int ow, bool wide_w, cudaStream_t s)
+{
+    const bool nchw = g->layout == QNN_LAYOUT_NCHW;
+    const uint32_t zh = 0x6400u + (uint32_t)z_in;  // fp16 1024 + z_in
+    const uint32_t zh2 = zh | (zh << 16);
+    uint8_t *xw = static_cast<uint8_t *>(workspace);
+    const int64_t n16 = (int64_t)g->N * g->H * g->W * g->C / 16;
+    int64_t blocks = (n16 + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (g->layout == QNN_LAYOUT_NHWC) {
+        expand_u8_kernel<false><<<(int)blocks, 256, 0, s>>>(p.A, n16, g->H * g->W, g->C, zh2, xw);
+    } else if (g->layout == QNN_LAYOUT_NCHW64) {
+        expand_u8_kernel<true><<<(int)blocks, 256, 0, s>>>(p.A, n16, g->H * g->W, g->C, zh2, xw);
+    } else {
+        const size_t rowbuf = (size_t)g->C * g->W;
+        if (rowbuf > 48 * 1024 || (int64_t)g->N * g->H > INT32_MAX) return QNN_ERR_UNSUPPORTED;
+        expand_u8_nchw_kernel<<<g->N * g->H, 256, rowbuf, s>>>(p.A, g->H, g->W, g->C, zh2, xw);
+    }
+    if (launch_status() != QNN_OK) return QNN_ERR_CUDA;
+    int TW, TH, TN;
+    choose_tiles(g->N, oh, ow, g->stride_w, g->stride_h, TW, TH, TN, nchw);
+    cuuint64_t dims[4] = {(cuuint64_t)g->C, (cuuint64_t)g->W, (cuuint64_t)g->H, (cuuint64_t)g->N};
+    cuuint64_t strides[3] = {(cuuint64_t)g->C * 2, (cuuint64_t)g->W * g->C * 2, (cuuint64_t)g->H * g->W * g->C * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)(TW * g->stride_w), (cuuint32_t)(TH * g->stride_h), (cuuint32_t)TN};
+    cuuint32_t estr[4] = {1, (cuuint32_t)g->stride_w, (cuuint32_t)g->stride_h, 1};
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return QNN_ERR_CUDA;
+    if (encode(&p.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, workspace, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return QNN_ERR_CUDA;
+    p.Nimg = g->N;
+    p.OH = oh;
+    p.TW = TW;
+    p.TH = TH;
+    p.TN = TN;
+    p.tiles_x = (ow + TW - 1) / TW;
+    p.tiles_y = (oh + TH - 1) / TH;
+    p.num_m = p.tiles_x * p.tiles_y * ((g->N + TN - 1) / TN);
+    p.cbn = g->C / 64;
+    p.KT = g->FH * g->FW * p.cbn;  // K steps of 64 channels = units
+    p.Bp = static_cast<const uint8_t *>(W_packed);
+    p.btrail = reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(W_packed) +
+                                                 gemm::packed_b_image_bytes(g->OC, g->FH * g->FW * g->C));
+    p.amax = z_in > 255 - z_in ? z_in : 255 - z_in;
+    if (p.amax == 0) p.amax = 1;
+    p.zcs = reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(W_packed) + colsum8_offset(g));
+    p.z_cs = z_in - 128;
+    if (g->OC <= 64) return conv_tma_u8_launch<64>(p, wide_w, s);
+    if (g->OC <= 128) return conv_tma_u8_launch<128>(p, wide_w, s);
+    return conv_tma_u8_launch<256>(p, wide_w, s);
 }
 
 // u4: qconv_u4s4; else the u8 conv, whose filter values reach 255 in magnitude
@@ -976,15 +1136,17 @@ qnn_status conv_run(const void *I, int32_t z_in, const void *W_packed, const qnn
     // (a 4-bit NCHW input always takes the pre-pass, which reorders it to NHWC)
     if (workspace && g->FH * g->FW == 1 && !(u4 && nchw)) workspace = nullptr;
     if (u4 && nchw && !workspace) return QNN_ERR_UNSUPPORTED;
+    // u8 inputs take the tensor-copy path when their channels fill 64-channel K steps
+    if (workspace && !u4 && g->C % 64 != 0) workspace = nullptr;
     if (workspace) {
-        if (!u4) return QNN_ERR_UNSUPPORTED;
-        if (workspace_bytes < (size_t)g->N * g->H * g->W * g->C) return QNN_ERR_INVALID_ARG;
+        if (workspace_bytes < (size_t)g->N * g->H * g->W * g->C * (u4 ? 1 : 2)) return QNN_ERR_INVALID_ARG;
         if (!aligned16(workspace)) return QNN_ERR_ALIGNMENT;
         if (g->stride_h > 8 || g->stride_w > 8) return QNN_ERR_UNSUPPORTED;
     }
     p.status = status_word();
     if (!p.status) return QNN_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
+    if (workspace && !u4) return conv_tma_u8_run(p, g, z_in, W_packed, workspace, oh, ow, wide_w, s);
     if (workspace) {
         // expanded input, then the tensor map over it: dims (C, W, H, N), bytes
         const int64_t n16 = (int64_t)g->N * g->H * g->W * g->C / 32;
@@ -1055,7 +1217,7 @@ extern "C" size_t qnn_conv_packed_w_bytes(const qnn_conv_geom *g, qnn_dtype w_dt
     if (!qnn::mk::geom_ok(g)) return 0;
     // u4 / u8 filters with zero points (qconv_prepack_w_u4 / _u8) take the images of s4 / s8
     if (w_dt == QNN_S4 || w_dt == QNN_U4) return qnn::mk::packed_w_u4_total(g);
-    if (w_dt == QNN_S8 || w_dt == QNN_U8) return qnn::gemm::packed_b_bytes(g->OC, g->FH * g->FW * g->C);
+    if (w_dt == QNN_S8 || w_dt == QNN_U8) return qnn::mk::packed_w_8_total(g);
     return 0;
 }
 
@@ -1074,8 +1236,15 @@ extern "C" qnn_status qconv_prepack_w(const void *W, qnn_dtype w_dt, const qnn_c
     if (!W || !W_packed || !qnn::mk::geom_ok(g)) return QNN_ERR_INVALID_ARG;
     const int K = g->FH * g->FW * g->C;
     if (w_dt == QNN_S8) {
-        // filters [OC][FH][FW][C] are the GEMM operand B [OC, K]
-        return qgemm_prepack_b(static_cast<const int8_t *>(W), g->OC, K, W_packed, colsum, stream);
+        // filters [OC][FH][FW][C] are the GEMM operand B [OC, K]; the column sums
+        // also go into the image (the tensor-copy path adds z_in * colsum back)
+        int32_t *cs_img = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(W_packed) + qnn::mk::colsum8_offset(g));
+        qnn_status st = qgemm_prepack_b(static_cast<const int8_t *>(W), g->OC, K, W_packed, cs_img, stream);
+        if (st != QNN_OK || !colsum) return st;
+        return cudaMemcpyAsync(colsum, cs_img, (size_t)g->OC * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream) ==
+                       cudaSuccess
+                   ? QNN_OK
+                   : QNN_ERR_CUDA;
     }
     if (w_dt != QNN_S4) return QNN_ERR_UNSUPPORTED;
     return qnn::mk::prepack_w4(W, nullptr, g, W_packed, colsum, stream);
@@ -1093,9 +1262,15 @@ extern "C" qnn_status qconv_prepack_w_u8(const void *W, const int32_t *z_w, cons
     if (g->C % 16 != 0) return QNN_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(W_packed) & 1023u) != 0) return QNN_ERR_ALIGNMENT;
     if (!qnn::aligned16(W) || !qnn::aligned16(z_w)) return QNN_ERR_ALIGNMENT;
-    // filters [OC][FH][FW][C] are the GEMM operand B [OC, K]
-    return qnn::prepack_b_u8_minus_zw(static_cast<const uint8_t *>(W), z_w, g->OC, g->FH * g->FW * g->C, W_packed,
-                                      colsum, (cudaStream_t)stream);
+    // filters [OC][FH][FW][C] are the GEMM operand B [OC, K]; column sums into the image too
+    int32_t *cs_img = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(W_packed) + qnn::mk::colsum8_offset(g));
+    qnn_status st = qnn::prepack_b_u8_minus_zw(static_cast<const uint8_t *>(W), z_w, g->OC, g->FH * g->FW * g->C,
+                                               W_packed, cs_img, (cudaStream_t)stream);
+    if (st != QNN_OK || !colsum) return st;
+    return cudaMemcpyAsync(colsum, cs_img, (size_t)g->OC * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream) ==
+                   cudaSuccess
+               ? QNN_OK
+               : QNN_ERR_CUDA;
 }
 
 extern "C" qnn_status qconv_prepack_w_u4(const void *W, const int32_t *z_w, const qnn_conv_geom *g, void *W_packed,
@@ -1150,8 +1325,11 @@ static qnn_status qnn::mk::prepack_w4(const void *W, const int32_t *z_w, const q
 
 extern "C" size_t qnn_conv_workspace_bytes(const qnn_conv_geom *g, qnn_dtype in_dt)
 {
-    if (!qnn::mk::geom_ok(g) || in_dt != QNN_U4) return 0;
-    return (size_t)g->N * g->H * g->W * g->C;
+    if (!qnn::mk::geom_ok(g)) return 0;
+    // the input expanded to one e4m3 byte (u4) or one fp16 value (u8) per channel
+    if (in_dt == QNN_U4) return (size_t)g->N * g->H * g->W * g->C;
+    if (in_dt == QNN_U8) return (size_t)g->N * g->H * g->W * g->C * 2;
+    return 0;
 }
 
 extern "C" qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_packed,
@@ -1165,15 +1343,16 @@ extern "C" qnn_status qconv_u4s4(const void *I, int32_t z_in, const void *W_pack
 
 extern "C" qnn_status qconv_u8s8(const void *I, int32_t z_in, const void *W_packed,
                                  const qnn_conv_geom *g, const qnn_epilogue *e, void *O,
-                                 int32_t *O_s32, qnn_stream_t stream)
+                                 int32_t *O_s32, void *workspace, size_t workspace_bytes, qnn_stream_t stream)
 {
-    return qnn::mk::conv_run<qnn::mk::ConvU8Op>(I, z_in, W_packed, g, e, O, O_s32, nullptr, 0, stream, false);
+    return qnn::mk::conv_run<qnn::mk::ConvU8Op>(I, z_in, W_packed, g, e, O, O_s32, workspace, workspace_bytes,
+                                                stream, false);
 }
 
 extern "C" qnn_status qconv_u8u8(const void *I, int32_t z_in, const void *W_packed,
                                  const qnn_conv_geom *g, const qnn_epilogue *e, void *O,
-                                 int32_t *O_s32, qnn_stream_t stream)
+                                 int32_t *O_s32, void *workspace, size_t workspace_bytes, qnn_stream_t stream)
 {
-    return qnn::mk::conv_run<qnn::mk::ConvU8Op>(I, z_in, W_packed, g, e, O, O_s32, nullptr, 0, stream, false,
-                                                true);
+    return qnn::mk::conv_run<qnn::mk::ConvU8Op>(I, z_in, W_packed, g, e, O, O_s32, workspace, workspace_bytes,
+                                                stream, false, true);
 }

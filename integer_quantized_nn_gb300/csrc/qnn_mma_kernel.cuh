@@ -87,6 +87,7 @@ struct Params {
     int chunk_steps, nchunks;
     const int32_t *btrail;
     int a_shift;
+    int amax;                // largest activation magnitude the MMA sees, if not 128 * 2^a_shift
     int ptf_max;             // GEMM with ptf: bound the host was given for every shift byte
     // epilogue
     int mode, relu, z_out, out_bits, out_signed;
@@ -206,7 +207,7 @@ __device__ __forceinline__ ChunkPlan chunk_plan(const Params &p, bool report)
         const int32_t kt = __ldg(p.btrail + gemm::TR_KT);
         if (magic == gemm::TRAILER_MAGIC && kt == p.KT) {
             L = gemm::certified_chunk_steps(__ldg(p.btrail + gemm::TR_STEP_MAX), __ldg(p.btrail + gemm::TR_TOTAL_MAX),
-                                            (int64_t)128 << p.a_shift, p.KT);
+                                            p.amax ? (int64_t)p.amax : (int64_t)128 << p.a_shift, p.KT);
         } else if (report) {
             atomicOr(p.status, kStatusBadArg);
         }

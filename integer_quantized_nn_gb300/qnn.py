@@ -82,8 +82,8 @@ def _declare(L):
         "qconv_prepack_w": (c_int, [vp, c_int, vp, vp, vp, vp]),
         "qnn_conv_workspace_bytes": (sz, [vp, c_int]),
         "qconv_u4s4": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
-        "qconv_u8s8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
-        "qconv_u8u8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp]),
+        "qconv_u8s8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "qconv_u8u8": (c_int, [vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "qconv_prepack_w_u8": (c_int, [vp, vp, vp, vp, vp, vp]),
         "q_log_int_softmax": (c_int, [vp, i64, i64, f32, c_int, vp, vp]),
         "q_attn_shift_v": (c_int, [vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp]),
@@ -310,18 +310,23 @@ def qconv_u4s4(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None
            "qconv_u4s4")
 
 
-def qconv_u8s8(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None, stream=None):
+def qconv_u8s8(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None, workspace=None, stream=None):
+    """workspace: optional uint8 device tensor of at least qnn_conv_workspace_bytes(g, "u8") bytes."""
     load()
+    ws_bytes = 0 if workspace is None else _nbytes(workspace)
     _check(_SYMBOLS["qconv_u8s8"](_ptr(I), int(z_in), _ptr(W_packed), ctypes.byref(g),
-                                  ctypes.byref(epi), _ptr(O), _ptr(O_s32), _stream(stream)),
+                                  ctypes.byref(epi), _ptr(O), _ptr(O_s32), _ptr(workspace),
+                                  ctypes.c_size_t(ws_bytes), _stream(stream)),
            "qconv_u8s8")
 
 
-def qconv_u8u8(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None, stream=None):
+def qconv_u8u8(I, z_in: int, W_packed, g: ConvGeom, epi: Epilogue, O, O_s32=None, workspace=None, stream=None):
     """u8 activations x u8 filters prepacked by qconv_prepack_w_u8."""
     load()
+    ws_bytes = 0 if workspace is None else _nbytes(workspace)
     _check(_SYMBOLS["qconv_u8u8"](_ptr(I), int(z_in), _ptr(W_packed), ctypes.byref(g),
-                                  ctypes.byref(epi), _ptr(O), _ptr(O_s32), _stream(stream)),
+                                  ctypes.byref(epi), _ptr(O), _ptr(O_s32), _ptr(workspace),
+                                  ctypes.c_size_t(ws_bytes), _stream(stream)),
            "qconv_u8u8")
 
 

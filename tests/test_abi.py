@@ -107,7 +107,8 @@ def test_invalid_arguments_rejected_on_host(lib):
     # conv workspace: its size, and a too-small one refused before any launch
     g = qnn.conv_geom(64, 56, 56, 64, 64, 3, 3)
     assert qnn.qnn_conv_workspace_bytes(g, "u4") == 64 * 56 * 56 * 64
-    assert qnn.qnn_conv_workspace_bytes(g, "u8") == 0
+    assert qnn.qnn_conv_workspace_bytes(g, "u8") == 2 * 64 * 56 * 56 * 64
+    assert qnn.qnn_conv_workspace_bytes(g, "s8") == 0
     cneed = qnn.qnn_conv_workspace_bytes(g, "u4")
     assert L.qconv_u4s4(16, 8, 1024, ctypes.byref(g), ctypes.byref(ok_epi), 16, None, 4096, cneed - 1,
                         None) == qnn.QNN_ERR_INVALID_ARG
@@ -242,7 +243,7 @@ def test_conv_u8_zero_point_rejected_on_host(lib):
     epi = qnn.epilogue("requant", out_dt="u8")
     epi.M, epi.Bq = 256, 512  # never dereferenced on the host
     big = qnn.conv_geom(1, 8, 8, 3680, 64, 3, 3)
-    assert L.qconv_u8u8(16, 8, 1024, ctypes.byref(big), ctypes.byref(epi), 16, None,
+    assert L.qconv_u8u8(16, 8, 1024, ctypes.byref(big), ctypes.byref(epi), 16, None, None, 0,
                         None) == qnn.QNN_ERR_OVERFLOW_RISK
 
 

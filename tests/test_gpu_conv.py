@@ -46,7 +46,7 @@ def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="re
     # u4: both paths -- the packed input re-encoded inside the conv kernel, and
     # the input expanded into a workspace (pre-filled with 0xFF) read by TMA
     outs = []
-    for path in (("fused", "workspace") if u4 else ("fused",)):
+    for path in ("fused", "workspace"):
         if mode == "requant":
             ob = OC // 2 if out_dt == "u4" else OC
             O = t.full((N, OH, OW, ob), 0x5A, dtype=t.uint8, device="cuda")
@@ -55,15 +55,18 @@ def _conv(oracle, I_pk, W_pk, geom, z_in, s_a, s_w, s_o, bias, u4=True, mode="re
         else:
             O = t.empty((N, OH, OW, OC), dtype=t.int32, device="cuda")
         O32 = t.zeros((N, OH, OW, OC), dtype=t.int32, device="cuda")
+        # the workspace paths: the input expanded (u4: e4m3 bytes; u8: fp16 q - z_in)
+        # into a workspace pre-filled with 0xFF and read by tensor copies
+        ws = None
         if path == "workspace":
-            ws = t.full((qnn.qnn_conv_workspace_bytes(g, "u4"),), 0xFF, dtype=t.uint8, device="cuda")
+            ws = t.full((qnn.qnn_conv_workspace_bytes(g, "u4" if u4 else "u8"),), 0xFF, dtype=t.uint8,
+                        device="cuda")
+        if u4:
             qnn.qconv_u4s4(Id, z_in, Wp, g, epi, O, O32, workspace=ws)
-        elif u4:
-            qnn.qconv_u4s4(Id, z_in, Wp, g, epi, O, O32)
         elif w_zp is None:
-            qnn.qconv_u8s8(Id, z_in, Wp, g, epi, O, O32)
+            qnn.qconv_u8s8(Id, z_in, Wp, g, epi, O, O32, workspace=ws)
         else:
-            qnn.qconv_u8u8(Id, z_in, Wp, g, epi, O, O32)
+            qnn.qconv_u8u8(Id, z_in, Wp, g, epi, O, O32, workspace=ws)
         assert qnn.qnn_check_device_error() == qnn.QNN_OK
         outs.append((path, O, O32))
 
@@ -425,7 +428,8 @@ def _conv_layout(oracle, geom, layout, u4=True, mode="requant", residual=True, w
         ws = t.full((qnn.qnn_conv_workspace_bytes(g, "u4"),), 0xFF, dtype=t.uint8, device="cuda") if workspace else None
         qnn.qconv_u4s4(Id, z_in, Wp, g, epi, O, O32, workspace=ws)
     else:
-        qnn.qconv_u8s8(Id, z_in, Wp, g, epi, O, O32)
+        ws = t.full((qnn.qnn_conv_workspace_bytes(g, "u8"),), 0xFF, dtype=t.uint8, device="cuda") if workspace else None
+        qnn.qconv_u8s8(Id, z_in, Wp, g, epi, O, O32, workspace=ws)
     assert qnn.qnn_check_device_error() == qnn.QNN_OK
     acc = oracle.conv_acc_layout(_to_layout(I, layout), Wc, z_in, N, H, W, C, layout, (pad, pad), (st, st))
     assert np.array_equal(host(O32), acc), f"{(host(O32) != acc).sum()} accumulator mismatches"
@@ -473,9 +477,11 @@ def test_conv_u4s4_layouts_modes(oracle, layout, mode):
 @pytest.mark.parametrize("layout,geom", [("nchw", (2, 9, 9, 64, 64, 3, 1, 1)), ("nchw", (1, 7, 7, 64, 96, 3, 1, 2)),
                                          ("nchw64", (2, 9, 9, 64, 64, 3, 1, 1)),
                                          ("nchw64", (1, 6, 6, 256, 128, 3, 1, 1))])
-def test_conv_u8s8_layouts(oracle, layout, geom):
-    """u8 x s8 convs with NCHW (channel planes gathered) and NCHW64 inputs / outputs."""
-    _conv_layout(oracle, geom, layout, u4=False)
+@pytest.mark.parametrize("workspace", [False, True])
+def test_conv_u8s8_layouts(oracle, layout, geom, workspace):
+    """u8 x s8 convs with NCHW and NCHW64 inputs / outputs: the converter warps
+    (NCHW channel planes gathered) and the fp16 expansion pre-pass + tensor copies."""
+    _conv_layout(oracle, geom, layout, u4=False, workspace=workspace)
 
 
 def test_conv_layout_errors():
