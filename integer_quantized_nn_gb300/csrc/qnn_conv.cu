@@ -116,6 +116,7 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 template <int ELEM_BITS, int GROUP_ELEMS, int STEP_ELEMS, int D>
 struct ConvStaging : OpBase {
     static constexpr bool CACHE_COLS = true;
+    static constexpr bool LAYOUTS = true;
     static constexpr int DEPTH = D;
     static constexpr int DEPTH_MULTI = D;
     static constexpr int STG_BYTES = D * 4 * 128 * 16;
@@ -176,6 +177,7 @@ struct ConvStaging : OpBase {
 template <int ELEM_BITS, int GROUP_ELEMS, int STEP_ELEMS>
 struct ConvRegRing : OpBase {
     static constexpr bool CACHE_COLS = true;
+    static constexpr bool LAYOUTS = true;
     static constexpr int DEPTH = 4;
     static constexpr int DEPTH_MULTI = 3;
     static constexpr int STG_BYTES = 16;  // no staging ring
@@ -285,6 +287,7 @@ struct ConvU4Op : ConvFetch<4, 32, 128, D> {
 template <bool THREAD_COPY>
 struct ConvU4PackedOp : OpBase {
     static constexpr bool CACHE_COLS = true;
+    static constexpr bool LAYOUTS = true;
     static constexpr bool TMA_A = false;
     static constexpr bool F8 = true;
     static constexpr int SCALE_LOG2 = 9;
@@ -574,6 +577,7 @@ constexpr int TMA_B_RES16 = 81920;
 template <int CB, int TBN_, int T, bool RES, int EB = 1>
 struct ConvTmaOp : OpBase {
     static constexpr bool CACHE_COLS = true;
+    static constexpr bool LAYOUTS = true;
     static constexpr bool TMA_A = true;
     static constexpr bool F8 = EB == 1;
     static constexpr int SCALE_LOG2 = EB == 1 ? 9 : 0;

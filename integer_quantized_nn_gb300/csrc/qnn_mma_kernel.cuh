@@ -125,6 +125,7 @@ struct OpBase {
     static constexpr int B_RES_BYTES = 0;
     static constexpr bool ROTATE_K = true;  // each CTA starts its tiles' K walk at its own offset
     static constexpr bool CACHE_COLS = false;  // epilogue keeps column constants across tiles of one column block
+    static constexpr bool LAYOUTS = false;     // outputs / residuals may be in a conv layout (qnn_layout)
     struct PState {};                        // producer-side state of a TMA_A Op
     struct RowInfo {                         // per-thread part of the row mapping
         int r;
@@ -564,28 +565,33 @@ __device__ __forceinline__ bool store_columns(const ColumnRegs<COLS> &cr, float 
 // of the output and the residual, and the distance between consecutive
 // columns: NHWC (and every GEMM) m * N + n; NCHW (image, channel, pixel); NCHW64
 // (image, channel block, pixel, channel in block).
+// LAY: the op supports conv layouts (conv ops); without it, every tensor is
+// [rows, N] row-major and none of the layout code is compiled in (GEMMs).
+template <bool LAY>
 __device__ __forceinline__ int64_t out_off(const Params &p, int m, int n)
 {
-    if (p.layout == QNN_LAYOUT_NHWC) return (int64_t)m * p.N + n;
+    if (!LAY || p.layout == QNN_LAYOUT_NHWC) return (int64_t)m * p.N + n;
     const int img = m / p.OHW;
     const int pix = m - img * p.OHW;
     if (p.layout == QNN_LAYOUT_NCHW) return ((int64_t)img * p.N + n) * p.OHW + pix;
     return (((int64_t)img * (p.N >> 6) + (n >> 6)) * p.OHW + pix) * 64 + (n & 63);
 }
+template <bool LAY>
 __device__ __forceinline__ int64_t out_cstride(const Params &p)
 {
-    return p.layout == QNN_LAYOUT_NCHW ? p.OHW : 1;
+    return LAY && p.layout == QNN_LAYOUT_NCHW ? p.OHW : 1;
 }
 
 // The residual codes of the 32 columns n0.. of row m (8-bit: 8 words of 4
 // codes; 4-bit: 4 words of 8 codes), or zeros without a residual.
+template <bool LAY>
 __device__ __forceinline__ void load_residual(const Params &p, int m, int n0, uint32_t (&rw)[8])
 {
 #pragma unroll
     for (int i = 0; i < 8; ++i) rw[i] = 0;
     if (!p.res || m >= p.M || n0 >= p.N) return;
-    const int64_t base = out_off(p, m, n0);
-    if (p.layout == QNN_LAYOUT_NCHW) {
+    const int64_t base = out_off<LAY>(p, m, n0);
+    if (LAY && p.layout == QNN_LAYOUT_NCHW) {
         // one code per channel plane
         const int64_t cs = p.OHW;
         for (int i = 0; i < 32 && n0 + i < p.N; ++i) {
@@ -623,6 +629,27 @@ __device__ __forceinline__ void load_residual(const Params &p, int m, int n0, ui
 // bits are the two's-complement low bits of that integer.
 constexpr float ROUND_MAGIC = 12582912.0f;
 constexpr uint32_t ROUND_MAGIC_BITS = 0x4B400000u;
+
+// Saturating packs of two int32 values: (c << 16) | sat8(a) << 8 | sat8(b), and
+// (c << 8) | satu4(a) << 4 | satu4(b).
+__device__ __forceinline__ uint32_t pack_sat_s8(int32_t a, int32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t pack_sat_u8(int32_t a, int32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t pack_sat_u4(int32_t a, int32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("cvt.pack.sat.u4.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 
 // Residual term t_n = float(r - z_res) * R + Bq_n for the 32 columns: the code
 // r - z_res is rebuilt as an fp32 value from the magic-number bits (exact, as
@@ -680,7 +707,7 @@ __device__ __forceinline__ void store_nchw_u4(const Params &p, int m, int n0, co
 {
     uint8_t *C = static_cast<uint8_t *>(p.C);
     const bool even = (threadIdx.x & 1) == 0;
-    const int64_t base = valid ? out_off(p, m, n0) : 0;
+    const int64_t base = valid ? out_off<true>(p, m, n0) : 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const uint32_t hi = __shfl_down_sync(0xffffffffu, c[i], 1);
@@ -689,18 +716,19 @@ __device__ __forceinline__ void store_nchw_u4(const Params &p, int m, int n0, co
     }
 }
 
-template <bool RS>
+template <bool RS, bool LAY>
 __device__ __forceinline__ void epilogue_float_t(const Params &p, int m, int n0, float (&a)[32],
                                                  const float *ca, const float *cb,
                                                  const uint32_t (&rw)[8])
 {
     const bool valid = m < p.M && n0 < p.N;
     // NCHW u4 outputs pair up lanes: every lane takes part (warp-uniform test)
-    const bool pair = p.layout == QNN_LAYOUT_NCHW && p.mode == QNN_EPI_REQUANT && p.out_bits == 4;
+    const bool pair = LAY && p.layout == QNN_LAYOUT_NCHW && p.mode == QNN_EPI_REQUANT && p.out_bits == 4;
     if (!valid && !pair) return;
-    const bool vec = p.vec_ok && p.layout != QNN_LAYOUT_NCHW;
-    const int64_t base = valid ? out_off(p, m, n0) : 0;  // element offset of (m, n0)
-    const int64_t cs = out_cstride(p);
+    const bool nchw = LAY && p.layout == QNN_LAYOUT_NCHW;
+    const bool vec = p.vec_ok && !nchw;
+    const int64_t base = valid ? out_off<LAY>(p, m, n0) : 0;  // element offset of (m, n0)
+    const int64_t cs = out_cstride<LAY>(p);
     float rs = 1.0f;
     if constexpr (RS) rs = valid ? __ldg(p.row_scale + m) : 1.0f;
     if (p.mode == QNN_EPI_DEQUANT) {
@@ -740,6 +768,64 @@ __device__ __forceinline__ void epilogue_float_t(const Params &p, int m, int n0,
         t[i + 3] = bq.w;
     }
     if (p.res) add_residual(p, rw, t);
+    uint8_t *C = static_cast<uint8_t *>(p.C);
+    if (!pair && !nchw) {
+        // The same formula: v = a M + t (one IEEE round-to-nearest product, then
+        // one sum); one fmax with the lower clip (0 with ReLU, else -2^22, which
+        // keeps v + 1.5 2^23 positive); the magic-number add that rounds half to
+        // even; z_out added to the integer; saturating packs to the output type's
+        // range -- together clip(rint(v) + z_out) to [qmin, qmax] (v beyond 2^22
+        // packs to qmax).
+        const float lo = p.relu ? p.clip_lo_f : -4194304.0f;
+        const uint32_t zoff = (uint32_t)p.z_out - ROUND_MAGIC_BITS;
+        int32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+            const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
+            float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+            if constexpr (RS) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mm[k] = __fmul_rn(rs, mm[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float v = fmaxf(__fadd_rn(__fmul_rn(a[i + k], mm[k]), t[i + k]), lo);
+                r[i + k] = (int32_t)(__float_as_uint(__fadd_rn(v, ROUND_MAGIC)) + zoff);
+            }
+        }
+        if (p.out_bits == 8) {
+            uint32_t ow[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                const int32_t *q = r + 4 * w;
+                ow[w] = p.out_signed ? pack_sat_s8(q[1], q[0], pack_sat_s8(q[3], q[2], 0u))
+                                     : pack_sat_u8(q[1], q[0], pack_sat_u8(q[3], q[2], 0u));
+            }
+            if (vec) {
+                st_v4(C + base, ow[0], ow[1], ow[2], ow[3]);
+                st_v4(C + base + 16, ow[4], ow[5], ow[6], ow[7]);
+            } else {
+                for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = (uint8_t)(ow[i >> 2] >> (8 * (i & 3)));
+            }
+        } else {
+            // u4: codes 2k (low nibble) and 2k + 1 (high nibble) share byte k
+            uint32_t ow[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int32_t *q = r + 8 * w;
+                ow[w] = pack_sat_u4(q[1], q[0], pack_sat_u4(q[3], q[2], pack_sat_u4(q[5], q[4],
+                                                                            pack_sat_u4(q[7], q[6], 0u))));
+            }
+            if (vec) {
+                st_v4(C + base / 2, ow[0], ow[1], ow[2], ow[3]);
+            } else {
+                // N is even: a byte holds columns (2i, 2i+1) of this thread's row only
+                for (int i = 0; i < 32 && n0 + i < p.N; i += 2)
+                    C[(base + i) / 2] = (uint8_t)(ow[i >> 3] >> (4 * (i & 7)));
+            }
+        }
+        return;
+    }
     uint32_t c[32];  // low bits: the output codes
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
@@ -760,67 +846,38 @@ __device__ __forceinline__ void epilogue_float_t(const Params &p, int m, int n0,
         store_nchw_u4(p, m, n0, c, valid);
         return;
     }
-    uint8_t *C = static_cast<uint8_t *>(p.C);
-    if (p.layout == QNN_LAYOUT_NCHW) {
-        // 8-bit codes, one per channel plane
-        for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i * cs] = (uint8_t)c[i];
-        return;
-    }
-    if (p.out_bits == 8) {
-        uint32_t ow[8];
-#pragma unroll
-        for (int w = 0; w < 8; ++w) ow[w] = pack_low_bytes(c[4 * w], c[4 * w + 1], c[4 * w + 2], c[4 * w + 3]);
-        if (vec) {
-            st_v4(C + base, ow[0], ow[1], ow[2], ow[3]);
-            st_v4(C + base + 16, ow[4], ow[5], ow[6], ow[7]);
-        } else {
-            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = (uint8_t)(ow[i >> 2] >> (8 * (i & 3)));
-        }
-    } else {
-        // codes 2k (low nibble) and 2k + 1 (high nibble) share byte k
-        uint32_t ow[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const uint32_t *q = c + 8 * w;
-            const uint32_t ev = pack_low_bytes(q[0], q[2], q[4], q[6]);
-            const uint32_t od = pack_low_bytes(q[1], q[3], q[5], q[7]);
-            ow[w] = (ev & 0x0F0F0F0Fu) | ((od << 4) & 0xF0F0F0F0u);
-        }
-        if (vec) {
-            st_v4(C + base / 2, ow[0], ow[1], ow[2], ow[3]);
-        } else {
-            // N is even: a byte holds columns (2i, 2i+1) of this thread's row only
-            for (int i = 0; i < 32 && n0 + i < p.N; i += 2)
-                C[(base + i) / 2] = (uint8_t)(ow[i >> 3] >> (4 * (i & 7)));
-        }
-    }
+    // NCHW 8-bit codes, one per channel plane
+    for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i * cs] = (uint8_t)c[i];
 }
 
+template <bool LAY>
 __device__ __forceinline__ void epilogue_float_rowscale(const Params &p, int m, int n0, float (&a)[32], const float *ca,
                                                      const float *cb, const uint32_t (&rw)[8])
 {
-    epilogue_float_t<true>(p, m, n0, a, ca, cb, rw);
+    epilogue_float_t<true, LAY>(p, m, n0, a, ca, cb, rw);
 }
 
+template <bool LAY>
 __device__ __forceinline__ void epilogue_float(const Params &p, int m, int n0, float (&a)[32], const float *ca,
                                                const float *cb, const uint32_t (&rw)[8])
 {
-    if (p.row_scale) epilogue_float_rowscale(p, m, n0, a, ca, cb, rw);
-    else epilogue_float_t<false>(p, m, n0, a, ca, cb, rw);
+    if (p.row_scale) epilogue_float_rowscale<LAY>(p, m, n0, a, ca, cb, rw);
+    else epilogue_float_t<false, LAY>(p, m, n0, a, ca, cb, rw);
 }
 
 // The same from int32 sums (multi-chunk K, raw int32 outputs, or zero-point
 // terms that are not fp32 values): subtracts zp_term (cz: its int bits), stores
 // the raw sums where asked, and converts for the float epilogue.
+template <bool LAY>
 __device__ __forceinline__ void epilogue_int(const Params &p, int m, int n0, int32_t (&ac)[32],
                                              const float *ca, const float *cb, const float *cz,
                                              const uint32_t (&rw)[8])
 {
     const bool valid = m < p.M && n0 < p.N;
-    const bool pair = p.layout == QNN_LAYOUT_NCHW && p.mode == QNN_EPI_REQUANT && p.out_bits == 4;
+    const bool pair = LAY && p.layout == QNN_LAYOUT_NCHW && p.mode == QNN_EPI_REQUANT && p.out_bits == 4;
     if (!valid && !pair) return;
-    const bool vec = p.vec_ok && p.layout != QNN_LAYOUT_NCHW;
-    const int64_t cs = out_cstride(p);
+    const bool vec = p.vec_ok && !(LAY && p.layout == QNN_LAYOUT_NCHW);
+    const int64_t cs = out_cstride<LAY>(p);
     if (p.zp) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
@@ -841,7 +898,7 @@ __device__ __forceinline__ void epilogue_int(const Params &p, int m, int n0, int
             ac[i] = (int32_t)((uint32_t)ac[i] + (uint32_t)(128 - __ldg(p.zw + n)) * rs);
         }
     }
-    const int64_t base = valid ? out_off(p, m, n0) : 0;
+    const int64_t base = valid ? out_off<LAY>(p, m, n0) : 0;
     if (p.C32 && valid) {
         if (vec) {
 #pragma unroll
@@ -865,7 +922,7 @@ __device__ __forceinline__ void epilogue_int(const Params &p, int m, int n0, int
     float a[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) a[k] = __int2float_rn(ac[k]);
-    epilogue_float(p, m, n0, a, ca, cb, rw);
+    epilogue_float<LAY>(p, m, n0, a, ca, cb, rw);
 }
 
 // fp32 accumulator value -> exact int32 (the fp32 value times 2^scale_log2 is an integer)
@@ -887,7 +944,7 @@ __device__ __forceinline__ bool epilogue_stream_tile(const Params &p, Smem<Op, T
                                                      uint32_t u, int lane)
 {
     uint32_t rw_next[8];
-    load_residual(p, m, nbase, rw_next);
+    load_residual<Op::LAYOUTS>(p, m, nbase, rw_next);
     if (!warp_wait_idle(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return false;
     tc_fence_after();
     if (fresh) exact = store_columns<COLS>(cr, cols, lane);
@@ -897,7 +954,7 @@ __device__ __forceinline__ bool epilogue_stream_tile(const Params &p, Smem<Op, T
         uint32_t rw[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) rw[k] = rw_next[k];
-        if (jp + 1 < npieces) load_residual(p, m, nbase + (jp + 1) * 32, rw_next);
+        if (jp + 1 < npieces) load_residual<Op::LAYOUTS>(p, m, nbase + (jp + 1) * 32, rw_next);
         uint32_t r[32];
         tmem_ld32(taddr0 + jp * 32, r);
         tmem_ld_wait();
@@ -922,13 +979,14 @@ __device__ __forceinline__ bool epilogue_stream_tile(const Params &p, Smem<Op, T
                                               : __fadd_rn(f, z4[e]);
                 }
             }
-            epilogue_float_t<false>(p, m, nbase + jp * 32, a, cols + jp * 32, cols + COLS + jp * 32, rw);
+            epilogue_float_t<false, Op::LAYOUTS>(p, m, nbase + jp * 32, a, cols + jp * 32, cols + COLS + jp * 32,
+                                                 rw);
         } else {
             int32_t acc[32];
 #pragma unroll
             for (int k = 0; k < 32; ++k) acc[k] = acc_to_int<Op::SCALE_LOG2>(r[k]);
-            epilogue_int(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
-                         cols + 3 * COLS + jp * 32, rw);
+            epilogue_int<Op::LAYOUTS>(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
+                                      cols + 3 * COLS + jp * 32, rw);
         }
     }
     return true;
@@ -1011,15 +1069,15 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
 #pragma unroll 1
             for (int jp = 0; jp < npieces; ++jp) {
                 uint32_t rw[8];
-                load_residual(p, m, nbase + jp * 32, rw);
+                load_residual<Op::LAYOUTS>(p, m, nbase + jp * 32, rw);
                 uint32_t r[32];
                 tmem_ld32(ibuf + jp * 32, r);
                 tmem_ld_wait();
                 int32_t acc[32];
 #pragma unroll
                 for (int k = 0; k < 32; ++k) acc[k] = (int32_t)r[k];
-                epilogue_int(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
-                             cols + 3 * COLS + jp * 32, rw);
+                epilogue_int<Op::LAYOUTS>(p, m, nbase + jp * 32, acc, cols + jp * 32, cols + COLS + jp * 32,
+                                          cols + 3 * COLS + jp * 32, rw);
             }
         }
     }
