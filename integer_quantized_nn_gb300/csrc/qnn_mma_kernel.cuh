@@ -826,28 +826,31 @@ __device__ __forceinline__ void epilogue_float_t(const Params &p, int m, int n0,
         }
         return;
     }
-    uint32_t c[32];  // low bits: the output codes
+    if constexpr (LAY) {
+        // NCHW outputs: the clip in fp32, codes stored one per channel plane (u4: lane pairs)
+        uint32_t c[32];  // low bits: the output codes
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-        const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
-        float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-        if constexpr (RS) {
+        for (int i = 0; i < 32; i += 4) {
+            const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
+            float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+            if constexpr (RS) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mm[k] = __fmul_rn(rs, mm[k]);
+                for (int k = 0; k < 4; ++k) mm[k] = __fmul_rn(rs, mm[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float v = __fadd_rn(__fmul_rn(a[i + k], mm[k]), t[i + k]);
+                v = fminf(fmaxf(v, p.clip_lo_f), p.clip_hi_f);
+                c[i + k] = __float_as_uint(__fadd_rn(v, ROUND_MAGIC)) + (uint32_t)p.z_out;
+            }
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float v = __fadd_rn(__fmul_rn(a[i + k], mm[k]), t[i + k]);
-            v = fminf(fmaxf(v, p.clip_lo_f), p.clip_hi_f);
-            c[i + k] = __float_as_uint(__fadd_rn(v, ROUND_MAGIC)) + (uint32_t)p.z_out;
+        if (pair) {
+            store_nchw_u4(p, m, n0, c, valid);
+            return;
         }
+        // NCHW 8-bit codes, one per channel plane
+        for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i * cs] = (uint8_t)c[i];
     }
-    if (pair) {
-        store_nchw_u4(p, m, n0, c, valid);
-        return;
-    }
-    // NCHW 8-bit codes, one per channel plane
-    for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i * cs] = (uint8_t)c[i];
 }
 
 template <bool LAY>
