@@ -630,27 +630,6 @@ __device__ __forceinline__ void load_residual(const Params &p, int m, int n0, ui
 constexpr float ROUND_MAGIC = 12582912.0f;
 constexpr uint32_t ROUND_MAGIC_BITS = 0x4B400000u;
 
-// Saturating packs of two int32 values: (c << 16) | sat8(a) << 8 | sat8(b), and
-// (c << 8) | satu4(a) << 4 | satu4(b).
-__device__ __forceinline__ uint32_t pack_sat_s8(int32_t a, int32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t pack_sat_u8(int32_t a, int32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t pack_sat_u4(int32_t a, int32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("cvt.pack.sat.u4.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
 // Residual term t_n = float(r - z_res) * R + Bq_n for the 32 columns: the code
 // r - z_res is rebuilt as an fp32 value from the magic-number bits (exact, as
 // |r - z_res| < 2^22), then one fmul and one fadd as in the requant formula.
@@ -769,87 +748,60 @@ __device__ __forceinline__ void epilogue_float_t(const Params &p, int m, int n0,
     }
     if (p.res) add_residual(p, rw, t);
     uint8_t *C = static_cast<uint8_t *>(p.C);
-    if (!pair && !nchw) {
-        // The same formula: v = a M + t (one IEEE round-to-nearest product, then
-        // one sum); one fmax with the lower clip (0 with ReLU, else -2^22, which
-        // keeps v + 1.5 2^23 positive); the magic-number add that rounds half to
-        // even; z_out added to the integer; saturating packs to the output type's
-        // range -- together clip(rint(v) + z_out) to [qmin, qmax] (v beyond 2^22
-        // packs to qmax).
-        const float lo = p.relu ? p.clip_lo_f : -4194304.0f;
-        const uint32_t zoff = (uint32_t)p.z_out - ROUND_MAGIC_BITS;
-        int32_t r[32];
+    uint32_t c[32];  // low bits: the output codes
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
-            float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-            if constexpr (RS) {
+    for (int i = 0; i < 32; i += 4) {
+        const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
+        float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+        if constexpr (RS) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mm[k] = __fmul_rn(rs, mm[k]);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float v = fmaxf(__fadd_rn(__fmul_rn(a[i + k], mm[k]), t[i + k]), lo);
-                r[i + k] = (int32_t)(__float_as_uint(__fadd_rn(v, ROUND_MAGIC)) + zoff);
-            }
+            for (int k = 0; k < 4; ++k) mm[k] = __fmul_rn(rs, mm[k]);
         }
-        if (p.out_bits == 8) {
-            uint32_t ow[8];
 #pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                const int32_t *q = r + 4 * w;
-                ow[w] = p.out_signed ? pack_sat_s8(q[1], q[0], pack_sat_s8(q[3], q[2], 0u))
-                                     : pack_sat_u8(q[1], q[0], pack_sat_u8(q[3], q[2], 0u));
-            }
-            if (vec) {
-                st_v4(C + base, ow[0], ow[1], ow[2], ow[3]);
-                st_v4(C + base + 16, ow[4], ow[5], ow[6], ow[7]);
-            } else {
-                for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = (uint8_t)(ow[i >> 2] >> (8 * (i & 3)));
-            }
-        } else {
-            // u4: codes 2k (low nibble) and 2k + 1 (high nibble) share byte k
-            uint32_t ow[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const int32_t *q = r + 8 * w;
-                ow[w] = pack_sat_u4(q[1], q[0], pack_sat_u4(q[3], q[2], pack_sat_u4(q[5], q[4],
-                                                                            pack_sat_u4(q[7], q[6], 0u))));
-            }
-            if (vec) {
-                st_v4(C + base / 2, ow[0], ow[1], ow[2], ow[3]);
-            } else {
-                // N is even: a byte holds columns (2i, 2i+1) of this thread's row only
-                for (int i = 0; i < 32 && n0 + i < p.N; i += 2)
-                    C[(base + i) / 2] = (uint8_t)(ow[i >> 3] >> (4 * (i & 7)));
-            }
+        for (int k = 0; k < 4; ++k) {
+            float v = __fadd_rn(__fmul_rn(a[i + k], mm[k]), t[i + k]);
+            v = fminf(fmaxf(v, p.clip_lo_f), p.clip_hi_f);
+            c[i + k] = __float_as_uint(__fadd_rn(v, ROUND_MAGIC)) + (uint32_t)p.z_out;
         }
-        return;
     }
     if constexpr (LAY) {
-        // NCHW outputs: the clip in fp32, codes stored one per channel plane (u4: lane pairs)
-        uint32_t c[32];  // low bits: the output codes
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            const float4 mv = *reinterpret_cast<const float4 *>(ca + i);
-            float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-            if constexpr (RS) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) mm[k] = __fmul_rn(rs, mm[k]);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float v = __fadd_rn(__fmul_rn(a[i + k], mm[k]), t[i + k]);
-                v = fminf(fmaxf(v, p.clip_lo_f), p.clip_hi_f);
-                c[i + k] = __float_as_uint(__fadd_rn(v, ROUND_MAGIC)) + (uint32_t)p.z_out;
-            }
-        }
         if (pair) {
             store_nchw_u4(p, m, n0, c, valid);
             return;
         }
-        // NCHW 8-bit codes, one per channel plane
-        for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i * cs] = (uint8_t)c[i];
+        if (nchw) {
+            // 8-bit codes, one per channel plane
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i * cs] = (uint8_t)c[i];
+            return;
+        }
+    }
+    if (p.out_bits == 8) {
+        uint32_t ow[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) ow[w] = pack_low_bytes(c[4 * w], c[4 * w + 1], c[4 * w + 2], c[4 * w + 3]);
+        if (vec) {
+            st_v4(C + base, ow[0], ow[1], ow[2], ow[3]);
+            st_v4(C + base + 16, ow[4], ow[5], ow[6], ow[7]);
+        } else {
+            for (int i = 0; i < 32 && n0 + i < p.N; ++i) C[base + i] = (uint8_t)(ow[i >> 2] >> (8 * (i & 3)));
+        }
+    } else {
+        // codes 2k (low nibble) and 2k + 1 (high nibble) share byte k
+        uint32_t ow[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t *q = c + 8 * w;
+            const uint32_t ev = pack_low_bytes(q[0], q[2], q[4], q[6]);
+            const uint32_t od = pack_low_bytes(q[1], q[3], q[5], q[7]);
+            ow[w] = (ev & 0x0F0F0F0Fu) | ((od << 4) & 0xF0F0F0F0u);
+        }
+        if (vec) {
+            st_v4(C + base / 2, ow[0], ow[1], ow[2], ow[3]);
+        } else {
+            // N is even: a byte holds columns (2i, 2i+1) of this thread's row only
+            for (int i = 0; i < 32 && n0 + i < p.N; i += 2)
+                C[(base + i) / 2] = (uint8_t)(ow[i >> 3] >> (4 * (i & 7)));
+        }
     }
 }
 
