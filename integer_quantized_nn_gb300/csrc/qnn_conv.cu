@@ -287,7 +287,7 @@ struct ConvU4Op : ConvFetch<4, 32, 128, D> {
 template <bool THREAD_COPY>
 struct ConvU4PackedOp : OpBase {
     static constexpr bool CACHE_COLS = true;
-    static constexpr bool LAYOUTS = true;
+    static constexpr bool LAYOUTS = false;     // taken for NHWC tensors only
     static constexpr bool TMA_A = false;
     static constexpr bool F8 = true;
     static constexpr int SCALE_LOG2 = 9;
