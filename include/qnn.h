@@ -306,15 +306,16 @@ size_t qnn_conv_workspace_bytes(const qnn_conv_geom *g, qnn_dtype in_dt);
 
 /* u4 activations x s4 weights [MG 緩解精度下降: UINT4 input/output, INT4
  * weights, FP32 bias], Conv_Relu / Conv_Add_Relu through `epi`
- * [MG 算子融合優化].  I: packed u4 NHWC; O: out_dt U4 (packed) or U8 codes, or
- * fp32 / int32 per epi->mode; O_s32: optional int32 acc_c.  C a multiple of
- * 32, OC even.
+ * [MG 算子融合優化].  I: packed u4 codes in g->layout (NHWC, NCHW or NCHW64); O
+ * (and the residual): the same layout, out_dt U4 (packed) or U8 codes, or fp32 /
+ * int32 per epi->mode; O_s32: optional int32 acc_c.  C a multiple of 32, OC even.
  * workspace: optional device scratch of at least qnn_conv_workspace_bytes(g,
  *   QNN_U4) bytes (16-byte aligned), owned by the caller and overwritten: for
  *   filters with more than one tap, a pre-pass expands the input to one byte
  *   per channel and the convolution reads its taps with tensor-memory copies
  *   (the faster path there); 1x1 filters and NULL: the convolution re-encodes
- *   the packed input itself.  Results are identical.  Calls in flight at the
+ *   the packed input itself (NHWC 1x1 stride-1 unpadded convs copy the packed
+ *   codes to shared memory and unpack them there).  Results are identical.  Calls in flight at the
  *   same time must not share a workspace.  An NCHW input needs the workspace
  *   (the pre-pass reads it and writes the expanded NHWC bytes the convolution
  *   reads, for every filter size): QNN_ERR_UNSUPPORTED without one. */
