@@ -542,22 +542,25 @@ __device__ __forceinline__ void load_columns(const Params &p, ColumnRegs<COLS> &
 // correctly rounded float(acc - zp_term), the conversion the requant formula
 // starts from, without an integer round trip.
 template <int COLS>
-__device__ __forceinline__ bool store_columns(const ColumnRegs<COLS> &cr, float *cols, int lane)
+__device__ __forceinline__ bool store_columns(const ColumnRegs<COLS> &cr, float *cols, int lane, bool &zp_zero)
 {
     __syncwarp();
     bool exact = true;
+    bool zero = true;
 #pragma unroll
     for (int k = 0; k < COLS / 32; ++k) {
         const int32_t z = cr.z[k];
         const int32_t nzi = (int32_t)(0u - (uint32_t)z);
         const float nz = __int2float_rn(nzi);
         exact = exact && z != INT32_MIN && __float2int_rn(nz) == nzi;
+        zero = zero && z == 0;
         cols[32 * k + lane] = cr.a[k];
         cols[COLS + 32 * k + lane] = cr.b[k];
         cols[2 * COLS + 32 * k + lane] = nz;
         cols[3 * COLS + 32 * k + lane] = __int_as_float(z);
     }
     __syncwarp();
+    zp_zero = __all_sync(0xffffffffu, zero);
     return __all_sync(0xffffffffu, exact);
 }
 
@@ -894,7 +897,8 @@ __device__ __forceinline__ int32_t acc_to_int(uint32_t bits)
 // (the accumulator buffer is released after the last piece is read).
 template <class Op, int TBN, int COLS>
 __device__ __forceinline__ bool epilogue_stream_tile(const Params &p, Smem<Op, TBN> &s, float *cols,
-                                                     const ColumnRegs<COLS> &cr, bool fresh, bool &exact, int m,
+                                                     const ColumnRegs<COLS> &cr, bool fresh, bool &exact,
+                                                     bool &zp_zero, int m,
                                                      int nbase, int npieces, uint32_t taddr0, uint32_t abuf,
                                                      uint32_t u, int lane)
 {
@@ -902,7 +906,7 @@ __device__ __forceinline__ bool epilogue_stream_tile(const Params &p, Smem<Op, T
     load_residual<Op::LAYOUTS>(p, m, nbase, rw_next);
     if (!warp_wait_idle(smem_u32(&s.acc_full[abuf]), (u >> 1) & 1u, p.status)) return false;
     tc_fence_after();
-    if (fresh) exact = store_columns<COLS>(cr, cols, lane);
+    if (fresh) exact = store_columns<COLS>(cr, cols, lane, zp_zero);
     const bool fast = exact && !p.C32 && p.mode != QNN_EPI_S32 && !p.rowsum && !p.row_scale;
 #pragma unroll 1
     for (int jp = 0; jp < npieces; ++jp) {
@@ -918,7 +922,16 @@ __device__ __forceinline__ bool epilogue_stream_tile(const Params &p, Smem<Op, T
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[abuf]));
         }
-        if (fast) {
+        if (fast && zp_zero && Op::SCALE_LOG2 == 0 && p.mode == QNN_EPI_REQUANT) {
+            // zp_term = 0 in every column (e.g. u8 activations with Z_a = 128): the
+            // fp32 sum is the exact integer acc_c, the conversion the formula starts
+            // from (a sum of -0 instead of +0 cannot change a requantized code)
+            float a[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) a[k] = __uint_as_float(r[k]);
+            epilogue_float_t<false, Op::LAYOUTS>(p, m, nbase + jp * 32, a, cols + jp * 32, cols + COLS + jp * 32,
+                                                 rw);
+        } else if (fast) {
             // the fp32 sum is an exact integer (times 2^-SCALE_LOG2); adding the
             // fp32 -zp_term rounds once, like the int32 -> fp32 conversion
             const float *cn = cols + 2 * COLS + jp * 32;
@@ -976,6 +989,7 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
     // block: they are loaded again only when the block changes
     int cur_nbase = -1;
     bool exact = false;
+    bool zp_zero = false;
     for (int i = 0; i < my_tiles; ++i) {
         const int t = blockIdx.x + i * gridDim.x;
         const int m = Op::out_row(p, t % p.num_m, ri);
@@ -987,8 +1001,8 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
         if (nch == 1) {
             const uint32_t abuf = u & 1u;
             const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + abuf * TBN + p0 * 32;
-            if (!epilogue_stream_tile<Op, TBN, COLS>(p, s, cols, cr, fresh, exact, m, nbase, npieces, taddr, abuf,
-                                                     u, lane))
+            if (!epilogue_stream_tile<Op, TBN, COLS>(p, s, cols, cr, fresh, exact, zp_zero, m, nbase, npieces, taddr,
+                                                     abuf, u, lane))
                 return;
             ++u;
         } else if constexpr (MULTI) {
@@ -1020,7 +1034,7 @@ __device__ void epilogue_role(const Params &p, Smem<Op, TBN> &s, int my_tiles, u
                 if (lane == 0) mbar_arrive(smem_u32(&s.acc_empty[0]));
                 ++u;
             }
-            if (fresh) exact = store_columns<COLS>(cr, cols, lane);
+            if (fresh) exact = store_columns<COLS>(cr, cols, lane, zp_zero);
 #pragma unroll 1
             for (int jp = 0; jp < npieces; ++jp) {
                 uint32_t rw[8];
