@@ -500,6 +500,14 @@ __device__ __forceinline__ void st_v4(void *ptr, uint32_t a, uint32_t b, uint32_
     *reinterpret_cast<uint4 *>(ptr) = make_uint4(a, b, c, d);
 }
 
+// 32 bytes in one 256-bit store (ptr 32-byte aligned).
+__device__ __forceinline__ void st_v8(void *ptr, const uint32_t (&w)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // Each epilogue warp keeps the per-column constants of its COLS columns in
 // shared memory: [0, COLS) M (requant) or D (dequant), [COLS, 2 COLS) Bq or
 // bias, [2 COLS, 3 COLS) -zp_term as an fp32 value, [3 COLS, 4 COLS) zp_term
@@ -782,7 +790,9 @@ __device__ __forceinline__ void epilogue_float_t(const Params &p, int m, int n0,
         uint32_t ow[8];
 #pragma unroll
         for (int w = 0; w < 8; ++w) ow[w] = pack_low_bytes(c[4 * w], c[4 * w + 1], c[4 * w + 2], c[4 * w + 3]);
-        if (vec) {
+        if (vec && (reinterpret_cast<uintptr_t>(C) & 31u) == 0) {
+            st_v8(C + base, ow);  // the 32 codes of one row in one store: whole 32-byte sectors
+        } else if (vec) {
             st_v4(C + base, ow[0], ow[1], ow[2], ow[3]);
             st_v4(C + base + 16, ow[4], ow[5], ow[6], ow[7]);
         } else {
